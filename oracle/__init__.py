@@ -1,0 +1,243 @@
+"""fp64 CPU oracle for the GMA forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never links, loads or
+calls it, and it imports nothing from the CUDA side.
+
+The arithmetic lives in ``gma_oracle.c`` (plain C, fp64, single-threaded);
+this module compiles it with gcc and exposes numpy wrappers that loop over
+(batch, head).  Every definition cites "Gaussian Mixture Attention:
+Linear-Time Sequence Mixing via Probabilistic Latent Routing" (arXiv
+2606.18283), written [GMA, ...]:
+
+* ``scores`` / ``responsibilities``  -- Eqs. (2)-(3) (reconstructed from prose)
+* ``forward_bidir``                  -- Eqs. (5)-(7), footnote 4
+* ``forward_causal``                 -- Eqs. (8a)/(8b), cumulative-sum remark
+* ``affinity`` / ``affinity_forward`` -- Eqs. (9)-(11), brute force for tiny N
+* ``bidir_rows`` / ``causal_rows``   -- the same definitions on selected rows
+
+Parity pins: see ``tests/test_oracle.py`` (closed forms, invariants, brute
+force, scipy / scikit-learn textbook routines, hand-derived golden values).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gma_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+_libs: dict = {}
+_ACTIVE = [0]  # which build the functions below call; 0 is the oracle
+
+_D = ctypes.POINTER(ctypes.c_double)
+_L = ctypes.POINTER(ctypes.c_long)
+
+
+def _lib_path(mutant: int) -> str:
+    name = "libgma_oracle.so" if mutant == 0 else f"libgma_oracle_mutant{mutant}.so"
+    return os.path.join(_BUILD_DIR, name)
+
+
+def build(force: bool = False, mutant: int = 0) -> str:
+    """Compile gma_oracle.c with gcc (no fast-math, no FMA contraction).
+
+    ``mutant`` != 0 builds a deliberately broken copy (see the list at the
+    top of gma_oracle.c); only the pin-strength tests ask for one.
+    """
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    path = _lib_path(mutant)
+    stale = (not os.path.exists(path)) or (os.path.getmtime(path) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+               "-ffp-contract=off", f"-DGMA_ORACLE_MUTANT={int(mutant)}", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, path)
+    return path
+
+
+def _load(mutant: int = 0):
+    with _lock:
+        lib = _libs.get(mutant)
+        if lib is None:
+            lib = ctypes.CDLL(build(mutant=mutant))
+            common = [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D, _D,
+                      ctypes.c_int, ctypes.c_double]
+            lib.gma_oracle_scores.argtypes = [_D, ctypes.c_int, ctypes.c_int, _D, _D, _D,
+                                              ctypes.c_int, _D]
+            lib.gma_oracle_responsibilities.argtypes = lib.gma_oracle_scores.argtypes
+            lib.gma_oracle_bidir.argtypes = common + [_D]
+            lib.gma_oracle_causal.argtypes = common + [_D]
+            lib.gma_oracle_bidir_rows.argtypes = common + [_L, ctypes.c_int, _D]
+            lib.gma_oracle_causal_rows.argtypes = common + [_L, ctypes.c_int, _D]
+            lib.gma_oracle_causal_rows.restype = ctypes.c_int
+            lib.gma_oracle_affinity_forward.argtypes = common + [ctypes.c_int, _D]
+            lib.gma_oracle_affinity.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, _D, _D,
+                                                _D, ctypes.c_int, _D]
+            _libs[mutant] = lib
+    return lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening to a C-contiguous fp64 array (accepts numpy or torch)."""
+    if hasattr(a, "detach"):  # torch tensor: widen on the CPU, exactly
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def _heads(x: np.ndarray, nd: int):
+    """View an array [..., rows, cols] as [(batch*heads), rows, cols]."""
+    return x.reshape((-1,) + x.shape[-nd:])
+
+
+def _params(mu, sigma2, log_pi):
+    mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
+    if mu.ndim == 2:
+        mu, sigma2, log_pi = mu[None], sigma2[None], log_pi[None]
+    return mu, sigma2, log_pi
+
+
+def _head_param(h_flat: int, H: int, mu, sigma2, log_pi):
+    h = h_flat % H
+    return (np.ascontiguousarray(mu[h]), np.ascontiguousarray(sigma2[h]),
+            np.ascontiguousarray(log_pi[h]))
+
+
+def scores(X, mu, sigma2, log_pi) -> np.ndarray:
+    """Scores s_ik for X [..., N, d_r] with one head's params [K, d_r], [K]."""
+    lib = _load(_ACTIVE[0])
+    X = _f64(X)
+    mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
+    N, d_r = X.shape[-2:]
+    K = mu.shape[0]
+    Xh = _heads(X, 2)
+    out = np.empty(Xh.shape[:-1] + (K,), np.float64)
+    for b in range(Xh.shape[0]):
+        xb = np.ascontiguousarray(Xh[b])
+        lib.gma_oracle_scores(_p(xb), N, d_r, _p(mu), _p(sigma2), _p(log_pi), K, _p(out[b]))
+    return out.reshape(X.shape[:-1] + (K,))
+
+
+def responsibilities(X, mu, sigma2, log_pi) -> np.ndarray:
+    """Gamma [B, H, N, K] for X [B, H, N, d_r], per-head params [H, K, d_r] / [H, K].
+
+    Two-dimensional X with [K, d_r] params is one head.
+    """
+    lib = _load(_ACTIVE[0])
+    X = _f64(X)
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H = mu.shape[0]
+    N, d_r = X.shape[-2:]
+    K = mu.shape[1]
+    Xh = _heads(X, 2)
+    out = np.empty(Xh.shape[:-1] + (K,), np.float64)
+    for b in range(Xh.shape[0]):
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        xb = np.ascontiguousarray(Xh[b])
+        lib.gma_oracle_responsibilities(_p(xb), N, d_r, _p(m), _p(s), _p(lp), K, _p(out[b]))
+    return out.reshape(X.shape[:-1] + (K,))
+
+
+def _forward(fn_name, Q, K_, V, mu, sigma2, log_pi, eps, extra=None):
+    lib = _load(_ACTIVE[0])
+    fn = getattr(lib, fn_name)
+    Q, K_, V = _f64(Q), _f64(K_), _f64(V)
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H = mu.shape[0]
+    N, d_r = Q.shape[-2:]
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    Qh, Kh, Vh = _heads(Q, 2), _heads(K_, 2), _heads(V, 2)
+    out = np.empty(Vh.shape, np.float64)
+    for b in range(Qh.shape[0]):
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        q, k, v = (np.ascontiguousarray(t[b]) for t in (Qh, Kh, Vh))
+        args = [_p(q), _p(k), _p(v), N, d_r, d_v, _p(m), _p(s), _p(lp), K, float(eps)]
+        if extra is not None:
+            args.append(extra)
+        fn(*args, _p(out[b]))
+    return out.reshape(V.shape)
+
+
+def forward_bidir(Q, K_, V, mu, sigma2, log_pi, eps) -> np.ndarray:
+    """Bidirectional O [B, H, N, d_v] ([GMA, Eqs. 5-7])."""
+    return _forward("gma_oracle_bidir", Q, K_, V, mu, sigma2, log_pi, eps)
+
+
+def forward_causal(Q, K_, V, mu, sigma2, log_pi, eps) -> np.ndarray:
+    """Causal O [B, H, N, d_v] ([GMA, Eq. 8b], j <= i inclusive)."""
+    return _forward("gma_oracle_causal", Q, K_, V, mu, sigma2, log_pi, eps)
+
+
+def affinity_forward(Q, K_, V, mu, sigma2, log_pi, eps, causal: bool) -> np.ndarray:
+    """Brute force O = A^GMA V through the materialised N x N affinity (tiny N)."""
+    return _forward("gma_oracle_affinity_forward", Q, K_, V, mu, sigma2, log_pi, eps,
+                    extra=int(bool(causal)))
+
+
+def affinity(Q, K_, mu, sigma2, log_pi) -> np.ndarray:
+    """Un-normalised affinity Gamma^Q (Gamma^K)^T for one head ([GMA, Eq. 11])."""
+    lib = _load(_ACTIVE[0])
+    Q, K_ = _f64(Q), _f64(K_)
+    mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
+    N, d_r = Q.shape
+    A = np.empty((N, N), np.float64)
+    lib.gma_oracle_affinity(_p(Q), _p(K_), N, d_r, _p(mu), _p(sigma2), _p(log_pi),
+                            mu.shape[0], _p(A))
+    return A
+
+
+def _rows(fn_name, q, k, v, mu_h, s2_h, lp_h, eps, rows):
+    lib = _load(_ACTIVE[0])
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    mu_h, s2_h, lp_h = _f64(mu_h), _f64(s2_h), _f64(lp_h)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    N, d_r = q.shape
+    d_v = v.shape[1]
+    out = np.empty((rows.shape[0], d_v), np.float64)
+    rc = getattr(lib, fn_name)(_p(q), _p(k), _p(v), N, d_r, d_v, _p(mu_h), _p(s2_h),
+                               _p(lp_h), mu_h.shape[0], float(eps),
+                               rows.ctypes.data_as(_L), int(rows.shape[0]), _p(out))
+    if rc not in (None, 0):
+        raise ValueError("rows must be sorted ascending and within [0, N)")
+    return out
+
+
+def bidir_rows(q, k, v, mu_h, s2_h, lp_h, eps, rows) -> np.ndarray:
+    """Bidirectional O rows of one head (q, k, v: [N, d]; params of that head)."""
+    return _rows("gma_oracle_bidir_rows", q, k, v, mu_h, s2_h, lp_h, eps, rows)
+
+
+def causal_rows(q, k, v, mu_h, s2_h, lp_h, eps, rows) -> np.ndarray:
+    """Causal O rows of one head; ``rows`` sorted ascending."""
+    return _rows("gma_oracle_causal_rows", q, k, v, mu_h, s2_h, lp_h, eps, rows)
+
+
+class use_mutant:
+    """Context manager: route the functions above to a planted-mistake build.
+
+    For the pin-strength tests only; ``with use_mutant(3): ...``.
+    """
+
+    def __init__(self, mutant: int):
+        self.mutant = int(mutant)
+
+    def __enter__(self):
+        self.prev = _ACTIVE[0]
+        _ACTIVE[0] = self.mutant
+        return self
+
+    def __exit__(self, *exc):
+        _ACTIVE[0] = self.prev
+        return False

@@ -1,0 +1,279 @@
+"""Pins for the fp64 oracle: checks against what the GMA paper and plain
+mathematics fix, independent of the oracle's own formulas.
+
+Each ``pin_*`` function raises AssertionError on a violation.  They are run
+against the oracle in ``test_oracle.py`` and against deliberately broken
+builds of it in ``test_oracle_mutants.py`` (where at least one must fail).
+
+Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+Probabilistic Latent Routing" (arXiv 2606.18283), cited [GMA, ...].
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def random_head(rng, N, d_r, d_v, K, mu_std=1.0):
+    Q = rng.normal(size=(N, d_r))
+    Kx = rng.normal(size=(N, d_r))
+    V = rng.normal(size=(N, d_v))
+    mu = rng.normal(scale=mu_std, size=(K, d_r))
+    sigma2 = np.log1p(np.exp(rng.normal(scale=math.sqrt(0.5), size=(K, d_r)))) + 1e-3
+    a = rng.normal(size=K)
+    log_pi = a - np.log(np.exp(a - a.max()).sum()) - a.max()
+    return Q, Kx, V, mu, sigma2, log_pi
+
+
+# ---------------------------------------------------------------- responsibilities
+
+def pin_simplex_rows():
+    """Rows of Gamma are probability distributions ([GMA, below Eq. 3])."""
+    rng = _rng(1)
+    for (N, d_r, K) in [(37, 5, 7), (16, 1, 1), (9, 16, 32)]:
+        X, _, _, mu, s2, lp = random_head(rng, N, d_r, 1, K)
+        G = oracle.responsibilities(X, mu, s2, lp)
+        assert G.shape == (N, K)
+        assert np.all(G >= 0)
+        assert np.max(np.abs(G.sum(-1) - 1.0)) < 1e-13
+
+
+def pin_identical_components_give_prior():
+    """All components equal => the posterior equals the prior pi for every x."""
+    rng = _rng(2)
+    K, d_r = 6, 4
+    mu = np.tile(rng.normal(size=(1, d_r)), (K, 1))
+    s2 = np.tile(rng.uniform(0.3, 2.0, size=(1, d_r)), (K, 1))
+    pi = rng.dirichlet(np.ones(K))
+    X = rng.normal(size=(11, d_r)) * 3
+    G = oracle.responsibilities(X, mu, s2, np.log(pi))
+    assert np.max(np.abs(G - pi[None])) < 1e-13
+
+
+def pin_single_component_is_one():
+    """K = 1 => gamma == 1 for every row."""
+    rng = _rng(3)
+    X, _, _, mu, s2, lp = random_head(rng, 13, 3, 1, 1)
+    G = oracle.responsibilities(X, mu, s2, lp)
+    assert np.max(np.abs(G - 1.0)) < 1e-15
+
+
+def pin_two_symmetric_components_logistic():
+    """d_r = 1, K = 2, mu = (-m, +m), equal variance v, equal priors.
+
+    Bayes' rule with two equal-variance Gaussians gives
+    p(z = 1 | x) = 1 / (1 + exp(2 m x / v)) (the logistic of the linear
+    discriminant), derived by hand, not from the oracle's score formula.
+    """
+    for m, v in [(1.0, 1.0), (0.7, 0.5), (2.0, 3.0)]:
+        x = np.linspace(-3, 3, 25)[:, None]
+        mu = np.array([[-m], [m]])
+        s2 = np.array([[v], [v]])
+        G = oracle.responsibilities(x, mu, s2, np.log([0.5, 0.5]))
+        expect = 1.0 / (1.0 + np.exp(2 * m * x[:, 0] / v))
+        assert np.max(np.abs(G[:, 0] - expect)) < 1e-13
+
+
+def pin_matches_scipy_textbook_posterior():
+    """Gamma_ik = pi_k prod_j Normal(x_j; mu_kj, sigma2_kj) / evidence, with the
+    normal log-pdf from scipy.stats and the normalisation from scipy.special."""
+    from scipy.special import softmax
+    from scipy.stats import norm
+    rng = _rng(4)
+    for (N, d_r, K) in [(20, 3, 5), (8, 16, 8)]:
+        X, _, _, mu, s2, lp = random_head(rng, N, d_r, 1, K)
+        logp = norm.logpdf(X[:, None, :], loc=mu[None], scale=np.sqrt(s2)[None]).sum(-1) + lp
+        expect = softmax(logp, axis=-1)
+        G = oracle.responsibilities(X, mu, s2, lp)
+        assert np.max(np.abs(G - expect)) < 1e-12
+
+
+def pin_matches_sklearn_gmm_predict_proba():
+    """scikit-learn's diagonal-covariance GaussianMixture with the same
+    weights, means and precisions yields the same posterior (host only)."""
+    try:
+        from sklearn.mixture import GaussianMixture
+    except ImportError:  # the GPU machine has no scikit-learn; scipy pin still runs
+        return
+    rng = _rng(5)
+    N, d_r, K = 30, 4, 5
+    X, _, _, mu, s2, lp = random_head(rng, N, d_r, 1, K)
+    pi = np.exp(lp)
+    pi /= pi.sum()
+    gm = GaussianMixture(n_components=K, covariance_type="diag")
+    gm.weights_ = pi
+    gm.means_ = mu
+    gm.covariances_ = s2
+    gm.precisions_cholesky_ = 1.0 / np.sqrt(s2)
+    expect = gm.predict_proba(X)
+    G = oracle.responsibilities(X, mu, s2, np.log(pi))
+    assert np.max(np.abs(G - expect)) < 1e-10
+
+
+def pin_responsibility_invariances():
+    """Gamma is unchanged by x -> c x + t with mu -> c mu + t, sigma2 -> c^2 sigma2,
+    by adding a constant to log pi, and permutes with the components."""
+    rng = _rng(6)
+    X, _, _, mu, s2, lp = random_head(rng, 17, 5, 1, 6)
+    G = oracle.responsibilities(X, mu, s2, lp)
+    c, t = 1.7, rng.normal(size=5)
+    G2 = oracle.responsibilities(c * X + t, c * mu + t, c * c * s2, lp)
+    assert np.max(np.abs(G - G2)) < 1e-12
+    G3 = oracle.responsibilities(X, mu, s2, lp + 3.25)
+    assert np.max(np.abs(G - G3)) < 1e-13
+    perm = rng.permutation(6)
+    G4 = oracle.responsibilities(X, mu[perm], s2[perm], lp[perm])
+    assert np.max(np.abs(G[:, perm] - G4)) < 1e-13
+
+
+# ---------------------------------------------------------------- forward
+
+def pin_bidir_equals_materialised_affinity():
+    """Eq. (7) O = Gamma^Q Vt / (Gamma^Q Z + eps) equals the row-normalised
+    materialised affinity applied to V ([GMA, Eqs. 9-11, footnote 4])."""
+    rng = _rng(7)
+    for (N, d_r, d_v, K, eps) in [(33, 4, 3, 5, 1e-6), (64, 8, 8, 16, 1e-2), (1, 2, 2, 3, 1e-6)]:
+        Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+        O = oracle.forward_bidir(Q, Kx, V, mu, s2, lp, eps)
+        A = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=False)
+        assert np.max(np.abs(O - A)) <= 1e-12 * max(1.0, np.abs(A).max())
+
+
+def pin_causal_equals_masked_affinity():
+    """Causal O equals the brute force with the inclusive lower-triangular
+    mask j <= i ([GMA, causal variant, Eq. 8b])."""
+    rng = _rng(8)
+    for (N, d_r, d_v, K, eps) in [(41, 4, 3, 5, 1e-6), (64, 8, 8, 16, 1e-2)]:
+        Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+        O = oracle.forward_causal(Q, Kx, V, mu, s2, lp, eps)
+        A = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=True)
+        assert np.max(np.abs(O - A)) <= 1e-12 * max(1.0, np.abs(A).max())
+
+
+def pin_affinity_properties():
+    """The un-normalised affinity <gQ_i, gK_j> is an inner product of two
+    probability vectors, so 0 <= A_ij <= 1; its rank is at most K; with the
+    same rows on both sides it is symmetric positive semi-definite
+    ([GMA, affinity section: non-negative, rank at most K])."""
+    rng = _rng(9)
+    N, d_r, K = 40, 3, 4
+    Q, Kx, _, mu, s2, lp = random_head(rng, N, d_r, 1, K)
+    A = oracle.affinity(Q, Kx, mu, s2, lp)
+    assert np.all(A >= 0) and np.all(A <= 1.0 + 1e-15)
+    assert np.linalg.matrix_rank(A, tol=1e-10) <= K
+    S = oracle.affinity(Q, Q, mu, s2, lp)
+    assert np.max(np.abs(S - S.T)) < 1e-15
+    assert np.linalg.eigvalsh(S).min() > -1e-12
+
+
+def pin_single_component_is_mean():
+    """K = 1: bidirectional O_i = sum_j V_j / (N + eps); causal O_i =
+    sum_{j<=i} V_j / (i + 1 + eps) (0-indexed)."""
+    rng = _rng(10)
+    N, d_r, d_v, eps = 29, 3, 4, 1e-3
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, 1)
+    Ob = oracle.forward_bidir(Q, Kx, V, mu, s2, lp, eps)
+    assert np.max(np.abs(Ob - V.sum(0) / (N + eps))) < 1e-13
+    Oc = oracle.forward_causal(Q, Kx, V, mu, s2, lp, eps)
+    expect = np.cumsum(V, 0) / (np.arange(1, N + 1)[:, None] + eps)
+    assert np.max(np.abs(Oc - expect)) < 1e-13
+
+
+def pin_identical_components_closed_form():
+    """All components equal => gamma = pi for every row, so
+    Gamma^Q (Gamma^K)^T has every entry p = sum_k pi_k^2 and
+    O_i = p sum_j V_j / (N p + eps) (causal: over j <= i, with (i+1) p)."""
+    rng = _rng(11)
+    N, d_r, d_v, K, eps = 23, 3, 2, 5, 1e-2
+    mu = np.tile(rng.normal(size=(1, d_r)), (K, 1))
+    s2 = np.tile(rng.uniform(0.5, 2, size=(1, d_r)), (K, 1))
+    pi = rng.dirichlet(np.ones(K))
+    Q, Kx, V = rng.normal(size=(N, d_r)), rng.normal(size=(N, d_r)), rng.normal(size=(N, d_v))
+    p = float((pi ** 2).sum())
+    Ob = oracle.forward_bidir(Q, Kx, V, mu, s2, np.log(pi), eps)
+    assert np.max(np.abs(Ob - p * V.sum(0) / (N * p + eps))) < 1e-13
+    Oc = oracle.forward_causal(Q, Kx, V, mu, s2, np.log(pi), eps)
+    expect = p * np.cumsum(V, 0) / (np.arange(1, N + 1)[:, None] * p + eps)
+    assert np.max(np.abs(Oc - expect)) < 1e-13
+
+
+def pin_causal_first_and_last_rows():
+    """O_0 reads only key 0: O_0 = (gQ_0 . gK_0) V_0 / (gQ_0 . gK_0 + eps);
+    the last causal row sees every key, so it equals the last bidirectional row."""
+    rng = _rng(12)
+    N, d_r, d_v, K, eps = 31, 4, 3, 6, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    Oc = oracle.forward_causal(Q, Kx, V, mu, s2, lp, eps)
+    Ob = oracle.forward_bidir(Q, Kx, V, mu, s2, lp, eps)
+    assert np.max(np.abs(Oc[-1] - Ob[-1])) < 1e-13
+    from scipy.special import softmax
+    from scipy.stats import norm
+    def gam(x):
+        return softmax(norm.logpdf(x[None, :], loc=mu, scale=np.sqrt(s2)).sum(-1) + lp)
+    a = float(gam(Q[0]) @ gam(Kx[0]))
+    assert np.max(np.abs(Oc[0] - a * V[0] / (a + eps))) < 1e-13
+
+
+def pin_causal_prefix_consistency():
+    """Causal O restricted to the first N' rows equals causal O computed on
+    the first N' tokens alone (output i depends only on j <= i)."""
+    rng = _rng(13)
+    N, d_r, d_v, K, eps = 50, 3, 4, 5, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    O = oracle.forward_causal(Q, Kx, V, mu, s2, lp, eps)
+    for n in (1, 7, 33):
+        On = oracle.forward_causal(Q[:n], Kx[:n], V[:n], mu, s2, lp, eps)
+        assert np.max(np.abs(O[:n] - On)) < 1e-13
+
+
+def pin_bidir_symmetries():
+    """Bidirectional O is invariant to a joint permutation of the (K_X, V_X)
+    rows, permutes with the Q_X rows and is linear in V_X."""
+    rng = _rng(14)
+    N, d_r, d_v, K, eps = 27, 3, 4, 5, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    O = oracle.forward_bidir(Q, Kx, V, mu, s2, lp, eps)
+    p = rng.permutation(N)
+    assert np.max(np.abs(O - oracle.forward_bidir(Q, Kx[p], V[p], mu, s2, lp, eps))) < 1e-13
+    assert np.max(np.abs(O[p] - oracle.forward_bidir(Q[p], Kx, V, mu, s2, lp, eps))) < 1e-13
+    V2 = rng.normal(size=V.shape)
+    O2 = oracle.forward_bidir(Q, Kx, V2, mu, s2, lp, eps)
+    O3 = oracle.forward_bidir(Q, Kx, 2.0 * V - 0.5 * V2, mu, s2, lp, eps)
+    assert np.max(np.abs(O3 - (2.0 * O - 0.5 * O2))) < 1e-12
+
+
+def pin_rows_agree_with_full():
+    """The selected-row routines give the same rows as the full forward."""
+    rng = _rng(15)
+    N, d_r, d_v, K, eps = 45, 4, 3, 6, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    rows = np.array([0, 1, 17, 44])
+    Ob = oracle.forward_bidir(Q, Kx, V, mu, s2, lp, eps)
+    Oc = oracle.forward_causal(Q, Kx, V, mu, s2, lp, eps)
+    assert np.max(np.abs(oracle.bidir_rows(Q, Kx, V, mu, s2, lp, eps, rows) - Ob[rows])) < 1e-13
+    assert np.max(np.abs(oracle.causal_rows(Q, Kx, V, mu, s2, lp, eps, rows) - Oc[rows])) < 1e-13
+
+
+def pin_batched_heads_use_their_own_parameters():
+    """[B, H, N, d] inputs take parameters per head h (same for every batch b)."""
+    rng = _rng(16)
+    B, H, N, d_r, d_v, K, eps = 2, 3, 9, 3, 2, 4, 1e-6
+    Q = rng.normal(size=(B, H, N, d_r)); Kx = rng.normal(size=(B, H, N, d_r))
+    V = rng.normal(size=(B, H, N, d_v))
+    mu = rng.normal(size=(H, K, d_r)); s2 = rng.uniform(0.2, 2, size=(H, K, d_r))
+    lp = np.log(rng.dirichlet(np.ones(K), size=H))
+    O = oracle.forward_bidir(Q, Kx, V, mu, s2, lp, eps)
+    for b in range(B):
+        for h in range(H):
+            Oh = oracle.forward_bidir(Q[b, h], Kx[b, h], V[b, h], mu[h], s2[h], lp[h], eps)
+            assert np.max(np.abs(O[b, h] - Oh)) == 0.0
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
