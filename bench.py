@@ -1,0 +1,392 @@
+"""Benchmark of the GMA forward hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gma|reference]
+
+One step = one bidirectional and one causal GMA forward (every step of the
+hot path: coefficient prep, responsibilities, latent write, read, causal
+scan) over a batch B=4, H=8, N=16384, d_r=d_v=K=64, bf16 inputs and fp32
+output O, each variant on its own seeded synthetic input set.  The metric is forward token*heads per
+second: 2 * B * H * N per step (both variants) divided by the step time.
+The step moves 2 x 335 MB of algorithmic traffic (Q_X, K_X, V_X read, O
+written), more than the 129 MB L2, so no separate L2 flush is done between
+steps.
+
+Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle is
+timed instead, on a bounded sample of the same workload (one head of each
+variant per step), in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(B=4, H=8, N=16384, d_r=64, d_v=64, K=64, dtype="bf16", eps=1e-6)
+METRIC = "GMA fwd tokens*heads/s (bidir & causal, N=16K, K=64); % of GB300 HBM roofline"
+UNIT = "token*heads/s"
+
+# Algorithmic HBM bytes each stage accounts for, as the tensors of the path it
+# reads or writes (Q_X, K_X, V_X read once, O written once per forward);
+# intermediate scratch traffic is not algorithmic.
+STAGE_TENSORS = {
+    "prep": "", "reduce": "", "scan": "",
+    "resp_q": "Q", "resp_k": "K", "write": "V", "read": "O", "causal": "VO",
+    "tc_write": "KV", "tc_read": "QO", "tc_causal": "QKVO", "tc_aggregate": "KV",
+}
+
+
+def tensor_bytes(t: str, w=WORKLOAD) -> int:
+    """Bytes of the named path tensors; O is written in fp32."""
+    es = 2 if w["dtype"] == "bf16" else 4
+    per = {"Q": es * w["d_r"], "K": es * w["d_r"], "V": es * w["d_v"], "O": 4 * w["d_v"]}
+    return sum(per[c] for c in t) * w["B"] * w["H"] * w["N"]
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(stage: str):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, if the
+    kernels have not changed since it was taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_digest") != source_digest():
+        return None
+    v = d.get("stages", {}).get(stage)
+    return None if v is None else float(v)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+def _oracle_head(args):
+    """One head of one variant through the fp64 oracle (runs in a worker)."""
+    causal, seed, head = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+    w = WORKLOAD
+    case = Case("sample", bool(causal), 1, 1, w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"])
+    inp = make_inputs(case, seed=seed * 1000 + head)
+    fn = oracle.forward_causal if causal else oracle.forward_bidir
+    t = time.perf_counter()
+    fn(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], w["eps"])
+    return time.perf_counter() - t
+
+
+class OraclePool:
+    """Spawned worker processes that run oracle heads (started once)."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+        self.procs = procs
+        self.pool = mp.get_context("spawn").Pool(procs)
+        self.pool.map(_oracle_head, [(0, 0, 0)] * procs)  # workers up, oracle loaded
+
+    def sample(self, pairs: int):
+        """Wall time and token*heads for `pairs` (bidir head, causal head) pairs."""
+        jobs = [(c, 7, i) for i in range(pairs) for c in (0, 1)]
+        t = time.perf_counter()
+        self.pool.map(_oracle_head, jobs)
+        return time.perf_counter() - t, len(jobs) * WORKLOAD["N"]
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    procs = 2
+    pool = OraclePool(procs)
+    times = []
+    for s in range(args.warmup + args.steps):
+        wall, th = pool.sample(1)
+        if s >= args.warmup:
+            times.append(wall)
+    pool.close()
+    ms = 1e3 * statistics.mean(times)
+    value = 2 * WORKLOAD["N"] / (ms / 1e3)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": "GMA forward, one bidirectional + one causal head per step "
+                                  "(sample of B=4,H=8,N=16384,d_r=d_v=K=64)", **WORKLOAD},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
+                            "sample": "1 bidirectional + 1 causal head of N=16384 per step, "
+                                      "fp64 C oracle, one process per variant"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gma(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300 import _native
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    cases = [Case("bidir", False, w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"]),
+             Case("causal", True, w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"])]
+    host = [make_inputs(c, seed=1000 * rank + i) for i, c in enumerate(cases)]
+    dinp = [{k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in h.items()} for h in host]
+    outs = [torch.empty(w["B"], w["H"], w["N"], w["d_v"], dtype=torch.float32, device=dev) for _ in cases]
+    paths = [gma.selected_path(w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"], int(c.causal)) for c in cases]
+    wss = [torch.empty(max(256, gma.workspace_size(w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"],
+                                                   w["dtype"], int(c.causal))), dtype=torch.uint8, device=dev)
+           for c in cases]
+    stages = [_native.stage_names(p, int(c.causal)) for p, c in zip(paths, cases)]
+    stream = torch.cuda.current_stream()
+    lib = gma.load()
+
+    def call(i, O=None, events=None):
+        c, d = cases[i], dinp[i]
+        fn = "gma_forward_causal" if c.causal else "gma_forward_bidir"
+        opt = _native.options(stage_events=events)
+        import ctypes
+        vp = ctypes.c_void_p
+        st = getattr(lib, fn)(vp(d["Q"].data_ptr()), vp(d["K"].data_ptr()), vp(d["V"].data_ptr()),
+                              _native.GMA_BF16, vp(d["mu"].data_ptr()), vp(d["sigma2"].data_ptr()),
+                              vp(d["log_pi"].data_ptr()), float(w["eps"]),
+                              vp((O if O is not None else outs[i]).data_ptr()),
+                              w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], ctypes.byref(opt),
+                              vp(wss[i].data_ptr()), wss[i].numel(), vp(stream.cuda_stream))
+        if st != 0:
+            raise gma.GmaError(st, fn)
+
+    # stage events: one list per (step, variant)
+    nst = [len(s) + 1 for s in stages]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(nst[i])] for i in range(2)]
+          for _ in range(args.steps)]
+
+    for _ in range(args.warmup):
+        call(0); call(1)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0.record(stream)
+        for s in range(args.steps):
+            call(0, events=ev[s][0])
+            call(1, events=ev[s][1])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * 2 * w["B"] * w["H"] * w["N"] / (ms / 1e3)
+
+    # per-stage averages over the timed region
+    stage_ms = {}
+    for i in range(2):
+        for j, name in enumerate(stages[i]):
+            key = f"{'causal' if cases[i].causal else 'bidir'}:{name}"
+            stage_ms[key] = statistics.mean(ev[s][i][j].elapsed_time(ev[s][i][j + 1]) for s in range(args.steps))
+    variant_ms = {("causal" if c.causal else "bidir"): statistics.mean(
+        ev[s][i][0].elapsed_time(ev[s][i][-1]) for s in range(args.steps)) for i, c in enumerate(cases)}
+    peak, peak_src = measured_peaks()
+    dom = max(stage_ms, key=stage_ms.get)
+    dom_stage = dom.split(":", 1)[1]
+    dom_bytes = tensor_bytes(STAGE_TENSORS.get(dom_stage, ""))
+    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+    traffic = recorded_traffic(dom)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "algorithmic_bytes": dom_bytes, "peak_source": peak_src}
+    fwd_bytes = tensor_bytes("QKVO")
+    variants = {k: {"ms": v, "token_heads_per_s": w["B"] * w["H"] * w["N"] / (v / 1e3),
+                    "hbm_frac_of_" + peak_src: fwd_bytes / (v / 1e3) / 1e9 / peak,
+                    "path": "tc" if paths[i] == gma.PATH_TC else "simt"}
+                for i, (k, v) in enumerate(variant_ms.items())}
+
+    # end to end through the public API: pinned host inputs, H2D + forward + D2H per step
+    pinned = [{k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in h.items()} for h in host]
+    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    h2d = sum(pinned[i][k].numel() * pinned[i][k].element_size() for i in range(2) for k in ("Q", "K", "V"))
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def e2e_step():
+        for i in range(2):
+            for k in ("Q", "K", "V"):
+                dinp[i][k].copy_(pinned[i][k], non_blocking=True)
+            call(i)
+            host_out[i].copy_(outs[i], non_blocking=True)
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e = {"value": world * 2 * w["B"] * w["H"] * w["N"] / (e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pairs, procs = 4, 4
+        pool = OraclePool(procs)
+        wall, th = pool.sample(pairs)
+        pool.close()
+        cpu = {"value": th / wall, "unit": UNIT, "cores": procs, "kind": "oracle",
+               "sample": f"{pairs} bidirectional + {pairs} causal heads of N=16384, d=K=64 "
+                         f"(fp64 C oracle, {procs} worker processes)"}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": "GMA forward, bidirectional + causal, B=4 H=8 N=16384 "
+                                      "d_r=d_v=K=64 bf16 (per GPU)",
+                          "global_batch": world * w["B"], "seq_len": w["N"], "heads": w["H"],
+                          "d_r": w["d_r"], "d_v": w["d_v"], "K": w["K"], "eps": w["eps"],
+                          "l2": "inputs larger than L2 (201 MB read + 134 MB written per variant), no flush",
+                          "output": "fp32 O",
+                          "parallelism": f"replicas x{world}"},
+               "gpu_launches": args.steps * sum(len(s) for s in stages),
+               "roofline": roofline, "variants": variants, "stage_ms": stage_ms,
+               "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_gma(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

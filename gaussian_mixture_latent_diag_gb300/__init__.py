@@ -1,0 +1,151 @@
+"""GMA forward hot path on GB300 (sm_103a): Python binding of libgma.so.
+
+    import gaussian_mixture_latent_diag_gb300 as gma
+    O = gma.forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6)
+    O = gma.forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6)
+    G = gma.responsibilities(X, mu, sigma2, log_pi)
+
+Tensors: Q, K, X [B, H, N, d_r], V [B, H, N, d_v] (CUDA, contiguous, fp32 or
+bf16); mu, sigma2 [H, K, d_r] and log_pi [H, K] fp32 CUDA.  The functions
+only marshal arguments; the arithmetic runs in libgma.so's CUDA kernels.
+PyTorch provides device memory and the current stream.
+
+Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+Probabilistic Latent Routing" (arXiv 2606.18283).
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError, load,
+                      options, status_string)
+
+__all__ = ["forward_bidir", "forward_causal", "responsibilities", "workspace_size",
+           "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
+           "PATH_TC", "load"]
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return GMA_F32
+    if t.dtype == torch.bfloat16:
+        return GMA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def workspace_size(B, H, N, d_r, d_v, K, dtype="bf16", causal=0, path=PATH_AUTO, splits=0) -> int:
+    """Workspace bytes for a call (causal: 0 bidir, 1 causal, -1 responsibilities)."""
+    code = GMA_F32 if dtype in ("f32", "float32") else GMA_BF16
+    opt = options(path=path, splits=splits)
+    return int(load().gma_workspace_size(B, H, N, d_r, d_v, K, code, causal, ctypes.byref(opt)))
+
+
+def selected_path(N, d_r, d_v, K, dtype="bf16", causal=0, path=PATH_AUTO) -> int:
+    code = GMA_F32 if dtype in ("f32", "float32") else GMA_BF16
+    opt = options(path=path)
+    return int(load().gma_selected_path(N, d_r, d_v, K, code, causal, ctypes.byref(opt)))
+
+
+def _workspace(nbytes: int, device, workspace):
+    import torch
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace too small: need {nbytes} bytes")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def last_device_status(workspace, stream=None) -> int:
+    """Synchronise the stream; device-side status of the last call on `workspace`."""
+    return int(load().gma_last_device_status(_ptr(workspace), _stream(stream)))
+
+
+def responsibilities(X, mu, sigma2, log_pi, out=None, workspace=None, stream=None,
+                     sync_status=False):
+    """Gamma [B, H, N, K] fp32: posterior responsibilities of the rows of X."""
+    import torch
+    lib = load()
+    _check_dev(X, mu, sigma2, log_pi)
+    B, H, N, d_r = X.shape
+    K = mu.shape[1]
+    code = _dtype_code(X)
+    if out is None:
+        out = torch.empty(B, H, N, K, dtype=torch.float32, device=X.device)
+    opt = options(sync_status=sync_status)
+    nb = int(lib.gma_workspace_size(B, H, N, d_r, 16, K, code, -1, ctypes.byref(opt)))
+    ws = _workspace(nb, X.device, workspace)
+    st = lib.gma_responsibilities(_ptr(X), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(out),
+                                  B, H, N, d_r, K, ctypes.byref(opt), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_responsibilities")
+    return out
+
+
+def _forward(fn_name, Q, K_, V, mu, sigma2, log_pi, eps, out, workspace, stream, path, splits,
+             sync_status, o_bf16=False, chunk=0):
+    import torch
+    lib = load()
+    _check_dev(Q, K_, V, mu, sigma2, log_pi)
+    B, H, N, d_r = Q.shape
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    if K_.shape != Q.shape or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("Q, K must be [B, H, N, d_r] and V [B, H, N, d_v]")
+    if mu.shape != (H, K, d_r) or sigma2.shape != (H, K, d_r) or log_pi.shape != (H, K):
+        raise ValueError("mu, sigma2 must be [H, K, d_r] and log_pi [H, K]")
+    code = _dtype_code(Q)
+    if K_.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K, V must share one dtype")
+    odt = torch.bfloat16 if o_bf16 else torch.float32
+    if out is None:
+        out = torch.empty(B, H, N, d_v, dtype=odt, device=Q.device)
+    elif out.dtype != odt or out.shape != V.shape:
+        raise ValueError(f"out must be {odt} of shape {tuple(V.shape)}")
+    causal = 1 if fn_name == "gma_forward_causal" else 0
+    opt = options(path=path, chunk=chunk, splits=splits, sync_status=sync_status, o_bf16=o_bf16)
+    nb = int(lib.gma_workspace_size(B, H, N, d_r, d_v, K, code, causal, ctypes.byref(opt)))
+    if nb == 0:
+        raise GmaError(2, fn_name)
+    ws = _workspace(nb, Q.device, workspace)
+    st = getattr(lib, fn_name)(_ptr(Q), _ptr(K_), _ptr(V), code, _ptr(mu), _ptr(sigma2),
+                               _ptr(log_pi), float(eps), _ptr(out), B, H, N, d_r, d_v, K,
+                               ctypes.byref(opt), _ptr(ws), ws.numel() * ws.element_size(),
+                               _stream(stream))
+    if st != 0:
+        raise GmaError(st, fn_name)
+    return out
+
+
+def forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None,
+                  path=PATH_AUTO, splits=0, sync_status=False, o_bf16=False):
+    """Bidirectional GMA: O = Gamma^Q (Gamma^K)^T V / (Gamma^Q Z + eps); O fp32 (or bf16)."""
+    return _forward("gma_forward_bidir", Q, K, V, mu, sigma2, log_pi, eps, out, workspace,
+                    stream, path, splits, sync_status, o_bf16)
+
+
+def forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None,
+                   path=PATH_AUTO, splits=0, sync_status=False, o_bf16=False):
+    """Causal GMA: prefix memories over keys j <= i; O fp32 (or bf16)."""
+    return _forward("gma_forward_causal", Q, K, V, mu, sigma2, log_pi, eps, out, workspace,
+                    stream, path, splits, sync_status, o_bf16)

@@ -1,0 +1,221 @@
+// gma_api.cu -- the C ABI of libgma.so: argument validation, workspace
+// sizing and dispatch to the kernel families.  Declarations and the contract
+// of every entry point are in include/gma.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "gma_internal.h"
+
+namespace {
+
+using gma::Problem;
+
+bool valid_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+bool shape_ok(int B, int H, int N, int d_r, int d_v, int K, bool need_dv) {
+    if (B < 1 || H < 1 || N < 1 || K < 1 || K > 128) return false;
+    if (!valid_dim(d_r)) return false;
+    if (need_dv && !valid_dim(d_v)) return false;
+    // element offsets must fit the 64-bit index arithmetic comfortably and
+    // B*H must fit a grid dimension
+    if ((long long)B * H > 65535LL) return false;
+    if ((long long)B * H * N > (1LL << 40)) return false;
+    return true;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+int choose_path(const Problem &p, int causal, const gma_options *opt) {
+    int path = opt ? opt->path : GMA_PATH_AUTO;
+    if (path == GMA_PATH_SIMT) return GMA_PATH_SIMT;
+    bool tc = causal >= 0 && gma::tc_supported(p, causal);
+    if (path == GMA_PATH_TC) return tc ? GMA_PATH_TC : -1;
+    if (path != GMA_PATH_AUTO) return -1;
+    return tc ? GMA_PATH_TC : GMA_PATH_SIMT;
+}
+
+size_t workspace_for(const Problem &p, int causal, const gma_options *opt, int path) {
+    int splits = opt ? opt->splits : 0;
+    if (path == GMA_PATH_TC) return gma::tc_workspace(p, causal, splits);
+    return gma::simt_layout(p, causal, splits).total;
+}
+
+gma::StageClock clock_for(const gma_options *opt, cudaStream_t s) {
+    gma::StageClock c;
+    if (opt && opt->stage_events && opt->n_stage_events > 0) {
+        c.events = opt->stage_events;
+        c.n = opt->n_stage_events;
+    }
+    c.stream = s;
+    return c;
+}
+
+gma_status finish(cudaError_t err, const gma_options *opt, void *ws, cudaStream_t s) {
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();  // clear a sticky launch error for the caller
+        return GMA_ERR_CUDA;
+    }
+    if (opt && opt->sync_status) return gma_last_device_status(ws, s);
+    return GMA_OK;
+}
+
+gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
+                   const float *mu, const float *sigma2, const float *log_pi, float eps,
+                   void *O, int B, int H, int N, int d_r, int d_v, int K,
+                   const gma_options *options, void *workspace, size_t workspace_bytes,
+                   void *stream, int causal) {
+    if (!Q_X || !K_X || !V_X || !mu || !sigma2 || !log_pi || !O || !workspace)
+        return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (options && (options->chunk < 0 || options->splits < 0)) return GMA_ERR_INVALID_ARG;
+
+    Problem p;
+    p.Q = Q_X; p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi;
+    p.O = O; p.dtype = dtype; p.eps = eps;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    p.o_bf16 = options && options->o_bf16;
+
+    const size_t es = dtype == GMA_F32 ? 4 : 2;
+    const size_t nr = es * (size_t)B * H * N * d_r, nv = es * (size_t)B * H * N * d_v;
+    const size_t no = (p.o_bf16 ? 2 : 4) * (size_t)B * H * N * d_v;
+    const int path = choose_path(p, causal, options);
+    if (path < 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = workspace_for(p, causal, options, path);
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    if (overlaps(O, no, Q_X, nr) || overlaps(O, no, K_X, nr) || overlaps(O, no, V_X, nv) ||
+        overlaps(O, no, workspace, need) || overlaps(workspace, need, Q_X, nr) ||
+        overlaps(workspace, need, K_X, nr) || overlaps(workspace, need, V_X, nv))
+        return GMA_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int splits = options ? options->splits : 0;
+    gma::StageClock clk = clock_for(options, s);
+    cudaError_t err;
+    if (path == GMA_PATH_TC)
+        err = causal ? gma::tc_causal(p, splits, workspace, s, clk) : gma::tc_bidir(p, splits, workspace, s, clk);
+    else
+        err = causal ? gma::simt_causal(p, workspace, s, clk) : gma::simt_bidir(p, splits, workspace, s, clk);
+    return finish(err, options, workspace, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gma_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
+                          int causal, const gma_options *options) {
+    if (causal < -1 || causal > 1) return 0;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return 0;
+    if (!shape_ok(B, H, N, d_r, d_v, K, causal >= 0)) return 0;
+    Problem p;
+    p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = causal >= 0 ? d_v : 16; p.K = K;
+    int path = choose_path(p, causal, options);
+    if (path < 0) return 0;
+    return workspace_for(p, causal, options, path);
+}
+
+gma_status gma_responsibilities(const void *X, gma_dtype dtype, const float *mu,
+                                const float *sigma2, const float *log_pi, float *Gamma,
+                                int B, int H, int N, int d_r, int K,
+                                const gma_options *options, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    if (!X || !mu || !sigma2 || !log_pi || !Gamma || !workspace) return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, 16, K, false)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (options && (options->path != GMA_PATH_AUTO && options->path != GMA_PATH_SIMT))
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+    Problem p;
+    p.Q = X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = Gamma; p.dtype = dtype;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = 16; p.K = K;
+    const size_t need = gma::simt_layout(p, -1, 0).total;
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t es = dtype == GMA_F32 ? 4 : 2;
+    const size_t nx = es * (size_t)B * H * N * d_r, ng = sizeof(float) * (size_t)B * H * N * K;
+    if (overlaps(Gamma, ng, X, nx) || overlaps(Gamma, ng, workspace, need) ||
+        overlaps(workspace, need, X, nx))
+        return GMA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    return finish(gma::simt_responsibilities(p, workspace, s, clk), options, workspace, s);
+}
+
+gma_status gma_forward_bidir(const void *Q_X, const void *K_X, const void *V_X,
+                             gma_dtype dtype, const float *mu, const float *sigma2,
+                             const float *log_pi, float eps, void *O,
+                             int B, int H, int N, int d_r, int d_v, int K,
+                             const gma_options *options, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    return forward(Q_X, K_X, V_X, dtype, mu, sigma2, log_pi, eps, O, B, H, N, d_r, d_v, K,
+                   options, workspace, workspace_bytes, stream, 0);
+}
+
+gma_status gma_forward_causal(const void *Q_X, const void *K_X, const void *V_X,
+                              gma_dtype dtype, const float *mu, const float *sigma2,
+                              const float *log_pi, float eps, void *O,
+                              int B, int H, int N, int d_r, int d_v, int K,
+                              const gma_options *options, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    return forward(Q_X, K_X, V_X, dtype, mu, sigma2, log_pi, eps, O, B, H, N, d_r, d_v, K,
+                   options, workspace, workspace_bytes, stream, 1);
+}
+
+gma_status gma_last_device_status(const void *workspace, void *stream) {
+    if (!workspace) return GMA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned st = 0;
+    if (cudaMemcpyAsync(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GMA_ERR_CUDA;
+    }
+    return static_cast<gma_status>(st);
+}
+
+const char *gma_status_string(gma_status status) {
+    switch (status) {
+        case GMA_OK: return "ok";
+        case GMA_ERR_INVALID_ARG: return "invalid argument";
+        case GMA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case GMA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case GMA_ERR_CUDA: return "CUDA error";
+        case GMA_ERR_TIMEOUT: return "device-side wait timed out";
+        case GMA_ERR_NONFINITE_PARAM: return "invalid mixture parameter (sigma2 <= 0 or non-finite)";
+    }
+    return "unknown status";
+}
+
+int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causal,
+                      const gma_options *options) {
+    if (causal < 0 || causal > 1 || (dtype != GMA_F32 && dtype != GMA_BF16)) return -1;
+    if (!shape_ok(1, 1, N, d_r, d_v, K, true)) return -1;
+    Problem p;
+    p.dtype = dtype; p.B = 1; p.H = 1; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    return choose_path(p, causal, options);
+}
+
+int gma_stage_count(int path, int variant) {
+    if (variant < -1 || variant > 1) return 0;
+    const char *const *names;
+    if (path == GMA_PATH_SIMT) names = gma::kSimtStages[variant + 1];
+    else if (path == GMA_PATH_TC) names = gma::kTcStages[variant + 1];
+    else return 0;
+    int n = 0;
+    while (n < 8 && names[n]) ++n;
+    return n;
+}
+
+const char *gma_stage_name(int path, int variant, int j) {
+    int n = gma_stage_count(path, variant);
+    if (j < 0 || j >= n) return nullptr;
+    return path == GMA_PATH_SIMT ? gma::kSimtStages[variant + 1][j] : gma::kTcStages[variant + 1][j];
+}
+
+}  // extern "C"

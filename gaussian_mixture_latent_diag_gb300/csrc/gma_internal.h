@@ -1,0 +1,72 @@
+// gma_internal.h -- declarations shared by the host API (gma_api.cu) and the
+// kernel translation units of libgma.so.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gma.h"
+
+namespace gma {
+
+struct Problem {
+    const void *Q = nullptr;   // or X for the responsibilities entry point
+    const void *Kx = nullptr;
+    const void *V = nullptr;
+    const float *mu = nullptr, *sigma2 = nullptr, *log_pi = nullptr;
+    void *O = nullptr;         // or Gamma (fp32) for the responsibilities entry point
+    gma_dtype dtype = GMA_F32;  // inputs
+    bool o_bf16 = false;        // output O in bf16 instead of fp32
+    float eps = 0.f;
+    int B = 0, H = 0, N = 0, d_r = 0, d_v = 0, K = 0;
+    int BH() const { return B * H; }
+};
+
+// Records stage boundaries on the caller's events (gma_options.stage_events).
+struct StageClock {
+    void **events = nullptr;
+    int n = 0, next = 0;
+    cudaStream_t stream = nullptr;
+    void mark() {
+        if (events && next < n && events[next]) {
+            // a failed record (e.g. a destroyed event) must not be reported as a
+            // launch failure of the next stage
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[next]), stream) != cudaSuccess)
+                (void)cudaGetLastError();
+        }
+        ++next;
+    }
+};
+
+// Every workspace region starts on a 256-byte boundary.
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device status word lives in the first 256 bytes of every workspace.
+constexpr size_t kStatusBytes = 256;
+
+// ---------------------------------------------------------------- SIMT path
+struct SimtLayout {
+    size_t inv_s2 = 0, cprime = 0;   // [H][K][d_r], [H][K] fp32
+    size_t gq = 0, gk = 0;           // [BH][K][N] fp32 (component-major)
+    size_t partial = 0;              // [BH][nsplit][K][d_v + 1] fp32
+    size_t mem = 0;                  // [BH][K][d_v + 1] fp32 (bidirectional only)
+    size_t total = 0;
+    int nsplit = 0, tokens_per_split = 0;
+};
+constexpr int kSimtCausalChunk = 64;
+SimtLayout simt_layout(const Problem &p, int mode /* -1 resp, 0 bidir, 1 causal */, int splits);
+
+cudaError_t simt_responsibilities(const Problem &p, void *ws, cudaStream_t s, StageClock &clk);
+cudaError_t simt_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
+cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &clk);
+extern const char *const kSimtStages[3][8];  // [variant + 1][j], NULL-terminated
+
+// ---------------------------------------------------------------- tensor-core path
+bool tc_supported(const Problem &p, int causal);
+size_t tc_workspace(const Problem &p, int causal, int splits);
+cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
+cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
+extern const char *const kTcStages[3][8];    // [variant + 1][j], NULL-terminated
+
+}  // namespace gma

@@ -1,0 +1,530 @@
+// gma_simt.cu -- fp32 CUDA-core kernels for the GMA forward pass.
+//
+// This family serves fp32 inputs and every supported size; it evaluates the
+// log-density in centred form in fp32, which is accurate enough for the
+// fp32 tolerance.  Each step materialises its result in the workspace:
+//   prep   : 1/sigma2 and c'_k = log pi_k - 1/2 sum_j log sigma2_kj per head
+//   resp   : Gamma^Q, Gamma^K, component-major [BH][K][N]
+//   write  : per-split (or per-chunk) partial latent memories [K][d_v + 1]
+//   reduce : fixed-order sum of the splits (bidirectional) /
+//   scan   : fixed-order exclusive prefix over chunks (causal)
+//   read   : O rows (bidirectional) / chunked causal outputs
+//
+// Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+// Probabilistic Latent Routing" (arXiv 2606.18283), cited [GMA, ...].
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "gma_internal.h"
+
+namespace gma {
+namespace {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ bool failed(const unsigned *status) {
+    return *reinterpret_cast<const volatile unsigned *>(status) != 0u;
+}
+
+// Records the first device-side error of a call (later ones are dropped).
+__device__ __forceinline__ void set_status(unsigned *status, unsigned code) {
+    atomicCAS(status, 0u, code);
+}
+
+// Per-head constants of the centred log-density ([GMA, Eqs. (2)-(3)]):
+//   s_ik = c'_k - 1/2 sum_j (x_j - mu_kj)^2 * inv_kj,
+//   inv_kj = 1 / sigma2_kj,  c'_k = log pi_k - 1/2 sum_j log sigma2_kj.
+// Also validates the parameter values.
+__global__ void prep_simt_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
+                                 const float *__restrict__ log_pi, int K, int d_r,
+                                 float *__restrict__ inv, float *__restrict__ cprime,
+                                 unsigned *status) {
+    const int h = blockIdx.x;
+    const size_t base = (size_t)h * K * d_r;
+    for (int e = threadIdx.x; e < K * d_r; e += blockDim.x) {
+        float s2 = sigma2[base + e], m = mu[base + e];
+        if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+        inv[base + e] = 1.0f / s2;
+    }
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        double acc = 0.0;
+        for (int j = 0; j < d_r; ++j) acc += log((double)sigma2[base + (size_t)k * d_r + j]);
+        float lp = log_pi[(size_t)h * K + k];
+        if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+        cprime[(size_t)h * K + k] = (float)((double)lp - 0.5 * acc);
+    }
+}
+
+// One thread per row: scores, then a max-subtracted softmax over k
+// ([GMA, Eq. (3)]).  The row is written three times to `out` (scores,
+// exponentials, normalised values); each thread only touches its own row.
+template <int D_R, typename T>
+__global__ void __launch_bounds__(128) resp_simt_kernel(
+    const T *__restrict__ X, int H, int N, int K, const float *__restrict__ mu,
+    const float *__restrict__ inv, const float *__restrict__ cprime, float *out,
+    long long out_bh_stride, long long out_stride_n, long long out_stride_k,
+    const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y, h = bh % H;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N) return;
+    float x[D_R];
+    const T *xr = X + ((size_t)bh * N + i) * D_R;
+#pragma unroll
+    for (int j = 0; j < D_R; ++j) x[j] = to_f32(xr[j]);
+    const float *muh = mu + (size_t)h * K * D_R;
+    const float *invh = inv + (size_t)h * K * D_R;
+    const float *ch = cprime + (size_t)h * K;
+    float *o = out + (size_t)bh * out_bh_stride + (size_t)i * out_stride_n;
+
+    float m = -INFINITY;
+    for (int k = 0; k < K; ++k) {
+        const float *mk = muh + (size_t)k * D_R, *ik = invh + (size_t)k * D_R;
+        // Eight interleaved partial sums, combined in fp64: the terms are
+        // positive and the total reaches several hundred at d_r = 128, where
+        // one sequential fp32 sum loses the fp32 tolerance.
+        float q8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q8[u] = 0.f;
+#pragma unroll
+        for (int j = 0; j < D_R; ++j) {
+            float d = x[j] - __ldg(mk + j);
+            q8[j & 7] = fmaf(d * d, __ldg(ik + j), q8[j & 7]);
+        }
+        double q = 0.0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q += (double)q8[u];
+        float s = (float)((double)__ldg(ch + k) - 0.5 * q);
+        o[(size_t)k * out_stride_k] = s;
+        m = fmaxf(m, s);
+    }
+    float z = 0.f;
+    for (int k = 0; k < K; ++k) {
+        float e = expf(o[(size_t)k * out_stride_k] - m);
+        o[(size_t)k * out_stride_k] = e;
+        z += e;
+    }
+    const float rz = 1.0f / z;
+    for (int k = 0; k < K; ++k) o[(size_t)k * out_stride_k] *= rz;
+}
+
+// Latent aggregation over one range of keys ([GMA, Eqs. (5)-(6)]):
+//   part[k][c] = sum_{j in range} gK_jk V_jc (c < d_v),  part[k][d_v] = sum gK_jk.
+// Block: 256 threads, each owns an 8 x 8 tile of (k, c); keys staged 32 at a
+// time in shared memory.  Fixed summation order.
+constexpr int kWT = 32;  // keys per shared-memory stage
+template <typename T>
+__global__ void __launch_bounds__(256) write_simt_kernel(
+    const float *__restrict__ gkt, const T *__restrict__ V, int N, int K, int d_v,
+    int tokens_per_split, int nsplit, float *__restrict__ part, const unsigned *status) {
+    if (failed(status)) return;
+    __shared__ float sg[128][kWT + 1];
+    __shared__ float sv[kWT][128 + 4];
+    const int split = blockIdx.x, bh = blockIdx.y;
+    const int t0 = split * tokens_per_split;
+    const int t1 = min(N, t0 + tokens_per_split);
+    const int tiles_c = (d_v + 7) / 8, tiles_k = (K + 7) / 8;
+    const int tk = threadIdx.x / tiles_c, tc = threadIdx.x % tiles_c;
+    const bool active = tk < tiles_k;
+    float acc[8][8];
+    float zacc[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        zacc[a] = 0.f;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+    }
+    const float *g = gkt + (size_t)bh * K * N;
+    const T *v = V + (size_t)bh * N * d_v;
+    for (int base = t0; base < t1; base += kWT) {
+        const int n = min(kWT, t1 - base);
+        __syncthreads();
+        for (int e = threadIdx.x; e < K * kWT; e += blockDim.x) {
+            int k = e / kWT, t = e % kWT;
+            sg[k][t] = t < n ? g[(size_t)k * N + base + t] : 0.f;
+        }
+        for (int e = threadIdx.x; e < kWT * d_v; e += blockDim.x) {
+            int t = e / d_v, c = e % d_v;
+            sv[t][c] = t < n ? to_f32(v[(size_t)(base + t) * d_v + c]) : 0.f;
+        }
+        __syncthreads();
+        if (active) {
+            for (int t = 0; t < n; ++t) {
+                float ga[8], vb[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    int k = tk * 8 + a;
+                    ga[a] = k < K ? sg[k][t] : 0.f;
+                }
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    int c = tc * 8 + b;
+                    vb[b] = c < d_v ? sv[t][c] : 0.f;
+                }
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    zacc[a] += ga[a];
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(ga[a], vb[b], acc[a][b]);
+                }
+            }
+        }
+    }
+    if (!active) return;
+    const int W = d_v + 1;
+    float *p = part + ((size_t)bh * nsplit + split) * K * W;
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        int k = tk * 8 + a;
+        if (k >= K) continue;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            int c = tc * 8 + b;
+            if (c < d_v) p[(size_t)k * W + c] = acc[a][b];
+        }
+        if (tc == 0) p[(size_t)k * W + d_v] = zacc[a];
+    }
+}
+
+// Fixed-order sum of the split partials: mem[bh] = sum_s part[bh][s].
+__global__ void reduce_splits_kernel(const float *__restrict__ part, int nsplit, int E,
+                                     float *__restrict__ mem, const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const float *p = part + (size_t)bh * nsplit * E + e;
+    float acc = 0.f;
+    for (int s = 0; s < nsplit; ++s) acc += p[(size_t)s * E];
+    mem[(size_t)bh * E + e] = acc;
+}
+
+// In-place exclusive prefix over the chunk partials of each head, in chunk
+// order: part[c] <- sum_{c' < c} part[c'] (the causal prefix memory at the
+// start of chunk c, [GMA, causal variant, cumulative sums]).
+__global__ void scan_chunks_kernel(float *__restrict__ part, int nchunk, int E,
+                                   const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float *p = part + (size_t)bh * nchunk * E + e;
+    float run = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+        float cur = p[(size_t)c * E];
+        p[(size_t)c * E] = run;
+        run += cur;
+    }
+}
+
+// Normalised broadcasting ([GMA, Eq. (7)]): one thread per query row,
+// O_i = (sum_k gQ_ik Vt_k) / (sum_k gQ_ik Z_k + eps).
+template <int D_V, typename TO>
+__global__ void __launch_bounds__(128) read_simt_kernel(
+    const float *__restrict__ gqt, const float *__restrict__ mem, int N, int K, float eps,
+    TO *__restrict__ O, const unsigned *status) {
+    if (failed(status)) return;
+    extern __shared__ float smem[];
+    const int W = D_V + 1;
+    const int bh = blockIdx.y;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) smem[e] = mem[(size_t)bh * K * W + e];
+    __syncthreads();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N) return;
+    float acc[D_V];
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    float den = 0.f;
+    const float *g = gqt + (size_t)bh * K * N + i;
+    for (int k = 0; k < K; ++k) {
+        float gk = g[(size_t)k * N];
+        const float *row = smem + k * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(gk, row[c], acc[c]);
+        den = fmaf(gk, row[D_V], den);
+    }
+    const float r = 1.0f / (den + eps);
+    TO *o = O + ((size_t)bh * N + i) * D_V;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) o[c] = from_f32<TO>(acc[c] * r);
+}
+
+// Causal outputs of one chunk of C = 64 queries ([GMA, Eq. (8b)]), given the
+// exclusive prefix memory (S, Z) at the chunk start:
+//   O_i = (gQ_i S + sum_{t0<=j<=i} <gQ_i, gK_j> V_j)
+//         / (gQ_i Z + sum_{t0<=j<=i} <gQ_i, gK_j> + eps).
+template <int D_V, typename T, typename TO>
+__global__ void __launch_bounds__(kSimtCausalChunk) causal_simt_kernel(
+    const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
+    const float *__restrict__ prefix, int N, int K, int nchunk, float eps, TO *__restrict__ O,
+    const unsigned *status) {
+    if (failed(status)) return;
+    constexpr int C = kSimtCausalChunk;
+    constexpr int W = D_V + 1;
+    extern __shared__ float smem[];
+    float *sgq = smem;              // [K][C]
+    float *sgk = sgq + K * C;       // [K][C]
+    float *sv = sgk + K * C;        // [C][D_V]
+    float *ss = sv + C * D_V;       // [K][W]
+    const int chunk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = chunk * C;
+    const int n = min(C, N - t0);
+    const float *gq = gqt + (size_t)bh * K * N, *gk = gkt + (size_t)bh * K * N;
+    for (int e = threadIdx.x; e < K * C; e += blockDim.x) {
+        int k = e / C, t = e % C;
+        sgq[e] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
+        sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
+    }
+    const T *v = V + ((size_t)bh * N + t0) * D_V;
+    for (int e = threadIdx.x; e < C * D_V; e += blockDim.x) sv[e] = e < n * D_V ? to_f32(v[e]) : 0.f;
+    const float *pre = prefix + ((size_t)bh * nchunk + chunk) * K * W;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) ss[e] = pre[e];
+    __syncthreads();
+    const int i = threadIdx.x;
+    if (i >= n) return;
+    float acc[D_V];
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    float den = 0.f;
+    for (int k = 0; k < K; ++k) {
+        float g = sgq[k * C + i];
+        const float *row = ss + k * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(g, row[c], acc[c]);
+        den = fmaf(g, row[D_V], den);
+    }
+    for (int j = 0; j <= i; ++j) {
+        float a = 0.f;
+        for (int k = 0; k < K; ++k) a = fmaf(sgq[k * C + i], sgk[k * C + j], a);
+        den += a;
+        const float *vr = sv + j * D_V;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(a, vr[c], acc[c]);
+    }
+    const float r = 1.0f / (den + eps);
+    TO *o = O + ((size_t)bh * N + t0 + i) * D_V;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) o[c] = from_f32<TO>(acc[c] * r);
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <typename T>
+cudaError_t launch_resp(const Problem &p, const void *X, const float *inv, const float *cprime,
+                        float *out, long long bh_stride, long long sn, long long sk,
+                        const unsigned *status, cudaStream_t s) {
+    dim3 grid((p.N + 127) / 128, p.BH());
+    const T *x = static_cast<const T *>(X);
+    switch (p.d_r) {
+        case 16: resp_simt_kernel<16, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 32: resp_simt_kernel<32, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 64: resp_simt_kernel<64, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 128: resp_simt_kernel<128, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template <int D_V, typename TO>
+cudaError_t launch_read_dv(const Problem &p, const float *gq, const float *mem,
+                           const unsigned *status, cudaStream_t s) {
+    size_t smem = (size_t)p.K * (D_V + 1) * sizeof(float);
+    auto kern = read_simt_kernel<D_V, TO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + 127) / 128, p.BH());
+    kern<<<grid, 128, smem, s>>>(gq, mem, p.N, p.K, p.eps, static_cast<TO *>(p.O), status);
+    return cudaGetLastError();
+}
+
+template <typename TO>
+cudaError_t launch_read(const Problem &p, const float *gq, const float *mem,
+                        const unsigned *status, cudaStream_t s) {
+    switch (p.d_v) {
+        case 16: return launch_read_dv<16, TO>(p, gq, mem, status, s);
+        case 32: return launch_read_dv<32, TO>(p, gq, mem, status, s);
+        case 64: return launch_read_dv<64, TO>(p, gq, mem, status, s);
+        case 128: return launch_read_dv<128, TO>(p, gq, mem, status, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D_V, typename T, typename TO>
+cudaError_t launch_causal_dv(const Problem &p, const float *gq, const float *gk,
+                             const float *prefix, int nchunk, const unsigned *status,
+                             cudaStream_t s) {
+    constexpr int C = kSimtCausalChunk;
+    size_t smem = ((size_t)2 * p.K * C + (size_t)C * D_V + (size_t)p.K * (D_V + 1)) * sizeof(float);
+    auto kern = causal_simt_kernel<D_V, T, TO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(nchunk, p.BH());
+    kern<<<grid, C, smem, s>>>(gq, gk, static_cast<const T *>(p.V), prefix, p.N, p.K, nchunk,
+                               p.eps, static_cast<TO *>(p.O), status);
+    return cudaGetLastError();
+}
+
+template <typename T, typename TO>
+cudaError_t launch_causal(const Problem &p, const float *gq, const float *gk,
+                          const float *prefix, int nchunk, const unsigned *status,
+                          cudaStream_t s) {
+    switch (p.d_v) {
+        case 16: return launch_causal_dv<16, T, TO>(p, gq, gk, prefix, nchunk, status, s);
+        case 32: return launch_causal_dv<32, T, TO>(p, gq, gk, prefix, nchunk, status, s);
+        case 64: return launch_causal_dv<64, T, TO>(p, gq, gk, prefix, nchunk, status, s);
+        case 128: return launch_causal_dv<128, T, TO>(p, gq, gk, prefix, nchunk, status, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+#define GMA_TRY(x)                              \
+    do {                                        \
+        cudaError_t err_ = (x);                 \
+        if (err_ != cudaSuccess) return err_;   \
+    } while (0)
+
+struct Ptrs {
+    unsigned *status;
+    float *inv, *cprime, *gq, *gk, *part, *mem;
+};
+
+Ptrs ptrs(const SimtLayout &L, void *ws) {
+    char *b = static_cast<char *>(ws);
+    return {reinterpret_cast<unsigned *>(b), reinterpret_cast<float *>(b + L.inv_s2),
+            reinterpret_cast<float *>(b + L.cprime), reinterpret_cast<float *>(b + L.gq),
+            reinterpret_cast<float *>(b + L.gk), reinterpret_cast<float *>(b + L.partial),
+            reinterpret_cast<float *>(b + L.mem)};
+}
+
+cudaError_t prep(const Problem &p, const Ptrs &P, cudaStream_t s) {
+    GMA_TRY(cudaMemsetAsync(P.status, 0, sizeof(unsigned), s));
+    prep_simt_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, P.inv, P.cprime, P.status);
+    return cudaGetLastError();
+}
+
+cudaError_t resp_both(const Problem &p, const Ptrs &P, cudaStream_t s, StageClock &clk) {
+    const long long bhs = (long long)p.K * p.N;
+    if (p.dtype == GMA_F32) {
+        GMA_TRY(launch_resp<float>(p, p.Q, P.inv, P.cprime, P.gq, bhs, 1, p.N, P.status, s));
+        clk.mark();
+        GMA_TRY(launch_resp<float>(p, p.Kx, P.inv, P.cprime, P.gk, bhs, 1, p.N, P.status, s));
+    } else {
+        GMA_TRY(launch_resp<__nv_bfloat16>(p, p.Q, P.inv, P.cprime, P.gq, bhs, 1, p.N, P.status, s));
+        clk.mark();
+        GMA_TRY(launch_resp<__nv_bfloat16>(p, p.Kx, P.inv, P.cprime, P.gk, bhs, 1, p.N, P.status, s));
+    }
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t write_parts(const Problem &p, const SimtLayout &L, const Ptrs &P, cudaStream_t s) {
+    dim3 grid(L.nsplit, p.BH());
+    if (p.dtype == GMA_F32)
+        write_simt_kernel<float><<<grid, 256, 0, s>>>(P.gk, static_cast<const float *>(p.V), p.N, p.K, p.d_v,
+                                                      L.tokens_per_split, L.nsplit, P.part, P.status);
+    else
+        write_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(P.gk, static_cast<const __nv_bfloat16 *>(p.V), p.N,
+                                                              p.K, p.d_v, L.tokens_per_split, L.nsplit, P.part, P.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+SimtLayout simt_layout(const Problem &p, int mode, int splits) {
+    SimtLayout L;
+    size_t off = kStatusBytes;
+    L.inv_s2 = off; off = align256(off + sizeof(float) * (size_t)p.H * p.K * p.d_r);
+    L.cprime = off; off = align256(off + sizeof(float) * (size_t)p.H * p.K);
+    if (mode >= 0) {
+        const size_t g = sizeof(float) * (size_t)p.BH() * p.K * p.N;
+        L.gq = off; off = align256(off + g);
+        L.gk = off; off = align256(off + g);
+        if (mode == 0) {
+            int ns = splits > 0 ? splits : (p.N + 1023) / 1024;
+            ns = ns < 1 ? 1 : (ns > p.N ? p.N : ns);
+            L.tokens_per_split = (p.N + ns - 1) / ns;
+            L.nsplit = (p.N + L.tokens_per_split - 1) / L.tokens_per_split;
+        } else {
+            L.tokens_per_split = kSimtCausalChunk;
+            L.nsplit = (p.N + kSimtCausalChunk - 1) / kSimtCausalChunk;
+        }
+        const size_t W = (size_t)p.d_v + 1;
+        L.partial = off; off = align256(off + sizeof(float) * (size_t)p.BH() * L.nsplit * p.K * W);
+        if (mode == 0) { L.mem = off; off = align256(off + sizeof(float) * (size_t)p.BH() * p.K * W); }
+    }
+    L.total = off;
+    return L;
+}
+
+const char *const kSimtStages[3][8] = {
+    {"prep", "resp", nullptr},
+    {"prep", "resp_q", "resp_k", "write", "reduce", "read", nullptr},
+    {"prep", "resp_q", "resp_k", "write", "scan", "causal", nullptr},
+};
+
+cudaError_t simt_responsibilities(const Problem &p, void *ws, cudaStream_t s, StageClock &clk) {
+    SimtLayout L = simt_layout(p, -1, 0);
+    Ptrs P = ptrs(L, ws);
+    clk.mark();
+    GMA_TRY(prep(p, P, s));
+    clk.mark();
+    float *G = static_cast<float *>(p.O);
+    const long long bhs = (long long)p.N * p.K;
+    if (p.dtype == GMA_F32) GMA_TRY(launch_resp<float>(p, p.Q, P.inv, P.cprime, G, bhs, p.K, 1, P.status, s));
+    else GMA_TRY(launch_resp<__nv_bfloat16>(p, p.Q, P.inv, P.cprime, G, bhs, p.K, 1, P.status, s));
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t simt_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
+    SimtLayout L = simt_layout(p, 0, splits);
+    Ptrs P = ptrs(L, ws);
+    clk.mark();
+    GMA_TRY(prep(p, P, s));
+    clk.mark();
+    GMA_TRY(resp_both(p, P, s, clk));
+    GMA_TRY(write_parts(p, L, P, s));
+    clk.mark();
+    const int E = p.K * (p.d_v + 1);
+    reduce_splits_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.mem, P.status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    if (p.o_bf16) GMA_TRY(launch_read<__nv_bfloat16>(p, P.gq, P.mem, P.status, s));
+    else GMA_TRY(launch_read<float>(p, P.gq, P.mem, P.status, s));
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &clk) {
+    SimtLayout L = simt_layout(p, 1, 0);
+    Ptrs P = ptrs(L, ws);
+    clk.mark();
+    GMA_TRY(prep(p, P, s));
+    clk.mark();
+    GMA_TRY(resp_both(p, P, s, clk));
+    GMA_TRY(write_parts(p, L, P, s));
+    clk.mark();
+    const int E = p.K * (p.d_v + 1);
+    scan_chunks_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    if (p.dtype == GMA_F32 && !p.o_bf16)
+        GMA_TRY((launch_causal<float, float>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    else if (p.dtype == GMA_F32)
+        GMA_TRY((launch_causal<float, __nv_bfloat16>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    else if (!p.o_bf16)
+        GMA_TRY((launch_causal<__nv_bfloat16, float>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    else
+        GMA_TRY((launch_causal<__nv_bfloat16, __nv_bfloat16>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    clk.mark();
+    return cudaSuccess;
+}
+
+}  // namespace gma

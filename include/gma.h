@@ -1,0 +1,164 @@
+/*
+ * gma.h -- C ABI of libgma.so: the forward hot path of Gaussian Mixture
+ * Attention (GMA) on NVIDIA GB300 (sm_103a).
+ *
+ * Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+ * Probabilistic Latent Routing" (arXiv 2606.18283), cited [GMA, ...].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, contiguous, row-major:
+ *     X, Q_X, K_X : [B, H, N, d_r]   V_X, O : [B, H, N, d_v]   Gamma : [B, H, N, K]
+ *   O is fp32 (the value of the fp32 accumulation, not rounded further)
+ *   unless gma_options.o_bf16 asks for bfloat16 output.
+ *     mu, sigma2  : [H, K, d_r] fp32 log_pi : [H, K] fp32
+ *   One mixture (mu, sigma2, pi) per head h, shared by every batch entry and
+ *   by the query and key side of that head ([GMA, "a shared Gaussian
+ *   mixture", applied separately to Q_X and K_X]).
+ * - Every pointer argument except the host-side `options` is a DEVICE pointer
+ *   on the current CUDA device.  The caller owns all buffers, including the
+ *   workspace; the library never allocates or frees device memory and keeps
+ *   no state between calls.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Calls are asynchronous on that stream.
+ * - Host-detectable errors (null pointers, bad sizes, aliasing, short
+ *   workspace) are returned before anything is launched.  Invalid parameter
+ *   VALUES (sigma2 <= 0 or non-finite, non-finite mu or log_pi) and device
+ *   timeouts are detected on the device: they are written to a status word
+ *   at the start of the workspace, the remaining kernels of the call skip
+ *   their work (O / Gamma are then left unwritten), and the status is
+ *   returned by gma_last_device_status() -- or directly, when
+ *   options->sync_status is set.
+ * - Inputs must not overlap O / Gamma or the workspace.
+ * - Results are deterministic: the same inputs, sizes and options give
+ *   bitwise-identical outputs (fixed-order reductions, no atomics on data).
+ * - Supported sizes: B, H, N >= 1; d_r, d_v in {16, 32, 64, 128};
+ *   1 <= K <= 128.  Anything else returns GMA_ERR_UNSUPPORTED_SHAPE.
+ */
+#ifndef GMA_H_
+#define GMA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of X / Q_X / K_X / V_X (Gamma and, by default, O are fp32). */
+typedef enum gma_dtype {
+    GMA_F32 = 0,  /* IEEE binary32 */
+    GMA_BF16 = 1  /* bfloat16 */
+} gma_dtype;
+
+typedef enum gma_status {
+    GMA_OK = 0,
+    GMA_ERR_INVALID_ARG = 1,        /* null pointer, eps <= 0 or non-finite, aliasing, bad option */
+    GMA_ERR_UNSUPPORTED_SHAPE = 2,  /* sizes outside the supported set */
+    GMA_ERR_WORKSPACE_TOO_SMALL = 3,
+    GMA_ERR_CUDA = 4,               /* a CUDA runtime call failed (launch, attribute, ...) */
+    GMA_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out */
+    GMA_ERR_NONFINITE_PARAM = 6     /* sigma2 <= 0 or non-finite, or non-finite mu / log_pi */
+} gma_status;
+
+/* Kernel family selector (gma_options.path). */
+enum {
+    GMA_PATH_AUTO = 0,   /* tensor-core path when the dtype/sizes allow it, else SIMT */
+    GMA_PATH_SIMT = 1,   /* fp32 CUDA-core kernels (every supported size, fp32 or bf16 input) */
+    GMA_PATH_TC = 2      /* tcgen05 tensor-core kernels; GMA_ERR_UNSUPPORTED_SHAPE if not eligible */
+};
+
+/* Optional knobs; pass NULL for all defaults.  Zero in a field = default. */
+typedef struct gma_options {
+    int path;         /* GMA_PATH_* */
+    int chunk;        /* causal chunk length in tokens (0 = the kernel family's only supported value) */
+    int splits;       /* number of N-splits of the key pass per head (0 = chosen from the grid) */
+    int sync_status;  /* nonzero: synchronise `stream` before returning and return the device status */
+    int o_bf16;       /* nonzero: O is bfloat16, rounded to nearest even from fp32 (default fp32) */
+    /* Optional profiling hook: an array of n_stage_events cudaEvent_t (passed
+     * as void*).  When non-NULL, event 0 is recorded on `stream` before the
+     * first stage of the call and event j+1 after stage j, for as many
+     * events as are given; the stages of a call are named by
+     * gma_stage_name().  The events are owned by the caller. */
+    void **stage_events;
+    int n_stage_events;
+} gma_options;
+
+/*
+ * Bytes of device workspace that a call with these sizes needs (256-byte
+ * aligned start required).  causal: 0 for gma_forward_bidir, 1 for
+ * gma_forward_causal, -1 for gma_responsibilities.  Returns 0 for sizes that
+ * are not supported.
+ */
+size_t gma_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
+                          int causal, const gma_options *options);
+
+/*
+ * Gamma[b,h,i,k] = p(z = k | x_i), the posterior responsibility of
+ * component k of head h for row i of X ([GMA, Eqs. (2)-(3)]): a softmax over
+ * k of log N(x_i; mu_k, diag sigma2_k) + log pi_k.  log_pi need not be
+ * normalised (the softmax is invariant to a shift).  Gamma is fp32.
+ */
+gma_status gma_responsibilities(const void *X, gma_dtype dtype, const float *mu,
+                                const float *sigma2, const float *log_pi, float *Gamma,
+                                int B, int H, int N, int d_r, int K,
+                                const gma_options *options, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * Bidirectional GMA forward ([GMA, Eqs. (5)-(7), footnote 4]):
+ *   Vt = (Gamma^K)^T V_X,  Z = (Gamma^K)^T 1,  O = Gamma^Q Vt / (Gamma^Q Z + eps)
+ * per (b, h), with Gamma^Q / Gamma^K the responsibilities of Q_X / K_X.
+ * eps > 0 is added after the sum over components.  O is fp32 (bf16 with
+ * options->o_bf16).
+ */
+gma_status gma_forward_bidir(const void *Q_X, const void *K_X, const void *V_X,
+                             gma_dtype dtype, const float *mu, const float *sigma2,
+                             const float *log_pi, float eps, void *O,
+                             int B, int H, int N, int d_r, int d_v, int K,
+                             const gma_options *options, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * Causal GMA forward ([GMA, causal variant, Eq. (8b)]): as above with the
+ * prefix memories Vt^(i) = sum_{j<=i} gamma^K_j V_j, Z^(i) = sum_{j<=i}
+ * gamma^K_j (j <= i inclusive):
+ *   O_i = Gamma^Q_i Vt^(i) / (Gamma^Q_i Z^(i) + eps).
+ */
+gma_status gma_forward_causal(const void *Q_X, const void *K_X, const void *V_X,
+                              gma_dtype dtype, const float *mu, const float *sigma2,
+                              const float *log_pi, float eps, void *O,
+                              int B, int H, int N, int d_r, int d_v, int K,
+                              const gma_options *options, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream` and returns the device-side status recorded in the
+ * workspace by the last call that used it (GMA_OK, GMA_ERR_NONFINITE_PARAM,
+ * GMA_ERR_TIMEOUT), or GMA_ERR_CUDA if the synchronisation itself failed.
+ */
+gma_status gma_last_device_status(const void *workspace, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *gma_status_string(gma_status status);
+
+/*
+ * Which kernel family a call with these arguments would run
+ * (GMA_PATH_SIMT or GMA_PATH_TC), or -1 if the call would be rejected.
+ */
+int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causal,
+                      const gma_options *options);
+
+/*
+ * Number of stages (kernel launches, plus the status reset of the first) of
+ * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
+ * `variant` (-1 responsibilities, 0 bidirectional, 1 causal), and the name of
+ * stage j (NULL if out of range).  Used with gma_options.stage_events.
+ */
+int gma_stage_count(int path, int variant);
+const char *gma_stage_name(int path, int variant, int j);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMA_H_ */
