@@ -77,6 +77,7 @@ def _load(mutant: int = 0):
             lib.gma_oracle_bidir_rows.argtypes = common + [_L, ctypes.c_int, _D]
             lib.gma_oracle_causal_rows.argtypes = common + [_L, ctypes.c_int, _D]
             lib.gma_oracle_causal_rows.restype = ctypes.c_int
+            lib.gma_oracle_bidir_rows.restype = None
             lib.gma_oracle_affinity_forward.argtypes = common + [ctypes.c_int, _D]
             lib.gma_oracle_affinity.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, _D, _D,
                                                 _D, ctypes.c_int, _D]
