@@ -23,7 +23,8 @@ STATUS_NAMES = {
 # Every symbol declared in include/gma.h (checked by the CPU test-suite).
 EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_forward_causal", "gma_last_device_status", "gma_status_string",
-            "gma_selected_path", "gma_stage_count", "gma_stage_name")
+            "gma_selected_path", "gma_stage_count", "gma_stage_name",
+            "gma_forward_bidir_noalloc")
 
 
 class Options(ctypes.Structure):
@@ -65,6 +66,8 @@ def load(path: str | None = None):
         lib.gma_forward_bidir.restype = i
         lib.gma_forward_causal.argtypes = fwd
         lib.gma_forward_causal.restype = i
+        lib.gma_forward_bidir_noalloc.argtypes = fwd[:16] + [vp]
+        lib.gma_forward_bidir_noalloc.restype = i
         lib.gma_last_device_status.argtypes = [vp, vp]
         lib.gma_last_device_status.restype = i
         lib.gma_status_string.argtypes = [i]

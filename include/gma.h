@@ -149,6 +149,40 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
                       const gma_options *options);
 
 /*
+ * Allocation-free variant of gma_forward_bidir.  The paper has no
+ * counterpart: this is a deployment convenience.
+ *
+ * Some callers cannot allocate device memory at all: code that runs inside
+ * another framework whose device memory is fully owned by that framework's
+ * allocator, real-time or embedded code that must not call cudaMalloc after
+ * start-up (it can fail at any time and it synchronises the whole device),
+ * and plug-ins that receive only input and output buffers.  This entry point
+ * takes no workspace: its scratch is a file-scope device array of
+ * GMA_NOALLOC_SCRATCH_BYTES inside libgma.so, which every GPU that loads the
+ * library holds until the process exits.  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.  The caller still passes the inputs and O.
+ *
+ * - Arguments and results are those of gma_forward_bidir.
+ * - Sizes whose workspace (gma_workspace_size(..., causal = 0, options))
+ *   exceeds GMA_NOALLOC_SCRATCH_BYTES return GMA_ERR_WORKSPACE_TOO_SMALL
+ *   without touching the device.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture on the device.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents.  Calls whose work overlaps on the GPU (different streams, or
+ *   different host threads without ordering) race on it: order them, e.g. on
+ *   one stream.  The device status word lives at its start, as for
+ *   gma_forward_bidir; read it with options->sync_status.
+ */
+#define GMA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+gma_status gma_forward_bidir_noalloc(const void *Q_X, const void *K_X, const void *V_X,
+                                     gma_dtype dtype, const float *mu, const float *sigma2,
+                                     const float *log_pi, float eps, void *O,
+                                     int B, int H, int N, int d_r, int d_v, int K,
+                                     const gma_options *options, void *stream);
+
+/*
  * Number of stages (kernel launches, plus the status reset of the first) of
  * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
  * `variant` (-1 responsibilities, 0 bidirectional, 1 causal), and the name of
