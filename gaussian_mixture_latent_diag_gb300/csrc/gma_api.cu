@@ -24,6 +24,8 @@ bool shape_ok(int B, int H, int N, int d_r, int d_v, int K, bool need_dv) {
     return true;
 }
 
+bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
     return pa < pb + nb && pb < pa + na;
@@ -73,6 +75,7 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
     if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(Q_X) || !aligned16(K_X) || !aligned16(V_X) || !aligned16(O)) return GMA_ERR_INVALID_ARG;
     if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (options && (options->chunk < 0 || options->splits < 0)) return GMA_ERR_INVALID_ARG;
 

@@ -1,10 +1,655 @@
-// gma_tc.cu -- tcgen05 tensor-core kernels (placeholder: not eligible yet).
+// gma_tc.cu -- tcgen05 tensor-core kernels for the GMA forward pass (bf16
+// inputs, d_r = 64, K <= 64, d_v in {64, 128}).
+//
+// Responsibilities ([GMA, Eqs. (2)-(3)]) are computed as a GEMM on the
+// expanded quadratic,
+//   s_ik * log2(e) = sum_j x_ij^2 a_kj + x_ij b_kj + c_k,
+//   a = -log2(e) / (2 sigma2),  b = log2(e) mu / sigma2,
+//   c = log2(e) (log pi_k - 1/2 sum_j (mu^2 / sigma2 + log sigma2)),
+// with every operand split into a bf16 high part and a bf16 low part so that
+// the five products x2hi*ahi + x2hi*alo + x2lo*ahi + x*bhi + x*blo carry
+// ~16 significant bits (x is bf16, so x^2 is exactly x2hi + x2lo).  The
+// softmax over k runs in fp32 on the TMEM accumulator rows.  Gamma is split
+// into bf16 hi + lo again for the value contractions:
+//   write (Eqs. (5)-(6)):  [Vt | Z] += [Ghi ; Glo]^T [V | 1]     (per key tile)
+//   read  (Eq. (7)):       [num | den] = Ghi [Vhi|Zhi] + Glo [Vhi|Zhi] + Ghi [Vlo|Zlo]
+// and O = num / (den + eps * r) with r the un-normalised query row sum.
+//
+// Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+// Probabilistic Latent Routing" (arXiv 2606.18283), cited [GMA, ...].
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "gma_internal.h"
+#include "tc_ptx.cuh"
 
 namespace gma {
-bool tc_supported(const Problem &, int) { return false; }
-size_t tc_workspace(const Problem &, int, int) { return 0; }
-const char *const kTcStages[3][8] = {{nullptr}, {nullptr}, {nullptr}};
-cudaError_t tc_bidir(const Problem &, int, void *, cudaStream_t, StageClock &) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace ptx;
+
+constexpr int kTile = 128;         // tokens per tile (UMMA M)
+constexpr int kDR = 64;            // routing dimension handled here
+constexpr int kKP = 64;            // padded number of components
+constexpr int kTileBytes = kTile * 128;                  // one [128 x 64] bf16 SW128 tile
+constexpr int kCoefMatBytes = kKP * kDR * 2;             // one coefficient matrix [KP x d_r] bf16
+constexpr int kCoefBytes = 4 * kCoefMatBytes + kKP * 4;  // a_hi | a_lo | b_hi | b_lo | c
+constexpr size_t kCoefStride = (kCoefBytes + 1023) & ~1023;
+constexpr int kGS = 2 * (kKP / 64) * 1024;               // Gamma buffer: bytes per 8-token group
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ bool failed(const unsigned *status) {
+    return *reinterpret_cast<const volatile unsigned *>(status) != 0u;
+}
+__device__ __forceinline__ void set_status(unsigned *status, unsigned code) { atomicCAS(status, 0u, code); }
+
+// Byte offset of element (row, col) of a K-major SW128 tile whose rows are
+// 128 bytes (64 bf16) and whose 8-row groups are `group_stride` bytes apart.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int group_stride) {
+    return (uint32_t)((row >> 3) * group_stride + (row & 7) * 128 + ((((col >> 3) ^ (row & 7)) & 7) << 4) +
+                      (col & 7) * 2);
+}
+
+// ------------------------------------------------------------------ coefficient prep
+// One block per head.  Writes the four bf16 coefficient matrices in the
+// K-major SW128 byte image the score MMA reads (rows = components, 128 B of
+// d_r per row), plus c_k (fp32, -inf for padded components).  Validates the
+// parameters.
+__global__ void coef_prep_tc_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
+                                    const float *__restrict__ log_pi, int K, uint8_t *__restrict__ img,
+                                    unsigned *status) {
+    const int h = blockIdx.x;
+    uint8_t *base = img + (size_t)h * kCoefStride;
+    __nv_bfloat16 *ahi = reinterpret_cast<__nv_bfloat16 *>(base);
+    for (int e = threadIdx.x; e < kKP * kDR; e += blockDim.x) {
+        const int k = e / kDR, j = e % kDR;
+        float vah = 0.f, val = 0.f, vbh = 0.f, vbl = 0.f;
+        if (k < K) {
+            const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
+            if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+            const double a = -0.5 * (double)kLog2e / (double)s2;
+            const double b = (double)kLog2e * (double)m / (double)s2;
+            vah = __bfloat162float(__float2bfloat16_rn((float)a));
+            val = (float)(a - (double)vah);
+            vbh = __bfloat162float(__float2bfloat16_rn((float)b));
+            vbl = (float)(b - (double)vbh);
+        }
+        const uint32_t off = sw128_offset(k, j, 1024) / 2;  // in bf16 elements
+        ahi[off] = __float2bfloat16_rn(vah);
+        ahi[kCoefMatBytes / 2 + off] = __float2bfloat16_rn(val);
+        ahi[2 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(vbh);
+        ahi[3 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(vbl);
+    }
+    float *cvec = reinterpret_cast<float *>(base + 4 * kCoefMatBytes);
+    for (int k = threadIdx.x; k < kKP; k += blockDim.x) {
+        if (k >= K) {
+            cvec[k] = -INFINITY;
+            continue;
+        }
+        double acc = 0.0;
+        for (int j = 0; j < kDR; ++j) {
+            const double s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
+            acc += m * m / s2 + log(s2);
+        }
+        const float lp = log_pi[(size_t)h * K + k];
+        if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+        cvec[k] = (float)((double)kLog2e * ((double)lp - 0.5 * acc));
+    }
+}
+
+// ------------------------------------------------------------------ shared pieces
+
+// x^2 split: for every bf16 x of a tile, x2hi = rn(x*x), x2lo = x*x - x2hi
+// (exact, since x*x has at most 16 significant bits).  Position-preserving on
+// the swizzled tile, so the outputs share the tile's layout.
+__device__ __forceinline__ void prep_x2(const uint8_t *x, uint8_t *x2h, uint8_t *x2l, int bytes, int tid,
+                                        int nthreads) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x);
+    uint4 *dh = reinterpret_cast<uint4 *>(x2h);
+    uint4 *dl = reinterpret_cast<uint4 *>(x2l);
+    for (int i = tid; i < bytes / 16; i += nthreads) {
+        const uint4 v = src[i];
+        uint4 h, l;
+        h.x = bf2_fma(v.x, v.x, 0x80008000u); l.x = bf2_fma(v.x, v.x, h.x ^ 0x80008000u);
+        h.y = bf2_fma(v.y, v.y, 0x80008000u); l.y = bf2_fma(v.y, v.y, h.y ^ 0x80008000u);
+        h.z = bf2_fma(v.z, v.z, 0x80008000u); l.z = bf2_fma(v.z, v.z, h.z ^ 0x80008000u);
+        h.w = bf2_fma(v.w, v.w, 0x80008000u); l.w = bf2_fma(v.w, v.w, h.w ^ 0x80008000u);
+        dh[i] = h;
+        dl[i] = l;
+    }
+}
+
+// The 20 score MMAs of one 128-token tile: D[128 x KP] = x2hi*ahi + x2hi*alo +
+// x2lo*ahi + x*bhi + x*blo, each over d_r = 64 in four K-steps of 16.
+__device__ __forceinline__ void issue_scores(uint32_t d_tmem, const uint8_t *x, const uint8_t *x2h,
+                                             const uint8_t *x2l, const uint8_t *coef) {
+    constexpr uint32_t idesc = idesc_bf16(kTile, kKP, false, false);
+    const uint32_t sx = smem_u32(x), sh = smem_u32(x2h), sl = smem_u32(x2l), sc = smem_u32(coef);
+#pragma unroll
+    for (int kk = 0; kk < kDR / 16; ++kk) {
+        const uint32_t o = kk * 32;
+        const uint64_t ax = sdesc_sw128(sx + o, 16, 1024), ah = sdesc_sw128(sh + o, 16, 1024),
+                       al = sdesc_sw128(sl + o, 16, 1024);
+        const uint64_t bah = sdesc_sw128(sc + o, 16, 1024), bal = sdesc_sw128(sc + kCoefMatBytes + o, 16, 1024),
+                       bbh = sdesc_sw128(sc + 2 * kCoefMatBytes + o, 16, 1024),
+                       bbl = sdesc_sw128(sc + 3 * kCoefMatBytes + o, 16, 1024);
+        umma_bf16(d_tmem, ah, bah, idesc, kk > 0 ? 1u : 0u);
+        umma_bf16(d_tmem, ah, bal, idesc, 1u);
+        umma_bf16(d_tmem, al, bah, idesc, 1u);
+        umma_bf16(d_tmem, ax, bbh, idesc, 1u);
+        umma_bf16(d_tmem, ax, bbl, idesc, 1u);
+    }
+}
+
+// Loads this thread's score row (KP columns) and turns it into exponentials
+// e_k = 2^(s_k + c_k - max) (un-normalised responsibilities, max e = 1).
+// Returns the row sum r.
+__device__ __forceinline__ float score_row_exp(uint32_t taddr, const float *cvec, float (&e)[kKP]) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(taddr, r0);
+    tmem_ld32(taddr + 32, r1);
+    tmem_wait_ld();
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        e[k] = __uint_as_float(r0[k]) + cvec[k];
+        e[k + 32] = __uint_as_float(r1[k]) + cvec[k + 32];
+        m = fmaxf(m, fmaxf(e[k], e[k + 32]));
+    }
+    float r = 0.f;
+#pragma unroll
+    for (int k = 0; k < kKP; ++k) {
+        e[k] = ex2(e[k] - m);
+        r += e[k];
+    }
+    return r;
+}
+
+// Writes one responsibility row (scaled by `scale`) as bf16 hi and lo parts
+// into the Gamma buffer: 8-token groups of kGS bytes, hi rows at +0, lo rows
+// at +1024 within a group, 16-byte chunks swizzled by (row % 8).
+__device__ __forceinline__ void store_gamma_row(uint8_t *gbuf, int t, const float (&e)[kKP], float scale) {
+    uint8_t *hi = gbuf + (t >> 3) * kGS + (t & 7) * 128;
+    uint8_t *lo = hi + 1024;
+#pragma unroll
+    for (int c = 0; c < kKP / 8; ++c) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float g0 = e[c * 8 + 2 * q] * scale, g1 = e[c * 8 + 2 * q + 1] * scale;
+            wh[q] = pack_bf2(g0, g1);
+            wl[q] = pack_bf2(g0 - bf_lo(wh[q]), g1 - bf_hi(wh[q]));
+        }
+        const uint32_t sw = (uint32_t)((c ^ (t & 7)) << 4);
+        *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+}
+
+// Aborts the CTA's work on a timed-out wait: records the status once.
+__device__ __forceinline__ void note_timeout(unsigned *status, int *abort_flag) {
+    set_status(status, GMA_ERR_TIMEOUT);
+    *reinterpret_cast<volatile int *>(abort_flag) = 1;
+}
+
+// ------------------------------------------------------------------ write kernel
+// Latent aggregation over one split of the keys of one head ([GMA, Eqs. (5)-(6)]):
+// part[k][c] = sum_{j in split} gamma^K_jk V_jc, part[k][d_v] = sum gamma^K_jk.
+// Grid (nsplit, B*H); 128 threads; thread t owns TMEM lane / tile row t.
+template <int D_V>
+struct WriteSmem {
+    static constexpr int kX = 0;                                  // K_X tile (16 KB)
+    static constexpr int kX2 = kX + kTileBytes;                   // x2hi | x2lo (32 KB), then Gamma
+    static constexpr int kV = kX2 + 2 * kTileBytes;               // V tile(s): D_V/64 boxes of 16 KB
+    static constexpr int kCoef = kV + (D_V / 64) * kTileBytes;    // 32 KB + c
+    static constexpr int kOnes = kCoef + ((kCoefBytes + 1023) & ~1023);  // 2 KB of bf16 1.0
+    static constexpr int kBars = kOnes + 2048;
+    static constexpr int kBytes = kBars + 64;
+    static constexpr int kAlloc = kBytes + 1024;                  // slack for 1 KB alignment
+};
+
+template <int D_V>
+__global__ void __launch_bounds__(128, 1) tc_write_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                           const __grid_constant__ CUtensorMap tmV,
+                                                           const uint8_t *__restrict__ coef_img, int H, int N,
+                                                           int tiles_per_split, int nsplit,
+                                                           float *__restrict__ part, unsigned *status) {
+    using L = WriteSmem<D_V>;
+    constexpr int kTmemCols = 256;
+    constexpr int kAccV = kKP, kAccZ = kKP + D_V;  // TMEM columns
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *xk = smem + L::kX, *x2 = smem + L::kX2, *vt = smem + L::kV, *coef = smem + L::kCoef,
+            *ones = smem + L::kOnes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);  // [0] TMA, [1] MMA
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    int *abort_flag = reinterpret_cast<int *>(bars + 3);
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int split = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int ntiles = (N + kTile - 1) / kTile;
+    const int tile0 = split * tiles_per_split, tile1 = min(ntiles, tile0 + tiles_per_split);
+    if (failed(status)) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(coef_img + (size_t)h * kCoefStride);
+        uint4 *dst = reinterpret_cast<uint4 *>(coef);
+        for (int i = tid; i < kCoefBytes / 16; i += blockDim.x) dst[i] = src[i];
+        uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        for (int i = tid; i < 2048 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(ones)[i] = one4;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    constexpr uint32_t kTxBytes = kTileBytes * (1 + D_V / 64);
+
+    if (tid == 0 && tile0 < tile1) {
+        mbar_arrive_expect_tx(&bars[0], kTxBytes);
+        tma_load_3d(xk, &tmK, 0, tile0 * kTile, bh, &bars[0]);
+#pragma unroll
+        for (int vb = 0; vb < D_V / 64; ++vb) tma_load_3d(vt + vb * kTileBytes, &tmV, vb * 64, tile0 * kTile, bh, &bars[0]);
+    }
+    uint32_t ph_tma = 0, ph_mma = 0;
+    constexpr uint32_t idesc_v = idesc_bf16(kTile, 64, true, true);
+    constexpr uint32_t idesc_z = idesc_bf16(kTile, 16, true, false);
+
+    for (int tile = tile0; tile < tile1; ++tile) {
+        if (!mbar_wait(&bars[0], ph_tma)) note_timeout(status, abort_flag);
+        ph_tma ^= 1;
+        prep_x2(xk, x2, x2 + kTileBytes, kTileBytes, tid, blockDim.x);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_scores(tmem, xk, x2, x2 + kTileBytes, coef);
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        tc_fence_after();
+        {
+            float e[kKP];
+            const float r = score_row_exp(tmem + lane_base, cvec, e);
+            const int tok = tile * kTile + tid;
+            const float scale = tok < N ? 1.0f / r : 0.0f;  // rows past N contribute nothing
+            store_gamma_row(x2, tid, e, scale);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t sg = smem_u32(x2), sv = smem_u32(vt), so = smem_u32(ones);
+            const uint64_t bz = sdesc_sw128(so, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint32_t acc = (tile > tile0 || kk > 0) ? 1u : 0u;
+                const uint64_t a = sdesc_sw128(sg + kk * 2 * kGS, 1024, kGS);
+#pragma unroll
+                for (int vb = 0; vb < D_V / 64; ++vb) {
+                    const uint64_t b = sdesc_sw128(sv + vb * kTileBytes + kk * 2048, 16, 1024);
+                    umma_bf16(tmem + kAccV + vb * 64, a, b, idesc_v, acc);
+                }
+                umma_bf16(tmem + kAccZ, a, bz, idesc_z, acc);
+            }
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0 && tile + 1 < tile1) {
+            mbar_arrive_expect_tx(&bars[0], kTxBytes);
+            tma_load_3d(xk, &tmK, 0, (tile + 1) * kTile, bh, &bars[0]);
+#pragma unroll
+            for (int vb = 0; vb < D_V / 64; ++vb)
+                tma_load_3d(vt + vb * kTileBytes, &tmV, vb * 64, (tile + 1) * kTile, bh, &bars[0]);
+        }
+    }
+
+    // Partial memory: rows 0..63 of the accumulator hold the hi-weighted sums,
+    // rows 64..127 the lo-weighted ones; add them and write [KP][D_V + 1].
+    const bool ok = !*reinterpret_cast<volatile int *>(abort_flag);
+    if (ok && tile0 < tile1) {
+        tc_fence_after();
+        float *red = reinterpret_cast<float *>(smem);  // [128][D_V + 1] fp32, over the tiles region
+        constexpr int W = D_V + 1;
+#pragma unroll
+        for (int cb = 0; cb < D_V / 32; ++cb) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kAccV + cb * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) red[tid * W + cb * 32 + q] = __uint_as_float(v[q]);
+        }
+        {
+            uint32_t z[16];
+            tmem_ld16(tmem + lane_base + kAccZ, z);
+            tmem_wait_ld();
+            red[tid * W + D_V] = __uint_as_float(z[0]);
+        }
+        __syncthreads();
+        float *out = part + ((size_t)bh * nsplit + split) * kKP * W;
+        for (int e = tid; e < kKP * W; e += blockDim.x) out[e] = red[e] + red[kKP * W + e];
+    } else if (ok) {  // a split without tiles contributes zeros
+        float *out = part + ((size_t)bh * nsplit + split) * kKP * (D_V + 1);
+        for (int e = tid; e < kKP * (D_V + 1); e += blockDim.x) out[e] = 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ read kernel
+// Normalised broadcasting ([GMA, Eq. (7)]) for a range of query tiles of one
+// head.  Prologue: fixed-order sum of the split partials of the head, stored
+// as the bf16 hi / lo B operand [NB = D_V + 16 rows x KP] (row n < D_V: Vt[:, n];
+// row D_V: Z; other rows 0).
+template <int D_V>
+struct ReadSmem {
+    static constexpr int NB = D_V + 16;
+    static constexpr int kX = 0;                                   // Q tile
+    static constexpr int kX2 = kX + kTileBytes;                    // x2hi | x2lo, then Gamma
+    static constexpr int kCoef = kX2 + 2 * kTileBytes;
+    static constexpr int kB = kCoef + ((kCoefBytes + 1023) & ~1023);  // hi [NB x 128 B] | lo
+    static constexpr int kBars = kB + 2 * NB * 128;
+    static constexpr int kBytes = kBars + 64;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+template <int D_V>
+__global__ void __launch_bounds__(128, 1) tc_read_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                          const uint8_t *__restrict__ coef_img,
+                                                          const float *__restrict__ part, int nsplit, int H,
+                                                          int N, int tiles_per_cta, float eps,
+                                                          void *__restrict__ O, int o_bf16, unsigned *status) {
+    using L = ReadSmem<D_V>;
+    constexpr int NB = L::NB;
+    constexpr int kTmemCols = 256;
+    constexpr int kAccO = kKP;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *xq = smem + L::kX, *x2 = smem + L::kX2, *coef = smem + L::kCoef, *bop = smem + L::kB;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    int *abort_flag = reinterpret_cast<int *>(bars + 3);
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.y, h = bh % H;
+    const int ntiles = (N + kTile - 1) / kTile;
+    const int tile0 = blockIdx.x * tiles_per_cta, tile1 = min(ntiles, tile0 + tiles_per_cta);
+    if (failed(status) || tile0 >= tile1) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        mbar_arrive_expect_tx(&bars[0], kTileBytes);
+        tma_load_3d(xq, &tmQ, 0, tile0 * kTile, bh, &bars[0]);
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(coef_img + (size_t)h * kCoefStride);
+        uint4 *dst = reinterpret_cast<uint4 *>(coef);
+        for (int i = tid; i < kCoefBytes / 16; i += blockDim.x) dst[i] = src[i];
+    }
+    {
+        constexpr int W = D_V + 1;
+        const float *p = part + (size_t)bh * nsplit * kKP * W;
+        __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(bop);
+        __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(bop + NB * 128);
+        for (int e = tid; e < NB * kKP; e += blockDim.x) {
+            const int n = e / kKP, k = e % kKP;
+            float v = 0.f;
+            if (n <= D_V)
+                for (int s = 0; s < nsplit; ++s) v += p[((size_t)s * kKP + k) * W + n];
+            const __nv_bfloat16 vh = __float2bfloat16_rn(v);
+            const uint32_t off = sw128_offset(n, k, 1024) / 2;
+            bhi[off] = vh;
+            blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    constexpr uint32_t idesc_o = idesc_bf16(kTile, NB, false, false);
+    uint32_t ph_tma = 0, ph_mma = 0;
+
+    for (int tile = tile0; tile < tile1; ++tile) {
+        if (!mbar_wait(&bars[0], ph_tma)) note_timeout(status, abort_flag);
+        ph_tma ^= 1;
+        prep_x2(xq, x2, x2 + kTileBytes, kTileBytes, tid, blockDim.x);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_scores(tmem, xq, x2, x2 + kTileBytes, coef);
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        tc_fence_after();
+        if (tid == 0 && tile + 1 < tile1) {  // Q tile and x^2 are free: fetch the next tile
+            mbar_arrive_expect_tx(&bars[0], kTileBytes);
+            tma_load_3d(xq, &tmQ, 0, (tile + 1) * kTile, bh, &bars[0]);
+        }
+        float r;
+        {
+            float e[kKP];
+            r = score_row_exp(tmem + lane_base, cvec, e);
+            store_gamma_row(x2, tid, e, 1.0f);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t sg = smem_u32(x2), sb = smem_u32(bop);
+#pragma unroll
+            for (int kk = 0; kk < kKP / 16; ++kk) {
+                const uint64_t ahi = sdesc_sw128(sg + kk * 32, 16, kGS), alo = sdesc_sw128(sg + 1024 + kk * 32, 16, kGS);
+                const uint64_t bhi = sdesc_sw128(sb + kk * 32, 16, 1024), blo = sdesc_sw128(sb + NB * 128 + kk * 32, 16, 1024);
+                umma_bf16(tmem + kAccO, ahi, bhi, idesc_o, kk > 0 ? 1u : 0u);
+                umma_bf16(tmem + kAccO, alo, bhi, idesc_o, 1u);
+                umma_bf16(tmem + kAccO, ahi, blo, idesc_o, 1u);
+            }
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        tc_fence_after();
+        {
+            uint32_t dz[16];
+            tmem_ld16(tmem + lane_base + kAccO + D_V, dz);
+            tmem_wait_ld();
+            const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * r);
+            const int tok = tile * kTile + tid;
+            const size_t row = (size_t)bh * N + tok;
+#pragma unroll
+            for (int cb = 0; cb < D_V / 32; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kAccO + cb * 32, v);
+                tmem_wait_ld();
+                if (tok < N) {
+                    if (o_bf16) {
+                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + row * D_V + cb * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            o[q] = make_uint4(pack_bf2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                                              pack_bf2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                                              pack_bf2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                                              pack_bf2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+                    } else {
+                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(O) + row * D_V + cb * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            o[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                               __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [BH][N][d] bf16 tensor, boxes of 64 columns x 128 rows x 1 head, 128-byte
+// swizzle; rows past N read as zero.
+bool make_map(CUtensorMap *map, const void *base, int BH, int N, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct TcLayout {
+    size_t coef = 0, part = 0, total = 0;
+    int nsplit = 0, tiles_per_split = 0;
+};
+
+constexpr int kTargetCtas = 2 * 152;
+
+TcLayout tc_layout(const Problem &p, int splits) {
+    TcLayout L;
+    const int ntiles = (p.N + kTile - 1) / kTile;
+    int ns = splits > 0 ? splits : (kTargetCtas + p.BH() - 1) / p.BH();
+    ns = ns < 1 ? 1 : (ns > ntiles ? ntiles : ns);
+    L.tiles_per_split = (ntiles + ns - 1) / ns;
+    L.nsplit = (ntiles + L.tiles_per_split - 1) / L.tiles_per_split;
+    size_t off = kStatusBytes;
+    L.coef = off;
+    off = align256(off + kCoefStride * p.H);
+    L.part = off;
+    off = align256(off + sizeof(float) * (size_t)p.BH() * L.nsplit * kKP * (p.d_v + 1));
+    L.total = off;
+    return L;
+}
+
+template <typename KernelT>
+cudaError_t set_smem(KernelT kern, int bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+#define GMA_TRY(x)                            \
+    do {                                      \
+        cudaError_t err_ = (x);               \
+        if (err_ != cudaSuccess) return err_; \
+    } while (0)
+
+template <int D_V>
+cudaError_t run_bidir(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
+    unsigned *status = reinterpret_cast<unsigned *>(ws);
+    uint8_t *coef = ws + L.coef;
+    float *part = reinterpret_cast<float *>(ws + L.part);
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
+        !make_map(&tv, p.V, p.BH(), p.N, D_V))
+        return cudaErrorInvalidValue;
+    clk.mark();
+    GMA_TRY(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
+    coef_prep_tc_kernel<<<p.H, 256, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    GMA_TRY(set_smem(tc_write_kernel<D_V>, WriteSmem<D_V>::kAlloc));
+    tc_write_kernel<D_V><<<dim3(L.nsplit, p.BH()), 128, WriteSmem<D_V>::kAlloc, s>>>(
+        tk, tv, coef, p.H, p.N, L.tiles_per_split, L.nsplit, part, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    const int ntiles = (p.N + kTile - 1) / kTile;
+    int per = (int)(((long long)ntiles * p.BH() + kTargetCtas - 1) / kTargetCtas);
+    per = per < 1 ? 1 : per;
+    const int nct = (ntiles + per - 1) / per;
+    GMA_TRY(set_smem(tc_read_kernel<D_V>, ReadSmem<D_V>::kAlloc));
+    tc_read_kernel<D_V><<<dim3(nct, p.BH()), 128, ReadSmem<D_V>::kAlloc, s>>>(
+        tq, coef, part, L.nsplit, p.H, p.N, per, p.eps, p.O, p.o_bf16 ? 1 : 0, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    return cudaSuccess;
+}
+
+}  // namespace
+
+const char *const kTcStages[3][8] = {
+    {nullptr},
+    {"prep", "tc_write", "tc_read", nullptr},
+    {nullptr},
+};
+
+bool tc_supported(const Problem &p, int causal) {
+    return causal == 0 && p.dtype == GMA_BF16 && p.d_r == kDR && p.K <= kKP && (p.d_v == 64 || p.d_v == 128);
+}
+
+size_t tc_workspace(const Problem &p, int causal, int splits) {
+    (void)causal;
+    return tc_layout(p, splits).total;
+}
+
+cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
+    TcLayout L = tc_layout(p, splits);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    if (p.d_v == 64) return run_bidir<64>(p, L, w, s, clk);
+    return run_bidir<128>(p, L, w, s, clk);
+}
+
 cudaError_t tc_causal(const Problem &, int, void *, cudaStream_t, StageClock &) { return cudaErrorNotSupported; }
+
 }  // namespace gma
