@@ -55,7 +55,7 @@ __global__ void prep_simt_kernel(const float *__restrict__ mu, const float *__re
     }
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
         double acc = 0.0;
-        for (int j = 0; j < d_r; ++j) acc += log((double)sigma2[base + (size_t)k * d_r + j]);
+        for (int j = 0; j < d_r; ++j) acc += (double)logf(sigma2[base + (size_t)k * d_r + j]);
         float lp = log_pi[(size_t)h * K + k];
         if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
         cprime[(size_t)h * K + k] = (float)((double)lp - 0.5 * acc);

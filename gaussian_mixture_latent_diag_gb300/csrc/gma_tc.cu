@@ -67,37 +67,41 @@ __global__ void coef_prep_tc_kernel(const float *__restrict__ mu, const float *_
     __nv_bfloat16 *ahi = reinterpret_cast<__nv_bfloat16 *>(base);
     for (int e = threadIdx.x; e < kKP * kDR; e += blockDim.x) {
         const int k = e / kDR, j = e % kDR;
-        float vah = 0.f, val = 0.f, vbh = 0.f, vbl = 0.f;
+        float a = 0.f, b = 0.f;
         if (k < K) {
             const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
             if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-            const double a = -0.5 * (double)kLog2e / (double)s2;
-            const double b = (double)kLog2e * (double)m / (double)s2;
-            vah = __bfloat162float(__float2bfloat16_rn((float)a));
-            val = (float)(a - (double)vah);
-            vbh = __bfloat162float(__float2bfloat16_rn((float)b));
-            vbl = (float)(b - (double)vbh);
+            a = -0.5f * kLog2e / s2;
+            b = kLog2e * m / s2;
         }
+        const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
         const uint32_t off = sw128_offset(k, j, 1024) / 2;  // in bf16 elements
-        ahi[off] = __float2bfloat16_rn(vah);
-        ahi[kCoefMatBytes / 2 + off] = __float2bfloat16_rn(val);
-        ahi[2 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(vbh);
-        ahi[3 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(vbl);
+        ahi[off] = ah;
+        ahi[kCoefMatBytes / 2 + off] = __float2bfloat16_rn(a - __bfloat162float(ah));
+        ahi[2 * kCoefMatBytes / 2 + off] = bh;
+        ahi[3 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(b - __bfloat162float(bh));
     }
+    // c_k: one warp per component, lanes over j, fp32 terms summed in fp64.
     float *cvec = reinterpret_cast<float *>(base + 4 * kCoefMatBytes);
-    for (int k = threadIdx.x; k < kKP; k += blockDim.x) {
-        if (k >= K) {
-            cvec[k] = -INFINITY;
-            continue;
-        }
+    const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int k = threadIdx.x >> 5; k < kKP; k += nwarps) {
         double acc = 0.0;
-        for (int j = 0; j < kDR; ++j) {
-            const double s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
-            acc += m * m / s2 + log(s2);
+        if (k < K)
+            for (int j = lane; j < kDR; j += 32) {
+                const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
+                acc += (double)(m * m / s2) + (double)logf(s2);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            if (k < K) {
+                const float lp = log_pi[(size_t)h * K + k];
+                if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+                cvec[k] = (float)((double)kLog2e * ((double)lp - 0.5 * acc));
+            } else {
+                cvec[k] = -INFINITY;
+            }
         }
-        const float lp = log_pi[(size_t)h * K + k];
-        if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-        cvec[k] = (float)((double)kLog2e * ((double)lp - 0.5 * acc));
     }
 }
 
@@ -530,6 +534,318 @@ __global__ void __launch_bounds__(128, 1) tc_read_kernel(const __grid_constant__
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ causal
+// Exclusive prefix over the segment aggregates of each head, in segment
+// order, in place: part[s] <- sum_{s' < s} part[s'] ([GMA, causal variant:
+// the prefix memories are cumulative sums along the sequence]).
+__global__ void scan_segments_kernel(float *__restrict__ part, int nseg, int E, const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float *p = part + (size_t)bh * nseg * E + e;
+    float run = 0.f;
+    for (int s = 0; s < nseg; ++s) {
+        const float cur = p[(size_t)s * E];
+        p[(size_t)s * E] = run;
+        run += cur;
+    }
+}
+
+// Writes the state B operand [NB x KP] (bf16 hi at `bop`, lo at bop + NB*128)
+// from the fp32 state S[k][n] (row n < D_V: S[:, n]; row D_V: Z; rows above: 0).
+template <int D_V>
+__device__ __forceinline__ void build_state_operand(const float *S, uint8_t *bop, int tid, int nthreads) {
+    constexpr int NB = D_V + 16, W = D_V + 1;
+    __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(bop);
+    __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(bop + NB * 128);
+    for (int e = tid; e < NB * kKP; e += nthreads) {
+        const int n = e / kKP, k = e % kKP;
+        const float v = n <= D_V ? S[k * W + n] : 0.f;
+        const __nv_bfloat16 vh = __float2bfloat16_rn(v);
+        const uint32_t off = sw128_offset(n, k, 1024) / 2;
+        bhi[off] = vh;
+        blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
+    }
+}
+
+// Causal GMA over one segment of one head ([GMA, Eq. (8b)]), in chunks of
+// C = 128 tokens.  With (S, Z) the prefix memory before the chunk and
+// P = mask_{j <= i}(Gamma^Q_c Gamma^K_c^T) the intra-chunk affinity:
+//   O_i = (sum_j P_ij V_j + gQ_i S) / (sum_j P_ij + gQ_i Z + eps r_i),
+// (gQ un-normalised, r_i its row sum), then S += Gamma^K_c^T V_c, Z += Gamma^K_c^T 1.
+// The segment's starting prefix comes from scan_segments_kernel.
+struct CausalSmem {
+    static constexpr int D_V = 64, NB = D_V + 16, W = D_V + 1;
+    static constexpr int kA = 0;                      // xq | xk | x2q (x2hi|x2lo) -> gq -> P (64 KB)
+    static constexpr int kXQ = kA, kXK = kA + kTileBytes, kX2Q = kA + 2 * kTileBytes;
+    static constexpr int kB = kA + 4 * kTileBytes;    // x2k (x2hi|x2lo) -> gk (32 KB)
+    static constexpr int kV = kB + 2 * kTileBytes;    // V tile (16 KB)
+    static constexpr int kCoef = kV + kTileBytes;
+    static constexpr int kBop = kCoef + ((kCoefBytes + 1023) & ~1023);  // state operand hi | lo
+    static constexpr int kOnes = kBop + 2 * NB * 128;
+    static constexpr int kS = kOnes + 2048;           // fp32 state [KP][W]
+    static constexpr int kBars = kS + ((kKP * W * 4 + 1023) & ~1023);
+    static constexpr int kBytes = kBars + 64;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+constexpr int kGSP = 4096;  // P buffer: bytes per 8-query group (128 keys, hi | lo)
+
+__global__ void __launch_bounds__(128, 1) tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                            const __grid_constant__ CUtensorMap tmK,
+                                                            const __grid_constant__ CUtensorMap tmV,
+                                                            const uint8_t *__restrict__ coef_img,
+                                                            const float *__restrict__ prefix, int H, int N,
+                                                            int tiles_per_seg, int nseg, float eps,
+                                                            void *__restrict__ O, int o_bf16, unsigned *status) {
+    using L = CausalSmem;
+    constexpr int D_V = L::D_V, NB = L::NB, W = L::W;
+    constexpr int kTmemCols = 256;
+    constexpr int kSQ = 0, kSK = kKP, kP = 0, kSc = 0, kO = 128;  // TMEM columns
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *xq = smem + L::kXQ, *xk = smem + L::kXK, *x2q = smem + L::kX2Q, *pbuf = smem + L::kA;
+    uint8_t *x2k = smem + L::kB, *vt = smem + L::kV, *coef = smem + L::kCoef, *bop = smem + L::kBop,
+            *ones = smem + L::kOnes;
+    float *S = reinterpret_cast<float *>(smem + L::kS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    int *abort_flag = reinterpret_cast<int *>(bars + 3);
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int ntiles = (N + kTile - 1) / kTile;
+    const int tile0 = seg * tiles_per_seg, tile1 = min(ntiles, tile0 + tiles_per_seg);
+    if (failed(status) || tile0 >= tile1) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    constexpr uint32_t kTx = 3 * kTileBytes;
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_arrive_expect_tx(&bars[0], kTx);
+        tma_load_3d(xq, &tmQ, 0, tile0 * kTile, bh, &bars[0]);
+        tma_load_3d(xk, &tmK, 0, tile0 * kTile, bh, &bars[0]);
+        tma_load_3d(vt, &tmV, 0, tile0 * kTile, bh, &bars[0]);
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(coef_img + (size_t)h * kCoefStride);
+        uint4 *dst = reinterpret_cast<uint4 *>(coef);
+        for (int i = tid; i < kCoefBytes / 16; i += blockDim.x) dst[i] = src[i];
+        const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        for (int i = tid; i < 2048 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(ones)[i] = one4;
+        const float *pre = prefix + ((size_t)bh * nseg + seg) * kKP * W;
+        for (int e = tid; e < kKP * W; e += blockDim.x) S[e] = pre[e];
+    }
+    __syncthreads();
+    build_state_operand<D_V>(S, bop, tid, blockDim.x);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    constexpr uint32_t idesc_p = idesc_bf16(kTile, kTile, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16(kTile, NB, false, false);
+    constexpr uint32_t idesc_v = idesc_bf16(kTile, 64, false, true);   // A K-major (P), B MN-major (V)
+    constexpr uint32_t idesc_z = idesc_bf16(kTile, 16, false, false);
+    constexpr uint32_t idesc_sv = idesc_bf16(kTile, 64, true, true);   // A MN-major (Gamma^K^T), B MN-major
+    constexpr uint32_t idesc_sz = idesc_bf16(kTile, 16, true, false);
+    uint32_t ph_tma = 0, ph_mma = 0;
+
+    for (int tile = tile0; tile < tile1; ++tile) {
+        const int tok = tile * kTile + tid;
+        if (!mbar_wait(&bars[0], ph_tma)) note_timeout(status, abort_flag);
+        ph_tma ^= 1;
+        prep_x2(xq, x2q, x2q + kTileBytes, kTileBytes, tid, blockDim.x);
+        prep_x2(xk, x2k, x2k + kTileBytes, kTileBytes, tid, blockDim.x);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_scores(tmem + kSQ, xq, x2q, x2q + kTileBytes, coef);
+            issue_scores(tmem + kSK, xk, x2k, x2k + kTileBytes, coef);
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        tc_fence_after();
+        float rq;
+        {
+            float e[kKP];
+            rq = score_row_exp(tmem + lane_base + kSQ, cvec, e);
+            store_gamma_row(x2q, tid, e, 1.0f);
+            const float rk = score_row_exp(tmem + lane_base + kSK, cvec, e);
+            store_gamma_row(x2k, tid, e, tok < N ? 1.0f / rk : 0.0f);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t sq = smem_u32(x2q), sk = smem_u32(x2k), sb = smem_u32(bop);
+#pragma unroll
+            for (int kk = 0; kk < kKP / 16; ++kk) {
+                const uint64_t qh = sdesc_sw128(sq + kk * 32, 16, kGS), ql = sdesc_sw128(sq + 1024 + kk * 32, 16, kGS);
+                const uint64_t kh = sdesc_sw128(sk + kk * 32, 16, kGS), kl = sdesc_sw128(sk + 1024 + kk * 32, 16, kGS);
+                const uint64_t bh_ = sdesc_sw128(sb + kk * 32, 16, 1024), bl_ = sdesc_sw128(sb + NB * 128 + kk * 32, 16, 1024);
+                const uint32_t acc = kk > 0 ? 1u : 0u;
+                umma_bf16(tmem + kP, qh, kh, idesc_p, acc);   // P = gQ gK^T (3 split terms)
+                umma_bf16(tmem + kP, ql, kh, idesc_p, 1u);
+                umma_bf16(tmem + kP, qh, kl, idesc_p, 1u);
+                umma_bf16(tmem + kO, qh, bh_, idesc_o, acc);  // [num | den] = gQ [S | Z]
+                umma_bf16(tmem + kO, ql, bh_, idesc_o, 1u);
+                umma_bf16(tmem + kO, qh, bl_, idesc_o, 1u);
+            }
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        tc_fence_after();
+        // Masked intra-chunk affinity row i = tid: keep keys j <= i, split hi / lo.
+        {
+            uint8_t *hi = pbuf + (tid >> 3) * kGSP + (tid & 7) * 128;
+            uint8_t *lo = hi + 2048;
+#pragma unroll
+            for (int cb = 0; cb < kTile / 32; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kP + cb * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t wh[4], wl[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j0 = cb * 32 + c4 * 8 + 2 * q;
+                        const float p0 = j0 <= tid ? __uint_as_float(v[c4 * 8 + 2 * q]) : 0.f;
+                        const float p1 = j0 + 1 <= tid ? __uint_as_float(v[c4 * 8 + 2 * q + 1]) : 0.f;
+                        wh[q] = pack_bf2(p0, p1);
+                        wl[q] = pack_bf2(p0 - bf_lo(wh[q]), p1 - bf_hi(wh[q]));
+                    }
+                    const int chunk = (cb * 32 + c4 * 8) >> 3;        // 16-byte chunk over 128 keys
+                    const int blk = chunk >> 3, c = chunk & 7;
+                    const uint32_t sw = (uint32_t)(blk * 1024 + ((c ^ (tid & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                    *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                }
+            }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t sp = smem_u32(pbuf), sv = smem_u32(vt), sk = smem_u32(x2k), so = smem_u32(ones);
+            const uint64_t bz = sdesc_sw128(so, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint32_t ao = (kk >> 2) * 1024 + (kk & 3) * 32;
+                const uint64_t ph = sdesc_sw128(sp + ao, 16, kGSP), pl = sdesc_sw128(sp + 2048 + ao, 16, kGSP);
+                const uint64_t bv = sdesc_sw128(sv + kk * 2048, 16, 1024);
+                umma_bf16(tmem + kO, ph, bv, idesc_v, 1u);          // num += P V
+                umma_bf16(tmem + kO, pl, bv, idesc_v, 1u);
+                umma_bf16(tmem + kO + D_V, ph, bz, idesc_z, 1u);    // den += P 1
+                umma_bf16(tmem + kO + D_V, pl, bz, idesc_z, 1u);
+                const uint64_t ag = sdesc_sw128(sk + kk * 2 * kGS, 1024, kGS);  // [gK_hi ; gK_lo]^T
+                const uint32_t acc = kk > 0 ? 1u : 0u;
+                umma_bf16(tmem + kSc, ag, bv, idesc_sv, acc);       // chunk state: gK^T V
+                umma_bf16(tmem + kSc + D_V, ag, bz, idesc_sz, acc); //              gK^T 1
+            }
+            umma_commit(&bars[1]);
+        }
+        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
+        ph_mma ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        if (tid == 0 && tile + 1 < tile1) {  // every tile buffer is free: fetch the next chunk
+            mbar_arrive_expect_tx(&bars[0], kTx);
+            tma_load_3d(xq, &tmQ, 0, (tile + 1) * kTile, bh, &bars[0]);
+            tma_load_3d(xk, &tmK, 0, (tile + 1) * kTile, bh, &bars[0]);
+            tma_load_3d(vt, &tmV, 0, (tile + 1) * kTile, bh, &bars[0]);
+        }
+        // Outputs of the chunk.
+        {
+            uint32_t dz[16];
+            tmem_ld16(tmem + lane_base + kO + D_V, dz);
+            tmem_wait_ld();
+            const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rq);
+            const size_t row = (size_t)bh * N + tok;
+#pragma unroll
+            for (int cb = 0; cb < D_V / 32; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kO + cb * 32, v);
+                tmem_wait_ld();
+                if (tok < N) {
+                    if (o_bf16) {
+                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + row * D_V + cb * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            o[q] = make_uint4(pack_bf2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                                              pack_bf2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                                              pack_bf2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                                              pack_bf2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+                    } else {
+                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(O) + row * D_V + cb * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            o[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                               __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+                    }
+                }
+            }
+        }
+        // Carry: S += (hi rows 0..63) + (lo rows 64..127) of the chunk state.
+        if (tile + 1 < tile1) {
+            // the gq area is free again (its MMAs are done and the next chunk's TMA
+            // writes only xq / xk): [64][W] fp32 = 16.6 KB
+            float *tmp = reinterpret_cast<float *>(x2q);
+            uint32_t v[32];
+            float row[W];
+#pragma unroll
+            for (int cb = 0; cb < D_V / 32; ++cb) {
+                tmem_ld32(tmem + lane_base + kSc + cb * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) row[cb * 32 + q] = __uint_as_float(v[q]);
+            }
+            {
+                uint32_t z[16];
+                tmem_ld16(tmem + lane_base + kSc + D_V, z);
+                tmem_wait_ld();
+                row[D_V] = __uint_as_float(z[0]);
+            }
+            if (tid >= kKP)
+#pragma unroll
+                for (int c = 0; c < W; ++c) tmp[(tid - kKP) * W + c] = row[c];
+            __syncthreads();
+            if (tid < kKP)
+#pragma unroll
+                for (int c = 0; c < W; ++c) S[tid * W + c] += row[c] + tmp[tid * W + c];
+            __syncthreads();
+            build_state_operand<D_V>(S, bop, tid, blockDim.x);
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -568,10 +884,14 @@ struct TcLayout {
 
 constexpr int kTargetCtas = 2 * 152;
 
-TcLayout tc_layout(const Problem &p, int splits) {
+constexpr int kCausalSegTiles = 8;  // default causal segment: 1024 tokens
+
+TcLayout tc_layout(const Problem &p, int causal, int splits) {
     TcLayout L;
     const int ntiles = (p.N + kTile - 1) / kTile;
-    int ns = splits > 0 ? splits : (kTargetCtas + p.BH() - 1) / p.BH();
+    int ns = splits > 0 ? splits
+                        : causal ? (ntiles + kCausalSegTiles - 1) / kCausalSegTiles
+                                 : (kTargetCtas + p.BH() - 1) / p.BH();
     ns = ns < 1 ? 1 : (ns > ntiles ? ntiles : ns);
     L.tiles_per_split = (ntiles + ns - 1) / ns;
     L.nsplit = (ntiles + L.tiles_per_split - 1) / L.tiles_per_split;
@@ -626,30 +946,63 @@ cudaError_t run_bidir(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStre
     return cudaSuccess;
 }
 
+cudaError_t run_causal(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
+    constexpr int D_V = CausalSmem::D_V;
+    unsigned *status = reinterpret_cast<unsigned *>(ws);
+    uint8_t *coef = ws + L.coef;
+    float *part = reinterpret_cast<float *>(ws + L.part);
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
+        !make_map(&tv, p.V, p.BH(), p.N, D_V))
+        return cudaErrorInvalidValue;
+    clk.mark();
+    GMA_TRY(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
+    coef_prep_tc_kernel<<<p.H, 256, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    GMA_TRY(set_smem(tc_write_kernel<D_V>, WriteSmem<D_V>::kAlloc));
+    tc_write_kernel<D_V><<<dim3(L.nsplit, p.BH()), 128, WriteSmem<D_V>::kAlloc, s>>>(
+        tk, tv, coef, p.H, p.N, L.tiles_per_split, L.nsplit, part, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    const int E = kKP * (D_V + 1);
+    scan_segments_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(part, L.nsplit, E, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    GMA_TRY(set_smem(tc_causal_kernel, CausalSmem::kAlloc));
+    tc_causal_kernel<<<dim3(L.nsplit, p.BH()), 128, CausalSmem::kAlloc, s>>>(
+        tq, tk, tv, coef, part, p.H, p.N, L.tiles_per_split, L.nsplit, p.eps, p.O, p.o_bf16 ? 1 : 0, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    return cudaSuccess;
+}
+
 }  // namespace
 
 const char *const kTcStages[3][8] = {
     {nullptr},
     {"prep", "tc_write", "tc_read", nullptr},
-    {nullptr},
+    {"prep", "tc_aggregate", "scan", "tc_causal", nullptr},
 };
 
 bool tc_supported(const Problem &p, int causal) {
-    return causal == 0 && p.dtype == GMA_BF16 && p.d_r == kDR && p.K <= kKP && (p.d_v == 64 || p.d_v == 128);
+    if (p.dtype != GMA_BF16 || p.d_r != kDR || p.K > kKP) return false;
+    if (causal == 0) return p.d_v == 64 || p.d_v == 128;
+    return causal == 1 && p.d_v == CausalSmem::D_V;
 }
 
-size_t tc_workspace(const Problem &p, int causal, int splits) {
-    (void)causal;
-    return tc_layout(p, splits).total;
-}
+size_t tc_workspace(const Problem &p, int causal, int splits) { return tc_layout(p, causal, splits).total; }
 
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
-    TcLayout L = tc_layout(p, splits);
+    TcLayout L = tc_layout(p, 0, splits);
     uint8_t *w = static_cast<uint8_t *>(ws);
     if (p.d_v == 64) return run_bidir<64>(p, L, w, s, clk);
     return run_bidir<128>(p, L, w, s, clk);
 }
 
-cudaError_t tc_causal(const Problem &, int, void *, cudaStream_t, StageClock &) { return cudaErrorNotSupported; }
+cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
+    TcLayout L = tc_layout(p, 1, splits);
+    return run_causal(p, L, static_cast<uint8_t *>(ws), s, clk);
+}
 
 }  // namespace gma
