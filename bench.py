@@ -39,7 +39,7 @@ UNIT = "token*heads/s"
 # reads or writes (Q_X, K_X, V_X read once, O written once per forward);
 # intermediate scratch traffic is not algorithmic.
 STAGE_TENSORS = {
-    "prep": "", "reduce": "", "scan": "",
+    "prep": "", "reset": "", "reduce": "", "scan": "",
     "resp_q": "Q", "resp_k": "K", "write": "V", "read": "O", "causal": "VO",
     "tc_write": "KV", "tc_read": "QO", "tc_causal": "QKVO", "tc_aggregate": "KV",
 }
@@ -355,7 +355,7 @@ def run_gma(args, rank: int, world: int, local_rank: int):
                           "l2": "inputs larger than L2 (201 MB read + 134 MB written per variant), no flush",
                           "output": "fp32 O",
                           "parallelism": f"replicas x{world}"},
-               "gpu_launches": args.steps * sum(len(s) for s in stages),
+               "gpu_launches": args.steps * sum(len([n for n in s if n != "reset"]) for s in stages),
                "roofline": roofline, "variants": variants, "stage_ms": stage_ms,
                "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu}
         print(json.dumps(out), flush=True)

@@ -366,174 +366,6 @@ __global__ void __launch_bounds__(128, 1) tc_write_kernel(const __grid_constant_
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ------------------------------------------------------------------ read kernel
-// Normalised broadcasting ([GMA, Eq. (7)]) for a range of query tiles of one
-// head.  Prologue: fixed-order sum of the split partials of the head, stored
-// as the bf16 hi / lo B operand [NB = D_V + 16 rows x KP] (row n < D_V: Vt[:, n];
-// row D_V: Z; other rows 0).
-template <int D_V>
-struct ReadSmem {
-    static constexpr int NB = D_V + 16;
-    static constexpr int kX = 0;                                   // Q tile
-    static constexpr int kX2 = kX + kTileBytes;                    // x2hi | x2lo, then Gamma
-    static constexpr int kCoef = kX2 + 2 * kTileBytes;
-    static constexpr int kB = kCoef + ((kCoefBytes + 1023) & ~1023);  // hi [NB x 128 B] | lo
-    static constexpr int kBars = kB + 2 * NB * 128;
-    static constexpr int kBytes = kBars + 64;
-    static constexpr int kAlloc = kBytes + 1024;
-};
-
-template <int D_V>
-__global__ void __launch_bounds__(128, 1) tc_read_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                          const uint8_t *__restrict__ coef_img,
-                                                          const float *__restrict__ part, int nsplit, int H,
-                                                          int N, int tiles_per_cta, float eps,
-                                                          void *__restrict__ O, int o_bf16, unsigned *status) {
-    using L = ReadSmem<D_V>;
-    constexpr int NB = L::NB;
-    constexpr int kTmemCols = 256;
-    constexpr int kAccO = kKP;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xq = smem + L::kX, *x2 = smem + L::kX2, *coef = smem + L::kCoef, *bop = smem + L::kB;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
-    int *abort_flag = reinterpret_cast<int *>(bars + 3);
-    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
-
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int bh = blockIdx.y, h = bh % H;
-    const int ntiles = (N + kTile - 1) / kTile;
-    const int tile0 = blockIdx.x * tiles_per_cta, tile1 = min(ntiles, tile0 + tiles_per_cta);
-    if (failed(status) || tile0 >= tile1) return;
-
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmQ);
-        mbar_arrive_expect_tx(&bars[0], kTileBytes);
-        tma_load_3d(xq, &tmQ, 0, tile0 * kTile, bh, &bars[0]);
-    }
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(coef_img + (size_t)h * kCoefStride);
-        uint4 *dst = reinterpret_cast<uint4 *>(coef);
-        for (int i = tid; i < kCoefBytes / 16; i += blockDim.x) dst[i] = src[i];
-    }
-    {
-        constexpr int W = D_V + 1;
-        const float *p = part + (size_t)bh * nsplit * kKP * W;
-        __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(bop);
-        __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(bop + NB * 128);
-        for (int e = tid; e < NB * kKP; e += blockDim.x) {
-            const int n = e / kKP, k = e % kKP;
-            float v = 0.f;
-            if (n <= D_V)
-                for (int s = 0; s < nsplit; ++s) v += p[((size_t)s * kKP + k) * W + n];
-            const __nv_bfloat16 vh = __float2bfloat16_rn(v);
-            const uint32_t off = sw128_offset(n, k, 1024) / 2;
-            bhi[off] = vh;
-            blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    constexpr uint32_t idesc_o = idesc_bf16(kTile, NB, false, false);
-    uint32_t ph_tma = 0, ph_mma = 0;
-
-    for (int tile = tile0; tile < tile1; ++tile) {
-        if (!mbar_wait(&bars[0], ph_tma)) note_timeout(status, abort_flag);
-        ph_tma ^= 1;
-        prep_x2(xq, x2, x2 + kTileBytes, kTileBytes, tid, blockDim.x);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            issue_scores(tmem, xq, x2, x2 + kTileBytes, coef);
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        tc_fence_after();
-        if (tid == 0 && tile + 1 < tile1) {  // Q tile and x^2 are free: fetch the next tile
-            mbar_arrive_expect_tx(&bars[0], kTileBytes);
-            tma_load_3d(xq, &tmQ, 0, (tile + 1) * kTile, bh, &bars[0]);
-        }
-        float r;
-        {
-            float e[kKP];
-            r = score_row_exp(tmem + lane_base, cvec, e);
-            store_gamma_row(x2, tid, e, 1.0f);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t sg = smem_u32(x2), sb = smem_u32(bop);
-#pragma unroll
-            for (int kk = 0; kk < kKP / 16; ++kk) {
-                const uint64_t ahi = sdesc_sw128(sg + kk * 32, 16, kGS), alo = sdesc_sw128(sg + 1024 + kk * 32, 16, kGS);
-                const uint64_t bhi = sdesc_sw128(sb + kk * 32, 16, 1024), blo = sdesc_sw128(sb + NB * 128 + kk * 32, 16, 1024);
-                umma_bf16(tmem + kAccO, ahi, bhi, idesc_o, kk > 0 ? 1u : 0u);
-                umma_bf16(tmem + kAccO, alo, bhi, idesc_o, 1u);
-                umma_bf16(tmem + kAccO, ahi, blo, idesc_o, 1u);
-            }
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        tc_fence_after();
-        {
-            uint32_t dz[16];
-            tmem_ld16(tmem + lane_base + kAccO + D_V, dz);
-            tmem_wait_ld();
-            const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * r);
-            const int tok = tile * kTile + tid;
-            const size_t row = (size_t)bh * N + tok;
-#pragma unroll
-            for (int cb = 0; cb < D_V / 32; ++cb) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kAccO + cb * 32, v);
-                tmem_wait_ld();
-                if (tok < N) {
-                    if (o_bf16) {
-                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + row * D_V + cb * 32);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            o[q] = make_uint4(pack_bf2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                                              pack_bf2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                                              pack_bf2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                                              pack_bf2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
-                    } else {
-                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(O) + row * D_V + cb * 32);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            o[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                               __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
-                    }
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-}
-
 // ------------------------------------------------------------------ causal
 // Exclusive prefix over the segment aggregates of each head, in segment
 // order, in place: part[s] <- sum_{s' < s} part[s'] ([GMA, causal variant:
@@ -846,6 +678,575 @@ __global__ void __launch_bounds__(128, 1) tc_causal_kernel(const __grid_constant
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ persistent pipelined kernels
+//
+// Work partition: the B*H*ntiles key/query tiles, in (head, tile) order, are
+// cut into one contiguous range per CTA (one CTA per SM).  A range that
+// crosses a head boundary is processed as one "job" per head.  Each CTA runs
+// 10 warps:
+//   warp 0      TMA producer (lane 0): tile loads into a ring of stages
+//   warp 1      MMA issuer (lane 0): tcgen05.mma + tcgen05.commit
+//   warps 2..5  epilogue group 0 \  alternate tiles (ping-pong): x^2 split,
+//   warps 6..9  epilogue group 1 /  softmax, Gamma split, outputs
+// Group g owns Gamma buffer g and TMEM score / output buffer g, so group g
+// handles every tile whose running index has parity g.
+constexpr int kThreads2 = 320;
+constexpr int kStages = 2;
+
+struct Part {
+    int ntiles;  // tiles per head
+    int total;   // B*H*ntiles
+    int tpc;     // tiles per CTA
+    int slots;   // partial slots per CTA (jobs per CTA, upper bound)
+};
+
+__host__ __device__ inline int first_cta_of_head(const Part &P, int bh) { return (bh * P.ntiles) / P.tpc; }
+__host__ __device__ inline int last_cta_of_head(const Part &P, int bh) {
+    return ((bh + 1) * P.ntiles - 1) / P.tpc;
+}
+// Slot of head bh's job inside CTA c (CTA c's range starts in head (c*tpc)/ntiles).
+__host__ __device__ inline int slot_of(const Part &P, int c, int bh) { return bh - (c * P.tpc) / P.ntiles; }
+
+// Coefficient image of head h built directly in shared memory (same layout
+// as coef_prep_tc_kernel writes), by every thread of the CTA.
+__device__ void build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
+                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, unsigned *status,
+                                int tid, int nthreads) {
+    __nv_bfloat16 *m16 = reinterpret_cast<__nv_bfloat16 *>(coef);
+    for (int e = tid; e < kKP * kDR; e += nthreads) {
+        const int k = e / kDR, j = e % kDR;
+        float a = 0.f, b = 0.f;
+        if (k < K) {
+            const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
+            if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+            a = -0.5f * kLog2e / s2;
+            b = kLog2e * m / s2;
+        }
+        const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
+        const uint32_t off = sw128_offset(k, j, 1024) / 2;
+        m16[off] = ah;
+        m16[kCoefMatBytes / 2 + off] = __float2bfloat16_rn(a - __bfloat162float(ah));
+        m16[kCoefMatBytes + off] = bh;
+        m16[3 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(b - __bfloat162float(bh));
+    }
+    float *cvec = reinterpret_cast<float *>(coef + 4 * kCoefMatBytes);
+    const int lane = tid & 31, nwarps = nthreads >> 5;
+    for (int k = tid >> 5; k < kKP; k += nwarps) {
+        double acc = 0.0;
+        if (k < K)
+            for (int j = lane; j < kDR; j += 32) {
+                const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
+                acc += (double)(m * m / s2) + (double)logf(s2);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            if (k < K) {
+                const float lp = log_pi[(size_t)h * K + k];
+                if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
+                cvec[k] = (float)((double)kLog2e * ((double)lp - 0.5 * acc));
+            } else {
+                cvec[k] = -INFINITY;
+            }
+        }
+    }
+}
+
+// Bounded polling: tick(progressed) returns false once kWaitLimitNs pass
+// without progress (or another role aborted).
+struct Stall {
+    uint64_t t0 = 0;
+    int spins = 0;
+    __device__ __forceinline__ bool tick(bool progressed, const int *abort_flag) {
+        if (progressed) {
+            spins = 0;
+            t0 = 0;
+            return true;
+        }
+        if (++spins < 256) return true;
+        spins = 0;
+        if (*reinterpret_cast<const volatile int *>(abort_flag)) return false;
+        const uint64_t now = globaltimer();
+        if (t0 == 0) t0 = now;
+        return now - t0 <= kWaitLimitNs;
+    }
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
+    if (mbar_wait(bar, parity)) return true;
+    note_timeout(status, abort_flag);
+    return false;
+}
+__device__ __forceinline__ bool aborted(const int *abort_flag) {
+    return *reinterpret_cast<const volatile int *>(abort_flag) != 0;
+}
+
+// Row of the tile / TMEM lane handled by an epilogue thread (warp w may only
+// read TMEM lanes 32*(w%4) .. 32*(w%4)+31).
+__device__ __forceinline__ int epi_row(int warp, int lane) { return 32 * (warp & 3) + lane; }
+
+// Writes one bf16 hi / lo B-operand image [NB rows x KP] for the read of the
+// latent memory: row n < D_V holds Vt[:, n], row D_V holds Z, other rows 0.
+template <int D_V>
+__device__ __forceinline__ void store_memory_operand(const float *S, int ldS, uint8_t *dst, int tid, int nthreads) {
+    constexpr int NB = D_V + 16;
+    __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(dst);
+    __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(dst + NB * 128);
+    for (int e = tid; e < NB * kKP; e += nthreads) {
+        const int n = e / kKP, k = e % kKP;
+        const float v = n <= D_V ? S[k * ldS + n] : 0.f;
+        const __nv_bfloat16 vh = __float2bfloat16_rn(v);
+        const uint32_t off = sw128_offset(n, k, 1024) / 2;
+        bhi[off] = vh;
+        blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
+    }
+}
+
+template <int D_V>
+struct Write2Smem {
+    static constexpr int W = D_V + 1;
+    static constexpr int kKst = 0;                                    // K stages
+    static constexpr int kVst = kKst + kStages * kTileBytes;          // V stages
+    static constexpr int kXG = kVst + kStages * (D_V / 64) * kTileBytes;  // x2 / Gamma buffers [2][32 KB]
+    static constexpr int kCoef = kXG + 2 * 2 * kTileBytes;
+    static constexpr int kOnes = kCoef + ((kCoefBytes + 1023) & ~1023);
+    static constexpr int kBars = kOnes + 2048;
+    static constexpr int kBytes = kBars + 256;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(128 * W * 4 <= kCoef, "reduction buffer must fit over the tile buffers");
+};
+
+// Latent aggregation ([GMA, Eqs. (5)-(6)]) over each job's keys:
+//   part[job][k][c] = sum_j gamma^K_jk V_jc,  part[job][k][d_v] = sum_j gamma^K_jk.
+// The last job of each head to finish combines the head's jobs in CTA order:
+//   mode 0: the bf16 hi / lo read operand of the whole-sequence memory (bidirectional),
+//   mode 1: in place, the exclusive prefix of each job (causal carry-in).
+template <int D_V>
+__global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
+    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    const float *__restrict__ mu, const float *__restrict__ sigma2, const float *__restrict__ log_pi, int K,
+    int H, int N, Part P, float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img,
+    size_t mem_img_stride, int mode, unsigned *status) {
+    using L = Write2Smem<D_V>;
+    constexpr int W = L::W;
+    constexpr int kTmemCols = D_V == 64 ? 256 : 512;
+    constexpr int kAccV = 2 * kKP, kAccZ = 2 * kKP + D_V;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *kst = smem + L::kKst, *vst = smem + L::kVst, *xg = smem + L::kXG, *coef = smem + L::kCoef,
+            *ones = smem + L::kOnes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *kvfull = bars, *kvempty = bars + 2, *xready = bars + 4, *sfull = bars + 6, *gready = bars + 8,
+             *wdone = bars + 10, *accfull = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    int *abort_flag = reinterpret_cast<int *>(bars + 15);
+    int *last_flag = abort_flag + 1;
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    if (failed(status) || g0 >= gend) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kvfull[i], 1);
+            mbar_init(&kvempty[i], 1);
+            mbar_init(&xready[i], 4);
+            mbar_init(&sfull[i], 1);
+            mbar_init(&gready[i], 4);
+            mbar_init(&wdone[i], 1);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    {
+        const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        for (int i = tid; i < 2048 / 16; i += kThreads2) reinterpret_cast<uint4 *>(ones)[i] = one4;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    constexpr uint32_t kTx = kTileBytes * (1 + D_V / 64);
+    constexpr uint32_t idesc_v = idesc_bf16(kTile, 64, true, true);
+    constexpr uint32_t idesc_z = idesc_bf16(kTile, 16, true, false);
+
+    int rbase = 0;   // running tile index of the CTA (barrier phases)
+    int njob = 0;
+    for (int g = g0; g < gend; ++njob) {
+        const int bh = g / P.ntiles, t0 = g % P.ntiles;
+        const int n = min(P.ntiles - t0, gend - g);
+        const int h = bh % H;
+        __syncthreads();
+        build_coef_smem(mu, sigma2, log_pi, h, K, coef, status, tid, kThreads2);
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        if (warp == 0) {
+            if (lane == 0)
+                for (int i = 0; i < n; ++i) {
+                    const int r = rbase + i, s = r % kStages;
+                    if (!wait_or_abort(&kvempty[s], ((r / kStages) & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(&kvfull[s], kTx);
+                    tma_load_3d(kst + s * kTileBytes, &tmK, 0, (t0 + i) * kTile, bh, &kvfull[s]);
+#pragma unroll
+                    for (int vb = 0; vb < D_V / 64; ++vb)
+                        tma_load_3d(vst + (s * (D_V / 64) + vb) * kTileBytes, &tmV, vb * 64, (t0 + i) * kTile, bh,
+                                    &kvfull[s]);
+                }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                // Poll both queues so that neither kind of MMA waits behind the other.
+                int ns = 0, nw = 0;
+                Stall st;
+                while (nw < n) {
+                    bool prog = false;
+                    if (ns < n) {
+                        const int r = rbase + ns, gb = r & 1, s = r % kStages;
+                        if (mbar_test(&xready[gb], (r >> 1) & 1)) {
+                            tc_fence_after();
+                            issue_scores(tmem + gb * kKP, kst + s * kTileBytes, xg + gb * 2 * kTileBytes,
+                                         xg + gb * 2 * kTileBytes + kTileBytes, coef);
+                            umma_commit(&sfull[gb]);
+                            ++ns;
+                            prog = true;
+                        }
+                    }
+                    if (nw < ns) {
+                        const int r = rbase + nw, gb = r & 1, s = r % kStages;
+                        if (mbar_test(&gready[gb], (r >> 1) & 1)) {
+                            tc_fence_after();
+                            const uint32_t sg = smem_u32(xg + gb * 2 * kTileBytes),
+                                           sv = smem_u32(vst + s * (D_V / 64) * kTileBytes);
+                            const uint64_t bz = sdesc_sw128(smem_u32(ones), 16, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < kTile / 16; ++kk) {
+                                const uint32_t acc = (nw > 0 || kk > 0) ? 1u : 0u;
+                                const uint64_t a = sdesc_sw128(sg + kk * 2 * kGS, 1024, kGS);
+#pragma unroll
+                                for (int vb = 0; vb < D_V / 64; ++vb)
+                                    umma_bf16(tmem + kAccV + vb * 64, a,
+                                              sdesc_sw128(sv + vb * kTileBytes + kk * 2048, 16, 1024), idesc_v, acc);
+                                umma_bf16(tmem + kAccZ, a, bz, idesc_z, acc);
+                            }
+                            umma_commit(&kvempty[s]);
+                            umma_commit(&wdone[gb]);
+                            ++nw;
+                            prog = true;
+                        }
+                    }
+                    if (!st.tick(prog, abort_flag)) {
+                        note_timeout(status, abort_flag);
+                        break;
+                    }
+                }
+                umma_commit(accfull);
+            }
+        } else {
+            const int grp = (warp - 2) >> 2;  // 0 or 1
+            const int row = epi_row(warp, lane);
+            const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+            for (int i = ((rbase & 1) == grp ? 0 : 1); i < n; i += 2) {
+                const int r = rbase + i, s = r % kStages;
+                uint8_t *gbuf = xg + grp * 2 * kTileBytes;
+                if (r >= 2 && !wait_or_abort(&wdone[grp], ((r - 2) >> 1) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&kvfull[s], (r / kStages) & 1, status, abort_flag)) break;
+                prep_x2(kst + s * kTileBytes, gbuf, gbuf + kTileBytes, kTileBytes, tid - 64 - 128 * grp, 128);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xready[grp]);
+                if (!wait_or_abort(&sfull[grp], (r >> 1) & 1, status, abort_flag)) break;
+                tc_fence_after();
+                float e[kKP];
+                const float rs = score_row_exp(tmem + lane_base + grp * kKP, cvec, e);
+                tc_fence_before();
+                const int tok = (t0 + i) * kTile + row;
+                store_gamma_row(gbuf, row, e, tok < N ? 1.0f / rs : 0.0f);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&gready[grp]);
+            }
+        }
+        // ---- job end: the accumulated memory -> partial of this job
+        __syncthreads();
+        const bool ok = !aborted(abort_flag);
+        float *red = reinterpret_cast<float *>(smem);  // [128][W] over the (now idle) tile buffers
+        if (ok && warp >= 2 && warp < 6) {
+            if (wait_or_abort(accfull, njob & 1, status, abort_flag)) {
+                tc_fence_after();
+                const int row = epi_row(warp, lane);
+                const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+#pragma unroll
+                for (int cb = 0; cb < D_V / 32; ++cb) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lb + kAccV + cb * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) red[row * W + cb * 32 + q] = __uint_as_float(v[q]);
+                }
+                uint32_t z[16];
+                tmem_ld16(tmem + lb + kAccZ, z);
+                tmem_wait_ld();
+                red[row * W + D_V] = __uint_as_float(z[0]);
+                tc_fence_before();
+            }
+        }
+        __syncthreads();
+        if (!aborted(abort_flag)) {
+            const int slot = slot_of(P, c, bh);
+            float *out = part + ((size_t)c * P.slots + slot) * kKP * W;
+            for (int e = tid; e < kKP * W; e += kThreads2) out[e] = red[e] + red[kKP * W + e];
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                const int njobs = last_cta_of_head(P, bh) - first_cta_of_head(P, bh) + 1;
+                const unsigned old = atomicAdd(&counters[bh], 1u);
+                *last_flag = (old == (unsigned)(njobs - 1));
+            }
+            __syncthreads();
+            if (*last_flag) {
+                __threadfence();
+                const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
+                if (mode == 0) {
+                    for (int e = tid; e < kKP * W; e += kThreads2) {
+                        float v = 0.f;
+                        for (int cc = cf; cc <= cl; ++cc)
+                            v += __ldcg(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kKP * W + e);
+                        red[e] = v;
+                    }
+                    __syncthreads();
+                    store_memory_operand<D_V>(red, W, mem_img + (size_t)bh * mem_img_stride, tid, kThreads2);
+                } else {
+                    for (int e = tid; e < kKP * W; e += kThreads2) {
+                        float run = 0.f;
+                        for (int cc = cf; cc <= cl; ++cc) {
+                            float *pp = part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kKP * W + e;
+                            const float cur = __ldcg(pp);
+                            *pp = run;
+                            run += cur;
+                        }
+                    }
+                }
+                if (tid == 0) counters[bh] = 0u;  // ready for the next call
+            }
+        }
+        rbase += n;
+        g += n;
+        if (aborted(abort_flag)) break;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D_V>
+struct Read2Smem {
+    static constexpr int NB = D_V + 16;
+    static constexpr int kQS = 3;
+    static constexpr int kQst = 0;
+    static constexpr int kXG = kQst + kQS * kTileBytes;
+    static constexpr int kCoef = kXG + 2 * 2 * kTileBytes;
+    static constexpr int kB = kCoef + ((kCoefBytes + 1023) & ~1023);
+    static constexpr int kBars = kB + ((2 * NB * 128 + 1023) & ~1023);
+    static constexpr int kBytes = kBars + 256;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+// Normalised broadcasting ([GMA, Eq. (7)]) over each job's query tiles.
+template <int D_V>
+__global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const float *__restrict__ mu, const float *__restrict__ sigma2,
+    const float *__restrict__ log_pi, int K, int H, int N, Part P, const uint8_t *__restrict__ mem_img,
+    size_t mem_img_stride, float eps, void *__restrict__ O, int o_bf16, unsigned *status) {
+    using L = Read2Smem<D_V>;
+    constexpr int NB = L::NB, QS = L::kQS;
+    constexpr int kTmemCols = 512;
+    constexpr int kAccO = 2 * kKP;  // O buffer g at kAccO + g * NB
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qst = smem + L::kQst, *xg = smem + L::kXG, *coef = smem + L::kCoef, *bop = smem + L::kB;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + 2, *gready = sfull + 2,
+             *ofull = gready + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ofull + 2);
+    int *abort_flag = reinterpret_cast<int *>(ofull + 3);
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    if (failed(status) || g0 >= gend) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int i = 0; i < QS; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xready[i], 4);
+            mbar_init(&sfull[i], 1);
+            mbar_init(&gready[i], 4);
+            mbar_init(&ofull[i], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    constexpr uint32_t idesc_o = idesc_bf16(kTile, NB, false, false);
+
+    int rbase = 0;
+    for (int g = g0; g < gend;) {
+        const int bh = g / P.ntiles, t0 = g % P.ntiles;
+        const int n = min(P.ntiles - t0, gend - g);
+        const int h = bh % H;
+        __syncthreads();
+        build_coef_smem(mu, sigma2, log_pi, h, K, coef, status, tid, kThreads2);
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(mem_img + (size_t)bh * mem_img_stride);
+            for (int i = tid; i < 2 * NB * 128 / 16; i += kThreads2) reinterpret_cast<uint4 *>(bop)[i] = __ldcg(src + i);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        if (warp == 0) {
+            if (lane == 0)
+                for (int i = 0; i < n; ++i) {
+                    const int r = rbase + i, s = r % QS;
+                    if (!wait_or_abort(&qempty[s], ((r / QS) & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(&qfull[s], kTileBytes);
+                    tma_load_3d(qst + s * kTileBytes, &tmQ, 0, (t0 + i) * kTile, bh, &qfull[s]);
+                }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                // Poll both queues so that neither kind of MMA waits behind the other.
+                int ns = 0, nr = 0;
+                Stall st;
+                while (nr < n) {
+                    bool prog = false;
+                    if (ns < n) {
+                        const int r = rbase + ns, gb = r & 1, s = r % QS;
+                        if (mbar_test(&xready[gb], (r >> 1) & 1)) {
+                            tc_fence_after();
+                            issue_scores(tmem + gb * kKP, qst + s * kTileBytes, xg + gb * 2 * kTileBytes,
+                                         xg + gb * 2 * kTileBytes + kTileBytes, coef);
+                            umma_commit(&sfull[gb]);
+                            umma_commit(&qempty[s]);
+                            ++ns;
+                            prog = true;
+                        }
+                    }
+                    if (nr < ns) {
+                        const int r = rbase + nr, gb = r & 1;
+                        if (mbar_test(&gready[gb], (r >> 1) & 1)) {
+                            tc_fence_after();
+                            const uint32_t sg = smem_u32(xg + gb * 2 * kTileBytes), sb = smem_u32(bop);
+                            const uint32_t d = tmem + kAccO + gb * NB;
+#pragma unroll
+                            for (int kk = 0; kk < kKP / 16; ++kk) {
+                                const uint64_t ahi = sdesc_sw128(sg + kk * 32, 16, kGS),
+                                               alo = sdesc_sw128(sg + 1024 + kk * 32, 16, kGS);
+                                const uint64_t bhi = sdesc_sw128(sb + kk * 32, 16, 1024),
+                                               blo = sdesc_sw128(sb + NB * 128 + kk * 32, 16, 1024);
+                                umma_bf16(d, ahi, bhi, idesc_o, kk > 0 ? 1u : 0u);
+                                umma_bf16(d, alo, bhi, idesc_o, 1u);
+                                umma_bf16(d, ahi, blo, idesc_o, 1u);
+                            }
+                            umma_commit(&ofull[gb]);
+                            ++nr;
+                            prog = true;
+                        }
+                    }
+                    if (!st.tick(prog, abort_flag)) {
+                        note_timeout(status, abort_flag);
+                        break;
+                    }
+                }
+            }
+        } else {
+            const int grp = (warp - 2) >> 2;
+            const int row = epi_row(warp, lane);
+            const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+            for (int i = ((rbase & 1) == grp ? 0 : 1); i < n; i += 2) {
+                const int r = rbase + i, s = r % QS;
+                uint8_t *gbuf = xg + grp * 2 * kTileBytes;
+                if (!wait_or_abort(&qfull[s], (r / QS) & 1, status, abort_flag)) break;
+                prep_x2(qst + s * kTileBytes, gbuf, gbuf + kTileBytes, kTileBytes, tid - 64 - 128 * grp, 128);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xready[grp]);
+                if (!wait_or_abort(&sfull[grp], (r >> 1) & 1, status, abort_flag)) break;
+                tc_fence_after();
+                float rs;
+                {
+                    float e[kKP];
+                    rs = score_row_exp(tmem + lane_base + grp * kKP, cvec, e);
+                    tc_fence_before();
+                    store_gamma_row(gbuf, row, e, 1.0f);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&gready[grp]);
+                if (!wait_or_abort(&ofull[grp], (r >> 1) & 1, status, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t ob = tmem + lane_base + kAccO + grp * NB;
+                uint32_t dz[16];
+                tmem_ld16(ob + D_V, dz);
+                tmem_wait_ld();
+                const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rs);
+                const int tok = (t0 + i) * kTile + row;
+                const size_t orow = (size_t)bh * N + tok;
+#pragma unroll
+                for (int cb = 0; cb < D_V / 32; ++cb) {
+                    uint32_t v[32];
+                    tmem_ld32(ob + cb * 32, v);
+                    tmem_wait_ld();
+                    if (tok < N) {
+                        if (o_bf16) {
+                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + orow * D_V + cb * 32);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                o[q] = make_uint4(pack_bf2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                                                  pack_bf2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                                                  pack_bf2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                                                  pack_bf2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+                        } else {
+                            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(O) + orow * D_V + cb * 32);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                o[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                                   __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+                        }
+                    }
+                }
+                tc_fence_before();
+            }
+        }
+        rbase += n;
+        g += n;
+        __syncthreads();
+        if (aborted(abort_flag)) break;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -915,32 +1316,67 @@ cudaError_t set_smem(KernelT kern, int bytes) {
         if (err_ != cudaSuccess) return err_; \
     } while (0)
 
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
+// Workspace of the persistent kernels: status | per-head counters | job
+// partials [ctas][slots][KP][d_v + 1] | per-head read operand images.
+struct TcLayout2 {
+    Part P;
+    int nctas = 0;
+    size_t counters = 0, part = 0, mem = 0, mem_stride = 0, total = 0, reset_bytes = 0;
+};
+
+TcLayout2 tc_layout2(const Problem &p, int splits) {
+    TcLayout2 L;
+    const int ntiles = (p.N + kTile - 1) / kTile;
+    const int total = p.BH() * ntiles;
+    int nct = splits > 0 ? splits : num_sms();
+    nct = nct < 1 ? 1 : (nct > total ? total : nct);
+    const int tpc = (total + nct - 1) / nct;
+    L.nctas = (total + tpc - 1) / tpc;
+    L.P = Part{ntiles, total, tpc, tpc / ntiles + 2};
+    size_t off = kStatusBytes;
+    L.counters = off;
+    off = align256(off + sizeof(unsigned) * (size_t)p.BH());
+    L.reset_bytes = off;
+    L.part = off;
+    off = align256(off + sizeof(float) * (size_t)L.nctas * L.P.slots * kKP * (p.d_v + 1));
+    L.mem_stride = ((size_t)2 * (p.d_v + 16) * 128 + 1023) & ~size_t(1023);
+    L.mem = off;
+    off = align256(off + L.mem_stride * p.BH());
+    L.total = off;
+    return L;
+}
+
 template <int D_V>
-cudaError_t run_bidir(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
+cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
     unsigned *status = reinterpret_cast<unsigned *>(ws);
-    uint8_t *coef = ws + L.coef;
+    unsigned *counters = reinterpret_cast<unsigned *>(ws + L.counters);
     float *part = reinterpret_cast<float *>(ws + L.part);
+    uint8_t *mem = ws + L.mem;
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
         !make_map(&tv, p.V, p.BH(), p.N, D_V))
         return cudaErrorInvalidValue;
     clk.mark();
-    GMA_TRY(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
-    coef_prep_tc_kernel<<<p.H, 256, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
+    GMA_TRY(cudaMemsetAsync(ws, 0, L.reset_bytes, s));
+    clk.mark();
+    GMA_TRY(set_smem(tc_write2_kernel<D_V>, Write2Smem<D_V>::kAlloc));
+    tc_write2_kernel<D_V><<<L.nctas, kThreads2, Write2Smem<D_V>::kAlloc, s>>>(
+        tk, tv, p.mu, p.sigma2, p.log_pi, p.K, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    GMA_TRY(set_smem(tc_write_kernel<D_V>, WriteSmem<D_V>::kAlloc));
-    tc_write_kernel<D_V><<<dim3(L.nsplit, p.BH()), 128, WriteSmem<D_V>::kAlloc, s>>>(
-        tk, tv, coef, p.H, p.N, L.tiles_per_split, L.nsplit, part, status);
-    GMA_TRY(cudaGetLastError());
-    clk.mark();
-    const int ntiles = (p.N + kTile - 1) / kTile;
-    int per = (int)(((long long)ntiles * p.BH() + kTargetCtas - 1) / kTargetCtas);
-    per = per < 1 ? 1 : per;
-    const int nct = (ntiles + per - 1) / per;
-    GMA_TRY(set_smem(tc_read_kernel<D_V>, ReadSmem<D_V>::kAlloc));
-    tc_read_kernel<D_V><<<dim3(nct, p.BH()), 128, ReadSmem<D_V>::kAlloc, s>>>(
-        tq, coef, part, L.nsplit, p.H, p.N, per, p.eps, p.O, p.o_bf16 ? 1 : 0, status);
+    GMA_TRY(set_smem(tc_read2_kernel<D_V>, Read2Smem<D_V>::kAlloc));
+    tc_read2_kernel<D_V><<<L.nctas, kThreads2, Read2Smem<D_V>::kAlloc, s>>>(
+        tq, p.mu, p.sigma2, p.log_pi, p.K, p.H, p.N, L.P, mem, L.mem_stride, p.eps, p.O, p.o_bf16 ? 1 : 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     return cudaSuccess;
@@ -981,7 +1417,7 @@ cudaError_t run_causal(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStr
 
 const char *const kTcStages[3][8] = {
     {nullptr},
-    {"prep", "tc_write", "tc_read", nullptr},
+    {"reset", "tc_write", "tc_read", nullptr},
     {"prep", "tc_aggregate", "scan", "tc_causal", nullptr},
 };
 
@@ -991,13 +1427,15 @@ bool tc_supported(const Problem &p, int causal) {
     return causal == 1 && p.d_v == CausalSmem::D_V;
 }
 
-size_t tc_workspace(const Problem &p, int causal, int splits) { return tc_layout(p, causal, splits).total; }
+size_t tc_workspace(const Problem &p, int causal, int splits) {
+    return causal ? tc_layout(p, causal, splits).total : tc_layout2(p, splits).total;
+}
 
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
-    TcLayout L = tc_layout(p, 0, splits);
+    TcLayout2 L = tc_layout2(p, splits);
     uint8_t *w = static_cast<uint8_t *>(ws);
-    if (p.d_v == 64) return run_bidir<64>(p, L, w, s, clk);
-    return run_bidir<128>(p, L, w, s, clk);
+    if (p.d_v == 64) return run_bidir2<64>(p, L, w, s, clk);
+    return run_bidir2<128>(p, L, w, s, clk);
 }
 
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
