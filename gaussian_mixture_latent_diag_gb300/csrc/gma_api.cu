@@ -75,7 +75,9 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
     if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
-    if (!aligned16(Q_X) || !aligned16(K_X) || !aligned16(V_X) || !aligned16(O)) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(Q_X) || !aligned16(K_X) || !aligned16(V_X) || !aligned16(O) || !aligned16(mu) ||
+        !aligned16(sigma2))
+        return GMA_ERR_INVALID_ARG;
     if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (options && (options->chunk < 0 || options->splits < 0)) return GMA_ERR_INVALID_ARG;
 

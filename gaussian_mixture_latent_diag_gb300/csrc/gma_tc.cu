@@ -59,53 +59,24 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
 // K-major SW128 byte image the score MMA reads (rows = components, 128 B of
 // d_r per row), plus c_k (fp32, -inf for padded components).  Validates the
 // parameters.
+__device__ void build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
+                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, unsigned *status,
+                                int tid, int nthreads);
+
 __global__ void coef_prep_tc_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
                                     const float *__restrict__ log_pi, int K, uint8_t *__restrict__ img,
                                     unsigned *status) {
-    const int h = blockIdx.x;
-    uint8_t *base = img + (size_t)h * kCoefStride;
-    __nv_bfloat16 *ahi = reinterpret_cast<__nv_bfloat16 *>(base);
-    for (int e = threadIdx.x; e < kKP * kDR; e += blockDim.x) {
-        const int k = e / kDR, j = e % kDR;
-        float a = 0.f, b = 0.f;
-        if (k < K) {
-            const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
-            if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-            a = -0.5f * kLog2e / s2;
-            b = kLog2e * m / s2;
-        }
-        const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
-        const uint32_t off = sw128_offset(k, j, 1024) / 2;  // in bf16 elements
-        ahi[off] = ah;
-        ahi[kCoefMatBytes / 2 + off] = __float2bfloat16_rn(a - __bfloat162float(ah));
-        ahi[2 * kCoefMatBytes / 2 + off] = bh;
-        ahi[3 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(b - __bfloat162float(bh));
-    }
-    // c_k: one warp per component, lanes over j, fp32 terms summed in fp64.
-    float *cvec = reinterpret_cast<float *>(base + 4 * kCoefMatBytes);
-    const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    for (int k = threadIdx.x >> 5; k < kKP; k += nwarps) {
-        double acc = 0.0;
-        if (k < K)
-            for (int j = lane; j < kDR; j += 32) {
-                const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
-                acc += (double)(m * m / s2) + (double)logf(s2);
-            }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) {
-            if (k < K) {
-                const float lp = log_pi[(size_t)h * K + k];
-                if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-                cvec[k] = (float)((double)kLog2e * ((double)lp - 0.5 * acc));
-            } else {
-                cvec[k] = -INFINITY;
-            }
-        }
-    }
+    build_coef_smem(mu, sigma2, log_pi, blockIdx.x, K, img + (size_t)blockIdx.x * kCoefStride, status, threadIdx.x,
+                    blockDim.x);
 }
 
 // ------------------------------------------------------------------ shared pieces
+
+// A shared-memory descriptor advanced by `bytes` (the start-address field is
+// the address >> 4 in the low bits; addresses stay below 256 KB, so a plain
+// add never carries out of the field).  Lets the single MMA-issuing thread
+// build each descriptor once and advance it with one add per MMA.
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
 
 // x^2 split: for every bf16 x of a tile, x2hi = rn(x*x), x2lo = x*x - x2hi
 // (exact, since x*x has at most 16 significant bits).  Position-preserving on
@@ -132,20 +103,16 @@ __device__ __forceinline__ void prep_x2(const uint8_t *x, uint8_t *x2h, uint8_t 
 __device__ __forceinline__ void issue_scores(uint32_t d_tmem, const uint8_t *x, const uint8_t *x2h,
                                              const uint8_t *x2l, const uint8_t *coef) {
     constexpr uint32_t idesc = idesc_bf16(kTile, kKP, false, false);
-    const uint32_t sx = smem_u32(x), sh = smem_u32(x2h), sl = smem_u32(x2l), sc = smem_u32(coef);
+    const uint64_t dx = sdesc_sw128(smem_u32(x), 16, 1024), dh = sdesc_sw128(smem_u32(x2h), 16, 1024),
+                   dl = sdesc_sw128(smem_u32(x2l), 16, 1024), dc = sdesc_sw128(smem_u32(coef), 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < kDR / 16; ++kk) {
         const uint32_t o = kk * 32;
-        const uint64_t ax = sdesc_sw128(sx + o, 16, 1024), ah = sdesc_sw128(sh + o, 16, 1024),
-                       al = sdesc_sw128(sl + o, 16, 1024);
-        const uint64_t bah = sdesc_sw128(sc + o, 16, 1024), bal = sdesc_sw128(sc + kCoefMatBytes + o, 16, 1024),
-                       bbh = sdesc_sw128(sc + 2 * kCoefMatBytes + o, 16, 1024),
-                       bbl = sdesc_sw128(sc + 3 * kCoefMatBytes + o, 16, 1024);
-        umma_bf16(d_tmem, ah, bah, idesc, kk > 0 ? 1u : 0u);
-        umma_bf16(d_tmem, ah, bal, idesc, 1u);
-        umma_bf16(d_tmem, al, bah, idesc, 1u);
-        umma_bf16(d_tmem, ax, bbh, idesc, 1u);
-        umma_bf16(d_tmem, ax, bbl, idesc, 1u);
+        umma_bf16(d_tmem, dadd(dh, o), dadd(dc, o), idesc, kk > 0 ? 1u : 0u);
+        umma_bf16(d_tmem, dadd(dh, o), dadd(dc, kCoefMatBytes + o), idesc, 1u);
+        umma_bf16(d_tmem, dadd(dl, o), dadd(dc, o), idesc, 1u);
+        umma_bf16(d_tmem, dadd(dx, o), dadd(dc, 2 * kCoefMatBytes + o), idesc, 1u);
+        umma_bf16(d_tmem, dadd(dx, o), dadd(dc, 3 * kCoefMatBytes + o), idesc, 1u);
     }
 }
 
@@ -305,15 +272,15 @@ __global__ void __launch_bounds__(128, 1) tc_write_kernel(const __grid_constant_
         if (*reinterpret_cast<volatile int *>(abort_flag)) break;
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t sg = smem_u32(x2), sv = smem_u32(vt), so = smem_u32(ones);
-            const uint64_t bz = sdesc_sw128(so, 16, 1024);
+            const uint64_t dg = sdesc_sw128(smem_u32(x2), 1024, kGS), dv = sdesc_sw128(smem_u32(vt), 16, 1024);
+            const uint64_t bz = sdesc_sw128(smem_u32(ones), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
                 const uint32_t acc = (tile > tile0 || kk > 0) ? 1u : 0u;
-                const uint64_t a = sdesc_sw128(sg + kk * 2 * kGS, 1024, kGS);
+                const uint64_t a = dadd(dg, kk * 2 * kGS);
 #pragma unroll
                 for (int vb = 0; vb < D_V / 64; ++vb) {
-                    const uint64_t b = sdesc_sw128(sv + vb * kTileBytes + kk * 2048, 16, 1024);
+                    const uint64_t b = dadd(dv, vb * kTileBytes + kk * 2048);
                     umma_bf16(tmem + kAccV + vb * 64, a, b, idesc_v, acc);
                 }
                 umma_bf16(tmem + kAccZ, a, bz, idesc_z, acc);
@@ -526,12 +493,13 @@ __global__ void __launch_bounds__(128, 1) tc_causal_kernel(const __grid_constant
         if (*reinterpret_cast<volatile int *>(abort_flag)) break;
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t sq = smem_u32(x2q), sk = smem_u32(x2k), sb = smem_u32(bop);
+            const uint64_t dq = sdesc_sw128(smem_u32(x2q), 16, kGS), dk = sdesc_sw128(smem_u32(x2k), 16, kGS),
+                           db = sdesc_sw128(smem_u32(bop), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kKP / 16; ++kk) {
-                const uint64_t qh = sdesc_sw128(sq + kk * 32, 16, kGS), ql = sdesc_sw128(sq + 1024 + kk * 32, 16, kGS);
-                const uint64_t kh = sdesc_sw128(sk + kk * 32, 16, kGS), kl = sdesc_sw128(sk + 1024 + kk * 32, 16, kGS);
-                const uint64_t bh_ = sdesc_sw128(sb + kk * 32, 16, 1024), bl_ = sdesc_sw128(sb + NB * 128 + kk * 32, 16, 1024);
+                const uint64_t qh = dadd(dq, kk * 32), ql = dadd(dq, 1024 + kk * 32);
+                const uint64_t kh = dadd(dk, kk * 32), kl = dadd(dk, 1024 + kk * 32);
+                const uint64_t bh_ = dadd(db, kk * 32), bl_ = dadd(db, NB * 128 + kk * 32);
                 const uint32_t acc = kk > 0 ? 1u : 0u;
                 umma_bf16(tmem + kP, qh, kh, idesc_p, acc);   // P = gQ gK^T (3 split terms)
                 umma_bf16(tmem + kP, ql, kh, idesc_p, 1u);
@@ -579,18 +547,19 @@ __global__ void __launch_bounds__(128, 1) tc_causal_kernel(const __grid_constant
         if (*reinterpret_cast<volatile int *>(abort_flag)) break;
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t sp = smem_u32(pbuf), sv = smem_u32(vt), sk = smem_u32(x2k), so = smem_u32(ones);
-            const uint64_t bz = sdesc_sw128(so, 16, 1024);
+            const uint64_t dp = sdesc_sw128(smem_u32(pbuf), 16, kGSP), dv = sdesc_sw128(smem_u32(vt), 16, 1024),
+                           dg = sdesc_sw128(smem_u32(x2k), 1024, kGS);
+            const uint64_t bz = sdesc_sw128(smem_u32(ones), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
                 const uint32_t ao = (kk >> 2) * 1024 + (kk & 3) * 32;
-                const uint64_t ph = sdesc_sw128(sp + ao, 16, kGSP), pl = sdesc_sw128(sp + 2048 + ao, 16, kGSP);
-                const uint64_t bv = sdesc_sw128(sv + kk * 2048, 16, 1024);
+                const uint64_t ph = dadd(dp, ao), pl = dadd(dp, 2048 + ao);
+                const uint64_t bv = dadd(dv, kk * 2048);
                 umma_bf16(tmem + kO, ph, bv, idesc_v, 1u);          // num += P V
                 umma_bf16(tmem + kO, pl, bv, idesc_v, 1u);
                 umma_bf16(tmem + kO + D_V, ph, bz, idesc_z, 1u);    // den += P 1
                 umma_bf16(tmem + kO + D_V, pl, bz, idesc_z, 1u);
-                const uint64_t ag = sdesc_sw128(sk + kk * 2 * kGS, 1024, kGS);  // [gK_hi ; gK_lo]^T
+                const uint64_t ag = dadd(dg, kk * 2 * kGS);  // [gK_hi ; gK_lo]^T
                 const uint32_t acc = kk > 0 ? 1u : 0u;
                 umma_bf16(tmem + kSc, ag, bv, idesc_sv, acc);       // chunk state: gK^T V
                 umma_bf16(tmem + kSc + D_V, ag, bz, idesc_sz, acc); //              gK^T 1
@@ -683,15 +652,16 @@ __global__ void __launch_bounds__(128, 1) tc_causal_kernel(const __grid_constant
 // Work partition: the B*H*ntiles key/query tiles, in (head, tile) order, are
 // cut into one contiguous range per CTA (one CTA per SM).  A range that
 // crosses a head boundary is processed as one "job" per head.  Each CTA runs
-// 10 warps:
-//   warp 0      TMA producer (lane 0): tile loads into a ring of stages
-//   warp 1      MMA issuer (lane 0): tcgen05.mma + tcgen05.commit
-//   warps 2..5  epilogue group 0 \  alternate tiles (ping-pong): x^2 split,
-//   warps 6..9  epilogue group 1 /  softmax, Gamma split, outputs
-// Group g owns Gamma buffer g and TMEM score / output buffer g, so group g
-// handles every tile whose running index has parity g.
-constexpr int kThreads2 = 320;
-constexpr int kStages = 2;
+// 2 + 4 NG warps:
+//   warp 0            TMA producer (lane 0): tile loads into NG stages
+//   warp 1            MMA issuer (lane 0): tcgen05.mma + tcgen05.commit,
+//                     polling every queue so no MMA waits behind another
+//   warps 2+4g..5+4g  epilogue group g: x^2 split, softmax, Gamma split,
+//                     outputs of every tile whose running index is g mod NG
+// Group g owns stage g, its Gamma buffer and its TMEM score / output area,
+// so NG tiles are in flight and their dependent MMA chains overlap.
+constexpr int kNG = 2;                       // epilogue groups (tiles in flight)
+constexpr int kThreadsG = 64 + 128 * kNG;    // TMA warp, MMA warp, NG x 4 epilogue warps
 
 struct Part {
     int ntiles;  // tiles per head
@@ -707,49 +677,87 @@ __host__ __device__ inline int last_cta_of_head(const Part &P, int bh) {
 // Slot of head bh's job inside CTA c (CTA c's range starts in head (c*tpc)/ntiles).
 __host__ __device__ inline int slot_of(const Part &P, int c, int bh) { return bh - (c * P.tpc) / P.ntiles; }
 
-// Coefficient image of head h built directly in shared memory (same layout
-// as coef_prep_tc_kernel writes), by every thread of the CTA.
+// Coefficient image of head h (K-major SW128 bf16 a_hi | a_lo | b_hi | b_lo,
+// then c_k) written through a generic pointer -- shared memory inside the
+// persistent kernels, global memory for coef_prep_tc_kernel -- by every
+// thread of the block.
 __device__ void build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
                                 const float *__restrict__ log_pi, int h, int K, uint8_t *coef, unsigned *status,
                                 int tid, int nthreads) {
-    __nv_bfloat16 *m16 = reinterpret_cast<__nv_bfloat16 *>(coef);
-    for (int e = tid; e < kKP * kDR; e += nthreads) {
-        const int k = e / kDR, j = e % kDR;
-        float a = 0.f, b = 0.f;
-        if (k < K) {
-            const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
-            if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-            a = -0.5f * kLog2e / s2;
-            b = kLog2e * m / s2;
+    // Four consecutive j of one component per step: float4 loads, issued for
+    // all of a thread's steps before any store, then 8-byte stores (the four
+    // bf16 values share one 16-byte chunk of the swizzled row).  With
+    // nthreads a multiple of 32, the 16 steps of one component sit in one
+    // half-warp, which also sums that component's log-determinant terms.
+    constexpr int kSteps = (kKP * kDR / 4 + 127) / 128;  // per thread, for >= 128 threads
+    float4 s4[kSteps], m4[kSteps];
+    float lp[kSteps];
+#pragma unroll
+    for (int q = 0; q < kSteps; ++q) {
+        const int e4 = tid + q * nthreads;  // index of a group of 4 elements
+        const int k = (e4 * 4) / kDR, j = (e4 * 4) % kDR;
+        s4[q] = make_float4(1.f, 1.f, 1.f, 1.f);
+        m4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        lp[q] = 0.f;
+        if (e4 * 4 < kKP * kDR && k < K) {
+            s4[q] = *reinterpret_cast<const float4 *>(sigma2 + ((size_t)h * K + k) * kDR + j);
+            m4[q] = *reinterpret_cast<const float4 *>(mu + ((size_t)h * K + k) * kDR + j);
+            lp[q] = log_pi[(size_t)h * K + k];
         }
-        const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
-        const uint32_t off = sw128_offset(k, j, 1024) / 2;
-        m16[off] = ah;
-        m16[kCoefMatBytes / 2 + off] = __float2bfloat16_rn(a - __bfloat162float(ah));
-        m16[kCoefMatBytes + off] = bh;
-        m16[3 * kCoefMatBytes / 2 + off] = __float2bfloat16_rn(b - __bfloat162float(bh));
     }
     float *cvec = reinterpret_cast<float *>(coef + 4 * kCoefMatBytes);
-    const int lane = tid & 31, nwarps = nthreads >> 5;
-    for (int k = tid >> 5; k < kKP; k += nwarps) {
-        double acc = 0.0;
-        if (k < K)
-            for (int j = lane; j < kDR; j += 32) {
-                const float s2 = sigma2[((size_t)h * K + k) * kDR + j], m = mu[((size_t)h * K + k) * kDR + j];
-                acc += (double)(m * m / s2) + (double)logf(s2);
-            }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) {
+    for (int q = 0; q < kSteps; ++q) {
+        const int e4 = tid + q * nthreads;
+        if (q * nthreads >= kKP * kDR / 4) break;  // uniform across the warp
+        const bool live = e4 * 4 < kKP * kDR;
+        const int k = (e4 * 4) / kDR, j = (e4 * 4) % kDR;
+        const float sv[4] = {s4[q].x, s4[q].y, s4[q].z, s4[q].w}, mv[4] = {m4[q].x, m4[q].y, m4[q].z, m4[q].w};
+        uint32_t ah[2], al[2], bh[2], bl[2];
+        float det = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            float a[2], b[2];
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                const float s2 = sv[2 * u + v], m = mv[2 * u + v];
+                const bool real = live && k < K;
+                if (real && (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m))) set_status(status, GMA_ERR_NONFINITE_PARAM);
+                const float inv = real ? __frcp_rn(s2) : 0.f;
+                a[v] = (-0.5f * kLog2e) * inv;
+                b[v] = (kLog2e * m) * inv;
+                det += real ? m * m * inv + __logf(s2) : 0.f;
+            }
+            ah[u] = pack_bf2(a[0], a[1]);
+            al[u] = pack_bf2(a[0] - bf_lo(ah[u]), a[1] - bf_hi(ah[u]));
+            bh[u] = pack_bf2(b[0], b[1]);
+            bl[u] = pack_bf2(b[0] - bf_lo(bh[u]), b[1] - bf_hi(bh[u]));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) det += __shfl_xor_sync(0xffffffffu, det, o);
+        if (!live) continue;
+        const uint32_t off = sw128_offset(k, j, 1024);  // 8-byte aligned (j % 4 == 0)
+        *reinterpret_cast<uint2 *>(coef + off) = make_uint2(ah[0], ah[1]);
+        *reinterpret_cast<uint2 *>(coef + kCoefMatBytes + off) = make_uint2(al[0], al[1]);
+        *reinterpret_cast<uint2 *>(coef + 2 * kCoefMatBytes + off) = make_uint2(bh[0], bh[1]);
+        *reinterpret_cast<uint2 *>(coef + 3 * kCoefMatBytes + off) = make_uint2(bl[0], bl[1]);
+        if (j == 0) {
             if (k < K) {
-                const float lp = log_pi[(size_t)h * K + k];
-                if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-                cvec[k] = (float)((double)kLog2e * ((double)lp - 0.5 * acc));
+                if (!isfinite(lp[q])) set_status(status, GMA_ERR_NONFINITE_PARAM);
+                cvec[k] = kLog2e * (lp[q] - 0.5f * det);
             } else {
                 cvec[k] = -INFINITY;
             }
         }
     }
+}
+
+// Copies head h's coefficient image (written once per call by
+// coef_prep_tc_kernel) into shared memory.
+__device__ __forceinline__ void copy_coef(const uint8_t *__restrict__ img, int h, uint8_t *coef, int tid, int nthreads) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(img + (size_t)h * kCoefStride);
+    uint4 *dst = reinterpret_cast<uint4 *>(coef);
+    for (int i = tid; i < kCoefBytes / 16; i += nthreads) dst[i] = __ldcg(src + i);
 }
 
 // Bounded polling: tick(progressed) returns false once kWaitLimitNs pass
@@ -802,44 +810,154 @@ __device__ __forceinline__ void store_memory_operand(const float *S, int ldS, ui
     }
 }
 
-template <int D_V>
+// x^2 split of this thread's row of a swizzled [128 x 64] bf16 tile, written
+// to tensor memory as an MMA A operand: x2hi at columns [0, 32), x2lo at
+// [32, 64) of `taddr` (this thread's lane).
+__device__ __forceinline__ void prep_x2_row_tmem(const uint8_t *x, int row, uint32_t taddr) {
+    uint32_t h[32], l[32];
+    const uint8_t *rp = x + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(rp + ((c ^ (row & 7)) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            h[4 * c + q] = bf2_fma(w[q], w[q], 0x80008000u);
+            l[4 * c + q] = bf2_fma(w[q], w[q], h[4 * c + q] ^ 0x80008000u);
+        }
+    }
+    tmem_st32(taddr, h);
+    tmem_st32(taddr + 32, l);
+    tmem_wait_st();
+}
+
+// Score MMAs of one tile, 12 instructions (4 K-steps x 3): the coefficient
+// image holds [a_hi ; a_lo] and [b_hi ; b_lo] as two N = 128 operands, so
+//   D[:, 0:128]  = x2hi [a_hi | a_lo] + x [b_hi | b_lo]   (N = 128)
+//   D[:, 0:64]  += x2lo a_hi                               (N = 64)
+// and the score of component k is D[:, k] + D[:, 64 + k] (+ c_k).
+// The x^2 operands come from tensor memory (a_tmem: x2hi +0, x2lo +32), x from
+// shared memory (descriptor dx), coefficients from shared memory (dc).
+__device__ __forceinline__ void issue_scores_tA(uint32_t d_tmem, uint32_t a_tmem, uint64_t dx, uint64_t dc) {
+    constexpr uint32_t i128 = idesc_bf16(kTile, 128, false, false);
+    constexpr uint32_t i64 = idesc_bf16(kTile, 64, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kDR / 16; ++kk) {
+        const uint32_t o = kk * 32;
+        umma_bf16_tA(d_tmem, a_tmem + kk * 8, dadd(dc, o), i128, kk > 0 ? 1u : 0u);
+        umma_bf16(d_tmem, dadd(dx, o), dadd(dc, 2 * kCoefMatBytes + o), i128, 1u);
+        umma_bf16_tA(d_tmem, a_tmem + 32 + kk * 8, dadd(dc, o), i64, 1u);
+    }
+}
+
+// Score row (two 64-column halves in TMEM) -> exponentials e_k = 2^(s_k - max);
+// returns the row sum.
+__device__ __forceinline__ float score_row_exp128(uint32_t taddr, const float *cvec, float (&e)[kKP]) {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32(taddr, r0);
+    tmem_ld32(taddr + 32, r1);
+    tmem_ld32(taddr + 64, r2);
+    tmem_ld32(taddr + 96, r3);
+    tmem_wait_ld();
+    const float4 *c4 = reinterpret_cast<const float4 *>(cvec);
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 ca = c4[q], cb = c4[q + 8];
+#define GMA_U(r, i) __uint_as_float(r[i])
+        const float2 a0 = f2_add(f2_add(make_float2(GMA_U(r0, 4 * q), GMA_U(r0, 4 * q + 1)),
+                                        make_float2(GMA_U(r2, 4 * q), GMA_U(r2, 4 * q + 1))), make_float2(ca.x, ca.y));
+        const float2 a1 = f2_add(f2_add(make_float2(GMA_U(r0, 4 * q + 2), GMA_U(r0, 4 * q + 3)),
+                                        make_float2(GMA_U(r2, 4 * q + 2), GMA_U(r2, 4 * q + 3))), make_float2(ca.z, ca.w));
+        const float2 b0 = f2_add(f2_add(make_float2(GMA_U(r1, 4 * q), GMA_U(r1, 4 * q + 1)),
+                                        make_float2(GMA_U(r3, 4 * q), GMA_U(r3, 4 * q + 1))), make_float2(cb.x, cb.y));
+        const float2 b1 = f2_add(f2_add(make_float2(GMA_U(r1, 4 * q + 2), GMA_U(r1, 4 * q + 3)),
+                                        make_float2(GMA_U(r3, 4 * q + 2), GMA_U(r3, 4 * q + 3))), make_float2(cb.z, cb.w));
+#undef GMA_U
+        e[4 * q] = a0.x; e[4 * q + 1] = a0.y; e[4 * q + 2] = a1.x; e[4 * q + 3] = a1.y;
+        e[32 + 4 * q] = b0.x; e[32 + 4 * q + 1] = b0.y; e[32 + 4 * q + 2] = b1.x; e[32 + 4 * q + 3] = b1.y;
+        m0 = fmaxf(m0, fmaxf(fmaxf(a0.x, a0.y), fmaxf(a1.x, a1.y)));
+        m1 = fmaxf(m1, fmaxf(fmaxf(b0.x, b0.y), fmaxf(b1.x, b1.y)));
+    }
+    const float m = fmaxf(m0, m1);
+    const float2 mm = make_float2(m, m);
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kKP; k += 4) {
+        const float2 d0 = f2_sub(make_float2(e[k], e[k + 1]), mm), d1 = f2_sub(make_float2(e[k + 2], e[k + 3]), mm);
+        e[k] = ex2(d0.x); e[k + 1] = ex2(d0.y); e[k + 2] = ex2(d1.x); e[k + 3] = ex2(d1.y);
+        s0 = f2_add(s0, make_float2(e[k], e[k + 1]));
+        s1 = f2_add(s1, make_float2(e[k + 2], e[k + 3]));
+    }
+    return (s0.x + s0.y) + (s1.x + s1.y);
+}
+
+// bf16 hi / lo words of a responsibility row scaled by `scale`.
+__device__ __forceinline__ void split_row(const float (&e)[kKP], float scale, uint32_t (&wh)[32], uint32_t (&wl)[32]) {
+    const float2 sc = make_float2(scale, scale);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        const float2 g = f2_mul(make_float2(e[2 * q], e[2 * q + 1]), sc);
+        wh[q] = pack_bf2(g.x, g.y);
+        const float2 r = f2_sub(g, make_float2(bf_lo(wh[q]), bf_hi(wh[q])));
+        wl[q] = pack_bf2(r.x, r.y);
+    }
+}
+
+// Same row written as the MN-major / K-major SMEM layout of a Gamma buffer.
+__device__ __forceinline__ void store_gamma_words(uint8_t *gbuf, int t, const uint32_t (&wh)[32],
+                                                  const uint32_t (&wl)[32]) {
+    uint8_t *hi = gbuf + (t >> 3) * kGS + (t & 7) * 128;
+    uint8_t *lo = hi + 1024;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t sw = (uint32_t)((c ^ (t & 7)) << 4);
+        *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[4 * c], wh[4 * c + 1], wh[4 * c + 2], wh[4 * c + 3]);
+        *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[4 * c], wl[4 * c + 1], wl[4 * c + 2], wl[4 * c + 3]);
+    }
+}
+
+// V stage of the write kernel: the TMA box [128 tokens x 64] (MN-major B
+// chunk 0) followed by a constant chunk of ones (chunk 1), so one N = 80 MMA
+// gives both Gamma^T V (columns 0..63) and Gamma^T 1 (column 64).
+constexpr int kVStageBytes = 2 * kTileBytes;
+
 struct Write2Smem {
-    static constexpr int W = D_V + 1;
-    static constexpr int kKst = 0;                                    // K stages
-    static constexpr int kVst = kKst + kStages * kTileBytes;          // V stages
-    static constexpr int kXG = kVst + kStages * (D_V / 64) * kTileBytes;  // x2 / Gamma buffers [2][32 KB]
-    static constexpr int kCoef = kXG + 2 * 2 * kTileBytes;
-    static constexpr int kOnes = kCoef + ((kCoefBytes + 1023) & ~1023);
-    static constexpr int kBars = kOnes + 2048;
+    static constexpr int W = 64 + 1;
+    static constexpr int kKst = 0;                              // K stages
+    static constexpr int kVst = kKst + kNG * kTileBytes;        // V | ones stages
+    static constexpr int kXG = kVst + kNG * kVStageBytes;       // Gamma^K buffers [NG][32 KB]
+    static constexpr int kCoef = kXG + kNG * 2 * kTileBytes;
+    static constexpr int kBars = kCoef + ((kCoefBytes + 1023) & ~1023);
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(128 * W * 4 <= kCoef, "reduction buffer must fit over the tile buffers");
 };
 
-// Latent aggregation ([GMA, Eqs. (5)-(6)]) over each job's keys:
-//   part[job][k][c] = sum_j gamma^K_jk V_jc,  part[job][k][d_v] = sum_j gamma^K_jk.
+// Latent aggregation ([GMA, Eqs. (5)-(6)]) over each job's keys (d_v = 64):
+//   part[job][k][c] = sum_j gamma^K_jk V_jc,  part[job][k][64] = sum_j gamma^K_jk.
 // The last job of each head to finish combines the head's jobs in CTA order:
 //   mode 0: the bf16 hi / lo read operand of the whole-sequence memory (bidirectional),
 //   mode 1: in place, the exclusive prefix of each job (causal carry-in).
-template <int D_V>
-__global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
+// TMEM: scores of group g at [128 g, +128); x^2 operand of group g at
+// [128 NG + 64 g, +64); accumulator [Vt | Z] (N = 80) at 192 NG.
+__global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-    const float *__restrict__ mu, const float *__restrict__ sigma2, const float *__restrict__ log_pi, int K,
-    int H, int N, Part P, float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img,
+    const uint8_t *__restrict__ coef_img, int H, int N, Part P, float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img,
     size_t mem_img_stride, int mode, unsigned *status) {
-    using L = Write2Smem<D_V>;
-    constexpr int W = L::W;
-    constexpr int kTmemCols = D_V == 64 ? 256 : 512;
-    constexpr int kAccV = 2 * kKP, kAccZ = 2 * kKP + D_V;
+    using L = Write2Smem;
+    constexpr int D_V = 64, W = L::W;
+    constexpr int kTmemCols = 512;
+    constexpr int kA = 2 * kNG * kKP, kAcc = 3 * kNG * kKP;
+    static_assert(kAcc + 80 <= kTmemCols, "TMEM budget");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *kst = smem + L::kKst, *vst = smem + L::kVst, *xg = smem + L::kXG, *coef = smem + L::kCoef,
-            *ones = smem + L::kOnes;
+    uint8_t *kst = smem + L::kKst, *vst = smem + L::kVst, *xg = smem + L::kXG, *coef = smem + L::kCoef;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint64_t *kvfull = bars, *kvempty = bars + 2, *xready = bars + 4, *sfull = bars + 6, *gready = bars + 8,
-             *wdone = bars + 10, *accfull = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
-    int *abort_flag = reinterpret_cast<int *>(bars + 15);
+    uint64_t *kvfull = bars, *kvempty = bars + kNG, *xready = bars + 2 * kNG, *sfull = bars + 3 * kNG,
+             *gready = bars + 4 * kNG, *wdone = bars + 5 * kNG, *accfull = bars + 6 * kNG;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 6 * kNG + 1);
+    int *abort_flag = reinterpret_cast<int *>(bars + 6 * kNG + 2);
     int *last_flag = abort_flag + 1;
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
@@ -853,7 +971,7 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
         tmem_relinquish();
     }
     if (tid == 32) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNG; ++i) {
             mbar_init(&kvfull[i], 1);
             mbar_init(&kvempty[i], 1);
             mbar_init(&xready[i], 4);
@@ -867,17 +985,18 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    {
+    {   // the constant ones chunk of every V stage
         const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int i = tid; i < 2048 / 16; i += kThreads2) reinterpret_cast<uint4 *>(ones)[i] = one4;
+        for (int st = 0; st < kNG; ++st)
+            for (int i = tid; i < kTileBytes / 16; i += kThreadsG)
+                reinterpret_cast<uint4 *>(vst + st * kVStageBytes + kTileBytes)[i] = one4;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t kTx = kTileBytes * (1 + D_V / 64);
-    constexpr uint32_t idesc_v = idesc_bf16(kTile, 64, true, true);
-    constexpr uint32_t idesc_z = idesc_bf16(kTile, 16, true, false);
+    constexpr uint32_t kTx = 2 * kTileBytes;
+    constexpr uint32_t idesc_w = idesc_bf16(kTile, 80, true, true);
 
     int rbase = 0;   // running tile index of the CTA (barrier phases)
     int njob = 0;
@@ -886,57 +1005,49 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
         __syncthreads();
-        build_coef_smem(mu, sigma2, log_pi, h, K, coef, status, tid, kThreads2);
+        copy_coef(coef_img, h, coef, tid, kThreadsG);
         fence_proxy_async_smem();
         __syncthreads();
 
         if (warp == 0) {
             if (lane == 0)
                 for (int i = 0; i < n; ++i) {
-                    const int r = rbase + i, s = r % kStages;
-                    if (!wait_or_abort(&kvempty[s], ((r / kStages) & 1) ^ 1, status, abort_flag)) break;
+                    const int r = rbase + i, s = r % kNG;
+                    if (!wait_or_abort(&kvempty[s], ((r / kNG) & 1) ^ 1, status, abort_flag)) break;
                     mbar_arrive_expect_tx(&kvfull[s], kTx);
                     tma_load_3d(kst + s * kTileBytes, &tmK, 0, (t0 + i) * kTile, bh, &kvfull[s]);
-#pragma unroll
-                    for (int vb = 0; vb < D_V / 64; ++vb)
-                        tma_load_3d(vst + (s * (D_V / 64) + vb) * kTileBytes, &tmV, vb * 64, (t0 + i) * kTile, bh,
-                                    &kvfull[s]);
+                    tma_load_3d(vst + s * kVStageBytes, &tmV, 0, (t0 + i) * kTile, bh, &kvfull[s]);
                 }
         } else if (warp == 1) {
             if (lane == 0) {
+                // Base descriptors, built once; each MMA advances one by an add.
+                const uint64_t dk0 = sdesc_sw128(smem_u32(kst), 16, 1024), dc0 = sdesc_sw128(smem_u32(coef), 16, 1024);
+                const uint64_t dg0 = sdesc_sw128(smem_u32(xg), 1024, kGS);
+                const uint64_t dv0 = sdesc_sw128(smem_u32(vst), kTileBytes, 1024);  // chunk stride = LBO
                 // Poll both queues so that neither kind of MMA waits behind the other.
                 int ns = 0, nw = 0;
                 Stall st;
                 while (nw < n) {
                     bool prog = false;
                     if (ns < n) {
-                        const int r = rbase + ns, gb = r & 1, s = r % kStages;
-                        if (mbar_test(&xready[gb], (r >> 1) & 1)) {
+                        const int r = rbase + ns, gb = r % kNG, s = gb;
+                        if (mbar_test(&xready[gb], (r / kNG) & 1)) {
                             tc_fence_after();
-                            issue_scores(tmem + gb * kKP, kst + s * kTileBytes, xg + gb * 2 * kTileBytes,
-                                         xg + gb * 2 * kTileBytes + kTileBytes, coef);
+                            issue_scores_tA(tmem + gb * 2 * kKP, tmem + kA + gb * kKP, dadd(dk0, s * kTileBytes), dc0);
                             umma_commit(&sfull[gb]);
                             ++ns;
                             prog = true;
                         }
                     }
                     if (nw < ns) {
-                        const int r = rbase + nw, gb = r & 1, s = r % kStages;
-                        if (mbar_test(&gready[gb], (r >> 1) & 1)) {
+                        const int r = rbase + nw, gb = r % kNG, s = gb;
+                        if (mbar_test(&gready[gb], (r / kNG) & 1)) {
                             tc_fence_after();
-                            const uint32_t sg = smem_u32(xg + gb * 2 * kTileBytes),
-                                           sv = smem_u32(vst + s * (D_V / 64) * kTileBytes);
-                            const uint64_t bz = sdesc_sw128(smem_u32(ones), 16, 1024);
+                            const uint64_t ag = dadd(dg0, gb * 2 * kTileBytes), bv = dadd(dv0, s * kVStageBytes);
 #pragma unroll
-                            for (int kk = 0; kk < kTile / 16; ++kk) {
-                                const uint32_t acc = (nw > 0 || kk > 0) ? 1u : 0u;
-                                const uint64_t a = sdesc_sw128(sg + kk * 2 * kGS, 1024, kGS);
-#pragma unroll
-                                for (int vb = 0; vb < D_V / 64; ++vb)
-                                    umma_bf16(tmem + kAccV + vb * 64, a,
-                                              sdesc_sw128(sv + vb * kTileBytes + kk * 2048, 16, 1024), idesc_v, acc);
-                                umma_bf16(tmem + kAccZ, a, bz, idesc_z, acc);
-                            }
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                umma_bf16(tmem + kAcc, dadd(ag, kk * 2 * kGS), dadd(bv, kk * 2048), idesc_w,
+                                          (nw > 0 || kk > 0) ? 1u : 0u);
                             umma_commit(&kvempty[s]);
                             umma_commit(&wdone[gb]);
                             ++nw;
@@ -951,25 +1062,27 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
                 umma_commit(accfull);
             }
         } else {
-            const int grp = (warp - 2) >> 2;  // 0 or 1
+            const int grp = (warp - 2) >> 2;  // 0 .. NG-1
             const int row = epi_row(warp, lane);
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-            for (int i = ((rbase & 1) == grp ? 0 : 1); i < n; i += 2) {
-                const int r = rbase + i, s = r % kStages;
+            for (int i = (grp - rbase % kNG + kNG) % kNG; i < n; i += kNG) {
+                const int r = rbase + i, s = grp;
                 uint8_t *gbuf = xg + grp * 2 * kTileBytes;
-                if (r >= 2 && !wait_or_abort(&wdone[grp], ((r - 2) >> 1) & 1, status, abort_flag)) break;
-                if (!wait_or_abort(&kvfull[s], (r / kStages) & 1, status, abort_flag)) break;
-                prep_x2(kst + s * kTileBytes, gbuf, gbuf + kTileBytes, kTileBytes, tid - 64 - 128 * grp, 128);
-                fence_proxy_async_smem();
+                if (!wait_or_abort(&kvfull[s], (r / kNG) & 1, status, abort_flag)) break;
+                prep_x2_row_tmem(kst + s * kTileBytes, row, tmem + lane_base + kA + grp * kKP);
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xready[grp]);
-                if (!wait_or_abort(&sfull[grp], (r >> 1) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&sfull[grp], (r / kNG) & 1, status, abort_flag)) break;
                 tc_fence_after();
                 float e[kKP];
-                const float rs = score_row_exp(tmem + lane_base + grp * kKP, cvec, e);
+                const float rs = score_row_exp128(tmem + lane_base + grp * 2 * kKP, cvec, e);
                 tc_fence_before();
                 const int tok = (t0 + i) * kTile + row;
-                store_gamma_row(gbuf, row, e, tok < N ? 1.0f / rs : 0.0f);
+                uint32_t wh[32], wl[32];
+                split_row(e, tok < N ? 1.0f / rs : 0.0f, wh, wl);
+                if (r >= kNG && !wait_or_abort(&wdone[grp], ((r - kNG) / kNG) & 1, status, abort_flag)) break;
+                store_gamma_words(gbuf, row, wh, wl);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&gready[grp]);
@@ -977,24 +1090,22 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
         }
         // ---- job end: the accumulated memory -> partial of this job
         __syncthreads();
-        const bool ok = !aborted(abort_flag);
         float *red = reinterpret_cast<float *>(smem);  // [128][W] over the (now idle) tile buffers
-        if (ok && warp >= 2 && warp < 6) {
+        if (!aborted(abort_flag) && warp >= 2 && warp < 6) {  // group 0 covers all 128 lanes
             if (wait_or_abort(accfull, njob & 1, status, abort_flag)) {
                 tc_fence_after();
                 const int row = epi_row(warp, lane);
                 const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-#pragma unroll
-                for (int cb = 0; cb < D_V / 32; ++cb) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lb + kAccV + cb * 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) red[row * W + cb * 32 + q] = __uint_as_float(v[q]);
-                }
-                uint32_t z[16];
-                tmem_ld16(tmem + lb + kAccZ, z);
+                uint32_t v0[32], v1[32], z[16];
+                tmem_ld32(tmem + lb + kAcc, v0);
+                tmem_ld32(tmem + lb + kAcc + 32, v1);
+                tmem_ld16(tmem + lb + kAcc + 64, z);
                 tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    red[row * W + q] = __uint_as_float(v0[q]);
+                    red[row * W + 32 + q] = __uint_as_float(v1[q]);
+                }
                 red[row * W + D_V] = __uint_as_float(z[0]);
                 tc_fence_before();
             }
@@ -1003,7 +1114,7 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
         if (!aborted(abort_flag)) {
             const int slot = slot_of(P, c, bh);
             float *out = part + ((size_t)c * P.slots + slot) * kKP * W;
-            for (int e = tid; e < kKP * W; e += kThreads2) out[e] = red[e] + red[kKP * W + e];
+            for (int e = tid; e < kKP * W; e += kThreadsG) out[e] = red[e] + red[kKP * W + e];
             __threadfence();
             __syncthreads();
             if (tid == 0) {
@@ -1016,16 +1127,16 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
                 __threadfence();
                 const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
                 if (mode == 0) {
-                    for (int e = tid; e < kKP * W; e += kThreads2) {
+                    for (int e = tid; e < kKP * W; e += kThreadsG) {
                         float v = 0.f;
                         for (int cc = cf; cc <= cl; ++cc)
                             v += __ldcg(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kKP * W + e);
                         red[e] = v;
                     }
                     __syncthreads();
-                    store_memory_operand<D_V>(red, W, mem_img + (size_t)bh * mem_img_stride, tid, kThreads2);
+                    store_memory_operand<D_V>(red, W, mem_img + (size_t)bh * mem_img_stride, tid, kThreadsG);
                 } else {
-                    for (int e = tid; e < kKP * W; e += kThreads2) {
+                    for (int e = tid; e < kKP * W; e += kThreadsG) {
                         float run = 0.f;
                         for (int cc = cf; cc <= cl; ++cc) {
                             float *pp = part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kKP * W + e;
@@ -1047,37 +1158,78 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_write2_kernel(
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D_V>
+// Output staging for TMA stores: each epilogue warp owns 8 KB (its 32 rows),
+// fp32: two [32 rows x 128 B] swizzled boxes (columns 0-31 | 32-63);
+// bf16: one [32 rows x 128 B] swizzled box.  o holds the row's 64 values.
+__device__ __forceinline__ void stage_and_store_rows(uint8_t *stage, const float (&o)[64], int r32, int lane,
+                                                     const CUtensorMap *tmO, int o_bf16, int row0, int bh) {
+    if (lane == 0) bulk_wait_read0();  // this warp's previous stores have read the staging area
+    __syncwarp();
+    if (o_bf16) {
+        uint8_t *rp = stage + r32 * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 w = make_uint4(pack_bf2(o[8 * c], o[8 * c + 1]), pack_bf2(o[8 * c + 2], o[8 * c + 3]),
+                                       pack_bf2(o[8 * c + 4], o[8 * c + 5]), pack_bf2(o[8 * c + 6], o[8 * c + 7]));
+            *reinterpret_cast<uint4 *>(rp + ((c ^ (r32 & 7)) << 4)) = w;
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            uint8_t *rp = stage + b * 4096 + r32 * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int k = 32 * b + 4 * c;
+                *reinterpret_cast<float4 *>(rp + ((c ^ (r32 & 7)) << 4)) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmO, stage, 0, row0, bh);
+        if (!o_bf16) tma_store_3d(tmO, stage + 4096, 32, row0, bh);
+        bulk_commit();
+    }
+}
+
 struct Read2Smem {
-    static constexpr int NB = D_V + 16;
-    static constexpr int kQS = 3;
+    static constexpr int NB = 64 + 16;
+    static constexpr int kQS = kNG;
     static constexpr int kQst = 0;
-    static constexpr int kXG = kQst + kQS * kTileBytes;
-    static constexpr int kCoef = kXG + 2 * 2 * kTileBytes;
+    static constexpr int kStage = kQst + kQS * kTileBytes;        // [NG groups][4 warps][8 KB]
+    static constexpr int kCoef = kStage + kNG * 4 * 8192;
     static constexpr int kB = kCoef + ((kCoefBytes + 1023) & ~1023);
     static constexpr int kBars = kB + ((2 * NB * 128 + 1023) & ~1023);
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
 };
 
-// Normalised broadcasting ([GMA, Eq. (7)]) over each job's query tiles.
-template <int D_V>
-__global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
-    const __grid_constant__ CUtensorMap tmQ, const float *__restrict__ mu, const float *__restrict__ sigma2,
-    const float *__restrict__ log_pi, int K, int H, int N, Part P, const uint8_t *__restrict__ mem_img,
-    size_t mem_img_stride, float eps, void *__restrict__ O, int o_bf16, unsigned *status) {
-    using L = Read2Smem<D_V>;
+// Normalised broadcasting ([GMA, Eq. (7)]) over each job's query tiles (d_v = 64).
+// Read MMAs, 8 per tile (4 K-steps x 2), with the memory operand stored as one
+// N = 160 K-major matrix [B_hi ; B_lo]:
+//   D[:, 0:160] = Ghi [B_hi | B_lo] ,  D[:, 0:80] += Glo B_hi ,
+// so [num | den] = D[:, 0:80] + D[:, 80:160].
+// TMEM, group g at [224 g, +224): operand area [+0, +64) (x^2 for the scores,
+// then Gamma^Q hi | lo); scores [+64, +192), then D over [+64, +224) once the
+// scores have been consumed.
+__global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+    const uint8_t *__restrict__ coef_img, int H, int N, Part P,
+    const uint8_t *__restrict__ mem_img, size_t mem_img_stride, float eps, int o_bf16, unsigned *status) {
+    using L = Read2Smem;
     constexpr int NB = L::NB, QS = L::kQS;
     constexpr int kTmemCols = 512;
-    constexpr int kAccO = 2 * kKP;  // O buffer g at kAccO + g * NB
+    constexpr int kGC = kKP + 2 * NB;  // TMEM columns per group
+    static_assert(kNG * kGC <= kTmemCols, "TMEM budget");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qst = smem + L::kQst, *xg = smem + L::kXG, *coef = smem + L::kCoef, *bop = smem + L::kB;
+    uint8_t *qst = smem + L::kQst, *stg = smem + L::kStage, *coef = smem + L::kCoef, *bop = smem + L::kB;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + 2, *gready = sfull + 2,
-             *ofull = gready + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ofull + 2);
-    int *abort_flag = reinterpret_cast<int *>(ofull + 3);
+    uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + kNG,
+             *gready = sfull + kNG, *ofull = gready + kNG;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ofull + kNG);
+    int *abort_flag = reinterpret_cast<int *>(ofull + kNG + 1);
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1094,7 +1246,7 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNG; ++i) {
             mbar_init(&xready[i], 4);
             mbar_init(&sfull[i], 1);
             mbar_init(&gready[i], 4);
@@ -1103,12 +1255,14 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t idesc_o = idesc_bf16(kTile, NB, false, false);
+    constexpr uint32_t i160 = idesc_bf16(kTile, 2 * NB, false, false);
+    constexpr uint32_t i80 = idesc_bf16(kTile, NB, false, false);
 
     int rbase = 0;
     for (int g = g0; g < gend;) {
@@ -1116,10 +1270,10 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
         __syncthreads();
-        build_coef_smem(mu, sigma2, log_pi, h, K, coef, status, tid, kThreads2);
+        copy_coef(coef_img, h, coef, tid, kThreadsG);
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(mem_img + (size_t)bh * mem_img_stride);
-            for (int i = tid; i < 2 * NB * 128 / 16; i += kThreads2) reinterpret_cast<uint4 *>(bop)[i] = __ldcg(src + i);
+            for (int i = tid; i < 2 * NB * 128 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(bop)[i] = __ldcg(src + i);
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -1134,17 +1288,17 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
                 }
         } else if (warp == 1) {
             if (lane == 0) {
-                // Poll both queues so that neither kind of MMA waits behind the other.
+                const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024), dc0 = sdesc_sw128(smem_u32(coef), 16, 1024);
+                const uint64_t db0 = sdesc_sw128(smem_u32(bop), 16, 1024);
                 int ns = 0, nr = 0;
                 Stall st;
                 while (nr < n) {
                     bool prog = false;
                     if (ns < n) {
-                        const int r = rbase + ns, gb = r & 1, s = r % QS;
-                        if (mbar_test(&xready[gb], (r >> 1) & 1)) {
+                        const int r = rbase + ns, gb = r % kNG, s = r % QS;
+                        if (mbar_test(&xready[gb], (r / kNG) & 1)) {
                             tc_fence_after();
-                            issue_scores(tmem + gb * kKP, qst + s * kTileBytes, xg + gb * 2 * kTileBytes,
-                                         xg + gb * 2 * kTileBytes + kTileBytes, coef);
+                            issue_scores_tA(tmem + gb * kGC + kKP, tmem + gb * kGC, dadd(dq0, s * kTileBytes), dc0);
                             umma_commit(&sfull[gb]);
                             umma_commit(&qempty[s]);
                             ++ns;
@@ -1152,20 +1306,14 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
                         }
                     }
                     if (nr < ns) {
-                        const int r = rbase + nr, gb = r & 1;
-                        if (mbar_test(&gready[gb], (r >> 1) & 1)) {
+                        const int r = rbase + nr, gb = r % kNG;
+                        if (mbar_test(&gready[gb], (r / kNG) & 1)) {
                             tc_fence_after();
-                            const uint32_t sg = smem_u32(xg + gb * 2 * kTileBytes), sb = smem_u32(bop);
-                            const uint32_t d = tmem + kAccO + gb * NB;
+                            const uint32_t d = tmem + gb * kGC + kKP, a = tmem + gb * kGC;
 #pragma unroll
                             for (int kk = 0; kk < kKP / 16; ++kk) {
-                                const uint64_t ahi = sdesc_sw128(sg + kk * 32, 16, kGS),
-                                               alo = sdesc_sw128(sg + 1024 + kk * 32, 16, kGS);
-                                const uint64_t bhi = sdesc_sw128(sb + kk * 32, 16, 1024),
-                                               blo = sdesc_sw128(sb + NB * 128 + kk * 32, 16, 1024);
-                                umma_bf16(d, ahi, bhi, idesc_o, kk > 0 ? 1u : 0u);
-                                umma_bf16(d, alo, bhi, idesc_o, 1u);
-                                umma_bf16(d, ahi, blo, idesc_o, 1u);
+                                umma_bf16_tA(d, a + kk * 8, dadd(db0, kk * 32), i160, kk > 0 ? 1u : 0u);
+                                umma_bf16_tA(d, a + 32 + kk * 8, dadd(db0, kk * 32), i80, 1u);
                             }
                             umma_commit(&ofull[gb]);
                             ++nr;
@@ -1182,59 +1330,423 @@ __global__ void __launch_bounds__(kThreads2, 1) tc_read2_kernel(
             const int grp = (warp - 2) >> 2;
             const int row = epi_row(warp, lane);
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-            for (int i = ((rbase & 1) == grp ? 0 : 1); i < n; i += 2) {
+            uint8_t *stage = stg + (grp * 4 + (warp & 3)) * 8192;
+            const uint32_t gbase = tmem + lane_base + grp * kGC;
+            for (int i = (grp - rbase % kNG + kNG) % kNG; i < n; i += kNG) {
                 const int r = rbase + i, s = r % QS;
-                uint8_t *gbuf = xg + grp * 2 * kTileBytes;
                 if (!wait_or_abort(&qfull[s], (r / QS) & 1, status, abort_flag)) break;
-                prep_x2(qst + s * kTileBytes, gbuf, gbuf + kTileBytes, kTileBytes, tid - 64 - 128 * grp, 128);
-                fence_proxy_async_smem();
+                prep_x2_row_tmem(qst + s * kTileBytes, row, gbase);
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xready[grp]);
-                if (!wait_or_abort(&sfull[grp], (r >> 1) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&sfull[grp], (r / kNG) & 1, status, abort_flag)) break;
                 tc_fence_after();
                 float rs;
                 {
                     float e[kKP];
-                    rs = score_row_exp(tmem + lane_base + grp * kKP, cvec, e);
-                    tc_fence_before();
-                    store_gamma_row(gbuf, row, e, 1.0f);
+                    rs = score_row_exp128(gbase + kKP, cvec, e);
+                    uint32_t wh[32], wl[32];
+                    split_row(e, 1.0f, wh, wl);
+                    tmem_st32(gbase, wh);
+                    tmem_st32(gbase + 32, wl);
+                    tmem_wait_st();
                 }
-                fence_proxy_async_smem();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&gready[grp]);
-                if (!wait_or_abort(&ofull[grp], (r >> 1) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&ofull[grp], (r / kNG) & 1, status, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t ob = tmem + lane_base + kAccO + grp * NB;
-                uint32_t dz[16];
-                tmem_ld16(ob + D_V, dz);
-                tmem_wait_ld();
-                const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rs);
-                const int tok = (t0 + i) * kTile + row;
-                const size_t orow = (size_t)bh * N + tok;
-#pragma unroll
-                for (int cb = 0; cb < D_V / 32; ++cb) {
-                    uint32_t v[32];
-                    tmem_ld32(ob + cb * 32, v);
+                const uint32_t ob = gbase + kKP;
+                float o[64];
+                {
+                    uint32_t d0[16], d1[16], a0[32], a1[32];
+                    tmem_ld16(ob + 64, d0);
+                    tmem_ld16(ob + 64 + NB, d1);
+                    tmem_ld32(ob, a0);
+                    tmem_ld32(ob + NB, a1);
                     tmem_wait_ld();
-                    if (tok < N) {
-                        if (o_bf16) {
-                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + orow * D_V + cb * 32);
+                    const float inv = 1.0f / (__uint_as_float(d0[0]) + __uint_as_float(d1[0]) + eps * rs);
+                    const float2 iv = make_float2(inv, inv);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                o[q] = make_uint4(pack_bf2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                                                  pack_bf2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                                                  pack_bf2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                                                  pack_bf2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
-                        } else {
-                            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(O) + orow * D_V + cb * 32);
+                    for (int q = 0; q < 16; ++q) {
+                        const float2 t = f2_mul(f2_add(make_float2(__uint_as_float(a0[2 * q]), __uint_as_float(a0[2 * q + 1])),
+                                                       make_float2(__uint_as_float(a1[2 * q]), __uint_as_float(a1[2 * q + 1]))), iv);
+                        o[2 * q] = t.x;
+                        o[2 * q + 1] = t.y;
+                    }
+                    tmem_ld32(ob + 32, a0);
+                    tmem_ld32(ob + NB + 32, a1);
+                    tmem_wait_ld();
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                o[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                                   __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
-                        }
+                    for (int q = 0; q < 16; ++q) {
+                        const float2 t = f2_mul(f2_add(make_float2(__uint_as_float(a0[2 * q]), __uint_as_float(a0[2 * q + 1])),
+                                                       make_float2(__uint_as_float(a1[2 * q]), __uint_as_float(a1[2 * q + 1]))), iv);
+                        o[32 + 2 * q] = t.x;
+                        o[32 + 2 * q + 1] = t.y;
                     }
                 }
                 tc_fence_before();
+                stage_and_store_rows(stage, o, lane, lane, &tmO, o_bf16, (t0 + i) * kTile + 32 * (warp & 3), bh);
+            }
+            if (lane == 0) bulk_wait0();
+        }
+        rbase += n;
+        g += n;
+        __syncthreads();
+        if (aborted(abort_flag)) break;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ causal, persistent
+//
+// Causal GMA ([GMA, Eq. (8b)]) over each job's tiles (chunks of C = 128
+// tokens), d_r = d_v = 64, K <= 64.  With (S, Z) the prefix memory before the
+// chunk, r_i the un-normalised query row sum and P = mask_{j<=i}(Gamma^Q_c Gamma^K_c^T):
+//   O_i = (gQ_i [S | Z] + sum_j P_ij [V_j | 1]) split as [num | den],  O_i = num / (den + eps r_i),
+// then (S, Z) += Gamma^K_c^T [V_c | 1].  The job's starting prefix is the
+// exclusive prefix left in the partials by tc_write2_kernel (mode 1).
+//
+// Warps: 0 TMA, 1 MMA issuer, 2..5 query group (x^2, softmax, P split,
+// outputs), 6..9 key group (x^2, softmax, Gamma^K, carry of the state).
+// One chunk is in flight; the query and key sides run in parallel.
+//
+// TMEM (512 columns):
+//   [0, 64)    x^2 of Q -> Gamma^Q hi | lo -> P hi   (MMA A operands)
+//   [64, 128)  x^2 of K ->                    P lo
+//   [128, 256) scores Q (N = 128) \  P = [gQhi (gKhi|gKlo)^T] + gQlo gKhi^T  (N = 256)
+//   [256, 384) scores K (N = 128) /  state increment U = gK^T [V | 1] at [128, 208)
+//   [384, 464) [num | den] (N = 80)
+// MMAs per chunk: scores 12 + 12, P 8, state read 12, P [V|1] 16, U 8.
+struct Causal2Smem {
+    static constexpr int W = 64 + 1;
+    static constexpr int kQK = 0;                          // Q tile | K tile (one stage)
+    static constexpr int kV = kQK + 2 * kTileBytes;        // V tile | ones chunk
+    static constexpr int kGK = kV + 2 * kTileBytes;        // Gamma^K: hi [128 x 128 B] | lo
+    static constexpr int kSop = kGK + 2 * kTileBytes;      // state operand, MN-major: hi (2 x 8 KB) | lo
+    static constexpr int kCoef = kSop + 4 * 8192;
+    static constexpr int kS = kCoef + ((kCoefBytes + 1023) & ~1023);  // fp32 state [64][W]
+    static constexpr int kX = kGK;  // carry exchange [64][W] fp32, over Gamma^K (idle during the carry)
+    static constexpr int kStage = kS + ((kKP * W * 4 + 1023) & ~1023);  // output staging 4 x 8 KB
+    static constexpr int kBars = kStage + 4 * 8192;
+    static constexpr int kBytes = kBars + 256;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+// One state-operand row: component k, 64 values of S plus Z, as bf16 hi / lo,
+// MN-major SW128 (row = component; chunk 0 = columns 0..63, chunk 1 at +8 KB
+// holds Z in column 64 and zeros).
+__device__ __forceinline__ void store_state_row(uint8_t *sop, int k, const float *srow) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float v0 = srow[8 * c + 2 * q], v1 = srow[8 * c + 2 * q + 1];
+            wh[q] = pack_bf2(v0, v1);
+            wl[q] = pack_bf2(v0 - bf_lo(wh[q]), v1 - bf_hi(wh[q]));
+        }
+        const uint32_t off = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((c ^ (k & 7)) << 4));
+        *reinterpret_cast<uint4 *>(sop + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(sop + 16384 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+    const float z = srow[64];
+    const uint32_t zh = pack_bf2(z, 0.f), zl = pack_bf2(z - bf_lo(zh), 0.f);
+    const uint32_t off0 = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((0 ^ (k & 7)) << 4));
+    const uint32_t off1 = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((1 ^ (k & 7)) << 4));
+    *reinterpret_cast<uint4 *>(sop + 8192 + off0) = make_uint4(zh, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(sop + 8192 + off1) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off0) = make_uint4(zl, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off1) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+    const uint8_t *__restrict__ coef_img, const float *__restrict__ prefix, int H, int N, Part P, float eps,
+    int o_bf16, unsigned *status) {
+    using L = Causal2Smem;
+    constexpr int W = L::W;
+    constexpr int kTmemCols = 512;
+    constexpr int kXQ = 0, kXK = 64, kSQ = 128, kSK = 256, kPD = 128, kU = 128, kO = 384;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qk = smem + L::kQK, *vt = smem + L::kV, *gk = smem + L::kGK, *sop = smem + L::kSop,
+            *coef = smem + L::kCoef;
+    float *S = reinterpret_cast<float *>(smem + L::kS), *X = reinterpret_cast<float *>(smem + L::kX);
+    uint8_t *stg = smem + L::kStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *qkfull = bars + 0, *qkempty = bars + 1, *vfull = bars + 2, *vempty = bars + 3, *xq = bars + 4,
+             *xk = bars + 5, *sq = bars + 6, *sk = bars + 7, *gq = bars + 8, *gkr = bars + 9, *sready = bars + 10,
+             *pfull = bars + 11, *pready = bars + 12, *ofull = bars + 13, *ufull = bars + 14;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+    int *abort_flag = reinterpret_cast<int *>(bars + 16);
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    if (failed(status) || g0 >= gend) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(qkfull, 1); mbar_init(qkempty, 1); mbar_init(vfull, 1); mbar_init(vempty, 1);
+        mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
+        mbar_init(gq, 4); mbar_init(gkr, 4); mbar_init(sready, 4); mbar_init(pfull, 1);
+        mbar_init(pready, 4); mbar_init(ofull, 1); mbar_init(ufull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
+    }
+    {   // constant ones chunk of the V stage; zero state operand (its padding must be 0)
+        const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        for (int i = tid; i < kTileBytes / 16; i += kThreadsG) reinterpret_cast<uint4 *>(vt + kTileBytes)[i] = one4;
+        for (int i = tid; i < 4 * 8192 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(sop)[i] = make_uint4(0, 0, 0, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int rbase = 0;
+    for (int g = g0; g < gend;) {
+        const int bh = g / P.ntiles, t0 = g % P.ntiles;
+        const int n = min(P.ntiles - t0, gend - g);
+        const int h = bh % H;
+        __syncthreads();
+        copy_coef(coef_img, h, coef, tid, kThreadsG);
+        {
+            const float *pre = prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W;
+            for (int e = tid; e < kKP * W; e += kThreadsG) S[e] = __ldcg(pre + e);
+        }
+        __syncthreads();
+        if (warp >= 8) {  // key-group warps holding component rows 0..63: initial state operand
+            const int k = epi_row(warp, lane);
+            store_state_row(sop, k, S + k * W);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (warp >= 6 && lane == 0) mbar_arrive(sready);  // state for the job's first chunk
+
+        if (warp == 0) {
+            if (lane == 0)
+                for (int i = 0; i < n; ++i) {
+                    const int r = rbase + i;
+                    if (!wait_or_abort(qkempty, (r & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(qkfull, 2 * kTileBytes);
+                    tma_load_3d(qk, &tmQ, 0, (t0 + i) * kTile, bh, qkfull);
+                    tma_load_3d(qk + kTileBytes, &tmK, 0, (t0 + i) * kTile, bh, qkfull);
+                    if (!wait_or_abort(vempty, (r & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(vfull, kTileBytes);
+                    tma_load_3d(vt, &tmV, 0, (t0 + i) * kTile, bh, vfull);
+                }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                const uint64_t dq = sdesc_sw128(smem_u32(qk), 16, 1024), dkx = sdesc_sw128(smem_u32(qk + kTileBytes), 16, 1024);
+                const uint64_t dc = sdesc_sw128(smem_u32(coef), 16, 1024);
+                const uint64_t dgk = sdesc_sw128(smem_u32(gk), 16, 1024);               // K-major Gamma^K (N = 128 / 256)
+                const uint64_t dgt = sdesc_sw128(smem_u32(gk), kTileBytes, 1024);       // MN-major Gamma^K^T (M = 128)
+                const uint64_t dso = sdesc_sw128(smem_u32(sop), 8192, 1024);            // MN-major state operand
+                const uint64_t dv = sdesc_sw128(smem_u32(vt), kTileBytes, 1024);        // MN-major [V | 1]
+                constexpr uint32_t i256 = idesc_bf16(kTile, 256, false, false), i128 = idesc_bf16(kTile, 128, false, false);
+                constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
+                for (int i = 0; i < n; ++i) {
+                    const int r = rbase + i, ph = r & 1;
+                    // scores of the chunk (the Q scores overwrite the previous state increment,
+                    // so they wait for the carry that read it)
+                    if (!wait_or_abort(sready, ph, status, abort_flag)) break;
+                    if (!wait_or_abort(xq, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    issue_scores_tA(tmem + kSQ, tmem + kXQ, dq, dc);
+                    umma_commit(sq);
+                    if (!wait_or_abort(xk, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    issue_scores_tA(tmem + kSK, tmem + kXK, dkx, dc);
+                    umma_commit(sk);
+                    umma_commit(qkempty);
+                    // P = gQhi [gKhi | gKlo]^T + gQlo gKhi^T, and the read of the carried state
+                    if (!wait_or_abort(gq, ph, status, abort_flag)) break;
+                    if (!wait_or_abort(gkr, ph, status, abort_flag)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kKP / 16; ++kk) {
+                        umma_bf16_tA(tmem + kPD, tmem + kXQ + kk * 8, dadd(dgk, kk * 32), i256, kk > 0 ? 1u : 0u);
+                        umma_bf16_tA(tmem + kPD, tmem + kXQ + 32 + kk * 8, dadd(dgk, kk * 32), i128, 1u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kKP / 16; ++kk) {
+                        const uint64_t bh_ = dadd(dso, kk * 2048), bl_ = dadd(dso, 16384 + kk * 2048);
+                        umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bh_, i80s, kk > 0 ? 1u : 0u);
+                        umma_bf16_tA(tmem + kO, tmem + kXQ + 32 + kk * 8, bh_, i80s, 1u);
+                        umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bl_, i80s, 1u);
+                    }
+                    umma_commit(pfull);
+                    // [num | den] += P [V | 1];  U = [gK_hi ; gK_lo]^T [V | 1]
+                    if (!wait_or_abort(pready, ph, status, abort_flag)) break;
+                    if (!wait_or_abort(vfull, ph, status, abort_flag)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t bv = dadd(dv, kk * 2048);
+                        umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bv, i80s, 1u);
+                        umma_bf16_tA(tmem + kO, tmem + kXK + kk * 8, bv, i80s, 1u);
+                    }
+                    umma_commit(ofull);
+                    if (i + 1 < n) {
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(ufull);
+                    umma_commit(vempty);
+                }
+            }
+        } else if (warp < 6) {
+            // ---------------- query group
+            const int row = epi_row(warp, lane);
+            const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            uint8_t *stage = stg + (warp & 3) * 8192;
+            for (int i = 0; i < n; ++i) {
+                const int r = rbase + i, ph = r & 1;
+                const int tok = (t0 + i) * kTile + row;
+                if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
+                prep_x2_row_tmem(qk, row, tmem + lb + kXQ);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xq);
+                if (!wait_or_abort(sq, ph, status, abort_flag)) break;
+                tc_fence_after();
+                float rq;
+                {
+                    float e[kKP];
+                    rq = score_row_exp128(tmem + lb + kSQ, cvec, e);
+                    uint32_t wh[32], wl[32];
+                    split_row(e, 1.0f, wh, wl);
+                    tmem_st32(tmem + lb + kXQ, wh);
+                    tmem_st32(tmem + lb + kXQ + 32, wl);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gq);
+                // masked intra-chunk affinity -> P hi | lo as the A operand of P [V | 1]
+                if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {  // keys 32 cb .. 32 cb + 31
+                    uint32_t p0[32], p1[32];
+                    tmem_ld32(tmem + lb + kPD + cb * 32, p0);
+                    tmem_ld32(tmem + lb + kPD + 128 + cb * 32, p1);
+                    tmem_wait_ld();
+                    uint32_t wh[16], wl[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int j = cb * 32 + 2 * q;
+                        const float2 pv = f2_add(make_float2(__uint_as_float(p0[2 * q]), __uint_as_float(p0[2 * q + 1])),
+                                                 make_float2(__uint_as_float(p1[2 * q]), __uint_as_float(p1[2 * q + 1])));
+                        const float a = j <= row ? pv.x : 0.f, b = j + 1 <= row ? pv.y : 0.f;
+                        wh[q] = pack_bf2(a, b);
+                        wl[q] = pack_bf2(a - bf_lo(wh[q]), b - bf_hi(wh[q]));
+                    }
+                    tmem_st16(tmem + lb + kXQ + cb * 16, wh);
+                    tmem_st16(tmem + lb + kXK + cb * 16, wl);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pready);
+                // outputs
+                if (!wait_or_abort(ofull, ph, status, abort_flag)) break;
+                tc_fence_after();
+                float o[64];
+                {
+                    uint32_t a0[32], a1[32], dz[16];
+                    tmem_ld32(tmem + lb + kO, a0);
+                    tmem_ld32(tmem + lb + kO + 32, a1);
+                    tmem_ld16(tmem + lb + kO + 64, dz);
+                    tmem_wait_ld();
+                    const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rq);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        o[q] = __uint_as_float(a0[q]) * inv;
+                        o[32 + q] = __uint_as_float(a1[q]) * inv;
+                    }
+                }
+                tc_fence_before();
+                (void)tok;
+                stage_and_store_rows(stage, o, lane, lane, &tmO, o_bf16, (t0 + i) * kTile + 32 * (warp & 3), bh);
+            }
+            if (lane == 0) bulk_wait0();
+        } else {
+            // ---------------- key group
+            const int row = epi_row(warp, lane);
+            const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            for (int i = 0; i < n; ++i) {
+                const int r = rbase + i, ph = r & 1;
+                if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
+                prep_x2_row_tmem(qk + kTileBytes, row, tmem + lb + kXK);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xk);
+                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
+                tc_fence_after();
+                {
+                    float e[kKP];
+                    const float rk = score_row_exp128(tmem + lb + kSK, cvec, e);
+                    tc_fence_before();
+                    const int tok = (t0 + i) * kTile + row;
+                    uint32_t wh[32], wl[32];
+                    split_row(e, tok < N ? 1.0f / rk : 0.0f, wh, wl);
+                    // Gamma^K rows: hi block then lo block, 128-byte rows, 8-row groups of 1 KB
+                    uint8_t *hi = gk + row * 128, *lo = gk + kTileBytes + row * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint32_t sw = (uint32_t)((cc ^ (row & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[4 * cc], wh[4 * cc + 1], wh[4 * cc + 2], wh[4 * cc + 3]);
+                        *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[4 * cc], wl[4 * cc + 1], wl[4 * cc + 2], wl[4 * cc + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gkr);
+                // carry: S += U_hi + U_lo, then the state operand of the next chunk
+                if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
+                if (i + 1 < n) {
+                    tc_fence_after();
+                    float u[W];
+                    {
+                        uint32_t a0[32], a1[32], z[16];
+                        tmem_ld32(tmem + lb + kU, a0);
+                        tmem_ld32(tmem + lb + kU + 32, a1);
+                        tmem_ld16(tmem + lb + kU + 64, z);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            u[q] = __uint_as_float(a0[q]);
+                            u[32 + q] = __uint_as_float(a1[q]);
+                        }
+                        u[64] = __uint_as_float(z[0]);
+                    }
+                    tc_fence_before();
+                    if (row >= kKP)
+#pragma unroll
+                        for (int q = 0; q < W; ++q) X[(row - kKP) * W + q] = u[q];
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (row < kKP) {
+                        float *sr = S + row * W;
+#pragma unroll
+                        for (int q = 0; q < W; ++q) sr[q] += u[q] + X[row * W + q];
+                        store_state_row(sop, row, sr);
+                    }
+                    fence_proxy_async_smem();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (lane == 0) mbar_arrive(sready);
+                }
             }
         }
         rbase += n;
@@ -1275,6 +1787,21 @@ bool make_map(CUtensorMap *map, const void *base, int BH, int N, int d) {
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// O [BH][N][64] (fp32 or bf16) for TMA stores of 32-row boxes, 128-byte swizzle.
+bool make_out_map(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)64 * es, (cuuint64_t)N * 64 * es};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1331,7 +1858,7 @@ int num_sms() {
 struct TcLayout2 {
     Part P;
     int nctas = 0;
-    size_t counters = 0, part = 0, mem = 0, mem_stride = 0, total = 0, reset_bytes = 0;
+    size_t counters = 0, coef = 0, part = 0, mem = 0, mem_stride = 0, total = 0, reset_bytes = 0;
 };
 
 TcLayout2 tc_layout2(const Problem &p, int splits) {
@@ -1347,6 +1874,8 @@ TcLayout2 tc_layout2(const Problem &p, int splits) {
     L.counters = off;
     off = align256(off + sizeof(unsigned) * (size_t)p.BH());
     L.reset_bytes = off;
+    L.coef = off;
+    off = align256(off + kCoefStride * p.H);
     L.part = off;
     off = align256(off + sizeof(float) * (size_t)L.nctas * L.P.slots * kKP * (p.d_v + 1));
     L.mem_stride = ((size_t)2 * (p.d_v + 16) * 128 + 1023) & ~size_t(1023);
@@ -1356,58 +1885,56 @@ TcLayout2 tc_layout2(const Problem &p, int splits) {
     return L;
 }
 
-template <int D_V>
 cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
     unsigned *status = reinterpret_cast<unsigned *>(ws);
     unsigned *counters = reinterpret_cast<unsigned *>(ws + L.counters);
     float *part = reinterpret_cast<float *>(ws + L.part);
     uint8_t *mem = ws + L.mem;
-    CUtensorMap tq, tk, tv;
+    uint8_t *coef = ws + L.coef;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
-        !make_map(&tv, p.V, p.BH(), p.N, D_V))
+        !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map(&to, p.O, p.BH(), p.N, p.o_bf16))
         return cudaErrorInvalidValue;
     clk.mark();
     GMA_TRY(cudaMemsetAsync(ws, 0, L.reset_bytes, s));
-    clk.mark();
-    GMA_TRY(set_smem(tc_write2_kernel<D_V>, Write2Smem<D_V>::kAlloc));
-    tc_write2_kernel<D_V><<<L.nctas, kThreads2, Write2Smem<D_V>::kAlloc, s>>>(
-        tk, tv, p.mu, p.sigma2, p.log_pi, p.K, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
+    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    GMA_TRY(set_smem(tc_read2_kernel<D_V>, Read2Smem<D_V>::kAlloc));
-    tc_read2_kernel<D_V><<<L.nctas, kThreads2, Read2Smem<D_V>::kAlloc, s>>>(
-        tq, p.mu, p.sigma2, p.log_pi, p.K, p.H, p.N, L.P, mem, L.mem_stride, p.eps, p.O, p.o_bf16 ? 1 : 0, status);
+    GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
+    tc_write2_kernel<<<L.nctas, kThreadsG, Write2Smem::kAlloc, s>>>(
+        tk, tv, coef, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    GMA_TRY(set_smem(tc_read2_kernel, Read2Smem::kAlloc));
+    tc_read2_kernel<<<L.nctas, kThreadsG, Read2Smem::kAlloc, s>>>(
+        tq, to, coef, p.H, p.N, L.P, mem, L.mem_stride, p.eps, p.o_bf16 ? 1 : 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     return cudaSuccess;
 }
 
-cudaError_t run_causal(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
-    constexpr int D_V = CausalSmem::D_V;
+cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
     unsigned *status = reinterpret_cast<unsigned *>(ws);
-    uint8_t *coef = ws + L.coef;
+    unsigned *counters = reinterpret_cast<unsigned *>(ws + L.counters);
     float *part = reinterpret_cast<float *>(ws + L.part);
-    CUtensorMap tq, tk, tv;
+    uint8_t *coef = ws + L.coef;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
-        !make_map(&tv, p.V, p.BH(), p.N, D_V))
+        !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map(&to, p.O, p.BH(), p.N, p.o_bf16))
         return cudaErrorInvalidValue;
     clk.mark();
-    GMA_TRY(cudaMemsetAsync(status, 0, sizeof(unsigned), s));
-    coef_prep_tc_kernel<<<p.H, 256, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
+    GMA_TRY(cudaMemsetAsync(ws, 0, L.reset_bytes, s));
+    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    GMA_TRY(set_smem(tc_write_kernel<D_V>, WriteSmem<D_V>::kAlloc));
-    tc_write_kernel<D_V><<<dim3(L.nsplit, p.BH()), 128, WriteSmem<D_V>::kAlloc, s>>>(
-        tk, tv, coef, p.H, p.N, L.tiles_per_split, L.nsplit, part, status);
+    GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
+    tc_write2_kernel<<<L.nctas, kThreadsG, Write2Smem::kAlloc, s>>>(
+        tk, tv, coef, p.H, p.N, L.P, part, counters, nullptr, 0, 1, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    const int E = kKP * (D_V + 1);
-    scan_segments_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(part, L.nsplit, E, status);
-    GMA_TRY(cudaGetLastError());
-    clk.mark();
-    GMA_TRY(set_smem(tc_causal_kernel, CausalSmem::kAlloc));
-    tc_causal_kernel<<<dim3(L.nsplit, p.BH()), 128, CausalSmem::kAlloc, s>>>(
-        tq, tk, tv, coef, part, p.H, p.N, L.tiles_per_split, L.nsplit, p.eps, p.O, p.o_bf16 ? 1 : 0, status);
+    GMA_TRY(set_smem(tc_causal2_kernel, Causal2Smem::kAlloc));
+    tc_causal2_kernel<<<L.nctas, kThreadsG, Causal2Smem::kAlloc, s>>>(
+        tq, tk, tv, to, coef, part, p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     return cudaSuccess;
@@ -1417,30 +1944,30 @@ cudaError_t run_causal(const Problem &p, const TcLayout &L, uint8_t *ws, cudaStr
 
 const char *const kTcStages[3][8] = {
     {nullptr},
-    {"reset", "tc_write", "tc_read", nullptr},
-    {"prep", "tc_aggregate", "scan", "tc_causal", nullptr},
+    {"prep", "tc_write", "tc_read", nullptr},
+    {"prep", "tc_aggregate", "tc_causal", nullptr},
 };
 
 bool tc_supported(const Problem &p, int causal) {
     if (p.dtype != GMA_BF16 || p.d_r != kDR || p.K > kKP) return false;
-    if (causal == 0) return p.d_v == 64 || p.d_v == 128;
-    return causal == 1 && p.d_v == CausalSmem::D_V;
+    if (causal == 0) return p.d_v == 64;
+    return causal == 1 && p.d_v == 64;
 }
 
 size_t tc_workspace(const Problem &p, int causal, int splits) {
-    return causal ? tc_layout(p, causal, splits).total : tc_layout2(p, splits).total;
+    (void)causal;
+    return tc_layout2(p, splits).total;
 }
 
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
     TcLayout2 L = tc_layout2(p, splits);
     uint8_t *w = static_cast<uint8_t *>(ws);
-    if (p.d_v == 64) return run_bidir2<64>(p, L, w, s, clk);
-    return run_bidir2<128>(p, L, w, s, clk);
+    return run_bidir2(p, L, w, s, clk);
 }
 
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
-    TcLayout L = tc_layout(p, 1, splits);
-    return run_causal(p, L, static_cast<uint8_t *>(ws), s, clk);
+    TcLayout2 L = tc_layout2(p, splits);
+    return run_causal2(p, L, static_cast<uint8_t *>(ws), s, clk);
 }
 
 }  // namespace gma

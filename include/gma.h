@@ -30,7 +30,7 @@
  *   returned by gma_last_device_status() -- or directly, when
  *   options->sync_status is set.
  * - Inputs must not overlap O / Gamma or the workspace.  Q_X, K_X, V_X and O
- *   must start on a 16-byte boundary, the workspace on a 256-byte boundary
+ *   (and mu, sigma2) must start on a 16-byte boundary, the workspace on a 256-byte boundary
  *   (GMA_ERR_INVALID_ARG otherwise).
  * - Results are deterministic: the same inputs, sizes and options give
  *   bitwise-identical outputs (fixed-order reductions, no atomics on data).
