@@ -1,5 +1,5 @@
 // gma_tc.cu -- tcgen05 tensor-core kernels for the GMA forward pass (bf16
-// inputs, d_r = 64, K <= 64, d_v in {64, 128}).
+// inputs, d_r = d_v = 64, K <= 64).
 //
 // Responsibilities ([GMA, Eqs. (2)-(3)]) are computed as a GEMM on the
 // expanded quadratic,
@@ -10,10 +10,15 @@
 // the five products x2hi*ahi + x2hi*alo + x2lo*ahi + x*bhi + x*blo carry
 // ~16 significant bits (x is bf16, so x^2 is exactly x2hi + x2lo).  The
 // softmax over k runs in fp32 on the TMEM accumulator rows.  Gamma is split
-// into bf16 hi + lo again for the value contractions:
-//   write (Eqs. (5)-(6)):  [Vt | Z] += [Ghi ; Glo]^T [V | 1]     (per key tile)
-//   read  (Eq. (7)):       [num | den] = Ghi [Vhi|Zhi] + Glo [Vhi|Zhi] + Ghi [Vlo|Zlo]
-// and O = num / (den + eps * r) with r the un-normalised query row sum.
+// into bf16 hi + lo again for the value contractions (write: Gamma^K^T [V | 1];
+// read: Gamma^Q [Vt | Z] with the memory split too; causal: the masked
+// intra-chunk Gamma^Q Gamma^K^T times [V | 1] plus Gamma^Q times the carried
+// prefix).  O = num / (den + eps * r) with r the un-normalised query row sum.
+//
+// Kernels:  coef_prep_tc_kernel (per-head split coefficients), then the
+// persistent, warp-specialised tc_write2_kernel (key side: latent memory per
+// job, combined per head by the last job), tc_read2_kernel (bidirectional
+// query side) and tc_causal2_kernel (causal chunked scan).
 //
 // Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
 // Probabilistic Latent Routing" (arXiv 2606.18283), cited [GMA, ...].
@@ -78,573 +83,10 @@ __global__ void coef_prep_tc_kernel(const float *__restrict__ mu, const float *_
 // build each descriptor once and advance it with one add per MMA.
 __device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
 
-// x^2 split: for every bf16 x of a tile, x2hi = rn(x*x), x2lo = x*x - x2hi
-// (exact, since x*x has at most 16 significant bits).  Position-preserving on
-// the swizzled tile, so the outputs share the tile's layout.
-__device__ __forceinline__ void prep_x2(const uint8_t *x, uint8_t *x2h, uint8_t *x2l, int bytes, int tid,
-                                        int nthreads) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(x);
-    uint4 *dh = reinterpret_cast<uint4 *>(x2h);
-    uint4 *dl = reinterpret_cast<uint4 *>(x2l);
-    for (int i = tid; i < bytes / 16; i += nthreads) {
-        const uint4 v = src[i];
-        uint4 h, l;
-        h.x = bf2_fma(v.x, v.x, 0x80008000u); l.x = bf2_fma(v.x, v.x, h.x ^ 0x80008000u);
-        h.y = bf2_fma(v.y, v.y, 0x80008000u); l.y = bf2_fma(v.y, v.y, h.y ^ 0x80008000u);
-        h.z = bf2_fma(v.z, v.z, 0x80008000u); l.z = bf2_fma(v.z, v.z, h.z ^ 0x80008000u);
-        h.w = bf2_fma(v.w, v.w, 0x80008000u); l.w = bf2_fma(v.w, v.w, h.w ^ 0x80008000u);
-        dh[i] = h;
-        dl[i] = l;
-    }
-}
-
-// The 20 score MMAs of one 128-token tile: D[128 x KP] = x2hi*ahi + x2hi*alo +
-// x2lo*ahi + x*bhi + x*blo, each over d_r = 64 in four K-steps of 16.
-__device__ __forceinline__ void issue_scores(uint32_t d_tmem, const uint8_t *x, const uint8_t *x2h,
-                                             const uint8_t *x2l, const uint8_t *coef) {
-    constexpr uint32_t idesc = idesc_bf16(kTile, kKP, false, false);
-    const uint64_t dx = sdesc_sw128(smem_u32(x), 16, 1024), dh = sdesc_sw128(smem_u32(x2h), 16, 1024),
-                   dl = sdesc_sw128(smem_u32(x2l), 16, 1024), dc = sdesc_sw128(smem_u32(coef), 16, 1024);
-#pragma unroll
-    for (int kk = 0; kk < kDR / 16; ++kk) {
-        const uint32_t o = kk * 32;
-        umma_bf16(d_tmem, dadd(dh, o), dadd(dc, o), idesc, kk > 0 ? 1u : 0u);
-        umma_bf16(d_tmem, dadd(dh, o), dadd(dc, kCoefMatBytes + o), idesc, 1u);
-        umma_bf16(d_tmem, dadd(dl, o), dadd(dc, o), idesc, 1u);
-        umma_bf16(d_tmem, dadd(dx, o), dadd(dc, 2 * kCoefMatBytes + o), idesc, 1u);
-        umma_bf16(d_tmem, dadd(dx, o), dadd(dc, 3 * kCoefMatBytes + o), idesc, 1u);
-    }
-}
-
-// Loads this thread's score row (KP columns) and turns it into exponentials
-// e_k = 2^(s_k + c_k - max) (un-normalised responsibilities, max e = 1).
-// Returns the row sum r.
-__device__ __forceinline__ float score_row_exp(uint32_t taddr, const float *cvec, float (&e)[kKP]) {
-    uint32_t r0[32], r1[32];
-    tmem_ld32(taddr, r0);
-    tmem_ld32(taddr + 32, r1);
-    tmem_wait_ld();
-    float m = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        e[k] = __uint_as_float(r0[k]) + cvec[k];
-        e[k + 32] = __uint_as_float(r1[k]) + cvec[k + 32];
-        m = fmaxf(m, fmaxf(e[k], e[k + 32]));
-    }
-    float r = 0.f;
-#pragma unroll
-    for (int k = 0; k < kKP; ++k) {
-        e[k] = ex2(e[k] - m);
-        r += e[k];
-    }
-    return r;
-}
-
-// Writes one responsibility row (scaled by `scale`) as bf16 hi and lo parts
-// into the Gamma buffer: 8-token groups of kGS bytes, hi rows at +0, lo rows
-// at +1024 within a group, 16-byte chunks swizzled by (row % 8).
-__device__ __forceinline__ void store_gamma_row(uint8_t *gbuf, int t, const float (&e)[kKP], float scale) {
-    uint8_t *hi = gbuf + (t >> 3) * kGS + (t & 7) * 128;
-    uint8_t *lo = hi + 1024;
-#pragma unroll
-    for (int c = 0; c < kKP / 8; ++c) {
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float g0 = e[c * 8 + 2 * q] * scale, g1 = e[c * 8 + 2 * q + 1] * scale;
-            wh[q] = pack_bf2(g0, g1);
-            wl[q] = pack_bf2(g0 - bf_lo(wh[q]), g1 - bf_hi(wh[q]));
-        }
-        const uint32_t sw = (uint32_t)((c ^ (t & 7)) << 4);
-        *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    }
-}
-
 // Aborts the CTA's work on a timed-out wait: records the status once.
 __device__ __forceinline__ void note_timeout(unsigned *status, int *abort_flag) {
     set_status(status, GMA_ERR_TIMEOUT);
     *reinterpret_cast<volatile int *>(abort_flag) = 1;
-}
-
-// ------------------------------------------------------------------ write kernel
-// Latent aggregation over one split of the keys of one head ([GMA, Eqs. (5)-(6)]):
-// part[k][c] = sum_{j in split} gamma^K_jk V_jc, part[k][d_v] = sum gamma^K_jk.
-// Grid (nsplit, B*H); 128 threads; thread t owns TMEM lane / tile row t.
-template <int D_V>
-struct WriteSmem {
-    static constexpr int kX = 0;                                  // K_X tile (16 KB)
-    static constexpr int kX2 = kX + kTileBytes;                   // x2hi | x2lo (32 KB), then Gamma
-    static constexpr int kV = kX2 + 2 * kTileBytes;               // V tile(s): D_V/64 boxes of 16 KB
-    static constexpr int kCoef = kV + (D_V / 64) * kTileBytes;    // 32 KB + c
-    static constexpr int kOnes = kCoef + ((kCoefBytes + 1023) & ~1023);  // 2 KB of bf16 1.0
-    static constexpr int kBars = kOnes + 2048;
-    static constexpr int kBytes = kBars + 64;
-    static constexpr int kAlloc = kBytes + 1024;                  // slack for 1 KB alignment
-};
-
-template <int D_V>
-__global__ void __launch_bounds__(128, 1) tc_write_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                           const __grid_constant__ CUtensorMap tmV,
-                                                           const uint8_t *__restrict__ coef_img, int H, int N,
-                                                           int tiles_per_split, int nsplit,
-                                                           float *__restrict__ part, unsigned *status) {
-    using L = WriteSmem<D_V>;
-    constexpr int kTmemCols = 256;
-    constexpr int kAccV = kKP, kAccZ = kKP + D_V;  // TMEM columns
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xk = smem + L::kX, *x2 = smem + L::kX2, *vt = smem + L::kV, *coef = smem + L::kCoef,
-            *ones = smem + L::kOnes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);  // [0] TMA, [1] MMA
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
-    int *abort_flag = reinterpret_cast<int *>(bars + 3);
-    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
-
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int split = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int ntiles = (N + kTile - 1) / kTile;
-    const int tile0 = split * tiles_per_split, tile1 = min(ntiles, tile0 + tiles_per_split);
-    if (failed(status)) return;
-
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-    }
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(coef_img + (size_t)h * kCoefStride);
-        uint4 *dst = reinterpret_cast<uint4 *>(coef);
-        for (int i = tid; i < kCoefBytes / 16; i += blockDim.x) dst[i] = src[i];
-        uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int i = tid; i < 2048 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(ones)[i] = one4;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    constexpr uint32_t kTxBytes = kTileBytes * (1 + D_V / 64);
-
-    if (tid == 0 && tile0 < tile1) {
-        mbar_arrive_expect_tx(&bars[0], kTxBytes);
-        tma_load_3d(xk, &tmK, 0, tile0 * kTile, bh, &bars[0]);
-#pragma unroll
-        for (int vb = 0; vb < D_V / 64; ++vb) tma_load_3d(vt + vb * kTileBytes, &tmV, vb * 64, tile0 * kTile, bh, &bars[0]);
-    }
-    uint32_t ph_tma = 0, ph_mma = 0;
-    constexpr uint32_t idesc_v = idesc_bf16(kTile, 64, true, true);
-    constexpr uint32_t idesc_z = idesc_bf16(kTile, 16, true, false);
-
-    for (int tile = tile0; tile < tile1; ++tile) {
-        if (!mbar_wait(&bars[0], ph_tma)) note_timeout(status, abort_flag);
-        ph_tma ^= 1;
-        prep_x2(xk, x2, x2 + kTileBytes, kTileBytes, tid, blockDim.x);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            issue_scores(tmem, xk, x2, x2 + kTileBytes, coef);
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        tc_fence_after();
-        {
-            float e[kKP];
-            const float r = score_row_exp(tmem + lane_base, cvec, e);
-            const int tok = tile * kTile + tid;
-            const float scale = tok < N ? 1.0f / r : 0.0f;  // rows past N contribute nothing
-            store_gamma_row(x2, tid, e, scale);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t dg = sdesc_sw128(smem_u32(x2), 1024, kGS), dv = sdesc_sw128(smem_u32(vt), 16, 1024);
-            const uint64_t bz = sdesc_sw128(smem_u32(ones), 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-                const uint32_t acc = (tile > tile0 || kk > 0) ? 1u : 0u;
-                const uint64_t a = dadd(dg, kk * 2 * kGS);
-#pragma unroll
-                for (int vb = 0; vb < D_V / 64; ++vb) {
-                    const uint64_t b = dadd(dv, vb * kTileBytes + kk * 2048);
-                    umma_bf16(tmem + kAccV + vb * 64, a, b, idesc_v, acc);
-                }
-                umma_bf16(tmem + kAccZ, a, bz, idesc_z, acc);
-            }
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0 && tile + 1 < tile1) {
-            mbar_arrive_expect_tx(&bars[0], kTxBytes);
-            tma_load_3d(xk, &tmK, 0, (tile + 1) * kTile, bh, &bars[0]);
-#pragma unroll
-            for (int vb = 0; vb < D_V / 64; ++vb)
-                tma_load_3d(vt + vb * kTileBytes, &tmV, vb * 64, (tile + 1) * kTile, bh, &bars[0]);
-        }
-    }
-
-    // Partial memory: rows 0..63 of the accumulator hold the hi-weighted sums,
-    // rows 64..127 the lo-weighted ones; add them and write [KP][D_V + 1].
-    const bool ok = !*reinterpret_cast<volatile int *>(abort_flag);
-    if (ok && tile0 < tile1) {
-        tc_fence_after();
-        float *red = reinterpret_cast<float *>(smem);  // [128][D_V + 1] fp32, over the tiles region
-        constexpr int W = D_V + 1;
-#pragma unroll
-        for (int cb = 0; cb < D_V / 32; ++cb) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kAccV + cb * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) red[tid * W + cb * 32 + q] = __uint_as_float(v[q]);
-        }
-        {
-            uint32_t z[16];
-            tmem_ld16(tmem + lane_base + kAccZ, z);
-            tmem_wait_ld();
-            red[tid * W + D_V] = __uint_as_float(z[0]);
-        }
-        __syncthreads();
-        float *out = part + ((size_t)bh * nsplit + split) * kKP * W;
-        for (int e = tid; e < kKP * W; e += blockDim.x) out[e] = red[e] + red[kKP * W + e];
-    } else if (ok) {  // a split without tiles contributes zeros
-        float *out = part + ((size_t)bh * nsplit + split) * kKP * (D_V + 1);
-        for (int e = tid; e < kKP * (D_V + 1); e += blockDim.x) out[e] = 0.f;
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-}
-
-// ------------------------------------------------------------------ causal
-// Exclusive prefix over the segment aggregates of each head, in segment
-// order, in place: part[s] <- sum_{s' < s} part[s'] ([GMA, causal variant:
-// the prefix memories are cumulative sums along the sequence]).
-__global__ void scan_segments_kernel(float *__restrict__ part, int nseg, int E, const unsigned *status) {
-    if (failed(status)) return;
-    const int bh = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    float *p = part + (size_t)bh * nseg * E + e;
-    float run = 0.f;
-    for (int s = 0; s < nseg; ++s) {
-        const float cur = p[(size_t)s * E];
-        p[(size_t)s * E] = run;
-        run += cur;
-    }
-}
-
-// Writes the state B operand [NB x KP] (bf16 hi at `bop`, lo at bop + NB*128)
-// from the fp32 state S[k][n] (row n < D_V: S[:, n]; row D_V: Z; rows above: 0).
-template <int D_V>
-__device__ __forceinline__ void build_state_operand(const float *S, uint8_t *bop, int tid, int nthreads) {
-    constexpr int NB = D_V + 16, W = D_V + 1;
-    __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(bop);
-    __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(bop + NB * 128);
-    for (int e = tid; e < NB * kKP; e += nthreads) {
-        const int n = e / kKP, k = e % kKP;
-        const float v = n <= D_V ? S[k * W + n] : 0.f;
-        const __nv_bfloat16 vh = __float2bfloat16_rn(v);
-        const uint32_t off = sw128_offset(n, k, 1024) / 2;
-        bhi[off] = vh;
-        blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
-    }
-}
-
-// Causal GMA over one segment of one head ([GMA, Eq. (8b)]), in chunks of
-// C = 128 tokens.  With (S, Z) the prefix memory before the chunk and
-// P = mask_{j <= i}(Gamma^Q_c Gamma^K_c^T) the intra-chunk affinity:
-//   O_i = (sum_j P_ij V_j + gQ_i S) / (sum_j P_ij + gQ_i Z + eps r_i),
-// (gQ un-normalised, r_i its row sum), then S += Gamma^K_c^T V_c, Z += Gamma^K_c^T 1.
-// The segment's starting prefix comes from scan_segments_kernel.
-struct CausalSmem {
-    static constexpr int D_V = 64, NB = D_V + 16, W = D_V + 1;
-    static constexpr int kA = 0;                      // xq | xk | x2q (x2hi|x2lo) -> gq -> P (64 KB)
-    static constexpr int kXQ = kA, kXK = kA + kTileBytes, kX2Q = kA + 2 * kTileBytes;
-    static constexpr int kB = kA + 4 * kTileBytes;    // x2k (x2hi|x2lo) -> gk (32 KB)
-    static constexpr int kV = kB + 2 * kTileBytes;    // V tile (16 KB)
-    static constexpr int kCoef = kV + kTileBytes;
-    static constexpr int kBop = kCoef + ((kCoefBytes + 1023) & ~1023);  // state operand hi | lo
-    static constexpr int kOnes = kBop + 2 * NB * 128;
-    static constexpr int kS = kOnes + 2048;           // fp32 state [KP][W]
-    static constexpr int kBars = kS + ((kKP * W * 4 + 1023) & ~1023);
-    static constexpr int kBytes = kBars + 64;
-    static constexpr int kAlloc = kBytes + 1024;
-};
-constexpr int kGSP = 4096;  // P buffer: bytes per 8-query group (128 keys, hi | lo)
-
-__global__ void __launch_bounds__(128, 1) tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                            const __grid_constant__ CUtensorMap tmK,
-                                                            const __grid_constant__ CUtensorMap tmV,
-                                                            const uint8_t *__restrict__ coef_img,
-                                                            const float *__restrict__ prefix, int H, int N,
-                                                            int tiles_per_seg, int nseg, float eps,
-                                                            void *__restrict__ O, int o_bf16, unsigned *status) {
-    using L = CausalSmem;
-    constexpr int D_V = L::D_V, NB = L::NB, W = L::W;
-    constexpr int kTmemCols = 256;
-    constexpr int kSQ = 0, kSK = kKP, kP = 0, kSc = 0, kO = 128;  // TMEM columns
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xq = smem + L::kXQ, *xk = smem + L::kXK, *x2q = smem + L::kX2Q, *pbuf = smem + L::kA;
-    uint8_t *x2k = smem + L::kB, *vt = smem + L::kV, *coef = smem + L::kCoef, *bop = smem + L::kBop,
-            *ones = smem + L::kOnes;
-    float *S = reinterpret_cast<float *>(smem + L::kS);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
-    int *abort_flag = reinterpret_cast<int *>(bars + 3);
-    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
-
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int ntiles = (N + kTile - 1) / kTile;
-    const int tile0 = seg * tiles_per_seg, tile1 = min(ntiles, tile0 + tiles_per_seg);
-    if (failed(status) || tile0 >= tile1) return;
-
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    constexpr uint32_t kTx = 3 * kTileBytes;
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        mbar_arrive_expect_tx(&bars[0], kTx);
-        tma_load_3d(xq, &tmQ, 0, tile0 * kTile, bh, &bars[0]);
-        tma_load_3d(xk, &tmK, 0, tile0 * kTile, bh, &bars[0]);
-        tma_load_3d(vt, &tmV, 0, tile0 * kTile, bh, &bars[0]);
-    }
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(coef_img + (size_t)h * kCoefStride);
-        uint4 *dst = reinterpret_cast<uint4 *>(coef);
-        for (int i = tid; i < kCoefBytes / 16; i += blockDim.x) dst[i] = src[i];
-        const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int i = tid; i < 2048 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(ones)[i] = one4;
-        const float *pre = prefix + ((size_t)bh * nseg + seg) * kKP * W;
-        for (int e = tid; e < kKP * W; e += blockDim.x) S[e] = pre[e];
-    }
-    __syncthreads();
-    build_state_operand<D_V>(S, bop, tid, blockDim.x);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    constexpr uint32_t idesc_p = idesc_bf16(kTile, kTile, false, false);
-    constexpr uint32_t idesc_o = idesc_bf16(kTile, NB, false, false);
-    constexpr uint32_t idesc_v = idesc_bf16(kTile, 64, false, true);   // A K-major (P), B MN-major (V)
-    constexpr uint32_t idesc_z = idesc_bf16(kTile, 16, false, false);
-    constexpr uint32_t idesc_sv = idesc_bf16(kTile, 64, true, true);   // A MN-major (Gamma^K^T), B MN-major
-    constexpr uint32_t idesc_sz = idesc_bf16(kTile, 16, true, false);
-    uint32_t ph_tma = 0, ph_mma = 0;
-
-    for (int tile = tile0; tile < tile1; ++tile) {
-        const int tok = tile * kTile + tid;
-        if (!mbar_wait(&bars[0], ph_tma)) note_timeout(status, abort_flag);
-        ph_tma ^= 1;
-        prep_x2(xq, x2q, x2q + kTileBytes, kTileBytes, tid, blockDim.x);
-        prep_x2(xk, x2k, x2k + kTileBytes, kTileBytes, tid, blockDim.x);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            issue_scores(tmem + kSQ, xq, x2q, x2q + kTileBytes, coef);
-            issue_scores(tmem + kSK, xk, x2k, x2k + kTileBytes, coef);
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        tc_fence_after();
-        float rq;
-        {
-            float e[kKP];
-            rq = score_row_exp(tmem + lane_base + kSQ, cvec, e);
-            store_gamma_row(x2q, tid, e, 1.0f);
-            const float rk = score_row_exp(tmem + lane_base + kSK, cvec, e);
-            store_gamma_row(x2k, tid, e, tok < N ? 1.0f / rk : 0.0f);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t dq = sdesc_sw128(smem_u32(x2q), 16, kGS), dk = sdesc_sw128(smem_u32(x2k), 16, kGS),
-                           db = sdesc_sw128(smem_u32(bop), 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kKP / 16; ++kk) {
-                const uint64_t qh = dadd(dq, kk * 32), ql = dadd(dq, 1024 + kk * 32);
-                const uint64_t kh = dadd(dk, kk * 32), kl = dadd(dk, 1024 + kk * 32);
-                const uint64_t bh_ = dadd(db, kk * 32), bl_ = dadd(db, NB * 128 + kk * 32);
-                const uint32_t acc = kk > 0 ? 1u : 0u;
-                umma_bf16(tmem + kP, qh, kh, idesc_p, acc);   // P = gQ gK^T (3 split terms)
-                umma_bf16(tmem + kP, ql, kh, idesc_p, 1u);
-                umma_bf16(tmem + kP, qh, kl, idesc_p, 1u);
-                umma_bf16(tmem + kO, qh, bh_, idesc_o, acc);  // [num | den] = gQ [S | Z]
-                umma_bf16(tmem + kO, ql, bh_, idesc_o, 1u);
-                umma_bf16(tmem + kO, qh, bl_, idesc_o, 1u);
-            }
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        tc_fence_after();
-        // Masked intra-chunk affinity row i = tid: keep keys j <= i, split hi / lo.
-        {
-            uint8_t *hi = pbuf + (tid >> 3) * kGSP + (tid & 7) * 128;
-            uint8_t *lo = hi + 2048;
-#pragma unroll
-            for (int cb = 0; cb < kTile / 32; ++cb) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kP + cb * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t wh[4], wl[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int j0 = cb * 32 + c4 * 8 + 2 * q;
-                        const float p0 = j0 <= tid ? __uint_as_float(v[c4 * 8 + 2 * q]) : 0.f;
-                        const float p1 = j0 + 1 <= tid ? __uint_as_float(v[c4 * 8 + 2 * q + 1]) : 0.f;
-                        wh[q] = pack_bf2(p0, p1);
-                        wl[q] = pack_bf2(p0 - bf_lo(wh[q]), p1 - bf_hi(wh[q]));
-                    }
-                    const int chunk = (cb * 32 + c4 * 8) >> 3;        // 16-byte chunk over 128 keys
-                    const int blk = chunk >> 3, c = chunk & 7;
-                    const uint32_t sw = (uint32_t)(blk * 1024 + ((c ^ (tid & 7)) << 4));
-                    *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                    *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-                }
-            }
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t dp = sdesc_sw128(smem_u32(pbuf), 16, kGSP), dv = sdesc_sw128(smem_u32(vt), 16, 1024),
-                           dg = sdesc_sw128(smem_u32(x2k), 1024, kGS);
-            const uint64_t bz = sdesc_sw128(smem_u32(ones), 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-                const uint32_t ao = (kk >> 2) * 1024 + (kk & 3) * 32;
-                const uint64_t ph = dadd(dp, ao), pl = dadd(dp, 2048 + ao);
-                const uint64_t bv = dadd(dv, kk * 2048);
-                umma_bf16(tmem + kO, ph, bv, idesc_v, 1u);          // num += P V
-                umma_bf16(tmem + kO, pl, bv, idesc_v, 1u);
-                umma_bf16(tmem + kO + D_V, ph, bz, idesc_z, 1u);    // den += P 1
-                umma_bf16(tmem + kO + D_V, pl, bz, idesc_z, 1u);
-                const uint64_t ag = dadd(dg, kk * 2 * kGS);  // [gK_hi ; gK_lo]^T
-                const uint32_t acc = kk > 0 ? 1u : 0u;
-                umma_bf16(tmem + kSc, ag, bv, idesc_sv, acc);       // chunk state: gK^T V
-                umma_bf16(tmem + kSc + D_V, ag, bz, idesc_sz, acc); //              gK^T 1
-            }
-            umma_commit(&bars[1]);
-        }
-        if (!mbar_wait(&bars[1], ph_mma)) note_timeout(status, abort_flag);
-        ph_mma ^= 1;
-        tc_fence_after();
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-        if (tid == 0 && tile + 1 < tile1) {  // every tile buffer is free: fetch the next chunk
-            mbar_arrive_expect_tx(&bars[0], kTx);
-            tma_load_3d(xq, &tmQ, 0, (tile + 1) * kTile, bh, &bars[0]);
-            tma_load_3d(xk, &tmK, 0, (tile + 1) * kTile, bh, &bars[0]);
-            tma_load_3d(vt, &tmV, 0, (tile + 1) * kTile, bh, &bars[0]);
-        }
-        // Outputs of the chunk.
-        {
-            uint32_t dz[16];
-            tmem_ld16(tmem + lane_base + kO + D_V, dz);
-            tmem_wait_ld();
-            const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rq);
-            const size_t row = (size_t)bh * N + tok;
-#pragma unroll
-            for (int cb = 0; cb < D_V / 32; ++cb) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kO + cb * 32, v);
-                tmem_wait_ld();
-                if (tok < N) {
-                    if (o_bf16) {
-                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + row * D_V + cb * 32);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            o[q] = make_uint4(pack_bf2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                                              pack_bf2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                                              pack_bf2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                                              pack_bf2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
-                    } else {
-                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(O) + row * D_V + cb * 32);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            o[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                               __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
-                    }
-                }
-            }
-        }
-        // Carry: S += (hi rows 0..63) + (lo rows 64..127) of the chunk state.
-        if (tile + 1 < tile1) {
-            // the gq area is free again (its MMAs are done and the next chunk's TMA
-            // writes only xq / xk): [64][W] fp32 = 16.6 KB
-            float *tmp = reinterpret_cast<float *>(x2q);
-            uint32_t v[32];
-            float row[W];
-#pragma unroll
-            for (int cb = 0; cb < D_V / 32; ++cb) {
-                tmem_ld32(tmem + lane_base + kSc + cb * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 32; ++q) row[cb * 32 + q] = __uint_as_float(v[q]);
-            }
-            {
-                uint32_t z[16];
-                tmem_ld16(tmem + lane_base + kSc + D_V, z);
-                tmem_wait_ld();
-                row[D_V] = __uint_as_float(z[0]);
-            }
-            if (tid >= kKP)
-#pragma unroll
-                for (int c = 0; c < W; ++c) tmp[(tid - kKP) * W + c] = row[c];
-            __syncthreads();
-            if (tid < kKP)
-#pragma unroll
-                for (int c = 0; c < W; ++c) S[tid * W + c] += row[c] + tmp[tid * W + c];
-            __syncthreads();
-            build_state_operand<D_V>(S, bop, tid, blockDim.x);
-            fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        __syncthreads();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ persistent pipelined kernels
@@ -1803,33 +1245,6 @@ bool make_out_map(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-struct TcLayout {
-    size_t coef = 0, part = 0, total = 0;
-    int nsplit = 0, tiles_per_split = 0;
-};
-
-constexpr int kTargetCtas = 2 * 152;
-
-constexpr int kCausalSegTiles = 8;  // default causal segment: 1024 tokens
-
-TcLayout tc_layout(const Problem &p, int causal, int splits) {
-    TcLayout L;
-    const int ntiles = (p.N + kTile - 1) / kTile;
-    int ns = splits > 0 ? splits
-                        : causal ? (ntiles + kCausalSegTiles - 1) / kCausalSegTiles
-                                 : (kTargetCtas + p.BH() - 1) / p.BH();
-    ns = ns < 1 ? 1 : (ns > ntiles ? ntiles : ns);
-    L.tiles_per_split = (ntiles + ns - 1) / ns;
-    L.nsplit = (ntiles + L.tiles_per_split - 1) / L.tiles_per_split;
-    size_t off = kStatusBytes;
-    L.coef = off;
-    off = align256(off + kCoefStride * p.H);
-    L.part = off;
-    off = align256(off + sizeof(float) * (size_t)p.BH() * L.nsplit * kKP * (p.d_v + 1));
-    L.total = off;
-    return L;
 }
 
 template <typename KernelT>
