@@ -63,16 +63,20 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
 // One block per head.  Writes the four bf16 coefficient matrices in the
 // K-major SW128 byte image the score MMA reads (rows = components, 128 B of
 // d_r per row), plus c_k (fp32, -inf for padded components).  Validates the
-// parameters.
-__device__ void build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
-                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, unsigned *status,
-                                int tid, int nthreads);
+// parameters into the head's error word.  It is the first kernel of a call, so
+// it also clears the call's status word and the per-head job counters.
+__device__ bool build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
+                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, int tid, int nthreads);
 
 __global__ void coef_prep_tc_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
                                     const float *__restrict__ log_pi, int K, uint8_t *__restrict__ img,
-                                    unsigned *status) {
-    build_coef_smem(mu, sigma2, log_pi, blockIdx.x, K, img + (size_t)blockIdx.x * kCoefStride, status, threadIdx.x,
-                    blockDim.x);
+                                    unsigned *status, unsigned *head_err, unsigned *counters, int BH) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < BH; i += gridDim.x * blockDim.x) counters[i] = 0u;
+    const bool bad = build_coef_smem(mu, sigma2, log_pi, blockIdx.x, K, img + (size_t)blockIdx.x * kCoefStride,
+                                     threadIdx.x, blockDim.x);
+    const int any = __syncthreads_or(bad ? 1 : 0);
+    if (threadIdx.x == 0) head_err[blockIdx.x] = any ? (unsigned)GMA_ERR_NONFINITE_PARAM : 0u;
 }
 
 // ------------------------------------------------------------------ shared pieces
@@ -123,9 +127,9 @@ __host__ __device__ inline int slot_of(const Part &P, int c, int bh) { return bh
 // then c_k) written through a generic pointer -- shared memory inside the
 // persistent kernels, global memory for coef_prep_tc_kernel -- by every
 // thread of the block.
-__device__ void build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
-                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, unsigned *status,
-                                int tid, int nthreads) {
+__device__ bool build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
+                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, int tid, int nthreads) {
+    bool bad = false;
     // Four consecutive j of one component per step: float4 loads, issued for
     // all of a thread's steps before any store, then 8-byte stores (the four
     // bf16 values share one 16-byte chunk of the swizzled row).  With
@@ -164,7 +168,7 @@ __device__ void build_coef_smem(const float *__restrict__ mu, const float *__res
             for (int v = 0; v < 2; ++v) {
                 const float s2 = sv[2 * u + v], m = mv[2 * u + v];
                 const bool real = live && k < K;
-                if (real && (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m))) set_status(status, GMA_ERR_NONFINITE_PARAM);
+                if (real && (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m))) bad = true;
                 const float inv = real ? __frcp_rn(s2) : 0.f;
                 a[v] = (-0.5f * kLog2e) * inv;
                 b[v] = (kLog2e * m) * inv;
@@ -185,21 +189,24 @@ __device__ void build_coef_smem(const float *__restrict__ mu, const float *__res
         *reinterpret_cast<uint2 *>(coef + 3 * kCoefMatBytes + off) = make_uint2(bl[0], bl[1]);
         if (j == 0) {
             if (k < K) {
-                if (!isfinite(lp[q])) set_status(status, GMA_ERR_NONFINITE_PARAM);
+                if (!isfinite(lp[q])) bad = true;
                 cvec[k] = kLog2e * (lp[q] - 0.5f * det);
             } else {
                 cvec[k] = -INFINITY;
             }
         }
     }
+    return bad;
 }
 
-// Copies head h's coefficient image (written once per call by
-// coef_prep_tc_kernel) into shared memory.
-__device__ __forceinline__ void copy_coef(const uint8_t *__restrict__ img, int h, uint8_t *coef, int tid, int nthreads) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(img + (size_t)h * kCoefStride);
-    uint4 *dst = reinterpret_cast<uint4 *>(coef);
-    for (int i = tid; i < kCoefBytes / 16; i += nthreads) dst[i] = __ldcg(src + i);
+// Head-error check of the first persistent kernel of a call: any head whose
+// parameters failed validation fails the call.  Returns the first error word.
+__device__ __forceinline__ unsigned first_head_error(const unsigned *head_err, int H) {
+    for (int h = 0; h < H; ++h) {
+        const unsigned e = __ldcg(head_err + h);
+        if (e) return e;
+    }
+    return 0u;
 }
 
 // Bounded polling: tick(progressed) returns false once kWaitLimitNs pass
@@ -359,21 +366,77 @@ __device__ __forceinline__ void store_gamma_words(uint8_t *gbuf, int t, const ui
     }
 }
 
-// V stage of the write kernel: the TMA box [128 tokens x 64] (MN-major B
-// chunk 0) followed by a constant chunk of ones (chunk 1), so one N = 80 MMA
-// gives both Gamma^T V (columns 0..63) and Gamma^T 1 (column 64).
-constexpr int kVStageBytes = 2 * kTileBytes;
+// Combines the job partials ([KP][d_v + 1] fp32 each) of head bh in CTA
+// order, so the result does not depend on which job finished last:
+//   mode 0: out (shared memory) = sum of the partials,
+//   mode 1: each partial replaced in place by the sum of the ones before it.
+// Each thread keeps 2 vectors x 8 CTAs of loads in flight.
+__device__ void combine_partials(float *__restrict__ part, const Part &P, int bh, int mode, float *out, int tid,
+                                 int nthreads) {
+    constexpr int kE4 = kKP * (64 + 1) / 4;
+    constexpr size_t kPS = (size_t)kKP * (64 + 1);
+    const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
+    for (int e0 = tid; e0 < kE4; e0 += 2 * nthreads) {
+        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        for (int cc0 = cf; cc0 <= cl; cc0 += 8) {
+            float4 v[8][2];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int cc = cc0 + u;
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kPS);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int e4 = e0 + q * nthreads;
+                    v[u][q] = (cc <= cl && e4 < kE4) ? __ldcg(src + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int cc = cc0 + u;
+                if (cc > cl) break;
+                float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kPS);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int e4 = e0 + q * nthreads;
+                    if (e4 >= kE4) continue;
+                    if (mode == 1) __stcg(dst + e4, acc[q]);
+                    acc[q].x += v[u][q].x;
+                    acc[q].y += v[u][q].y;
+                    acc[q].z += v[u][q].z;
+                    acc[q].w += v[u][q].w;
+                }
+            }
+        }
+        if (mode == 0)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e4 = e0 + q * nthreads;
+                if (e4 < kE4) reinterpret_cast<float4 *>(out)[e4] = acc[q];
+            }
+    }
+}
 
+// Write kernel stages.  K tiles are freed once their score MMAs complete, V
+// tiles once their write MMA completes, so the two rings are separate and the
+// loads run ahead of the epilogue groups.  The Z column comes from a constant
+// chunk of ones read as the second MN chunk of the V operand: each V stage's
+// descriptor sets its chunk stride (LBO) to the distance from that stage to
+// the ones chunk, so one N = 80 MMA gives Gamma^T V (columns 0..63) and
+// Gamma^T 1 (column 64).
 struct Write2Smem {
     static constexpr int W = 64 + 1;
+    static constexpr int kKS = 4, kVS = 3;                      // K / V ring depths
     static constexpr int kKst = 0;                              // K stages
-    static constexpr int kVst = kKst + kNG * kTileBytes;        // V | ones stages
-    static constexpr int kXG = kVst + kNG * kVStageBytes;       // Gamma^K buffers [NG][32 KB]
+    static constexpr int kVst = kKst + kKS * kTileBytes;        // V stages
+    static constexpr int kOnes = kVst + kVS * kTileBytes;       // chunk of ones (MN-major, 128 x 64)
+    static constexpr int kXG = kOnes + kTileBytes;              // Gamma^K buffers [NG][32 KB]
     static constexpr int kCoef = kXG + kNG * 2 * kTileBytes;
     static constexpr int kBars = kCoef + ((kCoefBytes + 1023) & ~1023);
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
-    static_assert(128 * W * 4 <= kCoef, "reduction buffer must fit over the tile buffers");
+    static_assert(128 * W * 4 <= kVst, "reduction buffer must fit over the K stages");
+    static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 // Latent aggregation ([GMA, Eqs. (5)-(6)]) over each job's keys (d_v = 64):
@@ -385,8 +448,9 @@ struct Write2Smem {
 // [128 NG + 64 g, +64); accumulator [Vt | Z] (N = 80) at 192 NG.
 __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-    const uint8_t *__restrict__ coef_img, int H, int N, Part P, float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img,
-    size_t mem_img_stride, int mode, unsigned *status) {
+    const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part P,
+    float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img, size_t mem_img_stride,
+    int mode, unsigned *status) {
     using L = Write2Smem;
     constexpr int D_V = 64, W = L::W;
     constexpr int kTmemCols = 512;
@@ -394,13 +458,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     static_assert(kAcc + 80 <= kTmemCols, "TMEM budget");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int KS = L::kKS, VS = L::kVS;
     uint8_t *kst = smem + L::kKst, *vst = smem + L::kVst, *xg = smem + L::kXG, *coef = smem + L::kCoef;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint64_t *kvfull = bars, *kvempty = bars + kNG, *xready = bars + 2 * kNG, *sfull = bars + 3 * kNG,
-             *gready = bars + 4 * kNG, *wdone = bars + 5 * kNG, *accfull = bars + 6 * kNG;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 6 * kNG + 1);
-    int *abort_flag = reinterpret_cast<int *>(bars + 6 * kNG + 2);
+    uint64_t *kfull = bars, *kempty = kfull + KS, *vfull = kempty + KS, *vempty = vfull + VS;
+    uint64_t *xready = vempty + VS, *sfull = xready + kNG, *gready = sfull + kNG, *wdone = gready + kNG,
+             *accfull = wdone + kNG, *cfull = accfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cfull + 1);
+    int *abort_flag = reinterpret_cast<int *>(cfull + 2);
     int *last_flag = abort_flag + 1;
+    static_assert((2 * KS + 2 * VS + 4 * kNG + 4) * 8 <= 256, "barrier area");
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -413,84 +480,121 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         tmem_relinquish();
     }
     if (tid == 32) {
+        for (int i = 0; i < KS; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
+            mbar_init(&vfull[i], 1);
+            mbar_init(&vempty[i], 1);
+        }
         for (int i = 0; i < kNG; ++i) {
-            mbar_init(&kvfull[i], 1);
-            mbar_init(&kvempty[i], 1);
             mbar_init(&xready[i], 4);
             mbar_init(&sfull[i], 1);
             mbar_init(&gready[i], 4);
             mbar_init(&wdone[i], 1);
         }
         mbar_init(accfull, 1);
-        *abort_flag = 0;
+        mbar_init(cfull, 1);
+        const unsigned e = first_head_error(head_err, H);
+        if (e) set_status(status, e);
+        *abort_flag = e ? 1 : 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    {   // the constant ones chunk of every V stage
+    {   // the constant ones chunk
         const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int st = 0; st < kNG; ++st)
-            for (int i = tid; i < kTileBytes / 16; i += kThreadsG)
-                reinterpret_cast<uint4 *>(vst + st * kVStageBytes + kTileBytes)[i] = one4;
+        for (int i = tid; i < kTileBytes / 16; i += kThreadsG) reinterpret_cast<uint4 *>(smem + L::kOnes)[i] = one4;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t kTx = 2 * kTileBytes;
     constexpr uint32_t idesc_w = idesc_bf16(kTile, 80, true, true);
 
     int rbase = 0;   // running tile index of the CTA (barrier phases)
     int njob = 0;
-    for (int g = g0; g < gend; ++njob) {
+    for (int g = aborted(abort_flag) ? gend : g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
-        __syncthreads();
-        copy_coef(coef_img, h, coef, tid, kThreadsG);
+        // The previous job's reads of the coefficients and its generic writes over
+        // the K ring are complete; the head's coefficients arrive on cfull.
         fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0) {
+            mbar_arrive_expect_tx(cfull, kCoefBytes);
+            bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
+        }
 
         if (warp == 0) {
-            if (lane == 0)
-                for (int i = 0; i < n; ++i) {
-                    const int r = rbase + i, s = r % kNG;
-                    if (!wait_or_abort(&kvempty[s], ((r / kNG) & 1) ^ 1, status, abort_flag)) break;
-                    mbar_arrive_expect_tx(&kvfull[s], kTx);
-                    tma_load_3d(kst + s * kTileBytes, &tmK, 0, (t0 + i) * kTile, bh, &kvfull[s]);
-                    tma_load_3d(vst + s * kVStageBytes, &tmV, 0, (t0 + i) * kTile, bh, &kvfull[s]);
+            if (lane == 0) {
+                // K loads as far ahead as the K ring allows; V loads follow, never ahead of their K.
+                int nk = 0, nv = 0;
+                Stall st;
+                while (nv < n) {
+                    bool prog = false;
+                    if (nk < n) {
+                        const int r = rbase + nk, s = r % KS;
+                        if (mbar_test(&kempty[s], ((r / KS) & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(&kfull[s], kTileBytes);
+                            tma_load_3d(kst + s * kTileBytes, &tmK, 0, (t0 + nk) * kTile, bh, &kfull[s]);
+                            ++nk;
+                            prog = true;
+                        }
+                    }
+                    if (nv < nk) {
+                        const int r = rbase + nv, s = r % VS;
+                        if (mbar_test(&vempty[s], ((r / VS) & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(&vfull[s], kTileBytes);
+                            tma_load_3d(vst + s * kTileBytes, &tmV, 0, (t0 + nv) * kTile, bh, &vfull[s]);
+                            ++nv;
+                            prog = true;
+                        }
+                    }
+                    if (!st.tick(prog, abort_flag)) {
+                        note_timeout(status, abort_flag);
+                        break;
+                    }
                 }
+            }
         } else if (warp == 1) {
             if (lane == 0) {
                 // Base descriptors, built once; each MMA advances one by an add.
                 const uint64_t dk0 = sdesc_sw128(smem_u32(kst), 16, 1024), dc0 = sdesc_sw128(smem_u32(coef), 16, 1024);
                 const uint64_t dg0 = sdesc_sw128(smem_u32(xg), 1024, kGS);
-                const uint64_t dv0 = sdesc_sw128(smem_u32(vst), kTileBytes, 1024);  // chunk stride = LBO
+                uint64_t dv[VS];  // per V stage: chunk stride (LBO) = distance to the ones chunk
+#pragma unroll
+                for (int s = 0; s < VS; ++s)
+                    dv[s] = sdesc_sw128(smem_u32(vst + s * kTileBytes), L::kOnes - (L::kVst + s * kTileBytes), 1024);
                 // Poll both queues so that neither kind of MMA waits behind the other.
                 int ns = 0, nw = 0;
                 Stall st;
-                while (nw < n) {
+                const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
+                while (coef_ok && nw < n) {
                     bool prog = false;
                     if (ns < n) {
-                        const int r = rbase + ns, gb = r % kNG, s = gb;
+                        const int r = rbase + ns, gb = r % kNG, sk = r % KS;
                         if (mbar_test(&xready[gb], (r / kNG) & 1)) {
                             tc_fence_after();
-                            issue_scores_tA(tmem + gb * 2 * kKP, tmem + kA + gb * kKP, dadd(dk0, s * kTileBytes), dc0);
+                            issue_scores_tA(tmem + gb * 2 * kKP, tmem + kA + gb * kKP, dadd(dk0, sk * kTileBytes), dc0);
                             umma_commit(&sfull[gb]);
+                            umma_commit(&kempty[sk]);
                             ++ns;
                             prog = true;
                         }
                     }
                     if (nw < ns) {
-                        const int r = rbase + nw, gb = r % kNG, s = gb;
-                        if (mbar_test(&gready[gb], (r / kNG) & 1)) {
+                        const int r = rbase + nw, gb = r % kNG, sv = r % VS;
+                        if (mbar_test(&vfull[sv], (r / VS) & 1) && mbar_test(&gready[gb], (r / kNG) & 1)) {
                             tc_fence_after();
-                            const uint64_t ag = dadd(dg0, gb * 2 * kTileBytes), bv = dadd(dv0, s * kVStageBytes);
+                            const uint64_t ag = dadd(dg0, gb * 2 * kTileBytes), bv = dv[sv];
 #pragma unroll
                             for (int kk = 0; kk < kTile / 16; ++kk)
                                 umma_bf16(tmem + kAcc, dadd(ag, kk * 2 * kGS), dadd(bv, kk * 2048), idesc_w,
                                           (nw > 0 || kk > 0) ? 1u : 0u);
-                            umma_commit(&kvempty[s]);
+                            umma_commit(&vempty[sv]);
                             umma_commit(&wdone[gb]);
                             ++nw;
                             prog = true;
@@ -508,14 +612,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
             const int row = epi_row(warp, lane);
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
             for (int i = (grp - rbase % kNG + kNG) % kNG; i < n; i += kNG) {
-                const int r = rbase + i, s = grp;
+                const int r = rbase + i, sk = r % KS;
                 uint8_t *gbuf = xg + grp * 2 * kTileBytes;
-                if (!wait_or_abort(&kvfull[s], (r / kNG) & 1, status, abort_flag)) break;
-                prep_x2_row_tmem(kst + s * kTileBytes, row, tmem + lane_base + kA + grp * kKP);
+                if (!wait_or_abort(&kfull[sk], (r / KS) & 1, status, abort_flag)) break;
+                prep_x2_row_tmem(kst + sk * kTileBytes, row, tmem + lane_base + kA + grp * kKP);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xready[grp]);
                 if (!wait_or_abort(&sfull[grp], (r / kNG) & 1, status, abort_flag)) break;
+                if (i < kNG && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 float e[kKP];
                 const float rs = score_row_exp128(tmem + lane_base + grp * 2 * kKP, cvec, e);
@@ -567,26 +672,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
             __syncthreads();
             if (*last_flag) {
                 __threadfence();
-                const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
+                combine_partials(part, P, bh, mode, red, tid, kThreadsG);
                 if (mode == 0) {
-                    for (int e = tid; e < kKP * W; e += kThreadsG) {
-                        float v = 0.f;
-                        for (int cc = cf; cc <= cl; ++cc)
-                            v += __ldcg(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kKP * W + e);
-                        red[e] = v;
-                    }
                     __syncthreads();
                     store_memory_operand<D_V>(red, W, mem_img + (size_t)bh * mem_img_stride, tid, kThreadsG);
-                } else {
-                    for (int e = tid; e < kKP * W; e += kThreadsG) {
-                        float run = 0.f;
-                        for (int cc = cf; cc <= cl; ++cc) {
-                            float *pp = part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kKP * W + e;
-                            const float cur = __ldcg(pp);
-                            *pp = run;
-                            run += cur;
-                        }
-                    }
                 }
                 if (tid == 0) counters[bh] = 0u;  // ready for the next call
             }
@@ -637,7 +726,7 @@ __device__ __forceinline__ void stage_and_store_rows(uint8_t *stage, const float
 
 struct Read2Smem {
     static constexpr int NB = 64 + 16;
-    static constexpr int kQS = kNG;
+    static constexpr int kQS = 4;  // Q ring depth (freed once the score MMAs complete)
     static constexpr int kQst = 0;
     static constexpr int kStage = kQst + kQS * kTileBytes;        // [NG groups][4 warps][8 KB]
     static constexpr int kCoef = kStage + kNG * 4 * 8192;
@@ -669,9 +758,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
     uint8_t *qst = smem + L::kQst, *stg = smem + L::kStage, *coef = smem + L::kCoef, *bop = smem + L::kB;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + kNG,
-             *gready = sfull + kNG, *ofull = gready + kNG;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ofull + kNG);
-    int *abort_flag = reinterpret_cast<int *>(ofull + kNG + 1);
+             *gready = sfull + kNG, *ofull = gready + kNG, *cfull = ofull + kNG;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cfull + 1);
+    int *abort_flag = reinterpret_cast<int *>(cfull + 2);
+    static_assert((2 * QS + 4 * kNG + 3) * 8 <= 256, "barrier area");
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -694,6 +784,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
             mbar_init(&gready[i], 4);
             mbar_init(&ofull[i], 1);
         }
+        mbar_init(cfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -706,19 +797,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
     constexpr uint32_t i160 = idesc_bf16(kTile, 2 * NB, false, false);
     constexpr uint32_t i80 = idesc_bf16(kTile, NB, false, false);
 
-    int rbase = 0;
-    for (int g = g0; g < gend;) {
+    int rbase = 0, njob = 0;
+    for (int g = g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
+        // The previous job's MMAs and epilogues are done with the coefficients
+        // and the memory operand; this head's arrive on cfull.
         __syncthreads();
-        copy_coef(coef_img, h, coef, tid, kThreadsG);
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(mem_img + (size_t)bh * mem_img_stride);
-            for (int i = tid; i < 2 * NB * 128 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(bop)[i] = __ldcg(src + i);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(cfull, kCoefBytes + 2 * NB * 128);
+            bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
+            bulk_load(bop, mem_img + (size_t)bh * mem_img_stride, 2 * NB * 128, cfull);
         }
-        fence_proxy_async_smem();
-        __syncthreads();
 
         if (warp == 0) {
             if (lane == 0)
@@ -734,7 +825,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
                 const uint64_t db0 = sdesc_sw128(smem_u32(bop), 16, 1024);
                 int ns = 0, nr = 0;
                 Stall st;
-                while (nr < n) {
+                const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
+                while (coef_ok && nr < n) {
                     bool prog = false;
                     if (ns < n) {
                         const int r = rbase + ns, gb = r % kNG, s = r % QS;
@@ -782,6 +874,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xready[grp]);
                 if (!wait_or_abort(&sfull[grp], (r / kNG) & 1, status, abort_flag)) break;
+                if (i < kNG && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 float rs;
                 {
@@ -922,9 +1015,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *qkfull = bars + 0, *qkempty = bars + 1, *vfull = bars + 2, *vempty = bars + 3, *xq = bars + 4,
              *xk = bars + 5, *sq = bars + 6, *sk = bars + 7, *gq = bars + 8, *gkr = bars + 9, *sready = bars + 10,
-             *pfull = bars + 11, *pready = bars + 12, *ofull = bars + 13, *ufull = bars + 14;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
-    int *abort_flag = reinterpret_cast<int *>(bars + 16);
+             *pfull = bars + 11, *pready = bars + 12, *ofull = bars + 13, *ufull = bars + 14, *cfull = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    int *abort_flag = reinterpret_cast<int *>(bars + 17);
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -940,7 +1033,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         mbar_init(qkfull, 1); mbar_init(qkempty, 1); mbar_init(vfull, 1); mbar_init(vempty, 1);
         mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
         mbar_init(gq, 4); mbar_init(gkr, 4); mbar_init(sready, 4); mbar_init(pfull, 1);
-        mbar_init(pready, 4); mbar_init(ofull, 1); mbar_init(ufull, 1);
+        mbar_init(pready, 4); mbar_init(ofull, 1); mbar_init(ufull, 1); mbar_init(cfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
@@ -955,25 +1048,31 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    int rbase = 0;
-    for (int g = g0; g < gend;) {
+    int rbase = 0, njob = 0;
+    for (int g = g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
-        __syncthreads();
-        copy_coef(coef_img, h, coef, tid, kThreadsG);
-        {
-            const float *pre = prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W;
-            for (int e = tid; e < kKP * W; e += kThreadsG) S[e] = __ldcg(pre + e);
-        }
-        __syncthreads();
-        if (warp >= 8) {  // key-group warps holding component rows 0..63: initial state operand
-            const int k = epi_row(warp, lane);
-            store_state_row(sop, k, S + k * W);
-        }
+        // The previous job is done with the coefficients, the state and the carry
+        // area; this head's coefficients and the job's carried-in prefix arrive on cfull.
         fence_proxy_async_smem();
         __syncthreads();
-        if (warp >= 6 && lane == 0) mbar_arrive(sready);  // state for the job's first chunk
+        if (tid == 0) {
+            mbar_arrive_expect_tx(cfull, kCoefBytes + kKP * W * 4);
+            bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
+            bulk_load(S, prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W, kKP * W * 4, cfull);
+        }
+        if (warp >= 6) {  // key group: state operand of the job's first chunk (rows 0..63 in warps 8, 9)
+            if (warp >= 8) {
+                if (wait_or_abort(cfull, njob & 1, status, abort_flag)) {
+                    const int k = epi_row(warp, lane);
+                    store_state_row(sop, k, S + k * W);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sready);
+        }
 
         if (warp == 0) {
             if (lane == 0)
@@ -997,7 +1096,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 const uint64_t dv = sdesc_sw128(smem_u32(vt), kTileBytes, 1024);        // MN-major [V | 1]
                 constexpr uint32_t i256 = idesc_bf16(kTile, 256, false, false), i128 = idesc_bf16(kTile, 128, false, false);
                 constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
-                for (int i = 0; i < n; ++i) {
+                const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
+                for (int i = 0; coef_ok && i < n; ++i) {
                     const int r = rbase + i, ph = r & 1;
                     // scores of the chunk (the Q scores overwrite the previous state increment,
                     // so they wait for the carry that read it)
@@ -1062,6 +1162,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xq);
                 if (!wait_or_abort(sq, ph, status, abort_flag)) break;
+                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 float rq;
                 {
@@ -1136,6 +1237,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xk);
                 if (!wait_or_abort(sk, ph, status, abort_flag)) break;
+                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 {
                     float e[kKP];
@@ -1268,12 +1370,15 @@ int num_sms() {
     return n;
 }
 
-// Workspace of the persistent kernels: status | per-head counters | job
-// partials [ctas][slots][KP][d_v + 1] | per-head read operand images.
+// Workspace of the persistent kernels: status | per-head job counters |
+// per-head parameter-error words | per-head coefficient images | job partials
+// [ctas][slots][KP][d_v + 1] | per-head read operand images.  Nothing needs
+// clearing by the caller: coef_prep_tc_kernel resets the status word and the
+// counters, and writes every error word.
 struct TcLayout2 {
     Part P;
     int nctas = 0;
-    size_t counters = 0, coef = 0, part = 0, mem = 0, mem_stride = 0, total = 0, reset_bytes = 0;
+    size_t counters = 0, head_err = 0, coef = 0, part = 0, mem = 0, mem_stride = 0, total = 0;
 };
 
 TcLayout2 tc_layout2(const Problem &p, int splits) {
@@ -1288,7 +1393,8 @@ TcLayout2 tc_layout2(const Problem &p, int splits) {
     size_t off = kStatusBytes;
     L.counters = off;
     off = align256(off + sizeof(unsigned) * (size_t)p.BH());
-    L.reset_bytes = off;
+    L.head_err = off;
+    off = align256(off + sizeof(unsigned) * (size_t)p.H);
     L.coef = off;
     off = align256(off + kCoefStride * p.H);
     L.part = off;
@@ -1310,14 +1416,14 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
         !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map(&to, p.O, p.BH(), p.N, p.o_bf16))
         return cudaErrorInvalidValue;
+    unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    GMA_TRY(cudaMemsetAsync(ws, 0, L.reset_bytes, s));
-    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
+    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     tc_write2_kernel<<<L.nctas, kThreadsG, Write2Smem::kAlloc, s>>>(
-        tk, tv, coef, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
+        tk, tv, coef, head_err, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_read2_kernel, Read2Smem::kAlloc));
@@ -1337,14 +1443,14 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
     if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
         !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map(&to, p.O, p.BH(), p.N, p.o_bf16))
         return cudaErrorInvalidValue;
+    unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    GMA_TRY(cudaMemsetAsync(ws, 0, L.reset_bytes, s));
-    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status);
+    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     tc_write2_kernel<<<L.nctas, kThreadsG, Write2Smem::kAlloc, s>>>(
-        tk, tv, coef, p.H, p.N, L.P, part, counters, nullptr, 0, 1, status);
+        tk, tv, coef, head_err, p.H, p.N, L.P, part, counters, nullptr, 0, 1, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_causal2_kernel, Causal2Smem::kAlloc));
