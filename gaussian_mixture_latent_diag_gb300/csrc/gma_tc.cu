@@ -237,6 +237,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, un
 __device__ __forceinline__ bool aborted(const int *abort_flag) {
     return *reinterpret_cast<const volatile int *>(abort_flag) != 0;
 }
+// Wait by polling (no suspension between probes), for the single MMA-issuing
+// thread whose wake-up latency is on the critical path; bounded like mbar_wait.
+__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
+    Stall st;
+    while (!mbar_test(bar, parity)) {
+        if (!st.tick(false, abort_flag)) {
+            note_timeout(status, abort_flag);
+            return false;
+        }
+    }
+    return true;
+}
 
 // Row of the tile / TMEM lane handled by an epilogue thread (warp w may only
 // read TMEM lanes 32*(w%4) .. 32*(w%4)+31).
@@ -944,17 +956,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
 // then (S, Z) += Gamma^K_c^T [V_c | 1].  The job's starting prefix is the
 // exclusive prefix left in the partials by tc_write2_kernel (mode 1).
 //
-// Warps: 0 TMA, 1 MMA issuer, 2..5 query group (x^2, softmax, P split,
-// outputs), 6..9 key group (x^2, softmax, Gamma^K, carry of the state).
-// One chunk is in flight; the query and key sides run in parallel.
+// Warps: 0 TMA, 1 MMA issuer, 2..5 query group (x^2, softmax, half of the P
+// split, outputs), 6..9 key group (x^2, softmax, Gamma^K, the other half of
+// the P split, carry of the state).  The state increment U is issued right
+// after P, so the carry runs beside the P split and the P [V | 1] MMAs; the
+// output epilogue of a chunk runs beside the score MMAs of the next.
 //
 // TMEM (512 columns):
 //   [0, 64)    x^2 of Q -> Gamma^Q hi | lo -> P hi   (MMA A operands)
 //   [64, 128)  x^2 of K ->                    P lo
-//   [128, 256) scores Q (N = 128) \  P = [gQhi (gKhi|gKlo)^T] + gQlo gKhi^T  (N = 256)
-//   [256, 384) scores K (N = 128) /  state increment U = gK^T [V | 1] at [128, 208)
+//   [128, 256) scores Q (N = 128) -> P = gQhi gKhi^T + gQhi gKlo^T + gQlo gKhi^T (N = 128)
+//   [256, 384) scores K (N = 128) -> state increment U = [gK_hi ; gK_lo]^T [V | 1] (N = 80)
 //   [384, 464) [num | den] (N = 80)
-// MMAs per chunk: scores 12 + 12, P 8, state read 12, P [V|1] 16, U 8.
+// MMAs per chunk: scores 12 + 12, P 12, state read 12, U 8, P [V|1] 16.
 struct Causal2Smem {
     static constexpr int W = 64 + 1;
     static constexpr int kQK = 0;                          // Q tile | K tile (one stage)
@@ -969,6 +983,112 @@ struct Causal2Smem {
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
 };
+
+// Epilogue pieces shared by the query and the key groups of the causal
+// kernel.  They are kept out of line so that both groups run one copy of the
+// code: the kernel's speed is bound by instruction fetch when each role has
+// its own inlined copy.
+__device__ __noinline__ void x2_row(const uint8_t *x, int row, uint32_t taddr) { prep_x2_row_tmem(x, row, taddr); }
+
+// Softmax of one score row and the bf16 hi / lo split of the responsibilities:
+// to_smem == 0: un-normalised (scale 1), hi words to taddr + 0..31, lo words to
+//               taddr + 32..63 (the A operand of the following MMAs);
+// to_smem != 0: normalised (scale 0 for rows past N), written as row `row` of
+//               the swizzled [128 x 64] hi block at gk and the lo block at gk + 16 KB.
+// Returns the row sum of the exponentials.
+__device__ __noinline__ float gamma_row(uint32_t s_taddr, const float *cvec, int to_smem, uint32_t taddr,
+                                        uint8_t *gk, int row, int valid) {
+    float e[kKP];
+    const float rs = score_row_exp128(s_taddr, cvec, e);
+    tc_fence_before();
+    uint32_t wh[32], wl[32];
+    split_row(e, to_smem ? (valid ? 1.0f / rs : 0.0f) : 1.0f, wh, wl);
+    if (!to_smem) {
+        tmem_st32(taddr, wh);
+        tmem_st32(taddr + 32, wl);
+        tmem_wait_st();
+    } else {
+        uint8_t *hi = gk + row * 128, *lo = gk + kTileBytes + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            const uint32_t sw = (uint32_t)((cc ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[4 * cc], wh[4 * cc + 1], wh[4 * cc + 2], wh[4 * cc + 3]);
+            *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[4 * cc], wl[4 * cc + 1], wl[4 * cc + 2], wl[4 * cc + 3]);
+        }
+    }
+    return rs;
+}
+
+// One key block (32 keys) of the masked bf16 hi / lo split of P for this
+// thread's query row: hi words to taddr_hi + 16 cb, lo words to taddr_lo + 16 cb.
+__device__ __forceinline__ void split_p_block(const uint32_t (&pp)[32], int cb, int row, uint32_t taddr_hi,
+                                              uint32_t taddr_lo) {
+    uint32_t wh[16], wl[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const int j = cb * 32 + 2 * q;
+        const float a = j <= row ? __uint_as_float(pp[2 * q]) : 0.f;
+        const float b = j + 1 <= row ? __uint_as_float(pp[2 * q + 1]) : 0.f;
+        wh[q] = pack_bf2(a, b);
+        wl[q] = pack_bf2(a - bf_lo(wh[q]), b - bf_hi(wh[q]));
+    }
+    tmem_st16(taddr_hi + cb * 16, wh);
+    tmem_st16(taddr_lo + cb * 16, wl);
+}
+__device__ __forceinline__ void zero_p_block(int cb, uint32_t taddr_hi, uint32_t taddr_lo) {
+    uint32_t z[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) z[q] = 0u;
+    tmem_st16(taddr_hi + cb * 16, z);
+    tmem_st16(taddr_lo + cb * 16, z);
+}
+
+// Masked split of P for key blocks cb0 and cb0 + 1 of this thread's query row.
+// Blocks entirely above the diagonal are written as zeros without reading P
+// (the block index of the row is uniform across a warp).
+__device__ __noinline__ void split_p_blocks(uint32_t p_taddr, uint32_t taddr_hi, uint32_t taddr_lo, int cb0,
+                                            int row) {
+    const int rb = row >> 5;
+    if (cb0 + 1 <= rb) {
+        uint32_t p0[32], p1[32];
+        tmem_ld32(p_taddr + cb0 * 32, p0);
+        tmem_ld32(p_taddr + (cb0 + 1) * 32, p1);
+        tmem_wait_ld();
+        split_p_block(p0, cb0, row, taddr_hi, taddr_lo);
+        split_p_block(p1, cb0 + 1, row, taddr_hi, taddr_lo);
+    } else if (cb0 <= rb) {
+        uint32_t p0[32];
+        tmem_ld32(p_taddr + cb0 * 32, p0);
+        tmem_wait_ld();
+        split_p_block(p0, cb0, row, taddr_hi, taddr_lo);
+        zero_p_block(cb0 + 1, taddr_hi, taddr_lo);
+    } else {
+        zero_p_block(cb0, taddr_hi, taddr_lo);
+        zero_p_block(cb0 + 1, taddr_hi, taddr_lo);
+    }
+    tmem_wait_st();
+}
+
+// Outputs of one query row of the causal kernel: [num | den] from TMEM,
+// O = num / (den + eps r), staged and stored by TMA (rows row0 .. row0 + 31
+// of head bh for the warp).
+__device__ __noinline__ void causal_output_row(uint32_t o_taddr, float rq, float eps, uint8_t *stage, int lane,
+                                               const CUtensorMap *tmO, int o_bf16, int row0, int bh) {
+    float o[64];
+    uint32_t a0[32], a1[32], dz[16];
+    tmem_ld32(o_taddr, a0);
+    tmem_ld32(o_taddr + 32, a1);
+    tmem_ld16(o_taddr + 64, dz);
+    tmem_wait_ld();
+    tc_fence_before();
+    const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rq);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        o[q] = __uint_as_float(a0[q]) * inv;
+        o[32 + q] = __uint_as_float(a1[q]) * inv;
+    }
+    stage_and_store_rows(stage, o, lane, lane, tmO, o_bf16, row0, bh);
+}
 
 // One state-operand row: component k, 64 values of S plus Z, as bf16 hi / lo,
 // MN-major SW128 (row = component; chunk 0 = columns 0..63, chunk 1 at +8 KB
@@ -997,6 +1117,32 @@ __device__ __forceinline__ void store_state_row(uint8_t *sop, int k, const float
     *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off1) = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Half of a state-operand row: columns 0..31 (half 0) or 32..63 plus Z
+// (half 1) of component k, as bf16 hi / lo (layout of store_state_row).
+__device__ __forceinline__ void store_state_half(uint8_t *sop, int k, const float *srow, int half) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * half + cc;
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float v0 = srow[8 * c + 2 * q], v1 = srow[8 * c + 2 * q + 1];
+            wh[q] = pack_bf2(v0, v1);
+            wl[q] = pack_bf2(v0 - bf_lo(wh[q]), v1 - bf_hi(wh[q]));
+        }
+        const uint32_t off = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((c ^ (k & 7)) << 4));
+        *reinterpret_cast<uint4 *>(sop + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(sop + 16384 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+    if (half) {
+        const float z = srow[64];
+        const uint32_t zh = pack_bf2(z, 0.f), zl = pack_bf2(z - bf_lo(zh), 0.f);
+        const uint32_t off0 = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((0 ^ (k & 7)) << 4));
+        *reinterpret_cast<uint4 *>(sop + 8192 + off0) = make_uint4(zh, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off0) = make_uint4(zl, 0u, 0u, 0u);
+    }
+}
+
 __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1005,7 +1151,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     using L = Causal2Smem;
     constexpr int W = L::W;
     constexpr int kTmemCols = 512;
-    constexpr int kXQ = 0, kXK = 64, kSQ = 128, kSK = 256, kPD = 128, kU = 128, kO = 384;
+    constexpr int kXQ = 0, kXK = 64, kSQ = 128, kSK = 256, kPD = 128, kU = 256, kO = 384;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qk = smem + L::kQK, *vt = smem + L::kV, *gk = smem + L::kGK, *sop = smem + L::kSop,
@@ -1033,7 +1179,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         mbar_init(qkfull, 1); mbar_init(qkempty, 1); mbar_init(vfull, 1); mbar_init(vempty, 1);
         mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
         mbar_init(gq, 4); mbar_init(gkr, 4); mbar_init(sready, 4); mbar_init(pfull, 1);
-        mbar_init(pready, 4); mbar_init(ofull, 1); mbar_init(ufull, 1); mbar_init(cfull, 1);
+        mbar_init(pready, 8); mbar_init(ofull, 1); mbar_init(ufull, 1); mbar_init(cfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
@@ -1090,35 +1236,36 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             if (lane == 0) {
                 const uint64_t dq = sdesc_sw128(smem_u32(qk), 16, 1024), dkx = sdesc_sw128(smem_u32(qk + kTileBytes), 16, 1024);
                 const uint64_t dc = sdesc_sw128(smem_u32(coef), 16, 1024);
-                const uint64_t dgk = sdesc_sw128(smem_u32(gk), 16, 1024);               // K-major Gamma^K (N = 128 / 256)
+                const uint64_t dgk = sdesc_sw128(smem_u32(gk), 16, 1024);               // K-major Gamma^K hi (N = 128)
                 const uint64_t dgt = sdesc_sw128(smem_u32(gk), kTileBytes, 1024);       // MN-major Gamma^K^T (M = 128)
                 const uint64_t dso = sdesc_sw128(smem_u32(sop), 8192, 1024);            // MN-major state operand
                 const uint64_t dv = sdesc_sw128(smem_u32(vt), kTileBytes, 1024);        // MN-major [V | 1]
-                constexpr uint32_t i256 = idesc_bf16(kTile, 256, false, false), i128 = idesc_bf16(kTile, 128, false, false);
+                constexpr uint32_t i128 = idesc_bf16(kTile, 128, false, false);
                 constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
                 const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
                 for (int i = 0; coef_ok && i < n; ++i) {
                     const int r = rbase + i, ph = r & 1;
-                    // scores of the chunk (the Q scores overwrite the previous state increment,
-                    // so they wait for the carry that read it)
-                    if (!wait_or_abort(sready, ph, status, abort_flag)) break;
-                    if (!wait_or_abort(xq, ph, status, abort_flag)) break;
-                    tc_fence_after();
-                    issue_scores_tA(tmem + kSQ, tmem + kXQ, dq, dc);
-                    umma_commit(sq);
-                    if (!wait_or_abort(xk, ph, status, abort_flag)) break;
+                    // scores of the chunk (the key side is the longer path: first)
+                    if (!spin_wait(xk, ph, status, abort_flag)) break;
                     tc_fence_after();
                     issue_scores_tA(tmem + kSK, tmem + kXK, dkx, dc);
                     umma_commit(sk);
+                    if (!spin_wait(xq, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    issue_scores_tA(tmem + kSQ, tmem + kXQ, dq, dc);
+                    umma_commit(sq);
                     umma_commit(qkempty);
-                    // P = gQhi [gKhi | gKlo]^T + gQlo gKhi^T, and the read of the carried state
-                    if (!wait_or_abort(gq, ph, status, abort_flag)) break;
-                    if (!wait_or_abort(gkr, ph, status, abort_flag)) break;
+                    // P and the read of the carried state (after the previous chunk's carry)
+                    if (!spin_wait(gq, ph, status, abort_flag)) break;
+                    if (!spin_wait(gkr, ph, status, abort_flag)) break;
+                    if (!spin_wait(sready, ph, status, abort_flag)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kKP / 16; ++kk) {
-                        umma_bf16_tA(tmem + kPD, tmem + kXQ + kk * 8, dadd(dgk, kk * 32), i256, kk > 0 ? 1u : 0u);
-                        umma_bf16_tA(tmem + kPD, tmem + kXQ + 32 + kk * 8, dadd(dgk, kk * 32), i128, 1u);
+                        const uint32_t aq = tmem + kXQ + kk * 8;
+                        umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kk * 32), i128, kk > 0 ? 1u : 0u);
+                        umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kTileBytes + kk * 32), i128, 1u);
+                        umma_bf16_tA(tmem + kPD, aq + 32, dadd(dgk, kk * 32), i128, 1u);
                     }
 #pragma unroll
                     for (int kk = 0; kk < kKP / 16; ++kk) {
@@ -1128,9 +1275,17 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                         umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bl_, i80s, 1u);
                     }
                     umma_commit(pfull);
-                    // [num | den] += P [V | 1];  U = [gK_hi ; gK_lo]^T [V | 1]
-                    if (!wait_or_abort(pready, ph, status, abort_flag)) break;
-                    if (!wait_or_abort(vfull, ph, status, abort_flag)) break;
+                    // U = [gK_hi ; gK_lo]^T [V | 1] for the carry (not needed after the job's last chunk)
+                    if (!spin_wait(vfull, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    if (i + 1 < n) {
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(ufull);
+                    // [num | den] += P [V | 1]
+                    if (!spin_wait(pready, ph, status, abort_flag)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -1139,12 +1294,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                         umma_bf16_tA(tmem + kO, tmem + kXK + kk * 8, bv, i80s, 1u);
                     }
                     umma_commit(ofull);
-                    if (i + 1 < n) {
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(ufull);
                     umma_commit(vempty);
                 }
             }
@@ -1153,143 +1302,118 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             uint8_t *stage = stg + (warp & 3) * 8192;
-            for (int i = 0; i < n; ++i) {
+            float rq_prev = 0.f;
+            int i = 0;
+            for (; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                const int tok = (t0 + i) * kTile + row;
                 if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
-                prep_x2_row_tmem(qk, row, tmem + lb + kXQ);
+                if (i > 0 && !wait_or_abort(ofull, ph ^ 1, status, abort_flag)) break;  // P hi of chunk i-1 consumed
+                x2_row(qk, row, tmem + lb + kXQ);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xq);
+                // outputs of the previous chunk, beside this chunk's score MMAs
+                if (i > 0) {
+                    tc_fence_after();
+                    causal_output_row(tmem + lb + kO, rq_prev, eps, stage, lane, &tmO, o_bf16, (t0 + i - 1) * kTile + 32 * (warp & 3), bh);
+                }
                 if (!wait_or_abort(sq, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
-                float rq;
-                {
-                    float e[kKP];
-                    rq = score_row_exp128(tmem + lb + kSQ, cvec, e);
-                    uint32_t wh[32], wl[32];
-                    split_row(e, 1.0f, wh, wl);
-                    tmem_st32(tmem + lb + kXQ, wh);
-                    tmem_st32(tmem + lb + kXQ + 32, wl);
-                    tmem_wait_st();
-                }
+                rq_prev = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, row, 1);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gq);
-                // masked intra-chunk affinity -> P hi | lo as the A operand of P [V | 1]
+                // masked intra-chunk affinity, key blocks 0 and 1 -> P hi | lo
                 if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {  // keys 32 cb .. 32 cb + 31
-                    uint32_t p0[32], p1[32];
-                    tmem_ld32(tmem + lb + kPD + cb * 32, p0);
-                    tmem_ld32(tmem + lb + kPD + 128 + cb * 32, p1);
-                    tmem_wait_ld();
-                    uint32_t wh[16], wl[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int j = cb * 32 + 2 * q;
-                        const float2 pv = f2_add(make_float2(__uint_as_float(p0[2 * q]), __uint_as_float(p0[2 * q + 1])),
-                                                 make_float2(__uint_as_float(p1[2 * q]), __uint_as_float(p1[2 * q + 1])));
-                        const float a = j <= row ? pv.x : 0.f, b = j + 1 <= row ? pv.y : 0.f;
-                        wh[q] = pack_bf2(a, b);
-                        wl[q] = pack_bf2(a - bf_lo(wh[q]), b - bf_hi(wh[q]));
-                    }
-                    tmem_st16(tmem + lb + kXQ + cb * 16, wh);
-                    tmem_st16(tmem + lb + kXK + cb * 16, wl);
-                }
-                tmem_wait_st();
+                split_p_blocks(tmem + lb + kPD, tmem + lb + kXQ, tmem + lb + kXK, 0, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
-                // outputs
-                if (!wait_or_abort(ofull, ph, status, abort_flag)) break;
+            }
+            if (i == n && n > 0 && wait_or_abort(ofull, (rbase + n - 1) & 1, status, abort_flag)) {
+                // outputs of the job's last chunk
                 tc_fence_after();
-                float o[64];
-                {
-                    uint32_t a0[32], a1[32], dz[16];
-                    tmem_ld32(tmem + lb + kO, a0);
-                    tmem_ld32(tmem + lb + kO + 32, a1);
-                    tmem_ld16(tmem + lb + kO + 64, dz);
-                    tmem_wait_ld();
-                    const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rq);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        o[q] = __uint_as_float(a0[q]) * inv;
-                        o[32 + q] = __uint_as_float(a1[q]) * inv;
-                    }
-                }
-                tc_fence_before();
-                (void)tok;
-                stage_and_store_rows(stage, o, lane, lane, &tmO, o_bf16, (t0 + i) * kTile + 32 * (warp & 3), bh);
+                causal_output_row(tmem + lb + kO, rq_prev, eps, stage, lane, &tmO, o_bf16, (t0 + n - 1) * kTile + 32 * (warp & 3), bh);
             }
             if (lane == 0) bulk_wait0();
         } else {
             // ---------------- key group
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            // Carry split: U row `row` holds the hi-part sums of component k = row
+            // (row < 64) or the lo-part sums of k = row - 64.  Thread k keeps
+            // columns 0..31 of its row and hands 32..64 over through X; thread
+            // 64 + k keeps 32..64 and hands over 0..31.  Each then adds both parts
+            // to S for the columns it kept and writes that half of the state operand.
+            const int kc = row & (kKP - 1), half = row >> 6;
+            float keep[33];
             for (int i = 0; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
                 if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
-                prep_x2_row_tmem(qk + kTileBytes, row, tmem + lb + kXK);
+                if (i > 0 && !wait_or_abort(ofull, ph ^ 1, status, abort_flag)) break;  // P lo of chunk i-1 consumed
+                x2_row(qk + kTileBytes, row, tmem + lb + kXK);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xk);
-                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
-                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
-                tc_fence_after();
-                {
-                    float e[kKP];
-                    const float rk = score_row_exp128(tmem + lb + kSK, cvec, e);
-                    tc_fence_before();
-                    const int tok = (t0 + i) * kTile + row;
-                    uint32_t wh[32], wl[32];
-                    split_row(e, tok < N ? 1.0f / rk : 0.0f, wh, wl);
-                    // Gamma^K rows: hi block then lo block, 128-byte rows, 8-row groups of 1 KB
-                    uint8_t *hi = gk + row * 128, *lo = gk + kTileBytes + row * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint32_t sw = (uint32_t)((cc ^ (row & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(hi + sw) = make_uint4(wh[4 * cc], wh[4 * cc + 1], wh[4 * cc + 2], wh[4 * cc + 3]);
-                        *reinterpret_cast<uint4 *>(lo + sw) = make_uint4(wl[4 * cc], wl[4 * cc + 1], wl[4 * cc + 2], wl[4 * cc + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(gkr);
-                // carry: S += U_hi + U_lo, then the state operand of the next chunk
-                if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
-                if (i + 1 < n) {
-                    tc_fence_after();
-                    float u[W];
-                    {
-                        uint32_t a0[32], a1[32], z[16];
-                        tmem_ld32(tmem + lb + kU, a0);
-                        tmem_ld32(tmem + lb + kU + 32, a1);
-                        tmem_ld16(tmem + lb + kU + 64, z);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            u[q] = __uint_as_float(a0[q]);
-                            u[32 + q] = __uint_as_float(a1[q]);
-                        }
-                        u[64] = __uint_as_float(z[0]);
-                    }
-                    tc_fence_before();
-                    if (row >= kKP)
-#pragma unroll
-                        for (int q = 0; q < W; ++q) X[(row - kKP) * W + q] = u[q];
+                if (i > 0) {  // finish the carry of chunk i-1: state operand of chunk i
                     asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (row < kKP) {
-                        float *sr = S + row * W;
+                    float *sr = S + kc * W;
+                    const float *xr = X + kc * W;
 #pragma unroll
-                        for (int q = 0; q < W; ++q) sr[q] += u[q] + X[row * W + q];
-                        store_state_row(sop, row, sr);
+                    for (int q = 0; q < 33; ++q) {
+                        const int col = 32 * half + q;
+                        if (q < 32 || half) sr[col] += keep[q] + xr[col];
                     }
+                    store_state_half(sop, kc, sr, half);
                     fence_proxy_async_smem();
                     asm volatile("bar.sync 1, 128;" ::: "memory");
                     if (lane == 0) mbar_arrive(sready);
+                }
+                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
+                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
+                tc_fence_after();
+                gamma_row(tmem + lb + kSK, cvec, 1, 0u, gk, row, (t0 + i) * kTile + row < N ? 1 : 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gkr);
+                // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo
+                if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
+                tc_fence_after();
+                split_p_blocks(tmem + lb + kPD, tmem + lb + kXQ, tmem + lb + kXK, 2, row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pready);
+                // first half of the carry: U out of tensor memory (its columns are the
+                // next chunk's key scores), the partner's columns into X (over Gamma^K,
+                // which P and U have consumed)
+                if (i + 1 < n) {
+                    if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    uint32_t a0[32], a1[32], z[16];
+                    tmem_ld32(tmem + lb + kU, a0);
+                    tmem_ld32(tmem + lb + kU + 32, a1);
+                    tmem_ld16(tmem + lb + kU + 64, z);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    float *xr = X + kc * W;
+                    if (half == 0) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            keep[q] = __uint_as_float(a0[q]);
+                            xr[32 + q] = __uint_as_float(a1[q]);
+                        }
+                        xr[64] = __uint_as_float(z[0]);
+                        keep[32] = 0.f;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            keep[q] = __uint_as_float(a1[q]);
+                            xr[q] = __uint_as_float(a0[q]);
+                        }
+                        keep[32] = __uint_as_float(z[0]);
+                    }
                 }
             }
         }

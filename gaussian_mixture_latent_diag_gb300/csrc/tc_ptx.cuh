@@ -65,8 +65,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // wait gives up and returns false, and the caller records GMA_ERR_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The polling loop is kept out of line: waits are inlined at many call
+// sites, and one shared copy of the slow path keeps the kernels' hot code
+// small (instruction fetch is a bottleneck of the persistent kernels).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
     while (true) {
 #pragma unroll 1
@@ -74,6 +76,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer() - t0 > kWaitLimitNs) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity);
 }
 
 // ------------------------------------------------------------------ fences
