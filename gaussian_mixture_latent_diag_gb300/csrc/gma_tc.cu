@@ -239,7 +239,8 @@ __device__ __forceinline__ bool aborted(const int *abort_flag) {
 }
 // Wait by polling (no suspension between probes), for the single MMA-issuing
 // thread whose wake-up latency is on the critical path; bounded like mbar_wait.
-__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
+// The polling loop is out of line (one copy for all call sites).
+__device__ __noinline__ bool spin_wait_slow(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
     Stall st;
     while (!mbar_test(bar, parity)) {
         if (!st.tick(false, abort_flag)) {
@@ -248,6 +249,9 @@ __device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsign
         }
     }
     return true;
+}
+__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
+    return mbar_test(bar, parity) || spin_wait_slow(bar, parity, status, abort_flag);
 }
 
 // Row of the tile / TMEM lane handled by an epilogue thread (warp w may only
@@ -309,6 +313,10 @@ __device__ __forceinline__ void issue_scores_tA(uint32_t d_tmem, uint32_t a_tmem
         umma_bf16(d_tmem, dadd(dx, o), dadd(dc, 2 * kCoefMatBytes + o), i128, 1u);
         umma_bf16_tA(d_tmem, a_tmem + 32 + kk * 8, dadd(dc, o), i64, 1u);
     }
+}
+
+__device__ __noinline__ void issue_scores_ool(uint32_t d_tmem, uint32_t a_tmem, uint64_t dx, uint64_t dc) {
+    issue_scores_tA(d_tmem, a_tmem, dx, dc);
 }
 
 // Score row (two 64-column halves in TMEM) -> exponentials e_k = 2^(s_k - max);
@@ -1248,11 +1256,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     // scores of the chunk (the key side is the longer path: first)
                     if (!spin_wait(xk, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    issue_scores_tA(tmem + kSK, tmem + kXK, dkx, dc);
+                    issue_scores_ool(tmem + kSK, tmem + kXK, dkx, dc);
                     umma_commit(sk);
                     if (!spin_wait(xq, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    issue_scores_tA(tmem + kSQ, tmem + kXQ, dq, dc);
+                    issue_scores_ool(tmem + kSQ, tmem + kXQ, dq, dc);
                     umma_commit(sq);
                     umma_commit(qkempty);
                     // P and the read of the carried state (after the previous chunk's carry)
@@ -1260,14 +1268,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     if (!spin_wait(gkr, ph, status, abort_flag)) break;
                     if (!spin_wait(sready, ph, status, abort_flag)) break;
                     tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                     for (int kk = 0; kk < kKP / 16; ++kk) {
                         const uint32_t aq = tmem + kXQ + kk * 8;
                         umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kk * 32), i128, kk > 0 ? 1u : 0u);
                         umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kTileBytes + kk * 32), i128, 1u);
                         umma_bf16_tA(tmem + kPD, aq + 32, dadd(dgk, kk * 32), i128, 1u);
                     }
-#pragma unroll
+#pragma unroll 1
                     for (int kk = 0; kk < kKP / 16; ++kk) {
                         const uint64_t bh_ = dadd(dso, kk * 2048), bl_ = dadd(dso, 16384 + kk * 2048);
                         umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bh_, i80s, kk > 0 ? 1u : 0u);
@@ -1279,7 +1287,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     if (!spin_wait(vfull, ph, status, abort_flag)) break;
                     tc_fence_after();
                     if (i + 1 < n) {
-#pragma unroll
+#pragma unroll 1
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
                     }
@@ -1287,7 +1295,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     // [num | den] += P [V | 1]
                     if (!spin_wait(pready, ph, status, abort_flag)) break;
                     tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                     for (int kk = 0; kk < kTile / 16; ++kk) {
                         const uint64_t bv = dadd(dv, kk * 2048);
                         umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bv, i80s, 1u);
