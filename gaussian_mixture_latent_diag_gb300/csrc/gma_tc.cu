@@ -17,7 +17,7 @@
 //
 // Kernels:  coef_prep_tc_kernel (per-head split coefficients), then the
 // persistent, warp-specialised tc_write2_kernel (key side: latent memory per
-// job, combined per head by the last job), tc_read2_kernel (bidirectional
+// job, combined per head by the last job), tc_read3_kernel (bidirectional
 // query side) and tc_causal2_kernel (causal chunked scan).
 //
 // Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
@@ -46,6 +46,9 @@ constexpr int kCoefBytes = 4 * kCoefMatBytes + kKP * 4;  // a_hi | a_lo | b_hi |
 constexpr size_t kCoefStride = (kCoefBytes + 1023) & ~1023;
 constexpr int kGS = 2 * (kKP / 64) * 1024;               // Gamma buffer: bytes per 8-token group
 constexpr float kLog2e = 1.4426950408889634f;
+// Row stride (floats) of a job partial / causal state [KP][kW]: 64 values of
+// Gamma^T V, then Z = Gamma^T 1, then 3 zero pads (rows stay 16-byte aligned).
+constexpr int kW = 68;
 
 __device__ __forceinline__ bool failed(const unsigned *status) {
     return *reinterpret_cast<const volatile unsigned *>(status) != 0u;
@@ -60,23 +63,69 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
 }
 
 // ------------------------------------------------------------------ coefficient prep
-// One block per head.  Writes the four bf16 coefficient matrices in the
-// K-major SW128 byte image the score MMA reads (rows = components, 128 B of
-// d_r per row), plus c_k (fp32, -inf for padded components).  Validates the
-// parameters into the head's error word.  It is the first kernel of a call, so
-// it also clears the call's status word and the per-head job counters.
-__device__ bool build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
-                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, int tid, int nthreads);
+// Grid (KP / 8, H): block (b, h) writes components 8b .. 8b + 7 of head h's
+// coefficient image -- the four bf16 matrices in the K-major SW128 byte image
+// the score MMA reads (rows = components, 128 B of d_r per row) and c_k (fp32,
+// -inf for padded components) -- and validates their parameters into its
+// error word err[h * (KP / 8) + b].  Each thread handles four consecutive j of
+// one component; the 16 threads of a component (one half-warp) also sum its
+// log-determinant terms.  Being the first kernel of a call, it also clears the
+// call's status word and the per-head job counters.
+constexpr int kPrepBlocks = kKP / 8;
 
-__global__ void coef_prep_tc_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
-                                    const float *__restrict__ log_pi, int K, uint8_t *__restrict__ img,
-                                    unsigned *status, unsigned *head_err, unsigned *counters, int BH) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < BH; i += gridDim.x * blockDim.x) counters[i] = 0u;
-    const bool bad = build_coef_smem(mu, sigma2, log_pi, blockIdx.x, K, img + (size_t)blockIdx.x * kCoefStride,
-                                     threadIdx.x, blockDim.x);
+__global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restrict__ mu,
+                                                           const float *__restrict__ sigma2,
+                                                           const float *__restrict__ log_pi, int K,
+                                                           uint8_t *__restrict__ img, unsigned *status,
+                                                           unsigned *head_err, unsigned *counters, int BH) {
+    const int tid = threadIdx.x, h = blockIdx.y;
+    const int gt = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + tid;
+    if (gt == 0) *status = 0u;
+    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
+    uint8_t *coef = img + (size_t)h * kCoefStride;
+    const int k = blockIdx.x * 8 + (tid >> 4), j = (tid & 15) * 4;
+    const bool real = k < K;
+    float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lp = 0.f;
+    if (real) {
+        s4 = *reinterpret_cast<const float4 *>(sigma2 + ((size_t)h * K + k) * kDR + j);
+        m4 = *reinterpret_cast<const float4 *>(mu + ((size_t)h * K + k) * kDR + j);
+        lp = log_pi[(size_t)h * K + k];
+    }
+    const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, mv[4] = {m4.x, m4.y, m4.z, m4.w};
+    bool bad = false;
+    uint32_t ah[2], al[2], bh[2], bl[2];
+    float det = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        float a[2], b[2];
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const float s2 = sv[2 * u + v], m = mv[2 * u + v];
+            if (real && (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m))) bad = true;
+            const float inv = real ? __frcp_rn(s2) : 0.f;
+            a[v] = (-0.5f * kLog2e) * inv;
+            b[v] = (kLog2e * m) * inv;
+            det += real ? m * m * inv + __logf(s2) : 0.f;
+        }
+        ah[u] = pack_bf2(a[0], a[1]);
+        al[u] = pack_bf2(a[0] - bf_lo(ah[u]), a[1] - bf_hi(ah[u]));
+        bh[u] = pack_bf2(b[0], b[1]);
+        bl[u] = pack_bf2(b[0] - bf_lo(bh[u]), b[1] - bf_hi(bh[u]));
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) det += __shfl_xor_sync(0xffffffffu, det, o);
+    const uint32_t off = sw128_offset(k, j, 1024);  // 8-byte aligned (j % 4 == 0)
+    *reinterpret_cast<uint2 *>(coef + off) = make_uint2(ah[0], ah[1]);
+    *reinterpret_cast<uint2 *>(coef + kCoefMatBytes + off) = make_uint2(al[0], al[1]);
+    *reinterpret_cast<uint2 *>(coef + 2 * kCoefMatBytes + off) = make_uint2(bh[0], bh[1]);
+    *reinterpret_cast<uint2 *>(coef + 3 * kCoefMatBytes + off) = make_uint2(bl[0], bl[1]);
+    if (j == 0) {
+        if (real && !isfinite(lp)) bad = true;
+        reinterpret_cast<float *>(coef + 4 * kCoefMatBytes)[k] = real ? kLog2e * (lp - 0.5f * det) : -INFINITY;
+    }
     const int any = __syncthreads_or(bad ? 1 : 0);
-    if (threadIdx.x == 0) head_err[blockIdx.x] = any ? (unsigned)GMA_ERR_NONFINITE_PARAM : 0u;
+    if (tid == 0) head_err[h * kPrepBlocks + blockIdx.x] = any ? (unsigned)GMA_ERR_NONFINITE_PARAM : 0u;
 }
 
 // ------------------------------------------------------------------ shared pieces
@@ -123,90 +172,14 @@ __host__ __device__ inline int last_cta_of_head(const Part &P, int bh) {
 // Slot of head bh's job inside CTA c (CTA c's range starts in head (c*tpc)/ntiles).
 __host__ __device__ inline int slot_of(const Part &P, int c, int bh) { return bh - (c * P.tpc) / P.ntiles; }
 
-// Coefficient image of head h (K-major SW128 bf16 a_hi | a_lo | b_hi | b_lo,
-// then c_k) written through a generic pointer -- shared memory inside the
-// persistent kernels, global memory for coef_prep_tc_kernel -- by every
-// thread of the block.
-__device__ bool build_coef_smem(const float *__restrict__ mu, const float *__restrict__ sigma2,
-                                const float *__restrict__ log_pi, int h, int K, uint8_t *coef, int tid, int nthreads) {
-    bool bad = false;
-    // Four consecutive j of one component per step: float4 loads, issued for
-    // all of a thread's steps before any store, then 8-byte stores (the four
-    // bf16 values share one 16-byte chunk of the swizzled row).  With
-    // nthreads a multiple of 32, the 16 steps of one component sit in one
-    // half-warp, which also sums that component's log-determinant terms.
-    constexpr int kSteps = (kKP * kDR / 4 + 127) / 128;  // per thread, for >= 128 threads
-    float4 s4[kSteps], m4[kSteps];
-    float lp[kSteps];
-#pragma unroll
-    for (int q = 0; q < kSteps; ++q) {
-        const int e4 = tid + q * nthreads;  // index of a group of 4 elements
-        const int k = (e4 * 4) / kDR, j = (e4 * 4) % kDR;
-        s4[q] = make_float4(1.f, 1.f, 1.f, 1.f);
-        m4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        lp[q] = 0.f;
-        if (e4 * 4 < kKP * kDR && k < K) {
-            s4[q] = *reinterpret_cast<const float4 *>(sigma2 + ((size_t)h * K + k) * kDR + j);
-            m4[q] = *reinterpret_cast<const float4 *>(mu + ((size_t)h * K + k) * kDR + j);
-            lp[q] = log_pi[(size_t)h * K + k];
-        }
-    }
-    float *cvec = reinterpret_cast<float *>(coef + 4 * kCoefMatBytes);
-#pragma unroll
-    for (int q = 0; q < kSteps; ++q) {
-        const int e4 = tid + q * nthreads;
-        if (q * nthreads >= kKP * kDR / 4) break;  // uniform across the warp
-        const bool live = e4 * 4 < kKP * kDR;
-        const int k = (e4 * 4) / kDR, j = (e4 * 4) % kDR;
-        const float sv[4] = {s4[q].x, s4[q].y, s4[q].z, s4[q].w}, mv[4] = {m4[q].x, m4[q].y, m4[q].z, m4[q].w};
-        uint32_t ah[2], al[2], bh[2], bl[2];
-        float det = 0.f;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            float a[2], b[2];
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-                const float s2 = sv[2 * u + v], m = mv[2 * u + v];
-                const bool real = live && k < K;
-                if (real && (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m))) bad = true;
-                const float inv = real ? __frcp_rn(s2) : 0.f;
-                a[v] = (-0.5f * kLog2e) * inv;
-                b[v] = (kLog2e * m) * inv;
-                det += real ? m * m * inv + __logf(s2) : 0.f;
-            }
-            ah[u] = pack_bf2(a[0], a[1]);
-            al[u] = pack_bf2(a[0] - bf_lo(ah[u]), a[1] - bf_hi(ah[u]));
-            bh[u] = pack_bf2(b[0], b[1]);
-            bl[u] = pack_bf2(b[0] - bf_lo(bh[u]), b[1] - bf_hi(bh[u]));
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) det += __shfl_xor_sync(0xffffffffu, det, o);
-        if (!live) continue;
-        const uint32_t off = sw128_offset(k, j, 1024);  // 8-byte aligned (j % 4 == 0)
-        *reinterpret_cast<uint2 *>(coef + off) = make_uint2(ah[0], ah[1]);
-        *reinterpret_cast<uint2 *>(coef + kCoefMatBytes + off) = make_uint2(al[0], al[1]);
-        *reinterpret_cast<uint2 *>(coef + 2 * kCoefMatBytes + off) = make_uint2(bh[0], bh[1]);
-        *reinterpret_cast<uint2 *>(coef + 3 * kCoefMatBytes + off) = make_uint2(bl[0], bl[1]);
-        if (j == 0) {
-            if (k < K) {
-                if (!isfinite(lp[q])) bad = true;
-                cvec[k] = kLog2e * (lp[q] - 0.5f * det);
-            } else {
-                cvec[k] = -INFINITY;
-            }
-        }
-    }
-    return bad;
-}
 
-// Head-error check of the first persistent kernel of a call: any head whose
-// parameters failed validation fails the call.  Returns the first error word.
-__device__ __forceinline__ unsigned first_head_error(const unsigned *head_err, int H) {
-    for (int h = 0; h < H; ++h) {
-        const unsigned e = __ldcg(head_err + h);
-        if (e) return e;
-    }
-    return 0u;
+// Parameter-error check of the first persistent kernel of a call, by one
+// whole warp: any coefficient-prep block that failed validation fails the
+// call.  Returns the OR of the error words (all of them carry the same code).
+__device__ __forceinline__ unsigned head_error_warp(const unsigned *head_err, int H, int lane) {
+    unsigned e = 0u;
+    for (int i = lane; i < H * kPrepBlocks; i += 32) e |= __ldcg(head_err + i);
+    return __reduce_or_sync(0xffffffffu, e);
 }
 
 // Bounded polling: tick(progressed) returns false once kWaitLimitNs pass
@@ -236,6 +209,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, un
 }
 __device__ __forceinline__ bool aborted(const int *abort_flag) {
     return *reinterpret_cast<const volatile int *>(abort_flag) != 0;
+}
+// CTA and named barriers of the warp-specialised kernels.  Roles run long
+// single-lane loops (the TMA and MMA threads, the last store wait of an
+// epilogue warp), and the barrier instructions expect whole warps: each warp
+// reconverges first.
+__device__ __forceinline__ void cta_sync() {
+    __syncwarp();
+    __syncthreads();
+}
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 // Wait by polling (no suspension between probes), for the single MMA-issuing
 // thread whose wake-up latency is on the critical path; bounded like mbar_wait.
@@ -386,15 +371,15 @@ __device__ __forceinline__ void store_gamma_words(uint8_t *gbuf, int t, const ui
     }
 }
 
-// Combines the job partials ([KP][d_v + 1] fp32 each) of head bh in CTA
+// Combines the job partials ([KP][kW] fp32 each) of head bh in CTA
 // order, so the result does not depend on which job finished last:
 //   mode 0: out (shared memory) = sum of the partials,
 //   mode 1: each partial replaced in place by the sum of the ones before it.
 // Each thread keeps 2 vectors x 8 CTAs of loads in flight.
 __device__ void combine_partials(float *__restrict__ part, const Part &P, int bh, int mode, float *out, int tid,
                                  int nthreads) {
-    constexpr int kE4 = kKP * (64 + 1) / 4;
-    constexpr size_t kPS = (size_t)kKP * (64 + 1);
+    constexpr int kE4 = kKP * kW / 4;
+    constexpr size_t kPS = (size_t)kKP * kW;
     const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
     for (int e0 = tid; e0 < kE4; e0 += 2 * nthreads) {
         float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
@@ -445,7 +430,7 @@ __device__ void combine_partials(float *__restrict__ part, const Part &P, int bh
 // the ones chunk, so one N = 80 MMA gives Gamma^T V (columns 0..63) and
 // Gamma^T 1 (column 64).
 struct Write2Smem {
-    static constexpr int W = 64 + 1;
+    static constexpr int W = kW;
     static constexpr int kKS = 4, kVS = 3;                      // K / V ring depths
     static constexpr int kKst = 0;                              // K stages
     static constexpr int kVst = kKst + kKS * kTileBytes;        // V stages
@@ -499,6 +484,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    const unsigned herr = warp == 1 ? head_error_warp(head_err, H, lane) : 0u;
     if (tid == 32) {
         for (int i = 0; i < KS; ++i) {
             mbar_init(&kfull[i], 1);
@@ -516,9 +502,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         }
         mbar_init(accfull, 1);
         mbar_init(cfull, 1);
-        const unsigned e = first_head_error(head_err, H);
-        if (e) set_status(status, e);
-        *abort_flag = e ? 1 : 0;
+        if (herr) set_status(status, herr);
+        *abort_flag = herr ? 1 : 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -528,7 +513,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         for (int i = tid; i < kTileBytes / 16; i += kThreadsG) reinterpret_cast<uint4 *>(smem + L::kOnes)[i] = one4;
     }
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t idesc_w = idesc_bf16(kTile, 80, true, true);
@@ -542,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         // The previous job's reads of the coefficients and its generic writes over
         // the K ring are complete; the head's coefficients arrive on cfull.
         fence_proxy_async_smem();
-        __syncthreads();
+        cta_sync();
         if (tid == 0) {
             mbar_arrive_expect_tx(cfull, kCoefBytes);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
@@ -656,7 +641,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
             }
         }
         // ---- job end: the accumulated memory -> partial of this job
-        __syncthreads();
+        cta_sync();
         float *red = reinterpret_cast<float *>(smem);  // [128][W] over the (now idle) tile buffers
         if (!aborted(abort_flag) && warp >= 2 && warp < 6) {  // group 0 covers all 128 lanes
             if (wait_or_abort(accfull, njob & 1, status, abort_flag)) {
@@ -668,33 +653,39 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
                 tmem_ld32(tmem + lb + kAcc + 32, v1);
                 tmem_ld16(tmem + lb + kAcc + 64, z);
                 tmem_wait_ld();
+                float4 *rr = reinterpret_cast<float4 *>(red + row * W);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    red[row * W + q] = __uint_as_float(v0[q]);
-                    red[row * W + 32 + q] = __uint_as_float(v1[q]);
+                for (int q = 0; q < 8; ++q) {
+                    rr[q] = make_float4(__uint_as_float(v0[4 * q]), __uint_as_float(v0[4 * q + 1]),
+                                        __uint_as_float(v0[4 * q + 2]), __uint_as_float(v0[4 * q + 3]));
+                    rr[8 + q] = make_float4(__uint_as_float(v1[4 * q]), __uint_as_float(v1[4 * q + 1]),
+                                            __uint_as_float(v1[4 * q + 2]), __uint_as_float(v1[4 * q + 3]));
                 }
-                red[row * W + D_V] = __uint_as_float(z[0]);
+                rr[16] = make_float4(__uint_as_float(z[0]), 0.f, 0.f, 0.f);
                 tc_fence_before();
             }
         }
-        __syncthreads();
+        cta_sync();
         if (!aborted(abort_flag)) {
             const int slot = slot_of(P, c, bh);
             float *out = part + ((size_t)c * P.slots + slot) * kKP * W;
-            for (int e = tid; e < kKP * W; e += kThreadsG) out[e] = red[e] + red[kKP * W + e];
+            for (int e = tid; e < kKP * W / 4; e += kThreadsG) {
+                const float4 a = reinterpret_cast<const float4 *>(red)[e], b = reinterpret_cast<const float4 *>(red + kKP * W)[e];
+                reinterpret_cast<float4 *>(out)[e] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+            }
             __threadfence();
-            __syncthreads();
+            cta_sync();
             if (tid == 0) {
                 const int njobs = last_cta_of_head(P, bh) - first_cta_of_head(P, bh) + 1;
                 const unsigned old = atomicAdd(&counters[bh], 1u);
                 *last_flag = (old == (unsigned)(njobs - 1));
             }
-            __syncthreads();
+            cta_sync();
             if (*last_flag) {
                 __threadfence();
                 combine_partials(part, P, bh, mode, red, tid, kThreadsG);
                 if (mode == 0) {
-                    __syncthreads();
+                    cta_sync();
                     store_memory_operand<D_V>(red, W, mem_img + (size_t)bh * mem_img_stride, tid, kThreadsG);
                 }
                 if (tid == 0) counters[bh] = 0u;  // ready for the next call
@@ -705,7 +696,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         if (aborted(abort_flag)) break;
     }
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -744,44 +735,151 @@ __device__ __forceinline__ void stage_and_store_rows(uint8_t *stage, const float
     }
 }
 
-struct Read2Smem {
+// ------------------------------------------------------------------ read, split rows
+//
+// Bidirectional read with the epilogue rows split in column halves: two groups
+// of 8 warps; warps w and w + 4 of a group share TMEM lanes 32 (w % 4) .. +31
+// (the tile rows) and take components (or output columns) 0..31 (half 0) and
+// 32..63 (half 1).  Twice the warps of a 4-warp group run the same code with
+// half the per-thread work, which hides more latency per tile.
+constexpr int kNGR = 2;
+constexpr int kThreadsR = 64 + 256 * kNGR;
+
+struct Read3Smem {
     static constexpr int NB = 64 + 16;
-    static constexpr int kQS = 4;  // Q ring depth (freed once the score MMAs complete)
+    static constexpr int kQS = 4;                                   // Q ring depth
     static constexpr int kQst = 0;
-    static constexpr int kStage = kQst + kQS * kTileBytes;        // [NG groups][4 warps][8 KB]
-    static constexpr int kCoef = kStage + kNG * 4 * 8192;
+    static constexpr int kStage = kQst + kQS * kTileBytes;          // output staging [NGR][8 warps][4 KB]
+    static constexpr int kCoef = kStage + kNGR * 8 * 4096;
     static constexpr int kB = kCoef + ((kCoefBytes + 1023) & ~1023);
-    static constexpr int kBars = kB + ((2 * NB * 128 + 1023) & ~1023);
+    static constexpr int kX = kB + ((2 * NB * 128 + 1023) & ~1023);  // (max, sum) exchange [NGR][2][128][2]
+    static constexpr int kBars = kX + kNGR * 2 * 128 * 2 * 8;
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-// Normalised broadcasting ([GMA, Eq. (7)]) over each job's query tiles (d_v = 64).
-// Read MMAs, 8 per tile (4 K-steps x 2), with the memory operand stored as one
-// N = 160 K-major matrix [B_hi ; B_lo]:
-//   D[:, 0:160] = Ghi [B_hi | B_lo] ,  D[:, 0:80] += Glo B_hi ,
-// so [num | den] = D[:, 0:80] + D[:, 80:160].
-// TMEM, group g at [224 g, +224): operand area [+0, +64) (x^2 for the scores,
-// then Gamma^Q hi | lo); scores [+64, +192), then D over [+64, +224) once the
-// scores have been consumed.
-__global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
+// x^2 split of columns 32 hf .. 32 hf + 31 of this thread's row of a swizzled
+// [128 x 64] bf16 tile, to the TMEM A operand at taddr (x2hi columns
+// [16 hf, +16), x2lo columns [32 + 16 hf, +16)).
+__device__ __forceinline__ void prep_x2_half_tmem(const uint8_t *x, int row, int hf, uint32_t taddr) {
+    uint32_t h[16], l[16];
+    const uint8_t *rp = x + row * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(rp + (((4 * hf + c) ^ (row & 7)) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            h[4 * c + q] = bf2_fma(w[q], w[q], 0x80008000u);
+            l[4 * c + q] = bf2_fma(w[q], w[q], h[4 * c + q] ^ 0x80008000u);
+        }
+    }
+    tmem_st16(taddr + 16 * hf, h);
+    tmem_st16(taddr + 32 + 16 * hf, l);
+    tmem_wait_st();
+}
+
+// Scores of components 32 hf .. 32 hf + 31 of this thread's row (the two
+// 64-column halves of the score accumulator plus c_k); returns their maximum.
+__device__ __forceinline__ float score_half(uint32_t s_taddr, const float *cvec, int hf, float (&e)[32]) {
+    uint32_t a[32], b[32];
+    tmem_ld32(s_taddr + 32 * hf, a);
+    tmem_ld32(s_taddr + 64 + 32 * hf, b);
+    tmem_wait_ld();
+    const float4 *c4 = reinterpret_cast<const float4 *>(cvec + 32 * hf);
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 c = c4[q];
+        const float2 s0 = f2_add(f2_add(make_float2(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1])),
+                                        make_float2(__uint_as_float(b[4 * q]), __uint_as_float(b[4 * q + 1]))),
+                                 make_float2(c.x, c.y));
+        const float2 s1 = f2_add(f2_add(make_float2(__uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3])),
+                                        make_float2(__uint_as_float(b[4 * q + 2]), __uint_as_float(b[4 * q + 3]))),
+                                 make_float2(c.z, c.w));
+        e[4 * q] = s0.x; e[4 * q + 1] = s0.y; e[4 * q + 2] = s1.x; e[4 * q + 3] = s1.y;
+        m0 = fmaxf(m0, fmaxf(s0.x, s0.y));
+        m1 = fmaxf(m1, fmaxf(s1.x, s1.y));
+    }
+    return fmaxf(m0, m1);
+}
+
+// e <- 2^(e - m); returns the sum.
+__device__ __forceinline__ float exp_half(float (&e)[32], float m) {
+    const float2 mm = make_float2(m, m);
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+        const float2 d0 = f2_sub(make_float2(e[k], e[k + 1]), mm), d1 = f2_sub(make_float2(e[k + 2], e[k + 3]), mm);
+        e[k] = ex2(d0.x); e[k + 1] = ex2(d0.y); e[k + 2] = ex2(d1.x); e[k + 3] = ex2(d1.y);
+        s0 = f2_add(s0, make_float2(e[k], e[k + 1]));
+        s1 = f2_add(s1, make_float2(e[k + 2], e[k + 3]));
+    }
+    return (s0.x + s0.y) + (s1.x + s1.y);
+}
+
+// bf16 hi / lo words of 32 values scaled by `scale`.
+__device__ __forceinline__ void split_half(const float (&e)[32], float scale, uint32_t (&wh)[16], uint32_t (&wl)[16]) {
+    const float2 sc = make_float2(scale, scale);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float2 g = f2_mul(make_float2(e[2 * q], e[2 * q + 1]), sc);
+        wh[q] = pack_bf2(g.x, g.y);
+        const float2 r = f2_sub(g, make_float2(bf_lo(wh[q]), bf_hi(wh[q])));
+        wl[q] = pack_bf2(r.x, r.y);
+    }
+}
+
+// Output staging of one warp's 32 rows x 32 columns (4 KB): fp32 as one
+// [32 x 128 B] box with 128-byte swizzle, bf16 as one [32 x 64 B] box with
+// 64-byte swizzle.  The box is stored at column 32 hf.
+__device__ __forceinline__ void stage_and_store_half(uint8_t *stage, const float (&o)[32], int r32, int lane,
+                                                     const CUtensorMap *tmO, int o_bf16, int hf, int row0, int bh) {
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    if (o_bf16) {
+        uint8_t *rp = stage + r32 * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 w = make_uint4(pack_bf2(o[8 * c], o[8 * c + 1]), pack_bf2(o[8 * c + 2], o[8 * c + 3]),
+                                       pack_bf2(o[8 * c + 4], o[8 * c + 5]), pack_bf2(o[8 * c + 6], o[8 * c + 7]));
+            *reinterpret_cast<uint4 *>(rp + ((c ^ ((r32 >> 1) & 3)) << 4)) = w;
+        }
+    } else {
+        uint8_t *rp = stage + r32 * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4 *>(rp + ((c ^ (r32 & 7)) << 4)) =
+                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmO, stage, 32 * hf, row0, bh);
+        bulk_commit();
+    }
+}
+
+__global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
     const uint8_t *__restrict__ coef_img, int H, int N, Part P,
     const uint8_t *__restrict__ mem_img, size_t mem_img_stride, float eps, int o_bf16, unsigned *status) {
-    using L = Read2Smem;
+    using L = Read3Smem;
     constexpr int NB = L::NB, QS = L::kQS;
     constexpr int kTmemCols = 512;
     constexpr int kGC = kKP + 2 * NB;  // TMEM columns per group
-    static_assert(kNG * kGC <= kTmemCols, "TMEM budget");
+    static_assert(kNGR * kGC <= kTmemCols, "TMEM budget");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qst = smem + L::kQst, *stg = smem + L::kStage, *coef = smem + L::kCoef, *bop = smem + L::kB;
+    float2 *xch = reinterpret_cast<float2 *>(smem + L::kX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + kNG,
-             *gready = sfull + kNG, *ofull = gready + kNG, *cfull = ofull + kNG;
+    uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + kNGR,
+             *gready = sfull + kNGR, *ofull = gready + kNGR, *cfull = ofull + kNGR;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cfull + 1);
     int *abort_flag = reinterpret_cast<int *>(cfull + 2);
-    static_assert((2 * QS + 4 * kNG + 3) * 8 <= 256, "barrier area");
+    static_assert((2 * QS + 4 * kNGR + 3) * 8 <= 256, "barrier area");
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -798,10 +896,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], 1);
         }
-        for (int i = 0; i < kNG; ++i) {
-            mbar_init(&xready[i], 4);
+        for (int i = 0; i < kNGR; ++i) {
+            mbar_init(&xready[i], 8);
             mbar_init(&sfull[i], 1);
-            mbar_init(&gready[i], 4);
+            mbar_init(&gready[i], 8);
             mbar_init(&ofull[i], 1);
         }
         mbar_init(cfull, 1);
@@ -811,7 +909,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
         tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t i160 = idesc_bf16(kTile, 2 * NB, false, false);
@@ -824,7 +922,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
         const int h = bh % H;
         // The previous job's MMAs and epilogues are done with the coefficients
         // and the memory operand; this head's arrive on cfull.
-        __syncthreads();
+        cta_sync();
         if (tid == 0) {
             mbar_arrive_expect_tx(cfull, kCoefBytes + 2 * NB * 128);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
@@ -849,8 +947,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
                 while (coef_ok && nr < n) {
                     bool prog = false;
                     if (ns < n) {
-                        const int r = rbase + ns, gb = r % kNG, s = r % QS;
-                        if (mbar_test(&xready[gb], (r / kNG) & 1)) {
+                        const int r = rbase + ns, gb = r % kNGR, s = r % QS;
+                        if (mbar_test(&xready[gb], (r / kNGR) & 1)) {
                             tc_fence_after();
                             issue_scores_tA(tmem + gb * kGC + kKP, tmem + gb * kGC, dadd(dq0, s * kTileBytes), dc0);
                             umma_commit(&sfull[gb]);
@@ -860,8 +958,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
                         }
                     }
                     if (nr < ns) {
-                        const int r = rbase + nr, gb = r % kNG;
-                        if (mbar_test(&gready[gb], (r / kNG) & 1)) {
+                        const int r = rbase + nr, gb = r % kNGR;
+                        if (mbar_test(&gready[gb], (r / kNGR) & 1)) {
                             tc_fence_after();
                             const uint32_t d = tmem + gb * kGC + kKP, a = tmem + gb * kGC;
 #pragma unroll
@@ -881,46 +979,56 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
                 }
             }
         } else {
-            const int grp = (warp - 2) >> 2;
-            const int row = epi_row(warp, lane);
-            const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-            uint8_t *stage = stg + (grp * 4 + (warp & 3)) * 8192;
+            const int grp = (warp - 2) >> 3;          // 0 .. NGR-1
+            const int hf = ((warp - 2) >> 2) & 1;     // column half
+            const int quad = warp & 3;                // TMEM lane quadrant
+            const int row = 32 * quad + lane;
+            const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
             const uint32_t gbase = tmem + lane_base + grp * kGC;
-            for (int i = (grp - rbase % kNG + kNG) % kNG; i < n; i += kNG) {
+            uint8_t *stage = stg + (grp * 8 + ((warp - 2) & 7)) * 4096;
+            const int pair_bar = 1 + grp * 4 + quad;  // named barrier of the two warps of these rows
+            for (int i = (grp - rbase % kNGR + kNGR) % kNGR; i < n; i += kNGR) {
                 const int r = rbase + i, s = r % QS;
+                float2 *xr = xch + ((grp * 2 + ((r / kNGR) & 1)) * 128 + row) * 2;  // [hf] (max, sum)
                 if (!wait_or_abort(&qfull[s], (r / QS) & 1, status, abort_flag)) break;
-                prep_x2_row_tmem(qst + s * kTileBytes, row, gbase);
+                prep_x2_half_tmem(qst + s * kTileBytes, row, hf, gbase);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xready[grp]);
-                if (!wait_or_abort(&sfull[grp], (r / kNG) & 1, status, abort_flag)) break;
-                if (i < kNG && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
+                if (!wait_or_abort(&sfull[grp], (r / kNGR) & 1, status, abort_flag)) break;
+                if (i < kNGR && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 float rs;
                 {
-                    float e[kKP];
-                    rs = score_row_exp128(gbase + kKP, cvec, e);
-                    uint32_t wh[32], wl[32];
-                    split_row(e, 1.0f, wh, wl);
-                    tmem_st32(gbase, wh);
-                    tmem_st32(gbase + 32, wl);
+                    float e[32];
+                    const float mh = score_half(gbase + kKP, cvec, hf, e);
+                    xr[hf].x = mh;
+                    named_sync(pair_bar, 64);
+                    const float m = fmaxf(mh, xr[hf ^ 1].x);
+                    const float sh = exp_half(e, m);
+                    uint32_t wh[16], wl[16];
+                    split_half(e, 1.0f, wh, wl);
+                    tmem_st16(gbase + 16 * hf, wh);
+                    tmem_st16(gbase + 32 + 16 * hf, wl);
+                    xr[hf].y = sh;
                     tmem_wait_st();
+                    named_sync(pair_bar, 64);
+                    rs = hf == 0 ? sh + xr[1].y : xr[0].y + sh;  // same order in both halves
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&gready[grp]);
-                if (!wait_or_abort(&ofull[grp], (r / kNG) & 1, status, abort_flag)) break;
+                if (!wait_or_abort(&ofull[grp], (r / kNGR) & 1, status, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t ob = gbase + kKP;
-                float o[64];
+                float o[32];
                 {
-                    uint32_t d0[16], d1[16], a0[32], a1[32];
-                    tmem_ld16(ob + 64, d0);
-                    tmem_ld16(ob + 64 + NB, d1);
-                    tmem_ld32(ob, a0);
-                    tmem_ld32(ob + NB, a1);
+                    uint32_t a0[32], a1[32];
+                    tmem_ld32(ob + 32 * hf, a0);
+                    tmem_ld32(ob + NB + 32 * hf, a1);
+                    const uint32_t d0 = tmem_ld1(ob + 64), d1 = tmem_ld1(ob + NB + 64);
                     tmem_wait_ld();
-                    const float inv = 1.0f / (__uint_as_float(d0[0]) + __uint_as_float(d1[0]) + eps * rs);
+                    const float inv = 1.0f / (__uint_as_float(d0) + __uint_as_float(d1) + eps * rs);
                     const float2 iv = make_float2(inv, inv);
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -929,29 +1037,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
                         o[2 * q] = t.x;
                         o[2 * q + 1] = t.y;
                     }
-                    tmem_ld32(ob + 32, a0);
-                    tmem_ld32(ob + NB + 32, a1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float2 t = f2_mul(f2_add(make_float2(__uint_as_float(a0[2 * q]), __uint_as_float(a0[2 * q + 1])),
-                                                       make_float2(__uint_as_float(a1[2 * q]), __uint_as_float(a1[2 * q + 1]))), iv);
-                        o[32 + 2 * q] = t.x;
-                        o[32 + 2 * q + 1] = t.y;
-                    }
                 }
                 tc_fence_before();
-                stage_and_store_rows(stage, o, lane, lane, &tmO, o_bf16, (t0 + i) * kTile + 32 * (warp & 3), bh);
+                stage_and_store_half(stage, o, lane, lane, &tmO, o_bf16, hf, (t0 + i) * kTile + 32 * quad, bh);
             }
-            if (lane == 0) bulk_wait0();
+            if (lane == 0) bulk_wait_read0();  // staging reusable; kernel completion publishes the stores
         }
         rbase += n;
         g += n;
-        __syncthreads();
+        cta_sync();
         if (aborted(abort_flag)) break;
     }
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -978,20 +1076,22 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_read2_kernel(
 //   [384, 464) [num | den] (N = 80)
 // MMAs per chunk: scores 12 + 12, P 12, state read 12, U 8, P [V|1] 16.
 struct Causal2Smem {
-    static constexpr int W = 64 + 1;
+    static constexpr int W = kW;                           // fp32 state rows (float4 access)
+    static constexpr int WX = 66;                          // carry exchange rows (float2 access)
     static constexpr int kQK = 0;                          // Q tile | K tile (one stage)
     static constexpr int kV = kQK + 2 * kTileBytes;        // V tile | ones chunk
     static constexpr int kGK = kV + 2 * kTileBytes;        // Gamma^K: hi [128 x 128 B] | lo
     static constexpr int kSop = kGK + 2 * kTileBytes;      // state operand, MN-major: hi (2 x 8 KB) | lo
-    static constexpr int kCoef = kSop + 4 * 8192;
-    static constexpr int kS = kCoef + ((kCoefBytes + 1023) & ~1023);  // fp32 state [64][W]
-    static constexpr int kX = kGK;  // carry exchange [64][W] fp32, over Gamma^K (idle during the carry)
-    static constexpr int kStage = kS + ((kKP * W * 4 + 1023) & ~1023);  // output staging 4 x 8 KB
-    static constexpr int kBars = kStage + 4 * 8192;
+    static constexpr int kStage = kSop + 4 * 8192;         // output staging 4 x 8 KB
+    static constexpr int kCoef = kStage + 4 * 8192;
+    static constexpr int kS = kCoef + kCoefBytes;          // fp32 state [64][W]
+    static constexpr int kX = kS + kKP * W * 4;            // carry exchange [64][WX]
+    static constexpr int kBars = kX + kKP * WX * 4;
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kS % 16 == 0 && kX % 16 == 0 && kBars % 8 == 0, "alignment");
+    static_assert(kAlloc <= 232448, "shared memory budget");
 };
-
 // Epilogue pieces shared by the query and the key groups of the causal
 // kernel.  They are kept out of line so that both groups run one copy of the
 // code: the kernel's speed is bound by instruction fetch when each role has
@@ -1151,6 +1251,65 @@ __device__ __forceinline__ void store_state_half(uint8_t *sop, int k, const floa
     }
 }
 
+// Carry of the causal state, S += U_hi + U_lo, in two halves.  U row `row`
+// holds the hi-part sums of component k = row (row < 64) or the lo-part sums
+// of k = row - 64.  Thread k owns columns 0..31 of S row k and thread 64 + k
+// owns columns 32..64.  S rows are kW floats apart, X rows 66.
+__device__ __forceinline__ void carry_take_cols(float4 *s4, float2 *x2, const uint32_t (&own)[32],
+                                                const uint32_t (&other)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 v = s4[q];
+        v.x += __uint_as_float(own[4 * q]);
+        v.y += __uint_as_float(own[4 * q + 1]);
+        v.z += __uint_as_float(own[4 * q + 2]);
+        v.w += __uint_as_float(own[4 * q + 3]);
+        s4[q] = v;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) x2[q] = make_float2(__uint_as_float(other[2 * q]), __uint_as_float(other[2 * q + 1]));
+}
+// carry_take: adds the thread's own part of its columns to S and hands the
+// partner's columns over through X (the U columns become free).
+__device__ __noinline__ void carry_take(uint32_t u_taddr, float *S, float *X, int row) {
+    const int kc = row & (kKP - 1), half = row >> 6;
+    uint32_t a0[32], a1[32], z[16];
+    tmem_ld32(u_taddr, a0);
+    tmem_ld32(u_taddr + 32, a1);
+    tmem_ld16(u_taddr + 64, z);
+    tmem_wait_ld();
+    tc_fence_before();
+    float4 *s4 = reinterpret_cast<float4 *>(S + kc * kW + 32 * half);
+    float2 *x2 = reinterpret_cast<float2 *>(X + kc * 66 + 32 * (1 - half));
+    if (half == 0) {
+        carry_take_cols(s4, x2, a0, a1);
+        X[kc * 66 + 64] = __uint_as_float(z[0]);
+    } else {
+        carry_take_cols(s4, x2, a1, a0);
+        S[kc * kW + 64] += __uint_as_float(z[0]);
+    }
+}
+// carry_finish (after a barrier of the key group): adds the partner's part and
+// writes the thread's half of the state operand.
+__device__ __noinline__ void carry_finish(float *S, const float *X, uint8_t *sop, int row) {
+    const int kc = row & (kKP - 1), half = row >> 6;
+    float *sr = S + kc * kW;
+    float4 *s4 = reinterpret_cast<float4 *>(sr + 32 * half);
+    const float2 *x2 = reinterpret_cast<const float2 *>(X + kc * 66 + 32 * half);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 v = s4[q];
+        const float2 a = x2[2 * q], b = x2[2 * q + 1];
+        v.x += a.x;
+        v.y += a.y;
+        v.z += b.x;
+        v.w += b.y;
+        s4[q] = v;
+    }
+    if (half) sr[64] += X[kc * 66 + 64];
+    store_state_half(sop, kc, sr, half);
+}
+
 __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1198,7 +1357,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         for (int i = tid; i < 4 * 8192 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(sop)[i] = make_uint4(0, 0, 0, 0);
     }
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -1210,7 +1369,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         // The previous job is done with the coefficients, the state and the carry
         // area; this head's coefficients and the job's carried-in prefix arrive on cfull.
         fence_proxy_async_smem();
-        __syncthreads();
+        cta_sync();
         if (tid == 0) {
             mbar_arrive_expect_tx(cfull, kCoefBytes + kKP * W * 4);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
@@ -1263,9 +1422,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     issue_scores_ool(tmem + kSQ, tmem + kXQ, dq, dc);
                     umma_commit(sq);
                     umma_commit(qkempty);
-                    // P and the read of the carried state (after the previous chunk's carry)
-                    if (!spin_wait(gq, ph, status, abort_flag)) break;
+                    // U = [gK_hi ; gK_lo]^T [V | 1] for the carry (into the key-score columns,
+                    // free once the key softmax is done; not needed after the job's last chunk)
                     if (!spin_wait(gkr, ph, status, abort_flag)) break;
+                    if (!spin_wait(vfull, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    if (i + 1 < n) {
+#pragma unroll 1
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(ufull);
+                    // P and the read of the carried state
+                    if (!spin_wait(gq, ph, status, abort_flag)) break;
                     if (!spin_wait(sready, ph, status, abort_flag)) break;
                     tc_fence_after();
 #pragma unroll 1
@@ -1283,15 +1452,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                         umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bl_, i80s, 1u);
                     }
                     umma_commit(pfull);
-                    // U = [gK_hi ; gK_lo]^T [V | 1] for the carry (not needed after the job's last chunk)
-                    if (!spin_wait(vfull, ph, status, abort_flag)) break;
-                    tc_fence_after();
-                    if (i + 1 < n) {
-#pragma unroll 1
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(ufull);
                     // [num | den] += P [V | 1]
                     if (!spin_wait(pready, ph, status, abort_flag)) break;
                     tc_fence_after();
@@ -1345,18 +1505,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 tc_fence_after();
                 causal_output_row(tmem + lb + kO, rq_prev, eps, stage, lane, &tmO, o_bf16, (t0 + n - 1) * kTile + 32 * (warp & 3), bh);
             }
-            if (lane == 0) bulk_wait0();
+            if (lane == 0) bulk_wait_read0();  // staging reusable; kernel completion publishes the stores
         } else {
             // ---------------- key group
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-            // Carry split: U row `row` holds the hi-part sums of component k = row
-            // (row < 64) or the lo-part sums of k = row - 64.  Thread k keeps
-            // columns 0..31 of its row and hands 32..64 over through X; thread
-            // 64 + k keeps 32..64 and hands over 0..31.  Each then adds both parts
-            // to S for the columns it kept and writes that half of the state operand.
-            const int kc = row & (kKP - 1), half = row >> 6;
-            float keep[33];
             for (int i = 0; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
                 if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
@@ -1365,20 +1518,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xk);
-                if (i > 0) {  // finish the carry of chunk i-1: state operand of chunk i
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    float *sr = S + kc * W;
-                    const float *xr = X + kc * W;
-#pragma unroll
-                    for (int q = 0; q < 33; ++q) {
-                        const int col = 32 * half + q;
-                        if (q < 32 || half) sr[col] += keep[q] + xr[col];
-                    }
-                    store_state_half(sop, kc, sr, half);
-                    fence_proxy_async_smem();
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (lane == 0) mbar_arrive(sready);
-                }
                 if (!wait_or_abort(sk, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
@@ -1386,52 +1525,39 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gkr);
-                // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo
+                // first half of the carry, beside the P MMAs: U out of tensor memory
+                // (its columns are the next chunk's key scores), the partner's columns
+                // through X
+                const bool carry = i + 1 < n;
+                if (carry) {
+                    if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    carry_take(tmem + lb + kU, S, X, row);
+                }
                 if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
                 tc_fence_after();
+                // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo
                 split_p_blocks(tmem + lb + kPD, tmem + lb + kXQ, tmem + lb + kXK, 2, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
-                // first half of the carry: U out of tensor memory (its columns are the
-                // next chunk's key scores), the partner's columns into X (over Gamma^K,
-                // which P and U have consumed)
-                if (i + 1 < n) {
-                    if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
-                    tc_fence_after();
-                    uint32_t a0[32], a1[32], z[16];
-                    tmem_ld32(tmem + lb + kU, a0);
-                    tmem_ld32(tmem + lb + kU + 32, a1);
-                    tmem_ld16(tmem + lb + kU + 64, z);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    float *xr = X + kc * W;
-                    if (half == 0) {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            keep[q] = __uint_as_float(a0[q]);
-                            xr[32 + q] = __uint_as_float(a1[q]);
-                        }
-                        xr[64] = __uint_as_float(z[0]);
-                        keep[32] = 0.f;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            keep[q] = __uint_as_float(a1[q]);
-                            xr[q] = __uint_as_float(a0[q]);
-                        }
-                        keep[32] = __uint_as_float(z[0]);
-                    }
+                // second half, beside the P [V | 1] MMAs: the state operand of the next chunk
+                if (carry) {
+                    named_sync(1, 128);
+                    carry_finish(S, X, sop, row);
+                    fence_proxy_async_smem();
+                    named_sync(1, 128);
+                    if (lane == 0) mbar_arrive(sready);
                 }
             }
         }
         rbase += n;
         g += n;
-        __syncthreads();
+        cta_sync();
         if (aborted(abort_flag)) break;
     }
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -1481,6 +1607,23 @@ bool make_out_map(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
     return r == CUDA_SUCCESS;
 }
 
+// O [BH][N][64] (fp32 or bf16) for TMA stores of [32 rows x 32 columns]
+// boxes: 128-byte swizzle for fp32, 64-byte swizzle for bf16.
+bool make_out_map_half(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)64 * es, (cuuint64_t)N * 64 * es};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <typename KernelT>
 cudaError_t set_smem(KernelT kern, int bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1503,8 +1646,8 @@ int num_sms() {
 }
 
 // Workspace of the persistent kernels: status | per-head job counters |
-// per-head parameter-error words | per-head coefficient images | job partials
-// [ctas][slots][KP][d_v + 1] | per-head read operand images.  Nothing needs
+// per-block parameter-error words of the coefficient prep | per-head coefficient images | job partials
+// [ctas][slots][KP][kW] | per-head read operand images.  Nothing needs
 // clearing by the caller: coef_prep_tc_kernel resets the status word and the
 // counters, and writes every error word.
 struct TcLayout2 {
@@ -1526,11 +1669,11 @@ TcLayout2 tc_layout2(const Problem &p, int splits) {
     L.counters = off;
     off = align256(off + sizeof(unsigned) * (size_t)p.BH());
     L.head_err = off;
-    off = align256(off + sizeof(unsigned) * (size_t)p.H);
+    off = align256(off + sizeof(unsigned) * (size_t)p.H * kPrepBlocks);
     L.coef = off;
     off = align256(off + kCoefStride * p.H);
     L.part = off;
-    off = align256(off + sizeof(float) * (size_t)L.nctas * L.P.slots * kKP * (p.d_v + 1));
+    off = align256(off + sizeof(float) * (size_t)L.nctas * L.P.slots * kKP * kW);
     L.mem_stride = ((size_t)2 * (p.d_v + 16) * 128 + 1023) & ~size_t(1023);
     L.mem = off;
     off = align256(off + L.mem_stride * p.BH());
@@ -1546,11 +1689,11 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     uint8_t *coef = ws + L.coef;
     CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
-        !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map(&to, p.O, p.BH(), p.N, p.o_bf16))
+        !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map_half(&to, p.O, p.BH(), p.N, p.o_bf16))
         return cudaErrorInvalidValue;
     unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
+    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
@@ -1558,8 +1701,8 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
         tk, tv, coef, head_err, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    GMA_TRY(set_smem(tc_read2_kernel, Read2Smem::kAlloc));
-    tc_read2_kernel<<<L.nctas, kThreadsG, Read2Smem::kAlloc, s>>>(
+    GMA_TRY(set_smem(tc_read3_kernel, Read3Smem::kAlloc));
+    tc_read3_kernel<<<L.nctas, kThreadsR, Read3Smem::kAlloc, s>>>(
         tq, to, coef, p.H, p.N, L.P, mem, L.mem_stride, p.eps, p.o_bf16 ? 1 : 0, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
@@ -1577,7 +1720,7 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
         return cudaErrorInvalidValue;
     unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    coef_prep_tc_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
+    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
