@@ -1128,9 +1128,9 @@ __device__ __noinline__ float gamma_row(uint32_t s_taddr, const float *cvec, int
 }
 
 // One key block (32 keys) of the masked bf16 hi / lo split of P for this
-// thread's query row: hi words to taddr_hi + 16 cb, lo words to taddr_lo + 16 cb.
-__device__ __forceinline__ void split_p_block(const uint32_t (&pp)[32], int cb, int row, uint32_t taddr_hi,
-                                              uint32_t taddr_lo) {
+// thread's query row, written in place over the block's 32 fp32 columns:
+// hi words to columns [32 cb, +16), lo words to [32 cb + 16, +16).
+__device__ __forceinline__ void split_p_block(const uint32_t (&pp)[32], int cb, int row, uint32_t p_taddr) {
     uint32_t wh[16], wl[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
@@ -1140,39 +1140,38 @@ __device__ __forceinline__ void split_p_block(const uint32_t (&pp)[32], int cb, 
         wh[q] = pack_bf2(a, b);
         wl[q] = pack_bf2(a - bf_lo(wh[q]), b - bf_hi(wh[q]));
     }
-    tmem_st16(taddr_hi + cb * 16, wh);
-    tmem_st16(taddr_lo + cb * 16, wl);
+    tmem_st16(p_taddr + 32 * cb, wh);
+    tmem_st16(p_taddr + 32 * cb + 16, wl);
 }
-__device__ __forceinline__ void zero_p_block(int cb, uint32_t taddr_hi, uint32_t taddr_lo) {
+__device__ __forceinline__ void zero_p_block(int cb, uint32_t p_taddr) {
     uint32_t z[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) z[q] = 0u;
-    tmem_st16(taddr_hi + cb * 16, z);
-    tmem_st16(taddr_lo + cb * 16, z);
+    tmem_st16(p_taddr + 32 * cb, z);
+    tmem_st16(p_taddr + 32 * cb + 16, z);
 }
 
-// Masked split of P for key blocks cb0 and cb0 + 1 of this thread's query row.
-// Blocks entirely above the diagonal are written as zeros without reading P
-// (the block index of the row is uniform across a warp).
-__device__ __noinline__ void split_p_blocks(uint32_t p_taddr, uint32_t taddr_hi, uint32_t taddr_lo, int cb0,
-                                            int row) {
+// Masked split of P for key blocks cb0 and cb0 + 1 of this thread's query row,
+// in place.  Blocks entirely above the diagonal are written as zeros without
+// reading P (the block index of the row is uniform across a warp).
+__device__ __noinline__ void split_p_blocks(uint32_t p_taddr, int cb0, int row) {
     const int rb = row >> 5;
     if (cb0 + 1 <= rb) {
         uint32_t p0[32], p1[32];
         tmem_ld32(p_taddr + cb0 * 32, p0);
         tmem_ld32(p_taddr + (cb0 + 1) * 32, p1);
         tmem_wait_ld();
-        split_p_block(p0, cb0, row, taddr_hi, taddr_lo);
-        split_p_block(p1, cb0 + 1, row, taddr_hi, taddr_lo);
+        split_p_block(p0, cb0, row, p_taddr);
+        split_p_block(p1, cb0 + 1, row, p_taddr);
     } else if (cb0 <= rb) {
         uint32_t p0[32];
         tmem_ld32(p_taddr + cb0 * 32, p0);
         tmem_wait_ld();
-        split_p_block(p0, cb0, row, taddr_hi, taddr_lo);
-        zero_p_block(cb0 + 1, taddr_hi, taddr_lo);
+        split_p_block(p0, cb0, row, p_taddr);
+        zero_p_block(cb0 + 1, p_taddr);
     } else {
-        zero_p_block(cb0, taddr_hi, taddr_lo);
-        zero_p_block(cb0 + 1, taddr_hi, taddr_lo);
+        zero_p_block(cb0, p_taddr);
+        zero_p_block(cb0 + 1, p_taddr);
     }
     tmem_wait_st();
 }
@@ -1388,17 +1387,37 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         }
 
         if (warp == 0) {
-            if (lane == 0)
-                for (int i = 0; i < n; ++i) {
-                    const int r = rbase + i;
-                    if (!wait_or_abort(qkempty, (r & 1) ^ 1, status, abort_flag)) break;
-                    mbar_arrive_expect_tx(qkfull, 2 * kTileBytes);
-                    tma_load_3d(qk, &tmQ, 0, (t0 + i) * kTile, bh, qkfull);
-                    tma_load_3d(qk + kTileBytes, &tmK, 0, (t0 + i) * kTile, bh, qkfull);
-                    if (!wait_or_abort(vempty, (r & 1) ^ 1, status, abort_flag)) break;
-                    mbar_arrive_expect_tx(vfull, kTileBytes);
-                    tma_load_3d(vt, &tmV, 0, (t0 + i) * kTile, bh, vfull);
+            if (lane == 0) {
+                // Q|K and V loads, each as soon as its stage is free.
+                int nq = 0, nv = 0;
+                Stall st;
+                while (nv < n) {
+                    bool prog = false;
+                    if (nq < n) {
+                        const int r = rbase + nq;
+                        if (mbar_test(qkempty, (r & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(qkfull, 2 * kTileBytes);
+                            tma_load_3d(qk, &tmQ, 0, (t0 + nq) * kTile, bh, qkfull);
+                            tma_load_3d(qk + kTileBytes, &tmK, 0, (t0 + nq) * kTile, bh, qkfull);
+                            ++nq;
+                            prog = true;
+                        }
+                    }
+                    if (nv < nq) {
+                        const int r = rbase + nv;
+                        if (mbar_test(vempty, (r & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(vfull, kTileBytes);
+                            tma_load_3d(vt, &tmV, 0, (t0 + nv) * kTile, bh, vfull);
+                            ++nv;
+                            prog = true;
+                        }
+                    }
+                    if (!st.tick(prog, abort_flag)) {
+                        note_timeout(status, abort_flag);
+                        break;
+                    }
                 }
+            }
         } else if (warp == 1) {
             if (lane == 0) {
                 const uint64_t dq = sdesc_sw128(smem_u32(qk), 16, 1024), dkx = sdesc_sw128(smem_u32(qk + kTileBytes), 16, 1024);
@@ -1409,60 +1428,97 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 const uint64_t dv = sdesc_sw128(smem_u32(vt), kTileBytes, 1024);        // MN-major [V | 1]
                 constexpr uint32_t i128 = idesc_bf16(kTile, 128, false, false);
                 constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
+                // Two issue streams, each in chunk order:
+                //   key:   K scores (c), U (c)                       -- runs up to a chunk ahead
+                //   query: Q scores (c), P + state read (c), P [V|1] (c)
+                // Q scores (c + 1) follow P [V|1] (c) in issue order, which they overwrite
+                // in the P / Q-score columns.  qkempty (c) is committed once both score
+                // sets of c are issued, vempty (c) once U (c) and P [V|1] (c) are.
+                int kdone = 0, udone = 0, qdone = 0, pdone = 0, vdone = 0;
+                Stall st;
                 const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
-                for (int i = 0; coef_ok && i < n; ++i) {
-                    const int r = rbase + i, ph = r & 1;
-                    // scores of the chunk (the key side is the longer path: first)
-                    if (!spin_wait(xk, ph, status, abort_flag)) break;
-                    tc_fence_after();
-                    issue_scores_ool(tmem + kSK, tmem + kXK, dkx, dc);
-                    umma_commit(sk);
-                    if (!spin_wait(xq, ph, status, abort_flag)) break;
-                    tc_fence_after();
-                    issue_scores_ool(tmem + kSQ, tmem + kXQ, dq, dc);
-                    umma_commit(sq);
-                    umma_commit(qkempty);
-                    // U = [gK_hi ; gK_lo]^T [V | 1] for the carry (into the key-score columns,
-                    // free once the key softmax is done; not needed after the job's last chunk)
-                    if (!spin_wait(gkr, ph, status, abort_flag)) break;
-                    if (!spin_wait(vfull, ph, status, abort_flag)) break;
-                    tc_fence_after();
-                    if (i + 1 < n) {
+                while (coef_ok && vdone < n) {
+                    bool prog = false;
+                    if (kdone < n && udone == kdone) {
+                        const int r = rbase + kdone;
+                        if (mbar_test(xk, r & 1)) {
+                            tc_fence_after();
+                            issue_scores_ool(tmem + kSK, tmem + kXK, dkx, dc);
+                            umma_commit(sk);
+                            ++kdone;
+                            if (qdone >= kdone) umma_commit(qkempty);
+                            prog = true;
+                        }
+                    } else if (udone < kdone) {
+                        const int r = rbase + udone;
+                        if (mbar_test(gkr, r & 1) && mbar_test(vfull, r & 1)) {
+                            tc_fence_after();
+                            if (udone + 1 < n) {
 #pragma unroll 1
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
+                            }
+                            umma_commit(ufull);
+                            ++udone;
+                            if (vdone >= udone) umma_commit(vempty);
+                            prog = true;
+                        }
                     }
-                    umma_commit(ufull);
-                    // P and the read of the carried state
-                    if (!spin_wait(gq, ph, status, abort_flag)) break;
-                    if (!spin_wait(sready, ph, status, abort_flag)) break;
-                    tc_fence_after();
+                    if (qdone < n && qdone == vdone) {
+                        const int r = rbase + qdone;
+                        if (mbar_test(xq, r & 1)) {
+                            tc_fence_after();
+                            issue_scores_ool(tmem + kSQ, tmem + kXQ, dq, dc);
+                            umma_commit(sq);
+                            ++qdone;
+                            if (kdone >= qdone) umma_commit(qkempty);
+                            prog = true;
+                        }
+                    } else if (pdone < qdone) {
+                        const int r = rbase + pdone;
+                        if (mbar_test(gq, r & 1) && mbar_test(gkr, r & 1) && mbar_test(sready, r & 1)) {
+                            tc_fence_after();
 #pragma unroll 1
-                    for (int kk = 0; kk < kKP / 16; ++kk) {
-                        const uint32_t aq = tmem + kXQ + kk * 8;
-                        umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kk * 32), i128, kk > 0 ? 1u : 0u);
-                        umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kTileBytes + kk * 32), i128, 1u);
-                        umma_bf16_tA(tmem + kPD, aq + 32, dadd(dgk, kk * 32), i128, 1u);
-                    }
+                            for (int kk = 0; kk < kKP / 16; ++kk) {
+                                const uint32_t aq = tmem + kXQ + kk * 8;
+                                umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kk * 32), i128, kk > 0 ? 1u : 0u);
+                                umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kTileBytes + kk * 32), i128, 1u);
+                                umma_bf16_tA(tmem + kPD, aq + 32, dadd(dgk, kk * 32), i128, 1u);
+                            }
 #pragma unroll 1
-                    for (int kk = 0; kk < kKP / 16; ++kk) {
-                        const uint64_t bh_ = dadd(dso, kk * 2048), bl_ = dadd(dso, 16384 + kk * 2048);
-                        umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bh_, i80s, kk > 0 ? 1u : 0u);
-                        umma_bf16_tA(tmem + kO, tmem + kXQ + 32 + kk * 8, bh_, i80s, 1u);
-                        umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bl_, i80s, 1u);
-                    }
-                    umma_commit(pfull);
-                    // [num | den] += P [V | 1]
-                    if (!spin_wait(pready, ph, status, abort_flag)) break;
-                    tc_fence_after();
+                            for (int kk = 0; kk < kKP / 16; ++kk) {
+                                const uint64_t bh_ = dadd(dso, kk * 2048), bl_ = dadd(dso, 16384 + kk * 2048);
+                                umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bh_, i80s, kk > 0 ? 1u : 0u);
+                                umma_bf16_tA(tmem + kO, tmem + kXQ + 32 + kk * 8, bh_, i80s, 1u);
+                                umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bl_, i80s, 1u);
+                            }
+                            umma_commit(pfull);
+                            ++pdone;
+                            prog = true;
+                        }
+                    } else if (vdone < pdone) {
+                        const int r = rbase + vdone;
+                        if (mbar_test(pready, r & 1) && mbar_test(vfull, r & 1)) {
+                            tc_fence_after();
+                            // [num | den] += P [V | 1]; P hi / lo sit in place in the P columns:
+                            // key block cb = kk / 2 holds hi words at 32 cb, lo words at 32 cb + 16.
 #pragma unroll 1
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t bv = dadd(dv, kk * 2048);
-                        umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bv, i80s, 1u);
-                        umma_bf16_tA(tmem + kO, tmem + kXK + kk * 8, bv, i80s, 1u);
+                            for (int kk = 0; kk < kTile / 16; ++kk) {
+                                const uint64_t bv = dadd(dv, kk * 2048);
+                                const uint32_t ap = tmem + kPD + 32 * (kk >> 1) + 8 * (kk & 1);
+                                umma_bf16_tA(tmem + kO, ap, bv, i80s, 1u);
+                                umma_bf16_tA(tmem + kO, ap + 16, bv, i80s, 1u);
+                            }
+                            umma_commit(ofull);
+                            ++vdone;
+                            if (udone >= vdone) umma_commit(vempty);
+                            prog = true;
+                        }
                     }
-                    umma_commit(ofull);
-                    umma_commit(vempty);
+                    if (!st.tick(prog, abort_flag)) {
+                        note_timeout(status, abort_flag);
+                        break;
+                    }
                 }
             }
         } else if (warp < 6) {
@@ -1470,40 +1526,41 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             uint8_t *stage = stg + (warp & 3) * 8192;
-            float rq_prev = 0.f;
-            int i = 0;
-            for (; i < n; ++i) {
+            for (int i = 0; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
-                if (i > 0 && !wait_or_abort(ofull, ph ^ 1, status, abort_flag)) break;  // P hi of chunk i-1 consumed
-                x2_row(qk, row, tmem + lb + kXQ);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xq);
-                // outputs of the previous chunk, beside this chunk's score MMAs
-                if (i > 0) {
-                    tc_fence_after();
-                    causal_output_row(tmem + lb + kO, rq_prev, eps, stage, lane, &tmO, o_bf16, (t0 + i - 1) * kTile + 32 * (warp & 3), bh);
+                if (i == 0) {  // x^2 of the job's first chunk (later ones are prepared a chunk ahead)
+                    if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
+                    x2_row(qk, row, tmem + lb + kXQ);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xq);
                 }
                 if (!wait_or_abort(sq, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
-                rq_prev = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, row, 1);
+                const float rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, row, 1);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gq);
-                // masked intra-chunk affinity, key blocks 0 and 1 -> P hi | lo
+                // masked intra-chunk affinity, key blocks 0 and 1 -> P hi | lo (in place)
                 if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
                 tc_fence_after();
-                split_p_blocks(tmem + lb + kPD, tmem + lb + kXQ, tmem + lb + kXK, 0, row);
+                split_p_blocks(tmem + lb + kPD, 0, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
-            }
-            if (i == n && n > 0 && wait_or_abort(ofull, (rbase + n - 1) & 1, status, abort_flag)) {
-                // outputs of the job's last chunk
+                // x^2 of the next chunk (its A columns held Gamma^Q, consumed by P and the state read)
+                if (i + 1 < n) {
+                    if (!wait_or_abort(qkfull, ph ^ 1, status, abort_flag)) break;
+                    x2_row(qk, row, tmem + lb + kXQ);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xq);
+                }
+                // outputs of this chunk
+                if (!wait_or_abort(ofull, ph, status, abort_flag)) break;
                 tc_fence_after();
-                causal_output_row(tmem + lb + kO, rq_prev, eps, stage, lane, &tmO, o_bf16, (t0 + n - 1) * kTile + 32 * (warp & 3), bh);
+                causal_output_row(tmem + lb + kO, rq, eps, stage, lane, &tmO, o_bf16, (t0 + i) * kTile + 32 * (warp & 3), bh);
             }
             if (lane == 0) bulk_wait_read0();  // staging reusable; kernel completion publishes the stores
         } else {
@@ -1512,12 +1569,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             for (int i = 0; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
-                if (i > 0 && !wait_or_abort(ofull, ph ^ 1, status, abort_flag)) break;  // P lo of chunk i-1 consumed
-                x2_row(qk + kTileBytes, row, tmem + lb + kXK);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xk);
+                if (i == 0) {  // x^2 of the job's first chunk (later ones are prepared a chunk ahead)
+                    if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
+                    x2_row(qk + kTileBytes, row, tmem + lb + kXK);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xk);
+                }
                 if (!wait_or_abort(sk, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
@@ -1525,23 +1583,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gkr);
-                // first half of the carry, beside the P MMAs: U out of tensor memory
-                // (its columns are the next chunk's key scores), the partner's columns
-                // through X
                 const bool carry = i + 1 < n;
                 if (carry) {
+                    // first half of the carry: U out of tensor memory (its columns take the
+                    // next chunk's key scores), the partner's columns through X
                     if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
                     tc_fence_after();
                     carry_take(tmem + lb + kU, S, X, row);
+                    // x^2 of the next chunk's keys (the score MMAs of this chunk have read it)
+                    if (!wait_or_abort(qkfull, ph ^ 1, status, abort_flag)) break;
+                    x2_row(qk + kTileBytes, row, tmem + lb + kXK);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xk);
                 }
+                // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo (in place)
                 if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
                 tc_fence_after();
-                // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo
-                split_p_blocks(tmem + lb + kPD, tmem + lb + kXQ, tmem + lb + kXK, 2, row);
+                split_p_blocks(tmem + lb + kPD, 2, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
-                // second half, beside the P [V | 1] MMAs: the state operand of the next chunk
+                // second half of the carry, beside the P [V | 1] MMAs: the state operand of
+                // the next chunk (the state read of this chunk is done: pfull)
                 if (carry) {
                     named_sync(1, 128);
                     carry_finish(S, X, sop, row);
