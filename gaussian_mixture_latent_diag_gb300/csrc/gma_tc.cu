@@ -222,23 +222,6 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
     __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-// Wait by polling (no suspension between probes), for the single MMA-issuing
-// thread whose wake-up latency is on the critical path; bounded like mbar_wait.
-// The polling loop is out of line (one copy for all call sites).
-__device__ __noinline__ bool spin_wait_slow(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
-    Stall st;
-    while (!mbar_test(bar, parity)) {
-        if (!st.tick(false, abort_flag)) {
-            note_timeout(status, abort_flag);
-            return false;
-        }
-    }
-    return true;
-}
-__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *status, int *abort_flag) {
-    return mbar_test(bar, parity) || spin_wait_slow(bar, parity, status, abort_flag);
-}
-
 // Row of the tile / TMEM lane handled by an epilogue thread (warp w may only
 // read TMEM lanes 32*(w%4) .. 32*(w%4)+31).
 __device__ __forceinline__ int epi_row(int warp, int lane) { return 32 * (warp & 3) + lane; }
@@ -1069,30 +1052,35 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
 // output epilogue of a chunk runs beside the score MMAs of the next.
 //
 // TMEM (512 columns):
-//   [0, 64)    x^2 of Q -> Gamma^Q hi | lo -> P hi   (MMA A operands)
-//   [64, 128)  x^2 of K ->                    P lo
-//   [128, 256) scores Q (N = 128) -> P = gQhi gKhi^T + gQhi gKlo^T + gQlo gKhi^T (N = 128)
-//   [256, 384) scores K (N = 128) -> state increment U = [gK_hi ; gK_lo]^T [V | 1] (N = 80)
-//   [384, 464) [num | den] (N = 80)
-// MMAs per chunk: scores 12 + 12, P 12, state read 12, U 8, P [V|1] 16.
+//   [0, 64)    x^2 of Q -> Gamma^Q hi | lo          (MMA A operands)
+//   [64, 128)  x^2 of K
+//   [128, 256) scores Q (N = 128) -> P, then P hi | lo in place per 32-key block
+//   [256, 336) [num | den]: one N = 208 accumulator with P for the P + state-read MMAs
+//   [336, 464) scores K (N = 128) -> state increment U = [gK_hi ; gK_lo]^T [V | 1] (N = 80)
+// The B operand of the P + state-read MMAs is [Gamma^K ; S^T] (128 + 80 K-major
+// rows), so P and the read of the carried state share each instruction.
+// MMAs per chunk: scores 12 + 12, P + state read 12 (N = 208), U 8, P [V|1] 16.
 struct Causal2Smem {
     static constexpr int W = kW;                           // fp32 state rows (float4 access)
     static constexpr int WX = 66;                          // carry exchange rows (float2 access)
+    // B operand of the P + state-read MMAs, K-major SW128, rows of 64 components:
+    // [Gamma^K_hi (128 token rows) ; S_hi^T (80 value rows)] then the same for lo.
+    static constexpr int kBRows = kTile + 80;
+    static constexpr int kBHalf = kBRows * 128;            // 26 KB, a multiple of 1 KB
     static constexpr int kQK = 0;                          // Q tile | K tile (one stage)
     static constexpr int kV = kQK + 2 * kTileBytes;        // V tile | ones chunk
-    static constexpr int kGK = kV + 2 * kTileBytes;        // Gamma^K: hi [128 x 128 B] | lo
-    static constexpr int kSop = kGK + 2 * kTileBytes;      // state operand, MN-major: hi (2 x 8 KB) | lo
-    static constexpr int kStage = kSop + 4 * 8192;         // output staging 4 x 8 KB
+    static constexpr int kGB = kV + 2 * kTileBytes;        // [Gamma^K ; S^T] hi | lo
+    static constexpr int kStage = kGB + 2 * kBHalf;        // output staging 4 x 8 KB
     static constexpr int kCoef = kStage + 4 * 8192;
     static constexpr int kS = kCoef + kCoefBytes;          // fp32 state [64][W]
     static constexpr int kX = kS + kKP * W * 4;            // carry exchange [64][WX]
     static constexpr int kBars = kX + kKP * WX * 4;
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kBHalf % 1024 == 0 && kStage % 1024 == 0, "SW128 alignment");
     static_assert(kS % 16 == 0 && kX % 16 == 0 && kBars % 8 == 0, "alignment");
     static_assert(kAlloc <= 232448, "shared memory budget");
-};
-// Epilogue pieces shared by the query and the key groups of the causal
+};// Epilogue pieces shared by the query and the key groups of the causal
 // kernel.  They are kept out of line so that both groups run one copy of the
 // code: the kernel's speed is bound by instruction fetch when each role has
 // its own inlined copy.
@@ -1102,10 +1090,10 @@ __device__ __noinline__ void x2_row(const uint8_t *x, int row, uint32_t taddr) {
 // to_smem == 0: un-normalised (scale 1), hi words to taddr + 0..31, lo words to
 //               taddr + 32..63 (the A operand of the following MMAs);
 // to_smem != 0: normalised (scale 0 for rows past N), written as row `row` of
-//               the swizzled [128 x 64] hi block at gk and the lo block at gk + 16 KB.
+//               the swizzled [128 x 64] hi block at gk and the lo block at gk + lo_off.
 // Returns the row sum of the exponentials.
 __device__ __noinline__ float gamma_row(uint32_t s_taddr, const float *cvec, int to_smem, uint32_t taddr,
-                                        uint8_t *gk, int row, int valid) {
+                                        uint8_t *gk, int lo_off, int row, int valid) {
     float e[kKP];
     const float rs = score_row_exp128(s_taddr, cvec, e);
     tc_fence_before();
@@ -1116,7 +1104,7 @@ __device__ __noinline__ float gamma_row(uint32_t s_taddr, const float *cvec, int
         tmem_st32(taddr + 32, wl);
         tmem_wait_st();
     } else {
-        uint8_t *hi = gk + row * 128, *lo = gk + kTileBytes + row * 128;
+        uint8_t *hi = gk + row * 128, *lo = gk + lo_off + row * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
             const uint32_t sw = (uint32_t)((cc ^ (row & 7)) << 4);
@@ -1197,56 +1185,26 @@ __device__ __noinline__ void causal_output_row(uint32_t o_taddr, float rq, float
     stage_and_store_rows(stage, o, lane, lane, tmO, o_bf16, row0, bh);
 }
 
-// One state-operand row: component k, 64 values of S plus Z, as bf16 hi / lo,
-// MN-major SW128 (row = component; chunk 0 = columns 0..63, chunk 1 at +8 KB
-// holds Z in column 64 and zeros).
-__device__ __forceinline__ void store_state_row(uint8_t *sop, int k, const float *srow) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
+// State operand: S^T stored K-major SW128 inside the B operand of the P +
+// state-read MMAs (gb: hi part, gb + kBHalf: lo part), row n = value column n
+// (n = 64 is Z; rows 65..79 stay zero), 64 components per 128-byte row.
+// Written by all 128 threads of the key group from the fp32 state S
+// ([64 components][kW]): item i < 65 * 8 is row n = i % 65, 8-component chunk
+// c = i / 65 (consecutive threads take consecutive n: conflict-free reads of S).
+__device__ __forceinline__ void state_operand_from_S(uint8_t *gb, const float *S, int t) {
+    uint8_t *sb = gb + kTile * 128;  // S^T rows follow the 128 Gamma^K rows
+    for (int i = t; i < 65 * 8; i += 128) {
+        const int n = i % 65, c = i / 65;
         uint32_t wh[4], wl[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float v0 = srow[8 * c + 2 * q], v1 = srow[8 * c + 2 * q + 1];
+            const float v0 = S[(8 * c + 2 * q) * kW + n], v1 = S[(8 * c + 2 * q + 1) * kW + n];
             wh[q] = pack_bf2(v0, v1);
             wl[q] = pack_bf2(v0 - bf_lo(wh[q]), v1 - bf_hi(wh[q]));
         }
-        const uint32_t off = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((c ^ (k & 7)) << 4));
-        *reinterpret_cast<uint4 *>(sop + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(sop + 16384 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    }
-    const float z = srow[64];
-    const uint32_t zh = pack_bf2(z, 0.f), zl = pack_bf2(z - bf_lo(zh), 0.f);
-    const uint32_t off0 = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((0 ^ (k & 7)) << 4));
-    const uint32_t off1 = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((1 ^ (k & 7)) << 4));
-    *reinterpret_cast<uint4 *>(sop + 8192 + off0) = make_uint4(zh, 0u, 0u, 0u);
-    *reinterpret_cast<uint4 *>(sop + 8192 + off1) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off0) = make_uint4(zl, 0u, 0u, 0u);
-    *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off1) = make_uint4(0u, 0u, 0u, 0u);
-}
-
-// Half of a state-operand row: columns 0..31 (half 0) or 32..63 plus Z
-// (half 1) of component k, as bf16 hi / lo (layout of store_state_row).
-__device__ __forceinline__ void store_state_half(uint8_t *sop, int k, const float *srow, int half) {
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int c = 4 * half + cc;
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float v0 = srow[8 * c + 2 * q], v1 = srow[8 * c + 2 * q + 1];
-            wh[q] = pack_bf2(v0, v1);
-            wl[q] = pack_bf2(v0 - bf_lo(wh[q]), v1 - bf_hi(wh[q]));
-        }
-        const uint32_t off = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((c ^ (k & 7)) << 4));
-        *reinterpret_cast<uint4 *>(sop + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(sop + 16384 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    }
-    if (half) {
-        const float z = srow[64];
-        const uint32_t zh = pack_bf2(z, 0.f), zl = pack_bf2(z - bf_lo(zh), 0.f);
-        const uint32_t off0 = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((0 ^ (k & 7)) << 4));
-        *reinterpret_cast<uint4 *>(sop + 8192 + off0) = make_uint4(zh, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(sop + 16384 + 8192 + off0) = make_uint4(zl, 0u, 0u, 0u);
+        const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
+        *reinterpret_cast<uint4 *>(sb + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(sb + Causal2Smem::kBHalf + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
     }
 }
 
@@ -1288,9 +1246,9 @@ __device__ __noinline__ void carry_take(uint32_t u_taddr, float *S, float *X, in
         S[kc * kW + 64] += __uint_as_float(z[0]);
     }
 }
-// carry_finish (after a barrier of the key group): adds the partner's part and
-// writes the thread's half of the state operand.
-__device__ __noinline__ void carry_finish(float *S, const float *X, uint8_t *sop, int row) {
+// carry_finish (after a barrier of the key group): adds the partner's part to
+// the thread's columns of S.
+__device__ __noinline__ void carry_finish(float *S, const float *X, int row) {
     const int kc = row & (kKP - 1), half = row >> 6;
     float *sr = S + kc * kW;
     float4 *s4 = reinterpret_cast<float4 *>(sr + 32 * half);
@@ -1306,8 +1264,10 @@ __device__ __noinline__ void carry_finish(float *S, const float *X, uint8_t *sop
         s4[q] = v;
     }
     if (half) sr[64] += X[kc * 66 + 64];
-    store_state_half(sop, kc, sr, half);
 }
+// The state operand of the next chunk from S, by the whole key group (out of
+// line: one copy for the job start and the carry).
+__device__ __noinline__ void state_operand(uint8_t *gb, const float *S, int t) { state_operand_from_S(gb, S, t); }
 
 __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -1317,11 +1277,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     using L = Causal2Smem;
     constexpr int W = L::W;
     constexpr int kTmemCols = 512;
-    constexpr int kXQ = 0, kXK = 64, kSQ = 128, kSK = 256, kPD = 128, kU = 256, kO = 384;
+    constexpr int kXQ = 0, kXK = 64, kSQ = 128, kPD = 128, kO = 256, kSK = 336, kU = 336;
+    static_assert(kO == kPD + 128, "[P | num den] is one N = 208 accumulator");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qk = smem + L::kQK, *vt = smem + L::kV, *gk = smem + L::kGK, *sop = smem + L::kSop,
-            *coef = smem + L::kCoef;
+    uint8_t *qk = smem + L::kQK, *vt = smem + L::kV, *gb = smem + L::kGB, *coef = smem + L::kCoef;
     float *S = reinterpret_cast<float *>(smem + L::kS), *X = reinterpret_cast<float *>(smem + L::kX);
     uint8_t *stg = smem + L::kStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
@@ -1350,10 +1310,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
     }
-    {   // constant ones chunk of the V stage; zero state operand (its padding must be 0)
+    {   // constant ones chunk of the V stage; zero B operand (the S^T padding rows must be 0)
         const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
         for (int i = tid; i < kTileBytes / 16; i += kThreadsG) reinterpret_cast<uint4 *>(vt + kTileBytes)[i] = one4;
-        for (int i = tid; i < 4 * 8192 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(sop)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 2 * L::kBHalf / 16; i += kThreadsG) reinterpret_cast<uint4 *>(gb)[i] = make_uint4(0, 0, 0, 0);
     }
     tc_fence_before();
     cta_sync();
@@ -1374,14 +1334,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
             bulk_load(S, prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W, kKP * W * 4, cfull);
         }
-        if (warp >= 6) {  // key group: state operand of the job's first chunk (rows 0..63 in warps 8, 9)
-            if (warp >= 8) {
-                if (wait_or_abort(cfull, njob & 1, status, abort_flag)) {
-                    const int k = epi_row(warp, lane);
-                    store_state_row(sop, k, S + k * W);
-                }
-                fence_proxy_async_smem();
-            }
+        if (warp >= 6) {  // key group: state operand of the job's first chunk
+            if (wait_or_abort(cfull, njob & 1, status, abort_flag)) state_operand(gb, S, tid - 192);
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(sready);
         }
@@ -1422,11 +1377,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             if (lane == 0) {
                 const uint64_t dq = sdesc_sw128(smem_u32(qk), 16, 1024), dkx = sdesc_sw128(smem_u32(qk + kTileBytes), 16, 1024);
                 const uint64_t dc = sdesc_sw128(smem_u32(coef), 16, 1024);
-                const uint64_t dgk = sdesc_sw128(smem_u32(gk), 16, 1024);               // K-major Gamma^K hi (N = 128)
-                const uint64_t dgt = sdesc_sw128(smem_u32(gk), kTileBytes, 1024);       // MN-major Gamma^K^T (M = 128)
-                const uint64_t dso = sdesc_sw128(smem_u32(sop), 8192, 1024);            // MN-major state operand
+                const uint64_t dbh = sdesc_sw128(smem_u32(gb), 16, 1024);               // K-major [Gamma^K ; S^T] hi (N = 208)
+                const uint64_t dbl = dadd(dbh, L::kBHalf);                              // ... lo
+                const uint64_t dgt = sdesc_sw128(smem_u32(gb), L::kBHalf, 1024);        // MN-major [Gamma^K_hi ; Gamma^K_lo]^T (M = 128)
                 const uint64_t dv = sdesc_sw128(smem_u32(vt), kTileBytes, 1024);        // MN-major [V | 1]
-                constexpr uint32_t i128 = idesc_bf16(kTile, 128, false, false);
+                constexpr uint32_t i208 = idesc_bf16(kTile, kTile + 80, false, false);
                 constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
                 // Two issue streams, each in chunk order:
                 //   key:   K scores (c), U (c)                       -- runs up to a chunk ahead
@@ -1478,19 +1433,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                         const int r = rbase + pdone;
                         if (mbar_test(gq, r & 1) && mbar_test(gkr, r & 1) && mbar_test(sready, r & 1)) {
                             tc_fence_after();
+                            // [P | num den] = gQhi [gK ; S^T]hi^T + gQhi [gK ; S^T]lo^T + gQlo [gK ; S^T]hi^T
 #pragma unroll 1
                             for (int kk = 0; kk < kKP / 16; ++kk) {
                                 const uint32_t aq = tmem + kXQ + kk * 8;
-                                umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kk * 32), i128, kk > 0 ? 1u : 0u);
-                                umma_bf16_tA(tmem + kPD, aq, dadd(dgk, kTileBytes + kk * 32), i128, 1u);
-                                umma_bf16_tA(tmem + kPD, aq + 32, dadd(dgk, kk * 32), i128, 1u);
-                            }
-#pragma unroll 1
-                            for (int kk = 0; kk < kKP / 16; ++kk) {
-                                const uint64_t bh_ = dadd(dso, kk * 2048), bl_ = dadd(dso, 16384 + kk * 2048);
-                                umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bh_, i80s, kk > 0 ? 1u : 0u);
-                                umma_bf16_tA(tmem + kO, tmem + kXQ + 32 + kk * 8, bh_, i80s, 1u);
-                                umma_bf16_tA(tmem + kO, tmem + kXQ + kk * 8, bl_, i80s, 1u);
+                                umma_bf16_tA(tmem + kPD, aq, dadd(dbh, kk * 32), i208, kk > 0 ? 1u : 0u);
+                                umma_bf16_tA(tmem + kPD, aq, dadd(dbl, kk * 32), i208, 1u);
+                                umma_bf16_tA(tmem + kPD, aq + 32, dadd(dbh, kk * 32), i208, 1u);
                             }
                             umma_commit(pfull);
                             ++pdone;
@@ -1538,7 +1487,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 if (!wait_or_abort(sq, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
-                const float rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, row, 1);
+                const float rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, 0, row, 1);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gq);
@@ -1579,7 +1528,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 if (!wait_or_abort(sk, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
-                gamma_row(tmem + lb + kSK, cvec, 1, 0u, gk, row, (t0 + i) * kTile + row < N ? 1 : 0);
+                gamma_row(tmem + lb + kSK, cvec, 1, 0u, gb, L::kBHalf, row, (t0 + i) * kTile + row < N ? 1 : 0);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gkr);
@@ -1608,9 +1557,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 // the next chunk (the state read of this chunk is done: pfull)
                 if (carry) {
                     named_sync(1, 128);
-                    carry_finish(S, X, sop, row);
-                    fence_proxy_async_smem();
+                    carry_finish(S, X, row);
                     named_sync(1, 128);
+                    state_operand(gb, S, tid - 192);
+                    fence_proxy_async_smem();
+                    __syncwarp();
                     if (lane == 0) mbar_arrive(sready);
                 }
             }
