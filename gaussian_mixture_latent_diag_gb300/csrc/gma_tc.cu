@@ -970,16 +970,19 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
             const uint32_t gbase = tmem + lane_base + grp * kGC;
             uint8_t *stage = stg + (grp * 8 + ((warp - 2) & 7)) * 4096;
             const int pair_bar = 1 + grp * 4 + quad;  // named barrier of the two warps of these rows
-            for (int i = (grp - rbase % kNGR + kNGR) % kNGR; i < n; i += kNGR) {
-                const int r = rbase + i, s = r % QS;
+            const int i0 = (grp - rbase % kNGR + kNGR) % kNGR;  // this group's first tile of the job
+            for (int i = i0; i < n; i += kNGR) {
+                const int r = rbase + i;
                 float2 *xr = xch + ((grp * 2 + ((r / kNGR) & 1)) * 128 + row) * 2;  // [hf] (max, sum)
-                if (!wait_or_abort(&qfull[s], (r / QS) & 1, status, abort_flag)) break;
-                prep_x2_half_tmem(qst + s * kTileBytes, row, hf, gbase);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xready[grp]);
+                if (i == i0) {  // x^2 of the group's first tile (later ones are prepared a tile ahead)
+                    if (!wait_or_abort(&qfull[r % QS], (r / QS) & 1, status, abort_flag)) break;
+                    prep_x2_half_tmem(qst + (r % QS) * kTileBytes, row, hf, gbase);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xready[grp]);
+                }
                 if (!wait_or_abort(&sfull[grp], (r / kNGR) & 1, status, abort_flag)) break;
-                if (i < kNGR && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
+                if (i == i0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 float rs;
                 {
@@ -1022,6 +1025,17 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
                     }
                 }
                 tc_fence_before();
+                // x^2 of the group's next tile: the read MMAs have consumed the A columns and the
+                // accumulator is in registers, so its score MMAs can start while these outputs
+                // are stored.
+                if (i + kNGR < n) {
+                    const int r2 = r + kNGR;
+                    if (!wait_or_abort(&qfull[r2 % QS], (r2 / QS) & 1, status, abort_flag)) break;
+                    prep_x2_half_tmem(qst + (r2 % QS) * kTileBytes, row, hf, gbase);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xready[grp]);
+                }
                 stage_and_store_half(stage, o, lane, lane, &tmO, o_bf16, hf, (t0 + i) * kTile + 32 * quad, bh);
             }
             if (lane == 0) bulk_wait_read0();  // staging reusable; kernel completion publishes the stores
