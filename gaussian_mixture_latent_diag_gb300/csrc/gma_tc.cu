@@ -1,5 +1,5 @@
 // gma_tc.cu -- tcgen05 tensor-core kernels for the GMA forward pass (bf16
-// inputs, d_r = d_v = 64, K <= 64).
+// inputs, d_r = 32 or 64 (32 runs zero-padded to 64), d_v = 64, K <= 64).
 //
 // Responsibilities ([GMA, Eqs. (2)-(3)]) are computed as a GEMM on the
 // expanded quadratic,
@@ -65,8 +65,8 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
 // ------------------------------------------------------------------ coefficient prep
 // Grid (KP / 8, H): block (b, h) writes components 8b .. 8b + 7 of head h's
 // coefficient image -- the four bf16 matrices in the K-major SW128 byte image
-// the score MMA reads (rows = components, 128 B of d_r per row) and c_k (fp32,
-// -inf for padded components) -- and validates their parameters into its
+// the score MMA reads (rows = components, 64 routing columns per row, zero past
+// d_r) and c_k (fp32, -inf for padded components) -- and validates their parameters into its
 // error word err[h * (KP / 8) + b].  Each thread handles four consecutive j of
 // one component; the 16 threads of a component (one half-warp) also sum its
 // log-determinant terms.  Being the first kernel of a call, it also clears the
@@ -75,7 +75,7 @@ constexpr int kPrepBlocks = kKP / 8;
 
 __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restrict__ mu,
                                                            const float *__restrict__ sigma2,
-                                                           const float *__restrict__ log_pi, int K,
+                                                           const float *__restrict__ log_pi, int K, int DR,
                                                            uint8_t *__restrict__ img, unsigned *status,
                                                            unsigned *head_err, unsigned *counters, int BH) {
     const int tid = threadIdx.x, h = blockIdx.y;
@@ -84,14 +84,15 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
     for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     uint8_t *coef = img + (size_t)h * kCoefStride;
     const int k = blockIdx.x * 8 + (tid >> 4), j = (tid & 15) * 4;
-    const bool real = k < K;
+    const bool realk = k < K;
+    const bool real = realk && j < DR;  // d_r < 64: columns DR .. 63 are zero padding
     float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float lp = 0.f;
     if (real) {
-        s4 = *reinterpret_cast<const float4 *>(sigma2 + ((size_t)h * K + k) * kDR + j);
-        m4 = *reinterpret_cast<const float4 *>(mu + ((size_t)h * K + k) * kDR + j);
-        lp = log_pi[(size_t)h * K + k];
+        s4 = *reinterpret_cast<const float4 *>(sigma2 + ((size_t)h * K + k) * DR + j);
+        m4 = *reinterpret_cast<const float4 *>(mu + ((size_t)h * K + k) * DR + j);
     }
+    if (realk) lp = log_pi[(size_t)h * K + k];
     const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, mv[4] = {m4.x, m4.y, m4.z, m4.w};
     bool bad = false;
     uint32_t ah[2], al[2], bh[2], bl[2];
@@ -121,8 +122,8 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
     *reinterpret_cast<uint2 *>(coef + 2 * kCoefMatBytes + off) = make_uint2(bh[0], bh[1]);
     *reinterpret_cast<uint2 *>(coef + 3 * kCoefMatBytes + off) = make_uint2(bl[0], bl[1]);
     if (j == 0) {
-        if (real && !isfinite(lp)) bad = true;
-        reinterpret_cast<float *>(coef + 4 * kCoefMatBytes)[k] = real ? kLog2e * (lp - 0.5f * det) : -INFINITY;
+        if (realk && !isfinite(lp)) bad = true;
+        reinterpret_cast<float *>(coef + 4 * kCoefMatBytes)[k] = realk ? kLog2e * (lp - 0.5f * det) : -INFINITY;
     }
     const int any = __syncthreads_or(bad ? 1 : 0);
     if (tid == 0) head_err[h * kPrepBlocks + blockIdx.x] = any ? (unsigned)GMA_ERR_NONFINITE_PARAM : 0u;
@@ -1606,8 +1607,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [BH][N][d] bf16 tensor, boxes of 64 columns x 128 rows x 1 head, 128-byte
-// swizzle; rows past N read as zero.
+// [BH][N][d] bf16 tensor (d = 32 or 64), boxes of 64 columns x 128 rows x 1
+// head, 128-byte swizzle; rows past N and columns past d read as zero (so a
+// d = 32 tile arrives zero-padded to the 64-column layout the kernels use).
 bool make_map(CUtensorMap *map, const void *base, int BH, int N, int d) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -1722,7 +1724,7 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
         return cudaErrorInvalidValue;
     unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
+    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, coef, status, head_err, counters, p.BH());
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
@@ -1749,7 +1751,7 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
         return cudaErrorInvalidValue;
     unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, coef, status, head_err, counters, p.BH());
+    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, coef, status, head_err, counters, p.BH());
     GMA_TRY(cudaGetLastError());
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
@@ -1774,7 +1776,7 @@ const char *const kTcStages[3][8] = {
 };
 
 bool tc_supported(const Problem &p, int causal) {
-    if (p.dtype != GMA_BF16 || p.d_r != kDR || p.K > kKP) return false;
+    if (p.dtype != GMA_BF16 || (p.d_r != kDR && p.d_r != kDR / 2) || p.K > kKP) return false;
     if (causal == 0) return p.d_v == 64;
     return causal == 1 && p.d_v == 64;
 }
