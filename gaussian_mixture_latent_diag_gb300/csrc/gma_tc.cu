@@ -669,8 +669,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
                 __threadfence();
                 combine_partials(part, P, bh, mode, red, tid, kThreadsG);
                 if (mode == 0) {
+                    // the bf16 hi / lo read operand, built in shared memory (over the idle K
+                    // ring, after the reduction buffer) and copied out with 16-byte stores
+                    constexpr int kImgBytes = 2 * (D_V + 16) * 128;
+                    uint8_t *img = smem + 128 * W * 4 + 1024;
+                    static_assert(128 * W * 4 + 1024 + kImgBytes <= L::kVst, "image fits over the K ring");
                     cta_sync();
-                    store_memory_operand<D_V>(red, W, mem_img + (size_t)bh * mem_img_stride, tid, kThreadsG);
+                    store_memory_operand<D_V>(red, W, img, tid, kThreadsG);
+                    cta_sync();
+                    uint4 *dst = reinterpret_cast<uint4 *>(mem_img + (size_t)bh * mem_img_stride);
+                    for (int e = tid; e < kImgBytes / 16; e += kThreadsG) __stcg(dst + e, reinterpret_cast<const uint4 *>(img)[e]);
                 }
                 if (tid == 0) counters[bh] = 0u;  // ready for the next call
             }
