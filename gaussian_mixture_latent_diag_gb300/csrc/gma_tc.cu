@@ -80,6 +80,9 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
                                                            unsigned *head_err, unsigned *counters, int BH) {
     const int tid = threadIdx.x, h = blockIdx.y;
     const int gt = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + tid;
+    // The previous call's kernels may still read the status, counters and images.
+    pdl_wait();
+    pdl_trigger();
     if (gt == 0) *status = 0u;
     for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     uint8_t *coef = img + (size_t)h * kCoefStride;
@@ -462,13 +465,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
-    if (failed(status) || g0 >= gend) return;
+    if (g0 >= gend) return;
 
     if (warp == 0) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    const unsigned herr = warp == 1 ? head_error_warp(head_err, H, lane) : 0u;
     if (tid == 32) {
         for (int i = 0; i < KS; ++i) {
             mbar_init(&kfull[i], 1);
@@ -486,8 +488,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         }
         mbar_init(accfull, 1);
         mbar_init(cfull, 1);
-        if (herr) set_status(status, herr);
-        *abort_flag = herr ? 1 : 0;
+        *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -495,6 +496,17 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     {   // the constant ones chunk
         const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
         for (int i = tid; i < kTileBytes / 16; i += kThreadsG) reinterpret_cast<uint4 *>(smem + L::kOnes)[i] = one4;
+    }
+    // Everything below reads the coefficient prep's output (and the workspace the
+    // previous call's kernels used): wait for it, then let the next kernel launch.
+    pdl_wait();
+    pdl_trigger();
+    {
+        const unsigned herr = warp == 1 ? head_error_warp(head_err, H, lane) : 0u;
+        if (tid == 32 && (herr || failed(status))) {
+            if (herr) set_status(status, herr);
+            *abort_flag = 1;
+        }
     }
     tc_fence_before();
     cta_sync();
@@ -868,10 +880,10 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
     float2 *xch = reinterpret_cast<float2 *>(smem + L::kX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *qfull = bars, *qempty = bars + QS, *xready = bars + 2 * QS, *sfull = xready + kNGR,
-             *gready = sfull + kNGR, *ofull = gready + kNGR, *cfull = ofull + kNGR;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cfull + 1);
-    int *abort_flag = reinterpret_cast<int *>(cfull + 2);
-    static_assert((2 * QS + 4 * kNGR + 3) * 8 <= 256, "barrier area");
+             *gready = sfull + kNGR, *ofull = gready + kNGR, *cfull = ofull + kNGR, *bfull = cfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + 1);
+    int *abort_flag = reinterpret_cast<int *>(bfull + 2);
+    static_assert((2 * QS + 4 * kNGR + 4) * 8 <= 256, "barrier area");
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -895,6 +907,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
             mbar_init(&ofull[i], 1);
         }
         mbar_init(cfull, 1);
+        mbar_init(bfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -903,6 +916,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
     tc_fence_before();
     cta_sync();
     tc_fence_after();
+    pdl_trigger();  // the next call's coefficient prep waits for this kernel's completion
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t i160 = idesc_bf16(kTile, 2 * NB, false, false);
     constexpr uint32_t i80 = idesc_bf16(kTile, NB, false, false);
@@ -913,12 +927,19 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
         // The previous job's MMAs and epilogues are done with the coefficients
-        // and the memory operand; this head's arrive on cfull.
+        // and the memory operand; this head's arrive on cfull / bfull.  The memory
+        // operand is written by the write kernel, which may still be finishing:
+        // only the thread that copies it waits for that kernel, so the Q loads,
+        // x^2 and score MMAs of the first tiles go ahead meanwhile.
         cta_sync();
         if (tid == 0) {
-            mbar_arrive_expect_tx(cfull, kCoefBytes + 2 * NB * 128);
+            mbar_arrive_expect_tx(cfull, kCoefBytes);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
-            bulk_load(bop, mem_img + (size_t)bh * mem_img_stride, 2 * NB * 128, cfull);
+        }
+        if (tid == 33) {
+            if (njob == 0) pdl_wait();
+            mbar_arrive_expect_tx(bfull, 2 * NB * 128);
+            bulk_load(bop, mem_img + (size_t)bh * mem_img_stride, 2 * NB * 128, bfull);
         }
 
         if (warp == 0) {
@@ -951,7 +972,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
                     }
                     if (nr < ns) {
                         const int r = rbase + nr, gb = r % kNGR;
-                        if (mbar_test(&gready[gb], (r / kNGR) & 1)) {
+                        if (mbar_test(&gready[gb], (r / kNGR) & 1) && (nr > 0 || mbar_test(bfull, njob & 1))) {
                             tc_fence_after();
                             const uint32_t d = tmem + gb * kGC + kKP, a = tmem + gb * kGC;
 #pragma unroll
@@ -1310,9 +1331,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *qkfull = bars + 0, *qkempty = bars + 1, *vfull = bars + 2, *vempty = bars + 3, *xq = bars + 4,
              *xk = bars + 5, *sq = bars + 6, *sk = bars + 7, *gq = bars + 8, *gkr = bars + 9, *sready = bars + 10,
-             *pfull = bars + 11, *pready = bars + 12, *ofull = bars + 13, *ufull = bars + 14, *cfull = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    int *abort_flag = reinterpret_cast<int *>(bars + 17);
+             *pfull = bars + 11, *pready = bars + 12, *ofull = bars + 13, *ufull = bars + 14, *cfull = bars + 15,
+             *xfull = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+    int *abort_flag = reinterpret_cast<int *>(bars + 18);
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1328,7 +1350,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         mbar_init(qkfull, 1); mbar_init(qkempty, 1); mbar_init(vfull, 1); mbar_init(vempty, 1);
         mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
         mbar_init(gq, 4); mbar_init(gkr, 4); mbar_init(sready, 4); mbar_init(pfull, 1);
-        mbar_init(pready, 8); mbar_init(ofull, 1); mbar_init(ufull, 1); mbar_init(cfull, 1);
+        mbar_init(pready, 8); mbar_init(ofull, 1); mbar_init(ufull, 1); mbar_init(cfull, 1); mbar_init(xfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
@@ -1341,6 +1363,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     tc_fence_before();
     cta_sync();
     tc_fence_after();
+    pdl_trigger();  // the next call's coefficient prep waits for this kernel's completion
     const uint32_t tmem = *tmem_slot;
 
     int rbase = 0, njob = 0;
@@ -1352,18 +1375,18 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         // area; this head's coefficients and the job's carried-in prefix arrive on cfull.
         fence_proxy_async_smem();
         cta_sync();
+        // The carried-in prefix is written by the aggregation kernel, which may still
+        // be finishing: only the thread that copies it waits for that kernel, so the
+        // loads and score MMAs of the first chunk go ahead meanwhile.
         if (tid == 0) {
-            mbar_arrive_expect_tx(cfull, kCoefBytes + kKP * W * 4);
+            mbar_arrive_expect_tx(cfull, kCoefBytes);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
-            bulk_load(S, prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W, kKP * W * 4, cfull);
         }
-        if (warp >= 6) {  // key group: state operand of the job's first chunk
-            if (wait_or_abort(cfull, njob & 1, status, abort_flag)) state_operand(gb, S, tid - 192);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sready);
+        if (tid == 33) {
+            if (njob == 0) pdl_wait();
+            mbar_arrive_expect_tx(xfull, kKP * W * 4);
+            bulk_load(S, prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W, kKP * W * 4, xfull);
         }
-
         if (warp == 0) {
             if (lane == 0) {
                 // Q|K and V loads, each as soon as its stage is free.
@@ -1552,6 +1575,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 tc_fence_after();
                 gamma_row(tmem + lb + kSK, cvec, 1, 0u, gb, L::kBHalf, row, (t0 + i) * kTile + row < N ? 1 : 0);
+                if (i == 0) {
+                    // State operand of the job's first chunk, from the carried-in prefix.
+                    // Before the gkr arrival: U of this chunk (which the carry adds into
+                    // S) is issued only after every key warp has arrived, i.e. has read S.
+                    if (wait_or_abort(xfull, njob & 1, status, abort_flag)) state_operand(gb, S, tid - 192);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sready);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gkr);
@@ -1663,6 +1695,24 @@ bool make_out_map_half(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
     return r == CUDA_SUCCESS;
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel of the stream finishes; it waits (pdl_wait) before
+// touching what that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 template <typename KernelT>
 cudaError_t set_smem(KernelT kern, int bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1732,18 +1782,16 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
         return cudaErrorInvalidValue;
     unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, coef, status, head_err, counters, p.BH());
-    GMA_TRY(cudaGetLastError());
+    GMA_TRY(launch_pdl(coef_prep_tc_kernel, dim3(kPrepBlocks, p.H), dim3(128), 0, s, p.mu, p.sigma2, p.log_pi, p.K,
+                       p.d_r, coef, status, head_err, counters, p.BH()));
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
-    tc_write2_kernel<<<L.nctas, kThreadsG, Write2Smem::kAlloc, s>>>(
-        tk, tv, coef, head_err, p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status);
-    GMA_TRY(cudaGetLastError());
+    GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
+                       p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status));
     clk.mark();
     GMA_TRY(set_smem(tc_read3_kernel, Read3Smem::kAlloc));
-    tc_read3_kernel<<<L.nctas, kThreadsR, Read3Smem::kAlloc, s>>>(
-        tq, to, coef, p.H, p.N, L.P, mem, L.mem_stride, p.eps, p.o_bf16 ? 1 : 0, status);
-    GMA_TRY(cudaGetLastError());
+    GMA_TRY(launch_pdl(tc_read3_kernel, dim3(L.nctas), dim3(kThreadsR), Read3Smem::kAlloc, s, tq, to, coef, p.H, p.N,
+                       L.P, mem, L.mem_stride, p.eps, p.o_bf16 ? 1 : 0, status));
     clk.mark();
     return cudaSuccess;
 }
@@ -1759,18 +1807,16 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
         return cudaErrorInvalidValue;
     unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
     clk.mark();
-    coef_prep_tc_kernel<<<dim3(kPrepBlocks, p.H), 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, coef, status, head_err, counters, p.BH());
-    GMA_TRY(cudaGetLastError());
+    GMA_TRY(launch_pdl(coef_prep_tc_kernel, dim3(kPrepBlocks, p.H), dim3(128), 0, s, p.mu, p.sigma2, p.log_pi, p.K,
+                       p.d_r, coef, status, head_err, counters, p.BH()));
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
-    tc_write2_kernel<<<L.nctas, kThreadsG, Write2Smem::kAlloc, s>>>(
-        tk, tv, coef, head_err, p.H, p.N, L.P, part, counters, nullptr, 0, 1, status);
-    GMA_TRY(cudaGetLastError());
+    GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
+                       p.H, p.N, L.P, part, counters, static_cast<uint8_t *>(nullptr), size_t(0), 1, status));
     clk.mark();
     GMA_TRY(set_smem(tc_causal2_kernel, Causal2Smem::kAlloc));
-    tc_causal2_kernel<<<L.nctas, kThreadsG, Causal2Smem::kAlloc, s>>>(
-        tq, tk, tv, to, coef, part, p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status);
-    GMA_TRY(cudaGetLastError());
+    GMA_TRY(launch_pdl(tc_causal2_kernel, dim3(L.nctas), dim3(kThreadsG), Causal2Smem::kAlloc, s, tq, tk, tv, to, coef,
+                       part, p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status));
     clk.mark();
     return cudaSuccess;
 }

@@ -116,6 +116,14 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream runs;
+// pdl_wait blocks the calling thread until that kernel has completed and its
+// memory is visible, pdl_trigger lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 // Allocation / deallocation are warp-wide (.sync.aligned).
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
