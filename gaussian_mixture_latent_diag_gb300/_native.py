@@ -31,7 +31,7 @@ class Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("chunk", ctypes.c_int), ("splits", ctypes.c_int),
                 ("sync_status", ctypes.c_int), ("o_bf16", ctypes.c_int),
                 ("stage_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("n_stage_events", ctypes.c_int)]
+                ("n_stage_events", ctypes.c_int), ("test_stall", ctypes.c_int)]
 
 
 class GmaError(RuntimeError):
@@ -91,10 +91,11 @@ def status_string(status: int) -> str:
 
 
 def options(path: int = PATH_AUTO, chunk: int = 0, splits: int = 0, sync_status: bool = False,
-            o_bf16: bool = False, stage_events=None):
-    """gma_options; `stage_events` is a list of torch.cuda.Event (or None)."""
+            o_bf16: bool = False, stage_events=None, test_stall: bool = False):
+    """gma_options; `stage_events` is a list of torch.cuda.Event (or None);
+    `test_stall` is the failure-path test hook (see include/gma.h)."""
     o = Options(int(path), int(chunk), int(splits), int(bool(sync_status)), int(bool(o_bf16)),
-                None, 0)
+                None, 0, int(bool(test_stall)))
     if stage_events:
         for e in stage_events:
             if not e.cuda_event:  # torch creates the CUDA event lazily, on first record

@@ -86,6 +86,7 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     p.O = O; p.dtype = dtype; p.eps = eps;
     p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     p.o_bf16 = options && options->o_bf16;
+    p.test_stall = options && options->test_stall;
 
     const size_t es = dtype == GMA_F32 ? 4 : 2;
     const size_t nr = es * (size_t)B * H * N * d_r, nv = es * (size_t)B * H * N * d_v;

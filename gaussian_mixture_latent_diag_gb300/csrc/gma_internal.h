@@ -18,6 +18,7 @@ struct Problem {
     void *O = nullptr;         // or Gamma (fp32) for the responsibilities entry point
     gma_dtype dtype = GMA_F32;  // inputs
     bool o_bf16 = false;        // output O in bf16 instead of fp32
+    bool test_stall = false;    // gma_options.test_stall (failure-path test hook)
     float eps = 0.f;
     int B = 0, H = 0, N = 0, d_r = 0, d_v = 0, K = 0;
     int BH() const { return B * H; }

@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part P,
     float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img, size_t mem_img_stride,
-    int mode, unsigned *status) {
+    int mode, int stall, unsigned *status) {
     using L = Write2Smem;
     constexpr int D_V = 64, W = L::W;
     constexpr int kTmemCols = 512;
@@ -516,6 +516,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
 
     int rbase = 0;   // running tile index of the CTA (barrier phases)
     int njob = 0;
+    int carm = -1;   // last job whose coefficient copy was armed (thread 0)
     for (int g = aborted(abort_flag) ? gend : g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
@@ -527,20 +528,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         if (tid == 0) {
             mbar_arrive_expect_tx(cfull, kCoefBytes);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
+            carm = njob;
         }
 
         if (warp == 0) {
             if (lane == 0) {
                 // K loads as far ahead as the K ring allows; V loads follow, never ahead of their K.
                 int nk = 0, nv = 0;
+                int karm[KS], varm[VS];  // running index of the last load armed per stage
+#pragma unroll
+                for (int q = 0; q < KS; ++q) karm[q] = -1;
+#pragma unroll
+                for (int q = 0; q < VS; ++q) varm[q] = -1;
                 Stall st;
                 while (nv < n) {
                     bool prog = false;
                     if (nk < n) {
                         const int r = rbase + nk, s = r % KS;
                         if (mbar_test(&kempty[s], ((r / KS) & 1) ^ 1)) {
-                            mbar_arrive_expect_tx(&kfull[s], kTileBytes);
-                            tma_load_3d(kst + s * kTileBytes, &tmK, 0, (t0 + nk) * kTile, bh, &kfull[s]);
+                            if (!(stall && r == 0)) {  // test hook: the first key tile is never loaded
+                                mbar_arrive_expect_tx(&kfull[s], kTileBytes);
+                                tma_load_3d(kst + s * kTileBytes, &tmK, 0, (t0 + nk) * kTile, bh, &kfull[s]);
+                                karm[s] = r;
+                            }
                             ++nk;
                             prog = true;
                         }
@@ -550,6 +560,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
                         if (mbar_test(&vempty[s], ((r / VS) & 1) ^ 1)) {
                             mbar_arrive_expect_tx(&vfull[s], kTileBytes);
                             tma_load_3d(vst + s * kTileBytes, &tmV, 0, (t0 + nv) * kTile, bh, &vfull[s]);
+                            varm[s] = r;
                             ++nv;
                             prog = true;
                         }
@@ -559,6 +570,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
                         break;
                     }
                 }
+                // Every load armed here has landed before the CTA moves on or leaves
+                // (immediate unless the job was aborted).
+#pragma unroll
+                for (int q = 0; q < KS; ++q)
+                    if (karm[q] >= 0) mbar_wait(&kfull[q], (karm[q] / KS) & 1);
+#pragma unroll
+                for (int q = 0; q < VS; ++q)
+                    if (varm[q] >= 0) mbar_wait(&vfull[q], (varm[q] / VS) & 1);
             }
         } else if (warp == 1) {
             if (lane == 0) {
@@ -699,6 +718,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
         g += n;
         if (aborted(abort_flag)) break;
     }
+    if (tid == 0 && carm >= 0) mbar_wait(cfull, carm & 1);  // the last coefficient copy has landed
     tc_fence_before();
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -922,6 +942,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
     constexpr uint32_t i80 = idesc_bf16(kTile, NB, false, false);
 
     int rbase = 0, njob = 0;
+    int barm = -1;  // last job whose coefficient and memory-operand copies were armed
     for (int g = g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
@@ -941,15 +962,25 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
             mbar_arrive_expect_tx(bfull, 2 * NB * 128);
             bulk_load(bop, mem_img + (size_t)bh * mem_img_stride, 2 * NB * 128, bfull);
         }
+        barm = njob;
 
         if (warp == 0) {
-            if (lane == 0)
+            if (lane == 0) {
+                int qarm[QS];  // running index of the last load armed per stage
+#pragma unroll
+                for (int q = 0; q < QS; ++q) qarm[q] = -1;
                 for (int i = 0; i < n; ++i) {
                     const int r = rbase + i, s = r % QS;
                     if (!wait_or_abort(&qempty[s], ((r / QS) & 1) ^ 1, status, abort_flag)) break;
                     mbar_arrive_expect_tx(&qfull[s], kTileBytes);
                     tma_load_3d(qst + s * kTileBytes, &tmQ, 0, (t0 + i) * kTile, bh, &qfull[s]);
+                    qarm[s] = r;
                 }
+                // every load armed here has landed before the CTA moves on or leaves
+#pragma unroll
+                for (int q = 0; q < QS; ++q)
+                    if (qarm[q] >= 0) mbar_wait(&qfull[q], (qarm[q] / QS) & 1);
+            }
         } else if (warp == 1) {
             if (lane == 0) {
                 const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024), dc0 = sdesc_sw128(smem_u32(coef), 16, 1024);
@@ -1075,6 +1106,9 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
         cta_sync();
         if (aborted(abort_flag)) break;
     }
+    // the last bulk copies have landed before the CTA leaves
+    if (tid == 0 && barm >= 0) mbar_wait(cfull, barm & 1);
+    if (tid == 33 && barm >= 0) mbar_wait(bfull, barm & 1);
     tc_fence_before();
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -1367,6 +1401,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     const uint32_t tmem = *tmem_slot;
 
     int rbase = 0, njob = 0;
+    int barm = -1;  // last job whose coefficient and prefix copies were armed
     for (int g = g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
@@ -1387,10 +1422,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             mbar_arrive_expect_tx(xfull, kKP * W * 4);
             bulk_load(S, prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W, kKP * W * 4, xfull);
         }
+        barm = njob;
         if (warp == 0) {
             if (lane == 0) {
                 // Q|K and V loads, each as soon as its stage is free.
-                int nq = 0, nv = 0;
+                int nq = 0, nv = 0, qarm = -1, varm = -1;
                 Stall st;
                 while (nv < n) {
                     bool prog = false;
@@ -1400,6 +1436,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                             mbar_arrive_expect_tx(qkfull, 2 * kTileBytes);
                             tma_load_3d(qk, &tmQ, 0, (t0 + nq) * kTile, bh, qkfull);
                             tma_load_3d(qk + kTileBytes, &tmK, 0, (t0 + nq) * kTile, bh, qkfull);
+                            qarm = r;
                             ++nq;
                             prog = true;
                         }
@@ -1409,6 +1446,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                         if (mbar_test(vempty, (r & 1) ^ 1)) {
                             mbar_arrive_expect_tx(vfull, kTileBytes);
                             tma_load_3d(vt, &tmV, 0, (t0 + nv) * kTile, bh, vfull);
+                            varm = r;
                             ++nv;
                             prog = true;
                         }
@@ -1418,6 +1456,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                         break;
                     }
                 }
+                // every load armed here has landed before the CTA moves on or leaves
+                if (qarm >= 0) mbar_wait(qkfull, qarm & 1);
+                if (varm >= 0) mbar_wait(vfull, varm & 1);
             }
         } else if (warp == 1) {
             if (lane == 0) {
@@ -1626,6 +1667,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         cta_sync();
         if (aborted(abort_flag)) break;
     }
+    // the last bulk copies have landed before the CTA leaves
+    if (tid == 0 && barm >= 0) mbar_wait(cfull, barm & 1);
+    if (tid == 33 && barm >= 0) mbar_wait(xfull, barm & 1);
     tc_fence_before();
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -1787,7 +1831,7 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
-                       p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, status));
+                       p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, p.test_stall ? 1 : 0, status));
     clk.mark();
     GMA_TRY(set_smem(tc_read3_kernel, Read3Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_read3_kernel, dim3(L.nctas), dim3(kThreadsR), Read3Smem::kAlloc, s, tq, to, coef, p.H, p.N,
@@ -1812,7 +1856,8 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
-                       p.H, p.N, L.P, part, counters, static_cast<uint8_t *>(nullptr), size_t(0), 1, status));
+                       p.H, p.N, L.P, part, counters, static_cast<uint8_t *>(nullptr), size_t(0), 1, p.test_stall ? 1 : 0,
+                       status));
     clk.mark();
     GMA_TRY(set_smem(tc_causal2_kernel, Causal2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_causal2_kernel, dim3(L.nctas), dim3(kThreadsG), Causal2Smem::kAlloc, s, tq, tk, tv, to, coef,

@@ -83,6 +83,12 @@ typedef struct gma_options {
      * gma_stage_name().  The events are owned by the caller. */
     void **stage_events;
     int n_stage_events;
+    /* Test hook for the failure path, leave 0.  Nonzero: the tensor-core key
+     * pass never loads its first key tile, so the first bounded device wait on
+     * it runs out (after 4 s) and the call reports GMA_ERR_TIMEOUT through the
+     * status word; every kernel still finishes and frees what it holds, and the
+     * stream and workspace stay usable.  No effect on the SIMT path. */
+    int test_stall;
 } gma_options;
 
 /*
