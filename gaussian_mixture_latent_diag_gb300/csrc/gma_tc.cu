@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part P,
     float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img, size_t mem_img_stride,
-    int mode, int stall, unsigned *status) {
+    uint8_t *__restrict__ gk_out, int mode, int stall, unsigned *status) {
     using L = Write2Smem;
     constexpr int D_V = 64, W = L::W;
     constexpr int kTmemCols = 512;
@@ -631,6 +631,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
             const int grp = (warp - 2) >> 2;  // 0 .. NG-1
             const int row = epi_row(warp, lane);
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+            // mode 1 also stores each tile's Gamma^K buffer (bf16 hi / lo, 32 KB) for the
+            // causal scan: a warp's 32 rows are four 8-row groups, one contiguous 8 KB
+            // slice, which the warp stores itself (no cross-warp barrier).
+            const int q4 = warp & 3;
             for (int i = (grp - rbase % kNG + kNG) % kNG; i < n; i += kNG) {
                 const int r = rbase + i, sk = r % KS;
                 uint8_t *gbuf = xg + grp * 2 * kTileBytes;
@@ -649,11 +653,23 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
                 uint32_t wh[32], wl[32];
                 split_row(e, tok < N ? 1.0f / rs : 0.0f, wh, wl);
                 if (r >= kNG && !wait_or_abort(&wdone[grp], ((r - kNG) / kNG) & 1, status, abort_flag)) break;
+                if (mode == 1) {  // the warp's previous bulk store has read its slice
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                }
                 store_gamma_words(gbuf, row, wh, wl);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&gready[grp]);
+                if (lane == 0) {
+                    mbar_arrive(&gready[grp]);
+                    if (mode == 1) {
+                        const size_t off = ((size_t)bh * P.ntiles + t0 + i) * (2 * kTileBytes) + 8192 * q4;
+                        bulk_store(gk_out + off, gbuf + 8192 * q4, 8192);
+                        bulk_commit();
+                    }
+                }
             }
+            if (mode == 1 && lane == 0) bulk_wait_read0();
         }
         // ---- job end: the accumulated memory -> partial of this job
         cta_sync();
@@ -722,41 +738,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     tc_fence_before();
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-}
-
-// Output staging for TMA stores: each epilogue warp owns 8 KB (its 32 rows),
-// fp32: two [32 rows x 128 B] swizzled boxes (columns 0-31 | 32-63);
-// bf16: one [32 rows x 128 B] swizzled box.  o holds the row's 64 values.
-__device__ __forceinline__ void stage_and_store_rows(uint8_t *stage, const float (&o)[64], int r32, int lane,
-                                                     const CUtensorMap *tmO, int o_bf16, int row0, int bh) {
-    if (lane == 0) bulk_wait_read0();  // this warp's previous stores have read the staging area
-    __syncwarp();
-    if (o_bf16) {
-        uint8_t *rp = stage + r32 * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 w = make_uint4(pack_bf2(o[8 * c], o[8 * c + 1]), pack_bf2(o[8 * c + 2], o[8 * c + 3]),
-                                       pack_bf2(o[8 * c + 4], o[8 * c + 5]), pack_bf2(o[8 * c + 6], o[8 * c + 7]));
-            *reinterpret_cast<uint4 *>(rp + ((c ^ (r32 & 7)) << 4)) = w;
-        }
-    } else {
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            uint8_t *rp = stage + b * 4096 + r32 * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int k = 32 * b + 4 * c;
-                *reinterpret_cast<float4 *>(rp + ((c ^ (r32 & 7)) << 4)) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-            }
-        }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        tma_store_3d(tmO, stage, 0, row0, bh);
-        if (!o_bf16) tma_store_3d(tmO, stage + 4096, 32, row0, bh);
-        bulk_commit();
-    }
 }
 
 // ------------------------------------------------------------------ read, split rows
@@ -1123,42 +1104,53 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
 // then (S, Z) += Gamma^K_c^T [V_c | 1].  The job's starting prefix is the
 // exclusive prefix left in the partials by tc_write2_kernel (mode 1).
 //
-// Warps: 0 TMA, 1 MMA issuer, 2..5 query group (x^2, softmax, half of the P
-// split, outputs), 6..9 key group (x^2, softmax, Gamma^K, the other half of
-// the P split, carry of the state).  The state increment U is issued right
-// after P, so the carry runs beside the P split and the P [V | 1] MMAs; the
-// output epilogue of a chunk runs beside the score MMAs of the next.
+// Gamma^K of each chunk is not recomputed: the aggregation pass (tc_write2_kernel,
+// mode 1) stores every key tile's normalised bf16 hi / lo Gamma^K, the same values
+// by the same arithmetic, and this kernel loads it by bulk copy.
+//
+// Warps: 0 lane 0 Q / V loads, 0 lane 1 Gamma^K loads, 1 MMA issuer, 2..5 query
+// group (x^2, softmax, half of the P split, outputs), 6..9 key group (the other
+// half of the P split, carry of the state).  The carry runs beside the P split
+// and the P [V | 1] MMAs; the next chunk's x^2 is prepared right after the P MMAs.
 //
 // TMEM (512 columns):
 //   [0, 64)    x^2 of Q -> Gamma^Q hi | lo          (MMA A operands)
-//   [64, 128)  x^2 of K
-//   [128, 256) scores Q (N = 128) -> P, then P hi | lo in place per 32-key block
-//   [256, 336) [num | den]: one N = 208 accumulator with P for the P + state-read MMAs
-//   [336, 464) scores K (N = 128) -> state increment U = [gK_hi ; gK_lo]^T [V | 1] (N = 80)
+//   [64, 192)  scores Q (N = 128): own columns, so the next chunk's score MMAs
+//              overlap this chunk's P split and P [V | 1]
+//   [192, 320) P, then P hi | lo in place per 32-key block
+//   [320, 400) [num | den]: one N = 208 accumulator with P for the P + state-read MMAs
+//   [400, 480) state increment U = [gK_hi ; gK_lo]^T [V | 1] (N = 80)
 // The B operand of the P + state-read MMAs is [Gamma^K ; S^T] (128 + 80 K-major
 // rows), so P and the read of the carried state share each instruction.
-// MMAs per chunk: scores 12 + 12, P + state read 12 (N = 208), U 8, P [V|1] 16.
+// MMAs per chunk: Q scores 12, P + state read 12 (N = 208), U 8, P [V|1] 16.
 struct Causal2Smem {
     static constexpr int W = kW;                           // fp32 state rows (float4 access)
     static constexpr int WX = 66;                          // carry exchange rows (float2 access)
-    // B operand of the P + state-read MMAs, K-major SW128, rows of 64 components:
-    // [Gamma^K_hi (128 token rows) ; S_hi^T (80 value rows)] then the same for lo.
-    static constexpr int kBRows = kTile + 80;
-    static constexpr int kBHalf = kBRows * 128;            // 26 KB, a multiple of 1 KB
-    static constexpr int kQK = 0;                          // Q tile | K tile (one stage)
-    static constexpr int kV = kQK + 2 * kTileBytes;        // V tile | ones chunk
-    static constexpr int kGB = kV + 2 * kTileBytes;        // [Gamma^K ; S^T] hi | lo
-    static constexpr int kStage = kGB + 2 * kBHalf;        // output staging 4 x 8 KB
+    // B operand of the P + state-read MMAs, K-major SW128 rows of 64 components in
+    // 8-row groups of 2 KB (hi rows | lo rows): 16 groups of Gamma^K (token rows, the
+    // aggregation pass's stored buffer as is) then 10 groups of S^T (value rows).
+    static constexpr int kGroups = (kTile + 80) / 8;
+    static constexpr int kQS = 2;                          // Q ring depth
+    static constexpr int kVS = 2;                          // V ring depth
+    static constexpr int kQ = 0;
+    static constexpr int kV = kQ + kQS * kTileBytes;       // V tiles
+    // ones columns of [V | 1]: every element is 1, so one K step (16 rows, 2 KB) serves
+    // all of them; each K step's descriptor points its second N chunk here (LBO)
+    static constexpr int kOnes = kV + kVS * kTileBytes;
+    static constexpr int kGB = kOnes + 2048;               // [Gamma^K ; S^T]
+    static constexpr int kStage = kGB + kGroups * 2048;    // output staging 4 x 8 KB
     static constexpr int kCoef = kStage + 4 * 8192;
     static constexpr int kS = kCoef + kCoefBytes;          // fp32 state [64][W]
     static constexpr int kX = kS + kKP * W * 4;            // carry exchange [64][WX]
     static constexpr int kBars = kX + kKP * WX * 4;
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
-    static_assert(kBHalf % 1024 == 0 && kStage % 1024 == 0, "SW128 alignment");
+    static_assert(kOnes % 1024 == 0 && kGB % 1024 == 0 && kStage % 1024 == 0, "SW128 alignment");
     static_assert(kS % 16 == 0 && kX % 16 == 0 && kBars % 8 == 0, "alignment");
     static_assert(kAlloc <= 232448, "shared memory budget");
-};// Epilogue pieces shared by the query and the key groups of the causal
+};
+
+// Epilogue pieces shared by the query and the key groups of the causal
 // kernel.  They are kept out of line so that both groups run one copy of the
 // code: the kernel's speed is bound by instruction fetch when each role has
 // its own inlined copy.
@@ -1242,35 +1234,57 @@ __device__ __noinline__ void split_p_blocks(uint32_t p_taddr, int cb0, int row) 
     tmem_wait_st();
 }
 
-// Outputs of one query row of the causal kernel: [num | den] from TMEM,
-// O = num / (den + eps r), staged and stored by TMA (rows row0 .. row0 + 31
-// of head bh for the warp).
-__device__ __noinline__ void causal_output_row(uint32_t o_taddr, float rq, float eps, uint8_t *stage, int lane,
-                                               const CUtensorMap *tmO, int o_bf16, int row0, int bh) {
-    float o[64];
-    uint32_t a0[32], a1[32], dz[16];
+// Outputs of one query row of the causal kernel, O = num / (den + eps r) from the
+// [num | den] accumulator, written into this warp's 8 KB staging area as TMA store
+// boxes of [32 rows x 128 B], 128-byte swizzled: fp32, two boxes (columns 0-31 |
+// 32-63); bf16, one box.  The caller issues the stores afterwards.  Once the
+// accumulator is in registers, lane 0 arrives on `freed` (if given): the columns
+// may be overwritten while the row is staged.
+__device__ __noinline__ void stage_output_row(uint32_t o_taddr, float rq, float eps, uint8_t *stage, int lane,
+                                              int o_bf16, uint64_t *freed) {
+    uint32_t a0[32], a1[32];
     tmem_ld32(o_taddr, a0);
     tmem_ld32(o_taddr + 32, a1);
-    tmem_ld16(o_taddr + 64, dz);
+    const uint32_t dz = tmem_ld1(o_taddr + 64);
     tmem_wait_ld();
     tc_fence_before();
-    const float inv = 1.0f / (__uint_as_float(dz[0]) + eps * rq);
-#pragma unroll
-    for (int q = 0; q < 32; ++q) {
-        o[q] = __uint_as_float(a0[q]) * inv;
-        o[32 + q] = __uint_as_float(a1[q]) * inv;
+    __syncwarp();
+    if (lane == 0) {
+        if (freed) mbar_arrive(freed);
+        bulk_wait_read0();  // this warp's previous stores have read the staging area
     }
-    stage_and_store_rows(stage, o, lane, lane, tmO, o_bf16, row0, bh);
+    __syncwarp();
+    const float inv = 1.0f / (__uint_as_float(dz) + eps * rq);
+    auto v = [&](int k) { return __uint_as_float(k < 32 ? a0[k] : a1[k - 32]) * inv; };
+    if (o_bf16) {
+        uint8_t *rp = stage + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 w = make_uint4(pack_bf2(v(8 * c), v(8 * c + 1)), pack_bf2(v(8 * c + 2), v(8 * c + 3)),
+                                       pack_bf2(v(8 * c + 4), v(8 * c + 5)), pack_bf2(v(8 * c + 6), v(8 * c + 7)));
+            *reinterpret_cast<uint4 *>(rp + ((c ^ (lane & 7)) << 4)) = w;
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            uint8_t *rp = stage + b * 4096 + lane * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int k = 32 * b + 4 * c;
+                *reinterpret_cast<float4 *>(rp + ((c ^ (lane & 7)) << 4)) = make_float4(v(k), v(k + 1), v(k + 2), v(k + 3));
+            }
+        }
+    }
+    fence_proxy_async_smem();
 }
 
-// State operand: S^T stored K-major SW128 inside the B operand of the P +
-// state-read MMAs (gb: hi part, gb + kBHalf: lo part), row n = value column n
-// (n = 64 is Z; rows 65..79 stay zero), 64 components per 128-byte row.
-// Written by all 128 threads of the key group from the fp32 state S
-// ([64 components][kW]): item i < 65 * 8 is row n = i % 65, 8-component chunk
-// c = i / 65 (consecutive threads take consecutive n: conflict-free reads of S).
+// State operand: S^T inside the B operand of the P + state-read MMAs, value
+// row n (n = 64 is Z; rows 65..79 stay zero) in 8-row group 16 + n / 8 (hi rows,
+// lo rows 1 KB further), 64 components per 128-byte row.  Written by all 128
+// threads of the key group from the fp32 state S ([64 components][kW]): item
+// i < 65 * 8 is row n = i % 65, 8-component chunk c = i / 65 (consecutive threads
+// take consecutive n: conflict-free reads of S).
 __device__ __forceinline__ void state_operand_from_S(uint8_t *gb, const float *S, int t) {
-    uint8_t *sb = gb + kTile * 128;  // S^T rows follow the 128 Gamma^K rows
     for (int i = t; i < 65 * 8; i += 128) {
         const int n = i % 65, c = i / 65;
         uint32_t wh[4], wl[4];
@@ -1280,9 +1294,9 @@ __device__ __forceinline__ void state_operand_from_S(uint8_t *gb, const float *S
             wh[q] = pack_bf2(v0, v1);
             wl[q] = pack_bf2(v0 - bf_lo(wh[q]), v1 - bf_hi(wh[q]));
         }
-        const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
-        *reinterpret_cast<uint4 *>(sb + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(sb + Causal2Smem::kBHalf + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        const uint32_t off = (uint32_t)((kTile / 8 + (n >> 3)) * 2048 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
+        *reinterpret_cast<uint4 *>(gb + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(gb + off + 1024) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
     }
 }
 
@@ -1348,27 +1362,27 @@ __device__ __noinline__ void carry_finish(float *S, const float *X, int row) {
 __device__ __noinline__ void state_operand(uint8_t *gb, const float *S, int t) { state_operand_from_S(gb, S, t); }
 
 __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
-    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-    const uint8_t *__restrict__ coef_img, const float *__restrict__ prefix, int H, int N, Part P, float eps,
-    int o_bf16, unsigned *status) {
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
+    const __grid_constant__ CUtensorMap tmO, const uint8_t *__restrict__ coef_img, const uint8_t *__restrict__ gk_in,
+    const float *__restrict__ prefix, int H, int N, Part P, float eps, int o_bf16, unsigned *status) {
     using L = Causal2Smem;
-    constexpr int W = L::W;
+    constexpr int W = L::W, QS = L::kQS, VS = L::kVS;
     constexpr int kTmemCols = 512;
-    constexpr int kXQ = 0, kXK = 64, kSQ = 128, kPD = 128, kO = 256, kSK = 336, kU = 336;
+    constexpr int kXQ = 0, kSQ = 64, kPD = 192, kO = 320, kU = 400;
     static_assert(kO == kPD + 128, "[P | num den] is one N = 208 accumulator");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qk = smem + L::kQK, *vt = smem + L::kV, *gb = smem + L::kGB, *coef = smem + L::kCoef;
+    uint8_t *qst = smem + L::kQ, *vt = smem + L::kV, *gb = smem + L::kGB, *coef = smem + L::kCoef;
     float *S = reinterpret_cast<float *>(smem + L::kS), *X = reinterpret_cast<float *>(smem + L::kX);
     uint8_t *stg = smem + L::kStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-    uint64_t *qkfull = bars + 0, *qkempty = bars + 1, *vfull = bars + 2, *vempty = bars + 3, *xq = bars + 4,
-             *xk = bars + 5, *sq = bars + 6, *sk = bars + 7, *gq = bars + 8, *gkr = bars + 9, *sready = bars + 10,
-             *pfull = bars + 11, *pready = bars + 12, *ofull = bars + 13, *ufull = bars + 14, *cfull = bars + 15,
-             *xfull = bars + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
-    int *abort_flag = reinterpret_cast<int *>(bars + 18);
+    uint64_t *qfull = bars + 0, *qempty = bars + QS, *vfull = bars + 2 * QS, *vempty = vfull + VS,
+             *gfull = vfull + 2 * VS, *gempty = gfull + 1, *xq = gfull + 2, *sq = gfull + 3, *gq = gfull + 4,
+             *sready = gfull + 5, *pfull = gfull + 6, *pready = gfull + 7, *ofull = gfull + 8, *ufull = gfull + 9,
+             *cfull = gfull + 10, *xfull = gfull + 11;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + 1);
+    int *abort_flag = reinterpret_cast<int *>(xfull + 2);
+    static_assert((2 * QS + 2 * VS + 15) * 8 <= 256, "barrier area");
     const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1381,18 +1395,26 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         tmem_relinquish();
     }
     if (tid == 32) {
-        mbar_init(qkfull, 1); mbar_init(qkempty, 1); mbar_init(vfull, 1); mbar_init(vempty, 1);
-        mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
-        mbar_init(gq, 4); mbar_init(gkr, 4); mbar_init(sready, 4); mbar_init(pfull, 1);
-        mbar_init(pready, 8); mbar_init(ofull, 1); mbar_init(ufull, 1); mbar_init(cfull, 1); mbar_init(xfull, 1);
+        for (int i = 0; i < QS; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
+            mbar_init(&vfull[i], 1);
+            mbar_init(&vempty[i], 1);
+        }
+        mbar_init(gfull, 1); mbar_init(gempty, 1);
+        mbar_init(xq, 4); mbar_init(sq, 1); mbar_init(gq, 4); mbar_init(sready, 4);
+        mbar_init(pfull, 1); mbar_init(pready, 8); mbar_init(ofull, 1); mbar_init(ufull, 1);
+        mbar_init(cfull, 1); mbar_init(xfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
+        tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
     }
-    {   // constant ones chunk of the V stage; zero B operand (the S^T padding rows must be 0)
+    {   // constant ones columns of [V | 1]; zero B operand (the S^T padding rows must be 0)
         const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int i = tid; i < kTileBytes / 16; i += kThreadsG) reinterpret_cast<uint4 *>(vt + kTileBytes)[i] = one4;
-        for (int i = tid; i < 2 * L::kBHalf / 16; i += kThreadsG) reinterpret_cast<uint4 *>(gb)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 2048 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(smem + L::kOnes)[i] = one4;
+        for (int i = tid; i < L::kGroups * 2048 / 16; i += kThreadsG) reinterpret_cast<uint4 *>(gb)[i] = make_uint4(0, 0, 0, 0);
     }
     tc_fence_before();
     cta_sync();
@@ -1406,13 +1428,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
-        // The previous job is done with the coefficients, the state and the carry
-        // area; this head's coefficients and the job's carried-in prefix arrive on cfull.
+        // The previous job is done with the coefficients, the state and the carry area.
+        // The carried-in prefix and the stored Gamma^K come from the aggregation kernel,
+        // which may still be finishing: only the threads that copy them wait for it, so
+        // the Q loads, x^2, score MMAs and query softmax of the first chunk go ahead.
         fence_proxy_async_smem();
         cta_sync();
-        // The carried-in prefix is written by the aggregation kernel, which may still
-        // be finishing: only the thread that copies it waits for that kernel, so the
-        // loads and score MMAs of the first chunk go ahead meanwhile.
         if (tid == 0) {
             mbar_arrive_expect_tx(cfull, kCoefBytes);
             bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
@@ -1423,30 +1444,35 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             bulk_load(S, prefix + ((size_t)c * P.slots + slot_of(P, c, bh)) * kKP * W, kKP * W * 4, xfull);
         }
         barm = njob;
+
         if (warp == 0) {
             if (lane == 0) {
-                // Q|K and V loads, each as soon as its stage is free.
-                int nq = 0, nv = 0, qarm = -1, varm = -1;
+                // Q (ring of QS) and V (ring of VS) loads, each as soon as its stage is free.
+                int nq = 0, nv = 0;
+                int qarm[QS], varm[VS];
+#pragma unroll
+                for (int q = 0; q < QS; ++q) qarm[q] = -1;
+#pragma unroll
+                for (int q = 0; q < VS; ++q) varm[q] = -1;
                 Stall st;
                 while (nv < n) {
                     bool prog = false;
                     if (nq < n) {
-                        const int r = rbase + nq;
-                        if (mbar_test(qkempty, (r & 1) ^ 1)) {
-                            mbar_arrive_expect_tx(qkfull, 2 * kTileBytes);
-                            tma_load_3d(qk, &tmQ, 0, (t0 + nq) * kTile, bh, qkfull);
-                            tma_load_3d(qk + kTileBytes, &tmK, 0, (t0 + nq) * kTile, bh, qkfull);
-                            qarm = r;
+                        const int r = rbase + nq, s = r % QS;
+                        if (mbar_test(&qempty[s], ((r / QS) & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(&qfull[s], kTileBytes);
+                            tma_load_3d(qst + s * kTileBytes, &tmQ, 0, (t0 + nq) * kTile, bh, &qfull[s]);
+                            qarm[s] = r;
                             ++nq;
                             prog = true;
                         }
                     }
                     if (nv < nq) {
-                        const int r = rbase + nv;
-                        if (mbar_test(vempty, (r & 1) ^ 1)) {
-                            mbar_arrive_expect_tx(vfull, kTileBytes);
-                            tma_load_3d(vt, &tmV, 0, (t0 + nv) * kTile, bh, vfull);
-                            varm = r;
+                        const int r = rbase + nv, s = r % VS;
+                        if (mbar_test(&vempty[s], ((r / VS) & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(&vfull[s], kTileBytes);
+                            tma_load_3d(vt + s * kTileBytes, &tmV, 0, (t0 + nv) * kTile, bh, &vfull[s]);
+                            varm[s] = r;
                             ++nv;
                             prog = true;
                         }
@@ -1457,68 +1483,90 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     }
                 }
                 // every load armed here has landed before the CTA moves on or leaves
-                if (qarm >= 0) mbar_wait(qkfull, qarm & 1);
-                if (varm >= 0) mbar_wait(vfull, varm & 1);
+#pragma unroll
+                for (int q = 0; q < QS; ++q)
+                    if (qarm[q] >= 0) mbar_wait(&qfull[q], (qarm[q] / QS) & 1);
+#pragma unroll
+                for (int q = 0; q < VS; ++q)
+                    if (varm[q] >= 0) mbar_wait(&vfull[q], (varm[q] / VS) & 1);
+            } else if (lane == 1) {
+                // Gamma^K of each chunk, stored by the aggregation kernel (one 32 KB buffer).
+                if (njob == 0) pdl_wait();
+                int ng = 0, garm = -1;
+                Stall st;
+                while (ng < n) {
+                    const int r = rbase + ng;
+                    bool prog = false;
+                    if (mbar_test(gempty, (r & 1) ^ 1)) {
+                        mbar_arrive_expect_tx(gfull, 2 * kTileBytes);
+                        bulk_load(gb, gk_in + ((size_t)bh * P.ntiles + t0 + ng) * (2 * kTileBytes), 2 * kTileBytes, gfull);
+                        garm = r;
+                        ++ng;
+                        prog = true;
+                    }
+                    if (!st.tick(prog, abort_flag)) {
+                        note_timeout(status, abort_flag);
+                        break;
+                    }
+                }
+                if (garm >= 0) mbar_wait(gfull, garm & 1);
             }
         } else if (warp == 1) {
             if (lane == 0) {
-                const uint64_t dq = sdesc_sw128(smem_u32(qk), 16, 1024), dkx = sdesc_sw128(smem_u32(qk + kTileBytes), 16, 1024);
+                const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024);
                 const uint64_t dc = sdesc_sw128(smem_u32(coef), 16, 1024);
-                const uint64_t dbh = sdesc_sw128(smem_u32(gb), 16, 1024);               // K-major [Gamma^K ; S^T] hi (N = 208)
-                const uint64_t dbl = dadd(dbh, L::kBHalf);                              // ... lo
-                const uint64_t dgt = sdesc_sw128(smem_u32(gb), L::kBHalf, 1024);        // MN-major [Gamma^K_hi ; Gamma^K_lo]^T (M = 128)
-                const uint64_t dv = sdesc_sw128(smem_u32(vt), kTileBytes, 1024);        // MN-major [V | 1]
+                const uint64_t dbh = sdesc_sw128(smem_u32(gb), 16, 2048);          // K-major [Gamma^K ; S^T] hi (N = 208)
+                const uint64_t dbl = dadd(dbh, 1024);                              // ... lo
+                const uint64_t dgt = sdesc_sw128(smem_u32(gb), 1024, 2048);        // MN-major [Gamma^K_hi ; Gamma^K_lo]^T (M = 128)
+                // MN-major [V | 1] of V stage s at K step kk: V rows 16 kk.. of the stage, the
+                // ones columns at the 2 KB ones block (the LBO shrinks as the start grows)
+                auto dvk = [&](int s, int kk) {
+                    const uint32_t a = smem_u32(vt + s * kTileBytes) + kk * 2048;
+                    return sdesc_sw128(a, smem_u32(smem + L::kOnes) - a, 1024);
+                };
                 constexpr uint32_t i208 = idesc_bf16(kTile, kTile + 80, false, false);
                 constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
-                // Two issue streams, each in chunk order:
-                //   key:   K scores (c), U (c)                       -- runs up to a chunk ahead
-                //   query: Q scores (c), P + state read (c), P [V|1] (c)
-                // Q scores (c + 1) follow P [V|1] (c) in issue order, which they overwrite
-                // in the P / Q-score columns.  qkempty (c) is committed once both score
-                // sets of c are issued, vempty (c) once U (c) and P [V|1] (c) are.
-                int kdone = 0, udone = 0, qdone = 0, pdone = 0, vdone = 0;
+                // Per chunk: Q scores (own columns: issued as soon as the chunk's x^2 is
+                // ready, possibly before the previous chunk's P [V|1]); P + state read (after
+                // the previous chunk's P [V|1], whose P columns it overwrites); P [V|1]; U
+                // whenever its inputs are loaded and the previous chunk's carry has read its
+                // columns (the previous P [V|1] issued).  Single-thread issue order is the
+                // tensor pipe's execution order.
+                int qd = 0, ud = 0, pd = 0, vd = 0;
                 Stall st;
                 const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
-                while (coef_ok && vdone < n) {
+                while (coef_ok && vd < n) {
                     bool prog = false;
-                    if (kdone < n && udone == kdone) {
-                        const int r = rbase + kdone;
-                        if (mbar_test(xk, r & 1)) {
+                    if (ud < n && ud <= vd) {
+                        const int r = rbase + ud;
+                        if (mbar_test(gfull, r & 1) && mbar_test(&vfull[r % VS], (r / VS) & 1)) {
                             tc_fence_after();
-                            issue_scores_ool(tmem + kSK, tmem + kXK, dkx, dc);
-                            umma_commit(sk);
-                            ++kdone;
-                            if (qdone >= kdone) umma_commit(qkempty);
-                            prog = true;
-                        }
-                    } else if (udone < kdone) {
-                        const int r = rbase + udone;
-                        if (mbar_test(gkr, r & 1) && mbar_test(vfull, r & 1)) {
-                            tc_fence_after();
-                            if (udone + 1 < n) {
+                            if (ud + 1 < n) {
 #pragma unroll 1
                                 for (int kk = 0; kk < kTile / 16; ++kk)
-                                    umma_bf16(tmem + kU, dadd(dgt, kk * 2048), dadd(dv, kk * 2048), i80u, kk > 0 ? 1u : 0u);
+                                    umma_bf16(tmem + kU, dadd(dgt, kk * 4096), dvk(r % VS, kk), i80u, kk > 0 ? 1u : 0u);
                             }
                             umma_commit(ufull);
-                            ++udone;
-                            if (vdone >= udone) umma_commit(vempty);
+                            ++ud;
+                            if (pd >= ud) umma_commit(gempty);
+                            if (vd >= ud) umma_commit(&vempty[r % VS]);
                             prog = true;
                         }
                     }
-                    if (qdone < n && qdone == vdone) {
-                        const int r = rbase + qdone;
+                    if (qd < n) {
+                        const int r = rbase + qd;
                         if (mbar_test(xq, r & 1)) {
                             tc_fence_after();
-                            issue_scores_ool(tmem + kSQ, tmem + kXQ, dq, dc);
+                            issue_scores_ool(tmem + kSQ, tmem + kXQ, dadd(dq0, (r % QS) * kTileBytes), dc);
                             umma_commit(sq);
-                            ++qdone;
-                            if (kdone >= qdone) umma_commit(qkempty);
+                            umma_commit(&qempty[r % QS]);
+                            ++qd;
                             prog = true;
                         }
-                    } else if (pdone < qdone) {
-                        const int r = rbase + pdone;
-                        if (mbar_test(gq, r & 1) && mbar_test(gkr, r & 1) && mbar_test(sready, r & 1)) {
+                    }
+                    if (pd < qd && pd == vd) {
+                        const int r = rbase + pd;
+                        if (mbar_test(gq, r & 1) && mbar_test(gfull, r & 1) && mbar_test(sready, r & 1)) {
                             tc_fence_after();
                             // [P | num den] = gQhi [gK ; S^T]hi^T + gQhi [gK ; S^T]lo^T + gQlo [gK ; S^T]hi^T
 #pragma unroll 1
@@ -1529,25 +1577,26 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                                 umma_bf16_tA(tmem + kPD, aq + 32, dadd(dbh, kk * 32), i208, 1u);
                             }
                             umma_commit(pfull);
-                            ++pdone;
+                            ++pd;
+                            if (ud >= pd) umma_commit(gempty);
                             prog = true;
                         }
-                    } else if (vdone < pdone) {
-                        const int r = rbase + vdone;
-                        if (mbar_test(pready, r & 1) && mbar_test(vfull, r & 1)) {
+                    } else if (vd < pd) {
+                        const int r = rbase + vd;
+                        if (mbar_test(pready, r & 1) && mbar_test(&vfull[r % VS], (r / VS) & 1)) {
                             tc_fence_after();
                             // [num | den] += P [V | 1]; P hi / lo sit in place in the P columns:
                             // key block cb = kk / 2 holds hi words at 32 cb, lo words at 32 cb + 16.
 #pragma unroll 1
                             for (int kk = 0; kk < kTile / 16; ++kk) {
-                                const uint64_t bv = dadd(dv, kk * 2048);
+                                const uint64_t bv = dvk(r % VS, kk);
                                 const uint32_t ap = tmem + kPD + 32 * (kk >> 1) + 8 * (kk & 1);
                                 umma_bf16_tA(tmem + kO, ap, bv, i80s, 1u);
                                 umma_bf16_tA(tmem + kO, ap + 16, bv, i80s, 1u);
                             }
                             umma_commit(ofull);
-                            ++vdone;
-                            if (udone >= vdone) umma_commit(vempty);
+                            ++vd;
+                            if (ud >= vd) umma_commit(&vempty[r % VS]);
                             prog = true;
                         }
                     }
@@ -1559,88 +1608,84 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             }
         } else if (warp < 6) {
             // ---------------- query group
+            // Iteration i: scores and softmax of chunk i, then the outputs of chunk i - 1
+            // (gq lets P + state read of chunk i overwrite its accumulator once that is in
+            // registers; staging and store go beside those MMAs), then the P split of chunk i.
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             uint8_t *stage = stg + (warp & 3) * 8192;
-            for (int i = 0; i < n; ++i) {
+            float rq_prev = 0.f, rq = 0.f;
+            for (int i = 0; i <= n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                if (i == 0) {  // x^2 of the job's first chunk (later ones are prepared a chunk ahead)
-                    if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
-                    x2_row(qk, row, tmem + lb + kXQ);
+                if (i < n) {
+                    if (i == 0) {  // x^2 of the job's first chunk (later ones are prepared a chunk ahead)
+                        if (!wait_or_abort(&qfull[r % QS], (r / QS) & 1, status, abort_flag)) break;
+                        x2_row(qst + (r % QS) * kTileBytes, row, tmem + lb + kXQ);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(xq);
+                    }
+                    if (!wait_or_abort(sq, ph, status, abort_flag)) break;
+                    if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
+                    tc_fence_after();
+                    rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, 0, row, 1);
+                }
+                if (i > 0) {
+                    if (!wait_or_abort(ofull, ph ^ 1, status, abort_flag)) break;
+                    tc_fence_after();
+                    stage_output_row(tmem + lb + kO, rq_prev, eps, stage, lane, o_bf16, i < n ? gq : nullptr);
+                } else {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(gq);
+                }
+                __syncwarp();
+                if (i > 0 && lane == 0) {
+                    const int row0 = (t0 + i - 1) * kTile + 32 * (warp & 3);
+                    tma_store_3d(&tmO, stage, 0, row0, bh);
+                    if (!o_bf16) tma_store_3d(&tmO, stage + 4096, 32, row0, bh);
+                    bulk_commit();
+                }
+                if (i == n) break;
+                rq_prev = rq;
+                if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
+                tc_fence_after();
+                // x^2 of the next chunk first (its A columns held Gamma^Q, consumed by P and
+                // the state read), so its score MMAs overlap this chunk's P split and P [V|1]
+                if (i + 1 < n) {
+                    const int r1 = r + 1;
+                    if (!wait_or_abort(&qfull[r1 % QS], (r1 / QS) & 1, status, abort_flag)) break;
+                    x2_row(qst + (r1 % QS) * kTileBytes, row, tmem + lb + kXQ);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xq);
                 }
-                if (!wait_or_abort(sq, ph, status, abort_flag)) break;
-                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
-                tc_fence_after();
-                const float rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, 0, row, 1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(gq);
                 // masked intra-chunk affinity, key blocks 0 and 1 -> P hi | lo (in place)
-                if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
-                tc_fence_after();
                 split_p_blocks(tmem + lb + kPD, 0, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
-                // x^2 of the next chunk (its A columns held Gamma^Q, consumed by P and the state read)
-                if (i + 1 < n) {
-                    if (!wait_or_abort(qkfull, ph ^ 1, status, abort_flag)) break;
-                    x2_row(qk, row, tmem + lb + kXQ);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xq);
-                }
-                // outputs of this chunk
-                if (!wait_or_abort(ofull, ph, status, abort_flag)) break;
-                tc_fence_after();
-                causal_output_row(tmem + lb + kO, rq, eps, stage, lane, &tmO, o_bf16, (t0 + i) * kTile + 32 * (warp & 3), bh);
             }
             if (lane == 0) bulk_wait_read0();  // staging reusable; kernel completion publishes the stores
         } else {
-            // ---------------- key group
+            // ---------------- key group: carry of the state and half of the P split
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             for (int i = 0; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                if (i == 0) {  // x^2 of the job's first chunk (later ones are prepared a chunk ahead)
-                    if (!wait_or_abort(qkfull, ph, status, abort_flag)) break;
-                    x2_row(qk + kTileBytes, row, tmem + lb + kXK);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xk);
-                }
-                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
-                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
-                tc_fence_after();
-                gamma_row(tmem + lb + kSK, cvec, 1, 0u, gb, L::kBHalf, row, (t0 + i) * kTile + row < N ? 1 : 0);
-                if (i == 0) {
-                    // State operand of the job's first chunk, from the carried-in prefix.
-                    // Before the gkr arrival: U of this chunk (which the carry adds into
-                    // S) is issued only after every key warp has arrived, i.e. has read S.
+                if (i == 0) {  // state operand of the job's first chunk, from the carried-in prefix
                     if (wait_or_abort(xfull, njob & 1, status, abort_flag)) state_operand(gb, S, tid - 192);
                     fence_proxy_async_smem();
-                    __syncwarp();
+                    named_sync(1, 128);  // every key thread has read S before the carry adds to it
                     if (lane == 0) mbar_arrive(sready);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(gkr);
                 const bool carry = i + 1 < n;
                 if (carry) {
-                    // first half of the carry: U out of tensor memory (its columns take the
-                    // next chunk's key scores), the partner's columns through X
+                    // first half of the carry, beside the P MMAs: U out of tensor memory,
+                    // the partner's columns through X
                     if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
                     tc_fence_after();
                     carry_take(tmem + lb + kU, S, X, row);
-                    // x^2 of the next chunk's keys (the score MMAs of this chunk have read it)
-                    if (!wait_or_abort(qkfull, ph ^ 1, status, abort_flag)) break;
-                    x2_row(qk + kTileBytes, row, tmem + lb + kXK);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xk);
                 }
                 // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo (in place)
                 if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
@@ -1657,7 +1702,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     named_sync(1, 128);
                     state_operand(gb, S, tid - 192);
                     fence_proxy_async_smem();
-                    __syncwarp();
+                    named_sync(1, 128);  // every key thread has read S before the next carry
                     if (lane == 0) mbar_arrive(sready);
                 }
             }
@@ -1780,16 +1825,16 @@ int num_sms() {
 
 // Workspace of the persistent kernels: status | per-head job counters |
 // per-block parameter-error words of the coefficient prep | per-head coefficient images | job partials
-// [ctas][slots][KP][kW] | per-head read operand images.  Nothing needs
+// [ctas][slots][KP][kW] | per-head read operand images | (causal) Gamma^K of every key tile.  Nothing needs
 // clearing by the caller: coef_prep_tc_kernel resets the status word and the
 // counters, and writes every error word.
 struct TcLayout2 {
     Part P;
     int nctas = 0;
-    size_t counters = 0, head_err = 0, coef = 0, part = 0, mem = 0, mem_stride = 0, total = 0;
+    size_t counters = 0, head_err = 0, coef = 0, part = 0, mem = 0, mem_stride = 0, gk = 0, total = 0;
 };
 
-TcLayout2 tc_layout2(const Problem &p, int splits) {
+TcLayout2 tc_layout2(const Problem &p, int splits, int causal) {
     TcLayout2 L;
     const int ntiles = (p.N + kTile - 1) / kTile;
     const int total = p.BH() * ntiles;
@@ -1810,6 +1855,10 @@ TcLayout2 tc_layout2(const Problem &p, int splits) {
     L.mem_stride = ((size_t)2 * (p.d_v + 16) * 128 + 1023) & ~size_t(1023);
     L.mem = off;
     off = align256(off + L.mem_stride * p.BH());
+    if (causal == 1) {  // Gamma^K of every key tile (bf16 hi / lo), from the aggregation to the scan
+        L.gk = off;
+        off = align256(off + (size_t)2 * kTileBytes * p.BH() * ntiles);
+    }
     L.total = off;
     return L;
 }
@@ -1831,7 +1880,8 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
-                       p.H, p.N, L.P, part, counters, mem, L.mem_stride, 0, p.test_stall ? 1 : 0, status));
+                       p.H, p.N, L.P, part, counters, mem, L.mem_stride, static_cast<uint8_t *>(nullptr), 0,
+                       p.test_stall ? 1 : 0, status));
     clk.mark();
     GMA_TRY(set_smem(tc_read3_kernel, Read3Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_read3_kernel, dim3(L.nctas), dim3(kThreadsR), Read3Smem::kAlloc, s, tq, to, coef, p.H, p.N,
@@ -1856,12 +1906,12 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
     clk.mark();
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
-                       p.H, p.N, L.P, part, counters, static_cast<uint8_t *>(nullptr), size_t(0), 1, p.test_stall ? 1 : 0,
-                       status));
+                       p.H, p.N, L.P, part, counters, static_cast<uint8_t *>(nullptr), size_t(0), ws + L.gk, 1,
+                       p.test_stall ? 1 : 0, status));
     clk.mark();
     GMA_TRY(set_smem(tc_causal2_kernel, Causal2Smem::kAlloc));
-    GMA_TRY(launch_pdl(tc_causal2_kernel, dim3(L.nctas), dim3(kThreadsG), Causal2Smem::kAlloc, s, tq, tk, tv, to, coef,
-                       part, p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status));
+    GMA_TRY(launch_pdl(tc_causal2_kernel, dim3(L.nctas), dim3(kThreadsG), Causal2Smem::kAlloc, s, tq, tv, to, coef,
+                       static_cast<const uint8_t *>(ws + L.gk), part, p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status));
     clk.mark();
     return cudaSuccess;
 }
@@ -1880,19 +1930,16 @@ bool tc_supported(const Problem &p, int causal) {
     return causal == 1 && p.d_v == 64;
 }
 
-size_t tc_workspace(const Problem &p, int causal, int splits) {
-    (void)causal;
-    return tc_layout2(p, splits).total;
-}
+size_t tc_workspace(const Problem &p, int causal, int splits) { return tc_layout2(p, splits, causal).total; }
 
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
-    TcLayout2 L = tc_layout2(p, splits);
+    TcLayout2 L = tc_layout2(p, splits, 0);
     uint8_t *w = static_cast<uint8_t *>(ws);
     return run_bidir2(p, L, w, s, clk);
 }
 
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
-    TcLayout2 L = tc_layout2(p, splits);
+    TcLayout2 L = tc_layout2(p, splits, 1);
     return run_causal2(p, L, static_cast<uint8_t *>(ws), s, clk);
 }
 

@@ -116,6 +116,15 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// Untiled bulk copy shared -> global in the thread's bulk async-group (both
+// addresses 16-byte aligned, bytes a multiple of 16); bulk_commit /
+// bulk_wait_read0 order it like the tiled stores.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ dependent launch
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel of the stream runs;
