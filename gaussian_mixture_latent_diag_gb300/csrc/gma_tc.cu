@@ -1111,12 +1111,14 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
 // Warps: 0 lane 0 Q / V loads, 0 lane 1 Gamma^K loads, 1 MMA issuer, 2..5 query
 // group (x^2, softmax, half of the P split, outputs), 6..9 key group (the other
 // half of the P split, carry of the state).  The carry runs beside the P split
-// and the P [V | 1] MMAs; the next chunk's x^2 is prepared right after the P MMAs.
+// and the P [V | 1] MMAs; the next chunk's x^2 is prepared beside the P MMAs, and
+// its score MMAs are issued right after them.
 //
 // TMEM (512 columns):
-//   [0, 64)    x^2 of Q -> Gamma^Q hi | lo          (MMA A operands)
-//   [64, 192)  scores Q (N = 128): own columns, so the next chunk's score MMAs
-//              overlap this chunk's P split and P [V | 1]
+//   [0, 64)    x^2 of Q hi | lo (A operand of the score MMAs; free once they end)
+//   [64, 192)  scores Q (N = 128); the softmax overwrites columns 64..127 with
+//              Gamma^Q hi | lo (A operand of P + state read), so the next chunk's
+//              score MMAs follow the P MMAs in issue order
 //   [192, 320) P, then P hi | lo in place per 32-key block
 //   [320, 400) [num | den]: one N = 208 accumulator with P for the P + state-read MMAs
 //   [400, 480) state increment U = [gK_hi ; gK_lo]^T [V | 1] (N = 80)
@@ -1368,7 +1370,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     using L = Causal2Smem;
     constexpr int W = L::W, QS = L::kQS, VS = L::kVS;
     constexpr int kTmemCols = 512;
-    constexpr int kXQ = 0, kSQ = 64, kPD = 192, kO = 320, kU = 400;
+    constexpr int kXQ = 0, kSQ = 64, kGQ = kSQ, kPD = 192, kO = 320, kU = 400;
     static_assert(kO == kPD + 128, "[P | num den] is one N = 208 accumulator");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1526,12 +1528,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 };
                 constexpr uint32_t i208 = idesc_bf16(kTile, kTile + 80, false, false);
                 constexpr uint32_t i80s = idesc_bf16(kTile, 80, false, true), i80u = idesc_bf16(kTile, 80, true, true);
-                // Per chunk: Q scores (own columns: issued as soon as the chunk's x^2 is
-                // ready, possibly before the previous chunk's P [V|1]); P + state read (after
-                // the previous chunk's P [V|1], whose P columns it overwrites); P [V|1]; U
-                // whenever its inputs are loaded and the previous chunk's carry has read its
-                // columns (the previous P [V|1] issued).  Single-thread issue order is the
-                // tensor pipe's execution order.
+                // Per chunk: Q scores (once the chunk's x^2 is ready and the previous P +
+                // state read, which reads Gamma^Q from the score columns, is issued);
+                // P + state read (after the previous chunk's P [V|1], whose P columns it
+                // overwrites); P [V|1]; U whenever its inputs are loaded and the previous
+                // chunk's carry has read its columns (the previous P [V|1] issued).
+                // Single-thread issue order is the tensor pipe's execution order.
                 int qd = 0, ud = 0, pd = 0, vd = 0;
                 Stall st;
                 const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
@@ -1553,7 +1555,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                             prog = true;
                         }
                     }
-                    if (qd < n) {
+                    if (qd < n && qd <= pd) {
                         const int r = rbase + qd;
                         if (mbar_test(xq, r & 1)) {
                             tc_fence_after();
@@ -1571,7 +1573,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                             // [P | num den] = gQhi [gK ; S^T]hi^T + gQhi [gK ; S^T]lo^T + gQlo [gK ; S^T]hi^T
 #pragma unroll 1
                             for (int kk = 0; kk < kKP / 16; ++kk) {
-                                const uint32_t aq = tmem + kXQ + kk * 8;
+                                const uint32_t aq = tmem + kGQ + kk * 8;
                                 umma_bf16_tA(tmem + kPD, aq, dadd(dbh, kk * 32), i208, kk > 0 ? 1u : 0u);
                                 umma_bf16_tA(tmem + kPD, aq, dadd(dbl, kk * 32), i208, 1u);
                                 umma_bf16_tA(tmem + kPD, aq + 32, dadd(dbh, kk * 32), i208, 1u);
@@ -1610,7 +1612,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
             // ---------------- query group
             // Iteration i: scores and softmax of chunk i, then the outputs of chunk i - 1
             // (gq lets P + state read of chunk i overwrite its accumulator once that is in
-            // registers; staging and store go beside those MMAs), then the P split of chunk i.
+            // registers; staging and store go beside those MMAs), the x^2 of chunk i + 1,
+            // then the P split of chunk i.
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             uint8_t *stage = stg + (warp & 3) * 8192;
@@ -1628,7 +1631,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     if (!wait_or_abort(sq, ph, status, abort_flag)) break;
                     if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                     tc_fence_after();
-                    rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kXQ, nullptr, 0, row, 1);
+                    rq = gamma_row(tmem + lb + kSQ, cvec, 0, tmem + lb + kGQ, nullptr, 0, row, 1);
                 }
                 if (i > 0) {
                     if (!wait_or_abort(ofull, ph ^ 1, status, abort_flag)) break;
@@ -1648,10 +1651,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                 }
                 if (i == n) break;
                 rq_prev = rq;
-                if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
-                tc_fence_after();
-                // x^2 of the next chunk first (its A columns held Gamma^Q, consumed by P and
-                // the state read), so its score MMAs overlap this chunk's P split and P [V|1]
+                // x^2 of the next chunk beside this chunk's P MMAs (the score MMAs of this
+                // chunk, the only readers of the x^2 columns, have completed: sq)
                 if (i + 1 < n) {
                     const int r1 = r + 1;
                     if (!wait_or_abort(&qfull[r1 % QS], (r1 / QS) & 1, status, abort_flag)) break;
@@ -1660,6 +1661,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xq);
                 }
+                if (!wait_or_abort(pfull, ph, status, abort_flag)) break;
+                tc_fence_after();
                 // masked intra-chunk affinity, key blocks 0 and 1 -> P hi | lo (in place)
                 split_p_blocks(tmem + lb + kPD, 0, row);
                 tc_fence_before();
