@@ -966,22 +966,13 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
             if (lane == 0) {
                 const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024), dc0 = sdesc_sw128(smem_u32(coef), 16, 1024);
                 const uint64_t db0 = sdesc_sw128(smem_u32(bop), 16, 1024);
+                // Read MMAs (the shorter kind, which ends a tile) go first whenever a
+                // group is ready for them.
                 int ns = 0, nr = 0;
                 Stall st;
                 const bool coef_ok = wait_or_abort(cfull, njob & 1, status, abort_flag);
                 while (coef_ok && nr < n) {
                     bool prog = false;
-                    if (ns < n) {
-                        const int r = rbase + ns, gb = r % kNGR, s = r % QS;
-                        if (mbar_test(&xready[gb], (r / kNGR) & 1)) {
-                            tc_fence_after();
-                            issue_scores_tA(tmem + gb * kGC + kKP, tmem + gb * kGC, dadd(dq0, s * kTileBytes), dc0);
-                            umma_commit(&sfull[gb]);
-                            umma_commit(&qempty[s]);
-                            ++ns;
-                            prog = true;
-                        }
-                    }
                     if (nr < ns) {
                         const int r = rbase + nr, gb = r % kNGR;
                         if (mbar_test(&gready[gb], (r / kNGR) & 1) && (nr > 0 || mbar_test(bfull, njob & 1))) {
@@ -994,6 +985,17 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
                             }
                             umma_commit(&ofull[gb]);
                             ++nr;
+                            prog = true;
+                        }
+                    }
+                    if (ns < n) {
+                        const int r = rbase + ns, gb = r % kNGR, s = r % QS;
+                        if (mbar_test(&xready[gb], (r / kNGR) & 1)) {
+                            tc_fence_after();
+                            issue_scores_tA(tmem + gb * kGC + kKP, tmem + gb * kGC, dadd(dq0, s * kTileBytes), dc0);
+                            umma_commit(&sfull[gb]);
+                            umma_commit(&qempty[s]);
+                            ++ns;
                             prog = true;
                         }
                     }
