@@ -230,23 +230,6 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 // read TMEM lanes 32*(w%4) .. 32*(w%4)+31).
 __device__ __forceinline__ int epi_row(int warp, int lane) { return 32 * (warp & 3) + lane; }
 
-// Writes one bf16 hi / lo B-operand image [NB rows x KP] for the read of the
-// latent memory: row n < D_V holds Vt[:, n], row D_V holds Z, other rows 0.
-template <int D_V>
-__device__ __forceinline__ void store_memory_operand(const float *S, int ldS, uint8_t *dst, int tid, int nthreads) {
-    constexpr int NB = D_V + 16;
-    __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(dst);
-    __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(dst + NB * 128);
-    for (int e = tid; e < NB * kKP; e += nthreads) {
-        const int n = e / kKP, k = e % kKP;
-        const float v = n <= D_V ? S[k * ldS + n] : 0.f;
-        const __nv_bfloat16 vh = __float2bfloat16_rn(v);
-        const uint32_t off = sw128_offset(n, k, 1024) / 2;
-        bhi[off] = vh;
-        blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
-    }
-}
-
 // x^2 split of this thread's row of a swizzled [128 x 64] bf16 tile, written
 // to tensor memory as an MMA A operand: x2hi at columns [0, 32), x2lo at
 // [32, 64) of `taddr` (this thread's lane).
@@ -358,54 +341,75 @@ __device__ __forceinline__ void store_gamma_words(uint8_t *gbuf, int t, const ui
     }
 }
 
-// Combines the job partials ([KP][kW] fp32 each) of head bh in CTA
-// order, so the result does not depend on which job finished last:
-//   mode 0: out (shared memory) = sum of the partials,
+// Combines the job partials ([KP][kW] fp32 each) of head bh in CTA order, so
+// the result does not depend on which job finished last:
+//   mode 0: img (shared memory) = the sum of the partials as the bf16 hi | lo
+//           read operand [NB = 80 rows x KP], K-major, 128-byte swizzled: row
+//           n < 64 Vt[:, n], row 64 Z, rows 65 .. 67 the partials' zero padding,
+//           rows 68 .. 79 zero;
 //   mode 1: each partial replaced in place by the sum of the ones before it.
-// Each thread keeps 2 vectors x 8 CTAs of loads in flight.
-__device__ void combine_partials(float *__restrict__ part, const Part &P, int bh, int mode, float *out, int tid,
+// Each thread owns four float4 slots of the [KP][kW] layout and keeps the loads
+// of six CTAs for all of them in flight (one round for up to six jobs).
+__device__ void combine_partials(float *__restrict__ part, const Part &P, int bh, int mode, uint8_t *img, int tid,
                                  int nthreads) {
-    constexpr int kE4 = kKP * kW / 4;
-    constexpr size_t kPS = (size_t)kKP * kW;
+    constexpr int kRow4 = kW / 4, kE4 = kKP * kRow4, NQ = 4, NB = 6;
+    constexpr size_t kPS4 = (size_t)kKP * kRow4;
     const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
-    for (int e0 = tid; e0 < kE4; e0 += 2 * nthreads) {
-        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        for (int cc0 = cf; cc0 <= cl; cc0 += 8) {
-            float4 v[8][2];
+    float4 acc[NQ];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int cc = cc0 + u;
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kPS);
+    for (int q = 0; q < NQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cb = cf; cb <= cl; cb += NB) {
+        float4 v[NB][NQ];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int e4 = e0 + q * nthreads;
-                    v[u][q] = (cc <= cl && e4 < kE4) ? __ldcg(src + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
+        for (int u = 0; u < NB; ++u) {
+            const int cc = cb + u;
+            const float4 *src = reinterpret_cast<const float4 *>(part) +
+                                ((size_t)cc * P.slots + (cc <= cl ? slot_of(P, cc, bh) : 0)) * kPS4;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int cc = cc0 + u;
-                if (cc > cl) break;
-                float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kPS);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int e4 = e0 + q * nthreads;
-                    if (e4 >= kE4) continue;
-                    if (mode == 1) __stcg(dst + e4, acc[q]);
-                    acc[q].x += v[u][q].x;
-                    acc[q].y += v[u][q].y;
-                    acc[q].z += v[u][q].z;
-                    acc[q].w += v[u][q].w;
-                }
+            for (int q = 0; q < NQ; ++q) {
+                const int e4 = tid + q * nthreads;
+                v[u][q] = (cc <= cl && e4 < kE4) ? __ldcg(src + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        if (mode == 0)
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int e4 = e0 + q * nthreads;
-                if (e4 < kE4) reinterpret_cast<float4 *>(out)[e4] = acc[q];
+        for (int u = 0; u < NB; ++u) {
+            const int cc = cb + u;
+            if (cc > cl) break;
+            float4 *dst = reinterpret_cast<float4 *>(part) + ((size_t)cc * P.slots + slot_of(P, cc, bh)) * kPS4;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int e4 = tid + q * nthreads;
+                if (e4 >= kE4) continue;
+                if (mode == 1) __stcg(dst + e4, acc[q]);
+                acc[q].x += v[u][q].x;
+                acc[q].y += v[u][q].y;
+                acc[q].z += v[u][q].z;
+                acc[q].w += v[u][q].w;
             }
+        }
+    }
+    if (mode == 0) {
+        constexpr int NBR = 64 + 16;
+        __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(img);
+        __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(img + NBR * 128);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int e4 = tid + q * nthreads;
+            if (e4 >= kE4) continue;
+            const int k = e4 / kRow4, n0 = 4 * (e4 % kRow4);
+            const float v[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat16 vh = __float2bfloat16_rn(v[j]);
+                const uint32_t off = sw128_offset(n0 + j, k, 1024) / 2;
+                bhi[off] = vh;
+                blo[off] = __float2bfloat16_rn(v[j] - __bfloat162float(vh));
+            }
+        }
+        // rows 4 kRow4 .. NBR - 1 (never a partial's column): zero, in both images
+        constexpr int kZ0 = 4 * kRow4 * 128, kZ16 = (NBR * 128 - kZ0) / 16;
+        for (int i = tid; i < 2 * kZ16; i += nthreads)
+            *reinterpret_cast<uint4 *>(img + (i / kZ16) * NBR * 128 + kZ0 + (i % kZ16) * 16) = make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -714,15 +718,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
             cta_sync();
             if (*last_flag) {
                 __threadfence();
-                combine_partials(part, P, bh, mode, red, tid, kThreadsG);
+                // mode 0: the bf16 hi / lo read operand, built in shared memory (over the
+                // idle K ring, after the reduction buffer) and copied out with 16-byte stores
+                constexpr int kImgBytes = 2 * (D_V + 16) * 128;
+                uint8_t *img = smem + 128 * W * 4 + 1024;
+                static_assert(128 * W * 4 + 1024 + kImgBytes <= L::kVst, "image fits over the K ring");
+                combine_partials(part, P, bh, mode, img, tid, kThreadsG);
                 if (mode == 0) {
-                    // the bf16 hi / lo read operand, built in shared memory (over the idle K
-                    // ring, after the reduction buffer) and copied out with 16-byte stores
-                    constexpr int kImgBytes = 2 * (D_V + 16) * 128;
-                    uint8_t *img = smem + 128 * W * 4 + 1024;
-                    static_assert(128 * W * 4 + 1024 + kImgBytes <= L::kVst, "image fits over the K ring");
-                    cta_sync();
-                    store_memory_operand<D_V>(red, W, img, tid, kThreadsG);
                     cta_sync();
                     uint4 *dst = reinterpret_cast<uint4 *>(mem_img + (size_t)bh * mem_img_stride);
                     for (int e = tid; e < kImgBytes / 16; e += kThreadsG) __stcg(dst + e, reinterpret_cast<const uint4 *>(img)[e]);
