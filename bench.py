@@ -37,11 +37,13 @@ UNIT = "token*heads/s"
 
 # Algorithmic HBM bytes each stage accounts for, as the tensors of the path it
 # reads or writes (Q_X, K_X, V_X read once, O written once per forward);
-# intermediate scratch traffic is not algorithmic.
+# intermediate scratch traffic is not algorithmic.  The tensor-core causal scan
+# reads Q and V and the key responsibilities its aggregation launch stored (K is
+# read, and credited, there).
 STAGE_TENSORS = {
     "prep": "", "reset": "", "reduce": "", "scan": "",
     "resp_q": "Q", "resp_k": "K", "write": "V", "read": "O", "causal": "VO",
-    "tc_write": "KV", "tc_read": "QO", "tc_causal": "QKVO", "tc_aggregate": "KV",
+    "tc_write": "KV", "tc_read": "QO", "tc_causal": "QVO", "tc_aggregate": "KV",
 }
 
 
