@@ -1136,7 +1136,7 @@ struct Causal2Smem {
     // 8-row groups of 2 KB (hi rows | lo rows): 16 groups of Gamma^K (token rows, the
     // aggregation pass's stored buffer as is) then 10 groups of S^T (value rows).
     static constexpr int kGroups = (kTile + 80) / 8;
-    static constexpr int kQS = 2;                          // Q ring depth
+    static constexpr int kQS = 1;                          // Q ring depth
     static constexpr int kVS = 2;                          // V ring depth
     static constexpr int kQ = 0;
     static constexpr int kV = kQ + kQS * kTileBytes;       // V tiles
