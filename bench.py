@@ -214,6 +214,29 @@ def run_reference(args, rank: int):
 
 # ------------------------------------------------------------------ GPU arm
 
+def rank_seed(rank: int, variant: int) -> int:
+    """Input seed of one variant on one rank: each rank draws its own heads (replicas
+    of the workload shape, no data shared between ranks)."""
+    return 1000 * rank + variant
+
+
+def job_ms(ms: float, world: int, device=None) -> float:
+    """Step time of the whole job: the slowest rank's, every rank holding the same work."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ms: float, world: int, w=WORKLOAD) -> float:
+    """token*heads/s of the whole job: per step every rank runs one bidirectional and
+    one causal forward of the workload."""
+    return world * 2 * w["B"] * w["H"] * w["N"] / (ms / 1e3)
+
+
 def run_gma(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -227,7 +250,7 @@ def run_gma(args, rank: int, world: int, local_rank: int):
     w = WORKLOAD
     cases = [Case("bidir", False, w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"]),
              Case("causal", True, w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"])]
-    host = [make_inputs(c, seed=1000 * rank + i) for i, c in enumerate(cases)]
+    host = [make_inputs(c, seed=rank_seed(rank, i)) for i, c in enumerate(cases)]
     dinp = [{k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in h.items()} for h in host]
     outs = [torch.empty(w["B"], w["H"], w["N"], w["d_v"], dtype=torch.float32, device=dev) for _ in cases]
     paths = [gma.selected_path(w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"], int(c.causal)) for c in cases]
@@ -287,11 +310,8 @@ def run_gma(args, rank: int, world: int, local_rank: int):
         call(0, events=ev[s][0])
         call(1, events=ev[s][1])
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * 2 * w["B"] * w["H"] * w["N"] / (ms / 1e3)
+    ms = job_ms(ms, world, dev)
+    value = job_throughput(ms, world)
 
     # per-stage averages over the breakdown pass
     stage_ms = {}
@@ -367,11 +387,8 @@ def run_gma(args, rank: int, world: int, local_rank: int):
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e = {"value": world * 2 * w["B"] * w["H"] * w["N"] / (e_ms / 1e3), "unit": UNIT,
+    e_ms = job_ms(e_ms, world, dev)
+    e2e = {"value": job_throughput(e_ms, world), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
            "schedule": "H2D and D2H on their own streams, device buffers double-buffered across steps"}
 
