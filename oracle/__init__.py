@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the GMA forward pass -- TEST INFRASTRUCTURE ONLY.
+"""fp64 CPU oracle for the GMA forward pass and its gradients -- TEST INFRASTRUCTURE ONLY.
 
 Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never links, loads or
@@ -15,9 +15,13 @@ Linear-Time Sequence Mixing via Probabilistic Latent Routing" (arXiv
 * ``forward_causal``                 -- Eqs. (8a)/(8b), cumulative-sum remark
 * ``affinity`` / ``affinity_forward`` -- Eqs. (9)-(11), brute force for tiny N
 * ``bidir_rows`` / ``causal_rows``   -- the same definitions on selected rows
+* ``backward_bidir`` / ``backward_causal`` -- gradients: gradient section,
+  Eq. (18) (score gradient) and the chain rule through the score
 
 Parity pins: see ``tests/test_oracle.py`` (closed forms, invariants, brute
-force, scipy / scikit-learn textbook routines, hand-derived golden values).
+force, scipy / scikit-learn textbook routines, hand-derived golden values)
+and ``tests/test_oracle_backward.py`` (central finite differences of the
+forward, shift and translation invariances, K = 1).
 """
 from __future__ import annotations
 
@@ -81,6 +85,8 @@ def _load(mutant: int = 0):
             lib.gma_oracle_affinity_forward.argtypes = common + [ctypes.c_int, _D]
             lib.gma_oracle_affinity.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, _D, _D,
                                                 _D, ctypes.c_int, _D]
+            lib.gma_oracle_bidir_backward.argtypes = common + [_D] * 7
+            lib.gma_oracle_causal_backward.argtypes = common + [_D] * 7
             _libs[mutant] = lib
     return lib
 
@@ -197,6 +203,47 @@ def affinity(Q, K_, mu, sigma2, log_pi) -> np.ndarray:
     lib.gma_oracle_affinity(_p(Q), _p(K_), N, d_r, _p(mu), _p(sigma2), _p(log_pi),
                             mu.shape[0], _p(A))
     return A
+
+
+def _backward(fn_name, Q, K_, V, mu, sigma2, log_pi, eps, dO) -> dict:
+    lib = _load(_ACTIVE[0])
+    fn = getattr(lib, fn_name)
+    Q, K_, V, dO = _f64(Q), _f64(K_), _f64(V), _f64(dO)
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H = mu.shape[0]
+    N, d_r = Q.shape[-2:]
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    Qh, Kh, Vh, dOh = _heads(Q, 2), _heads(K_, 2), _heads(V, 2), _heads(dO, 2)
+    dQ, dK, dV = np.empty(Qh.shape), np.empty(Kh.shape), np.empty(Vh.shape)
+    dmu, ds2, dlp = np.zeros(mu.shape), np.zeros(sigma2.shape), np.zeros(log_pi.shape)
+    for b in range(Qh.shape[0]):
+        h = b % H
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        q, k, v, g = (np.ascontiguousarray(t[b]) for t in (Qh, Kh, Vh, dOh))
+        gm, gs, gl = np.zeros_like(m), np.zeros_like(s), np.zeros_like(lp)
+        fn(_p(q), _p(k), _p(v), N, d_r, d_v, _p(m), _p(s), _p(lp), K, float(eps), _p(g),
+           _p(dQ[b]), _p(dK[b]), _p(dV[b]), _p(gm), _p(gs), _p(gl))
+        dmu[h] += gm
+        ds2[h] += gs
+        dlp[h] += gl
+    return {"dQ": dQ.reshape(Q.shape), "dK": dK.reshape(K_.shape), "dV": dV.reshape(V.shape),
+            "dmu": dmu, "dsigma2": ds2, "dlog_pi": dlp}
+
+
+def backward_bidir(Q, K_, V, mu, sigma2, log_pi, eps, dO) -> dict:
+    """Gradients of the bidirectional forward for upstream dO ([GMA, gradient
+    section, Eq. 18 and the chain rule through the score]): dQ, dK, dV shaped
+    like the inputs; dmu, dsigma2 [H, K, d_r] and dlog_pi [H, K] summed over
+    the batch (per-head parameters; a single head's [K, d_r] params give a
+    leading axis of 1)."""
+    return _backward("gma_oracle_bidir_backward", Q, K_, V, mu, sigma2, log_pi, eps, dO)
+
+
+def backward_causal(Q, K_, V, mu, sigma2, log_pi, eps, dO) -> dict:
+    """Gradients of the causal forward ([GMA, Eq. 8b] differentiated: prefix
+    memories forward, suffix sums backward); same outputs as backward_bidir."""
+    return _backward("gma_oracle_causal_backward", Q, K_, V, mu, sigma2, log_pi, eps, dO)
 
 
 def _rows(fn_name, q, k, v, mu_h, s2_h, lp_h, eps, rows):

@@ -1,6 +1,6 @@
 /*
  * gma_oracle.c -- plain, slow, single-threaded fp64 CPU oracle for the
- * Gaussian Mixture Attention (GMA) forward pass.
+ * Gaussian Mixture Attention (GMA) forward pass and its gradients.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file: only the test-suite, the smoke check and the CPU-baseline
@@ -32,6 +32,8 @@
  *   4: eps added to the numerator as well as the denominator
  *   5: write with query responsibilities, read with key responsibilities
  *   6: prior enters with the wrong sign
+ *   7: backward: the gradient entering the score is not mean-centred (Eq. 18)
+ *   8: backward: the causal key gradient uses prefix (j <= i) instead of suffix sums
  */
 #ifndef GMA_ORACLE_MUTANT
 #define GMA_ORACLE_MUTANT 0
@@ -327,4 +329,206 @@ void gma_oracle_affinity(const double *Q, const double *Kx, int N, int d_r,
             A[(size_t)i * N + j] = a;
         }
     free(GQ); free(GK);
+}
+
+/*
+ * ---------------------------------------------------------------- gradients
+ *
+ * Backward pass of one head ([GMA, gradient section]: the upstream gradient
+ * g_ik = dL/dgamma_ik arriving at a responsibility row, the softmax Jacobian
+ * (Eq. 17) and the gradient entering the score (Eq. 18),
+ *   dL/ds_ik = gamma_ik (g_ik - sum_l gamma_il g_il),
+ * then the chain rule for every quantity that enters the score).  Through
+ *   s_ik = log pi_k - 1/2 sum_m [ (x_im - mu_km)^2 / sigma2_km + log sigma2_km ]
+ * the score gradient reaches
+ *   dL/dx_im       = sum_k ds_ik (mu_km - x_im) / sigma2_km
+ *   dL/dmu_km      = sum_i ds_ik (x_im - mu_km) / sigma2_km
+ *   dL/dsigma2_km  = sum_i ds_ik ((x_im - mu_km)^2 / sigma2_km^2 - 1 / sigma2_km) / 2
+ *   dL/dlog_pi_k   = sum_i ds_ik
+ * for the query rows (x = q) and the key rows (x = k) alike.  dmu, dsigma2 and
+ * dlog_pi are ACCUMULATED (the caller zeroes them once and sums every head and
+ * batch row that shares the parameters); dX is written.
+ */
+static void score_backward(const double *X, const double *G, const double *Gup, int N,
+                           int d_r, const double *mu, const double *sigma2, int K,
+                           double *dX, double *dmu, double *dsigma2, double *dlog_pi)
+{
+    double *ds = malloc(sizeof(double) * (size_t)K);
+    for (int i = 0; i < N; ++i) {
+        const double *g = G + (size_t)i * K, *up = Gup + (size_t)i * K;
+        const double *x = X + (size_t)i * d_r;
+        double mean = 0.0;
+        for (int l = 0; l < K; ++l) mean += g[l] * up[l];
+        for (int k = 0; k < K; ++k) {
+#if GMA_ORACLE_MUTANT == 7
+            ds[k] = g[k] * up[k];
+#else
+            ds[k] = g[k] * (up[k] - mean);
+#endif
+        }
+        for (int m = 0; m < d_r; ++m) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k)
+                acc += ds[k] * (mu[(size_t)k * d_r + m] - x[m]) / sigma2[(size_t)k * d_r + m];
+            dX[(size_t)i * d_r + m] = acc;
+        }
+        for (int k = 0; k < K; ++k) {
+            dlog_pi[k] += ds[k];
+            for (int m = 0; m < d_r; ++m) {
+                const double s2 = sigma2[(size_t)k * d_r + m];
+                const double diff = x[m] - mu[(size_t)k * d_r + m];
+                dmu[(size_t)k * d_r + m] += ds[k] * diff / s2;
+                dsigma2[(size_t)k * d_r + m] += ds[k] * 0.5 * (diff * diff / (s2 * s2) - 1.0 / s2);
+            }
+        }
+    }
+    free(ds);
+}
+
+/*
+ * Bidirectional backward ([GMA, Eqs. 5-7] differentiated).  With
+ *   num_i = sum_k gQ_ik Vt_k,  den_i = sum_k gQ_ik Z_k + eps,  O_i = num_i / den_i
+ * and the upstream dO:
+ *   dnum_i = dO_i / den_i,                 dden_i = -(dO_i . O_i) / den_i
+ *   dL/dgQ_ik = dnum_i . Vt_k + dden_i Z_k
+ *   dVt_k = sum_i gQ_ik dnum_i,            dZ_k = sum_i gQ_ik dden_i
+ *   dL/dgK_jk = V_j . dVt_k + dZ_k,        dV_j = sum_k gK_jk dVt_k
+ * then score_backward for both sides.
+ */
+void gma_oracle_bidir_backward(const double *Q, const double *Kx, const double *V, int N,
+                               int d_r, int d_v, const double *mu, const double *sigma2,
+                               const double *log_pi, int K, double eps, const double *dO,
+                               double *dQ, double *dK, double *dV, double *dmu,
+                               double *dsigma2, double *dlog_pi)
+{
+    double *GQ = malloc(sizeof(double) * (size_t)N * K);
+    double *GK = malloc(sizeof(double) * (size_t)N * K);
+    double *UQ = malloc(sizeof(double) * (size_t)N * K);
+    double *UK = malloc(sizeof(double) * (size_t)N * K);
+    double *Vt = calloc((size_t)K * d_v, sizeof(double));
+    double *Z = calloc((size_t)K, sizeof(double));
+    double *dVt = calloc((size_t)K * d_v, sizeof(double));
+    double *dZ = calloc((size_t)K, sizeof(double));
+    double *dnum = malloc(sizeof(double) * (size_t)d_v);
+    gma_oracle_responsibilities(Q, N, d_r, mu, sigma2, log_pi, K, GQ);
+    gma_oracle_responsibilities(Kx, N, d_r, mu, sigma2, log_pi, K, GK);
+    for (int j = 0; j < N; ++j)
+        for (int k = 0; k < K; ++k) {
+            double g = GK[(size_t)j * K + k];
+            Z[k] += g;
+            for (int c = 0; c < d_v; ++c) Vt[(size_t)k * d_v + c] += g * V[(size_t)j * d_v + c];
+        }
+    for (int i = 0; i < N; ++i) {
+        const double *gq = GQ + (size_t)i * K;
+        double den = eps;
+        for (int k = 0; k < K; ++k) den += gq[k] * Z[k];
+        double dot = 0.0;
+        for (int c = 0; c < d_v; ++c) {
+            double num = 0.0;
+            for (int k = 0; k < K; ++k) num += gq[k] * Vt[(size_t)k * d_v + c];
+            dot += dO[(size_t)i * d_v + c] * (num / den);
+            dnum[c] = dO[(size_t)i * d_v + c] / den;
+        }
+        const double dden = -dot / den;
+        for (int k = 0; k < K; ++k) {
+            double u = dden * Z[k];
+            for (int c = 0; c < d_v; ++c) u += dnum[c] * Vt[(size_t)k * d_v + c];
+            UQ[(size_t)i * K + k] = u;
+            dZ[k] += gq[k] * dden;
+            for (int c = 0; c < d_v; ++c) dVt[(size_t)k * d_v + c] += gq[k] * dnum[c];
+        }
+    }
+    for (int j = 0; j < N; ++j)
+        for (int k = 0; k < K; ++k) {
+            double u = dZ[k];
+            for (int c = 0; c < d_v; ++c) u += V[(size_t)j * d_v + c] * dVt[(size_t)k * d_v + c];
+            UK[(size_t)j * K + k] = u;
+        }
+    for (int j = 0; j < N; ++j)
+        for (int c = 0; c < d_v; ++c) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += GK[(size_t)j * K + k] * dVt[(size_t)k * d_v + c];
+            dV[(size_t)j * d_v + c] = acc;
+        }
+    score_backward(Q, GQ, UQ, N, d_r, mu, sigma2, K, dQ, dmu, dsigma2, dlog_pi);
+    score_backward(Kx, GK, UK, N, d_r, mu, sigma2, K, dK, dmu, dsigma2, dlog_pi);
+    free(GQ); free(GK); free(UQ); free(UK); free(Vt); free(Z); free(dVt); free(dZ); free(dnum);
+}
+
+/*
+ * Causal backward ([GMA, Eq. 8b] differentiated).  The query side is as in the
+ * bidirectional case with the prefix memories Vt^(i), Z^(i) (j <= i) in place
+ * of the whole-sequence ones; a key j reaches every query i >= j, so its
+ * gradient collects the SUFFIX sums
+ *   D^(j)_k = sum_{i>=j} gQ_ik dnum_i,     E^(j)_k = sum_{i>=j} gQ_ik dden_i
+ *   dL/dgK_jk = V_j . D^(j)_k + E^(j)_k,   dV_j = sum_k gK_jk D^(j)_k
+ * The prefix memories are carried forward one position at a time, the suffix
+ * sums backward one position at a time.
+ */
+void gma_oracle_causal_backward(const double *Q, const double *Kx, const double *V, int N,
+                                int d_r, int d_v, const double *mu, const double *sigma2,
+                                const double *log_pi, int K, double eps, const double *dO,
+                                double *dQ, double *dK, double *dV, double *dmu,
+                                double *dsigma2, double *dlog_pi)
+{
+    double *GQ = malloc(sizeof(double) * (size_t)N * K);
+    double *GK = malloc(sizeof(double) * (size_t)N * K);
+    double *UQ = malloc(sizeof(double) * (size_t)N * K);
+    double *UK = malloc(sizeof(double) * (size_t)N * K);
+    double *DN = malloc(sizeof(double) * (size_t)N * d_v);   /* dnum_i */
+    double *DD = malloc(sizeof(double) * (size_t)N);         /* dden_i */
+    double *Vt = calloc((size_t)K * d_v, sizeof(double));
+    double *Z = calloc((size_t)K, sizeof(double));
+    double *D = calloc((size_t)K * d_v, sizeof(double));
+    double *E = calloc((size_t)K, sizeof(double));
+    gma_oracle_responsibilities(Q, N, d_r, mu, sigma2, log_pi, K, GQ);
+    gma_oracle_responsibilities(Kx, N, d_r, mu, sigma2, log_pi, K, GK);
+    for (int i = 0; i < N; ++i) {
+        for (int k = 0; k < K; ++k) {
+            double g = GK[(size_t)i * K + k];
+            Z[k] += g;
+            for (int c = 0; c < d_v; ++c) Vt[(size_t)k * d_v + c] += g * V[(size_t)i * d_v + c];
+        }
+        const double *gq = GQ + (size_t)i * K;
+        double den = eps;
+        for (int k = 0; k < K; ++k) den += gq[k] * Z[k];
+        double dot = 0.0;
+        for (int c = 0; c < d_v; ++c) {
+            double num = 0.0;
+            for (int k = 0; k < K; ++k) num += gq[k] * Vt[(size_t)k * d_v + c];
+            dot += dO[(size_t)i * d_v + c] * (num / den);
+            DN[(size_t)i * d_v + c] = dO[(size_t)i * d_v + c] / den;
+        }
+        DD[i] = -dot / den;
+        for (int k = 0; k < K; ++k) {
+            double u = DD[i] * Z[k];
+            for (int c = 0; c < d_v; ++c) u += DN[(size_t)i * d_v + c] * Vt[(size_t)k * d_v + c];
+            UQ[(size_t)i * K + k] = u;
+        }
+    }
+#if GMA_ORACLE_MUTANT == 8
+    for (int j = 0; j < N; ++j) {
+#else
+    for (int j = N - 1; j >= 0; --j) {
+#endif
+        for (int k = 0; k < K; ++k) {
+            double g = GQ[(size_t)j * K + k];
+            E[k] += g * DD[j];
+            for (int c = 0; c < d_v; ++c) D[(size_t)k * d_v + c] += g * DN[(size_t)j * d_v + c];
+        }
+        for (int k = 0; k < K; ++k) {
+            double u = E[k];
+            for (int c = 0; c < d_v; ++c) u += V[(size_t)j * d_v + c] * D[(size_t)k * d_v + c];
+            UK[(size_t)j * K + k] = u;
+        }
+        for (int c = 0; c < d_v; ++c) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += GK[(size_t)j * K + k] * D[(size_t)k * d_v + c];
+            dV[(size_t)j * d_v + c] = acc;
+        }
+    }
+    score_backward(Q, GQ, UQ, N, d_r, mu, sigma2, K, dQ, dmu, dsigma2, dlog_pi);
+    score_backward(Kx, GK, UK, N, d_r, mu, sigma2, K, dK, dmu, dsigma2, dlog_pi);
+    free(GQ); free(GK); free(UQ); free(UK); free(DN); free(DD);
+    free(Vt); free(Z); free(D); free(E);
 }
