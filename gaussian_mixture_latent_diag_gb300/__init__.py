@@ -20,7 +20,7 @@ import ctypes
 from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError, load,
                       options, status_string)
 
-__all__ = ["forward_bidir", "forward_causal", "responsibilities", "workspace_size",
+__all__ = ["forward_bidir", "forward_causal", "backward_bidir", "responsibilities", "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
            "PATH_TC", "load"]
 
@@ -149,3 +149,45 @@ def forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=No
     """Causal GMA: prefix memories over keys j <= i; O fp32 (or bf16)."""
     return _forward("gma_forward_causal", Q, K, V, mu, sigma2, log_pi, eps, out, workspace,
                     stream, path, splits, sync_status, o_bf16)
+
+
+def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, stream=None,
+                   splits=0, sync_status=False) -> dict:
+    """Gradients of forward_bidir for upstream dO (fp32, like O): dict of dQ, dK, dV
+    (fp32, shaped like Q, K, V) and dmu, dsigma2 [H, K, d_r], dlog_pi [H, K] summed
+    over the batch and over the query and key rows."""
+    import torch
+    lib = load()
+    _check_dev(Q, K, V, mu, sigma2, log_pi, dO)
+    B, H, N, d_r = Q.shape
+    d_v = V.shape[-1]
+    Kc = mu.shape[1]
+    if K.shape != Q.shape or V.shape[:3] != Q.shape[:3] or dO.shape != V.shape:
+        raise ValueError("Q, K must be [B, H, N, d_r], V and dO [B, H, N, d_v]")
+    if mu.shape != (H, Kc, d_r) or sigma2.shape != (H, Kc, d_r) or log_pi.shape != (H, Kc):
+        raise ValueError("mu, sigma2 must be [H, K, d_r] and log_pi [H, K]")
+    if dO.dtype != torch.float32:
+        raise TypeError("dO must be fp32")
+    code = _dtype_code(Q)
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K, V must share one dtype")
+    dev = Q.device
+    out = {"dQ": torch.empty(B, H, N, d_r, dtype=torch.float32, device=dev),
+           "dK": torch.empty(B, H, N, d_r, dtype=torch.float32, device=dev),
+           "dV": torch.empty(B, H, N, d_v, dtype=torch.float32, device=dev),
+           "dmu": torch.empty(H, Kc, d_r, dtype=torch.float32, device=dev),
+           "dsigma2": torch.empty(H, Kc, d_r, dtype=torch.float32, device=dev),
+           "dlog_pi": torch.empty(H, Kc, dtype=torch.float32, device=dev)}
+    opt = options(splits=splits, sync_status=sync_status)
+    nb = int(lib.gma_backward_workspace_size(B, H, N, d_r, d_v, Kc, code, 0, ctypes.byref(opt)))
+    if nb == 0:
+        raise GmaError(2, "gma_backward_bidir")
+    ws = _workspace(nb, dev, workspace)
+    st = lib.gma_backward_bidir(_ptr(Q), _ptr(K), _ptr(V), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi),
+                                float(eps), _ptr(dO), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
+                                _ptr(out["dmu"]), _ptr(out["dsigma2"]), _ptr(out["dlog_pi"]),
+                                B, H, N, d_r, d_v, Kc, ctypes.byref(opt), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_backward_bidir")
+    return out

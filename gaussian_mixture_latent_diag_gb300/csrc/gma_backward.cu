@@ -1,0 +1,504 @@
+// gma_backward.cu -- fp32 CUDA-core kernels for the gradients of the
+// bidirectional GMA forward.
+//
+// Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+// Probabilistic Latent Routing" (arXiv 2606.18283), gradient section: the
+// upstream gradient g_ik = dL/dgamma_ik of a responsibility row, the softmax
+// Jacobian (Eq. (17)) and the gradient entering the score (Eq. (18)),
+//   ds_ik = gamma_ik (g_ik - sum_l gamma_il g_il),
+// then the chain rule for everything that enters the score.  Differentiating
+// Eqs. (5)-(7) with num_i = Gamma^Q_i Vt, den_i = Gamma^Q_i Z + eps:
+//   dnum_i = dO_i / den_i,  dden_i = -(dO_i . O_i) / den_i
+//   g^Q_ik = dnum_i . Vt_k + dden_i Z_k
+//   dVt_k = sum_i gQ_ik dnum_i,  dZ_k = sum_i gQ_ik dden_i
+//   g^K_jk = V_j . dVt_k + dZ_k,  dV_j = sum_k gK_jk dVt_k
+// and through s_ik = c'_k - 1/2 sum_m (x_im - mu_km)^2 / sigma2_km:
+//   dx_im = sum_k ds_ik (mu_km - x_im) / sigma2_km
+//   dmu_km = sum_i ds_ik (x_im - mu_km) / sigma2_km
+//   dsigma2_km = 1/2 sum_i ds_ik ((x_im - mu_km)^2 / sigma2_km^2 - 1 / sigma2_km)
+//   dlog_pi_k = sum_i ds_ik
+// summed over the query and the key rows of every batch row of the head.
+//
+// Steps (each materialises its result in the workspace; fixed summation
+// orders throughout, so results are bitwise reproducible):
+//   state    : the forward up to the latent memory (simt_bidir_state)
+//   upstream : dnum | dden per query row
+//   ds_q     : query score gradients
+//   dmem     : [dVt | dZ] = Gamma^Q^T [dnum | dden], split over N, fixed-order sum
+//   ds_k     : key score gradients;  dV = Gamma^K dVt
+//   dx       : dQ, dK
+//   params   : sum ds, sum ds (x - mu), sum ds (x - mu)^2 per split, then per head
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "gma_internal.h"
+
+namespace gma {
+namespace {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ bool failed(const unsigned *status) {
+    return *reinterpret_cast<const volatile unsigned *>(status) != 0u;
+}
+
+// upstream: one thread per query row.  mem [K][D_V + 1] = [Vt | Z] of the head.
+// dn[i] = [dnum_i (D_V) | dden_i].
+template <int D_V>
+__global__ void __launch_bounds__(128) bwd_upstream_kernel(const float *__restrict__ gqt,
+                                                           const float *__restrict__ mem,
+                                                           const float *__restrict__ dO, int N, int K,
+                                                           float eps, float *__restrict__ dn,
+                                                           const unsigned *status) {
+    if (failed(status)) return;
+    extern __shared__ float smem[];
+    constexpr int W = D_V + 1;
+    const int bh = blockIdx.y;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) smem[e] = mem[(size_t)bh * K * W + e];
+    __syncthreads();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N) return;
+    float num[D_V];
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) num[c] = 0.f;
+    float den = 0.f;
+    const float *g = gqt + (size_t)bh * K * N + i;
+    for (int k = 0; k < K; ++k) {
+        const float gk = g[(size_t)k * N];
+        const float *row = smem + k * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) num[c] = fmaf(gk, row[c], num[c]);
+        den = fmaf(gk, row[D_V], den);
+    }
+    den += eps;
+    const float r = 1.0f / den;
+    const float *go = dO + ((size_t)bh * N + i) * D_V;
+    float *out = dn + ((size_t)bh * N + i) * W;
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) {
+        const float d = go[c];
+        dot = fmaf(d, num[c] * r, dot);
+        out[c] = d * r;
+    }
+    out[D_V] = -dot * r;
+}
+
+// Score gradients of one side, one thread per row ([GMA, Eq. (18)]):
+//   u_ik = a_i . M_k[0:D_V] + beta_i M_k[D_V],   ds_ik = gamma_ik (u_ik - sum_l gamma_il u_il)
+// a_i is row i of A (lda elements apart); beta_i = A[i][D_V] (query side: dden) or 1
+// (key side).  ds [K][N] (component-major, like gamma).
+template <int D_V, bool BETA_IN_A, typename TA>
+__global__ void __launch_bounds__(128) bwd_score_grad_kernel(const float *__restrict__ gt,
+                                                             const TA *__restrict__ A, int lda,
+                                                             const float *__restrict__ M, int N, int K,
+                                                             float *__restrict__ ds, const unsigned *status) {
+    if (failed(status)) return;
+    extern __shared__ float smem[];
+    constexpr int W = D_V + 1;
+    const int bh = blockIdx.y;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) smem[e] = M[(size_t)bh * K * W + e];
+    __syncthreads();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N) return;
+    float a[D_V];
+    const TA *ar = A + ((size_t)bh * N + i) * lda;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) a[c] = to_f32(ar[c]);
+    const float beta = BETA_IN_A ? to_f32(ar[D_V]) : 1.0f;
+    const float *g = gt + (size_t)bh * K * N + i;
+    float *d = ds + (size_t)bh * K * N + i;
+    float mean = 0.f;
+    for (int k = 0; k < K; ++k) {
+        const float *row = smem + k * W;
+        float u = beta * row[D_V];
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) u = fmaf(a[c], row[c], u);
+        d[(size_t)k * N] = u;
+        mean = fmaf(g[(size_t)k * N], u, mean);
+    }
+    for (int k = 0; k < K; ++k) d[(size_t)k * N] = g[(size_t)k * N] * (d[(size_t)k * N] - mean);
+}
+
+// Column sums over a range of rows: part[bh][split][k][c] = sum_{i in split} G[k][i] B[i][c]
+// for c in [64 z, 64 z + 64) and c < ncol.  G [K][N] (component-major), B rows of
+// ldb floats.  Block: 256 threads, each an 4 (k) x 8 (c) tile; rows staged 32 at a
+// time in shared memory; fixed summation order.
+constexpr int kCT = 32;
+__global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict__ Gt,
+                                                         const float *__restrict__ B, int ldb, int ncol,
+                                                         int N, int K, int rows_per_split, int nsplit,
+                                                         float *__restrict__ part, const unsigned *status) {
+    if (failed(status)) return;
+    __shared__ float sg[128][kCT + 1];
+    __shared__ float sb[kCT][64 + 4];
+    const int split = blockIdx.x, bh = blockIdx.y, c0 = 64 * blockIdx.z;
+    const int r0 = split * rows_per_split, r1 = min(N, r0 + rows_per_split);
+    const int tk = threadIdx.x >> 3, tc = threadIdx.x & 7;  // k tile (4 rows), c tile (8 columns)
+    const bool active = 4 * tk < K;
+    float acc[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+    const float *g = Gt + (size_t)bh * K * N;
+    const float *bb = B + (size_t)bh * N * ldb;
+    for (int base = r0; base < r1; base += kCT) {
+        const int n = min(kCT, r1 - base);
+        __syncthreads();
+        for (int e = threadIdx.x; e < K * kCT; e += blockDim.x) {
+            const int k = e / kCT, t = e % kCT;
+            sg[k][t] = t < n ? g[(size_t)k * N + base + t] : 0.f;
+        }
+        for (int e = threadIdx.x; e < kCT * 64; e += blockDim.x) {
+            const int t = e / 64, c = e % 64;
+            sb[t][c] = (t < n && c0 + c < ncol) ? bb[(size_t)(base + t) * ldb + c0 + c] : 0.f;
+        }
+        __syncthreads();
+        if (active) {
+            for (int t = 0; t < n; ++t) {
+                float ga[4], vb[8];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) ga[a] = 4 * tk + a < K ? sg[4 * tk + a][t] : 0.f;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) vb[b] = sb[t][8 * tc + b];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(ga[a], vb[b], acc[a][b]);
+            }
+        }
+    }
+    if (!active) return;
+    float *p = part + ((size_t)bh * nsplit + split) * K * ncol;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int k = 4 * tk + a;
+        if (k >= K) continue;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int c = c0 + 8 * tc + b;
+            if (c < ncol) p[(size_t)k * ncol + c] = acc[a][b];
+        }
+    }
+}
+
+// Fixed-order sum of split partials: out[bh][e] = sum_s part[bh][s][e].
+__global__ void bwd_reduce_kernel(const float *__restrict__ part, int nsplit, int E, float *__restrict__ out,
+                                  const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const float *p = part + (size_t)bh * nsplit * E + e;
+    float acc = 0.f;
+    for (int s = 0; s < nsplit; ++s) acc += p[(size_t)s * E];
+    out[(size_t)bh * E + e] = acc;
+}
+
+// dV_j = sum_k gK_jk dVt_k, one thread per key row.  dmem [K][D_V + 1].
+template <int D_V>
+__global__ void __launch_bounds__(128) bwd_dv_kernel(const float *__restrict__ gkt, const float *__restrict__ dmem,
+                                                     int N, int K, float *__restrict__ dV,
+                                                     const unsigned *status) {
+    if (failed(status)) return;
+    extern __shared__ float smem[];
+    constexpr int W = D_V + 1;
+    const int bh = blockIdx.y;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) smem[e] = dmem[(size_t)bh * K * W + e];
+    __syncthreads();
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= N) return;
+    float acc[D_V];
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    const float *g = gkt + (size_t)bh * K * N + j;
+    for (int k = 0; k < K; ++k) {
+        const float gk = g[(size_t)k * N];
+        const float *row = smem + k * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(gk, row[c], acc[c]);
+    }
+    float *o = dV + ((size_t)bh * N + j) * D_V;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) o[c] = acc[c];
+}
+
+// dx_im = sum_k ds_ik (mu_km - x_im) / sigma2_km for columns [32 z, 32 z + 32),
+// one thread per row.
+template <typename T>
+__global__ void __launch_bounds__(128) bwd_dx_kernel(const T *__restrict__ X, const float *__restrict__ ds,
+                                                     const float *__restrict__ mu, const float *__restrict__ inv,
+                                                     int H, int N, int K, int d_r, float *__restrict__ dX,
+                                                     const unsigned *status) {
+    if (failed(status)) return;
+    constexpr int JC = 32;
+    const int bh = blockIdx.y, h = bh % H, j0 = JC * blockIdx.z;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N) return;
+    const int nj = min(JC, d_r - j0);
+    float x[JC], acc[JC];
+    const T *xr = X + ((size_t)bh * N + i) * d_r + j0;
+#pragma unroll
+    for (int j = 0; j < JC; ++j) {
+        x[j] = j < nj ? to_f32(xr[j]) : 0.f;
+        acc[j] = 0.f;
+    }
+    const float *d = ds + (size_t)bh * K * N + i;
+    const float *muh = mu + (size_t)h * K * d_r + j0, *invh = inv + (size_t)h * K * d_r + j0;
+    for (int k = 0; k < K; ++k) {
+        const float dk = d[(size_t)k * N];
+#pragma unroll
+        for (int j = 0; j < JC; ++j) {
+            if (j < nj) {
+                const float m = __ldg(muh + (size_t)k * d_r + j), v = __ldg(invh + (size_t)k * d_r + j);
+                acc[j] = fmaf(dk * v, m - x[j], acc[j]);
+            }
+        }
+    }
+    float *o = dX + ((size_t)bh * N + i) * d_r + j0;
+#pragma unroll
+    for (int j = 0; j < JC; ++j)
+        if (j < nj) o[j] = acc[j];
+}
+
+// Parameter statistics of one side over a range of rows, columns [32 z, 32 z + 32):
+//   st[k][0] = sum ds_ik,  st[k][1 + m] = sum ds_ik (x_im - mu_km),
+//   st[k][1 + d_r + m] = sum ds_ik (x_im - mu_km)^2
+// (centred on mu_km, so no cancellation).  Block: 256 threads, each a 4 (k) x 4 (m)
+// tile; rows staged 32 at a time in shared memory.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_param_stats_kernel(const T *__restrict__ X, const float *__restrict__ ds,
+                                                              const float *__restrict__ mu, int H, int N, int K,
+                                                              int d_r, int rows_per_split, int nsplit, int side,
+                                                              float *__restrict__ st, const unsigned *status) {
+    if (failed(status)) return;
+    __shared__ float sd[128][kCT + 1];
+    __shared__ float sx[kCT][32 + 1];
+    const int split = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int m0 = 32 * blockIdx.z;
+    const int r0 = split * rows_per_split, r1 = min(N, r0 + rows_per_split);
+    const int tk = threadIdx.x >> 3, tm = threadIdx.x & 7;
+    const bool active = 4 * tk < K;
+    float a1[4][4], a2[4][4], a0[4], mk[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        a0[a] = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            a1[a][b] = a2[a][b] = 0.f;
+            const int k = 4 * tk + a, m = m0 + 4 * tm + b;
+            mk[a][b] = (k < K && m < d_r) ? mu[((size_t)h * K + k) * d_r + m] : 0.f;
+        }
+    }
+    const float *dsb = ds + (size_t)bh * K * N;
+    const T *xb = X + (size_t)bh * N * d_r;
+    for (int base = r0; base < r1; base += kCT) {
+        const int n = min(kCT, r1 - base);
+        __syncthreads();
+        for (int e = threadIdx.x; e < K * kCT; e += blockDim.x) {
+            const int k = e / kCT, t = e % kCT;
+            sd[k][t] = t < n ? dsb[(size_t)k * N + base + t] : 0.f;
+        }
+        for (int e = threadIdx.x; e < kCT * 32; e += blockDim.x) {
+            const int t = e / 32, m = e % 32;
+            sx[t][m] = (t < n && m0 + m < d_r) ? to_f32(xb[(size_t)(base + t) * d_r + m0 + m]) : 0.f;
+        }
+        __syncthreads();
+        if (active) {
+            for (int t = 0; t < n; ++t) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float d = 4 * tk + a < K ? sd[4 * tk + a][t] : 0.f;
+                    a0[a] += d;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const float diff = sx[t][4 * tm + b] - mk[a][b];
+                        const float dd = d * diff;
+                        a1[a][b] += dd;
+                        a2[a][b] = fmaf(dd, diff, a2[a][b]);
+                    }
+                }
+            }
+        }
+    }
+    if (!active) return;
+    const int E = 1 + 2 * d_r;
+    float *p = st + (((size_t)bh * 2 + side) * nsplit + split) * K * E;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int k = 4 * tk + a;
+        if (k >= K) continue;
+        if (m0 == 0 && tm == 0) p[(size_t)k * E] = a0[a];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int m = m0 + 4 * tm + b;
+            if (m < d_r) {
+                p[(size_t)k * E + 1 + m] = a1[a][b];
+                p[(size_t)k * E + 1 + d_r + m] = a2[a][b];
+            }
+        }
+    }
+}
+
+// Per head: the statistics of every batch row, side and split summed in that
+// order, then dlog_pi, dmu, dsigma2.  One thread per (k, m) (and per k for dlog_pi).
+__global__ void bwd_param_final_kernel(const float *__restrict__ st, const float *__restrict__ inv, int B, int H,
+                                       int K, int d_r, int nsplit, float *__restrict__ dmu,
+                                       float *__restrict__ dsigma2, float *__restrict__ dlog_pi,
+                                       const unsigned *status) {
+    if (failed(status)) return;
+    const int h = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= K * d_r) return;
+    const int k = e / d_r, m = e % d_r;
+    const int E = 1 + 2 * d_r;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+    for (int b = 0; b < B; ++b)
+        for (int side = 0; side < 2; ++side)
+            for (int s = 0; s < nsplit; ++s) {
+                const float *p = st + ((((size_t)(b * H + h) * 2 + side) * nsplit + s) * K + k) * E;
+                s0 += p[0];
+                s1 += p[1 + m];
+                s2 += p[1 + d_r + m];
+            }
+    const float v = inv[((size_t)h * K + k) * d_r + m];
+    dmu[((size_t)h * K + k) * d_r + m] = v * s1;
+    dsigma2[((size_t)h * K + k) * d_r + m] = 0.5f * (v * v * s2 - v * s0);
+    if (m == 0) dlog_pi[(size_t)h * K + k] = s0;
+}
+
+struct BwdLayout {
+    SimtLayout F;     // the forward's regions (status, 1/sigma2, c', Gamma^Q, Gamma^K, partials, memory)
+    size_t dn = 0;    // [BH][N][d_v + 1]
+    size_t dsq = 0, dsk = 0;  // [BH][K][N]
+    size_t dpart = 0; // [BH][nsplit][K][d_v + 1]
+    size_t dmem = 0;  // [BH][K][d_v + 1]
+    size_t st = 0;    // [BH][2][nsplit][K][1 + 2 d_r]
+    size_t total = 0;
+};
+
+BwdLayout bwd_layout(const Problem &p, int splits) {
+    BwdLayout L;
+    L.F = simt_layout(p, 0, splits);
+    size_t off = L.F.total;
+    const size_t W = (size_t)p.d_v + 1, BH = p.BH();
+    L.dn = off; off = align256(off + sizeof(float) * BH * p.N * W);
+    L.dsq = off; off = align256(off + sizeof(float) * BH * p.K * p.N);
+    L.dsk = off; off = align256(off + sizeof(float) * BH * p.K * p.N);
+    L.dpart = off; off = align256(off + sizeof(float) * BH * L.F.nsplit * p.K * W);
+    L.dmem = off; off = align256(off + sizeof(float) * BH * p.K * W);
+    L.st = off; off = align256(off + sizeof(float) * BH * 2 * L.F.nsplit * p.K * (1 + 2 * (size_t)p.d_r));
+    L.total = off;
+    return L;
+}
+
+#define GMA_TRY(x)                              \
+    do {                                        \
+        cudaError_t err_ = (x);                 \
+        if (err_ != cudaSuccess) return err_;   \
+    } while (0)
+
+template <int D_V>
+cudaError_t launch_rows(const Problem &p, const BwdLayout &L, const BackwardArgs &g, char *b, cudaStream_t s,
+                        StageClock &clk) {
+    const unsigned *status = reinterpret_cast<const unsigned *>(b);
+    const float *gq = reinterpret_cast<const float *>(b + L.F.gq), *gk = reinterpret_cast<const float *>(b + L.F.gk);
+    const float *mem = reinterpret_cast<const float *>(b + L.F.mem);
+    float *dn = reinterpret_cast<float *>(b + L.dn), *dsq = reinterpret_cast<float *>(b + L.dsq);
+    float *dsk = reinterpret_cast<float *>(b + L.dsk), *dpart = reinterpret_cast<float *>(b + L.dpart);
+    float *dmem = reinterpret_cast<float *>(b + L.dmem);
+    const dim3 grid((p.N + 127) / 128, p.BH());
+    const size_t sm = sizeof(float) * (size_t)p.K * (D_V + 1);
+    auto big = [&](const void *k) {
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    };
+    GMA_TRY(big((const void *)bwd_upstream_kernel<D_V>));
+    bwd_upstream_kernel<D_V><<<grid, 128, sm, s>>>(gq, mem, g.dO, p.N, p.K, p.eps, dn, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    GMA_TRY(big((const void *)bwd_score_grad_kernel<D_V, true, float>));
+    bwd_score_grad_kernel<D_V, true, float><<<grid, 128, sm, s>>>(gq, dn, D_V + 1, mem, p.N, p.K, dsq, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    const int W = D_V + 1;
+    bwd_colsum_kernel<<<dim3(L.F.nsplit, p.BH(), (W + 63) / 64), 256, 0, s>>>(gq, dn, W, W, p.N, p.K,
+                                                                             L.F.tokens_per_split, L.F.nsplit,
+                                                                             dpart, status);
+    GMA_TRY(cudaGetLastError());
+    bwd_reduce_kernel<<<dim3((p.K * W + 255) / 256, p.BH()), 256, 0, s>>>(dpart, L.F.nsplit, p.K * W, dmem, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    if (p.dtype == GMA_F32) {
+        GMA_TRY(big((const void *)bwd_score_grad_kernel<D_V, false, float>));
+        bwd_score_grad_kernel<D_V, false, float><<<grid, 128, sm, s>>>(gk, static_cast<const float *>(p.V), D_V,
+                                                                       dmem, p.N, p.K, dsk, status);
+    } else {
+        GMA_TRY(big((const void *)bwd_score_grad_kernel<D_V, false, __nv_bfloat16>));
+        bwd_score_grad_kernel<D_V, false, __nv_bfloat16><<<grid, 128, sm, s>>>(
+            gk, static_cast<const __nv_bfloat16 *>(p.V), D_V, dmem, p.N, p.K, dsk, status);
+    }
+    GMA_TRY(cudaGetLastError());
+    GMA_TRY(big((const void *)bwd_dv_kernel<D_V>));
+    bwd_dv_kernel<D_V><<<grid, 128, sm, s>>>(gk, dmem, p.N, p.K, g.dV, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t launch_inputs(const Problem &p, const BwdLayout &L, const BackwardArgs &g, char *b, cudaStream_t s,
+                          StageClock &clk) {
+    const unsigned *status = reinterpret_cast<const unsigned *>(b);
+    const float *inv = reinterpret_cast<const float *>(b + L.F.inv_s2);
+    const float *dsq = reinterpret_cast<const float *>(b + L.dsq), *dsk = reinterpret_cast<const float *>(b + L.dsk);
+    float *st = reinterpret_cast<float *>(b + L.st);
+    const T *Q = static_cast<const T *>(p.Q), *Kx = static_cast<const T *>(p.Kx);
+    const dim3 gx((p.N + 127) / 128, p.BH(), (p.d_r + 31) / 32);
+    bwd_dx_kernel<T><<<gx, 128, 0, s>>>(Q, dsq, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dQ, status);
+    GMA_TRY(cudaGetLastError());
+    bwd_dx_kernel<T><<<gx, 128, 0, s>>>(Kx, dsk, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dK, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    const dim3 gs(L.F.nsplit, p.BH(), (p.d_r + 31) / 32);  // z: 32-column block of d_r
+    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Q, dsq, p.mu, p.H, p.N, p.K, p.d_r, L.F.tokens_per_split,
+                                                L.F.nsplit, 0, st, status);
+    GMA_TRY(cudaGetLastError());
+    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Kx, dsk, p.mu, p.H, p.N, p.K, p.d_r, L.F.tokens_per_split,
+                                                L.F.nsplit, 1, st, status);
+    GMA_TRY(cudaGetLastError());
+    bwd_param_final_kernel<<<dim3((p.K * p.d_r + 127) / 128, p.H), 128, 0, s>>>(
+        st, inv, p.B, p.H, p.K, p.d_r, L.F.nsplit, g.dmu, g.dsigma2, g.dlog_pi, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    return cudaSuccess;
+}
+
+}  // namespace
+
+const char *const kBackwardStages[8] = {"state", "upstream", "ds_q", "dmem", "ds_k_dv", "dx", "params", nullptr};
+
+size_t backward_workspace(const Problem &p, int splits) { return bwd_layout(p, splits).total; }
+
+cudaError_t simt_backward_bidir(const Problem &p, const BackwardArgs &g, int splits, void *ws, cudaStream_t s,
+                                StageClock &clk) {
+    const BwdLayout L = bwd_layout(p, splits);
+    char *b = static_cast<char *>(ws);
+    clk.mark();
+    GMA_TRY(simt_bidir_state(p, splits, ws, s));
+    clk.mark();
+    switch (p.d_v) {
+        case 16: GMA_TRY(launch_rows<16>(p, L, g, b, s, clk)); break;
+        case 32: GMA_TRY(launch_rows<32>(p, L, g, b, s, clk)); break;
+        case 64: GMA_TRY(launch_rows<64>(p, L, g, b, s, clk)); break;
+        case 128: GMA_TRY(launch_rows<128>(p, L, g, b, s, clk)); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (p.dtype == GMA_F32) GMA_TRY(launch_inputs<float>(p, L, g, b, s, clk));
+    else GMA_TRY(launch_inputs<__nv_bfloat16>(p, L, g, b, s, clk));
+    return cudaSuccess;
+}
+
+}  // namespace gma

@@ -62,6 +62,22 @@ cudaError_t simt_responsibilities(const Problem &p, void *ws, cudaStream_t s, St
 cudaError_t simt_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &clk);
 extern const char *const kSimtStages[3][8];  // [variant + 1][j], NULL-terminated
+// Everything of the bidirectional SIMT forward before the read: 1/sigma2, c',
+// Gamma^Q, Gamma^K and the latent memory [Vt | Z] in the simt_layout(p, 0, splits)
+// regions of ws.
+cudaError_t simt_bidir_state(const Problem &p, int splits, void *ws, cudaStream_t s);
+
+// ---------------------------------------------------------------- backward (gma_backward.cu)
+struct BackwardArgs {
+    const float *dO = nullptr;                       // [BH][N][d_v]
+    float *dQ = nullptr, *dK = nullptr, *dV = nullptr;  // [BH][N][d_r] / [BH][N][d_v]
+    float *dmu = nullptr, *dsigma2 = nullptr;        // [H][K][d_r]
+    float *dlog_pi = nullptr;                        // [H][K]
+};
+size_t backward_workspace(const Problem &p, int splits);
+cudaError_t simt_backward_bidir(const Problem &p, const BackwardArgs &g, int splits, void *ws, cudaStream_t s,
+                                StageClock &clk);
+extern const char *const kBackwardStages[8];     // NULL-terminated
 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);

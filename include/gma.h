@@ -191,10 +191,42 @@ gma_status gma_forward_bidir_noalloc(const void *Q_X, const void *K_X, const voi
                                      const gma_options *options, void *stream);
 
 /*
+ * Gradients of gma_forward_bidir ([GMA, gradient section]: the upstream
+ * gradient of a responsibility row, the softmax Jacobian (Eq. (17)) and the
+ * gradient entering the score (Eq. (18)), then the chain rule through the
+ * score into the routing rows and the mixture parameters).  Given
+ * dO = dL/dO of the forward with the same arguments:
+ *   dO          : [B, H, N, d_v] fp32 (input)
+ *   dQ_X, dK_X  : [B, H, N, d_r] fp32     dV_X : [B, H, N, d_v] fp32
+ *   dmu, dsigma2: [H, K, d_r] fp32        dlog_pi : [H, K] fp32
+ * The parameter gradients are summed over the batch and over the query and
+ * key rows (one mixture per head).  Every output is written, none is
+ * accumulated into.  The forward's responsibilities and latent memory are
+ * recomputed; everything runs on the CUDA cores in fp32
+ * (options->path must be GMA_PATH_AUTO or GMA_PATH_SIMT, o_bf16 must be 0).
+ * Inputs as for gma_forward_bidir; dO and every output but dlog_pi must start
+ * on a 16-byte boundary, and no output may overlap an input, another output
+ * or the workspace (GMA_ERR_INVALID_ARG).  Device-side parameter errors and
+ * the status word behave as for the forward.
+ *
+ * gma_backward_workspace_size: bytes of workspace for these sizes (causal must
+ * be 0; 0 is returned for unsupported arguments).
+ */
+size_t gma_backward_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
+                                   int causal, const gma_options *options);
+gma_status gma_backward_bidir(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
+                              const float *mu, const float *sigma2, const float *log_pi, float eps,
+                              const float *dO, float *dQ_X, float *dK_X, float *dV_X, float *dmu,
+                              float *dsigma2, float *dlog_pi, int B, int H, int N, int d_r, int d_v,
+                              int K, const gma_options *options, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/*
  * Number of stages (kernel launches, plus the status reset of the first) of
  * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
- * `variant` (-1 responsibilities, 0 bidirectional, 1 causal), and the name of
- * stage j (NULL if out of range).  Used with gma_options.stage_events.
+ * `variant` (-1 responsibilities, 0 bidirectional, 1 causal, 2 bidirectional
+ * backward -- SIMT only), and the name of stage j (NULL if out of range).
+ * Used with gma_options.stage_events.
  */
 int gma_stage_count(int path, int variant);
 const char *gma_stage_name(int path, int variant, int j);

@@ -1,0 +1,125 @@
+"""Parity of the CUDA backward (gma_backward_bidir) with the fp64 oracle.
+
+The gradients are those of "Gaussian Mixture Attention: Linear-Time Sequence
+Mixing via Probabilistic Latent Routing", gradient section (Eq. (18) and the
+chain rule through the score), for the bidirectional forward of Eqs. (5)-(7).
+The kernels compute in fp32 from the same (bf16-rounded, for bf16 cases)
+inputs the oracle widens to fp64.  Metric per output tensor:
+max |g - g_ref| / RMS(g_ref), bound 1e-3 for every gradient.  The bound comes
+from the arithmetic: the score gradient of Eq. (18) subtracts the
+responsibility-weighted mean of the upstream gradient from each component's
+value, which cancels most of them, so fp32 rounding of those values is
+amplified.  A plain numpy fp32 evaluation of the same definitions (no kernel
+involved) already reaches 3.4e-4 (dK) and 3.5e-4 (dsigma2) on these cases;
+the bound leaves a factor of about 3 over that.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = {k: 1e-3 for k in ("dQ", "dK", "dV", "dmu", "dsigma2", "dlog_pi")}
+
+
+def _inputs(B, H, N, d_r, d_v, K, dtype, seed):
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+    d = make_inputs(Case("bwd", False, B, H, N, d_r, d_v, K, dtype), seed=seed)
+    g = torch.Generator().manual_seed(seed + 17)
+    dO = torch.randn(B, H, N, d_v, generator=g, dtype=torch.float32)
+    return d, dO
+
+
+def _run(B, H, N, d_r, d_v, K, dtype, seed=0, splits=0):
+    import gaussian_mixture_latent_diag_gb300 as gma
+    d, dO = _inputs(B, H, N, d_r, d_v, K, dtype, seed)
+    dev = torch.device("cuda")
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    got = gma.backward_bidir(dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev),
+                             eps=d["eps"], splits=splits, sync_status=True)
+    ref = oracle.backward_bidir(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], d["eps"], dO)
+    errs = {}
+    for k, r in ref.items():
+        gk = got[k].double().cpu().numpy()
+        rms = float(np.sqrt((r ** 2).mean()))
+        errs[k] = float(np.abs(gk - r).max()) / max(rms, 1e-300)
+    return errs
+
+
+CASES = [
+    # B, H, N, d_r, d_v, K, dtype
+    (1, 2, 300, 16, 32, 8, "f32"),
+    (2, 2, 300, 64, 64, 64, "bf16"),
+    (1, 2, 257, 32, 16, 5, "bf16"),
+    (1, 1, 129, 128, 128, 128, "f32"),
+    (2, 1, 1000, 64, 64, 64, "f32"),
+    (1, 3, 64, 16, 16, 1, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dN%d_dr%d_dv%d_K%d_%s" % c)
+def test_backward_matches_oracle(case):
+    errs = _run(*case)
+    for k, e in errs.items():
+        if case[5] == 1 and k in ("dQ", "dK", "dmu", "dsigma2", "dlog_pi"):
+            continue  # K = 1: these are exactly zero in the oracle (checked below)
+        assert e <= TOL[k], f"{k}: {e:.3e} > {TOL[k]}"
+
+
+def test_backward_k1_routing_gradients_vanish():
+    import gaussian_mixture_latent_diag_gb300 as gma
+    d, dO = _inputs(1, 2, 200, 16, 16, 1, "f32", 3)
+    dev = torch.device("cuda")
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    got = gma.backward_bidir(dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev),
+                             eps=d["eps"], sync_status=True)
+    for k in ("dQ", "dK", "dmu", "dsigma2", "dlog_pi"):
+        assert float(got[k].abs().max()) == 0.0, k
+
+
+@pytest.mark.parametrize("splits", [1, 3, 7])
+def test_backward_split_count_does_not_change_the_result_beyond_rounding(splits):
+    errs = _run(1, 2, 700, 32, 32, 16, "f32", seed=5, splits=splits)
+    for k, e in errs.items():
+        assert e <= TOL[k], f"{k}: {e:.3e}"
+
+
+def test_backward_is_deterministic():
+    import gaussian_mixture_latent_diag_gb300 as gma
+    d, dO = _inputs(2, 2, 513, 64, 64, 64, "bf16", 7)
+    dev = torch.device("cuda")
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    a = gma.backward_bidir(dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev),
+                           eps=d["eps"], sync_status=True)
+    b = gma.backward_bidir(dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev),
+                           eps=d["eps"], sync_status=True)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_backward_bench_dimensions():
+    # the bench's per-head dimensions (d_r = d_v = K = 64, bf16) at N = 4096
+    errs = _run(2, 2, 4096, 64, 64, 64, "bf16", seed=11)
+    for k, e in errs.items():
+        assert e <= TOL[k], f"{k}: {e:.3e}"
+
+
+def test_backward_rejects_bad_arguments():
+    import ctypes
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300 import _native
+    lib = gma.load()
+    opt = _native.options(path=_native.PATH_TC)
+    assert lib.gma_backward_workspace_size(1, 1, 128, 64, 64, 64, 1, 0, ctypes.byref(opt)) == 0
+    opt = _native.options()
+    assert lib.gma_backward_workspace_size(1, 1, 128, 64, 64, 64, 1, 1, ctypes.byref(opt)) == 0
+    assert lib.gma_backward_workspace_size(1, 1, 128, 48, 64, 64, 1, 0, ctypes.byref(opt)) == 0
+    d, dO = _inputs(1, 1, 128, 16, 16, 4, "f32", 1)
+    dev = torch.device("cuda")
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    with pytest.raises(TypeError):
+        gma.backward_bidir(dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"],
+                           dO.to(dev).double(), eps=d["eps"])
