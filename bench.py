@@ -55,8 +55,10 @@ def tensor_bytes(t: str, w=WORKLOAD) -> int:
 
 
 def source_digest() -> str:
+    """Digest of the sources of the profiled tensor-core kernels."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", "*"))):
+    for f in sorted(glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", "gma_tc.cu")) +
+                    glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", "tc_ptx.cuh"))):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -164,6 +166,20 @@ def _oracle_head(args):
     return time.perf_counter() - t
 
 
+def _oracle_backward_head(seed):
+    """One head of the bidirectional backward through the fp64 oracle (single process)."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import oracle
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+    w = WORKLOAD
+    inp = make_inputs(Case("sample", False, 1, 1, w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"]), seed=seed)
+    dO = np.random.default_rng(seed).standard_normal((1, 1, w["N"], w["d_v"]))
+    t = time.perf_counter()
+    oracle.backward_bidir(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], w["eps"], dO)
+    return time.perf_counter() - t
+
+
 class OraclePool:
     """Spawned worker processes that run oracle heads (started once)."""
 
@@ -213,6 +229,101 @@ def run_reference(args, rank: int):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+BWD_METRIC = "GMA bidirectional backward tokens*heads/s (N=16K, K=64); % of GB300 HBM roofline"
+
+
+def run_backward(args, rank: int, world: int, local_rank: int):
+    """Bidirectional backward over the forward bench's workload: inputs Q, K, V (bf16)
+    and dO (fp32) resident, gradients dQ, dK, dV (fp32) and the parameter
+    gradients written every step.  Algorithmic bytes per token*head: Q, K, V
+    2*64 each, dO 4*64, dQ, dK, dV 4*64 each = 1408 B."""
+    import ctypes
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300 import _native
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    B, H, N, d_r, d_v, K = w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"]
+    inp = make_inputs(Case("bwd", False, B, H, N, d_r, d_v, K, w["dtype"]), seed=rank_seed(rank, 2))
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    g = torch.Generator().manual_seed(rank_seed(rank, 3))
+    dO = torch.randn(B, H, N, d_v, generator=g, dtype=torch.float32).to(dev)
+    outs = [torch.empty(B, H, N, d_r, device=dev), torch.empty(B, H, N, d_r, device=dev),
+            torch.empty(B, H, N, d_v, device=dev), torch.empty(H, K, d_r, device=dev),
+            torch.empty(H, K, d_r, device=dev), torch.empty(H, K, device=dev)]
+    lib = gma.load()
+    opt0 = _native.options()
+    nb = int(lib.gma_backward_workspace_size(B, H, N, d_r, d_v, K, _native.GMA_BF16, 0, ctypes.byref(opt0)))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    stages = _native.stage_names(_native.PATH_SIMT, 2)
+    stream = torch.cuda.current_stream()
+    vp = ctypes.c_void_p
+
+    def call(events=None):
+        opt = _native.options(stage_events=events)
+        st = lib.gma_backward_bidir(vp(d["Q"].data_ptr()), vp(d["K"].data_ptr()), vp(d["V"].data_ptr()),
+                                    _native.GMA_BF16, vp(d["mu"].data_ptr()), vp(d["sigma2"].data_ptr()),
+                                    vp(d["log_pi"].data_ptr()), float(w["eps"]), vp(dO.data_ptr()),
+                                    *[vp(t.data_ptr()) for t in outs], B, H, N, d_r, d_v, K, ctypes.byref(opt),
+                                    vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream))
+        if st != 0:
+            raise gma.GmaError(st, "gma_backward_bidir")
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0.record(stream)
+        for _ in range(args.steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = job_ms(t0.elapsed_time(t1) / args.steps, world, dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        call(events=ev[s])
+    torch.cuda.synchronize()
+    stage_ms = {name: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
+                for j, name in enumerate(stages)}
+    units = world * B * H * N
+    value = units / (ms / 1e3)
+    peak, peak_src = measured_peaks()
+    alg = B * H * N * (3 * 2 * 64 + 4 * 64 + 3 * 4 * 64)
+    achieved = alg / (ms / 1e3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        secs = _oracle_backward_head(7)
+        cpu = {"value": N / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "one head of the same workload (N=16384, d=K=64) through the fp64 C oracle "
+                         f"backward, {secs:.1f} s on one core"}
+    if rank == 0:
+        out = {"metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+               "config": {"workload": "GMA bidirectional backward, B=4 H=8 N=16384 d_r=d_v=K=64, bf16 inputs, "
+                                      "fp32 dO and gradients (per GPU)", **{k: w[k] for k in ("B", "H", "N", "d_r",
+                                                                                           "d_v", "K")},
+                          "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
+               # per call: prep, 2 responsibilities, write, reduce (state); upstream; ds_q;
+               # colsum + reduce (dmem); ds_k + dV; dQ + dK; 2 statistics + final (params)
+               "gpu_launches": 16 * args.steps,
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                            "frac": achieved / peak, "traffic": None, "kernel": "whole call (all stages)",
+                            "algorithmic_bytes": alg, "peak_source": peak_src},
+               "stage_ms": stage_ms, "clocks": clocks.summary(), "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+
 
 def rank_seed(rank: int, variant: int) -> int:
     """Input seed of one variant on one rank: each rank draws its own heads (replicas
@@ -429,6 +540,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["forward", "backward"], default="forward",
+                    help="forward: the bidirectional + causal forward step (default); "
+                         "backward: the bidirectional backward")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -442,7 +556,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     try:
-        run_gma(args, rank, world, local_rank)
+        if args.workload == "backward":
+            run_backward(args, rank, world, local_rank)
+        else:
+            run_gma(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist
