@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(128) bwd_dv_kernel(const float *__restrict__ g
 }
 
 // dx_im = sum_k ds_ik (mu_km - x_im) / sigma2_km for columns [32 z, 32 z + 32),
-// one thread per row.
+// one thread per row; the block's (mu, 1/sigma2) columns are staged in shared
+// memory (K x 32 pairs).
 template <typename T>
 __global__ void __launch_bounds__(128) bwd_dx_kernel(const T *__restrict__ X, const float *__restrict__ ds,
                                                      const float *__restrict__ mu, const float *__restrict__ inv,
@@ -235,10 +236,17 @@ __global__ void __launch_bounds__(128) bwd_dx_kernel(const T *__restrict__ X, co
                                                      const unsigned *status) {
     if (failed(status)) return;
     constexpr int JC = 32;
+    __shared__ float2 sp[128][JC];
     const int bh = blockIdx.y, h = bh % H, j0 = JC * blockIdx.z;
+    const int nj = min(JC, d_r - j0);
+    for (int e = threadIdx.x; e < K * JC; e += blockDim.x) {
+        const int k = e / JC, j = e % JC;
+        const size_t o = ((size_t)h * K + k) * d_r + j0 + j;
+        sp[k][j] = j < nj ? make_float2(mu[o], inv[o]) : make_float2(0.f, 0.f);
+    }
+    __syncthreads();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= N) return;
-    const int nj = min(JC, d_r - j0);
     float x[JC], acc[JC];
     const T *xr = X + ((size_t)bh * N + i) * d_r + j0;
 #pragma unroll
@@ -247,15 +255,12 @@ __global__ void __launch_bounds__(128) bwd_dx_kernel(const T *__restrict__ X, co
         acc[j] = 0.f;
     }
     const float *d = ds + (size_t)bh * K * N + i;
-    const float *muh = mu + (size_t)h * K * d_r + j0, *invh = inv + (size_t)h * K * d_r + j0;
     for (int k = 0; k < K; ++k) {
         const float dk = d[(size_t)k * N];
 #pragma unroll
         for (int j = 0; j < JC; ++j) {
-            if (j < nj) {
-                const float m = __ldg(muh + (size_t)k * d_r + j), v = __ldg(invh + (size_t)k * d_r + j);
-                acc[j] = fmaf(dk * v, m - x[j], acc[j]);
-            }
+            const float2 mv = sp[k][j];
+            acc[j] = fmaf(dk * mv.y, mv.x - x[j], acc[j]);
         }
     }
     float *o = dX + ((size_t)bh * N + i) * d_r + j0;

@@ -65,6 +65,9 @@ __global__ void prep_simt_kernel(const float *__restrict__ mu, const float *__re
 // One thread per row: scores, then a max-subtracted softmax over k
 // ([GMA, Eq. (3)]).  The row is written three times to `out` (scores,
 // exponentials, normalised values); each thread only touches its own row.
+// The head's (mu, 1/sigma2) are staged in shared memory 32 components at a
+// time; every thread of the block takes part in the staging.
+constexpr int kRespKC = 32;
 template <int D_R, typename T>
 __global__ void __launch_bounds__(128) resp_simt_kernel(
     const T *__restrict__ X, int H, int N, int K, const float *__restrict__ mu,
@@ -72,39 +75,55 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
     long long out_bh_stride, long long out_stride_n, long long out_stride_k,
     const unsigned *status) {
     if (failed(status)) return;
+    __shared__ float2 sp[kRespKC][D_R];
     const int bh = blockIdx.y, h = bh % H;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= N) return;
+    const bool valid = i < N;
     float x[D_R];
-    const T *xr = X + ((size_t)bh * N + i) * D_R;
+    const T *xr = X + ((size_t)bh * N + (valid ? i : 0)) * D_R;
 #pragma unroll
     for (int j = 0; j < D_R; ++j) x[j] = to_f32(xr[j]);
     const float *muh = mu + (size_t)h * K * D_R;
     const float *invh = inv + (size_t)h * K * D_R;
     const float *ch = cprime + (size_t)h * K;
-    float *o = out + (size_t)bh * out_bh_stride + (size_t)i * out_stride_n;
+    float *o = out + (size_t)bh * out_bh_stride + (size_t)(valid ? i : 0) * out_stride_n;
 
     float m = -INFINITY;
-    for (int k = 0; k < K; ++k) {
-        const float *mk = muh + (size_t)k * D_R, *ik = invh + (size_t)k * D_R;
-        // Eight interleaved partial sums, combined in fp64: the terms are
-        // positive and the total reaches several hundred at d_r = 128, where
-        // one sequential fp32 sum loses the fp32 tolerance.
-        float q8[8];
+    for (int k0 = 0; k0 < K; k0 += kRespKC) {
+        const int nk = min(kRespKC, K - k0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nk * D_R; e += blockDim.x)
+            sp[e / D_R][e % D_R] = make_float2(muh[(size_t)k0 * D_R + e], invh[(size_t)k0 * D_R + e]);
+        __syncthreads();
+        if (!valid) continue;
+        for (int kk = 0; kk < nk; ++kk) {
+            // Eight interleaved partial sums, combined without rounding error
+            // into hi + lo (TwoSum, Knuth): the terms are positive and the total
+            // reaches several hundred at d_r = 128, where one sequential fp32 sum
+            // loses the fp32 tolerance.
+            float q8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) q8[u] = 0.f;
+            for (int u = 0; u < 8; ++u) q8[u] = 0.f;
 #pragma unroll
-        for (int j = 0; j < D_R; ++j) {
-            float d = x[j] - __ldg(mk + j);
-            q8[j & 7] = fmaf(d * d, __ldg(ik + j), q8[j & 7]);
+            for (int j = 0; j < D_R; ++j) {
+                const float2 mv = sp[kk][j];
+                float d = x[j] - mv.x;
+                q8[j & 7] = fmaf(d * d, mv.y, q8[j & 7]);
+            }
+            float hi = q8[0], lo = 0.f;
+#pragma unroll
+            for (int u = 1; u < 8; ++u) {
+                const float t = hi + q8[u], bb = t - hi;
+                lo += (hi - (t - bb)) + (q8[u] - bb);
+                hi = t;
+            }
+            const int k = k0 + kk;
+            float s = (__ldg(ch + k) - 0.5f * hi) - 0.5f * lo;
+            o[(size_t)k * out_stride_k] = s;
+            m = fmaxf(m, s);
         }
-        double q = 0.0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) q += (double)q8[u];
-        float s = (float)((double)__ldg(ch + k) - 0.5 * q);
-        o[(size_t)k * out_stride_k] = s;
-        m = fmaxf(m, s);
     }
+    if (!valid) return;
     float z = 0.f;
     for (int k = 0; k < K; ++k) {
         float e = expf(o[(size_t)k * out_stride_k] - m);
