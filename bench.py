@@ -230,14 +230,14 @@ def run_reference(args, rank: int):
 
 # ------------------------------------------------------------------ GPU arm
 
-BWD_METRIC = "GMA bidirectional backward tokens*heads/s (N=16K, K=64); % of GB300 HBM roofline"
+BWD_METRIC = "GMA backward tokens*heads/s (bidir & causal, N=16K, K=64); % of GB300 HBM roofline"
 
 
 def run_backward(args, rank: int, world: int, local_rank: int):
-    """Bidirectional backward over the forward bench's workload: inputs Q, K, V (bf16)
-    and dO (fp32) resident, gradients dQ, dK, dV (fp32) and the parameter
-    gradients written every step.  Algorithmic bytes per token*head: Q, K, V
-    2*64 each, dO 4*64, dQ, dK, dV 4*64 each = 1408 B."""
+    """One bidirectional and one causal backward per step over the forward bench's
+    workload: inputs Q, K, V (bf16) and dO (fp32) resident, gradients dQ, dK, dV
+    (fp32) and the parameter gradients written every step.  Algorithmic bytes per
+    token*head and variant: Q, K, V 2*64 each, dO 4*64, dQ, dK, dV 4*64 each = 1408 B."""
     import ctypes
     import torch
     import gaussian_mixture_latent_diag_gb300 as gma
@@ -258,20 +258,26 @@ def run_backward(args, rank: int, world: int, local_rank: int):
     lib = gma.load()
     opt0 = _native.options()
     nb = int(lib.gma_backward_workspace_size(B, H, N, d_r, d_v, K, _native.GMA_BF16, 0, ctypes.byref(opt0)))
+    nb = max(nb, int(lib.gma_backward_workspace_size(B, H, N, d_r, d_v, K, _native.GMA_BF16, 1,
+                                                     ctypes.byref(opt0))))
     ws = torch.empty(nb, dtype=torch.uint8, device=dev)
-    stages = _native.stage_names(_native.PATH_SIMT, 2)
+    stages = [_native.stage_names(_native.PATH_SIMT, 2), _native.stage_names(_native.PATH_SIMT, 3)]
     stream = torch.cuda.current_stream()
     vp = ctypes.c_void_p
 
-    def call(events=None):
+    def call1(fn, events=None):
         opt = _native.options(stage_events=events)
-        st = lib.gma_backward_bidir(vp(d["Q"].data_ptr()), vp(d["K"].data_ptr()), vp(d["V"].data_ptr()),
+        st = getattr(lib, fn)(vp(d["Q"].data_ptr()), vp(d["K"].data_ptr()), vp(d["V"].data_ptr()),
                                     _native.GMA_BF16, vp(d["mu"].data_ptr()), vp(d["sigma2"].data_ptr()),
                                     vp(d["log_pi"].data_ptr()), float(w["eps"]), vp(dO.data_ptr()),
                                     *[vp(t.data_ptr()) for t in outs], B, H, N, d_r, d_v, K, ctypes.byref(opt),
                                     vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream))
         if st != 0:
-            raise gma.GmaError(st, "gma_backward_bidir")
+            raise gma.GmaError(st, fn)
+
+    def call(events=None):
+        call1("gma_backward_bidir", events[0] if events else None)
+        call1("gma_backward_causal", events[1] if events else None)
 
     for _ in range(args.warmup):
         call()
@@ -288,16 +294,20 @@ def run_backward(args, rank: int, world: int, local_rank: int):
         t1.record(stream)
         torch.cuda.synchronize()
     ms = job_ms(t0.elapsed_time(t1) / args.steps, world, dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(stages[v]) + 1)] for v in range(2)]
+          for _ in range(args.steps)]
     for s in range(args.steps):
         call(events=ev[s])
     torch.cuda.synchronize()
-    stage_ms = {name: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
-                for j, name in enumerate(stages)}
-    units = world * B * H * N
+    stage_ms = {f"{('bidir', 'causal')[v]}:{name}": statistics.mean(ev[s][v][j].elapsed_time(ev[s][v][j + 1])
+                                                                   for s in range(args.steps))
+                for v in range(2) for j, name in enumerate(stages[v])}
+    variant_ms = {("bidir", "causal")[v]: statistics.mean(ev[s][v][0].elapsed_time(ev[s][v][-1])
+                                                         for s in range(args.steps)) for v in range(2)}
+    units = world * 2 * B * H * N
     value = units / (ms / 1e3)
     peak, peak_src = measured_peaks()
-    alg = B * H * N * (3 * 2 * 64 + 4 * 64 + 3 * 4 * 64)
+    alg = 2 * B * H * N * (3 * 2 * 64 + 4 * 64 + 3 * 4 * 64)
     achieved = alg / (ms / 1e3) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -305,23 +315,25 @@ def run_backward(args, rank: int, world: int, local_rank: int):
         oracle.build()
         secs = _oracle_backward_head(7)
         cpu = {"value": N / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "one head of the same workload (N=16384, d=K=64) through the fp64 C oracle "
-                         f"backward, {secs:.1f} s on one core"}
+               "sample": "one bidirectional head of the same workload (N=16384, d=K=64) through the fp64 C "
+                         f"oracle backward, {secs:.1f} s on one core"}
     if rank == 0:
         out = {"metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-               "config": {"workload": "GMA bidirectional backward, B=4 H=8 N=16384 d_r=d_v=K=64, bf16 inputs, "
-                                      "fp32 dO and gradients (per GPU)", **{k: w[k] for k in ("B", "H", "N", "d_r",
+               "config": {"workload": "GMA backward, bidirectional + causal, B=4 H=8 N=16384 d_r=d_v=K=64, bf16 "
+                                      "inputs, fp32 dO and gradients (per GPU)", **{k: w[k] for k in ("B", "H", "N", "d_r",
                                                                                            "d_v", "K")},
                           "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
-               # per call: prep, 2 responsibilities, write, reduce (state); upstream; ds_q;
-               # colsum + reduce (dmem); ds_k + dV; dQ + dK; 2 statistics + final (params)
-               "gpu_launches": 16 * args.steps,
+               # bidirectional: prep, 2 responsibilities, write, reduce (state); upstream; ds_q;
+               # colsum + reduce (dmem); ds_k + dV; dQ + dK; 2 statistics + final (params) = 16;
+               # causal: prep, 2 responsibilities, write, scan (state); query; colsum + suffix;
+               # key; dQ + dK; 2 statistics + final = 15
+               "gpu_launches": (16 + 15) * args.steps,
                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                             "frac": achieved / peak, "traffic": None, "kernel": "whole call (all stages)",
                             "algorithmic_bytes": alg, "peak_source": peak_src},
-               "stage_ms": stage_ms, "clocks": clocks.summary(), "cpu_baseline": cpu}
+               "variants_ms": variant_ms, "stage_ms": stage_ms, "clocks": clocks.summary(), "cpu_baseline": cpu}
         print(json.dumps(out), flush=True)
 
 

@@ -20,7 +20,8 @@ import ctypes
 from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError, load,
                       options, status_string)
 
-__all__ = ["forward_bidir", "forward_causal", "backward_bidir", "responsibilities", "workspace_size",
+__all__ = ["forward_bidir", "forward_causal", "backward_bidir", "backward_causal", "responsibilities",
+           "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
            "PATH_TC", "load"]
 
@@ -156,6 +157,18 @@ def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, st
     """Gradients of forward_bidir for upstream dO (fp32, like O): dict of dQ, dK, dV
     (fp32, shaped like Q, K, V) and dmu, dsigma2 [H, K, d_r], dlog_pi [H, K] summed
     over the batch and over the query and key rows."""
+    return _backward("gma_backward_bidir", Q, K, V, mu, sigma2, log_pi, dO, eps, workspace, stream, splits,
+                     sync_status)
+
+
+def backward_causal(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, stream=None,
+                    sync_status=False) -> dict:
+    """Gradients of forward_causal for upstream dO; same outputs as backward_bidir."""
+    return _backward("gma_backward_causal", Q, K, V, mu, sigma2, log_pi, dO, eps, workspace, stream, 0,
+                     sync_status)
+
+
+def _backward(fn_name, Q, K, V, mu, sigma2, log_pi, dO, eps, workspace, stream, splits, sync_status) -> dict:
     import torch
     lib = load()
     _check_dev(Q, K, V, mu, sigma2, log_pi, dO)
@@ -179,15 +192,16 @@ def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, st
            "dsigma2": torch.empty(H, Kc, d_r, dtype=torch.float32, device=dev),
            "dlog_pi": torch.empty(H, Kc, dtype=torch.float32, device=dev)}
     opt = options(splits=splits, sync_status=sync_status)
-    nb = int(lib.gma_backward_workspace_size(B, H, N, d_r, d_v, Kc, code, 0, ctypes.byref(opt)))
+    causal = 1 if fn_name == "gma_backward_causal" else 0
+    nb = int(lib.gma_backward_workspace_size(B, H, N, d_r, d_v, Kc, code, causal, ctypes.byref(opt)))
     if nb == 0:
-        raise GmaError(2, "gma_backward_bidir")
+        raise GmaError(2, fn_name)
     ws = _workspace(nb, dev, workspace)
-    st = lib.gma_backward_bidir(_ptr(Q), _ptr(K), _ptr(V), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi),
+    st = getattr(lib, fn_name)(_ptr(Q), _ptr(K), _ptr(V), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi),
                                 float(eps), _ptr(dO), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]),
                                 _ptr(out["dmu"]), _ptr(out["dsigma2"]), _ptr(out["dlog_pi"]),
                                 B, H, N, d_r, d_v, Kc, ctypes.byref(opt), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream))
     if st != 0:
-        raise GmaError(st, "gma_backward_bidir")
+        raise GmaError(st, fn_name)
     return out

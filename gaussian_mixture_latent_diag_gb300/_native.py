@@ -24,7 +24,8 @@ STATUS_NAMES = {
 EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_forward_causal", "gma_last_device_status", "gma_status_string",
             "gma_selected_path", "gma_stage_count", "gma_stage_name",
-            "gma_forward_bidir_noalloc", "gma_backward_workspace_size", "gma_backward_bidir")
+            "gma_forward_bidir_noalloc", "gma_backward_workspace_size", "gma_backward_bidir",
+            "gma_backward_causal")
 
 
 class Options(ctypes.Structure):
@@ -72,6 +73,8 @@ def load(path: str | None = None):
         lib.gma_backward_workspace_size.restype = sz
         lib.gma_backward_bidir.argtypes = [vp, vp, vp, i, vp, vp, vp, f] + [vp] * 7 + [i] * 6 + [opt, vp, sz, vp]
         lib.gma_backward_bidir.restype = i
+        lib.gma_backward_causal.argtypes = lib.gma_backward_bidir.argtypes
+        lib.gma_backward_causal.restype = i
         lib.gma_last_device_status.argtypes = [vp, vp]
         lib.gma_last_device_status.restype = i
         lib.gma_status_string.argtypes = [i]

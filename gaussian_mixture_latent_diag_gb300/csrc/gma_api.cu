@@ -111,6 +111,61 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     return finish(err, options, workspace, s);
 }
 
+gma_status backward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype, const float *mu,
+                    const float *sigma2, const float *log_pi, float eps, const float *dO, float *dQ_X,
+                    float *dK_X, float *dV_X, float *dmu, float *dsigma2, float *dlog_pi, int B, int H, int N,
+                    int d_r, int d_v, int K, const gma_options *options, void *workspace,
+                    size_t workspace_bytes, void *stream, int causal) {
+    if (!Q_X || !K_X || !V_X || !mu || !sigma2 || !log_pi || !dO || !dQ_X || !dK_X || !dV_X || !dmu ||
+        !dsigma2 || !dlog_pi || !workspace)
+        return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(Q_X) || !aligned16(K_X) || !aligned16(V_X) || !aligned16(mu) || !aligned16(sigma2) ||
+        !aligned16(dO) || !aligned16(dQ_X) || !aligned16(dK_X) || !aligned16(dV_X) || !aligned16(dmu) ||
+        !aligned16(dsigma2) || reinterpret_cast<uintptr_t>(dlog_pi) % 4 != 0)
+        return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (options && options->splits < 0) return GMA_ERR_INVALID_ARG;
+    if (options && (options->o_bf16 || (options->path != GMA_PATH_AUTO && options->path != GMA_PATH_SIMT)))
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+
+    Problem p;
+    p.Q = Q_X; p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi;
+    p.dtype = dtype; p.eps = eps;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    const int splits = options ? options->splits : 0;
+    const size_t need = gma::backward_workspace(p, causal, splits);
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+
+    const size_t es = dtype == GMA_F32 ? 4 : 2;
+    const size_t rows = (size_t)B * H * N;
+    const size_t nr = es * rows * d_r, nv = es * rows * d_v;
+    const size_t fr = 4 * rows * d_r, fv = 4 * rows * d_v, fp = 4 * (size_t)H * K * d_r, fl = 4 * (size_t)H * K;
+    const void *in[] = {Q_X, K_X, V_X, dO, mu, sigma2, log_pi, workspace};
+    const size_t nin[] = {nr, nr, nv, fv, fp, fp, fl, need};
+    const void *out[] = {dQ_X, dK_X, dV_X, dmu, dsigma2, dlog_pi};
+    const size_t nout[] = {fr, fr, fv, fp, fp, fl};
+    for (int a = 0; a < 6; ++a) {
+        for (int b = 0; b < 8; ++b)
+            if (overlaps(out[a], nout[a], in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 6; ++b)
+            if (overlaps(out[a], nout[a], out[b], nout[b])) return GMA_ERR_INVALID_ARG;
+    }
+    if (overlaps(workspace, need, Q_X, nr) || overlaps(workspace, need, K_X, nr) ||
+        overlaps(workspace, need, V_X, nv) || overlaps(workspace, need, dO, fv))
+        return GMA_ERR_INVALID_ARG;
+
+    gma::BackwardArgs g;
+    g.dO = dO; g.dQ = dQ_X; g.dK = dK_X; g.dV = dV_X; g.dmu = dmu; g.dsigma2 = dsigma2; g.dlog_pi = dlog_pi;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    const cudaError_t err = causal ? gma::simt_backward_causal(p, g, workspace, s, clk)
+                                   : gma::simt_backward_bidir(p, g, splits, workspace, s, clk);
+    return finish(err, options, workspace, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -175,14 +230,14 @@ gma_status gma_forward_causal(const void *Q_X, const void *K_X, const void *V_X,
 
 size_t gma_backward_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
                                    int causal, const gma_options *options) {
-    if (causal != 0 || (dtype != GMA_F32 && dtype != GMA_BF16)) return 0;
+    if ((causal != 0 && causal != 1) || (dtype != GMA_F32 && dtype != GMA_BF16)) return 0;
     if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
     if (options && (options->splits < 0 || options->o_bf16 ||
                     (options->path != GMA_PATH_AUTO && options->path != GMA_PATH_SIMT)))
         return 0;
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    return gma::backward_workspace(p, options ? options->splits : 0);
+    return gma::backward_workspace(p, causal, options ? options->splits : 0);
 }
 
 gma_status gma_backward_bidir(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
@@ -191,52 +246,18 @@ gma_status gma_backward_bidir(const void *Q_X, const void *K_X, const void *V_X,
                               float *dsigma2, float *dlog_pi, int B, int H, int N, int d_r, int d_v,
                               int K, const gma_options *options, void *workspace,
                               size_t workspace_bytes, void *stream) {
-    if (!Q_X || !K_X || !V_X || !mu || !sigma2 || !log_pi || !dO || !dQ_X || !dK_X || !dV_X || !dmu ||
-        !dsigma2 || !dlog_pi || !workspace)
-        return GMA_ERR_INVALID_ARG;
-    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
-    if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
-    if (!aligned16(Q_X) || !aligned16(K_X) || !aligned16(V_X) || !aligned16(mu) || !aligned16(sigma2) ||
-        !aligned16(dO) || !aligned16(dQ_X) || !aligned16(dK_X) || !aligned16(dV_X) || !aligned16(dmu) ||
-        !aligned16(dsigma2) || reinterpret_cast<uintptr_t>(dlog_pi) % 4 != 0)
-        return GMA_ERR_INVALID_ARG;
-    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
-    if (options && options->splits < 0) return GMA_ERR_INVALID_ARG;
-    if (options && (options->o_bf16 || (options->path != GMA_PATH_AUTO && options->path != GMA_PATH_SIMT)))
-        return GMA_ERR_UNSUPPORTED_SHAPE;
+    return backward(Q_X, K_X, V_X, dtype, mu, sigma2, log_pi, eps, dO, dQ_X, dK_X, dV_X, dmu, dsigma2, dlog_pi,
+                    B, H, N, d_r, d_v, K, options, workspace, workspace_bytes, stream, 0);
+}
 
-    Problem p;
-    p.Q = Q_X; p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi;
-    p.dtype = dtype; p.eps = eps;
-    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    const int splits = options ? options->splits : 0;
-    const size_t need = gma::backward_workspace(p, splits);
-    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
-
-    const size_t es = dtype == GMA_F32 ? 4 : 2;
-    const size_t rows = (size_t)B * H * N;
-    const size_t nr = es * rows * d_r, nv = es * rows * d_v;
-    const size_t fr = 4 * rows * d_r, fv = 4 * rows * d_v, fp = 4 * (size_t)H * K * d_r, fl = 4 * (size_t)H * K;
-    const void *in[] = {Q_X, K_X, V_X, dO, mu, sigma2, log_pi, workspace};
-    const size_t nin[] = {nr, nr, nv, fv, fp, fp, fl, need};
-    const void *out[] = {dQ_X, dK_X, dV_X, dmu, dsigma2, dlog_pi};
-    const size_t nout[] = {fr, fr, fv, fp, fp, fl};
-    for (int a = 0; a < 6; ++a) {
-        for (int b = 0; b < 8; ++b)
-            if (overlaps(out[a], nout[a], in[b], nin[b])) return GMA_ERR_INVALID_ARG;
-        for (int b = a + 1; b < 6; ++b)
-            if (overlaps(out[a], nout[a], out[b], nout[b])) return GMA_ERR_INVALID_ARG;
-    }
-    if (overlaps(workspace, need, Q_X, nr) || overlaps(workspace, need, K_X, nr) ||
-        overlaps(workspace, need, V_X, nv) || overlaps(workspace, need, dO, fv))
-        return GMA_ERR_INVALID_ARG;
-
-    gma::BackwardArgs g;
-    g.dO = dO; g.dQ = dQ_X; g.dK = dK_X; g.dV = dV_X; g.dmu = dmu; g.dsigma2 = dsigma2; g.dlog_pi = dlog_pi;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    gma::StageClock clk = clock_for(options, s);
-    return finish(gma::simt_backward_bidir(p, g, splits, workspace, s, clk), options, workspace, s);
+gma_status gma_backward_causal(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
+                               const float *mu, const float *sigma2, const float *log_pi, float eps,
+                               const float *dO, float *dQ_X, float *dK_X, float *dV_X, float *dmu,
+                               float *dsigma2, float *dlog_pi, int B, int H, int N, int d_r, int d_v,
+                               int K, const gma_options *options, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    return backward(Q_X, K_X, V_X, dtype, mu, sigma2, log_pi, eps, dO, dQ_X, dK_X, dV_X, dmu, dsigma2, dlog_pi,
+                    B, H, N, d_r, d_v, K, options, workspace, workspace_bytes, stream, 1);
 }
 
 gma_status gma_last_device_status(const void *workspace, void *stream) {
@@ -274,9 +295,9 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
 }
 
 int gma_stage_count(int path, int variant) {
-    if (variant < -1 || variant > 2 || (variant == 2 && path != GMA_PATH_SIMT)) return 0;
+    if (variant < -1 || variant > 3 || (variant >= 2 && path != GMA_PATH_SIMT)) return 0;
     const char *const *names;
-    if (variant == 2) names = gma::kBackwardStages;
+    if (variant >= 2) names = gma::kBackwardStages[variant - 2];
     else if (path == GMA_PATH_SIMT) names = gma::kSimtStages[variant + 1];
     else if (path == GMA_PATH_TC) names = gma::kTcStages[variant + 1];
     else return 0;
@@ -288,7 +309,7 @@ int gma_stage_count(int path, int variant) {
 const char *gma_stage_name(int path, int variant, int j) {
     int n = gma_stage_count(path, variant);
     if (j < 0 || j >= n) return nullptr;
-    if (variant == 2) return gma::kBackwardStages[j];
+    if (variant >= 2) return gma::kBackwardStages[variant - 2][j];
     return path == GMA_PATH_SIMT ? gma::kSimtStages[variant + 1][j] : gma::kTcStages[variant + 1][j];
 }
 

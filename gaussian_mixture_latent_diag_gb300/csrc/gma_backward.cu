@@ -1,5 +1,5 @@
 // gma_backward.cu -- fp32 CUDA-core kernels for the gradients of the
-// bidirectional GMA forward.
+// bidirectional and the causal GMA forward.
 //
 // Paper: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
 // Probabilistic Latent Routing" (arXiv 2606.18283), gradient section: the
@@ -18,6 +18,15 @@
 //   dsigma2_km = 1/2 sum_i ds_ik ((x_im - mu_km)^2 / sigma2_km^2 - 1 / sigma2_km)
 //   dlog_pi_k = sum_i ds_ik
 // summed over the query and the key rows of every batch row of the head.
+//
+// Causal variant ([GMA, Eq. (8b)] differentiated): the query side reads the
+// prefix memories Vt^(i), Z^(i) (j <= i) instead, and a key j collects the
+// SUFFIX sums over the queries i >= j:
+//   g^K_jk = V_j . D^(j)_k + E^(j)_k,  dV_j = sum_k gK_jk D^(j)_k,
+//   D^(j)_k = sum_{i>=j} gQ_ik dnum_i,  E^(j)_k = sum_{i>=j} gQ_ik dden_i,
+// computed in chunks of kSimtCausalChunk tokens: the sums over earlier (later)
+// chunks come from an exclusive prefix (suffix) over per-chunk aggregates, the
+// rest inside the chunk.
 //
 // Steps (each materialises its result in the workspace; fixed summation
 // orders throughout, so results are bitwise reproducible):
@@ -375,27 +384,222 @@ __global__ void bwd_param_final_kernel(const float *__restrict__ st, const float
     if (m == 0) dlog_pi[(size_t)h * K + k] = s0;
 }
 
+// Causal query rows, one block per chunk of C tokens, one thread per query
+// row i: num_i, den_i from the chunk's exclusive prefix (S, Z) plus the
+// intra-chunk terms j <= i; dnum_i, dden_i (written to dn); then
+//   u_ik = dnum_i . S_k + dden_i Z_k + sum_{t0<=j<=i} gK_jk (dnum_i . V_j + dden_i)
+// and ds^Q_ik = gQ_ik (u_ik - sum_l gQ_il u_il) ([GMA, Eq. (18)]).
+template <int D_V, typename T>
+__global__ void __launch_bounds__(kSimtCausalChunk) bwd_causal_query_kernel(
+    const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
+    const float *__restrict__ prefix, const float *__restrict__ dO, int N, int K, int nchunk, float eps,
+    float *__restrict__ dn, float *__restrict__ dsq, const unsigned *status) {
+    if (failed(status)) return;
+    constexpr int C = kSimtCausalChunk;
+    constexpr int W = D_V + 1;
+    extern __shared__ float smem[];
+    float *sgq = smem;              // [K][C]
+    float *sgk = sgq + K * C;       // [K][C]
+    float *sv = sgk + K * C;        // [C][D_V]
+    float *ss = sv + C * D_V;       // [K][W]
+    float *sb = ss + K * W;         // [C][C + 1]: b_ij of query row i
+    const int chunk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = chunk * C;
+    const int n = min(C, N - t0);
+    const float *gq = gqt + (size_t)bh * K * N, *gk = gkt + (size_t)bh * K * N;
+    for (int e = threadIdx.x; e < K * C; e += blockDim.x) {
+        const int k = e / C, t = e % C;
+        sgq[e] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
+        sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
+    }
+    const T *v = V + ((size_t)bh * N + t0) * D_V;
+    for (int e = threadIdx.x; e < C * D_V; e += blockDim.x) sv[e] = e < n * D_V ? to_f32(v[e]) : 0.f;
+    const float *pre = prefix + ((size_t)bh * nchunk + chunk) * K * W;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) ss[e] = pre[e];
+    __syncthreads();
+    const int i = threadIdx.x;
+    if (i >= n) return;
+    float acc[D_V];
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    float den = 0.f;
+    for (int k = 0; k < K; ++k) {
+        const float g = sgq[k * C + i];
+        const float *row = ss + k * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(g, row[c], acc[c]);
+        den = fmaf(g, row[D_V], den);
+    }
+    for (int j = 0; j <= i; ++j) {
+        float a = 0.f;
+        for (int k = 0; k < K; ++k) a = fmaf(sgq[k * C + i], sgk[k * C + j], a);
+        den += a;
+        const float *vr = sv + j * D_V;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(a, vr[c], acc[c]);
+    }
+    den += eps;
+    const float r = 1.0f / den;
+    const float *go = dO + ((size_t)bh * N + t0 + i) * D_V;
+    float *out = dn + ((size_t)bh * N + t0 + i) * W;
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) {
+        const float d = go[c];
+        dot = fmaf(d, acc[c] * r, dot);
+        acc[c] = d * r;  // dnum
+        out[c] = acc[c];
+    }
+    const float dden = -dot * r;
+    out[D_V] = dden;
+    float *bi = sb + i * (C + 1);
+    for (int j = 0; j <= i; ++j) {
+        const float *vr = sv + j * D_V;
+        float b = dden;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) b = fmaf(acc[c], vr[c], b);
+        bi[j] = b;
+    }
+    float *d = dsq + (size_t)bh * K * N + t0 + i;
+    float mean = 0.f;
+    for (int k = 0; k < K; ++k) {
+        const float *row = ss + k * W;
+        float u = dden * row[D_V];
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) u = fmaf(acc[c], row[c], u);
+        for (int j = 0; j <= i; ++j) u = fmaf(sgk[k * C + j], bi[j], u);
+        d[(size_t)k * N] = u;
+        mean = fmaf(sgq[k * C + i], u, mean);
+    }
+    for (int k = 0; k < K; ++k) d[(size_t)k * N] = sgq[k * C + i] * (d[(size_t)k * N] - mean);
+}
+
+// In-place exclusive suffix over the chunk aggregates of each head, in reverse
+// chunk order: part[c] <- sum_{c' > c} part[c'].
+__global__ void bwd_suffix_scan_kernel(float *__restrict__ part, int nchunk, int E, const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float *p = part + (size_t)bh * nchunk * E + e;
+    float run = 0.f;
+    for (int c = nchunk - 1; c >= 0; --c) {
+        const float cur = p[(size_t)c * E];
+        p[(size_t)c * E] = run;
+        run += cur;
+    }
+}
+
+// Causal key rows, one block per chunk, one thread per key row j: with (D, E)
+// the suffix over the later chunks (suf) plus the intra-chunk queries i >= j,
+//   u_jk = V_j . D_k + E_k,   ds^K_jk = gK_jk (u_jk - sum_l gK_jl u_jl),
+//   dV_j = sum_k gK_jk D_k = gK_j . suf + sum_{i>=j} <gK_j, gQ_i> dnum_i.
+template <int D_V, typename T>
+__global__ void __launch_bounds__(kSimtCausalChunk) bwd_causal_key_kernel(
+    const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
+    const float *__restrict__ dn, const float *__restrict__ suf, int N, int K, int nchunk,
+    float *__restrict__ dsk, float *__restrict__ dV, const unsigned *status) {
+    if (failed(status)) return;
+    constexpr int C = kSimtCausalChunk;
+    constexpr int W = D_V + 1;
+    extern __shared__ float smem[];
+    float *sgq = smem;              // [K][C]
+    float *sgk = sgq + K * C;       // [K][C]
+    float *sdn = sgk + K * C;       // [C][W]: dnum | dden of the chunk's queries
+    float *ss = sdn + C * W;        // [K][W]: suffix over the later chunks
+    float *sb = ss + K * W;         // [C][C + 1]: b_ji of key row j
+    const int chunk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = chunk * C;
+    const int n = min(C, N - t0);
+    const float *gq = gqt + (size_t)bh * K * N, *gk = gkt + (size_t)bh * K * N;
+    for (int e = threadIdx.x; e < K * C; e += blockDim.x) {
+        const int k = e / C, t = e % C;
+        sgq[e] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
+        sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
+    }
+    const float *dnc = dn + ((size_t)bh * N + t0) * W;
+    for (int e = threadIdx.x; e < C * W; e += blockDim.x) sdn[e] = e < n * W ? dnc[e] : 0.f;
+    const float *sp = suf + ((size_t)bh * nchunk + chunk) * K * W;
+    for (int e = threadIdx.x; e < K * W; e += blockDim.x) ss[e] = sp[e];
+    __syncthreads();
+    const int j = threadIdx.x;
+    if (j >= n) return;
+    float *bj = sb + j * (C + 1);
+    float *d = dsk + (size_t)bh * K * N + t0 + j;
+    {
+        float v[D_V];
+        const T *vr = V + ((size_t)bh * N + t0 + j) * D_V;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) v[c] = to_f32(vr[c]);
+        for (int i = j; i < n; ++i) {
+            const float *dr = sdn + i * W;
+            float b = dr[D_V];
+#pragma unroll
+            for (int c = 0; c < D_V; ++c) b = fmaf(v[c], dr[c], b);
+            bj[i] = b;
+        }
+        float mean = 0.f;
+        for (int k = 0; k < K; ++k) {
+            const float *row = ss + k * W;
+            float u = row[D_V];
+#pragma unroll
+            for (int c = 0; c < D_V; ++c) u = fmaf(v[c], row[c], u);
+            for (int i = j; i < n; ++i) u = fmaf(sgq[k * C + i], bj[i], u);
+            d[(size_t)k * N] = u;
+            mean = fmaf(sgk[k * C + j], u, mean);
+        }
+        for (int k = 0; k < K; ++k) d[(size_t)k * N] = sgk[k * C + j] * (d[(size_t)k * N] - mean);
+    }
+    float acc[D_V];
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    for (int k = 0; k < K; ++k) {
+        const float g = sgk[k * C + j];
+        const float *row = ss + k * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(g, row[c], acc[c]);
+    }
+    for (int i = j; i < n; ++i) {
+        float w = 0.f;
+        for (int k = 0; k < K; ++k) w = fmaf(sgk[k * C + j], sgq[k * C + i], w);
+        const float *dr = sdn + i * W;
+#pragma unroll
+        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(w, dr[c], acc[c]);
+    }
+    float *o = dV + ((size_t)bh * N + t0 + j) * D_V;
+#pragma unroll
+    for (int c = 0; c < D_V; ++c) o[c] = acc[c];
+}
+
 struct BwdLayout {
     SimtLayout F;     // the forward's regions (status, 1/sigma2, c', Gamma^Q, Gamma^K, partials, memory)
     size_t dn = 0;    // [BH][N][d_v + 1]
     size_t dsq = 0, dsk = 0;  // [BH][K][N]
-    size_t dpart = 0; // [BH][nsplit][K][d_v + 1]
-    size_t dmem = 0;  // [BH][K][d_v + 1]
-    size_t st = 0;    // [BH][2][nsplit][K][1 + 2 d_r]
+    size_t dpart = 0; // [BH][nsplit][K][d_v + 1] (causal: per chunk, then the suffixes)
+    size_t dmem = 0;  // [BH][K][d_v + 1] (bidirectional)
+    size_t st = 0;    // [BH][2][sn][K][1 + 2 d_r]
+    int sn = 0, srows = 0;  // row splits of the parameter statistics
     size_t total = 0;
 };
 
-BwdLayout bwd_layout(const Problem &p, int splits) {
+BwdLayout bwd_layout(const Problem &p, int causal, int splits) {
     BwdLayout L;
-    L.F = simt_layout(p, 0, splits);
+    L.F = simt_layout(p, causal, causal ? 0 : splits);
+    if (causal) {
+        L.srows = 1024;
+        L.sn = (p.N + L.srows - 1) / L.srows;
+    } else {
+        L.srows = L.F.tokens_per_split;
+        L.sn = L.F.nsplit;
+    }
     size_t off = L.F.total;
     const size_t W = (size_t)p.d_v + 1, BH = p.BH();
     L.dn = off; off = align256(off + sizeof(float) * BH * p.N * W);
     L.dsq = off; off = align256(off + sizeof(float) * BH * p.K * p.N);
     L.dsk = off; off = align256(off + sizeof(float) * BH * p.K * p.N);
     L.dpart = off; off = align256(off + sizeof(float) * BH * L.F.nsplit * p.K * W);
-    L.dmem = off; off = align256(off + sizeof(float) * BH * p.K * W);
-    L.st = off; off = align256(off + sizeof(float) * BH * 2 * L.F.nsplit * p.K * (1 + 2 * (size_t)p.d_r));
+    if (!causal) { L.dmem = off; off = align256(off + sizeof(float) * BH * p.K * W); }
+    L.st = off; off = align256(off + sizeof(float) * BH * 2 * L.sn * p.K * (1 + 2 * (size_t)p.d_r));
     L.total = off;
     return L;
 }
@@ -467,29 +671,97 @@ cudaError_t launch_inputs(const Problem &p, const BwdLayout &L, const BackwardAr
     bwd_dx_kernel<T><<<gx, 128, 0, s>>>(Kx, dsk, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dK, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    const dim3 gs(L.F.nsplit, p.BH(), (p.d_r + 31) / 32);  // z: 32-column block of d_r
-    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Q, dsq, p.mu, p.H, p.N, p.K, p.d_r, L.F.tokens_per_split,
-                                                L.F.nsplit, 0, st, status);
+    const dim3 gs(L.sn, p.BH(), (p.d_r + 31) / 32);  // z: 32-column block of d_r
+    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Q, dsq, p.mu, p.H, p.N, p.K, p.d_r, L.srows, L.sn, 0, st,
+                                                status);
     GMA_TRY(cudaGetLastError());
-    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Kx, dsk, p.mu, p.H, p.N, p.K, p.d_r, L.F.tokens_per_split,
-                                                L.F.nsplit, 1, st, status);
+    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Kx, dsk, p.mu, p.H, p.N, p.K, p.d_r, L.srows, L.sn, 1, st,
+                                                status);
     GMA_TRY(cudaGetLastError());
     bwd_param_final_kernel<<<dim3((p.K * p.d_r + 127) / 128, p.H), 128, 0, s>>>(
-        st, inv, p.B, p.H, p.K, p.d_r, L.F.nsplit, g.dmu, g.dsigma2, g.dlog_pi, status);
+        st, inv, p.B, p.H, p.K, p.d_r, L.sn, g.dmu, g.dsigma2, g.dlog_pi, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     return cudaSuccess;
 }
 
+template <int D_V, typename T>
+cudaError_t launch_causal_rows(const Problem &p, const BwdLayout &L, const BackwardArgs &g, char *b,
+                               cudaStream_t s, StageClock &clk) {
+    constexpr int C = kSimtCausalChunk, W = D_V + 1;
+    const unsigned *status = reinterpret_cast<const unsigned *>(b);
+    const float *gq = reinterpret_cast<const float *>(b + L.F.gq), *gk = reinterpret_cast<const float *>(b + L.F.gk);
+    const float *prefix = reinterpret_cast<const float *>(b + L.F.partial);
+    float *dn = reinterpret_cast<float *>(b + L.dn), *dsq = reinterpret_cast<float *>(b + L.dsq);
+    float *dsk = reinterpret_cast<float *>(b + L.dsk), *dpart = reinterpret_cast<float *>(b + L.dpart);
+    const T *V = static_cast<const T *>(p.V);
+    const int nchunk = L.F.nsplit;
+    const dim3 grid(nchunk, p.BH());
+    const size_t smq = sizeof(float) * ((size_t)2 * p.K * C + (size_t)C * D_V + (size_t)p.K * W + (size_t)C * (C + 1));
+    const size_t smk = sizeof(float) * ((size_t)2 * p.K * C + (size_t)C * W + (size_t)p.K * W + (size_t)C * (C + 1));
+    GMA_TRY(cudaFuncSetAttribute(bwd_causal_query_kernel<D_V, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smq));
+    bwd_causal_query_kernel<D_V, T><<<grid, C, smq, s>>>(gq, gk, V, prefix, g.dO, p.N, p.K, nchunk, p.eps, dn, dsq,
+                                                         status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    bwd_colsum_kernel<<<dim3(nchunk, p.BH(), (W + 63) / 64), 256, 0, s>>>(gq, dn, W, W, p.N, p.K, C, nchunk, dpart,
+                                                                         status);
+    GMA_TRY(cudaGetLastError());
+    bwd_suffix_scan_kernel<<<dim3((p.K * W + 255) / 256, p.BH()), 256, 0, s>>>(dpart, nchunk, p.K * W, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    GMA_TRY(cudaFuncSetAttribute(bwd_causal_key_kernel<D_V, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smk));
+    bwd_causal_key_kernel<D_V, T><<<grid, C, smk, s>>>(gq, gk, V, dn, dpart, p.N, p.K, nchunk, dsk, g.dV, status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t causal_rows(const Problem &p, const BwdLayout &L, const BackwardArgs &g, char *b, cudaStream_t s,
+                        StageClock &clk) {
+    switch (p.d_v) {
+        case 16: return launch_causal_rows<16, T>(p, L, g, b, s, clk);
+        case 32: return launch_causal_rows<32, T>(p, L, g, b, s, clk);
+        case 64: return launch_causal_rows<64, T>(p, L, g, b, s, clk);
+        case 128: return launch_causal_rows<128, T>(p, L, g, b, s, clk);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
-const char *const kBackwardStages[8] = {"state", "upstream", "ds_q", "dmem", "ds_k_dv", "dx", "params", nullptr};
+const char *const kBackwardStages[2][8] = {
+    {"state", "upstream", "ds_q", "dmem", "ds_k_dv", "dx", "params", nullptr},
+    {"state", "query", "suffix", "key", "dx", "params", nullptr},
+};
 
-size_t backward_workspace(const Problem &p, int splits) { return bwd_layout(p, splits).total; }
+size_t backward_workspace(const Problem &p, int causal, int splits) {
+    return bwd_layout(p, causal, splits).total;
+}
+
+cudaError_t simt_backward_causal(const Problem &p, const BackwardArgs &g, void *ws, cudaStream_t s,
+                                 StageClock &clk) {
+    const BwdLayout L = bwd_layout(p, 1, 0);
+    char *b = static_cast<char *>(ws);
+    clk.mark();
+    GMA_TRY(simt_causal_state(p, ws, s));
+    clk.mark();
+    if (p.dtype == GMA_F32) {
+        GMA_TRY(causal_rows<float>(p, L, g, b, s, clk));
+        GMA_TRY(launch_inputs<float>(p, L, g, b, s, clk));
+    } else {
+        GMA_TRY(causal_rows<__nv_bfloat16>(p, L, g, b, s, clk));
+        GMA_TRY(launch_inputs<__nv_bfloat16>(p, L, g, b, s, clk));
+    }
+    return cudaSuccess;
+}
 
 cudaError_t simt_backward_bidir(const Problem &p, const BackwardArgs &g, int splits, void *ws, cudaStream_t s,
                                 StageClock &clk) {
-    const BwdLayout L = bwd_layout(p, splits);
+    const BwdLayout L = bwd_layout(p, 0, splits);
     char *b = static_cast<char *>(ws);
     clk.mark();
     GMA_TRY(simt_bidir_state(p, splits, ws, s));

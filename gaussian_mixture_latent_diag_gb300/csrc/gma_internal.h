@@ -66,6 +66,10 @@ extern const char *const kSimtStages[3][8];  // [variant + 1][j], NULL-terminate
 // Gamma^Q, Gamma^K and the latent memory [Vt | Z] in the simt_layout(p, 0, splits)
 // regions of ws.
 cudaError_t simt_bidir_state(const Problem &p, int splits, void *ws, cudaStream_t s);
+// The causal SIMT forward before its output kernel: 1/sigma2, c', Gamma^Q, Gamma^K
+// and the exclusive prefix memory at the start of every chunk of kSimtCausalChunk
+// tokens (the `partial` region of simt_layout(p, 1, 0)).
+cudaError_t simt_causal_state(const Problem &p, void *ws, cudaStream_t s);
 
 // ---------------------------------------------------------------- backward (gma_backward.cu)
 struct BackwardArgs {
@@ -74,10 +78,12 @@ struct BackwardArgs {
     float *dmu = nullptr, *dsigma2 = nullptr;        // [H][K][d_r]
     float *dlog_pi = nullptr;                        // [H][K]
 };
-size_t backward_workspace(const Problem &p, int splits);
+size_t backward_workspace(const Problem &p, int causal, int splits);
 cudaError_t simt_backward_bidir(const Problem &p, const BackwardArgs &g, int splits, void *ws, cudaStream_t s,
                                 StageClock &clk);
-extern const char *const kBackwardStages[8];     // NULL-terminated
+cudaError_t simt_backward_causal(const Problem &p, const BackwardArgs &g, void *ws, cudaStream_t s,
+                                 StageClock &clk);
+extern const char *const kBackwardStages[2][8];  // [causal][j], NULL-terminated
 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);

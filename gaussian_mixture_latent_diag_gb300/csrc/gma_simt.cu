@@ -534,6 +534,19 @@ cudaError_t simt_bidir_state(const Problem &p, int splits, void *ws, cudaStream_
     return cudaGetLastError();
 }
 
+cudaError_t simt_causal_state(const Problem &p, void *ws, cudaStream_t s) {
+    SimtLayout L = simt_layout(p, 1, 0);
+    Ptrs P = ptrs(L, ws);
+    StageClock none;
+    none.stream = s;
+    GMA_TRY(prep(p, P, s));
+    GMA_TRY(resp_both(p, P, s, none));
+    GMA_TRY(write_parts(p, L, P, s));
+    const int E = p.K * (p.d_v + 1);
+    scan_chunks_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.status);
+    return cudaGetLastError();
+}
+
 cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &clk) {
     SimtLayout L = simt_layout(p, 1, 0);
     Ptrs P = ptrs(L, ws);

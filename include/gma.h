@@ -191,7 +191,7 @@ gma_status gma_forward_bidir_noalloc(const void *Q_X, const void *K_X, const voi
                                      const gma_options *options, void *stream);
 
 /*
- * Gradients of gma_forward_bidir ([GMA, gradient section]: the upstream
+ * Gradients of gma_forward_bidir / gma_forward_causal ([GMA, gradient section]: the upstream
  * gradient of a responsibility row, the softmax Jacobian (Eq. (17)) and the
  * gradient entering the score (Eq. (18)), then the chain rule through the
  * score into the routing rows and the mixture parameters).  Given
@@ -209,8 +209,13 @@ gma_status gma_forward_bidir_noalloc(const void *Q_X, const void *K_X, const voi
  * or the workspace (GMA_ERR_INVALID_ARG).  Device-side parameter errors and
  * the status word behave as for the forward.
  *
- * gma_backward_workspace_size: bytes of workspace for these sizes (causal must
- * be 0; 0 is returned for unsupported arguments).
+ * The causal variant differentiates Eq. (8b): the query side reads the
+ * prefix memories, and a key j collects the suffix sums over the queries
+ * i >= j; it runs in chunks of 64 tokens (options->splits is ignored).
+ *
+ * gma_backward_workspace_size: bytes of workspace for these sizes (causal 0
+ * for gma_backward_bidir, 1 for gma_backward_causal; 0 is returned for
+ * unsupported arguments).
  */
 size_t gma_backward_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
                                    int causal, const gma_options *options);
@@ -220,12 +225,19 @@ gma_status gma_backward_bidir(const void *Q_X, const void *K_X, const void *V_X,
                               float *dsigma2, float *dlog_pi, int B, int H, int N, int d_r, int d_v,
                               int K, const gma_options *options, void *workspace,
                               size_t workspace_bytes, void *stream);
+gma_status gma_backward_causal(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
+                               const float *mu, const float *sigma2, const float *log_pi, float eps,
+                               const float *dO, float *dQ_X, float *dK_X, float *dV_X, float *dmu,
+                               float *dsigma2, float *dlog_pi, int B, int H, int N, int d_r, int d_v,
+                               int K, const gma_options *options, void *workspace,
+                               size_t workspace_bytes, void *stream);
 
 /*
  * Number of stages (kernel launches, plus the status reset of the first) of
  * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
  * `variant` (-1 responsibilities, 0 bidirectional, 1 causal, 2 bidirectional
- * backward -- SIMT only), and the name of stage j (NULL if out of range).
+ * backward, 3 causal backward -- the last two SIMT only), and the name of
+ * stage j (NULL if out of range).
  * Used with gma_options.stage_events.
  */
 int gma_stage_count(int path, int variant);

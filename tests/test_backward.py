@@ -1,8 +1,11 @@
-"""Parity of the CUDA backward (gma_backward_bidir) with the fp64 oracle.
+"""Parity of the CUDA backward (gma_backward_bidir / gma_backward_causal) with
+the fp64 oracle.
 
 The gradients are those of "Gaussian Mixture Attention: Linear-Time Sequence
 Mixing via Probabilistic Latent Routing", gradient section (Eq. (18) and the
-chain rule through the score), for the bidirectional forward of Eqs. (5)-(7).
+chain rule through the score), for the bidirectional forward of Eqs. (5)-(7)
+and the causal forward of Eq. (8b) (prefix memories for the queries, suffix
+sums for the keys, in chunks of 64 tokens on the GPU).
 The kernels compute in fp32 from the same (bf16-rounded, for bf16 cases)
 inputs the oracle widens to fp64.  Metric per output tensor:
 max |g - g_ref| / RMS(g_ref), bound 1e-3 for every gradient.  The bound comes
@@ -33,14 +36,18 @@ def _inputs(B, H, N, d_r, d_v, K, dtype, seed):
     return d, dO
 
 
-def _run(B, H, N, d_r, d_v, K, dtype, seed=0, splits=0):
+def _run(B, H, N, d_r, d_v, K, dtype, seed=0, splits=0, causal=False):
     import gaussian_mixture_latent_diag_gb300 as gma
     d, dO = _inputs(B, H, N, d_r, d_v, K, dtype, seed)
     dev = torch.device("cuda")
     dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-    got = gma.backward_bidir(dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev),
-                             eps=d["eps"], splits=splits, sync_status=True)
-    ref = oracle.backward_bidir(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], d["eps"], dO)
+    args = (dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev))
+    if causal:
+        got = gma.backward_causal(*args, eps=d["eps"], sync_status=True)
+        ref = oracle.backward_causal(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], d["eps"], dO)
+    else:
+        got = gma.backward_bidir(*args, eps=d["eps"], splits=splits, sync_status=True)
+        ref = oracle.backward_bidir(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], d["eps"], dO)
     errs = {}
     for k, r in ref.items():
         gk = got[k].double().cpu().numpy()
@@ -67,6 +74,44 @@ def test_backward_matches_oracle(case):
         if case[5] == 1 and k in ("dQ", "dK", "dmu", "dsigma2", "dlog_pi"):
             continue  # K = 1: these are exactly zero in the oracle (checked below)
         assert e <= TOL[k], f"{k}: {e:.3e} > {TOL[k]}"
+
+
+CAUSAL_CASES = [
+    # B, H, N, d_r, d_v, K, dtype
+    (1, 2, 300, 16, 32, 8, "f32"),
+    (2, 2, 257, 64, 64, 64, "bf16"),
+    (1, 1, 63, 32, 16, 5, "f32"),
+    (1, 1, 129, 128, 128, 128, "f32"),
+    (1, 2, 1000, 64, 64, 64, "bf16"),
+    (1, 2, 200, 16, 16, 1, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL_CASES, ids=lambda c: "B%dH%dN%d_dr%d_dv%d_K%d_%s" % c)
+def test_causal_backward_matches_oracle(case):
+    errs = _run(*case, causal=True)
+    for k, e in errs.items():
+        if case[5] == 1 and k in ("dQ", "dK", "dmu", "dsigma2", "dlog_pi"):
+            continue  # K = 1: exactly zero in the oracle
+        assert e <= TOL[k], f"{k}: {e:.3e} > {TOL[k]}"
+
+
+def test_causal_backward_bench_dimensions():
+    errs = _run(1, 2, 4096, 64, 64, 64, "bf16", seed=13, causal=True)
+    for k, e in errs.items():
+        assert e <= TOL[k], f"{k}: {e:.3e}"
+
+
+def test_causal_backward_is_deterministic():
+    import gaussian_mixture_latent_diag_gb300 as gma
+    d, dO = _inputs(1, 2, 333, 32, 32, 16, "bf16", 9)
+    dev = torch.device("cuda")
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    args = (dd["Q"], dd["K"], dd["V"], dd["mu"], dd["sigma2"], dd["log_pi"], dO.to(dev))
+    a = gma.backward_causal(*args, eps=d["eps"], sync_status=True)
+    b = gma.backward_causal(*args, eps=d["eps"], sync_status=True)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
 
 
 def test_backward_k1_routing_gradients_vanish():
@@ -115,7 +160,8 @@ def test_backward_rejects_bad_arguments():
     opt = _native.options(path=_native.PATH_TC)
     assert lib.gma_backward_workspace_size(1, 1, 128, 64, 64, 64, 1, 0, ctypes.byref(opt)) == 0
     opt = _native.options()
-    assert lib.gma_backward_workspace_size(1, 1, 128, 64, 64, 64, 1, 1, ctypes.byref(opt)) == 0
+    assert lib.gma_backward_workspace_size(1, 1, 128, 64, 64, 64, 1, 2, ctypes.byref(opt)) == 0
+    assert lib.gma_backward_workspace_size(1, 1, 128, 64, 64, 64, 1, 1, ctypes.byref(opt)) > 0
     assert lib.gma_backward_workspace_size(1, 1, 128, 48, 64, 64, 1, 0, ctypes.byref(opt)) == 0
     d, dO = _inputs(1, 1, 128, 16, 16, 4, "f32", 1)
     dev = torch.device("cuda")
