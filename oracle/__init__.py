@@ -17,6 +17,10 @@ Linear-Time Sequence Mixing via Probabilistic Latent Routing" (arXiv
 * ``bidir_rows`` / ``causal_rows``   -- the same definitions on selected rows
 * ``backward_bidir`` / ``backward_causal`` -- gradients: gradient section,
   Eq. (18) (score gradient) and the chain rule through the score
+* ``latent_memory``                  -- Eqs. (5)-(6): Vt, Z of a key/value sequence
+* ``decode_step`` / ``decode``        -- Eq. (8b) one position at a time (carried Vt, Z)
+* ``routing_stats``                  -- component usage, hard assignments, usage entropy
+  (the introduction's usage / hard-assignment diagnostics)
 
 Parity pins: see ``tests/test_oracle.py`` (closed forms, invariants, brute
 force, scipy / scikit-learn textbook routines, hand-derived golden values)
@@ -87,6 +91,17 @@ def _load(mutant: int = 0):
                                                 _D, ctypes.c_int, _D]
             lib.gma_oracle_bidir_backward.argtypes = common + [_D] * 7
             lib.gma_oracle_causal_backward.argtypes = common + [_D] * 7
+            lib.gma_oracle_latent_memory.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, _D, _D, _D, ctypes.c_int,
+                                                     _D, _D]
+            lib.gma_oracle_latent_memory.restype = None
+            lib.gma_oracle_decode_step.argtypes = [_D, _D, _D, ctypes.c_int, ctypes.c_int, _D,
+                                                   _D, _D, ctypes.c_int, ctypes.c_double, _D,
+                                                   _D, _D]
+            lib.gma_oracle_decode_step.restype = None
+            lib.gma_oracle_routing_stats.argtypes = [_D, ctypes.c_int, ctypes.c_int, _D, _D, _D,
+                                                     ctypes.c_int, _D, _L, _L, _D]
+            lib.gma_oracle_routing_stats.restype = None
             _libs[mutant] = lib
     return lib
 
@@ -270,6 +285,93 @@ def bidir_rows(q, k, v, mu_h, s2_h, lp_h, eps, rows) -> np.ndarray:
 def causal_rows(q, k, v, mu_h, s2_h, lp_h, eps, rows) -> np.ndarray:
     """Causal O rows of one head; ``rows`` sorted ascending."""
     return _rows("gma_oracle_causal_rows", q, k, v, mu_h, s2_h, lp_h, eps, rows)
+
+
+def latent_memory(K_, V, mu, sigma2, log_pi):
+    """Latent memory ([GMA, Eqs. 5-6]) of K_X [B, H, N, d_r], V_X [B, H, N, d_v]:
+    returns (Vt [B, H, K, d_v], Z [B, H, K]).  Also the causal carried state
+    after the last position."""
+    lib = _load(_ACTIVE[0])
+    K_, V = _f64(K_), _f64(V)
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H, K = mu.shape[0], mu.shape[1]
+    N, d_r = K_.shape[-2:]
+    d_v = V.shape[-1]
+    Kh, Vh = _heads(K_, 2), _heads(V, 2)
+    Vt = np.empty((Kh.shape[0], K, d_v))
+    Z = np.empty((Kh.shape[0], K))
+    for b in range(Kh.shape[0]):
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        k, v = np.ascontiguousarray(Kh[b]), np.ascontiguousarray(Vh[b])
+        lib.gma_oracle_latent_memory(_p(k), _p(v), N, d_r, d_v, _p(m), _p(s), _p(lp), K,
+                                     _p(Vt[b]), _p(Z[b]))
+    lead = K_.shape[:-2]
+    return Vt.reshape(lead + (K, d_v)), Z.reshape(lead + (K,))
+
+
+def decode_step(q, k, v, mu, sigma2, log_pi, eps, Vt, Z):
+    """One causal position ([GMA, Eq. 8b]) for every (b, h): q, k [B, H, d_r],
+    v [B, H, d_v], carried Vt [B, H, K, d_v], Z [B, H, K].  Returns
+    (o [B, H, d_v], Vt', Z'); the inputs are not modified."""
+    lib = _load(_ACTIVE[0])
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Vt, Z = _f64(Vt).copy(), _f64(Z).copy()
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H, K = mu.shape[0], mu.shape[1]
+    d_r, d_v = q.shape[-1], v.shape[-1]
+    qh, kh, vh = q.reshape(-1, d_r), k.reshape(-1, d_r), v.reshape(-1, d_v)
+    Vth, Zh = Vt.reshape(-1, K, d_v), Z.reshape(-1, K)
+    o = np.empty((qh.shape[0], d_v))
+    for b in range(qh.shape[0]):
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        qb, kb, vb = (np.ascontiguousarray(t[b]) for t in (qh, kh, vh))
+        vt_b, z_b = np.ascontiguousarray(Vth[b]), np.ascontiguousarray(Zh[b])
+        lib.gma_oracle_decode_step(_p(qb), _p(kb), _p(vb), d_r, d_v, _p(m), _p(s), _p(lp), K,
+                                   float(eps), _p(vt_b), _p(z_b), _p(o[b]))
+        Vth[b], Zh[b] = vt_b, z_b
+    return o.reshape(v.shape), Vth.reshape(Vt.shape), Zh.reshape(Z.shape)
+
+
+def decode(Q, K_, V, mu, sigma2, log_pi, eps, Vt=None, Z=None):
+    """Run decode_step over the positions of Q, K_X, V_X [B, H, T, d] in order,
+    starting from (Vt, Z) (zeros if None).  Returns (O [B, H, T, d_v], Vt, Z)."""
+    Q, K_, V = _f64(Q), _f64(K_), _f64(V)
+    K = _params(mu, sigma2, log_pi)[0].shape[1]
+    lead, T, d_v = Q.shape[:-2], Q.shape[-2], V.shape[-1]
+    Vt = np.zeros(lead + (K, d_v)) if Vt is None else _f64(Vt)
+    Z = np.zeros(lead + (K,)) if Z is None else _f64(Z)
+    O = np.empty(lead + (T, d_v))
+    for t in range(T):
+        O[..., t, :], Vt, Z = decode_step(Q[..., t, :], K_[..., t, :], V[..., t, :], mu, sigma2,
+                                          log_pi, eps, Vt, Z)
+    return O, Vt, Z
+
+
+def routing_stats(X, mu, sigma2, log_pi) -> dict:
+    """Component-usage diagnostics of X [B, H, N, d_r] per (b, h): usage
+    [B, H, K] (sum of responsibilities), counts [B, H, K] and z [B, H, N] (hard
+    assignments, smallest k on ties), entropy / entropy_norm / used [B, H]."""
+    lib = _load(_ACTIVE[0])
+    X = _f64(X)
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H, K = mu.shape[0], mu.shape[1]
+    N, d_r = X.shape[-2:]
+    Xh = _heads(X, 2)
+    nb = Xh.shape[0]
+    usage = np.empty((nb, K))
+    counts = np.empty((nb, K), np.int64)
+    z = np.empty((nb, N), np.int64)
+    st = np.empty((nb, 3))
+    for b in range(nb):
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        xb = np.ascontiguousarray(Xh[b])
+        u_b, c_b, z_b, s_b = usage[b], counts[b], z[b], st[b]
+        lib.gma_oracle_routing_stats(_p(xb), N, d_r, _p(m), _p(s), _p(lp), K, _p(u_b),
+                                     c_b.ctypes.data_as(_L), z_b.ctypes.data_as(_L), _p(s_b))
+    lead = X.shape[:-2]
+    return {"usage": usage.reshape(lead + (K,)), "counts": counts.reshape(lead + (K,)),
+            "z": z.reshape(lead + (N,)), "entropy": st[:, 0].reshape(lead),
+            "entropy_norm": st[:, 1].reshape(lead), "used": st[:, 2].astype(np.int64).reshape(lead)}
 
 
 class use_mutant:

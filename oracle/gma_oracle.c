@@ -34,6 +34,8 @@
  *   6: prior enters with the wrong sign
  *   7: backward: the gradient entering the score is not mean-centred (Eq. 18)
  *   8: backward: the causal key gradient uses prefix (j <= i) instead of suffix sums
+ *   9: decode step reads the memory before the new key enters it (exclusive)
+ *  10: marginal usage counts hard assignments instead of summing responsibilities
  */
 #ifndef GMA_ORACLE_MUTANT
 #define GMA_ORACLE_MUTANT 0
@@ -531,4 +533,115 @@ void gma_oracle_causal_backward(const double *Q, const double *Kx, const double 
     score_backward(Kx, GK, UK, N, d_r, mu, sigma2, K, dK, dmu, dsigma2, dlog_pi);
     free(GQ); free(GK); free(UQ); free(UK); free(DN); free(DD);
     free(Vt); free(Z); free(D); free(E);
+}
+
+/*
+ * Latent memory of a key/value sequence ([GMA, Eqs. 5-6], latent aggregation):
+ *   Vt_k = sum_j gK_jk V_j,   Z_k = sum_j gK_jk.
+ * This is also the causal carried state after the last position ([GMA, causal
+ * variant]: the prefix memories at i = N - 1), i.e. what a decoder holds after
+ * reading a prompt of N tokens.  Vt [K, d_v], Z [K] are overwritten.
+ */
+void gma_oracle_latent_memory(const double *Kx, const double *V, int N, int d_r, int d_v,
+                              const double *mu, const double *sigma2, const double *log_pi,
+                              int K, double *Vt, double *Z)
+{
+    double *gk = malloc(sizeof(double) * (size_t)K);
+    for (int k = 0; k < K; ++k) {
+        Z[k] = 0.0;
+        for (int c = 0; c < d_v; ++c) Vt[(size_t)k * d_v + c] = 0.0;
+    }
+    for (int j = 0; j < N; ++j) {
+        gma_oracle_responsibilities(Kx + (size_t)j * d_r, 1, d_r, mu, sigma2, log_pi, K, gk);
+        for (int k = 0; k < K; ++k) {
+            Z[k] += gk[k];
+            for (int c = 0; c < d_v; ++c) Vt[(size_t)k * d_v + c] += gk[k] * V[(size_t)j * d_v + c];
+        }
+    }
+    free(gk);
+}
+
+/*
+ * One autoregressive step of the causal variant ([GMA, causal variant, Eq. 8b]
+ * with the prefix memories carried as running sums).  Given the memory of the
+ * positions before i (Vt, Z) and the new position's query q, key k and value v:
+ *   Vt_k += gK_k v,  Z_k += gK_k          (position i enters its own prefix: j <= i)
+ *   o = (sum_k gQ_k Vt_k) / (sum_k gQ_k Z_k + eps)
+ * Vt [K, d_v] and Z [K] are updated in place; o [d_v] is written.
+ */
+void gma_oracle_decode_step(const double *q, const double *kx, const double *v, int d_r, int d_v,
+                            const double *mu, const double *sigma2, const double *log_pi, int K,
+                            double eps, double *Vt, double *Z, double *o)
+{
+    double *gk = malloc(sizeof(double) * (size_t)K);
+    double *gq = malloc(sizeof(double) * (size_t)K);
+    gma_oracle_responsibilities(kx, 1, d_r, mu, sigma2, log_pi, K, gk);
+    gma_oracle_responsibilities(q, 1, d_r, mu, sigma2, log_pi, K, gq);
+#if GMA_ORACLE_MUTANT != 9
+    for (int k = 0; k < K; ++k) {
+        Z[k] += gk[k];
+        for (int c = 0; c < d_v; ++c) Vt[(size_t)k * d_v + c] += gk[k] * v[c];
+    }
+#endif
+    double den = eps;
+    for (int k = 0; k < K; ++k) den += gq[k] * Z[k];
+    for (int c = 0; c < d_v; ++c) {
+        double num = 0.0;
+        for (int k = 0; k < K; ++k) num += gq[k] * Vt[(size_t)k * d_v + c];
+        o[c] = num / den;
+    }
+#if GMA_ORACLE_MUTANT == 9
+    for (int k = 0; k < K; ++k) {
+        Z[k] += gk[k];
+        for (int c = 0; c < d_v; ++c) Vt[(size_t)k * d_v + c] += gk[k] * v[c];
+    }
+#endif
+    free(gk); free(gq);
+}
+
+/*
+ * Component-usage diagnostics of one head's responsibilities ([GMA,
+ * introduction: the marginal usage of the mixture components shows whether
+ * the routing space is used broadly or collapses onto a few components, and
+ * the hard assignment z_i = argmax_k gamma_ik can be compared with token
+ * categories]; the interpretability results quote the number of components
+ * used and a usage entropy).
+ *   usage_k  = sum_i gamma_ik                       (soft, marginal usage)
+ *   z_i      = argmax_k gamma_ik, the smallest such k on ties (hard assignment)
+ *   counts_k = #{i : z_i = k}
+ *   p_k      = usage_k / N,  H = -sum_{k: p_k > 0} p_k log p_k  (nats)
+ *   H_norm   = H / log K  (K >= 2), 1 for K = 1 (one component is trivially uniform)
+ *   used     = #{k : counts_k > 0}
+ * z may be NULL.  stats[0] = H, stats[1] = H_norm, stats[2] = used.
+ */
+void gma_oracle_routing_stats(const double *X, int N, int d_r, const double *mu,
+                              const double *sigma2, const double *log_pi, int K,
+                              double *usage, long *counts, long *z, double *stats)
+{
+    double *g = malloc(sizeof(double) * (size_t)K);
+    for (int k = 0; k < K; ++k) { usage[k] = 0.0; counts[k] = 0; }
+    for (int i = 0; i < N; ++i) {
+        gma_oracle_responsibilities(X + (size_t)i * d_r, 1, d_r, mu, sigma2, log_pi, K, g);
+        int best = 0;
+        for (int k = 1; k < K; ++k)
+            if (g[k] > g[best]) best = k;
+        counts[best] += 1;
+        if (z) z[i] = best;
+#if GMA_ORACLE_MUTANT == 10
+        usage[best] += 1.0;
+#else
+        for (int k = 0; k < K; ++k) usage[k] += g[k];
+#endif
+    }
+    double H = 0.0;
+    long used = 0;
+    for (int k = 0; k < K; ++k) {
+        double p = usage[k] / (double)N;
+        if (p > 0.0) H -= p * log(p);
+        if (counts[k] > 0) used += 1;
+    }
+    stats[0] = H;
+    stats[1] = K >= 2 ? H / log((double)K) : 1.0;
+    stats[2] = (double)used;
+    free(g);
 }

@@ -276,4 +276,153 @@ def pin_batched_heads_use_their_own_parameters():
             assert np.max(np.abs(O[b, h] - Oh)) == 0.0
 
 
+# ---------------------------------------------------------------- decode step and latent memory
+
+def _rel(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+def pin_decode_equals_masked_affinity():
+    """Position-by-position decoding from an empty memory reproduces the
+    causal output computed through the materialised, masked affinity
+    ([GMA, causal variant, Eq. 8b]: each step adds its own key, then reads)."""
+    rng = _rng(21)
+    for (N, d_r, d_v, K) in [(23, 3, 4, 5), (9, 16, 2, 1), (12, 2, 3, 8)]:
+        Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+        O, _, _ = oracle.decode(Q[None, None], Kx[None, None], V[None, None], mu, s2, lp, 1e-6)
+        ref = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, 1e-6, causal=True)
+        assert _rel(O[0, 0], ref) < 1e-12
+
+
+def pin_decode_single_component_running_mean():
+    """K = 1: every gamma is 1, so o_t = sum_{j<=t} V_j / (t + 1 + eps)."""
+    rng = _rng(22)
+    N, d_r, d_v, eps = 15, 4, 3, 1e-3
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, 1)
+    O, Vt, Z = oracle.decode(Q[None], Kx[None], V[None], mu, s2, lp, eps)
+    t = np.arange(N)[:, None]
+    assert np.max(np.abs(O[0] - np.cumsum(V, 0) / (t + 1 + eps))) < 1e-12
+    assert abs(Z[0, 0] - N) < 1e-12 and np.max(np.abs(Vt[0, 0] - V.sum(0))) < 1e-12
+
+
+def pin_latent_memory_mass_and_prior():
+    """Rows of Gamma^K sum to one, so sum_k Z_k = N and sum_k Vt_k = sum_j V_j;
+    with identical components gamma = pi, so Vt_k = pi_k sum_j V_j, Z_k = N pi_k."""
+    rng = _rng(23)
+    N, d_r, d_v, K = 31, 5, 3, 6
+    _, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    Vt, Z = oracle.latent_memory(Kx, V, mu, s2, lp)
+    assert abs(Z.sum() - N) < 1e-11
+    assert np.max(np.abs(Vt.sum(0) - V.sum(0))) < 1e-11
+    mu_same = np.tile(mu[:1], (K, 1)); s2_same = np.tile(s2[:1], (K, 1))
+    pi = rng.dirichlet(np.ones(K))
+    Vt, Z = oracle.latent_memory(Kx, V, mu_same, s2_same, np.log(pi))
+    assert np.max(np.abs(Z - N * pi)) < 1e-11
+    assert np.max(np.abs(Vt - pi[:, None] * V.sum(0)[None])) < 1e-11
+
+
+def pin_latent_memory_read_gives_bidir_affinity():
+    """Reading the latent memory with the query responsibilities (Eq. 7)
+    equals the bidirectional output through the materialised affinity."""
+    rng = _rng(24)
+    N, d_r, d_v, K, eps = 27, 3, 4, 5, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    Vt, Z = oracle.latent_memory(Kx, V, mu, s2, lp)
+    GQ = oracle.responsibilities(Q, mu, s2, lp)
+    O = (GQ @ Vt) / (GQ @ Z + eps)[:, None]
+    ref = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=False)
+    assert _rel(O, ref) < 1e-12
+
+
+def pin_decode_continues_a_prompt():
+    """The memory of a prompt (latent memory of its keys) is the carried
+    state: decoding the rest from it gives the causal rows after the prompt,
+    and the final state is the latent memory of the whole sequence."""
+    rng = _rng(25)
+    N, N0, d_r, d_v, K, eps = 20, 13, 4, 3, 6, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    Vt0, Z0 = oracle.latent_memory(Kx[:N0], V[:N0], mu, s2, lp)
+    O, Vt, Z = oracle.decode(Q[None, N0:], Kx[None, N0:], V[None, N0:], mu, s2, lp, eps,
+                             Vt0[None], Z0[None])
+    ref = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=True)[N0:]
+    assert _rel(O[0], ref) < 1e-12
+    Vt_all, Z_all = oracle.latent_memory(Kx, V, mu, s2, lp)
+    assert np.max(np.abs(Vt[0] - Vt_all)) < 1e-11 and np.max(np.abs(Z[0] - Z_all)) < 1e-11
+
+
+# ---------------------------------------------------------------- component-usage diagnostics
+
+def pin_stats_totals():
+    """usage and counts each sum to N; used = number of non-empty counts;
+    the normalised entropy lies in [0, 1]."""
+    rng = _rng(26)
+    for (N, d_r, K) in [(40, 3, 7), (5, 2, 9)]:
+        X, _, _, mu, s2, lp = random_head(rng, N, d_r, 1, K)
+        st = oracle.routing_stats(X, mu, s2, lp)
+        assert abs(st["usage"].sum() - N) < 1e-11 and st["counts"].sum() == N
+        assert st["used"] == np.count_nonzero(st["counts"])
+        assert np.all(np.bincount(st["z"], minlength=K) == st["counts"])
+        assert -1e-12 <= st["entropy_norm"] <= 1 + 1e-12
+
+
+def pin_stats_match_sklearn_and_scipy():
+    """Hard assignments equal scikit-learn's GaussianMixture.predict and the
+    usage its predict_proba column sums (host only); the entropy equals
+    scipy.stats.entropy of the usage, and the normalised one that over log K."""
+    from scipy.stats import entropy
+    rng = _rng(27)
+    N, d_r, K = 60, 3, 6
+    X, _, _, mu, s2, lp = random_head(rng, N, d_r, 1, K)
+    pi = np.exp(lp); pi /= pi.sum()
+    st = oracle.routing_stats(X, mu, s2, np.log(pi))
+    H = entropy(st["usage"])
+    assert abs(st["entropy"] - H) < 1e-12
+    assert abs(st["entropy_norm"] - H / math.log(K)) < 1e-12
+    try:
+        from sklearn.mixture import GaussianMixture
+    except ImportError:  # the GPU box has no scikit-learn
+        return
+    gm = GaussianMixture(n_components=K, covariance_type="diag")
+    gm.weights_, gm.means_, gm.covariances_ = pi, mu, s2
+    gm.precisions_cholesky_ = 1.0 / np.sqrt(s2)
+    assert np.all(st["z"] == gm.predict(X))
+    assert np.max(np.abs(st["usage"] - gm.predict_proba(X).sum(0))) < 1e-10
+
+
+def pin_stats_identical_components():
+    """Identical components: gamma = pi on every row, so usage = N pi, every
+    row is assigned to the largest prior, and uniform priors give H_norm = 1."""
+    rng = _rng(28)
+    N, d_r, K = 17, 4, 5
+    X = rng.normal(size=(N, d_r))
+    mu = np.tile(rng.normal(size=(1, d_r)), (K, 1)); s2 = np.tile(rng.uniform(0.5, 2, (1, d_r)), (K, 1))
+    pi = rng.dirichlet(np.ones(K))
+    st = oracle.routing_stats(X, mu, s2, np.log(pi))
+    assert np.max(np.abs(st["usage"] - N * pi)) < 1e-11
+    assert np.all(st["z"] == np.argmax(pi)) and st["used"] == 1
+    st = oracle.routing_stats(X, mu, s2, np.full(K, -math.log(K)))
+    assert abs(st["entropy_norm"] - 1.0) < 1e-12 and np.all(st["z"] == 0)
+
+
+def pin_stats_rows_at_component_means():
+    """Equal variances and priors, well-separated means, x_i placed exactly on
+    the mean of component c_i: the hard assignment is c_i."""
+    rng = _rng(29)
+    N, d_r, K = 50, 3, 8
+    mu = rng.normal(scale=5.0, size=(K, d_r))
+    c = rng.integers(0, K, size=N)
+    st = oracle.routing_stats(mu[c], mu, np.ones((K, d_r)), np.full(K, -math.log(K)))
+    assert np.all(st["z"] == c)
+    assert np.all(st["counts"] == np.bincount(c, minlength=K))
+
+
+def pin_stats_single_component():
+    """K = 1: usage = counts = N, entropy 0, normalised entropy 1, one used."""
+    rng = _rng(30)
+    X, _, _, mu, s2, lp = random_head(rng, 11, 2, 1, 1)
+    st = oracle.routing_stats(X, mu, s2, lp)
+    assert abs(st["usage"][0] - 11) < 1e-12 and st["counts"][0] == 11
+    assert st["entropy"] == 0.0 and st["entropy_norm"] == 1.0 and st["used"] == 1
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -14,6 +14,8 @@ MUTANTS = {
     4: "eps in the numerator",
     5: "query/key responsibilities swapped",
     6: "prior with the wrong sign",
+    9: "decode step reads before its key enters the memory",
+    10: "usage counts hard assignments",
 }
 
 
