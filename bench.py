@@ -337,6 +337,196 @@ def run_backward(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------------ decode step and usage diagnostics
+
+DEC_WORKLOAD = dict(B=2048, H=8, d_r=64, d_v=64, K=64, dtype="bf16", eps=1e-6)
+DEC_METRIC = "GMA causal decode step token*heads/s (B=2048 x H=8, K=64); % of GB300 HBM roofline"
+STAT_WORKLOAD = dict(B=16, H=4, N=16384, d_r=32, K=32, dtype="bf16")
+STAT_METRIC = "GMA component-usage diagnostics token*heads/s (peaked routing, N=16K, K=32)"
+
+
+def _oracle_decode_sample(pairs: int):
+    """`pairs` (b, h) decode steps of the decode workload's shape through the fp64 oracle."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import oracle
+    w = DEC_WORKLOAD
+    rng = np.random.default_rng(3)
+    q, k = rng.standard_normal((pairs, 1, w["d_r"])), rng.standard_normal((pairs, 1, w["d_r"]))
+    v = rng.standard_normal((pairs, 1, w["d_v"]))
+    mu = rng.standard_normal((1, w["K"], w["d_r"]))
+    s2 = np.log1p(np.exp(rng.standard_normal((1, w["K"], w["d_r"])) * 0.5 ** 0.5)) + 1e-3
+    lp = np.log(np.full((1, w["K"]), 1.0 / w["K"]))
+    Vt, Z = rng.standard_normal((pairs, 1, w["K"], w["d_v"])), rng.random((pairs, 1, w["K"])) * 50
+    t = time.perf_counter()
+    oracle.decode_step(q, k, v, mu, s2, lp, w["eps"], Vt, Z)
+    return time.perf_counter() - t
+
+
+def _oracle_stats_head(seed: int):
+    """One head of the diagnostics workload through the fp64 oracle."""
+    sys.path.insert(0, ROOT)
+    import oracle
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+    w = STAT_WORKLOAD
+    inp = make_inputs(Case("stats", False, 1, 1, w["N"], w["d_r"], 16, w["K"], w["dtype"], routing="mixture",
+                           mu_std=3.0), seed=seed)
+    t = time.perf_counter()
+    oracle.routing_stats(inp["Q"], inp["mu"], inp["sigma2"], inp["log_pi"])
+    return time.perf_counter() - t
+
+
+def run_aux(args, rank: int, world: int, local_rank: int):
+    """--workload decode: one gma_decode_step over B=2048 x H=8 carried states
+    (K = d_v = 64, fp32 state of 272 MB, larger than L2) per step; algorithmic
+    bytes per (b, h): q, k, v (bf16) 384 + state read and written 2 * 4 * K * (d_v + 1)
+    + o (fp32) 256 = 33920 B.
+    --workload stats: one gma_routing_stats over the peaked-routing workload
+    (B=16, H=4, N=16384, d_r = K = 32, bf16, rows drawn from the mixture) per step,
+    hard assignments written; it runs on the CUDA cores and is bound by their
+    fp32 issue rate: 3 K d_r operations per row (difference, square, scaled
+    accumulate per component and dimension) against 152 SMs x 128 lanes x the
+    measured SM clock."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300 import _native
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    decode = args.workload == "decode"
+    if decode:
+        w = DEC_WORKLOAD
+        B, H, d_r, d_v, K = w["B"], w["H"], w["d_r"], w["d_v"], w["K"]
+        g = torch.Generator().manual_seed(rank_seed(rank, 4))
+        q, k, v = (torch.randn(B, H, d, generator=g).to(torch.bfloat16).to(dev) for d in (d_r, d_r, d_v))
+        mu = torch.randn(H, K, d_r, generator=g).to(dev)
+        s2 = (torch.nn.functional.softplus(torch.randn(H, K, d_r, generator=g) * 0.5 ** 0.5) + 1e-3).to(dev)
+        lp = torch.log_softmax(torch.randn(H, K, generator=g), -1).to(dev)
+        Vt = torch.randn(B, H, K, d_v, device=dev)
+        Z = torch.rand(B, H, K, device=dev) * 100
+        o = torch.empty(B, H, d_v, device=dev)
+        ws = torch.empty(int(gma.load().gma_decode_workspace_size(H, d_r, K)), dtype=torch.uint8, device=dev)
+        stages = _native.stage_names(_native.PATH_SIMT, 5)
+        units = B * H
+        alg = B * H * (3 * 2 * 64 + 2 * 4 * K * (d_v + 1) + 4 * d_v)
+        kernel_stage = "step"
+
+        def call(events=None):
+            gma.decode_step(q, k, v, mu, s2, lp, Vt, Z, eps=w["eps"], out=o, workspace=ws)
+    else:
+        w = STAT_WORKLOAD
+        B, H, N, d_r, K = w["B"], w["H"], w["N"], w["d_r"], w["K"]
+        inp = make_inputs(Case("stats", False, B, H, N, d_r, 16, K, w["dtype"], routing="mixture", mu_std=3.0),
+                          seed=rank_seed(rank, 5))
+        X, mu, s2, lp = (inp[n].to(dev) for n in ("Q", "mu", "sigma2", "log_pi"))
+        ws = torch.empty(int(gma.load().gma_routing_stats_workspace_size(B, H, N, d_r, K, _native.GMA_BF16)),
+                         dtype=torch.uint8, device=dev)
+        stages = _native.stage_names(_native.PATH_SIMT, 6)
+        units = B * H * N
+        kernel_stage = "rows"
+
+        def call(events=None):
+            gma.routing_stats(X, mu, s2, lp, want_z=True, workspace=ws)
+
+    def call_ev(events):
+        # the binding builds its options itself; stage events go through the C ABI call here
+        import ctypes
+        opt = _native.options(stage_events=events)
+        lib = gma.load()
+        vp = ctypes.c_void_p
+        if decode:
+            st = lib.gma_decode_step(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), _native.GMA_BF16,
+                                     vp(mu.data_ptr()), vp(s2.data_ptr()), vp(lp.data_ptr()), float(w["eps"]),
+                                     vp(Vt.data_ptr()), vp(Z.data_ptr()), vp(o.data_ptr()), B, H, d_r, d_v, K,
+                                     ctypes.byref(opt), vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream))
+        else:
+            st = lib.gma_routing_stats(vp(X.data_ptr()), _native.GMA_BF16, vp(mu.data_ptr()), vp(s2.data_ptr()),
+                                       vp(lp.data_ptr()), vp(usage.data_ptr()), vp(counts.data_ptr()),
+                                       vp(zbuf.data_ptr()), vp(ent.data_ptr()), B, H, N, d_r, K, ctypes.byref(opt),
+                                       vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream))
+        if st != 0:
+            raise gma.GmaError(st, "stage-event pass")
+
+    if not decode:
+        usage = torch.empty(B, H, K, device=dev)
+        counts = torch.empty(B, H, K, dtype=torch.int32, device=dev)
+        zbuf = torch.empty(B, H, N, dtype=torch.int32, device=dev)
+        ent = torch.empty(B, H, device=dev)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0.record(stream)
+        for _ in range(args.steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = job_ms(t0.elapsed_time(t1) / args.steps, world, dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        call_ev(ev[s])
+    torch.cuda.synchronize()
+    stage_ms = {name: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
+                for j, name in enumerate(stages)}
+    value = world * units / (ms / 1e3)
+    clk = clocks.summary()
+    kms = stage_ms[kernel_stage]
+    if decode:
+        peak, peak_src = measured_peaks()
+        achieved = alg / (kms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": f"decode:{kernel_stage}", "algorithmic_bytes": alg, "peak_source": peak_src}
+    else:
+        mhz = (clk or {}).get("sm_mhz") or 2070.0
+        peak = 152 * 128 * mhz * 1e6 / 1e12
+        ops = units * 3 * K * d_r
+        achieved = ops / (kms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Top/s", "frac": achieved / peak,
+                "traffic": None, "kernel": f"stats:{kernel_stage}", "algorithmic_ops": ops,
+                "peak_source": "152 SMs x 128 fp32 lanes x median SM clock under load"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        if decode:
+            pairs = 2048
+            secs = _oracle_decode_sample(pairs)
+            cpu = {"value": pairs / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{pairs} (b, h) decode steps of the workload's shape through the fp64 C oracle, "
+                             f"{secs:.2f} s on one core"}
+        else:
+            heads = 8
+            secs = sum(_oracle_stats_head(7 + i) for i in range(heads))
+            cpu = {"value": heads * STAT_WORKLOAD["N"] / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{heads} heads of the workload (N=16384, d_r=K=32, peaked) through the fp64 C "
+                             f"oracle, {secs:.2f} s on one core"}
+    if rank == 0:
+        if decode:
+            cfg = {"workload": "GMA causal decode step, B=2048 sequences x H=8 heads, d_r=d_v=K=64, bf16 q/k/v, "
+                               "fp32 carried state (per GPU)", **{k_: w[k_] for k_ in ("B", "H", "d_r", "d_v", "K")},
+                   "l2": "state (272 MB) larger than L2, no flush"}
+        else:
+            cfg = {"workload": "GMA component-usage diagnostics (usage, hard assignments, usage entropy), B=16 H=4 "
+                               "N=16384 d_r=K=32 bf16, peaked routing (per GPU)",
+                   **{k_: w[k_] for k_ in ("B", "H", "N", "d_r", "K")},
+                   "l2": "inputs (67 MB) smaller than L2, compute-bound: no flush"}
+        cfg["parallelism"] = f"replicas x{world}"
+        out = {"metric": DEC_METRIC if decode else STAT_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+               "gpu_launches": (2 if decode else 3) * args.steps, "roofline": roof, "stage_ms": stage_ms,
+               "clocks": clk, "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+
+
 def rank_seed(rank: int, variant: int) -> int:
     """Input seed of one variant on one rank: each rank draws its own heads (replicas
     of the workload shape, no data shared between ranks)."""
@@ -552,9 +742,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["forward", "backward"], default="forward",
+    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats"], default="forward",
                     help="forward: the bidirectional + causal forward step (default); "
-                         "backward: the bidirectional backward")
+                         "backward: the bidirectional + causal backward; decode: one causal decode "
+                         "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -570,6 +761,8 @@ def main():
     try:
         if args.workload == "backward":
             run_backward(args, rank, world, local_rank)
+        elif args.workload in ("decode", "stats"):
+            run_aux(args, rank, world, local_rank)
         else:
             run_gma(args, rank, world, local_rank)
     finally:

@@ -4,6 +4,9 @@
     O = gma.forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6)
     O = gma.forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6)
     G = gma.responsibilities(X, mu, sigma2, log_pi)
+    Vt, Z = gma.latent_memory(K, V, mu, sigma2, log_pi)          # prompt -> carried state
+    o = gma.decode_step(q, k, v, mu, sigma2, log_pi, Vt, Z)      # one position, state in place
+    st = gma.routing_stats(X, mu, sigma2, log_pi)                 # usage, hard assignments, entropy
 
 Tensors: Q, K, X [B, H, N, d_r], V [B, H, N, d_v] (CUDA, contiguous, fp32 or
 bf16); mu, sigma2 [H, K, d_r] and log_pi [H, K] fp32 CUDA.  The functions
@@ -21,7 +24,7 @@ from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError
                       options, status_string)
 
 __all__ = ["forward_bidir", "forward_causal", "backward_bidir", "backward_causal", "responsibilities",
-           "workspace_size",
+           "latent_memory", "decode_step", "routing_stats", "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
            "PATH_TC", "load"]
 
@@ -205,3 +208,103 @@ def _backward(fn_name, Q, K, V, mu, sigma2, log_pi, dO, eps, workspace, stream, 
     if st != 0:
         raise GmaError(st, fn_name)
     return out
+
+
+def _params_check(H, d_r, mu, sigma2, log_pi):
+    K = mu.shape[1]
+    if mu.shape != (H, K, d_r) or sigma2.shape != (H, K, d_r) or log_pi.shape != (H, K):
+        raise ValueError("mu, sigma2 must be [H, K, d_r] and log_pi [H, K]")
+    return K
+
+
+def latent_memory(K, V, mu, sigma2, log_pi, workspace=None, stream=None, splits=0, sync_status=False):
+    """Latent memory of a key/value sequence: (Vt [B, H, K, d_v], Z [B, H, K]) fp32,
+    Vt = Gamma^K^T V, Z = Gamma^K^T 1.  It is also the causal state after the last
+    position, i.e. what decode_step continues from after a prompt."""
+    import torch
+    lib = load()
+    _check_dev(K, V, mu, sigma2, log_pi)
+    B, H, N, d_r = K.shape
+    d_v = V.shape[-1]
+    if V.shape[:3] != K.shape[:3]:
+        raise ValueError("K must be [B, H, N, d_r] and V [B, H, N, d_v]")
+    Kc = _params_check(H, d_r, mu, sigma2, log_pi)
+    code = _dtype_code(K)
+    if V.dtype != K.dtype:
+        raise TypeError("K, V must share one dtype")
+    Vt = torch.empty(B, H, Kc, d_v, dtype=torch.float32, device=K.device)
+    Z = torch.empty(B, H, Kc, dtype=torch.float32, device=K.device)
+    opt = options(splits=splits, sync_status=sync_status)
+    nb = int(lib.gma_latent_memory_workspace_size(B, H, N, d_r, d_v, Kc, code, ctypes.byref(opt)))
+    if nb == 0:
+        raise GmaError(2, "gma_latent_memory")
+    ws = _workspace(nb, K.device, workspace)
+    st = lib.gma_latent_memory(_ptr(K), _ptr(V), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(Vt), _ptr(Z),
+                               B, H, N, d_r, d_v, Kc, ctypes.byref(opt), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_latent_memory")
+    return Vt, Z
+
+
+def decode_step(q, k, v, mu, sigma2, log_pi, Vt, Z, eps=1e-6, out=None, workspace=None, stream=None,
+                sync_status=False):
+    """One causal position for every (b, h): q, k [B, H, d_r], v [B, H, d_v]; the
+    carried state Vt [B, H, K, d_v], Z [B, H, K] (fp32) is updated in place.
+    Returns o [B, H, d_v] fp32."""
+    import torch
+    lib = load()
+    _check_dev(q, k, v, mu, sigma2, log_pi, Vt, Z)
+    B, H, d_r = q.shape
+    d_v = v.shape[-1]
+    Kc = _params_check(H, d_r, mu, sigma2, log_pi)
+    if k.shape != q.shape or v.shape[:2] != q.shape[:2]:
+        raise ValueError("q, k must be [B, H, d_r] and v [B, H, d_v]")
+    if Vt.shape != (B, H, Kc, d_v) or Z.shape != (B, H, Kc) or Vt.dtype != torch.float32 \
+            or Z.dtype != torch.float32:
+        raise ValueError("Vt must be fp32 [B, H, K, d_v] and Z fp32 [B, H, K]")
+    code = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if out is None:
+        out = torch.empty(B, H, d_v, dtype=torch.float32, device=q.device)
+    nb = int(lib.gma_decode_workspace_size(H, d_r, Kc))
+    if nb == 0:
+        raise GmaError(2, "gma_decode_step")
+    ws = _workspace(nb, q.device, workspace)
+    opt = options(sync_status=sync_status)
+    st = lib.gma_decode_step(_ptr(q), _ptr(k), _ptr(v), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi), float(eps),
+                             _ptr(Vt), _ptr(Z), _ptr(out), B, H, d_r, d_v, Kc, ctypes.byref(opt), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_decode_step")
+    return out
+
+
+def routing_stats(X, mu, sigma2, log_pi, want_z=True, workspace=None, stream=None, sync_status=False) -> dict:
+    """Component-usage diagnostics per (b, h): usage [B, H, K] fp32 (sum of the
+    responsibilities), counts [B, H, K] int32 (hard assignments), z [B, H, N] int32
+    (if want_z), entropy [B, H] fp32 (usage entropy over log K), used [B, H]
+    (non-empty counts, derived here from counts)."""
+    import torch
+    lib = load()
+    _check_dev(X, mu, sigma2, log_pi)
+    B, H, N, d_r = X.shape
+    Kc = _params_check(H, d_r, mu, sigma2, log_pi)
+    code = _dtype_code(X)
+    dev = X.device
+    usage = torch.empty(B, H, Kc, dtype=torch.float32, device=dev)
+    counts = torch.empty(B, H, Kc, dtype=torch.int32, device=dev)
+    z = torch.empty(B, H, N, dtype=torch.int32, device=dev) if want_z else None
+    entropy = torch.empty(B, H, dtype=torch.float32, device=dev)
+    nb = int(lib.gma_routing_stats_workspace_size(B, H, N, d_r, Kc, code))
+    if nb == 0:
+        raise GmaError(2, "gma_routing_stats")
+    ws = _workspace(nb, dev, workspace)
+    opt = options(sync_status=sync_status)
+    st = lib.gma_routing_stats(_ptr(X), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(usage), _ptr(counts),
+                               _ptr(z) if z is not None else None, _ptr(entropy), B, H, N, d_r, Kc,
+                               ctypes.byref(opt), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_routing_stats")
+    return {"usage": usage, "counts": counts, "z": z, "entropy": entropy, "used": (counts > 0).sum(-1)}

@@ -25,7 +25,9 @@ EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_forward_causal", "gma_last_device_status", "gma_status_string",
             "gma_selected_path", "gma_stage_count", "gma_stage_name",
             "gma_forward_bidir_noalloc", "gma_backward_workspace_size", "gma_backward_bidir",
-            "gma_backward_causal")
+            "gma_backward_causal", "gma_latent_memory_workspace_size", "gma_latent_memory",
+            "gma_decode_workspace_size", "gma_decode_step", "gma_routing_stats_workspace_size",
+            "gma_routing_stats")
 
 
 class Options(ctypes.Structure):
@@ -75,6 +77,18 @@ def load(path: str | None = None):
         lib.gma_backward_bidir.restype = i
         lib.gma_backward_causal.argtypes = lib.gma_backward_bidir.argtypes
         lib.gma_backward_causal.restype = i
+        lib.gma_latent_memory_workspace_size.argtypes = [i, i, i, i, i, i, i, opt]
+        lib.gma_latent_memory_workspace_size.restype = sz
+        lib.gma_latent_memory.argtypes = [vp, vp, i, vp, vp, vp, vp, vp] + [i] * 6 + [opt, vp, sz, vp]
+        lib.gma_latent_memory.restype = i
+        lib.gma_decode_workspace_size.argtypes = [i, i, i]
+        lib.gma_decode_workspace_size.restype = sz
+        lib.gma_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, f, vp, vp, vp] + [i] * 5 + [opt, vp, sz, vp]
+        lib.gma_decode_step.restype = i
+        lib.gma_routing_stats_workspace_size.argtypes = [i, i, i, i, i, i]
+        lib.gma_routing_stats_workspace_size.restype = sz
+        lib.gma_routing_stats.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp] + [i] * 5 + [opt, vp, sz, vp]
+        lib.gma_routing_stats.restype = i
         lib.gma_last_device_status.argtypes = [vp, vp]
         lib.gma_last_device_status.restype = i
         lib.gma_status_string.argtypes = [i]

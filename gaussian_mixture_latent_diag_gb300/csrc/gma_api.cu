@@ -46,6 +46,11 @@ size_t workspace_for(const Problem &p, int causal, const gma_options *opt, int p
     return gma::simt_layout(p, causal, splits).total;
 }
 
+// The auxiliary entry points have only a CUDA-core implementation.
+bool simt_only(const gma_options *opt) {
+    return !opt || opt->path == GMA_PATH_AUTO || opt->path == GMA_PATH_SIMT;
+}
+
 gma::StageClock clock_for(const gma_options *opt, cudaStream_t s) {
     gma::StageClock c;
     if (opt && opt->stage_events && opt->n_stage_events > 0) {
@@ -260,6 +265,145 @@ gma_status gma_backward_causal(const void *Q_X, const void *K_X, const void *V_X
                     B, H, N, d_r, d_v, K, options, workspace, workspace_bytes, stream, 1);
 }
 
+size_t gma_latent_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
+                                        const gma_options *options) {
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return 0;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return 0;
+    if (options && options->splits < 0) return 0;
+    Problem p;
+    p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    return gma::simt_layout(p, 2, options ? options->splits : 0).total;
+}
+
+gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, const float *mu,
+                             const float *sigma2, const float *log_pi, float *Vt, float *Z,
+                             int B, int H, int N, int d_r, int d_v, int K,
+                             const gma_options *options, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    if (!K_X || !V_X || !mu || !sigma2 || !log_pi || !Vt || !Z || !workspace) return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(K_X) || !aligned16(V_X) || !aligned16(Vt) || !aligned16(Z) || !aligned16(mu) ||
+        !aligned16(sigma2))
+        return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (options && options->splits < 0) return GMA_ERR_INVALID_ARG;
+    Problem p;
+    p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.dtype = dtype;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    const int splits = options ? options->splits : 0;
+    const size_t need = gma::simt_layout(p, 2, splits).total;
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
+    const size_t nvt = 4 * (size_t)B * H * K * d_v, nz = 4 * (size_t)B * H * K;
+    const void *in[] = {K_X, V_X, mu, sigma2, log_pi, workspace};
+    const size_t nin[] = {es * rows * d_r, es * rows * d_v, 4 * (size_t)H * K * d_r, 4 * (size_t)H * K * d_r,
+                          4 * (size_t)H * K, need};
+    for (int a = 0; a < 6; ++a)
+        if (overlaps(Vt, nvt, in[a], nin[a]) || overlaps(Z, nz, in[a], nin[a])) return GMA_ERR_INVALID_ARG;
+    if (overlaps(Vt, nvt, Z, nz) || overlaps(workspace, need, K_X, nin[0]) || overlaps(workspace, need, V_X, nin[1]))
+        return GMA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    return finish(gma::simt_latent_memory(p, splits, Vt, Z, workspace, s, clk), options, workspace, s);
+}
+
+size_t gma_decode_workspace_size(int H, int d_r, int K) {
+    if (!shape_ok(1, H, 1, d_r, 16, K, false)) return 0;
+    return gma::decode_workspace();
+}
+
+gma_status gma_decode_step(const void *q, const void *k, const void *v, gma_dtype dtype,
+                           const float *mu, const float *sigma2, const float *log_pi, float eps,
+                           float *Vt, float *Z, float *o, int B, int H, int d_r, int d_v, int K,
+                           const gma_options *options, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    if (!q || !k || !v || !mu || !sigma2 || !log_pi || !Vt || !Z || !o || !workspace) return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    const size_t es = dtype == GMA_F32 ? 4 : 2;
+    // q, k, v are read element by element, Vt as float4
+    const void *elem[] = {q, k, v};
+    for (const void *ptr : elem)
+        if (reinterpret_cast<uintptr_t>(ptr) % es != 0) return GMA_ERR_INVALID_ARG;
+    const void *word[] = {mu, sigma2, log_pi, Z, o};
+    for (const void *ptr : word)
+        if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(Vt)) return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, 1, d_r, d_v, K, true) || !simt_only(options) || (options && options->o_bf16))
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+    Problem p;
+    p.Q = q; p.Kx = k; p.V = v; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = o;
+    p.dtype = dtype; p.eps = eps;
+    p.B = B; p.H = H; p.N = 1; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    const size_t need = gma::decode_workspace();
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t bh = (size_t)B * H;
+    const size_t nvt = 4 * bh * K * d_v, nz = 4 * bh * K, no = 4 * bh * d_v;
+    const void *in[] = {q, k, v, mu, sigma2, log_pi, workspace};
+    const size_t nin[] = {es * bh * d_r, es * bh * d_r, es * bh * d_v, 4 * (size_t)H * K * d_r,
+                          4 * (size_t)H * K * d_r, 4 * (size_t)H * K, need};
+    const void *out[] = {Vt, Z, o};
+    const size_t nout[] = {nvt, nz, no};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 7; ++b)
+            if (overlaps(out[a], nout[a], in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(out[a], nout[a], out[b], nout[b])) return GMA_ERR_INVALID_ARG;
+    }
+    for (int b = 0; b < 3; ++b)
+        if (overlaps(workspace, need, in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    return finish(gma::simt_decode_step(p, Vt, Z, workspace, s, clk), options, workspace, s);
+}
+
+size_t gma_routing_stats_workspace_size(int B, int H, int N, int d_r, int K, gma_dtype dtype) {
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return 0;
+    if (!shape_ok(B, H, N, d_r, 16, K, false)) return 0;
+    Problem p;
+    p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = 16; p.K = K;
+    return gma::stats_workspace(p);
+}
+
+gma_status gma_routing_stats(const void *X, gma_dtype dtype, const float *mu, const float *sigma2,
+                             const float *log_pi, float *usage, int *counts, int *z, float *entropy,
+                             int B, int H, int N, int d_r, int K, const gma_options *options,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    if (!X || !mu || !sigma2 || !log_pi || !usage || !counts || !workspace) return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(usage) || !aligned16(counts) || !aligned16(mu) || !aligned16(sigma2) ||
+        reinterpret_cast<uintptr_t>(z) % 4 || reinterpret_cast<uintptr_t>(entropy) % 4)
+        return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, 16, K, false) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    Problem p;
+    p.Q = X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.dtype = dtype;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = 16; p.K = K;
+    const size_t need = gma::stats_workspace(p);
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t es = dtype == GMA_F32 ? 4 : 2, bh = (size_t)B * H;
+    const void *in[] = {X, mu, sigma2, log_pi, workspace};
+    const size_t nin[] = {es * bh * N * d_r, 4 * (size_t)H * K * d_r, 4 * (size_t)H * K * d_r, 4 * (size_t)H * K,
+                          need};
+    const void *out[] = {usage, counts, z, entropy};
+    const size_t nout[] = {4 * bh * K, 4 * bh * K, z ? 4 * bh * N : 0, entropy ? 4 * bh : 0};
+    for (int a = 0; a < 4; ++a) {
+        if (!out[a]) continue;
+        for (int b = 0; b < 5; ++b)
+            if (overlaps(out[a], nout[a], in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 4; ++b)
+            if (out[b] && overlaps(out[a], nout[a], out[b], nout[b])) return GMA_ERR_INVALID_ARG;
+    }
+    if (overlaps(workspace, need, X, nin[0])) return GMA_ERR_INVALID_ARG;
+    gma::StatsArgs a;
+    a.usage = usage; a.counts = counts; a.z = z; a.entropy = entropy;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    return finish(gma::simt_routing_stats(p, a, workspace, s, clk), options, workspace, s);
+}
+
 gma_status gma_last_device_status(const void *workspace, void *stream) {
     if (!workspace) return GMA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -295,9 +439,10 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
 }
 
 int gma_stage_count(int path, int variant) {
-    if (variant < -1 || variant > 3 || (variant >= 2 && path != GMA_PATH_SIMT)) return 0;
+    if (variant < -1 || variant > 6 || (variant >= 2 && path != GMA_PATH_SIMT)) return 0;
     const char *const *names;
-    if (variant >= 2) names = gma::kBackwardStages[variant - 2];
+    if (variant >= 4) names = gma::kAuxStages[variant - 4];
+    else if (variant >= 2) names = gma::kBackwardStages[variant - 2];
     else if (path == GMA_PATH_SIMT) names = gma::kSimtStages[variant + 1];
     else if (path == GMA_PATH_TC) names = gma::kTcStages[variant + 1];
     else return 0;
@@ -309,6 +454,7 @@ int gma_stage_count(int path, int variant) {
 const char *gma_stage_name(int path, int variant, int j) {
     int n = gma_stage_count(path, variant);
     if (j < 0 || j >= n) return nullptr;
+    if (variant >= 4) return gma::kAuxStages[variant - 4][j];
     if (variant >= 2) return gma::kBackwardStages[variant - 2][j];
     return path == GMA_PATH_SIMT ? gma::kSimtStages[variant + 1][j] : gma::kTcStages[variant + 1][j];
 }

@@ -56,8 +56,26 @@ struct SimtLayout {
     int nsplit = 0, tokens_per_split = 0;
 };
 constexpr int kSimtCausalChunk = 64;
-SimtLayout simt_layout(const Problem &p, int mode /* -1 resp, 0 bidir, 1 causal */, int splits);
+SimtLayout simt_layout(const Problem &p,
+                       int mode /* -1 resp, 0 bidir, 1 causal, 2 latent memory, 3 read from a memory */,
+                       int splits);
+// Clears the status word and writes 1/sigma2 and c' (with parameter validation)
+// into the simt_layout(p, -1, 0) regions of ws.
+cudaError_t simt_prep(const Problem &p, void *ws, cudaStream_t s);
+// Latent memory of (p.Kx, p.V) into the caller's Vt [BH][K][d_v] and Z [BH][K]
+// (stages prep, resp_k, write, reduce; workspace simt_layout(p, 2, splits)).
+cudaError_t simt_latent_memory(const Problem &p, int splits, float *Vt, float *Z, void *ws, cudaStream_t s,
+                               StageClock &clk);
 
+// Eq. (7) from the caller's memory Vt [BH][K][d_v], Z [BH][K] (stages prep,
+// resp_q, pack, read; workspace simt_layout(p, 3, 0)).
+cudaError_t simt_read_memory(const Problem &p, const float *Vt, const float *Z, void *ws, cudaStream_t s,
+                             StageClock &clk);
+// Causal forward whose prefix starts from (Vt_in, Z_in) (zero when null); the
+// prefix after the last position goes to (Vt_out, Z_out) when given (stages as
+// simt_causal; workspace simt_layout(p, 1, 0)).
+cudaError_t simt_causal_carry(const Problem &p, const float *Vt_in, const float *Z_in, float *Vt_out, float *Z_out,
+                              void *ws, cudaStream_t s, StageClock &clk);
 cudaError_t simt_responsibilities(const Problem &p, void *ws, cudaStream_t s, StageClock &clk);
 cudaError_t simt_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &clk);
@@ -84,6 +102,29 @@ cudaError_t simt_backward_bidir(const Problem &p, const BackwardArgs &g, int spl
 cudaError_t simt_backward_causal(const Problem &p, const BackwardArgs &g, void *ws, cudaStream_t s,
                                  StageClock &clk);
 extern const char *const kBackwardStages[2][8];  // [causal][j], NULL-terminated
+
+// ---------------------------------------------------------------- decode step (gma_decode.cu)
+// One causal position for every (b, h): q, k [BH][d_r], v [BH][d_v] (p.Q, p.Kx,
+// p.V), carried state Vt [BH][K][d_v], Z [BH][K] updated in place, output p.O
+// [BH][d_v].  Workspace: decode_workspace() bytes (the status word).  Stages:
+// reset (status word), step.
+size_t decode_workspace();
+cudaError_t simt_decode_step(const Problem &p, float *Vt, float *Z, void *ws, cudaStream_t s, StageClock &clk);
+
+// ---------------------------------------------------------------- usage diagnostics (gma_stats.cu)
+struct StatsArgs {
+    float *usage = nullptr;    // [BH][K]
+    int *counts = nullptr;     // [BH][K]
+    int *z = nullptr;          // [BH][N] or null
+    float *entropy = nullptr;  // [BH] or null (normalised usage entropy)
+};
+size_t stats_workspace(const Problem &p);
+cudaError_t simt_routing_stats(const Problem &p, const StatsArgs &a, void *ws, cudaStream_t s, StageClock &clk);
+
+// Stage names of the auxiliary entry points: [0] latent memory, [1] decode step,
+// [2] routing statistics, [3] read from a memory, [4] causal forward with a
+// carried-in prefix; NULL-terminated.
+extern const char *const kAuxStages[5][8];
 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);

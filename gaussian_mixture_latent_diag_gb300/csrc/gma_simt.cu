@@ -225,6 +225,62 @@ __global__ void reduce_splits_kernel(const float *__restrict__ part, int nsplit,
     mem[(size_t)bh * E + e] = acc;
 }
 
+// Fixed-order sum of the split partials into the caller's latent memory:
+// Vt[bh][k][c] = sum_s part[bh][s][k][c] (c < d_v), Z[bh][k] = sum_s part[bh][s][k][d_v].
+__global__ void reduce_to_memory_kernel(const float *__restrict__ part, int nsplit, int K, int d_v,
+                                        float *__restrict__ Vt, float *__restrict__ Z,
+                                        const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y, W = d_v + 1, E = K * W;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const float *p = part + (size_t)bh * nsplit * E + e;
+    float acc = 0.f;
+    for (int s = 0; s < nsplit; ++s) acc += p[(size_t)s * E];
+    const int k = e / W, c = e % W;
+    if (c < d_v) Vt[((size_t)bh * K + k) * d_v + c] = acc;
+    else Z[(size_t)bh * K + k] = acc;
+}
+
+// Packs a caller's latent memory into the read kernel's layout:
+// mem[bh][k] = [Vt[bh][k][0..d_v) | Z[bh][k]].
+__global__ void pack_memory_kernel(const float *__restrict__ Vt, const float *__restrict__ Z, int K, int d_v,
+                                   float *__restrict__ mem, const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y, W = d_v + 1, E = K * W;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const int k = e / W, c = e % W;
+    mem[(size_t)bh * E + e] = c < d_v ? Vt[((size_t)bh * K + k) * d_v + c] : Z[(size_t)bh * K + k];
+}
+
+// As scan_chunks_kernel, with the prefix starting from a carried-in memory
+// (Vt_in, Z_in; zero when null) instead of zero, and the total after the last
+// chunk -- the prefix memory after position N - 1 -- written to (Vt_out, Z_out)
+// when given.
+__global__ void scan_chunks_carry_kernel(float *__restrict__ part, int nchunk, int K, int d_v,
+                                         const float *__restrict__ Vt_in, const float *__restrict__ Z_in,
+                                         float *__restrict__ Vt_out, float *__restrict__ Z_out,
+                                         const unsigned *status) {
+    if (failed(status)) return;
+    const int bh = blockIdx.y, W = d_v + 1, E = K * W;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const int k = e / W, c = e % W;
+    float run = 0.f;
+    if (Vt_in) run = c < d_v ? Vt_in[((size_t)bh * K + k) * d_v + c] : Z_in[(size_t)bh * K + k];
+    float *p = part + (size_t)bh * nchunk * E + e;
+    for (int ch = 0; ch < nchunk; ++ch) {
+        const float cur = p[(size_t)ch * E];
+        p[(size_t)ch * E] = run;
+        run += cur;
+    }
+    if (Vt_out) {
+        if (c < d_v) Vt_out[((size_t)bh * K + k) * d_v + c] = run;
+        else Z_out[(size_t)bh * K + k] = run;
+    }
+}
+
 // In-place exclusive prefix over the chunk partials of each head, in chunk
 // order: part[c] <- sum_{c' < c} part[c'] (the causal prefix memory at the
 // start of chunk c, [GMA, causal variant, cumulative sums]).
@@ -461,11 +517,14 @@ SimtLayout simt_layout(const Problem &p, int mode, int splits) {
     size_t off = kStatusBytes;
     L.inv_s2 = off; off = align256(off + sizeof(float) * (size_t)p.H * p.K * p.d_r);
     L.cprime = off; off = align256(off + sizeof(float) * (size_t)p.H * p.K);
-    if (mode >= 0) {
+    if (mode == 3) {  // read from a given memory: Gamma^Q and the packed [Vt | Z]
+        L.gq = off; off = align256(off + sizeof(float) * (size_t)p.BH() * p.K * p.N);
+        L.mem = off; off = align256(off + sizeof(float) * (size_t)p.BH() * p.K * ((size_t)p.d_v + 1));
+    } else if (mode >= 0) {
         const size_t g = sizeof(float) * (size_t)p.BH() * p.K * p.N;
-        L.gq = off; off = align256(off + g);
+        if (mode != 2) { L.gq = off; off = align256(off + g); }
         L.gk = off; off = align256(off + g);
-        if (mode == 0) {
+        if (mode == 0 || mode == 2) {
             int ns = splits > 0 ? splits : (p.N + 1023) / 1024;
             ns = ns < 1 ? 1 : (ns > p.N ? p.N : ns);
             L.tokens_per_split = (p.N + ns - 1) / ns;
@@ -568,6 +627,79 @@ cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &
         GMA_TRY((launch_causal<__nv_bfloat16, float>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
     else
         GMA_TRY((launch_causal<__nv_bfloat16, __nv_bfloat16>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t simt_read_memory(const Problem &p, const float *Vt, const float *Z, void *ws, cudaStream_t s,
+                             StageClock &clk) {
+    SimtLayout L = simt_layout(p, 3, 0);
+    Ptrs P = ptrs(L, ws);
+    clk.mark();
+    GMA_TRY(prep(p, P, s));
+    clk.mark();
+    const long long bhs = (long long)p.K * p.N;
+    if (p.dtype == GMA_F32) GMA_TRY(launch_resp<float>(p, p.Q, P.inv, P.cprime, P.gq, bhs, 1, p.N, P.status, s));
+    else GMA_TRY(launch_resp<__nv_bfloat16>(p, p.Q, P.inv, P.cprime, P.gq, bhs, 1, p.N, P.status, s));
+    clk.mark();
+    const int E = p.K * (p.d_v + 1);
+    pack_memory_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(Vt, Z, p.K, p.d_v, P.mem, P.status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    if (p.o_bf16) GMA_TRY(launch_read<__nv_bfloat16>(p, P.gq, P.mem, P.status, s));
+    else GMA_TRY(launch_read<float>(p, P.gq, P.mem, P.status, s));
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t simt_causal_carry(const Problem &p, const float *Vt_in, const float *Z_in, float *Vt_out, float *Z_out,
+                              void *ws, cudaStream_t s, StageClock &clk) {
+    SimtLayout L = simt_layout(p, 1, 0);
+    Ptrs P = ptrs(L, ws);
+    clk.mark();
+    GMA_TRY(prep(p, P, s));
+    clk.mark();
+    GMA_TRY(resp_both(p, P, s, clk));
+    GMA_TRY(write_parts(p, L, P, s));
+    clk.mark();
+    const int E = p.K * (p.d_v + 1);
+    scan_chunks_carry_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, p.K, p.d_v, Vt_in, Z_in,
+                                                                           Vt_out, Z_out, P.status);
+    GMA_TRY(cudaGetLastError());
+    clk.mark();
+    if (p.dtype == GMA_F32 && !p.o_bf16)
+        GMA_TRY((launch_causal<float, float>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    else if (p.dtype == GMA_F32)
+        GMA_TRY((launch_causal<float, __nv_bfloat16>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    else if (!p.o_bf16)
+        GMA_TRY((launch_causal<__nv_bfloat16, float>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    else
+        GMA_TRY((launch_causal<__nv_bfloat16, __nv_bfloat16>(p, P.gq, P.gk, P.part, L.nsplit, P.status, s)));
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t simt_prep(const Problem &p, void *ws, cudaStream_t s) {
+    return prep(p, ptrs(simt_layout(p, -1, 0), ws), s);
+}
+
+cudaError_t simt_latent_memory(const Problem &p, int splits, float *Vt, float *Z, void *ws, cudaStream_t s,
+                               StageClock &clk) {
+    SimtLayout L = simt_layout(p, 2, splits);
+    Ptrs P = ptrs(L, ws);
+    clk.mark();
+    GMA_TRY(prep(p, P, s));
+    clk.mark();
+    const long long bhs = (long long)p.K * p.N;
+    if (p.dtype == GMA_F32) GMA_TRY(launch_resp<float>(p, p.Kx, P.inv, P.cprime, P.gk, bhs, 1, p.N, P.status, s));
+    else GMA_TRY(launch_resp<__nv_bfloat16>(p, p.Kx, P.inv, P.cprime, P.gk, bhs, 1, p.N, P.status, s));
+    clk.mark();
+    GMA_TRY(write_parts(p, L, P, s));
+    clk.mark();
+    const int E = p.K * (p.d_v + 1);
+    reduce_to_memory_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, p.K, p.d_v, Vt, Z,
+                                                                          P.status);
+    GMA_TRY(cudaGetLastError());
     clk.mark();
     return cudaSuccess;
 }

@@ -233,10 +233,87 @@ gma_status gma_backward_causal(const void *Q_X, const void *K_X, const void *V_X
                                size_t workspace_bytes, void *stream);
 
 /*
+ * Latent memory of a key/value sequence ([GMA, Eqs. (5)-(6), latent
+ * aggregation]):
+ *   Vt[b,h] = (Gamma^K)^T V_X  : [B, H, K, d_v] fp32
+ *   Z[b,h]  = (Gamma^K)^T 1    : [B, H, K] fp32
+ * with Gamma^K the responsibilities of K_X.  This is also the carried state
+ * of the causal variant after the last position (the prefix memories of
+ * Eq. (8b) at i = N - 1): it primes gma_decode_step with a prompt of N tokens.
+ * Runs on the CUDA cores (options->path must be GMA_PATH_AUTO or
+ * GMA_PATH_SIMT; options->splits sets the number of N-splits, 0 = default).
+ * K_X, V_X, Vt, Z must start on a 16-byte boundary, the workspace on a
+ * 256-byte boundary; Vt and Z may not overlap an input, each other or the
+ * workspace (GMA_ERR_INVALID_ARG).  Parameter errors and the status word
+ * behave as for the forward.  Workspace bytes:
+ * gma_latent_memory_workspace_size (0 for unsupported arguments).
+ */
+size_t gma_latent_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
+                                        const gma_options *options);
+gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, const float *mu,
+                             const float *sigma2, const float *log_pi, float *Vt, float *Z,
+                             int B, int H, int N, int d_r, int d_v, int K,
+                             const gma_options *options, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * One autoregressive position of the causal GMA for every (b, h) ([GMA, causal
+ * variant, Eq. (8b)], prefix memories carried as running sums).  The new
+ * position's key enters its own prefix before its query reads it (j <= i):
+ *   Vt[b,h,k,:] += gamma^K_k v[b,h,:],   Z[b,h,k] += gamma^K_k
+ *   o[b,h,:]     = sum_k gamma^Q_k Vt[b,h,k,:] / (sum_k gamma^Q_k Z[b,h,k] + eps)
+ *   q, k : [B, H, d_r]   v : [B, H, d_v]   (dtype)
+ *   Vt   : [B, H, K, d_v] fp32, Z : [B, H, K] fp32 -- read and updated in place
+ *   o    : [B, H, d_v] fp32
+ * Start from zeros (an empty prefix) or from gma_latent_memory of a prompt.
+ * Calling it for positions 0..N-1 in order reproduces gma_forward_causal row by
+ * row.  Runs on the CUDA cores (options->path GMA_PATH_AUTO or GMA_PATH_SIMT;
+ * options->o_bf16 is not supported, GMA_ERR_UNSUPPORTED_SHAPE).  Vt must start
+ * on a 16-byte boundary and the workspace on a 256-byte boundary; Vt, Z and o
+ * may not overlap an input, each other or the workspace (GMA_ERR_INVALID_ARG).
+ * Invalid parameter values are reported through the status word as for the
+ * forward; the rows of a head with an invalid value are left unchanged (Vt, Z
+ * and o), the other heads are updated.  The workspace
+ * (gma_decode_workspace_size bytes, independent of B) holds the status word.
+ */
+size_t gma_decode_workspace_size(int H, int d_r, int K);
+gma_status gma_decode_step(const void *q, const void *k, const void *v, gma_dtype dtype,
+                           const float *mu, const float *sigma2, const float *log_pi, float eps,
+                           float *Vt, float *Z, float *o, int B, int H, int d_r, int d_v, int K,
+                           const gma_options *options, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
+ * Component-usage diagnostics of the responsibilities of X ([GMA,
+ * introduction: the marginal usage of the components and the hard assignment
+ * z_i = argmax_k gamma_ik; the interpretability results' components-used count
+ * and usage entropy]), per (b, h), computed beside the responsibilities
+ * without writing Gamma:
+ *   usage   : [B, H, K] fp32   usage_k = sum_i gamma_ik
+ *   counts  : [B, H, K] int32  number of rows whose hard assignment is k
+ *   z       : [B, H, N] int32  hard assignment of each row: the smallest k
+ *             that maximises the row's score (and so gamma); may be NULL
+ *   entropy : [B, H] fp32      -sum_k p_k log p_k / log K with p = usage / N
+ *             (1 when K = 1); may be NULL
+ * The number of components used is the number of non-zero counts.  Runs on the
+ * CUDA cores (options->path GMA_PATH_AUTO or GMA_PATH_SIMT).  X, usage and
+ * counts must start on a 16-byte boundary, the workspace on a 256-byte
+ * boundary; no output may overlap an input, another output or the workspace
+ * (GMA_ERR_INVALID_ARG).  Parameter errors and the status word behave as for
+ * the forward.  Workspace bytes: gma_routing_stats_workspace_size.
+ */
+size_t gma_routing_stats_workspace_size(int B, int H, int N, int d_r, int K, gma_dtype dtype);
+gma_status gma_routing_stats(const void *X, gma_dtype dtype, const float *mu, const float *sigma2,
+                             const float *log_pi, float *usage, int *counts, int *z, float *entropy,
+                             int B, int H, int N, int d_r, int K, const gma_options *options,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Number of stages (kernel launches, plus the status reset of the first) of
  * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
  * `variant` (-1 responsibilities, 0 bidirectional, 1 causal, 2 bidirectional
- * backward, 3 causal backward -- the last two SIMT only), and the name of
+ * backward, 3 causal backward, 4 latent memory, 5 decode step, 6 routing
+ * statistics -- variants 2 to 6 SIMT only), and the name of
  * stage j (NULL if out of range).
  * Used with gma_options.stage_events.
  */

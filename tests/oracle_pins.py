@@ -328,10 +328,30 @@ def pin_latent_memory_read_gives_bidir_affinity():
     N, d_r, d_v, K, eps = 27, 3, 4, 5, 1e-6
     Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
     Vt, Z = oracle.latent_memory(Kx, V, mu, s2, lp)
-    GQ = oracle.responsibilities(Q, mu, s2, lp)
-    O = (GQ @ Vt) / (GQ @ Z + eps)[:, None]
     ref = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=False)
-    assert _rel(O, ref) < 1e-12
+    assert _rel(oracle.read_memory(Q, mu, s2, lp, eps, Vt, Z), ref) < 1e-12
+
+
+def pin_sharded_memories_add_up():
+    """Latent memories of key/value shards add up to the memory of the whole
+    sequence (the sums of Eqs. 5-6 split over N), so reading their sum gives the
+    bidirectional output, and decoding a shard from the exclusive prefix of the
+    shard memories gives that shard's causal rows."""
+    rng = _rng(31)
+    N, d_r, d_v, K, eps = 40, 3, 2, 4, 1e-6
+    Q, Kx, V, mu, s2, lp = random_head(rng, N, d_r, d_v, K)
+    cuts = [0, 9, 10, 31, 40]
+    mems = [oracle.latent_memory(Kx[a:b], V[a:b], mu, s2, lp) for a, b in zip(cuts[:-1], cuts[1:])]
+    Vt, Z = sum(m[0] for m in mems), sum(m[1] for m in mems)
+    ref_b = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=False)
+    assert _rel(oracle.read_memory(Q[:20], mu, s2, lp, eps, Vt, Z), ref_b[:20]) < 1e-12
+    ref_c = oracle.affinity_forward(Q, Kx, V, mu, s2, lp, eps, causal=True)
+    carry_v, carry_z = np.zeros((K, d_v)), np.zeros(K)
+    for (a, b), (mv, mz) in zip(zip(cuts[:-1], cuts[1:]), mems):
+        O, _, _ = oracle.decode(Q[None, a:b], Kx[None, a:b], V[None, a:b], mu, s2, lp, eps, carry_v[None],
+                                carry_z[None])
+        assert _rel(O[0], ref_c[a:b]) < 1e-12
+        carry_v, carry_z = carry_v + mv, carry_z + mz
 
 
 def pin_decode_continues_a_prompt():
