@@ -18,6 +18,7 @@ Linear-Time Sequence Mixing via Probabilistic Latent Routing" (arXiv
 * ``backward_bidir`` / ``backward_causal`` -- gradients: gradient section,
   Eq. (18) (score gradient) and the chain rule through the score
 * ``latent_memory``                  -- Eqs. (5)-(6): Vt, Z of a key/value sequence
+* ``read_memory``                    -- Eq. (7) from a given memory (Vt, Z)
 * ``decode_step`` / ``decode``        -- Eq. (8b) one position at a time (carried Vt, Z)
 * ``routing_stats``                  -- component usage, hard assignments, usage entropy
   (the introduction's usage / hard-assignment diagnostics)
@@ -102,6 +103,9 @@ def _load(mutant: int = 0):
             lib.gma_oracle_routing_stats.argtypes = [_D, ctypes.c_int, ctypes.c_int, _D, _D, _D,
                                                      ctypes.c_int, _D, _L, _L, _D]
             lib.gma_oracle_routing_stats.restype = None
+            lib.gma_oracle_read_memory.argtypes = [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
+                                                   _D, ctypes.c_int, ctypes.c_double, _D, _D, _D]
+            lib.gma_oracle_read_memory.restype = None
             _libs[mutant] = lib
     return lib
 
@@ -307,6 +311,25 @@ def latent_memory(K_, V, mu, sigma2, log_pi):
                                      _p(Vt[b]), _p(Z[b]))
     lead = K_.shape[:-2]
     return Vt.reshape(lead + (K, d_v)), Z.reshape(lead + (K,))
+
+
+def read_memory(Q, mu, sigma2, log_pi, eps, Vt, Z) -> np.ndarray:
+    """O [B, H, N, d_v] = Gamma^Q Vt / (Gamma^Q Z + eps) ([GMA, Eq. 7]) for Q
+    [B, H, N, d_r] and a given memory Vt [B, H, K, d_v], Z [B, H, K]."""
+    lib = _load(_ACTIVE[0])
+    Q, Vt, Z = _f64(Q), _f64(Vt), _f64(Z)
+    mu, sigma2, log_pi = _params(mu, sigma2, log_pi)
+    H, K = mu.shape[0], mu.shape[1]
+    N, d_r = Q.shape[-2:]
+    d_v = Vt.shape[-1]
+    Qh, Vth, Zh = _heads(Q, 2), Vt.reshape(-1, K, d_v), Z.reshape(-1, K)
+    O = np.empty((Qh.shape[0], N, d_v))
+    for b in range(Qh.shape[0]):
+        m, s, lp = _head_param(b, H, mu, sigma2, log_pi)
+        q, vt, z = (np.ascontiguousarray(t[b]) for t in (Qh, Vth, Zh))
+        lib.gma_oracle_read_memory(_p(q), N, d_r, d_v, _p(m), _p(s), _p(lp), K, float(eps), _p(vt), _p(z),
+                                   _p(O[b]))
+    return O.reshape(Q.shape[:-1] + (d_v,))
 
 
 def decode_step(q, k, v, mu, sigma2, log_pi, eps, Vt, Z):

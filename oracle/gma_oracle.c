@@ -645,3 +645,27 @@ void gma_oracle_routing_stats(const double *X, int N, int d_r, const double *mu,
     stats[2] = (double)used;
     free(g);
 }
+
+/*
+ * Normalized broadcasting from a given latent memory ([GMA, Eq. 7], footnote 4):
+ *   O_i = (sum_k gQ_ik Vt_k) / (sum_k gQ_ik Z_k + eps)
+ * with Vt [K, d_v], Z [K] supplied by the caller (for example the sum of the
+ * latent memories of several key/value shards).
+ */
+void gma_oracle_read_memory(const double *Q, int N, int d_r, int d_v, const double *mu,
+                            const double *sigma2, const double *log_pi, int K, double eps,
+                            const double *Vt, const double *Z, double *O)
+{
+    double *gq = malloc(sizeof(double) * (size_t)K);
+    for (int i = 0; i < N; ++i) {
+        gma_oracle_responsibilities(Q + (size_t)i * d_r, 1, d_r, mu, sigma2, log_pi, K, gq);
+        double den = eps;
+        for (int k = 0; k < K; ++k) den += gq[k] * Z[k];
+        for (int c = 0; c < d_v; ++c) {
+            double num = 0.0;
+            for (int k = 0; k < K; ++k) num += gq[k] * Vt[(size_t)k * d_v + c];
+            O[(size_t)i * d_v + c] = num / den;
+        }
+    }
+    free(gq);
+}
