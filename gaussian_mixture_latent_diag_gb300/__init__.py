@@ -24,7 +24,8 @@ from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError
                       options, status_string)
 
 __all__ = ["forward_bidir", "forward_causal", "backward_bidir", "backward_causal", "responsibilities",
-           "latent_memory", "decode_step", "routing_stats", "workspace_size",
+           "latent_memory", "read_memory", "forward_causal_carry", "decode_step", "routing_stats",
+           "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
            "PATH_TC", "load"]
 
@@ -308,3 +309,80 @@ def routing_stats(X, mu, sigma2, log_pi, want_z=True, workspace=None, stream=Non
     if st != 0:
         raise GmaError(st, "gma_routing_stats")
     return {"usage": usage, "counts": counts, "z": z, "entropy": entropy, "used": (counts > 0).sum(-1)}
+
+
+def read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps=1e-6, out=None, workspace=None, stream=None, o_bf16=False,
+                sync_status=False):
+    """O = Gamma^Q Vt / (Gamma^Q Z + eps) for Q [B, H, N, d_r] and a given latent
+    memory Vt [B, H, K, d_v], Z [B, H, K] (fp32); O fp32 (or bf16)."""
+    import torch
+    lib = load()
+    _check_dev(Q, mu, sigma2, log_pi, Vt, Z)
+    B, H, N, d_r = Q.shape
+    Kc = _params_check(H, d_r, mu, sigma2, log_pi)
+    d_v = Vt.shape[-1]
+    if Vt.shape != (B, H, Kc, d_v) or Z.shape != (B, H, Kc) or Vt.dtype != torch.float32 \
+            or Z.dtype != torch.float32:
+        raise ValueError("Vt must be fp32 [B, H, K, d_v] and Z fp32 [B, H, K]")
+    code = _dtype_code(Q)
+    odt = torch.bfloat16 if o_bf16 else torch.float32
+    if out is None:
+        out = torch.empty(B, H, N, d_v, dtype=odt, device=Q.device)
+    nb = int(lib.gma_read_memory_workspace_size(B, H, N, d_r, d_v, Kc, code))
+    if nb == 0:
+        raise GmaError(2, "gma_read_memory")
+    ws = _workspace(nb, Q.device, workspace)
+    opt = options(sync_status=sync_status, o_bf16=o_bf16)
+    st = lib.gma_read_memory(_ptr(Q), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi), float(eps), _ptr(Vt), _ptr(Z),
+                             _ptr(out), B, H, N, d_r, d_v, Kc, ctypes.byref(opt), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_read_memory")
+    return out
+
+
+def forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in=None, Z_in=None, eps=1e-6, want_state=True,
+                         out=None, workspace=None, stream=None, o_bf16=False, sync_status=False):
+    """Causal forward whose prefix starts from (Vt_in, Z_in) (an empty prefix if
+    None).  Returns (O, Vt_out, Z_out): the outputs and, if want_state, the
+    prefix memory after the last position (else None, None)."""
+    import torch
+    lib = load()
+    _check_dev(Q, K, V, mu, sigma2, log_pi)
+    B, H, N, d_r = Q.shape
+    d_v = V.shape[-1]
+    Kc = _params_check(H, d_r, mu, sigma2, log_pi)
+    if K.shape != Q.shape or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("Q, K must be [B, H, N, d_r] and V [B, H, N, d_v]")
+    if (Vt_in is None) != (Z_in is None):
+        raise ValueError("give both Vt_in and Z_in, or neither")
+    if Vt_in is not None:
+        _check_dev(Vt_in, Z_in)
+        if Vt_in.shape != (B, H, Kc, d_v) or Z_in.shape != (B, H, Kc) or Vt_in.dtype != torch.float32 \
+                or Z_in.dtype != torch.float32:
+            raise ValueError("Vt_in must be fp32 [B, H, K, d_v] and Z_in fp32 [B, H, K]")
+    code = _dtype_code(Q)
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K, V must share one dtype")
+    dev = Q.device
+    odt = torch.bfloat16 if o_bf16 else torch.float32
+    if out is None:
+        out = torch.empty(B, H, N, d_v, dtype=odt, device=dev)
+    Vt_out = torch.empty(B, H, Kc, d_v, device=dev) if want_state else None
+    Z_out = torch.empty(B, H, Kc, device=dev) if want_state else None
+    nb = int(lib.gma_causal_carry_workspace_size(B, H, N, d_r, d_v, Kc, code))
+    if nb == 0:
+        raise GmaError(2, "gma_forward_causal_carry")
+    ws = _workspace(nb, dev, workspace)
+    opt = options(sync_status=sync_status, o_bf16=o_bf16)
+
+    def p(t):
+        return _ptr(t) if t is not None else None
+
+    st = lib.gma_forward_causal_carry(_ptr(Q), _ptr(K), _ptr(V), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi),
+                                      float(eps), p(Vt_in), p(Z_in), p(Vt_out), p(Z_out), _ptr(out), B, H, N, d_r,
+                                      d_v, Kc, ctypes.byref(opt), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_forward_causal_carry")
+    return out, Vt_out, Z_out

@@ -27,7 +27,8 @@ EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_forward_bidir_noalloc", "gma_backward_workspace_size", "gma_backward_bidir",
             "gma_backward_causal", "gma_latent_memory_workspace_size", "gma_latent_memory",
             "gma_decode_workspace_size", "gma_decode_step", "gma_routing_stats_workspace_size",
-            "gma_routing_stats")
+            "gma_routing_stats", "gma_read_memory_workspace_size", "gma_read_memory",
+            "gma_causal_carry_workspace_size", "gma_forward_causal_carry")
 
 
 class Options(ctypes.Structure):
@@ -89,6 +90,15 @@ def load(path: str | None = None):
         lib.gma_routing_stats_workspace_size.restype = sz
         lib.gma_routing_stats.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp] + [i] * 5 + [opt, vp, sz, vp]
         lib.gma_routing_stats.restype = i
+        lib.gma_read_memory_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        lib.gma_read_memory_workspace_size.restype = sz
+        lib.gma_read_memory.argtypes = [vp, i, vp, vp, vp, f, vp, vp, vp] + [i] * 6 + [opt, vp, sz, vp]
+        lib.gma_read_memory.restype = i
+        lib.gma_causal_carry_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        lib.gma_causal_carry_workspace_size.restype = sz
+        lib.gma_forward_causal_carry.argtypes = [vp, vp, vp, i, vp, vp, vp, f, vp, vp, vp, vp, vp] + [i] * 6 + \
+            [opt, vp, sz, vp]
+        lib.gma_forward_causal_carry.restype = i
         lib.gma_last_device_status.argtypes = [vp, vp]
         lib.gma_last_device_status.restype = i
         lib.gma_status_string.argtypes = [i]

@@ -323,14 +323,14 @@ gma_status gma_decode_step(const void *q, const void *k, const void *v, gma_dtyp
     if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
     const size_t es = dtype == GMA_F32 ? 4 : 2;
-    // q, k, v are read element by element, Vt as float4
+    // q, k, v are read element by element, Vt and o as float4
     const void *elem[] = {q, k, v};
     for (const void *ptr : elem)
         if (reinterpret_cast<uintptr_t>(ptr) % es != 0) return GMA_ERR_INVALID_ARG;
-    const void *word[] = {mu, sigma2, log_pi, Z, o};
+    const void *word[] = {mu, sigma2, log_pi, Z};
     for (const void *ptr : word)
         if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return GMA_ERR_INVALID_ARG;
-    if (!aligned16(Vt)) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(Vt) || !aligned16(o)) return GMA_ERR_INVALID_ARG;
     if (!shape_ok(B, H, 1, d_r, d_v, K, true) || !simt_only(options) || (options && options->o_bf16))
         return GMA_ERR_UNSUPPORTED_SHAPE;
     Problem p;
@@ -404,6 +404,96 @@ gma_status gma_routing_stats(const void *X, gma_dtype dtype, const float *mu, co
     return finish(gma::simt_routing_stats(p, a, workspace, s, clk), options, workspace, s);
 }
 
+size_t gma_read_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype) {
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return 0;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
+    Problem p;
+    p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    return gma::simt_layout(p, 3, 0).total;
+}
+
+gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, const float *sigma2,
+                           const float *log_pi, float eps, const float *Vt, const float *Z, void *O,
+                           int B, int H, int N, int d_r, int d_v, int K, const gma_options *options,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    if (!Q_X || !mu || !sigma2 || !log_pi || !Vt || !Z || !O || !workspace) return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    if (!aligned16(Q_X) || !aligned16(Vt) || !aligned16(Z) || !aligned16(O) || !aligned16(mu) || !aligned16(sigma2))
+        return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    Problem p;
+    p.Q = Q_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = O; p.dtype = dtype; p.eps = eps;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    p.o_bf16 = options && options->o_bf16;
+    const size_t need = gma::simt_layout(p, 3, 0).total;
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
+    const size_t no = (p.o_bf16 ? 2 : 4) * rows * d_v;
+    const void *in[] = {Q_X, Vt, Z, mu, sigma2, log_pi, workspace};
+    const size_t nin[] = {es * rows * d_r, 4 * (size_t)B * H * K * d_v, 4 * (size_t)B * H * K,
+                          4 * (size_t)H * K * d_r, 4 * (size_t)H * K * d_r, 4 * (size_t)H * K, need};
+    for (int a = 0; a < 7; ++a)
+        if (overlaps(O, no, in[a], nin[a])) return GMA_ERR_INVALID_ARG;
+    for (int a = 0; a < 3; ++a)
+        if (overlaps(workspace, need, in[a], nin[a])) return GMA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    return finish(gma::simt_read_memory(p, Vt, Z, workspace, s, clk), options, workspace, s);
+}
+
+size_t gma_causal_carry_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype) {
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return 0;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
+    Problem p;
+    p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    return gma::simt_layout(p, 1, 0).total;
+}
+
+gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
+                                    const float *mu, const float *sigma2, const float *log_pi, float eps,
+                                    const float *Vt_in, const float *Z_in, float *Vt_out, float *Z_out,
+                                    void *O, int B, int H, int N, int d_r, int d_v, int K,
+                                    const gma_options *options, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (!Q_X || !K_X || !V_X || !mu || !sigma2 || !log_pi || !O || !workspace) return GMA_ERR_INVALID_ARG;
+    if (!Vt_in != !Z_in || !Vt_out != !Z_out) return GMA_ERR_INVALID_ARG;
+    if (dtype != GMA_F32 && dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    const void *al[] = {Q_X, K_X, V_X, O, mu, sigma2, Vt_in, Z_in, Vt_out, Z_out};
+    for (const void *ptr : al)
+        if (ptr && !aligned16(ptr)) return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    Problem p;
+    p.Q = Q_X; p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = O;
+    p.dtype = dtype; p.eps = eps;
+    p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
+    p.o_bf16 = options && options->o_bf16;
+    const size_t need = gma::simt_layout(p, 1, 0).total;
+    if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
+    const size_t nvt = 4 * (size_t)B * H * K * d_v, nz = 4 * (size_t)B * H * K;
+    const void *in[] = {Q_X, K_X, V_X, Vt_in, Z_in, mu, sigma2, log_pi, workspace};
+    const size_t nin[] = {es * rows * d_r, es * rows * d_r, es * rows * d_v, Vt_in ? nvt : 0, Z_in ? nz : 0,
+                          4 * (size_t)H * K * d_r, 4 * (size_t)H * K * d_r, 4 * (size_t)H * K, need};
+    const void *out[] = {O, Vt_out, Z_out};
+    const size_t nout[] = {(p.o_bf16 ? 2 : 4) * rows * d_v, Vt_out ? nvt : 0, Z_out ? nz : 0};
+    for (int a = 0; a < 3; ++a) {
+        if (!out[a]) continue;
+        for (int b = 0; b < 9; ++b)
+            if (in[b] && overlaps(out[a], nout[a], in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (out[b] && overlaps(out[a], nout[a], out[b], nout[b])) return GMA_ERR_INVALID_ARG;
+    }
+    for (int b = 0; b < 5; ++b)
+        if (in[b] && overlaps(workspace, need, in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gma::StageClock clk = clock_for(options, s);
+    return finish(gma::simt_causal_carry(p, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk), options, workspace, s);
+}
+
 gma_status gma_last_device_status(const void *workspace, void *stream) {
     if (!workspace) return GMA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -439,7 +529,7 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
 }
 
 int gma_stage_count(int path, int variant) {
-    if (variant < -1 || variant > 6 || (variant >= 2 && path != GMA_PATH_SIMT)) return 0;
+    if (variant < -1 || variant > 8 || (variant >= 2 && path != GMA_PATH_SIMT)) return 0;
     const char *const *names;
     if (variant >= 4) names = gma::kAuxStages[variant - 4];
     else if (variant >= 2) names = gma::kBackwardStages[variant - 2];

@@ -268,8 +268,8 @@ gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, 
  * Start from zeros (an empty prefix) or from gma_latent_memory of a prompt.
  * Calling it for positions 0..N-1 in order reproduces gma_forward_causal row by
  * row.  Runs on the CUDA cores (options->path GMA_PATH_AUTO or GMA_PATH_SIMT;
- * options->o_bf16 is not supported, GMA_ERR_UNSUPPORTED_SHAPE).  Vt must start
- * on a 16-byte boundary and the workspace on a 256-byte boundary; Vt, Z and o
+ * options->o_bf16 is not supported, GMA_ERR_UNSUPPORTED_SHAPE).  Vt and o must
+ * start on a 16-byte boundary and the workspace on a 256-byte boundary; Vt, Z and o
  * may not overlap an input, each other or the workspace (GMA_ERR_INVALID_ARG).
  * Invalid parameter values are reported through the status word as for the
  * forward; the rows of a head with an invalid value are left unchanged (Vt, Z
@@ -309,11 +309,57 @@ gma_status gma_routing_stats(const void *X, gma_dtype dtype, const float *mu, co
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Normalized broadcasting from a given latent memory ([GMA, Eq. (7),
+ * footnote 4]):
+ *   O[b,h,i,:] = sum_k gamma^Q_ik Vt[b,h,k,:] / (sum_k gamma^Q_ik Z[b,h,k] + eps)
+ *   Q_X : [B, H, N, d_r] (dtype)   Vt : [B, H, K, d_v] fp32   Z : [B, H, K] fp32
+ *   O   : [B, H, N, d_v] fp32 (bf16 with options->o_bf16)
+ * With gma_latent_memory this splits the bidirectional forward at the latent
+ * memory: the memories of several key/value shards add up (the sums of
+ * Eqs. (5)-(6) split over N), so a sequence sharded over N needs one sum of
+ * [K, d_v + 1] per head between the two calls.  Runs on the CUDA cores
+ * (options->path GMA_PATH_AUTO or GMA_PATH_SIMT).  Q_X, Vt, Z and O must start
+ * on a 16-byte boundary, the workspace on a 256-byte boundary; O may not
+ * overlap an input or the workspace (GMA_ERR_INVALID_ARG).  Workspace bytes:
+ * gma_read_memory_workspace_size.
+ */
+size_t gma_read_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype);
+gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, const float *sigma2,
+                           const float *log_pi, float eps, const float *Vt, const float *Z, void *O,
+                           int B, int H, int N, int d_r, int d_v, int K, const gma_options *options,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Causal GMA forward that continues a prefix ([GMA, causal variant, Eq. (8b)]):
+ * the prefix memories start from a carried-in memory instead of zero,
+ *   Vt^(i) = Vt_in + sum_{j<=i} gamma^K_j V_j,  Z^(i) = Z_in + sum_{j<=i} gamma^K_j,
+ *   O_i    = Gamma^Q_i Vt^(i) / (Gamma^Q_i Z^(i) + eps),
+ * and the prefix after the last position (Vt^(N-1), Z^(N-1)) is written to
+ * (Vt_out, Z_out) when they are given.  Vt_in / Vt_out : [B, H, K, d_v] fp32,
+ * Z_in / Z_out : [B, H, K] fp32; Vt_in and Z_in are both NULL (an empty prefix)
+ * or both given, and so are Vt_out and Z_out.  Uses: a sequence sharded over N
+ * (shard r starts from the sum of the memories of shards 0..r-1), a long prompt
+ * processed in pieces, and priming gma_decode_step.  Runs on the CUDA cores
+ * (options->path GMA_PATH_AUTO or GMA_PATH_SIMT).  Alignment and overlap rules
+ * as for gma_forward_causal, plus: the carry buffers start on a 16-byte
+ * boundary and the outputs (O, Vt_out, Z_out) overlap no input, each other or
+ * the workspace.  Workspace bytes: gma_causal_carry_workspace_size.
+ */
+size_t gma_causal_carry_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype);
+gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
+                                    const float *mu, const float *sigma2, const float *log_pi, float eps,
+                                    const float *Vt_in, const float *Z_in, float *Vt_out, float *Z_out,
+                                    void *O, int B, int H, int N, int d_r, int d_v, int K,
+                                    const gma_options *options, void *workspace, size_t workspace_bytes,
+                                    void *stream);
+
+/*
  * Number of stages (kernel launches, plus the status reset of the first) of
  * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
  * `variant` (-1 responsibilities, 0 bidirectional, 1 causal, 2 bidirectional
  * backward, 3 causal backward, 4 latent memory, 5 decode step, 6 routing
- * statistics -- variants 2 to 6 SIMT only), and the name of
+ * statistics, 7 read from a memory, 8 causal forward with a carried-in prefix
+ * -- variants 2 to 8 SIMT only), and the name of
  * stage j (NULL if out of range).
  * Used with gma_options.stage_events.
  */

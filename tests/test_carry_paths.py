@@ -1,0 +1,106 @@
+"""GPU vs fp64 oracle for the two entry points that split the forward at the
+latent memory -- gma_read_memory (Eq. 7 from a given memory) and
+gma_forward_causal_carry (causal forward from a carried-in prefix, returning
+the prefix after its last position) -- and for sequence sharding over N
+emulated on one GPU: P shards run one after the other through the CUDA path,
+their memories combined in shard order by the functions the multi-rank path
+uses, against the unsharded oracle forward."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import gaussian_mixture_latent_diag_gb300 as gma
+from gaussian_mixture_latent_diag_gb300 import sharded
+from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+from gpu_helpers import to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4  # fp32 arithmetic on exact inputs, max |x - x_ref| / RMS(x_ref)
+
+
+def _rel(gpu, ref) -> float:
+    g = gpu.detach().to("cpu", torch.float64).numpy()
+    return float(np.max(np.abs(g - ref)) / np.sqrt(np.mean(ref ** 2)))
+
+
+SHAPES = [  # (B, H, N, d_r, d_v, K)
+    (2, 3, 300, 16, 32, 8),
+    (1, 2, 517, 64, 64, 64),
+    (1, 1, 200, 128, 128, 128),
+    (2, 1, 70, 32, 16, 1),
+]
+
+
+def _case(shape, dtype):
+    B, H, N, d_r, d_v, K = shape
+    return Case(f"carry_{dtype}_{B}_{H}_{N}_{d_r}_{d_v}_{K}", True, B, H, N, d_r, d_v, K, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%d_H%d_N%d_r%d_v%d_K%d" % s)
+def test_read_memory_matches_oracle(shape, dtype):
+    import oracle
+    case = _case(shape, dtype)
+    inp = make_inputs(case, seed=zlib.crc32(case.name.encode()) % 1000)
+    d = to_dev(inp)
+    g = torch.Generator().manual_seed(3)
+    B, H, N, d_r, d_v, K = shape
+    Vt = torch.randn(B, H, K, d_v, generator=g, dtype=torch.float64) * 20
+    Z = torch.rand(B, H, K, generator=g, dtype=torch.float64) * 40
+    Vt32, Z32 = Vt.float(), Z.float()
+    O = gma.read_memory(d["Q"], d["mu"], d["sigma2"], d["log_pi"], Vt32.cuda(), Z32.cuda(), eps=case.eps,
+                        sync_status=True)
+    ref = oracle.read_memory(inp["Q"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps, Vt32, Z32)
+    assert _rel(O, ref) <= TOL
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%d_H%d_N%d_r%d_v%d_K%d" % s)
+def test_causal_carry_continues_a_prefix(shape, dtype):
+    """The first N0 positions through gma_forward_causal_carry from an empty
+    prefix, the rest from the returned state: both blocks equal the oracle's
+    causal rows and the final state equals the oracle's latent memory."""
+    import oracle
+    case = _case(shape, dtype)
+    inp = make_inputs(case, seed=zlib.crc32(case.name.encode()) % 1000 + 1)
+    d = to_dev(inp)
+    N = shape[2]
+    N0 = N // 3 + 1
+    prm = (d["mu"], d["sigma2"], d["log_pi"])
+    blk = lambda a, b: [d[n][:, :, a:b].contiguous() for n in ("Q", "K", "V")]  # noqa: E731
+    O1, vt, z = gma.forward_causal_carry(*blk(0, N0), *prm, eps=case.eps, sync_status=True)
+    O2, vt2, z2 = gma.forward_causal_carry(*blk(N0, N), *prm, Vt_in=vt, Z_in=z, eps=case.eps, sync_status=True)
+    ref = oracle.forward_causal(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps)
+    assert _rel(torch.cat([O1, O2], dim=2), ref) <= TOL
+    Vt_ref, Z_ref = oracle.latent_memory(inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"])
+    assert _rel(vt2, Vt_ref) <= TOL and _rel(z2, Z_ref) <= TOL
+    # an empty carried-in prefix is the plain causal forward
+    O0, _, _ = gma.forward_causal_carry(d["Q"], d["K"], d["V"], *prm, eps=case.eps, want_state=False,
+                                        sync_status=True)
+    Os = gma.forward_causal(d["Q"], d["K"], d["V"], *prm, eps=case.eps, path=gma.PATH_SIMT, sync_status=True)
+    assert torch.equal(O0, Os)
+
+
+@pytest.mark.parametrize("P", [2, 5])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sharded_over_n_emulated_on_one_gpu(P, dtype):
+    import oracle
+    case = Case(f"shard_gpu_{dtype}", True, 2, 2, 700, 64, 64, 64, dtype)
+    inp = make_inputs(case, seed=21)
+    d = to_dev(inp)
+    prm = (d["mu"], d["sigma2"], d["log_pi"])
+    cuts = np.linspace(0, case.N, P + 1).astype(int)
+    cuts[1] += 3  # uneven shards
+    ops = sharded.CudaOps()
+    blocks = [[d[n][:, :, a:b].contiguous() for n in ("Q", "K", "V")] for a, b in zip(cuts[:-1], cuts[1:])]
+    parts = [ops.latent_memory(k, v, *prm) for _, k, v in blocks]
+    Vt, Z = sharded.combine_total(parts)
+    Ob = torch.cat([ops.read_memory(q, *prm, Vt, Z, case.eps) for q, _, _ in blocks], dim=2)
+    Oc = torch.cat([ops.forward_causal_carry(q, k, v, *prm, *sharded.combine_exclusive(parts, r), case.eps)
+                    for r, (q, k, v) in enumerate(blocks)], dim=2)
+    args = (inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps)
+    assert _rel(Ob, oracle.forward_bidir(*args)) <= TOL
+    assert _rel(Oc, oracle.forward_causal(*args)) <= TOL
