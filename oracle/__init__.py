@@ -20,6 +20,8 @@ Linear-Time Sequence Mixing via Probabilistic Latent Routing" (arXiv
 * ``latent_memory``                  -- Eqs. (5)-(6): Vt, Z of a key/value sequence
 * ``read_memory``                    -- Eq. (7) from a given memory (Vt, Z)
 * ``decode_step`` / ``decode``        -- Eq. (8b) one position at a time (carried Vt, Z)
+* ``reparameterize`` (+ ``_backward``) -- Eqs. (14)-(15): sigma2 = softplus(omega) + eps,
+  log pi = log_softmax(alpha), and the chain rule through them
 * ``routing_stats``                  -- component usage, hard assignments, usage entropy
   (the introduction's usage / hard-assignment diagnostics)
 
@@ -106,6 +108,12 @@ def _load(mutant: int = 0):
             lib.gma_oracle_read_memory.argtypes = [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
                                                    _D, ctypes.c_int, ctypes.c_double, _D, _D, _D]
             lib.gma_oracle_read_memory.restype = None
+            lib.gma_oracle_reparameterize.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                      _D, _D]
+            lib.gma_oracle_reparameterize.restype = None
+            lib.gma_oracle_reparameterize_backward.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, _D, _D, _D,
+                                                               _D]
+            lib.gma_oracle_reparameterize_backward.restype = None
             _libs[mutant] = lib
     return lib
 
@@ -395,6 +403,43 @@ def routing_stats(X, mu, sigma2, log_pi) -> dict:
     return {"usage": usage.reshape(lead + (K,)), "counts": counts.reshape(lead + (K,)),
             "z": z.reshape(lead + (N,)), "entropy": st[:, 0].reshape(lead),
             "entropy_norm": st[:, 1].reshape(lead), "used": st[:, 2].astype(np.int64).reshape(lead)}
+
+
+def reparameterize(omega, alpha, eps_sigma=1e-3):
+    """([GMA, Eqs. 14-15]) sigma2 = softplus(omega) + eps_sigma, log_pi =
+    log_softmax(alpha), per head: omega [H, K, d_r], alpha [H, K] (a 2-D omega
+    with a 1-D alpha is one head)."""
+    lib = _load(_ACTIVE[0])
+    omega, alpha = _f64(omega), _f64(alpha)
+    one = omega.ndim == 2
+    if one:
+        omega, alpha = omega[None], alpha[None]
+    H, K, d_r = omega.shape
+    s2, lp = np.empty_like(omega), np.empty_like(alpha)
+    for h in range(H):
+        w, a = np.ascontiguousarray(omega[h]), np.ascontiguousarray(alpha[h])
+        s_h, l_h = np.empty((K, d_r)), np.empty(K)
+        lib.gma_oracle_reparameterize(_p(w), _p(a), K, d_r, float(eps_sigma), _p(s_h), _p(l_h))
+        s2[h], lp[h] = s_h, l_h
+    return (s2[0], lp[0]) if one else (s2, lp)
+
+
+def reparameterize_backward(omega, alpha, dsigma2, dlog_pi):
+    """Gradients of reparameterize: (domega, dalpha) for upstream (dsigma2, dlog_pi)."""
+    lib = _load(_ACTIVE[0])
+    omega, alpha, dsigma2, dlog_pi = _f64(omega), _f64(alpha), _f64(dsigma2), _f64(dlog_pi)
+    one = omega.ndim == 2
+    if one:
+        omega, alpha, dsigma2, dlog_pi = omega[None], alpha[None], dsigma2[None], dlog_pi[None]
+    H, K, d_r = omega.shape
+    dw, da = np.empty_like(omega), np.empty_like(alpha)
+    for h in range(H):
+        w, a = np.ascontiguousarray(omega[h]), np.ascontiguousarray(alpha[h])
+        gs, gl = np.ascontiguousarray(dsigma2[h]), np.ascontiguousarray(dlog_pi[h])
+        dw_h, da_h = np.empty((K, d_r)), np.empty(K)
+        lib.gma_oracle_reparameterize_backward(_p(w), _p(a), K, d_r, _p(gs), _p(gl), _p(dw_h), _p(da_h))
+        dw[h], da[h] = dw_h, da_h
+    return (dw[0], da[0]) if one else (dw, da)
 
 
 class use_mutant:

@@ -669,3 +669,50 @@ void gma_oracle_read_memory(const double *Q, int N, int d_r, int d_v, const doub
     }
     free(gq);
 }
+
+/*
+ * Reparameterised mixture parameters of one head ([GMA, Eqs. 14-15]):
+ *   sigma2_kj = log(1 + exp(omega_kj)) + eps_sigma        (softplus, Eq. 14)
+ *   pi_k      = exp(alpha_k) / sum_l exp(alpha_l)          (softmax, Eq. 15)
+ * returned as log_pi_k = alpha_k - log sum_l exp(alpha_l).  The softplus is
+ * evaluated as max(w, 0) + log1p(exp(-|w|)) and the log-sum-exp with the
+ * maximum taken out, which are the same functions without overflow.
+ */
+void gma_oracle_reparameterize(const double *omega, const double *alpha, int K, int d_r,
+                               double eps_sigma, double *sigma2, double *log_pi)
+{
+    for (int e = 0; e < K * d_r; ++e) {
+        double w = omega[e];
+        sigma2[e] = (w > 0.0 ? w : 0.0) + log1p(exp(-fabs(w))) + eps_sigma;
+    }
+    double m = alpha[0];
+    for (int k = 1; k < K; ++k)
+        if (alpha[k] > m) m = alpha[k];
+    double z = 0.0;
+    for (int k = 0; k < K; ++k) z += exp(alpha[k] - m);
+    double lse = m + log(z);
+    for (int k = 0; k < K; ++k) log_pi[k] = alpha[k] - lse;
+}
+
+/*
+ * Chain rule through the reparameterisations (the gradient appendix's
+ * reparameterised means, covariances and prior logits):
+ *   d omega_kj = d sigma2_kj * sigmoid(omega_kj)          (d softplus / d w = sigmoid(w))
+ *   d alpha_k  = d log_pi_k - pi_k * sum_l d log_pi_l      (Jacobian of log-softmax)
+ */
+void gma_oracle_reparameterize_backward(const double *omega, const double *alpha, int K, int d_r,
+                                        const double *dsigma2, const double *dlog_pi,
+                                        double *domega, double *dalpha)
+{
+    for (int e = 0; e < K * d_r; ++e) {
+        double w = omega[e];
+        double sg = w >= 0.0 ? 1.0 / (1.0 + exp(-w)) : exp(w) / (1.0 + exp(w));
+        domega[e] = dsigma2[e] * sg;
+    }
+    double m = alpha[0];
+    for (int k = 1; k < K; ++k)
+        if (alpha[k] > m) m = alpha[k];
+    double z = 0.0, g = 0.0;
+    for (int k = 0; k < K; ++k) { z += exp(alpha[k] - m); g += dlog_pi[k]; }
+    for (int k = 0; k < K; ++k) dalpha[k] = dlog_pi[k] - exp(alpha[k] - m) / z * g;
+}

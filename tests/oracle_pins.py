@@ -445,4 +445,47 @@ def pin_stats_single_component():
     assert st["entropy"] == 0.0 and st["entropy_norm"] == 1.0 and st["used"] == 1
 
 
+# ---------------------------------------------------------------- reparameterisation (Eqs. 14-15)
+
+def pin_reparameterize_matches_torch_and_scipy():
+    """sigma2 = torch softplus(omega) + eps (fp64) and log_pi = scipy
+    log_softmax(alpha); extreme omega (+-80) neither overflows nor loses the
+    identity softplus(w) - softplus(-w) = w."""
+    import torch
+    from scipy.special import log_softmax
+    rng = _rng(40)
+    omega = rng.normal(scale=3.0, size=(3, 5, 4))
+    omega[0, 0, :2] = [80.0, -80.0]
+    alpha = rng.normal(scale=4.0, size=(3, 5))
+    s2, lp = oracle.reparameterize(omega, alpha, 1e-3)
+    ref = torch.nn.functional.softplus(torch.from_numpy(omega)).numpy() + 1e-3
+    assert np.max(np.abs(s2 - ref) / ref) < 1e-14
+    assert np.max(np.abs(lp - log_softmax(alpha, axis=-1))) < 1e-13
+    s2n, _ = oracle.reparameterize(-omega, alpha, 0.0)
+    assert np.max(np.abs((s2 - 1e-3) - s2n - omega)) < 1e-12
+
+
+def pin_reparameterize_gradient_by_finite_differences():
+    """Chain rule through Eqs. 14-15 against central differences of a random
+    linear functional L = <G1, sigma2> + <G2, log_pi>; the prior-logit gradient
+    sums to zero (log_pi is invariant to a shift of alpha)."""
+    rng = _rng(41)
+    K, d_r, h = 6, 3, 1e-6
+    omega, alpha = rng.normal(size=(K, d_r)), rng.normal(size=K)
+    G1, G2 = rng.normal(size=(K, d_r)), rng.normal(size=K)
+    dw, da = oracle.reparameterize_backward(omega, alpha, G1, G2)
+
+    def L(w, a):
+        s2, lp = oracle.reparameterize(w, a, 1e-3)
+        return float((G1 * s2).sum() + (G2 * lp).sum())
+
+    for idx in [(0, 0), (3, 2), (5, 1)]:
+        e = np.zeros_like(omega); e[idx] = h
+        assert abs((L(omega + e, alpha) - L(omega - e, alpha)) / (2 * h) - dw[idx]) < 1e-8
+    for k in range(K):
+        e = np.zeros(K); e[k] = h
+        assert abs((L(omega, alpha + e) - L(omega, alpha - e)) / (2 * h) - da[k]) < 1e-8
+    assert abs(da.sum()) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
