@@ -527,6 +527,81 @@ def run_aux(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+PARAM_WORKLOAD = dict(H=32, K=128, d_r=128)
+PARAM_METRIC = "GMA parameter reparameterisation + its gradient, elements/s (H=32, K=128, d_r=128)"
+
+
+def run_params(args, rank: int, world: int, local_rank: int):
+    """--workload params: one gma_reparameterize and one gma_reparameterize_backward
+    (Eqs. 14-15 and their chain rule) per step over the largest parameter shape of
+    the workloads (H=32, K=d_r=128: 524288 covariance elements).  Algorithmic bytes
+    per covariance element: omega read and sigma2 written (8), then omega and
+    dsigma2 read and domega written (12) = 20 B; the priors are K per head.  The
+    two launches are latency-bound at this size."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    w = PARAM_WORKLOAD
+    H, K, d_r = w["H"], w["K"], w["d_r"]
+    g = torch.Generator().manual_seed(rank_seed(rank, 6))
+    omega = torch.randn(H, K, d_r, generator=g).to(dev)
+    alpha = torch.randn(H, K, generator=g).to(dev)
+    ds2 = torch.randn(H, K, d_r, generator=g).to(dev)
+    dlp = torch.randn(H, K, generator=g).to(dev)
+
+    def call():
+        gma.reparameterize(omega, alpha)
+        gma.reparameterize_backward(omega, alpha, ds2, dlp)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0.record(stream)
+        for _ in range(args.steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = job_ms(t0.elapsed_time(t1) / args.steps, world, dev)
+    units = H * K * d_r
+    alg = units * 20 + H * K * 4 * 5
+    peak, peak_src = measured_peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        oracle.build()
+        o_np, a_np, d_np, l_np = (t.double().cpu().numpy() for t in (omega, alpha, ds2, dlp))
+        t = time.perf_counter()
+        oracle.reparameterize(o_np, a_np, 1e-3)
+        oracle.reparameterize_backward(o_np, a_np, d_np, l_np)
+        secs = time.perf_counter() - t
+        cpu = {"value": units / secs, "unit": "elements/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole parameter set (H=32, K=d_r=128) through the fp64 C oracle, {secs:.3f} s"}
+    if rank == 0:
+        out = {"metric": PARAM_METRIC, "value": world * units / (ms / 1e3), "unit": "elements/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+               "config": {"workload": "GMA reparameterisation (Eqs. 14-15) forward + gradient, H=32 K=128 d_r=128",
+                          **w, "l2": "2 MB parameter set, L2-resident (latency-bound launches)",
+                          "parallelism": f"replicas x{world}"},
+               "gpu_launches": 2 * args.steps,
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                            "frac": achieved / peak, "traffic": None, "kernel": "both launches",
+                            "algorithmic_bytes": alg, "peak_source": peak_src},
+               "clocks": clocks.summary(), "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+
+
 def rank_seed(rank: int, variant: int) -> int:
     """Input seed of one variant on one rank: each rank draws its own heads (replicas
     of the workload shape, no data shared between ranks)."""
@@ -742,10 +817,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats"], default="forward",
+    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params"], default="forward",
                     help="forward: the bidirectional + causal forward step (default); "
                          "backward: the bidirectional + causal backward; decode: one causal decode "
-                         "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics")
+                         "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics; "
+                         "params: the reparameterisation and its gradient")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -763,6 +839,8 @@ def main():
             run_backward(args, rank, world, local_rank)
         elif args.workload in ("decode", "stats"):
             run_aux(args, rank, world, local_rank)
+        elif args.workload == "params":
+            run_params(args, rank, world, local_rank)
         else:
             run_gma(args, rank, world, local_rank)
     finally:

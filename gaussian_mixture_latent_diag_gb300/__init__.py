@@ -25,6 +25,7 @@ from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError
 
 __all__ = ["forward_bidir", "forward_causal", "backward_bidir", "backward_causal", "responsibilities",
            "latent_memory", "read_memory", "forward_causal_carry", "decode_step", "routing_stats",
+           "reparameterize", "reparameterize_backward",
            "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
            "PATH_TC", "load"]
@@ -386,3 +387,34 @@ def forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in=None, Z_in=None, eps
     if st != 0:
         raise GmaError(st, "gma_forward_causal_carry")
     return out, Vt_out, Z_out
+
+
+def reparameterize(omega, alpha, eps_sigma=1e-3, stream=None):
+    """Eqs. (14)-(15): (sigma2 = softplus(omega) + eps_sigma, log_pi = log_softmax(alpha))
+    for omega [H, K, d_r], alpha [H, K] fp32 CUDA tensors."""
+    import torch
+    _check_dev(omega, alpha)
+    H, K, d_r = omega.shape
+    if alpha.shape != (H, K) or omega.dtype != torch.float32 or alpha.dtype != torch.float32:
+        raise ValueError("omega must be fp32 [H, K, d_r] and alpha fp32 [H, K]")
+    sigma2, log_pi = torch.empty_like(omega), torch.empty_like(alpha)
+    st = load().gma_reparameterize(_ptr(omega), _ptr(alpha), H, K, d_r, float(eps_sigma), _ptr(sigma2),
+                                   _ptr(log_pi), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_reparameterize")
+    return sigma2, log_pi
+
+
+def reparameterize_backward(omega, alpha, dsigma2, dlog_pi, stream=None):
+    """Chain rule through reparameterize: (domega, dalpha)."""
+    import torch
+    _check_dev(omega, alpha, dsigma2, dlog_pi)
+    H, K, d_r = omega.shape
+    if alpha.shape != (H, K) or dsigma2.shape != omega.shape or dlog_pi.shape != alpha.shape:
+        raise ValueError("omega, dsigma2 must be [H, K, d_r] and alpha, dlog_pi [H, K]")
+    domega, dalpha = torch.empty_like(omega), torch.empty_like(alpha)
+    st = load().gma_reparameterize_backward(_ptr(omega), _ptr(alpha), _ptr(dsigma2), _ptr(dlog_pi), H, K, d_r,
+                                            _ptr(domega), _ptr(dalpha), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_reparameterize_backward")
+    return domega, dalpha

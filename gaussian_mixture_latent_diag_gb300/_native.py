@@ -28,7 +28,8 @@ EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_backward_causal", "gma_latent_memory_workspace_size", "gma_latent_memory",
             "gma_decode_workspace_size", "gma_decode_step", "gma_routing_stats_workspace_size",
             "gma_routing_stats", "gma_read_memory_workspace_size", "gma_read_memory",
-            "gma_causal_carry_workspace_size", "gma_forward_causal_carry")
+            "gma_causal_carry_workspace_size", "gma_forward_causal_carry", "gma_reparameterize",
+            "gma_reparameterize_backward")
 
 
 class Options(ctypes.Structure):
@@ -99,6 +100,10 @@ def load(path: str | None = None):
         lib.gma_forward_causal_carry.argtypes = [vp, vp, vp, i, vp, vp, vp, f, vp, vp, vp, vp, vp] + [i] * 6 + \
             [opt, vp, sz, vp]
         lib.gma_forward_causal_carry.restype = i
+        lib.gma_reparameterize.argtypes = [vp, vp, i, i, i, f, vp, vp, vp]
+        lib.gma_reparameterize.restype = i
+        lib.gma_reparameterize_backward.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp]
+        lib.gma_reparameterize_backward.restype = i
         lib.gma_last_device_status.argtypes = [vp, vp]
         lib.gma_last_device_status.restype = i
         lib.gma_status_string.argtypes = [i]

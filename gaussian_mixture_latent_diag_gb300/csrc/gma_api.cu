@@ -310,7 +310,7 @@ gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, 
 
 size_t gma_decode_workspace_size(int H, int d_r, int K) {
     if (!shape_ok(1, H, 1, d_r, 16, K, false)) return 0;
-    return gma::decode_workspace();
+    return gma::decode_workspace(H, K, d_r);
 }
 
 gma_status gma_decode_step(const void *q, const void *k, const void *v, gma_dtype dtype,
@@ -337,7 +337,7 @@ gma_status gma_decode_step(const void *q, const void *k, const void *v, gma_dtyp
     p.Q = q; p.Kx = k; p.V = v; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = o;
     p.dtype = dtype; p.eps = eps;
     p.B = B; p.H = H; p.N = 1; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    const size_t need = gma::decode_workspace();
+    const size_t need = gma::decode_workspace(H, K, d_r);
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     const size_t bh = (size_t)B * H;
     const size_t nvt = 4 * bh * K * d_v, nz = 4 * bh * K, no = 4 * bh * d_v;
@@ -492,6 +492,48 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gma::StageClock clk = clock_for(options, s);
     return finish(gma::simt_causal_carry(p, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk), options, workspace, s);
+}
+
+gma_status gma_reparameterize(const float *omega, const float *alpha, int H, int K, int d_r, float eps_sigma,
+                              float *sigma2, float *log_pi, void *stream) {
+    if (!omega || !alpha || !sigma2 || !log_pi) return GMA_ERR_INVALID_ARG;
+    if (!(eps_sigma > 0.f) || !std::isfinite(eps_sigma)) return GMA_ERR_INVALID_ARG;
+    const void *al[] = {omega, alpha, sigma2, log_pi};
+    for (const void *ptr : al)
+        if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(1, H, 1, d_r, 16, K, false)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    const size_t np = 4 * (size_t)H * K * d_r, nl = 4 * (size_t)H * K;
+    if (overlaps(sigma2, np, omega, np) || overlaps(sigma2, np, alpha, nl) || overlaps(log_pi, nl, omega, np) ||
+        overlaps(log_pi, nl, alpha, nl) || overlaps(sigma2, np, log_pi, nl))
+        return GMA_ERR_INVALID_ARG;
+    if (gma::reparameterize(omega, alpha, H, K, d_r, eps_sigma, sigma2, log_pi, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return GMA_ERR_CUDA;
+    }
+    return GMA_OK;
+}
+
+gma_status gma_reparameterize_backward(const float *omega, const float *alpha, const float *dsigma2,
+                                       const float *dlog_pi, int H, int K, int d_r, float *domega,
+                                       float *dalpha, void *stream) {
+    if (!omega || !alpha || !dsigma2 || !dlog_pi || !domega || !dalpha) return GMA_ERR_INVALID_ARG;
+    const void *al[] = {omega, alpha, dsigma2, dlog_pi, domega, dalpha};
+    for (const void *ptr : al)
+        if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return GMA_ERR_INVALID_ARG;
+    if (!shape_ok(1, H, 1, d_r, 16, K, false)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    const size_t np = 4 * (size_t)H * K * d_r, nl = 4 * (size_t)H * K;
+    const void *in[] = {omega, alpha, dsigma2, dlog_pi};
+    const size_t nin[] = {np, nl, np, nl};
+    for (int b = 0; b < 4; ++b)
+        if (overlaps(domega, np, in[b], nin[b]) || overlaps(dalpha, nl, in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+    if (overlaps(domega, np, dalpha, nl)) return GMA_ERR_INVALID_ARG;
+    if (gma::reparameterize_backward(omega, alpha, dsigma2, dlog_pi, H, K, d_r, domega, dalpha,
+                                     static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GMA_ERR_CUDA;
+    }
+    return GMA_OK;
 }
 
 gma_status gma_last_device_status(const void *workspace, void *stream) {

@@ -106,9 +106,10 @@ extern const char *const kBackwardStages[2][8];  // [causal][j], NULL-terminated
 // ---------------------------------------------------------------- decode step (gma_decode.cu)
 // One causal position for every (b, h): q, k [BH][d_r], v [BH][d_v] (p.Q, p.Kx,
 // p.V), carried state Vt [BH][K][d_v], Z [BH][K] updated in place, output p.O
-// [BH][d_v].  Workspace: decode_workspace() bytes (the status word).  Stages:
-// reset (status word), step.
-size_t decode_workspace();
+// [BH][d_v].  Workspace: decode_workspace(H, K, d_r) bytes (the status word and
+// the per-head constants of the log-density).  Stages: prep (per-head
+// constants, validation, status reset), step.
+size_t decode_workspace(int H, int K, int d_r);
 cudaError_t simt_decode_step(const Problem &p, float *Vt, float *Z, void *ws, cudaStream_t s, StageClock &clk);
 
 // ---------------------------------------------------------------- usage diagnostics (gma_stats.cu)
@@ -125,6 +126,13 @@ cudaError_t simt_routing_stats(const Problem &p, const StatsArgs &a, void *ws, c
 // [2] routing statistics, [3] read from a memory, [4] causal forward with a
 // carried-in prefix; NULL-terminated.
 extern const char *const kAuxStages[5][8];
+
+// ---------------------------------------------------------------- parameters (gma_param.cu)
+cudaError_t reparameterize(const float *omega, const float *alpha, int H, int K, int d_r, float eps_sigma,
+                           float *sigma2, float *log_pi, cudaStream_t s);
+cudaError_t reparameterize_backward(const float *omega, const float *alpha, const float *dsigma2,
+                                    const float *dlog_pi, int H, int K, int d_r, float *domega, float *dalpha,
+                                    cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);

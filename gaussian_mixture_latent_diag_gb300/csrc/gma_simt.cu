@@ -41,32 +41,50 @@ __device__ __forceinline__ void set_status(unsigned *status, unsigned code) {
 // Per-head constants of the centred log-density ([GMA, Eqs. (2)-(3)]):
 //   s_ik = c'_k - 1/2 sum_j (x_j - mu_kj)^2 * inv_kj,
 //   inv_kj = 1 / sigma2_kj,  c'_k = log pi_k - 1/2 sum_j log sigma2_kj.
-// Also validates the parameter values.
-__global__ void prep_simt_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
+// Also validates the parameter values.  The logs are taken in the coalesced
+// pass over the elements and kept in shared memory (rows padded to d_r + 1
+// floats, so the threads, one per component, read distinct banks); thread k
+// then sums its component's log-determinant in fp32 as hi + lo, carrying every
+// rounding error in lo (TwoSum, Knuth): a plain fp32 sum of up to 128 terms
+// would lose the fp32 tolerance, and fp64 arithmetic is slow on this GPU.
+constexpr int kPrepThreads = 512;  // many loads in flight: only H CTAs run
+
+__global__ void __launch_bounds__(kPrepThreads) prep_simt_kernel(const float *__restrict__ mu, const float *__restrict__ sigma2,
                                  const float *__restrict__ log_pi, int K, int d_r,
                                  float *__restrict__ inv, float *__restrict__ cprime,
                                  unsigned *status) {
+    extern __shared__ float slog[];  // [K][d_r + 1]
     const int h = blockIdx.x;
     const size_t base = (size_t)h * K * d_r;
+#pragma unroll 4
     for (int e = threadIdx.x; e < K * d_r; e += blockDim.x) {
         float s2 = sigma2[base + e], m = mu[base + e];
         if (!(s2 > 0.f) || !isfinite(s2) || !isfinite(m)) set_status(status, GMA_ERR_NONFINITE_PARAM);
         inv[base + e] = 1.0f / s2;
+        slog[(e / d_r) * (d_r + 1) + e % d_r] = logf(s2);
     }
+    __syncthreads();
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        double acc = 0.0;
-        for (int j = 0; j < d_r; ++j) acc += (double)logf(sigma2[base + (size_t)k * d_r + j]);
+        float hi = 0.f, lo = 0.f;
+        for (int j = 0; j < d_r; ++j) {
+            const float y = slog[k * (d_r + 1) + j];
+            const float t = hi + y, bb = t - hi;
+            lo += (hi - (t - bb)) + (y - bb);
+            hi = t;
+        }
         float lp = log_pi[(size_t)h * K + k];
         if (!isfinite(lp)) set_status(status, GMA_ERR_NONFINITE_PARAM);
-        cprime[(size_t)h * K + k] = (float)((double)lp - 0.5 * acc);
+        cprime[(size_t)h * K + k] = (lp - 0.5f * hi) - 0.5f * lo;
     }
 }
 
 // One thread per row: scores, then a max-subtracted softmax over k
 // ([GMA, Eq. (3)]).  The row is written three times to `out` (scores,
 // exponentials, normalised values); each thread only touches its own row.
-// The head's (mu, 1/sigma2) are staged in shared memory 32 components at a
-// time; every thread of the block takes part in the staging.
+// The head's parameters are staged in shared memory 32 components at a time as
+// float4 {-mu_j, -mu_j+1, 1/sigma2_j, 1/sigma2_j+1}; every thread of the block
+// takes part in the staging.  The score arithmetic runs on packed f32x2 pairs
+// (j, j + 1), which round each element as the scalar operations would.
 constexpr int kRespKC = 32;
 template <int D_R, typename T>
 __global__ void __launch_bounds__(128) resp_simt_kernel(
@@ -75,14 +93,15 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
     long long out_bh_stride, long long out_stride_n, long long out_stride_k,
     const unsigned *status) {
     if (failed(status)) return;
-    __shared__ float2 sp[kRespKC][D_R];
+    constexpr int D2 = D_R / 2;
+    __shared__ float4 sp[kRespKC][D2];
     const int bh = blockIdx.y, h = bh % H;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = i < N;
-    float x[D_R];
+    float2 x[D2];
     const T *xr = X + ((size_t)bh * N + (valid ? i : 0)) * D_R;
 #pragma unroll
-    for (int j = 0; j < D_R; ++j) x[j] = to_f32(xr[j]);
+    for (int j2 = 0; j2 < D2; ++j2) x[j2] = make_float2(to_f32(xr[2 * j2]), to_f32(xr[2 * j2 + 1]));
     const float *muh = mu + (size_t)h * K * D_R;
     const float *invh = inv + (size_t)h * K * D_R;
     const float *ch = cprime + (size_t)h * K;
@@ -92,24 +111,27 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
     for (int k0 = 0; k0 < K; k0 += kRespKC) {
         const int nk = min(kRespKC, K - k0);
         __syncthreads();
-        for (int e = threadIdx.x; e < nk * D_R; e += blockDim.x)
-            sp[e / D_R][e % D_R] = make_float2(muh[(size_t)k0 * D_R + e], invh[(size_t)k0 * D_R + e]);
+        for (int e = threadIdx.x; e < nk * D2; e += blockDim.x) {
+            const size_t o2 = (size_t)k0 * D_R + 2 * (size_t)e;
+            sp[e / D2][e % D2] = make_float4(-muh[o2], -muh[o2 + 1], invh[o2], invh[o2 + 1]);
+        }
         __syncthreads();
         if (!valid) continue;
         for (int kk = 0; kk < nk; ++kk) {
-            // Eight interleaved partial sums, combined without rounding error
-            // into hi + lo (TwoSum, Knuth): the terms are positive and the total
-            // reaches several hundred at d_r = 128, where one sequential fp32 sum
-            // loses the fp32 tolerance.
-            float q8[8];
+            // Eight interleaved partial sums (j mod 8, two per packed register),
+            // combined without rounding error into hi + lo (TwoSum, Knuth): the
+            // terms are positive and the total reaches several hundred at
+            // d_r = 128, where one sequential fp32 sum loses the fp32 tolerance.
+            float2 acc[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) q8[u] = 0.f;
+            for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < D_R; ++j) {
-                const float2 mv = sp[kk][j];
-                float d = x[j] - mv.x;
-                q8[j & 7] = fmaf(d * d, mv.y, q8[j & 7]);
+            for (int j2 = 0; j2 < D2; ++j2) {
+                const float4 pv = sp[kk][j2];
+                const float2 d = __fadd2_rn(x[j2], make_float2(pv.x, pv.y));
+                acc[j2 & 3] = __ffma2_rn(__fmul2_rn(d, d), make_float2(pv.z, pv.w), acc[j2 & 3]);
             }
+            const float q8[8] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y, acc[2].x, acc[2].y, acc[3].x, acc[3].y};
             float hi = q8[0], lo = 0.f;
 #pragma unroll
             for (int u = 1; u < 8; ++u) {
@@ -480,7 +502,10 @@ Ptrs ptrs(const SimtLayout &L, void *ws) {
 
 cudaError_t prep(const Problem &p, const Ptrs &P, cudaStream_t s) {
     GMA_TRY(cudaMemsetAsync(P.status, 0, sizeof(unsigned), s));
-    prep_simt_kernel<<<p.H, 128, 0, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, P.inv, P.cprime, P.status);
+    const size_t smem = sizeof(float) * (size_t)p.K * (p.d_r + 1);
+    if (smem > 48 * 1024)  // above the default limit only: the call costs host time
+        GMA_TRY(cudaFuncSetAttribute(prep_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    prep_simt_kernel<<<p.H, kPrepThreads, smem, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, P.inv, P.cprime, P.status);
     return cudaGetLastError();
 }
 

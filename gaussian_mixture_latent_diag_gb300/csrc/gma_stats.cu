@@ -53,8 +53,10 @@ StatsLayout stats_layout(const Problem &p) {
 }
 
 // grid (nblk, BH), kStatRows threads.  Dynamic shared memory: the parameter
-// stage [kStatKC][D_R] float2 (mu, 1/sigma2), the CTA's scores / responsibilities
-// [kStatRows][K + 1] and the rows' argmax [kStatRows].
+// stage [kStatKC][D_R / 2] float4 {-mu_j, -mu_j+1, 1/sigma2_j, 1/sigma2_j+1}, the
+// CTA's scores / responsibilities [kStatRows][K + 1] and the rows' argmax
+// [kStatRows].  The score arithmetic runs on packed f32x2 pairs (j, j + 1),
+// which round each element as the scalar operations would.
 template <int D_R, typename T>
 __global__ void __launch_bounds__(kStatRows) stats_rows_kernel(
     const T *__restrict__ X, int H, int N, int K, const float *__restrict__ mu, const float *__restrict__ inv,
@@ -62,7 +64,8 @@ __global__ void __launch_bounds__(kStatRows) stats_rows_kernel(
     int *__restrict__ z, const unsigned *status) {
     if (failed(status)) return;
     extern __shared__ float smem[];
-    float2 *sp = reinterpret_cast<float2 *>(smem);  // [kStatKC][D_R]
+    constexpr int D2 = D_R / 2;
+    float4 *sp = reinterpret_cast<float4 *>(smem);  // [kStatKC][D2]
     float *sgam = smem + 2 * kStatKC * D_R;         // [kStatRows][K + 1]
     int *sz = reinterpret_cast<int *>(sgam + kStatRows * (K + 1));
     const int KP = K + 1;
@@ -71,10 +74,10 @@ __global__ void __launch_bounds__(kStatRows) stats_rows_kernel(
     const bool valid = i < N;
     const int nvalid = min(kStatRows, N - blk * kStatRows);
 
-    float x[D_R];
+    float2 x[D2];
     const T *xr = X + ((size_t)bh * N + (valid ? i : 0)) * D_R;
 #pragma unroll
-    for (int j = 0; j < D_R; ++j) x[j] = to_f32(xr[j]);
+    for (int j2 = 0; j2 < D2; ++j2) x[j2] = make_float2(to_f32(xr[2 * j2]), to_f32(xr[2 * j2 + 1]));
     const float *muh = mu + (size_t)h * K * D_R, *invh = inv + (size_t)h * K * D_R;
     const float *ch = cprime + (size_t)h * K;
     float *row = sgam + r * KP;
@@ -84,21 +87,25 @@ __global__ void __launch_bounds__(kStatRows) stats_rows_kernel(
     for (int k0 = 0; k0 < K; k0 += kStatKC) {
         const int nk = min(kStatKC, K - k0);
         __syncthreads();
-        for (int e = threadIdx.x; e < nk * D_R; e += kStatRows)
-            sp[e] = make_float2(muh[(size_t)k0 * D_R + e], invh[(size_t)k0 * D_R + e]);
+        for (int e = threadIdx.x; e < nk * D2; e += kStatRows) {
+            const size_t o = (size_t)k0 * D_R + 2 * (size_t)e;
+            sp[e] = make_float4(-muh[o], -muh[o + 1], invh[o], invh[o + 1]);
+        }
         __syncthreads();
         if (!valid) continue;
         for (int kk = 0; kk < nk; ++kk) {
-            // centred form, eight partial sums combined exactly (TwoSum)
-            float q8[8];
+            // centred form, eight partial sums (j mod 8, two per packed
+            // register) combined exactly (TwoSum)
+            float2 acc[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) q8[u] = 0.f;
+            for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < D_R; ++j) {
-                const float2 mv = sp[kk * D_R + j];
-                const float d = x[j] - mv.x;
-                q8[j & 7] = fmaf(d * d, mv.y, q8[j & 7]);
+            for (int j2 = 0; j2 < D2; ++j2) {
+                const float4 pv = sp[kk * D2 + j2];
+                const float2 d = __fadd2_rn(x[j2], make_float2(pv.x, pv.y));
+                acc[j2 & 3] = __ffma2_rn(__fmul2_rn(d, d), make_float2(pv.z, pv.w), acc[j2 & 3]);
             }
+            const float q8[8] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y, acc[2].x, acc[2].y, acc[3].x, acc[3].y};
             float hi = q8[0], lo = 0.f;
 #pragma unroll
             for (int u = 1; u < 8; ++u) {

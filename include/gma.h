@@ -272,9 +272,10 @@ gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, 
  * start on a 16-byte boundary and the workspace on a 256-byte boundary; Vt, Z and o
  * may not overlap an input, each other or the workspace (GMA_ERR_INVALID_ARG).
  * Invalid parameter values are reported through the status word as for the
- * forward; the rows of a head with an invalid value are left unchanged (Vt, Z
- * and o), the other heads are updated.  The workspace
- * (gma_decode_workspace_size bytes, independent of B) holds the status word.
+ * forward; the (b, h) rows of a head with an invalid value are left unchanged
+ * (Vt, Z and o), the other heads are updated.  The workspace
+ * (gma_decode_workspace_size bytes, independent of B) holds the status word and
+ * the per-head constants of the log-density.
  */
 size_t gma_decode_workspace_size(int H, int d_r, int K);
 gma_status gma_decode_step(const void *q, const void *k, const void *v, gma_dtype dtype,
@@ -352,6 +353,26 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
                                     void *O, int B, int H, int N, int d_r, int d_v, int K,
                                     const gma_options *options, void *workspace, size_t workspace_bytes,
                                     void *stream);
+
+/*
+ * Reparameterised mixture parameters ([GMA, Eqs. (14)-(15)]), per head h:
+ *   sigma2[h,k,j] = log(1 + exp(omega[h,k,j])) + eps_sigma   (softplus: positive covariances)
+ *   log_pi[h,k]   = alpha[h,k] - log sum_l exp(alpha[h,l])   (log of the softmax priors)
+ *   omega, sigma2 : [H, K, d_r] fp32   alpha, log_pi : [H, K] fp32
+ * and the chain rule through them, for upstream gradients dsigma2, dlog_pi
+ * (e.g. from gma_backward_bidir / gma_backward_causal):
+ *   domega = dsigma2 * sigmoid(omega),  dalpha_k = dlog_pi_k - pi_k sum_l dlog_pi_l.
+ * The outputs feed the forward entry points directly.  Device pointers, 4-byte
+ * aligned; outputs may not overlap inputs (GMA_ERR_INVALID_ARG); eps_sigma must
+ * be finite and > 0.  No workspace.  Sizes: H >= 1, 1 <= K <= 128, d_r in
+ * {16, 32, 64, 128}.  Non-finite omega or alpha give non-finite outputs, which
+ * the forward entry points then reject (GMA_ERR_NONFINITE_PARAM).
+ */
+gma_status gma_reparameterize(const float *omega, const float *alpha, int H, int K, int d_r, float eps_sigma,
+                              float *sigma2, float *log_pi, void *stream);
+gma_status gma_reparameterize_backward(const float *omega, const float *alpha, const float *dsigma2,
+                                       const float *dlog_pi, int H, int K, int d_r, float *domega,
+                                       float *dalpha, void *stream);
 
 /*
  * Number of stages (kernel launches, plus the status reset of the first) of

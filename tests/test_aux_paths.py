@@ -117,7 +117,8 @@ def test_decode_step_against_oracle_step_from_random_state():
 
 def test_decode_invalid_parameters_leave_that_head_unchanged():
     """An invalid sigma2 in head 1: the call reports GMA_ERR_NONFINITE_PARAM and
-    leaves head 1's state untouched; head 0 is still updated."""
+    leaves head 1's rows untouched; head 0 is still updated.  The next valid
+    call on the same workspace reports GMA_OK again."""
     B, H, d_r, d_v, K = 9, 2, 32, 32, 16
     q = torch.randn(B, H, d_r, device="cuda")
     v = torch.randn(B, H, d_v, device="cuda")
@@ -133,6 +134,11 @@ def test_decode_invalid_parameters_leave_that_head_unchanged():
     assert e.value.status == 6
     assert torch.equal(Vt[:, 1], Vt0[:, 1]) and torch.equal(Z[:, 1], Z0[:, 1])
     assert not torch.equal(Z[:, 0], Z0[:, 0])
+    ws = torch.empty(int(gma.load().gma_decode_workspace_size(H, d_r, K)), dtype=torch.uint8, device="cuda")
+    with pytest.raises(gma.GmaError):
+        gma.decode_step(q, q.clone(), v, mu, s2, lp, Vt, Z, workspace=ws, sync_status=True)
+    s2[1, 3, 5] = 1.0
+    gma.decode_step(q, q.clone(), v, mu, s2, lp, Vt, Z, workspace=ws, sync_status=True)
 
 
 # ---------------------------------------------------------------- usage diagnostics

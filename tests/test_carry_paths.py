@@ -104,3 +104,47 @@ def test_sharded_over_n_emulated_on_one_gpu(P, dtype):
     args = (inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps)
     assert _rel(Ob, oracle.forward_bidir(*args)) <= TOL
     assert _rel(Oc, oracle.forward_causal(*args)) <= TOL
+
+
+# ---------------------------------------------------------------- reparameterisation (Eqs. 14-15)
+
+@pytest.mark.parametrize("shape", [(1, 1, 16), (3, 37, 32), (8, 128, 128)], ids=lambda s: "H%d_K%d_r%d" % s)
+def test_reparameterize_matches_oracle(shape):
+    """sigma2 = softplus(omega) + eps_sigma and log_pi = log_softmax(alpha) on the
+    GPU against the fp64 oracle (fp32 rounding: 1e-6 relative on sigma2, 2e-6 on
+    log_pi over max(1, |log_pi|)); extreme omega included.  The gradients of
+    both against the oracle's chain rule."""
+    import oracle
+    H, K, d_r = shape
+    g = torch.Generator().manual_seed(H * 1000 + K)
+    omega = torch.randn(H, K, d_r, generator=g) * 3
+    omega[0, 0, :2] = torch.tensor([60.0, -60.0])
+    alpha = torch.randn(H, K, generator=g) * 4
+    s2, lp = gma.reparameterize(omega.cuda(), alpha.cuda(), eps_sigma=1e-3)
+    s2_ref, lp_ref = oracle.reparameterize(omega, alpha, 1e-3)
+    s2g = s2.double().cpu().numpy()
+    assert np.max(np.abs(s2g - s2_ref) / s2_ref) < 1e-6
+    lpg = lp.double().cpu().numpy()
+    assert np.max(np.abs(lpg - lp_ref) / np.maximum(1.0, np.abs(lp_ref))) < 2e-6
+    ds2 = torch.randn(H, K, d_r, generator=g)
+    dlp = torch.randn(H, K, generator=g)
+    dw, da = gma.reparameterize_backward(omega.cuda(), alpha.cuda(), ds2.cuda(), dlp.cuda())
+    dw_ref, da_ref = oracle.reparameterize_backward(omega, alpha, ds2, dlp)
+    assert np.max(np.abs(dw.double().cpu().numpy() - dw_ref)) <= 1e-6 * np.max(np.abs(dw_ref))
+    assert np.max(np.abs(da.double().cpu().numpy() - da_ref)) <= 2e-6 * np.max(np.abs(da_ref))
+
+
+def test_reparameterized_parameters_drive_the_forward():
+    """The reparameterisation's outputs are valid forward parameters: the forward
+    from them equals the oracle forward from the oracle's reparameterisation."""
+    import oracle
+    case = Case("reparam_fwd", False, 1, 2, 300, 32, 32, 16, "f32")
+    inp = make_inputs(case, seed=4)
+    g = torch.Generator().manual_seed(9)
+    omega, alpha = torch.randn(2, 16, 32, generator=g) * 0.7, torch.randn(2, 16, generator=g)
+    s2, lp = gma.reparameterize(omega.cuda(), alpha.cuda())
+    s2_ref, lp_ref = oracle.reparameterize(omega, alpha, 1e-3)
+    d = to_dev(inp)
+    O = gma.forward_bidir(d["Q"], d["K"], d["V"], d["mu"], s2, lp, eps=case.eps, sync_status=True)
+    ref = oracle.forward_bidir(inp["Q"], inp["K"], inp["V"], inp["mu"], s2_ref, lp_ref, case.eps)
+    assert _rel(O, ref) <= TOL
