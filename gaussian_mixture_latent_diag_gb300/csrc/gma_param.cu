@@ -9,7 +9,9 @@
 // produced as log_pi (what the forward entry points take), and the gradients
 //   d omega_kj = d sigma2_kj * sigmoid(omega_kj)
 //   d alpha_k  = d log_pi_k - pi_k * sum_l d log_pi_l.
-// One CTA per head; the per-head log-sum-exp and gradient sum are taken by one
+// Grid (element chunks, H): every CTA takes kParamChunk covariance elements of
+// its head (many CTAs, so many loads in flight), and the first CTA of each head
+// also does the priors, whose log-sum-exp and gradient sum are taken by one
 // thread in component order (K <= 128), so results are reproducible.
 #include <cmath>
 
@@ -19,6 +21,7 @@ namespace gma {
 namespace {
 
 constexpr int kParamThreads = 256;
+constexpr int kParamChunk = 4 * kParamThreads;  // covariance elements per CTA
 
 // softplus(w) = max(w, 0) + log1p(exp(-|w|)): no overflow for large |w|
 __device__ __forceinline__ float softplus_f(float w) { return fmaxf(w, 0.f) + log1pf(expf(-fabsf(w))); }
@@ -47,9 +50,13 @@ __global__ void __launch_bounds__(kParamThreads) reparam_kernel(const float *__r
                                                                 float eps_sigma, float *__restrict__ sigma2,
                                                                 float *__restrict__ log_pi) {
     __shared__ float sm[2];
-    const int h = blockIdx.x;
+    const int h = blockIdx.y;
     const size_t base = (size_t)h * K * d_r;
-    for (int e = threadIdx.x; e < K * d_r; e += kParamThreads) sigma2[base + e] = softplus_f(omega[base + e]) + eps_sigma;
+    const int e1 = min(K * d_r, (int)(blockIdx.x + 1) * kParamChunk);
+#pragma unroll 4
+    for (int e = blockIdx.x * kParamChunk + threadIdx.x; e < e1; e += kParamThreads)
+        sigma2[base + e] = softplus_f(omega[base + e]) + eps_sigma;
+    if (blockIdx.x != 0) return;
     const float *a = alpha + (size_t)h * K;
     prior_lse(a, K, sm);
     const float lse = sm[0] + logf(sm[1]);
@@ -60,10 +67,13 @@ __global__ void __launch_bounds__(kParamThreads) reparam_backward_kernel(
     const float *__restrict__ omega, const float *__restrict__ alpha, const float *__restrict__ dsigma2,
     const float *__restrict__ dlog_pi, int K, int d_r, float *__restrict__ domega, float *__restrict__ dalpha) {
     __shared__ float sm[3];
-    const int h = blockIdx.x;
+    const int h = blockIdx.y;
     const size_t base = (size_t)h * K * d_r;
-    for (int e = threadIdx.x; e < K * d_r; e += kParamThreads)
+    const int e1 = min(K * d_r, (int)(blockIdx.x + 1) * kParamChunk);
+#pragma unroll 4
+    for (int e = blockIdx.x * kParamChunk + threadIdx.x; e < e1; e += kParamThreads)
         domega[base + e] = dsigma2[base + e] * sigmoid_f(omega[base + e]);
+    if (blockIdx.x != 0) return;
     const float *a = alpha + (size_t)h * K, *g = dlog_pi + (size_t)h * K;
     if (threadIdx.x == 0) {
         float gs = 0.f;
@@ -80,14 +90,16 @@ __global__ void __launch_bounds__(kParamThreads) reparam_backward_kernel(
 
 cudaError_t reparameterize(const float *omega, const float *alpha, int H, int K, int d_r, float eps_sigma,
                            float *sigma2, float *log_pi, cudaStream_t s) {
-    reparam_kernel<<<H, kParamThreads, 0, s>>>(omega, alpha, K, d_r, eps_sigma, sigma2, log_pi);
+    const dim3 grid((K * d_r + kParamChunk - 1) / kParamChunk, H);
+    reparam_kernel<<<grid, kParamThreads, 0, s>>>(omega, alpha, K, d_r, eps_sigma, sigma2, log_pi);
     return cudaGetLastError();
 }
 
 cudaError_t reparameterize_backward(const float *omega, const float *alpha, const float *dsigma2,
                                     const float *dlog_pi, int H, int K, int d_r, float *domega, float *dalpha,
                                     cudaStream_t s) {
-    reparam_backward_kernel<<<H, kParamThreads, 0, s>>>(omega, alpha, dsigma2, dlog_pi, K, d_r, domega, dalpha);
+    const dim3 grid((K * d_r + kParamChunk - 1) / kParamChunk, H);
+    reparam_backward_kernel<<<grid, kParamThreads, 0, s>>>(omega, alpha, dsigma2, dlog_pi, K, d_r, domega, dalpha);
     return cudaGetLastError();
 }
 
