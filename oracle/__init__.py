@@ -20,6 +20,7 @@ Linear-Time Sequence Mixing via Probabilistic Latent Routing" (arXiv
 * ``latent_memory``                  -- Eqs. (5)-(6): Vt, Z of a key/value sequence
 * ``read_memory``                    -- Eq. (7) from a given memory (Vt, Z)
 * ``decode_step`` / ``decode``        -- Eq. (8b) one position at a time (carried Vt, Z)
+* ``project_qkv``                    -- Eq. (4): Q_X, K_X, V_X = X W^T, split into heads
 * ``reparameterize`` (+ ``_backward``) -- Eqs. (14)-(15): sigma2 = softplus(omega) + eps,
   log pi = log_softmax(alpha), and the chain rule through them
 * ``routing_stats``                  -- component usage, hard assignments, usage entropy
@@ -108,6 +109,8 @@ def _load(mutant: int = 0):
             lib.gma_oracle_read_memory.argtypes = [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
                                                    _D, ctypes.c_int, ctypes.c_double, _D, _D, _D]
             lib.gma_oracle_read_memory.restype = None
+            lib.gma_oracle_project.argtypes = [_D, ctypes.c_int, ctypes.c_int, _D, ctypes.c_int, _D]
+            lib.gma_oracle_project.restype = None
             lib.gma_oracle_reparameterize.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                       _D, _D]
             lib.gma_oracle_reparameterize.restype = None
@@ -403,6 +406,24 @@ def routing_stats(X, mu, sigma2, log_pi) -> dict:
     return {"usage": usage.reshape(lead + (K,)), "counts": counts.reshape(lead + (K,)),
             "z": z.reshape(lead + (N,)), "entropy": st[:, 0].reshape(lead),
             "entropy_norm": st[:, 1].reshape(lead), "used": st[:, 2].astype(np.int64).reshape(lead)}
+
+
+def project_qkv(X, W_q, W_k, W_v, H: int):
+    """Q_X, K_X, V_X [B, H, N, d] of the layer input X [B, N, D] ([GMA, Eq. 4],
+    Q_X = X W_Q^T with W_Q [H * d_r, D] stored one output feature per row;
+    output feature h * d + c of a projection is column c of head h)."""
+    lib = _load(_ACTIVE[0])
+    X = _f64(X)
+    B, N, D = X.shape
+    outs = []
+    for W in (W_q, W_k, W_v):
+        W = _f64(W)
+        O = W.shape[0]
+        Y = np.empty((B * N, O))
+        x = np.ascontiguousarray(X.reshape(B * N, D))
+        lib.gma_oracle_project(_p(x), B * N, D, _p(W), O, _p(Y))
+        outs.append(np.ascontiguousarray(Y.reshape(B, N, H, O // H).transpose(0, 2, 1, 3)))
+    return tuple(outs)
 
 
 def reparameterize(omega, alpha, eps_sigma=1e-3):

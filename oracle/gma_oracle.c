@@ -716,3 +716,21 @@ void gma_oracle_reparameterize_backward(const double *omega, const double *alpha
     for (int k = 0; k < K; ++k) { z += exp(alpha[k] - m); g += dlog_pi[k]; }
     for (int k = 0; k < K; ++k) dalpha[k] = dlog_pi[k] - exp(alpha[k] - m) / z * g;
 }
+
+/*
+ * Projection of the input rows into the routing and value spaces ([GMA, the
+ * projections of Eq. 4]: Q_X, K_X, V_X are linear maps of the layer input X;
+ * the display equation was lost in extraction, the plainest reading being
+ * Q_X = X W_Q and the like).  Weights are stored [out, in] (one output
+ * feature per row):
+ *   Y[m, o] = sum_i X[m, i] W[o, i]      X : [M, D]   W : [O, D]   Y : [M, O]
+ */
+void gma_oracle_project(const double *X, int M, int D, const double *W, int O, double *Y)
+{
+    for (int m = 0; m < M; ++m)
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0;
+            for (int i = 0; i < D; ++i) acc += X[(size_t)m * D + i] * W[(size_t)o * D + i];
+            Y[(size_t)m * O + o] = acc;
+        }
+}

@@ -488,4 +488,22 @@ def pin_reparameterize_gradient_by_finite_differences():
     assert abs(da.sum()) < 1e-12
 
 
+# ---------------------------------------------------------------- projections (Eq. 4)
+
+def pin_project_matches_einsum_and_selects_heads():
+    """Q_X[b, h, n, c] = sum_i X[b, n, i] W[h d + c, i] equals numpy's einsum; a
+    weight that copies input column (h d + c) gives back the head-split input."""
+    rng = _rng(50)
+    B, N, D, H, d_r, d_v = 2, 7, 24, 3, 4, 8
+    X = rng.normal(size=(B, N, D))
+    Wq, Wk, Wv = rng.normal(size=(H * d_r, D)), rng.normal(size=(H * d_r, D)), rng.normal(size=(H * d_v, D))
+    Q, K, V = oracle.project_qkv(X, Wq, Wk, Wv, H)
+    for P, W, d in ((Q, Wq, d_r), (K, Wk, d_r), (V, Wv, d_v)):
+        ref = np.einsum("bni,oi->bno", X, W).reshape(B, N, H, d).transpose(0, 2, 1, 3)
+        assert P.shape == (B, H, N, d) and np.max(np.abs(P - ref)) < 1e-12
+    sel = np.eye(H * d_v, D)
+    _, _, V = oracle.project_qkv(X, Wq, Wk, sel, H)
+    assert np.array_equal(V, X[:, :, :H * d_v].reshape(B, N, H, d_v).transpose(0, 2, 1, 3))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
