@@ -527,6 +527,83 @@ def run_aux(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+PROJ_WORKLOAD = dict(B=4, N=16384, D=1024, H=8, d_r=64, d_v=64)
+PROJ_METRIC = "GMA Q/K/V projection (Eq. 4) token/s (B=4 N=16K D=1024 -> H=8 x (64+64+64)); % of GB300 bf16 peak"
+
+
+def run_project(args, rank: int, world: int, local_rank: int):
+    """--workload project: one gma_project_qkv per step, X [4, 16384, 1024] bf16 and
+    the three weights [512, 1024] bf16 to Q_X, K_X, V_X [4, 8, 16384, 64] bf16.
+    Algorithmic work 2 * B N * D * H (2 d_r + d_v) = 206 GFLOP per call (a dense
+    contraction: tensor-bound against the measured bf16 peak); algorithmic bytes
+    X 128 MB + W 3 MB + outputs 192 MB."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    w = PROJ_WORKLOAD
+    B, N, D, H, d_r, d_v = w["B"], w["N"], w["D"], w["H"], w["d_r"], w["d_v"]
+    g = torch.Generator().manual_seed(rank_seed(rank, 7))
+    X = torch.randn(B, N, D, generator=g).to(torch.bfloat16).to(dev)
+    Ws = [(torch.randn(H * d, D, generator=g) / D ** 0.5).to(torch.bfloat16).to(dev) for d in (d_r, d_r, d_v)]
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    outs = []
+
+    def call():
+        outs.clear()
+        outs.extend(gma.project_qkv(X, *Ws, H, workspace=ws))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0.record(stream)
+        for _ in range(args.steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = job_ms(t0.elapsed_time(t1) / args.steps, world, dev)
+    flops = 2.0 * B * N * D * H * (2 * d_r + d_v)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, src = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        peak, src = 1900.0, "fallback"
+    achieved = flops / (ms / 1e3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rows = 256
+        xs = X[0, :rows].float().cpu().numpy()[None]
+        t = time.perf_counter()
+        oracle.project_qkv(xs, *(W.float().cpu().numpy() for W in Ws), H)
+        secs = time.perf_counter() - t
+        cpu = {"value": rows / secs, "unit": "token/s", "cores": 1, "kind": "oracle",
+               "sample": f"{rows} tokens of the workload through the fp64 C oracle, {secs:.2f} s on one core"}
+    if rank == 0:
+        out = {"metric": PROJ_METRIC, "value": world * B * N / (ms / 1e3), "unit": "token/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": "GMA Q/K/V projection, X [4, 16384, 1024] bf16 -> Q_X, K_X, V_X "
+                                      "[4, 8, 16384, 64] bf16 (fp32 accumulation)", **w,
+                          "l2": "X (128 MB) and outputs (192 MB) larger than L2, no flush",
+                          "parallelism": f"replicas x{world}"},
+               "gpu_launches": args.steps,
+               "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                            "frac": achieved / peak, "traffic": None, "kernel": "proj_kernel",
+                            "algorithmic_flops": flops, "peak_source": src},
+               "clocks": clocks.summary(), "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+
+
 PARAM_WORKLOAD = dict(H=32, K=128, d_r=128)
 PARAM_METRIC = "GMA parameter reparameterisation + its gradient, elements/s (H=32, K=128, d_r=128)"
 
@@ -551,10 +628,32 @@ def run_params(args, rank: int, world: int, local_rank: int):
     alpha = torch.randn(H, K, generator=g).to(dev)
     ds2 = torch.randn(H, K, d_r, generator=g).to(dev)
     dlp = torch.randn(H, K, generator=g).to(dev)
+    s2, lp = torch.empty_like(omega), torch.empty_like(alpha)
+    dw, da = torch.empty_like(omega), torch.empty_like(alpha)
+    lib = gma.load()
+    import ctypes
+    vp = ctypes.c_void_p
+
+    def launch(strm):
+        st = lib.gma_reparameterize(vp(omega.data_ptr()), vp(alpha.data_ptr()), H, K, d_r, 1e-3, vp(s2.data_ptr()),
+                                    vp(lp.data_ptr()), vp(strm.cuda_stream))
+        st |= lib.gma_reparameterize_backward(vp(omega.data_ptr()), vp(alpha.data_ptr()), vp(ds2.data_ptr()),
+                                              vp(dlp.data_ptr()), H, K, d_r, vp(dw.data_ptr()), vp(da.data_ptr()),
+                                              vp(strm.cuda_stream))
+        if st != 0:
+            raise gma.GmaError(st, "gma_reparameterize")
+
+    # the two launches are a few microseconds each: replaying them from a CUDA
+    # graph keeps the host's call overhead out of the measurement
+    for _ in range(args.warmup):
+        launch(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launch(torch.cuda.current_stream())
 
     def call():
-        gma.reparameterize(omega, alpha)
-        gma.reparameterize_backward(omega, alpha, ds2, dlp)
+        graph.replay()
 
     for _ in range(args.warmup):
         call()
@@ -593,6 +692,7 @@ def run_params(args, rank: int, world: int, local_rank: int):
                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                "config": {"workload": "GMA reparameterisation (Eqs. 14-15) forward + gradient, H=32 K=128 d_r=128",
                           **w, "l2": "2 MB parameter set, L2-resident (latency-bound launches)",
+                          "launch": "both C-ABI calls captured once in a CUDA graph, replayed each step",
                           "parallelism": f"replicas x{world}"},
                "gpu_launches": 2 * args.steps,
                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -817,11 +917,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params"], default="forward",
+    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params", "project"],
+                    default="forward",
                     help="forward: the bidirectional + causal forward step (default); "
                          "backward: the bidirectional + causal backward; decode: one causal decode "
                          "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics; "
-                         "params: the reparameterisation and its gradient")
+                         "params: the reparameterisation and its gradient; project: the Q/K/V projections")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -841,6 +942,8 @@ def main():
             run_aux(args, rank, world, local_rank)
         elif args.workload == "params":
             run_params(args, rank, world, local_rank)
+        elif args.workload == "project":
+            run_project(args, rank, world, local_rank)
         else:
             run_gma(args, rank, world, local_rank)
     finally:

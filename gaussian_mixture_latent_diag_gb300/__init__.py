@@ -25,7 +25,7 @@ from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError
 
 __all__ = ["forward_bidir", "forward_causal", "backward_bidir", "backward_causal", "responsibilities",
            "latent_memory", "read_memory", "forward_causal_carry", "decode_step", "routing_stats",
-           "reparameterize", "reparameterize_backward",
+           "reparameterize", "reparameterize_backward", "project_qkv",
            "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
            "PATH_TC", "load"]
@@ -418,3 +418,30 @@ def reparameterize_backward(omega, alpha, dsigma2, dlog_pi, stream=None):
     if st != 0:
         raise GmaError(st, "gma_reparameterize_backward")
     return domega, dalpha
+
+
+def project_qkv(X, W_q, W_k, W_v, H, out_dtype=None, workspace=None, stream=None, sync_status=False):
+    """Eq. (4): Q_X, K_X, V_X [B, H, N, d] = X W^T split into heads, for X [B, N, D]
+    and weights [H d, D] (bf16, one output feature per row); outputs bf16 by
+    default (the forward's input type), or out_dtype=torch.float32."""
+    import torch
+    lib = load()
+    _check_dev(X, W_q, W_k, W_v)
+    if any(t.dtype != torch.bfloat16 for t in (X, W_q, W_k, W_v)):
+        raise TypeError("X and the weights must be bfloat16")
+    B, N, D = X.shape
+    if W_q.shape[1] != D or W_k.shape != W_q.shape or W_v.shape[1] != D or W_q.shape[0] % H or W_v.shape[0] % H:
+        raise ValueError("weights must be [H * d, D]")
+    d_r, d_v = W_q.shape[0] // H, W_v.shape[0] // H
+    odt = torch.bfloat16 if out_dtype is None else out_dtype
+    code = GMA_BF16 if odt == torch.bfloat16 else GMA_F32
+    Q = torch.empty(B, H, N, d_r, dtype=odt, device=X.device)
+    K = torch.empty(B, H, N, d_r, dtype=odt, device=X.device)
+    V = torch.empty(B, H, N, d_v, dtype=odt, device=X.device)
+    ws = _workspace(int(lib.gma_project_workspace_size()), X.device, workspace)
+    opt = options(sync_status=sync_status)
+    st = lib.gma_project_qkv(_ptr(X), _ptr(W_q), _ptr(W_k), _ptr(W_v), _ptr(Q), _ptr(K), _ptr(V), code, B, N, D, H,
+                             d_r, d_v, ctypes.byref(opt), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_project_qkv")
+    return Q, K, V

@@ -536,6 +536,41 @@ gma_status gma_reparameterize_backward(const float *omega, const float *alpha, c
     return GMA_OK;
 }
 
+size_t gma_project_workspace_size(void) { return gma::proj_workspace(); }
+
+gma_status gma_project_qkv(const void *X, const void *W_Q, const void *W_K, const void *W_V, void *Q_X, void *K_X,
+                           void *V_X, gma_dtype out_dtype, int B, int N, int D, int H, int d_r, int d_v,
+                           const gma_options *options, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!X || !W_Q || !W_K || !W_V || !Q_X || !K_X || !V_X || !workspace) return GMA_ERR_INVALID_ARG;
+    if (out_dtype != GMA_F32 && out_dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
+    const void *al[] = {X, W_Q, W_K, W_V, Q_X, K_X, V_X};
+    for (const void *ptr : al)
+        if (!aligned16(ptr)) return GMA_ERR_INVALID_ARG;
+    if (B < 1 || N < 1 || H < 1 || D < 8 || D % 8 != 0 || !valid_dim(d_r) || !valid_dim(d_v))
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * N > 65535LL * 128 || (long long)H * (d_r > d_v ? d_r : d_v) > (1LL << 24) ||
+        (long long)B * N * D > (1LL << 40))
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (workspace_bytes < gma::proj_workspace()) return GMA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t oe = out_dtype == GMA_BF16 ? 2 : 4, rows = (size_t)B * N;
+    const void *in[] = {X, W_Q, W_K, W_V, workspace};
+    const size_t nin[] = {2 * rows * D, 2 * (size_t)H * d_r * D, 2 * (size_t)H * d_r * D, 2 * (size_t)H * d_v * D,
+                          gma::proj_workspace()};
+    void *out[] = {Q_X, K_X, V_X};
+    const size_t nout[] = {oe * rows * H * d_r, oe * rows * H * d_r, oe * rows * H * d_v};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 5; ++b)
+            if (overlaps(out[a], nout[a], in[b], nin[b])) return GMA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(out[a], nout[a], out[b], nout[b])) return GMA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t err = gma::tc_project_qkv(X, W_Q, W_K, W_V, Q_X, K_X, V_X, out_dtype == GMA_BF16, B, N, D, H,
+                                                d_r, d_v, workspace, s);
+    return finish(err, options, workspace, s);
+}
+
 gma_status gma_last_device_status(const void *workspace, void *stream) {
     if (!workspace) return GMA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

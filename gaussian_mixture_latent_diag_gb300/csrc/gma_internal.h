@@ -134,6 +134,13 @@ cudaError_t reparameterize_backward(const float *omega, const float *alpha, cons
                                     const float *dlog_pi, int H, int K, int d_r, float *domega, float *dalpha,
                                     cudaStream_t s);
 
+// ---------------------------------------------------------------- projections (gma_proj.cu)
+// Q_X, K_X, V_X [B][H][N][d] (bf16 or fp32) = X [B N][D] W^T, W [H d][D], all
+// bf16; tcgen05 GEMM.  Workspace: proj_workspace() bytes (the status word).
+size_t proj_workspace();
+cudaError_t tc_project_qkv(const void *X, const void *Wq, const void *Wk, const void *Wv, void *Q, void *Kx, void *V,
+                           bool out_bf16, int B, int N, int D, int H, int d_r, int d_v, void *ws, cudaStream_t s);
+
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);
 size_t tc_workspace(const Problem &p, int causal, int splits);

@@ -67,8 +67,9 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
 // The polling loop is kept out of line: waits are inlined at many call
 // sites, and one shared copy of the slow path keeps the kernels' hot code
-// small (instruction fetch is a bottleneck of the persistent kernels).
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity) {
+// small (instruction fetch is a bottleneck of the persistent kernels).  Internal
+// linkage: every translation unit that includes this header has its own copy.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
     while (true) {
 #pragma unroll 1

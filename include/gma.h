@@ -375,6 +375,28 @@ gma_status gma_reparameterize_backward(const float *omega, const float *alpha, c
                                        float *dalpha, void *stream);
 
 /*
+ * The Q/K/V projections in front of the hot path ([GMA, Eq. (4)]: the layer
+ * input X is mapped linearly to the routing rows and the values), as one
+ * tensor-core GEMM per call that writes the head-major layouts the forward
+ * entry points read:
+ *   Q_X[b,h,n,c] = sum_i X[b,n,i] W_Q[h*d_r + c, i]   (K_X with W_K, V_X with W_V, d_v)
+ *   X   : [B, N, D] bf16      W_Q, W_K : [H*d_r, D] bf16   W_V : [H*d_v, D] bf16
+ *         (weights stored one output feature per row)
+ *   Q_X, K_X : [B, H, N, d_r], V_X : [B, H, N, d_v] in out_dtype (GMA_BF16, rounded
+ *         to nearest even from the fp32 accumulator, or GMA_F32)
+ * D must be a multiple of 8 (1 <= D); B*N <= 65535*128; d_r, d_v in {16, 32, 64,
+ * 128}; H >= 1.  Every pointer starts on a 16-byte boundary (the workspace on a
+ * 256-byte one); outputs may not overlap inputs, each other or the workspace
+ * (GMA_ERR_INVALID_ARG).  The workspace (gma_project_workspace_size bytes) holds
+ * the status word; a bounded device wait that runs out reports GMA_ERR_TIMEOUT
+ * there.  options: only sync_status is read.
+ */
+size_t gma_project_workspace_size(void);
+gma_status gma_project_qkv(const void *X, const void *W_Q, const void *W_K, const void *W_V, void *Q_X, void *K_X,
+                           void *V_X, gma_dtype out_dtype, int B, int N, int D, int H, int d_r, int d_v,
+                           const gma_options *options, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Number of stages (kernel launches, plus the status reset of the first) of
  * a call on kernel family `path` (GMA_PATH_SIMT / GMA_PATH_TC) for
  * `variant` (-1 responsibilities, 0 bidirectional, 1 causal, 2 bidirectional
