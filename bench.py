@@ -527,6 +527,77 @@ def run_aux(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+CFG_METRIC = "GMA fwd tokens*heads/s on each of the five configured workloads; % of GB300 HBM roofline"
+
+
+def run_configs(args, rank: int, world: int, local_rank: int):
+    """--workload configs: one forward of each configured workload (the
+    small fp32 bidirectional, bidirectional N=4096, causal N=16384, peaked
+    bidirectional N=16384, causal large-head N=32768 K=d=128) per step, timed
+    separately, each on the kernel family the library selects for it.  The
+    headline step (bidirectional + causal at N=16384, K=64) is the default
+    workload; this leg puts the others on record.  Per workload: token*heads/s
+    and the whole call's algorithmic bytes (Q, K, V read, fp32 O written)
+    against the measured HBM peak."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300.synthetic import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    peak, peak_src = measured_peaks()
+    per = {}
+    with ClockSampler(local_rank) as clocks:
+        for name, case in WORKLOADS.items():
+            inp = make_inputs(case, seed=rank_seed(rank, 8))
+            d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+            fn = gma.forward_causal if case.causal else gma.forward_bidir
+            out = torch.empty(case.B, case.H, case.N, case.d_v, device=dev)
+            code = "f32" if case.dtype == "f32" else "bf16"
+            ws = torch.empty(gma.workspace_size(case.B, case.H, case.N, case.d_r, case.d_v, case.K, code,
+                                                int(case.causal)), dtype=torch.uint8, device=dev)
+
+            def call():
+                fn(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], eps=case.eps, out=out, workspace=ws)
+
+            for _ in range(args.warmup):
+                call()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            steps = max(1, args.steps if case.token_heads >= 1 << 20 else 5 * args.steps)
+            t0.record(stream)
+            for _ in range(steps):
+                call()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1) / steps
+            es = 4 if case.dtype == "f32" else 2
+            alg = case.token_heads * (es * (2 * case.d_r + case.d_v) + 4 * case.d_v)
+            path = gma.selected_path(case.N, case.d_r, case.d_v, case.K, code, int(case.causal))
+            from gaussian_mixture_latent_diag_gb300 import _native
+            launches = len(_native.stage_names(path, int(case.causal))) * steps
+            per[name] = {"ms": ms, "token_heads_per_s": case.token_heads / (ms / 1e3),
+                         "hbm_frac": alg / (ms / 1e3) / 1e9 / peak,
+                         "path": "tc" if path == gma.PATH_TC else "simt", "algorithmic_bytes": alg,
+                         "timed_calls": steps, "stages_launched": launches}
+            del d, out, ws
+    if rank == 0:
+        total = sum(v["ms"] for v in per.values())
+        units = sum(WORKLOADS[n].token_heads for n in per)
+        out = {"metric": CFG_METRIC, "value": world * units / (total / 1e3), "unit": UNIT, "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": total, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": "one forward of each of the five configured workloads per step",
+                          "l2": "inputs at or above L2 size except the small fp32 case; no flush",
+                          "parallelism": f"replicas x{world}"},
+               "gpu_launches": sum(v["stages_launched"] for v in per.values()), "per_config": per,
+               "roofline": {"bound": "hbm", "peak": peak, "unit": "GB/s", "peak_source": peak_src,
+                            "note": "per workload in per_config.hbm_frac (whole call)"},
+               "clocks": clocks.summary()}
+        print(json.dumps(out), flush=True)
+
+
 PROJ_WORKLOAD = dict(B=4, N=16384, D=1024, H=8, d_r=64, d_v=64)
 PROJ_METRIC = "GMA Q/K/V projection (Eq. 4) token/s (B=4 N=16K D=1024 -> H=8 x (64+64+64)); % of GB300 bf16 peak"
 
@@ -917,12 +988,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params", "project"],
+    ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params", "project",
+                                           "configs"],
                     default="forward",
                     help="forward: the bidirectional + causal forward step (default); "
                          "backward: the bidirectional + causal backward; decode: one causal decode "
                          "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics; "
-                         "params: the reparameterisation and its gradient; project: the Q/K/V projections")
+                         "params: the reparameterisation and its gradient; project: the Q/K/V projections; "
+                         "configs: each of the five configured workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -944,6 +1017,8 @@ def main():
             run_params(args, rank, world, local_rank)
         elif args.workload == "project":
             run_project(args, rank, world, local_rank)
+        elif args.workload == "configs":
+            run_configs(args, rank, world, local_rank)
         else:
             run_gma(args, rank, world, local_rank)
     finally:

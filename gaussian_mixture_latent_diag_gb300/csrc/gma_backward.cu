@@ -483,7 +483,20 @@ __global__ void bwd_suffix_scan_kernel(float *__restrict__ part, int nchunk, int
     if (e >= E) return;
     float *p = part + (size_t)bh * nchunk * E + e;
     float run = 0.f;
-    for (int c = nchunk - 1; c >= 0; --c) {
+    int c = nchunk - 1;
+    // eight loads before their sums, so eight memory round trips overlap; the
+    // summation order is the reverse chunk order
+    for (; c >= 7; c -= 8) {
+        float cur[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) cur[u] = p[(size_t)(c - u) * E];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            p[(size_t)(c - u) * E] = run;
+            run += cur[u];
+        }
+    }
+    for (; c >= 0; --c) {
         const float cur = p[(size_t)c * E];
         p[(size_t)c * E] = run;
         run += cur;

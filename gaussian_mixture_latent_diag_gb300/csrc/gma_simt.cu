@@ -264,6 +264,28 @@ __global__ void reduce_to_memory_kernel(const float *__restrict__ part, int nspl
     else Z[(size_t)bh * K + k] = acc;
 }
 
+// In-place exclusive prefix of p[0], p[E], p[2E], ... (n terms) starting from
+// `run`, which returns the total.  Eight loads are issued before their sums, so
+// eight memory round trips overlap; the summation order is the chunk order.
+__device__ __forceinline__ void exclusive_prefix_strided(float *p, int n, int E, float &run) {
+    int c = 0;
+    for (; c + 8 <= n; c += 8) {
+        float cur[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) cur[u] = p[(size_t)(c + u) * E];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            p[(size_t)(c + u) * E] = run;
+            run += cur[u];
+        }
+    }
+    for (; c < n; ++c) {
+        const float cur = p[(size_t)c * E];
+        p[(size_t)c * E] = run;
+        run += cur;
+    }
+}
+
 // Packs a caller's latent memory into the read kernel's layout:
 // mem[bh][k] = [Vt[bh][k][0..d_v) | Z[bh][k]].
 __global__ void pack_memory_kernel(const float *__restrict__ Vt, const float *__restrict__ Z, int K, int d_v,
@@ -292,11 +314,7 @@ __global__ void scan_chunks_carry_kernel(float *__restrict__ part, int nchunk, i
     float run = 0.f;
     if (Vt_in) run = c < d_v ? Vt_in[((size_t)bh * K + k) * d_v + c] : Z_in[(size_t)bh * K + k];
     float *p = part + (size_t)bh * nchunk * E + e;
-    for (int ch = 0; ch < nchunk; ++ch) {
-        const float cur = p[(size_t)ch * E];
-        p[(size_t)ch * E] = run;
-        run += cur;
-    }
+    exclusive_prefix_strided(p, nchunk, E, run);
     if (Vt_out) {
         if (c < d_v) Vt_out[((size_t)bh * K + k) * d_v + c] = run;
         else Z_out[(size_t)bh * K + k] = run;
@@ -314,11 +332,7 @@ __global__ void scan_chunks_kernel(float *__restrict__ part, int nchunk, int E,
     if (e >= E) return;
     float *p = part + (size_t)bh * nchunk * E + e;
     float run = 0.f;
-    for (int c = 0; c < nchunk; ++c) {
-        float cur = p[(size_t)c * E];
-        p[(size_t)c * E] = run;
-        run += cur;
-    }
+    exclusive_prefix_strided(p, nchunk, E, run);
 }
 
 // Normalised broadcasting ([GMA, Eq. (7)]): one thread per query row,
@@ -357,19 +371,37 @@ __global__ void __launch_bounds__(128) read_simt_kernel(
 // exclusive prefix memory (S, Z) at the chunk start:
 //   O_i = (gQ_i S + sum_{t0<=j<=i} <gQ_i, gK_j> V_j)
 //         / (gQ_i Z + sum_{t0<=j<=i} <gQ_i, gK_j> + eps).
+// Four threads per query row (kCausalParts), each owning a quarter of the
+// output columns.  The intra-chunk dots <gQ_i, gK_j> are split over j: part q
+// computes them for j = 4m + q and the four parts exchange them by shuffles,
+// so the shared-memory reads are broadcasts without padding.  The prefix rows
+// are staged kCausalKT at a time, each row as four padded column quarters and
+// Z, and V likewise in padded quarters, so the four parts read distinct banks.
+// Summation orders are those of the definition: k for the prefix, then j.
+constexpr int kCausalParts = 4;
+constexpr int kCausalKT = 16;
+template <int D_V>
+struct CausalSmem {
+    static constexpr int P = kCausalParts, CW = D_V / P, SQ = CW + 1, SR = P * SQ + 1;
+    static size_t floats(int K) {
+        return (size_t)2 * K * kSimtCausalChunk + (size_t)kSimtCausalChunk * P * SQ + (size_t)kCausalKT * SR;
+    }
+};
 template <int D_V, typename T, typename TO>
-__global__ void __launch_bounds__(kSimtCausalChunk) causal_simt_kernel(
+__global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_kernel(
     const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
     const float *__restrict__ prefix, int N, int K, int nchunk, float eps, TO *__restrict__ O,
     const unsigned *status) {
     if (failed(status)) return;
     constexpr int C = kSimtCausalChunk;
     constexpr int W = D_V + 1;
+    using L = CausalSmem<D_V>;
+    constexpr int P = L::P, CW = L::CW, SQ = L::SQ, SR = L::SR;
     extern __shared__ float smem[];
     float *sgq = smem;              // [K][C]
     float *sgk = sgq + K * C;       // [K][C]
-    float *sv = sgk + K * C;        // [C][D_V]
-    float *ss = sv + C * D_V;       // [K][W]
+    float *sv = sgk + K * C;        // [C][P * SQ]: V rows in padded quarters
+    float *ss = sv + C * P * SQ;    // [kCausalKT][SR]: prefix rows in padded quarters, then Z
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int t0 = chunk * C;
     const int n = min(C, N - t0);
@@ -380,35 +412,57 @@ __global__ void __launch_bounds__(kSimtCausalChunk) causal_simt_kernel(
         sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
     }
     const T *v = V + ((size_t)bh * N + t0) * D_V;
-    for (int e = threadIdx.x; e < C * D_V; e += blockDim.x) sv[e] = e < n * D_V ? to_f32(v[e]) : 0.f;
-    const float *pre = prefix + ((size_t)bh * nchunk + chunk) * K * W;
-    for (int e = threadIdx.x; e < K * W; e += blockDim.x) ss[e] = pre[e];
-    __syncthreads();
-    const int i = threadIdx.x;
-    if (i >= n) return;
-    float acc[D_V];
+    for (int e = threadIdx.x; e < C * D_V; e += blockDim.x) {
+        const int t = e / D_V, c = e % D_V;
+        sv[t * P * SQ + (c / CW) * SQ + c % CW] = t < n ? to_f32(v[e]) : 0.f;
+    }
+    const int i = threadIdx.x / P, q = threadIdx.x % P, lane = threadIdx.x & 31;
+    float acc[CW];
 #pragma unroll
-    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    for (int c = 0; c < CW; ++c) acc[c] = 0.f;
     float den = 0.f;
-    for (int k = 0; k < K; ++k) {
-        float g = sgq[k * C + i];
-        const float *row = ss + k * W;
+    const float *pre = prefix + ((size_t)bh * nchunk + chunk) * K * W;
+    for (int k0 = 0; k0 < K; k0 += kCausalKT) {
+        const int nk = min(kCausalKT, K - k0);
+        __syncthreads();  // the previous stage is consumed (the first time: sgq, sgk, sv are staged)
+        for (int e = threadIdx.x; e < nk * W; e += blockDim.x) {
+            const int kk = e / W, c = e % W;
+            ss[kk * SR + (c < D_V ? (c / CW) * SQ + c % CW : P * SQ)] = pre[(size_t)k0 * W + e];
+        }
+        __syncthreads();
+        for (int kk = 0; kk < nk; ++kk) {
+            const float g = sgq[(k0 + kk) * C + i];
+            const float *row = ss + kk * SR + q * SQ;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(g, row[c], acc[c]);
-        den = fmaf(g, row[D_V], den);
+            for (int c = 0; c < CW; ++c) acc[c] = fmaf(g, row[c], acc[c]);
+            den = fmaf(g, ss[kk * SR + P * SQ], den);
+        }
     }
-    for (int j = 0; j <= i; ++j) {
+    // intra-chunk terms j <= i; the loop runs to the warp's last row, so every
+    // lane of the warp takes part in every shuffle
+    const int wlast = min(n - 1, (threadIdx.x / 32) * (32 / P) + (32 / P) - 1);
+    for (int j0 = 0; j0 <= wlast; j0 += P) {
+        const int j = j0 + q;
         float a = 0.f;
-        for (int k = 0; k < K; ++k) a = fmaf(sgq[k * C + i], sgk[k * C + j], a);
-        den += a;
-        const float *vr = sv + j * D_V;
+        if (j <= wlast)
+            for (int k = 0; k < K; ++k) a = fmaf(sgq[k * C + i], sgk[k * C + j], a);
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(a, vr[c], acc[c]);
+        for (int p2 = 0; p2 < P; ++p2) {
+            const float ap = __shfl_sync(0xffffffffu, a, (lane & ~(P - 1)) | p2);
+            const int jj = j0 + p2;
+            if (jj <= i) {
+                den += ap;
+                const float *vr = sv + jj * P * SQ + q * SQ;
+#pragma unroll
+                for (int c = 0; c < CW; ++c) acc[c] = fmaf(ap, vr[c], acc[c]);
+            }
+        }
     }
+    if (i >= n) return;
     const float r = 1.0f / (den + eps);
-    TO *o = O + ((size_t)bh * N + t0 + i) * D_V;
+    TO *o = O + ((size_t)bh * N + t0 + i) * D_V + q * CW;
 #pragma unroll
-    for (int c = 0; c < D_V; ++c) o[c] = from_f32<TO>(acc[c] * r);
+    for (int c = 0; c < CW; ++c) o[c] = from_f32<TO>(acc[c] * r);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -458,13 +512,15 @@ cudaError_t launch_causal_dv(const Problem &p, const float *gq, const float *gk,
                              const float *prefix, int nchunk, const unsigned *status,
                              cudaStream_t s) {
     constexpr int C = kSimtCausalChunk;
-    size_t smem = ((size_t)2 * p.K * C + (size_t)C * D_V + (size_t)p.K * (D_V + 1)) * sizeof(float);
+    const size_t smem = CausalSmem<D_V>::floats(p.K) * sizeof(float);
     auto kern = causal_simt_kernel<D_V, T, TO>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    if (smem > 48 * 1024) {  // above the default limit only: the call costs host time
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     dim3 grid(nchunk, p.BH());
-    kern<<<grid, C, smem, s>>>(gq, gk, static_cast<const T *>(p.V), prefix, p.N, p.K, nchunk,
-                               p.eps, static_cast<TO *>(p.O), status);
+    kern<<<grid, C * kCausalParts, smem, s>>>(gq, gk, static_cast<const T *>(p.V), prefix, p.N, p.K, nchunk,
+                                              p.eps, static_cast<TO *>(p.O), status);
     return cudaGetLastError();
 }
 
