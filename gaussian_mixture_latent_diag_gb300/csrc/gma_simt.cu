@@ -375,14 +375,15 @@ __global__ void __launch_bounds__(128) read_simt_kernel(
 // output columns.  The intra-chunk dots <gQ_i, gK_j> are split over j: part q
 // computes them for j = 4m + q and the four parts exchange them by shuffles,
 // so the shared-memory reads are broadcasts without padding.  The prefix rows
-// are staged kCausalKT at a time, each row as four padded column quarters and
-// Z, and V likewise in padded quarters, so the four parts read distinct banks.
+// are staged kCausalKT at a time, each row as four column quarters padded to a
+// multiple of 4 floats, then Z, and V likewise, so the four parts read
+// distinct banks with 16-byte loads.
 // Summation orders are those of the definition: k for the prefix, then j.
 constexpr int kCausalParts = 4;
 constexpr int kCausalKT = 16;
 template <int D_V>
 struct CausalSmem {
-    static constexpr int P = kCausalParts, CW = D_V / P, SQ = CW + 1, SR = P * SQ + 1;
+    static constexpr int P = kCausalParts, CW = D_V / P, SQ = CW + 4, SR = P * SQ + 4;
     static size_t floats(int K) {
         return (size_t)2 * K * kSimtCausalChunk + (size_t)kSimtCausalChunk * P * SQ + (size_t)kCausalKT * SR;
     }
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
     constexpr int W = D_V + 1;
     using L = CausalSmem<D_V>;
     constexpr int P = L::P, CW = L::CW, SQ = L::SQ, SR = L::SR;
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *sgq = smem;              // [K][C]
     float *sgk = sgq + K * C;       // [K][C]
     float *sv = sgk + K * C;        // [C][P * SQ]: V rows in padded quarters
@@ -432,9 +433,15 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
         __syncthreads();
         for (int kk = 0; kk < nk; ++kk) {
             const float g = sgq[(k0 + kk) * C + i];
-            const float *row = ss + kk * SR + q * SQ;
+            const float4 *row = reinterpret_cast<const float4 *>(ss + kk * SR + q * SQ);
 #pragma unroll
-            for (int c = 0; c < CW; ++c) acc[c] = fmaf(g, row[c], acc[c]);
+            for (int c4 = 0; c4 < CW / 4; ++c4) {
+                const float4 r = row[c4];
+                acc[4 * c4 + 0] = fmaf(g, r.x, acc[4 * c4 + 0]);
+                acc[4 * c4 + 1] = fmaf(g, r.y, acc[4 * c4 + 1]);
+                acc[4 * c4 + 2] = fmaf(g, r.z, acc[4 * c4 + 2]);
+                acc[4 * c4 + 3] = fmaf(g, r.w, acc[4 * c4 + 3]);
+            }
             den = fmaf(g, ss[kk * SR + P * SQ], den);
         }
     }
@@ -452,9 +459,15 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
             const int jj = j0 + p2;
             if (jj <= i) {
                 den += ap;
-                const float *vr = sv + jj * P * SQ + q * SQ;
+                const float4 *vr = reinterpret_cast<const float4 *>(sv + jj * P * SQ + q * SQ);
 #pragma unroll
-                for (int c = 0; c < CW; ++c) acc[c] = fmaf(ap, vr[c], acc[c]);
+                for (int c4 = 0; c4 < CW / 4; ++c4) {
+                    const float4 r = vr[c4];
+                    acc[4 * c4 + 0] = fmaf(ap, r.x, acc[4 * c4 + 0]);
+                    acc[4 * c4 + 1] = fmaf(ap, r.y, acc[4 * c4 + 1]);
+                    acc[4 * c4 + 2] = fmaf(ap, r.z, acc[4 * c4 + 2]);
+                    acc[4 * c4 + 3] = fmaf(ap, r.w, acc[4 * c4 + 3]);
+                }
             }
         }
     }
