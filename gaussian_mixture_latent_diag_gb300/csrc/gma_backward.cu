@@ -133,8 +133,9 @@ __global__ void __launch_bounds__(128) bwd_score_grad_kernel(const float *__rest
 
 // Column sums over a range of rows: part[bh][split][k][c] = sum_{i in split} G[k][i] B[i][c]
 // for c in [64 z, 64 z + 64) and c < ncol.  G [K][N] (component-major), B rows of
-// ldb floats.  Block: 256 threads, each an 4 (k) x 8 (c) tile; rows staged 32 at a
-// time in shared memory; fixed summation order.
+// ldb floats.  Block: 256 threads, each 4 components (k) x 8 columns (c, taken
+// interleaved, c = tc + 8 b, so a warp reads consecutive columns); rows staged
+// 32 at a time in shared memory; fixed summation order.
 constexpr int kCT = 32;
 __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict__ Gt,
                                                          const float *__restrict__ B, int ldb, int ncol,
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict
 #pragma unroll
                 for (int a = 0; a < 4; ++a) ga[a] = 4 * tk + a < K ? sg[4 * tk + a][t] : 0.f;
 #pragma unroll
-                for (int b = 0; b < 8; ++b) vb[b] = sb[t][8 * tc + b];
+                for (int b = 0; b < 8; ++b) vb[b] = sb[t][tc + 8 * b];  // interleaved: no bank conflicts
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict
         if (k >= K) continue;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-            const int c = c0 + 8 * tc + b;
+            const int c = c0 + tc + 8 * b;
             if (c < ncol) p[(size_t)k * ncol + c] = acc[a][b];
         }
     }

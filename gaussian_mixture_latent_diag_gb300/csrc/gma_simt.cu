@@ -158,8 +158,10 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
 
 // Latent aggregation over one range of keys ([GMA, Eqs. (5)-(6)]):
 //   part[k][c] = sum_{j in range} gK_jk V_jc (c < d_v),  part[k][d_v] = sum gK_jk.
-// Block: 256 threads, each owns an 8 x 8 tile of (k, c); keys staged 32 at a
-// time in shared memory.  Fixed summation order.
+// Block: 256 threads, each owns 8 components k = 8 tk + a and 8 value columns
+// c = tc + b * tiles_c (interleaved, so the threads of a warp read consecutive
+// columns of a staged key row: no bank conflicts); keys staged 32 at a time in
+// shared memory.  Fixed summation order.
 constexpr int kWT = 32;  // keys per shared-memory stage
 template <typename T>
 __global__ void __launch_bounds__(256) write_simt_kernel(
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(256) write_simt_kernel(
                 }
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    int c = tc * 8 + b;
+                    int c = tc + b * tiles_c;
                     vb[b] = c < d_v ? sv[t][c] : 0.f;
                 }
 #pragma unroll
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(256) write_simt_kernel(
         if (k >= K) continue;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-            int c = tc * 8 + b;
+            int c = tc + b * tiles_c;
             if (c < d_v) p[(size_t)k * W + c] = acc[a][b];
         }
         if (tc == 0) p[(size_t)k * W + d_v] = zacc[a];
