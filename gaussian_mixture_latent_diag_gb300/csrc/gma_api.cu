@@ -567,7 +567,7 @@ gma_status gma_project_qkv(const void *X, const void *W_Q, const void *W_K, cons
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t err = gma::tc_project_qkv(X, W_Q, W_K, W_V, Q_X, K_X, V_X, out_dtype == GMA_BF16, B, N, D, H,
-                                                d_r, d_v, workspace, s);
+                                                d_r, d_v, options && options->test_stall, workspace, s);
     return finish(err, options, workspace, s);
 }
 

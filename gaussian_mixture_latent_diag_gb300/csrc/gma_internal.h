@@ -139,7 +139,8 @@ cudaError_t reparameterize_backward(const float *omega, const float *alpha, cons
 // bf16; tcgen05 GEMM.  Workspace: proj_workspace() bytes (the status word).
 size_t proj_workspace();
 cudaError_t tc_project_qkv(const void *X, const void *Wq, const void *Wk, const void *Wv, void *Q, void *Kx, void *V,
-                           bool out_bf16, int B, int N, int D, int H, int d_r, int d_v, void *ws, cudaStream_t s);
+                           bool out_bf16, int B, int N, int D, int H, int d_r, int d_v, bool stall, void *ws,
+                           cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);

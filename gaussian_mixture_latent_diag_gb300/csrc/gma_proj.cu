@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) proj_kernel(const __grid_cons
                                                                const __grid_constant__ CUtensorMap tmWk,
                                                                const __grid_constant__ CUtensorMap tmWv,
                                                                ProjOut out, int Bn, int N, int H, int D,
-                                                               unsigned *status) {
+                                                               int stall, unsigned *status) {
     extern __shared__ __align__(1024) uint8_t proj_smem[];
     // SW128 tiles want 1024-byte aligned stages
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(proj_smem) + 1023) & ~uintptr_t(1023));
@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) proj_kernel(const __grid_cons
                         give_up(status, &abort_flag);
                         break;
                     }
+                    if (stall && g == 0) continue;  // test hook: the first stage is never loaded
                     mbar_arrive_expect_tx(&full[s], kProjXBytes + kProjWBytes);
                     tma_load_3d(sx + s * kProjXBytes, &tmX, kb * kProjK, m0, 0, &full[s]);
                     tma_load_3d(sw + s * kProjWBytes, tmW, kb * kProjK, o0, 0, &full[s]);
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) proj_kernel(const __grid_cons
             }
             // every load armed here has landed before the CTA leaves
             for (long j = g - kProjStages < 0 ? 0 : g - kProjStages; j < g; ++j)
-                mbar_wait(&full[j % kProjStages], (uint32_t)(j / kProjStages) & 1);
+                if (!(stall && j == 0)) mbar_wait(&full[j % kProjStages], (uint32_t)(j / kProjStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -281,7 +282,8 @@ bool proj_map(CUtensorMap *map, const void *ptr, int rows, int D, int box_rows) 
 size_t proj_workspace() { return kStatusBytes; }
 
 cudaError_t tc_project_qkv(const void *X, const void *Wq, const void *Wk, const void *Wv, void *Q, void *Kx, void *V,
-                           bool out_bf16, int B, int N, int D, int H, int d_r, int d_v, void *ws, cudaStream_t s) {
+                           bool out_bf16, int B, int N, int D, int H, int d_r, int d_v, bool stall, void *ws,
+                           cudaStream_t s) {
     CUtensorMap tx, tq, tk, tv;
     const int M = B * N;
     if (!proj_map(&tx, X, M, D, kProjM) || !proj_map(&tq, Wq, H * d_r, D, kProjN) ||
@@ -304,11 +306,13 @@ cudaError_t tc_project_qkv(const void *X, const void *Wq, const void *Wk, const 
     if (out_bf16) {
         e = cudaFuncSetAttribute(proj_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProjSmem);
         if (e != cudaSuccess) return e;
-        proj_kernel<true><<<grid, kProjThreads, kProjSmem, s>>>(tx, tq, tk, tv, out, B, N, H, D, status);
+        proj_kernel<true><<<grid, kProjThreads, kProjSmem, s>>>(tx, tq, tk, tv, out, B, N, H, D, stall ? 1 : 0,
+                                                                status);
     } else {
         e = cudaFuncSetAttribute(proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProjSmem);
         if (e != cudaSuccess) return e;
-        proj_kernel<false><<<grid, kProjThreads, kProjSmem, s>>>(tx, tq, tk, tv, out, B, N, H, D, status);
+        proj_kernel<false><<<grid, kProjThreads, kProjSmem, s>>>(tx, tq, tk, tv, out, B, N, H, D, stall ? 1 : 0,
+                                                                 status);
     }
     return cudaGetLastError();
 }

@@ -389,7 +389,8 @@ gma_status gma_reparameterize_backward(const float *omega, const float *alpha, c
  * 256-byte one); outputs may not overlap inputs, each other or the workspace
  * (GMA_ERR_INVALID_ARG).  The workspace (gma_project_workspace_size bytes) holds
  * the status word; a bounded device wait that runs out reports GMA_ERR_TIMEOUT
- * there.  options: only sync_status is read.
+ * there.  options: sync_status, and test_stall (the first stage of the first
+ * tile is never loaded, so the MMA issuer's bounded wait runs out after 4 s).
  */
 size_t gma_project_workspace_size(void);
 gma_status gma_project_qkv(const void *X, const void *W_Q, const void *W_K, const void *W_V, void *Q_X, void *K_X,

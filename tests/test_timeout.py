@@ -41,3 +41,26 @@ def test_forced_timeout_reports_status_and_recovers(causal):
     # the stream still works: a normal call right after matches the oracle
     O2 = run_gpu(case, d)
     assert normalised_error(O2, oracle_full(case, inp)) <= TOL["bf16"]
+
+
+def test_projection_forced_timeout_reports_status_and_recovers():
+    """The projection GEMM's bounded waits: with test_stall its first stage is
+    never loaded, so the MMA issuer gives up after 4 s; the call reports
+    GMA_ERR_TIMEOUT and a normal call right after is correct."""
+    import numpy as np
+    import oracle
+    lib = _native.load()
+    B, N, D, H, dh = 1, 300, 256, 2, 64
+    g = torch.Generator().manual_seed(3)
+    X = torch.randn(B, N, D, generator=g).to(torch.bfloat16).cuda()
+    Ws = [(torch.randn(H * dh, D, generator=g) / 16).to(torch.bfloat16).cuda() for _ in range(3)]
+    outs = [torch.empty(B, H, N, dh, dtype=torch.float32, device="cuda") for _ in range(3)]
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    opt = _native.options(sync_status=True, test_stall=True)
+    st = lib.gma_project_qkv(*(vp(t.data_ptr()) for t in [X] + Ws + outs), _native.GMA_F32, B, N, D, H, dh, dh,
+                             ctypes.byref(opt), vp(ws.data_ptr()), 256, vp(torch.cuda.current_stream().cuda_stream))
+    assert st == GMA_ERR_TIMEOUT, _native.status_string(st)
+    torch.cuda.synchronize()
+    Q, K, V = gma.project_qkv(X, *Ws, H, out_dtype=torch.float32, sync_status=True)
+    ref = oracle.project_qkv(X.cpu(), *(w.cpu() for w in Ws), H)
+    assert np.max(np.abs(Q.double().cpu().numpy() - ref[0])) < 1e-3
