@@ -598,6 +598,104 @@ def run_configs(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+SHARD_METRIC = "GMA per-shard steps of sequence sharding token*heads/s (N=16K, K=64); % of GB300 HBM roofline"
+
+
+def run_shard(args, rank: int, world: int, local_rank: int):
+    """--workload shard: the three per-shard steps of a sequence sharded over N
+    (gaussian_mixture_latent_diag_gb300.sharded), each timed on the headline
+    shape (B=4, H=8, N=16384, d_r=d_v=K=64, bf16): gma_latent_memory (reads K, V),
+    gma_read_memory (reads Q, writes fp32 O) and gma_forward_causal_carry (reads
+    Q, K, V, writes fp32 O and the final state).  One step = the three calls,
+    on the kernel family sharded.CudaOps picks for the shape: the tensor-core
+    kernels here (Gamma never leaves the SM).  per_call_simt times the same
+    calls on the CUDA-core kernels for comparison."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    w = WORKLOAD
+    B, H, N, d_r, d_v, K = w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"]
+    inp = make_inputs(Case("shard", True, B, H, N, d_r, d_v, K, w["dtype"]), seed=rank_seed(rank, 9))
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    prm = (d["mu"], d["sigma2"], d["log_pi"])
+    Vt, Z = gma.latent_memory(d["K"], d["V"], *prm)
+    O = torch.empty(B, H, N, d_v, device=dev)
+    import ctypes
+    from gaussian_mixture_latent_diag_gb300.sharded import CudaOps
+    path = CudaOps._path(d["K"], d["V"], d["mu"])
+    ws = {}
+
+    def wsp(name, nbytes):  # one workspace per call, allocated outside the timed region
+        if name not in ws:
+            ws[name] = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        return ws[name]
+
+    code = gma.GMA_BF16
+    nb_lm = lambda pth: int(gma.load().gma_latent_memory_workspace_size(  # noqa: E731
+        B, H, N, d_r, d_v, K, code, ctypes.byref(gma.options(path=pth))))
+    nb_rd = int(gma.load().gma_read_memory_workspace_size(B, H, N, d_r, d_v, K, code))
+    nb_cc = int(gma.load().gma_causal_carry_workspace_size(B, H, N, d_r, d_v, K, code))
+
+    def calls_for(pth):
+        return {
+            "latent_memory": lambda: gma.latent_memory(d["K"], d["V"], *prm, path=pth,
+                                                       workspace=wsp(f"lm{pth}", nb_lm(pth))),
+            "read_memory": lambda: gma.read_memory(d["Q"], *prm, Vt, Z, eps=w["eps"], out=O, path=pth,
+                                                   workspace=wsp("rd", nb_rd)),
+            "causal_carry": lambda: gma.forward_causal_carry(d["Q"], d["K"], d["V"], *prm, Vt, Z, eps=w["eps"],
+                                                             out=O, path=pth, workspace=wsp("cc", nb_cc)),
+        }
+
+    es = 2
+    alg = {"latent_memory": B * H * N * es * (d_r + d_v), "read_memory": B * H * N * (es * d_r + 4 * d_v),
+           "causal_carry": B * H * N * (es * (2 * d_r + d_v) + 4 * d_v)}
+    peak, peak_src = measured_peaks()
+
+    def time_calls(calls):
+        per = {}
+        for name, fn in calls.items():
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1) / args.steps
+            per[name] = {"ms": ms, "hbm_frac": alg[name] / (ms / 1e3) / 1e9 / peak, "algorithmic_bytes": alg[name]}
+        return per
+
+    with ClockSampler(local_rank) as clocks:
+        per = time_calls(calls_for(path))
+    per_simt = time_calls(calls_for(gma.PATH_SIMT)) if path != gma.PATH_SIMT else None
+    tc = path == gma.PATH_TC
+    if rank == 0:
+        total = sum(v["ms"] for v in per.values())
+        out = {"metric": SHARD_METRIC, "value": world * 3 * B * H * N / (total / 1e3), "unit": UNIT,
+               "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+               "data": "synthetic",
+               "config": {"workload": "latent memory + read from it + carried-prefix causal forward, B=4 H=8 "
+                                      "N=16384 d_r=d_v=K=64 bf16 (per GPU)", **{k: w[k] for k in ("B", "H", "N", "K")},
+                          "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
+               "path": "tc" if tc else "simt",
+               "gpu_launches": ((2 + 3 + 3) if tc else (4 + 4 + 6)) * args.steps, "per_call": per,
+               "per_call_simt": per_simt,
+               "roofline": {"bound": "hbm", "peak": peak, "unit": "GB/s", "peak_source": peak_src,
+                            "achieved": sum(alg.values()) / (total / 1e3) / 1e9,
+                            "frac": sum(alg.values()) / (total / 1e3) / 1e9 / peak, "traffic": None,
+                            "kernel": "the three calls together (" + ("tensor-core kernels" if tc else
+                                      "CUDA-core stages, Gamma materialised") + ")"},
+               "clocks": clocks.summary()}
+        print(json.dumps(out), flush=True)
+
+
 PROJ_WORKLOAD = dict(B=4, N=16384, D=1024, H=8, d_r=64, d_v=64)
 PROJ_METRIC = "GMA Q/K/V projection (Eq. 4) token/s (B=4 N=16K D=1024 -> H=8 x (64+64+64)); % of GB300 bf16 peak"
 
@@ -989,13 +1087,14 @@ def main():
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params", "project",
-                                           "configs"],
+                                           "configs", "shard"],
                     default="forward",
                     help="forward: the bidirectional + causal forward step (default); "
                          "backward: the bidirectional + causal backward; decode: one causal decode "
                          "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics; "
                          "params: the reparameterisation and its gradient; project: the Q/K/V projections; "
-                         "configs: each of the five configured workloads")
+                         "configs: each of the five configured workloads; shard: the per-shard steps of "
+                         "sequence sharding")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1019,6 +1118,8 @@ def main():
             run_project(args, rank, world, local_rank)
         elif args.workload == "configs":
             run_configs(args, rank, world, local_rank)
+        elif args.workload == "shard":
+            run_shard(args, rank, world, local_rank)
         else:
             run_gma(args, rank, world, local_rank)
     finally:

@@ -219,10 +219,12 @@ def _params_check(H, d_r, mu, sigma2, log_pi):
     return K
 
 
-def latent_memory(K, V, mu, sigma2, log_pi, workspace=None, stream=None, splits=0, sync_status=False):
+def latent_memory(K, V, mu, sigma2, log_pi, workspace=None, stream=None, splits=0, sync_status=False,
+                  path=PATH_AUTO):
     """Latent memory of a key/value sequence: (Vt [B, H, K, d_v], Z [B, H, K]) fp32,
     Vt = Gamma^K^T V, Z = Gamma^K^T 1.  It is also the causal state after the last
-    position, i.e. what decode_step continues from after a prompt."""
+    position, i.e. what decode_step continues from after a prompt.  path=PATH_TC
+    runs it on the tensor-core kernels (bf16, d_r in {32, 64}, d_v = 64, K <= 64)."""
     import torch
     lib = load()
     _check_dev(K, V, mu, sigma2, log_pi)
@@ -236,7 +238,7 @@ def latent_memory(K, V, mu, sigma2, log_pi, workspace=None, stream=None, splits=
         raise TypeError("K, V must share one dtype")
     Vt = torch.empty(B, H, Kc, d_v, dtype=torch.float32, device=K.device)
     Z = torch.empty(B, H, Kc, dtype=torch.float32, device=K.device)
-    opt = options(splits=splits, sync_status=sync_status)
+    opt = options(path=path, splits=splits, sync_status=sync_status)
     nb = int(lib.gma_latent_memory_workspace_size(B, H, N, d_r, d_v, Kc, code, ctypes.byref(opt)))
     if nb == 0:
         raise GmaError(2, "gma_latent_memory")
@@ -313,7 +315,7 @@ def routing_stats(X, mu, sigma2, log_pi, want_z=True, workspace=None, stream=Non
 
 
 def read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps=1e-6, out=None, workspace=None, stream=None, o_bf16=False,
-                sync_status=False):
+                sync_status=False, path=PATH_AUTO):
     """O = Gamma^Q Vt / (Gamma^Q Z + eps) for Q [B, H, N, d_r] and a given latent
     memory Vt [B, H, K, d_v], Z [B, H, K] (fp32); O fp32 (or bf16)."""
     import torch
@@ -333,7 +335,7 @@ def read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps=1e-6, out=None, workspace=None
     if nb == 0:
         raise GmaError(2, "gma_read_memory")
     ws = _workspace(nb, Q.device, workspace)
-    opt = options(sync_status=sync_status, o_bf16=o_bf16)
+    opt = options(path=path, sync_status=sync_status, o_bf16=o_bf16)
     st = lib.gma_read_memory(_ptr(Q), code, _ptr(mu), _ptr(sigma2), _ptr(log_pi), float(eps), _ptr(Vt), _ptr(Z),
                              _ptr(out), B, H, N, d_r, d_v, Kc, ctypes.byref(opt), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream))
@@ -343,7 +345,7 @@ def read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps=1e-6, out=None, workspace=None
 
 
 def forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in=None, Z_in=None, eps=1e-6, want_state=True,
-                         out=None, workspace=None, stream=None, o_bf16=False, sync_status=False):
+                         out=None, workspace=None, stream=None, o_bf16=False, sync_status=False, path=PATH_AUTO):
     """Causal forward whose prefix starts from (Vt_in, Z_in) (an empty prefix if
     None).  Returns (O, Vt_out, Z_out): the outputs and, if want_state, the
     prefix memory after the last position (else None, None)."""
@@ -375,7 +377,7 @@ def forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in=None, Z_in=None, eps
     if nb == 0:
         raise GmaError(2, "gma_forward_causal_carry")
     ws = _workspace(nb, dev, workspace)
-    opt = options(sync_status=sync_status, o_bf16=o_bf16)
+    opt = options(path=path, sync_status=sync_status, o_bf16=o_bf16)
 
     def p(t):
         return _ptr(t) if t is not None else None

@@ -46,9 +46,21 @@ size_t workspace_for(const Problem &p, int causal, const gma_options *opt, int p
     return gma::simt_layout(p, causal, splits).total;
 }
 
-// The auxiliary entry points have only a CUDA-core implementation.
+// The decode step and the routing statistics have only a CUDA-core implementation.
 bool simt_only(const gma_options *opt) {
     return !opt || opt->path == GMA_PATH_AUTO || opt->path == GMA_PATH_SIMT;
+}
+
+// Kernel family of the latent-memory calls (latent memory, read from a memory,
+// carried-prefix causal forward): GMA_PATH_AUTO and GMA_PATH_SIMT keep them on
+// the CUDA cores (fp32 accuracy for state carried from call to call);
+// GMA_PATH_TC runs them on the tensor-core kernels where those support the
+// sizes, else -1.
+int memory_path(const Problem &p, int causal, const gma_options *opt) {
+    const int path = opt ? opt->path : GMA_PATH_AUTO;
+    if (path == GMA_PATH_AUTO || path == GMA_PATH_SIMT) return GMA_PATH_SIMT;
+    if (path == GMA_PATH_TC) return gma::tc_supported(p, causal) ? GMA_PATH_TC : -1;
+    return -1;
 }
 
 gma::StageClock clock_for(const gma_options *opt, cudaStream_t s) {
@@ -268,11 +280,13 @@ gma_status gma_backward_causal(const void *Q_X, const void *K_X, const void *V_X
 size_t gma_latent_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
                                         const gma_options *options) {
     if (dtype != GMA_F32 && dtype != GMA_BF16) return 0;
-    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return 0;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
     if (options && options->splits < 0) return 0;
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    return gma::simt_layout(p, 2, options ? options->splits : 0).total;
+    const int path = memory_path(p, 0, options), splits = options ? options->splits : 0;
+    if (path < 0) return 0;
+    return path == GMA_PATH_TC ? gma::tc_workspace(p, 0, splits) : gma::simt_layout(p, 2, splits).total;
 }
 
 gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, const float *mu,
@@ -286,13 +300,15 @@ gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, 
     if (!aligned16(K_X) || !aligned16(V_X) || !aligned16(Vt) || !aligned16(Z) || !aligned16(mu) ||
         !aligned16(sigma2))
         return GMA_ERR_INVALID_ARG;
-    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (options && options->splits < 0) return GMA_ERR_INVALID_ARG;
     Problem p;
     p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.dtype = dtype;
     p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     const int splits = options ? options->splits : 0;
-    const size_t need = gma::simt_layout(p, 2, splits).total;
+    const int path = memory_path(p, 0, options);
+    if (path < 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = path == GMA_PATH_TC ? gma::tc_workspace(p, 0, splits) : gma::simt_layout(p, 2, splits).total;
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
     const size_t nvt = 4 * (size_t)B * H * K * d_v, nz = 4 * (size_t)B * H * K;
@@ -305,7 +321,9 @@ gma_status gma_latent_memory(const void *K_X, const void *V_X, gma_dtype dtype, 
         return GMA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gma::StageClock clk = clock_for(options, s);
-    return finish(gma::simt_latent_memory(p, splits, Vt, Z, workspace, s, clk), options, workspace, s);
+    const cudaError_t err = path == GMA_PATH_TC ? gma::tc_latent_memory(p, splits, Vt, Z, workspace, s, clk)
+                                               : gma::simt_latent_memory(p, splits, Vt, Z, workspace, s, clk);
+    return finish(err, options, workspace, s);
 }
 
 size_t gma_decode_workspace_size(int H, int d_r, int K) {
@@ -409,7 +427,9 @@ size_t gma_read_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int
     if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    return gma::simt_layout(p, 3, 0).total;
+    const size_t simt = gma::simt_layout(p, 3, 0).total;
+    const size_t tc = gma::tc_supported(p, 0) ? gma::tc_workspace(p, 0, 0) : 0;
+    return simt > tc ? simt : tc;  // enough for either kernel family
 }
 
 gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, const float *sigma2,
@@ -422,12 +442,14 @@ gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, co
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GMA_ERR_INVALID_ARG;
     if (!aligned16(Q_X) || !aligned16(Vt) || !aligned16(Z) || !aligned16(O) || !aligned16(mu) || !aligned16(sigma2))
         return GMA_ERR_INVALID_ARG;
-    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
     Problem p;
     p.Q = Q_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = O; p.dtype = dtype; p.eps = eps;
     p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     p.o_bf16 = options && options->o_bf16;
-    const size_t need = gma::simt_layout(p, 3, 0).total;
+    const int path = memory_path(p, 0, options);
+    if (path < 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = path == GMA_PATH_TC ? gma::tc_workspace(p, 0, 0) : gma::simt_layout(p, 3, 0).total;
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
     const size_t no = (p.o_bf16 ? 2 : 4) * rows * d_v;
@@ -440,7 +462,9 @@ gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, co
         if (overlaps(workspace, need, in[a], nin[a])) return GMA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gma::StageClock clk = clock_for(options, s);
-    return finish(gma::simt_read_memory(p, Vt, Z, workspace, s, clk), options, workspace, s);
+    const cudaError_t err = path == GMA_PATH_TC ? gma::tc_read_memory(p, Vt, Z, workspace, s, clk)
+                                               : gma::simt_read_memory(p, Vt, Z, workspace, s, clk);
+    return finish(err, options, workspace, s);
 }
 
 size_t gma_causal_carry_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype) {
@@ -448,7 +472,9 @@ size_t gma_causal_carry_workspace_size(int B, int H, int N, int d_r, int d_v, in
     if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    return gma::simt_layout(p, 1, 0).total;
+    const size_t simt = gma::simt_layout(p, 1, 0).total;
+    const size_t tc = gma::tc_supported(p, 1) ? gma::tc_workspace(p, 1, 0) : 0;
+    return simt > tc ? simt : tc;  // enough for either kernel family
 }
 
 gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
@@ -465,13 +491,15 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
     const void *al[] = {Q_X, K_X, V_X, O, mu, sigma2, Vt_in, Z_in, Vt_out, Z_out};
     for (const void *ptr : al)
         if (ptr && !aligned16(ptr)) return GMA_ERR_INVALID_ARG;
-    if (!shape_ok(B, H, N, d_r, d_v, K, true) || !simt_only(options)) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!shape_ok(B, H, N, d_r, d_v, K, true)) return GMA_ERR_UNSUPPORTED_SHAPE;
     Problem p;
     p.Q = Q_X; p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi; p.O = O;
     p.dtype = dtype; p.eps = eps;
     p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     p.o_bf16 = options && options->o_bf16;
-    const size_t need = gma::simt_layout(p, 1, 0).total;
+    const int path = memory_path(p, 1, options);
+    if (path < 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = path == GMA_PATH_TC ? gma::tc_workspace(p, 1, 0) : gma::simt_layout(p, 1, 0).total;
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
     const size_t nvt = 4 * (size_t)B * H * K * d_v, nz = 4 * (size_t)B * H * K;
@@ -491,7 +519,10 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
         if (in[b] && overlaps(workspace, need, in[b], nin[b])) return GMA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gma::StageClock clk = clock_for(options, s);
-    return finish(gma::simt_causal_carry(p, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk), options, workspace, s);
+    const cudaError_t err =
+        path == GMA_PATH_TC ? gma::tc_causal_carry(p, 0, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk)
+                            : gma::simt_causal_carry(p, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk);
+    return finish(err, options, workspace, s);
 }
 
 gma_status gma_reparameterize(const float *omega, const float *alpha, int H, int K, int d_r, float eps_sigma,
@@ -606,9 +637,11 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
 }
 
 int gma_stage_count(int path, int variant) {
-    if (variant < -1 || variant > 8 || (variant >= 2 && path != GMA_PATH_SIMT)) return 0;
+    const bool tc_aux = path == GMA_PATH_TC && (variant == 4 || variant == 7 || variant == 8);
+    if (variant < -1 || variant > 8 || (variant >= 2 && path != GMA_PATH_SIMT && !tc_aux)) return 0;
     const char *const *names;
-    if (variant >= 4) names = gma::kAuxStages[variant - 4];
+    if (tc_aux) names = gma::kAuxTcStages[variant - 4];
+    else if (variant >= 4) names = gma::kAuxStages[variant - 4];
     else if (variant >= 2) names = gma::kBackwardStages[variant - 2];
     else if (path == GMA_PATH_SIMT) names = gma::kSimtStages[variant + 1];
     else if (path == GMA_PATH_TC) names = gma::kTcStages[variant + 1];
@@ -621,7 +654,7 @@ int gma_stage_count(int path, int variant) {
 const char *gma_stage_name(int path, int variant, int j) {
     int n = gma_stage_count(path, variant);
     if (j < 0 || j >= n) return nullptr;
-    if (variant >= 4) return gma::kAuxStages[variant - 4][j];
+    if (variant >= 4) return path == GMA_PATH_TC ? gma::kAuxTcStages[variant - 4][j] : gma::kAuxStages[variant - 4][j];
     if (variant >= 2) return gma::kBackwardStages[variant - 2][j];
     return path == GMA_PATH_SIMT ? gma::kSimtStages[variant + 1][j] : gma::kTcStages[variant + 1][j];
 }

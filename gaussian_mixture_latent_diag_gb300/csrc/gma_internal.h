@@ -148,5 +148,15 @@ size_t tc_workspace(const Problem &p, int causal, int splits);
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 extern const char *const kTcStages[3][8];    // [variant + 1][j], NULL-terminated
+// The latent memory, the read from a caller's memory and the carried-prefix
+// causal forward on the tensor-core kernels (tc_supported sizes; workspace
+// tc_workspace(p, 0 | 0 | 1, splits)).
+cudaError_t tc_latent_memory(const Problem &p, int splits, float *Vt, float *Z, void *ws, cudaStream_t s,
+                             StageClock &clk);
+cudaError_t tc_read_memory(const Problem &p, const float *Vt, const float *Z, void *ws, cudaStream_t s,
+                           StageClock &clk);
+cudaError_t tc_causal_carry(const Problem &p, int splits, const float *Vt_in, const float *Z_in, float *Vt_out,
+                            float *Z_out, void *ws, cudaStream_t s, StageClock &clk);
+extern const char *const kAuxTcStages[5][8];  // as kAuxStages, tensor-core path (entries 0, 3, 4)
 
 }  // namespace gma

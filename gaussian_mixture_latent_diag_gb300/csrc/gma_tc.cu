@@ -341,6 +341,43 @@ __device__ __forceinline__ void store_gamma_words(uint8_t *gbuf, int t, const ui
     }
 }
 
+// Optional fp32 inputs and outputs of the per-head combine (caller buffers,
+// or null):
+//   mode 0: out = the head's memory [Vt | Z], the sum of every job's partial;
+//   mode 1: the running prefix starts at carry instead of zero, and out = the
+//           prefix after the head's last job.
+// Vt [BH][K][64], Z [BH][K] fp32; K <= KP (components past K are not touched).
+struct CombineIO {
+    const float *carry_vt, *carry_z;
+    float *out_vt, *out_z;
+    int K;
+};
+
+// Element (k, n0 .. n0 + 3) of a [KP][kW] partial from / to the caller's
+// [Vt | Z]: n < 64 is Vt[k][n], n = 64 is Z[k], n > 64 is padding (zero).
+__device__ __forceinline__ float4 io_load(const CombineIO &io, int bh, int k, int n0) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = n0 + j;
+        v[j] = k >= io.K ? 0.f
+               : n < 64  ? io.carry_vt[((size_t)bh * io.K + k) * 64 + n]
+               : n == 64 ? io.carry_z[(size_t)bh * io.K + k]
+                         : 0.f;
+    }
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void io_store(const CombineIO &io, int bh, int k, int n0, float4 a) {
+    if (k >= io.K) return;
+    const float v[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = n0 + j;
+        if (n < 64) io.out_vt[((size_t)bh * io.K + k) * 64 + n] = v[j];
+        else if (n == 64) io.out_z[(size_t)bh * io.K + k] = v[j];
+    }
+}
+
 // Combines the job partials ([KP][kW] fp32 each) of head bh in CTA order, so
 // the result does not depend on which job finished last:
 //   mode 0: img (shared memory) = the sum of the partials as the bf16 hi | lo
@@ -351,13 +388,17 @@ __device__ __forceinline__ void store_gamma_words(uint8_t *gbuf, int t, const ui
 // Each thread owns four float4 slots of the [KP][kW] layout and keeps the loads
 // of six CTAs for all of them in flight (one round for up to six jobs).
 __device__ void combine_partials(float *__restrict__ part, const Part &P, int bh, int mode, uint8_t *img, int tid,
-                                 int nthreads) {
+                                 int nthreads, const CombineIO &io) {
     constexpr int kRow4 = kW / 4, kE4 = kKP * kRow4, NQ = 4, NB = 6;
     constexpr size_t kPS4 = (size_t)kKP * kRow4;
     const int cf = first_cta_of_head(P, bh), cl = last_cta_of_head(P, bh);
     float4 acc[NQ];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < NQ; ++q) {
+        const int e4 = tid + q * nthreads;
+        acc[q] = (mode == 1 && io.carry_vt && e4 < kE4) ? io_load(io, bh, e4 / kRow4, 4 * (e4 % kRow4))
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     for (int cb = cf; cb <= cl; cb += NB) {
         float4 v[NB][NQ];
 #pragma unroll
@@ -386,6 +427,13 @@ __device__ void combine_partials(float *__restrict__ part, const Part &P, int bh
                 acc[q].z += v[u][q].z;
                 acc[q].w += v[u][q].w;
             }
+        }
+    }
+    if (io.out_vt) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int e4 = tid + q * nthreads;
+            if (e4 < kE4) io_store(io, bh, e4 / kRow4, 4 * (e4 % kRow4), acc[q]);
         }
     }
     if (mode == 0) {
@@ -446,7 +494,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part P,
     float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img, size_t mem_img_stride,
-    uint8_t *__restrict__ gk_out, int mode, int stall, unsigned *status) {
+    uint8_t *__restrict__ gk_out, int mode, int stall, CombineIO io, unsigned *status) {
     using L = Write2Smem;
     constexpr int D_V = 64, W = L::W;
     constexpr int kTmemCols = 512;
@@ -723,7 +771,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
                 constexpr int kImgBytes = 2 * (D_V + 16) * 128;
                 uint8_t *img = smem + 128 * W * 4 + 1024;
                 static_assert(128 * W * 4 + 1024 + kImgBytes <= L::kVst, "image fits over the K ring");
-                combine_partials(part, P, bh, mode, img, tid, kThreadsG);
+                combine_partials(part, P, bh, mode, img, tid, kThreadsG, io);
                 if (mode == 0) {
                     cta_sync();
                     uint4 *dst = reinterpret_cast<uint4 *>(mem_img + (size_t)bh * mem_img_stride);
@@ -1870,7 +1918,35 @@ TcLayout2 tc_layout2(const Problem &p, int splits, int causal) {
     return L;
 }
 
-cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
+// Read operand image of a caller's memory [Vt | Z] (fp32) for each head, the
+// same bf16 hi | lo layout the combine builds: row n < 64 holds Vt[:, n], row 64
+// Z, rows 65 .. 79 zero; column k of every row is component k (zero past K).
+__global__ void __launch_bounds__(256) pack_memory_tc_kernel(const float *__restrict__ Vt, const float *__restrict__ Z,
+                                                             int K, uint8_t *__restrict__ mem, size_t stride) {
+    constexpr int NBR = 64 + 16;
+    const int bh = blockIdx.x;
+    __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(mem + (size_t)bh * stride);
+    __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(mem + (size_t)bh * stride + NBR * 128);
+    for (int e = threadIdx.x; e < NBR * kKP; e += blockDim.x) {
+        const int n = e / kKP, k = e % kKP;
+        const float v = k >= K  ? 0.f
+                        : n < 64 ? Vt[((size_t)bh * K + k) * 64 + n]
+                        : n == 64 ? Z[(size_t)bh * K + k]
+                                  : 0.f;
+        const __nv_bfloat16 vh = __float2bfloat16_rn(v);
+        const uint32_t off = sw128_offset(n, k, 1024) / 2;
+        bhi[off] = vh;
+        blo[off] = __float2bfloat16_rn(v - __bfloat162float(vh));
+    }
+}
+
+// The bidirectional call: coefficient prep, the key side (write) and the query
+// side (read).  io.out_vt: also the fp32 memory; read = false: stop after the
+// write (the latent memory alone); pack_from: read the caller's memory
+// (io.carry_vt / carry_z) instead of writing one.
+cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk,
+                       CombineIO io = CombineIO{nullptr, nullptr, nullptr, nullptr, 0}, bool read = true,
+                       bool pack_from = false) {
     unsigned *status = reinterpret_cast<unsigned *>(ws);
     unsigned *counters = reinterpret_cast<unsigned *>(ws + L.counters);
     float *part = reinterpret_cast<float *>(ws + L.part);
@@ -1885,11 +1961,19 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     GMA_TRY(launch_pdl(coef_prep_tc_kernel, dim3(kPrepBlocks, p.H), dim3(128), 0, s, p.mu, p.sigma2, p.log_pi, p.K,
                        p.d_r, coef, status, head_err, counters, p.BH()));
     clk.mark();
-    GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
-    GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
-                       p.H, p.N, L.P, part, counters, mem, L.mem_stride, static_cast<uint8_t *>(nullptr), 0,
-                       p.test_stall ? 1 : 0, status));
+    if (pack_from) {
+        // after the prep (a plain launch: the read's dependent-launch wait then
+        // covers both), so the read sees the coefficients and the operand images
+        pack_memory_tc_kernel<<<p.BH(), 256, 0, s>>>(io.carry_vt, io.carry_z, p.K, mem, L.mem_stride);
+        GMA_TRY(cudaGetLastError());
+    } else {
+        GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
+        GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef,
+                           head_err, p.H, p.N, L.P, part, counters, mem, L.mem_stride, static_cast<uint8_t *>(nullptr),
+                           0, p.test_stall ? 1 : 0, io, status));
+    }
     clk.mark();
+    if (!read) return cudaSuccess;
     GMA_TRY(set_smem(tc_read3_kernel, Read3Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_read3_kernel, dim3(L.nctas), dim3(kThreadsR), Read3Smem::kAlloc, s, tq, to, coef, p.H, p.N,
                        L.P, mem, L.mem_stride, p.eps, p.o_bf16 ? 1 : 0, status));
@@ -1897,7 +1981,11 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     return cudaSuccess;
 }
 
-cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk) {
+// The causal call: coefficient prep, aggregation (job prefixes, stored Gamma^K)
+// and the chunk scan.  io.carry_vt: the prefix starts from the caller's memory;
+// io.out_vt: the prefix after the last position is written there.
+cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaStream_t s, StageClock &clk,
+                        CombineIO io = CombineIO{nullptr, nullptr, nullptr, nullptr, 0}) {
     unsigned *status = reinterpret_cast<unsigned *>(ws);
     unsigned *counters = reinterpret_cast<unsigned *>(ws + L.counters);
     float *part = reinterpret_cast<float *>(ws + L.part);
@@ -1914,7 +2002,7 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
     GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_write2_kernel, dim3(L.nctas), dim3(kThreadsG), Write2Smem::kAlloc, s, tk, tv, coef, head_err,
                        p.H, p.N, L.P, part, counters, static_cast<uint8_t *>(nullptr), size_t(0), ws + L.gk, 1,
-                       p.test_stall ? 1 : 0, status));
+                       p.test_stall ? 1 : 0, io, status));
     clk.mark();
     GMA_TRY(set_smem(tc_causal2_kernel, Causal2Smem::kAlloc));
     GMA_TRY(launch_pdl(tc_causal2_kernel, dim3(L.nctas), dim3(kThreadsG), Causal2Smem::kAlloc, s, tq, tv, to, coef,
@@ -1928,6 +2016,14 @@ cudaError_t run_causal2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaS
 const char *const kTcStages[3][8] = {
     {nullptr},
     {"prep", "tc_write", "tc_read", nullptr},
+    {"prep", "tc_aggregate", "tc_causal", nullptr},
+};
+
+const char *const kAuxTcStages[5][8] = {
+    {"prep", "tc_write", nullptr},
+    {nullptr},
+    {nullptr},
+    {"prep", "pack", "tc_read", nullptr},
     {"prep", "tc_aggregate", "tc_causal", nullptr},
 };
 
@@ -1948,6 +2044,25 @@ cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, Sta
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
     TcLayout2 L = tc_layout2(p, splits, 1);
     return run_causal2(p, L, static_cast<uint8_t *>(ws), s, clk);
+}
+
+cudaError_t tc_latent_memory(const Problem &p, int splits, float *Vt, float *Z, void *ws, cudaStream_t s,
+                             StageClock &clk) {
+    TcLayout2 L = tc_layout2(p, splits, 0);
+    return run_bidir2(p, L, static_cast<uint8_t *>(ws), s, clk, CombineIO{nullptr, nullptr, Vt, Z, p.K}, false);
+}
+
+cudaError_t tc_read_memory(const Problem &p, const float *Vt, const float *Z, void *ws, cudaStream_t s,
+                           StageClock &clk) {
+    TcLayout2 L = tc_layout2(p, 0, 0);
+    return run_bidir2(p, L, static_cast<uint8_t *>(ws), s, clk, CombineIO{Vt, Z, nullptr, nullptr, p.K}, true,
+                      true);
+}
+
+cudaError_t tc_causal_carry(const Problem &p, int splits, const float *Vt_in, const float *Z_in, float *Vt_out,
+                            float *Z_out, void *ws, cudaStream_t s, StageClock &clk) {
+    TcLayout2 L = tc_layout2(p, splits, 1);
+    return run_causal2(p, L, static_cast<uint8_t *>(ws), s, clk, CombineIO{Vt_in, Z_in, Vt_out, Z_out, p.K});
 }
 
 }  // namespace gma

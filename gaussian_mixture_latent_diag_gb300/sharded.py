@@ -26,19 +26,31 @@ import torch.distributed as dist
 
 
 class CudaOps:
-    """The per-shard steps, on the CUDA path of libgma.so."""
+    """The per-shard steps in libgma.so's kernels: on the tensor cores whenever
+    the unsharded forward would run there (bf16, d_r in {32, 64}, d_v = 64,
+    K <= 64), so a sharded call has the unsharded call's accuracy, else on the
+    CUDA cores."""
+
+    @staticmethod
+    def _path(X, V, mu, causal=0):
+        from . import PATH_SIMT, PATH_TC, selected_path
+        dtype = "bf16" if X.dtype == torch.bfloat16 else "f32"
+        N, d_r = X.shape[-2:]
+        tc = selected_path(max(N, 1), d_r, V.shape[-1], mu.shape[1], dtype, causal) == PATH_TC
+        return PATH_TC if tc else PATH_SIMT
 
     def latent_memory(self, K, V, mu, sigma2, log_pi):
         from . import latent_memory
-        return latent_memory(K, V, mu, sigma2, log_pi)
+        return latent_memory(K, V, mu, sigma2, log_pi, path=self._path(K, V, mu))
 
     def read_memory(self, Q, mu, sigma2, log_pi, Vt, Z, eps):
         from . import read_memory
-        return read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps=eps)
+        return read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps=eps, path=self._path(Q, Vt, mu))
 
     def forward_causal_carry(self, Q, K, V, mu, sigma2, log_pi, Vt_in, Z_in, eps):
         from . import forward_causal_carry
-        return forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in, Z_in, eps=eps, want_state=False)[0]
+        return forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in, Z_in, eps=eps, want_state=False,
+                                    path=self._path(Q, V, mu, causal=1))[0]
 
 
 def combine_total(parts):

@@ -240,13 +240,18 @@ gma_status gma_backward_causal(const void *Q_X, const void *K_X, const void *V_X
  * with Gamma^K the responsibilities of K_X.  This is also the carried state
  * of the causal variant after the last position (the prefix memories of
  * Eq. (8b) at i = N - 1): it primes gma_decode_step with a prompt of N tokens.
- * Runs on the CUDA cores (options->path must be GMA_PATH_AUTO or
- * GMA_PATH_SIMT; options->splits sets the number of N-splits, 0 = default).
+ * Kernel family (options->path): GMA_PATH_AUTO and GMA_PATH_SIMT run it on
+ * the CUDA cores (fp32 responsibilities, any supported size); GMA_PATH_TC on
+ * the tensor-core write kernel of the bidirectional forward (bf16 inputs,
+ * d_r in {32, 64}, d_v = 64, K <= 64; other sizes GMA_ERR_UNSUPPORTED_SHAPE),
+ * whose fp32 memory is the sum of per-job partials in job order.
+ * options->splits sets the number of N-splits (0 = default).
  * K_X, V_X, Vt, Z must start on a 16-byte boundary, the workspace on a
  * 256-byte boundary; Vt and Z may not overlap an input, each other or the
  * workspace (GMA_ERR_INVALID_ARG).  Parameter errors and the status word
  * behave as for the forward.  Workspace bytes:
- * gma_latent_memory_workspace_size (0 for unsupported arguments).
+ * gma_latent_memory_workspace_size for the same options (0 for unsupported
+ * arguments or a kernel family that does not take them).
  */
 size_t gma_latent_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype,
                                         const gma_options *options);
@@ -318,11 +323,17 @@ gma_status gma_routing_stats(const void *X, gma_dtype dtype, const float *mu, co
  * With gma_latent_memory this splits the bidirectional forward at the latent
  * memory: the memories of several key/value shards add up (the sums of
  * Eqs. (5)-(6) split over N), so a sequence sharded over N needs one sum of
- * [K, d_v + 1] per head between the two calls.  Runs on the CUDA cores
- * (options->path GMA_PATH_AUTO or GMA_PATH_SIMT).  Q_X, Vt, Z and O must start
+ * [K, d_v + 1] per head between the two calls.  Kernel family
+ * (options->path): GMA_PATH_AUTO and GMA_PATH_SIMT run it on the CUDA cores;
+ * GMA_PATH_TC packs the memory into the tensor-core read kernel's operand
+ * (each fp32 value as a bf16 high part plus a bf16 low part) and runs the
+ * read of the bidirectional forward (bf16 inputs, d_r in {32, 64}, d_v = 64,
+ * K <= 64; other sizes GMA_ERR_UNSUPPORTED_SHAPE).  A GMA_PATH_TC memory from
+ * gma_latent_memory read this way gives the GMA_PATH_TC bidirectional
+ * forward's O bit for bit.  Q_X, Vt, Z and O must start
  * on a 16-byte boundary, the workspace on a 256-byte boundary; O may not
  * overlap an input or the workspace (GMA_ERR_INVALID_ARG).  Workspace bytes:
- * gma_read_memory_workspace_size.
+ * gma_read_memory_workspace_size (enough for either kernel family).
  */
 size_t gma_read_memory_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype);
 gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, const float *sigma2,
@@ -340,11 +351,17 @@ gma_status gma_read_memory(const void *Q_X, gma_dtype dtype, const float *mu, co
  * Z_in / Z_out : [B, H, K] fp32; Vt_in and Z_in are both NULL (an empty prefix)
  * or both given, and so are Vt_out and Z_out.  Uses: a sequence sharded over N
  * (shard r starts from the sum of the memories of shards 0..r-1), a long prompt
- * processed in pieces, and priming gma_decode_step.  Runs on the CUDA cores
- * (options->path GMA_PATH_AUTO or GMA_PATH_SIMT).  Alignment and overlap rules
+ * processed in pieces, and priming gma_decode_step.  Kernel family
+ * (options->path): GMA_PATH_AUTO and GMA_PATH_SIMT run it on the CUDA cores;
+ * GMA_PATH_TC on the tensor-core causal forward, whose per-head prefix
+ * combine starts at the carried-in memory and writes the final prefix
+ * (bf16 inputs, d_r in {32, 64}, d_v = 64, K <= 64; other sizes
+ * GMA_ERR_UNSUPPORTED_SHAPE); with an empty carried-in prefix it gives the
+ * GMA_PATH_TC causal forward's O bit for bit.  Alignment and overlap rules
  * as for gma_forward_causal, plus: the carry buffers start on a 16-byte
  * boundary and the outputs (O, Vt_out, Z_out) overlap no input, each other or
- * the workspace.  Workspace bytes: gma_causal_carry_workspace_size.
+ * the workspace.  Workspace bytes: gma_causal_carry_workspace_size (enough
+ * for either kernel family).
  */
 size_t gma_causal_carry_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtype dtype);
 gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
@@ -403,7 +420,7 @@ gma_status gma_project_qkv(const void *X, const void *W_Q, const void *W_K, cons
  * `variant` (-1 responsibilities, 0 bidirectional, 1 causal, 2 bidirectional
  * backward, 3 causal backward, 4 latent memory, 5 decode step, 6 routing
  * statistics, 7 read from a memory, 8 causal forward with a carried-in prefix
- * -- variants 2 to 8 SIMT only), and the name of
+ * -- variants 2, 3, 5 and 6 SIMT only), and the name of
  * stage j (NULL if out of range).
  * Used with gma_options.stage_events.
  */

@@ -34,8 +34,11 @@ def test_workspace_queries(lib):
     assert lib.gma_read_memory_workspace_size(1, 1, 64, 64, 64, 64, 1) > 0
     assert lib.gma_causal_carry_workspace_size(1, 1, 64, 64, 64, 64, 9) == 0
     assert lib.gma_project_workspace_size() >= 4
-    simt = _native.Options(2, 0, 0, 0)  # the auxiliary paths have no tensor-core variant
-    assert lib.gma_latent_memory_workspace_size(1, 1, 64, 64, 64, 64, 1, ctypes.byref(simt)) == 0
+    tc = _native.Options(2, 0, 0, 0)  # the tensor-core path: bf16, d_r in {32, 64}, d_v = 64, K <= 64
+    assert lib.gma_latent_memory_workspace_size(1, 1, 64, 64, 64, 64, 1, ctypes.byref(tc)) > 0
+    assert lib.gma_latent_memory_workspace_size(1, 1, 64, 64, 64, 64, 0, ctypes.byref(tc)) == 0
+    assert lib.gma_latent_memory_workspace_size(1, 1, 64, 64, 64, 128, 1, ctypes.byref(tc)) == 0
+    assert lib.gma_decode_workspace_size(8, 64, 64) > 0
 
 
 def test_stage_names(lib):
@@ -43,6 +46,9 @@ def test_stage_names(lib):
     assert _native.stage_names(1, 6) == ["prep", "rows", "final"]
     assert _native.stage_names(1, 7) == ["prep", "resp_q", "pack", "read"]
     assert lib.gma_stage_count(2, 5) == 0 and lib.gma_stage_count(1, 9) == 0
+    assert _native.stage_names(2, 4) == ["prep", "tc_write"]
+    assert _native.stage_names(2, 7) == ["prep", "pack", "tc_read"]
+    assert _native.stage_names(2, 8) == ["prep", "tc_aggregate", "tc_causal"]
 
 
 def test_decode_validation(lib):

@@ -102,8 +102,9 @@ def test_sharded_over_n_emulated_on_one_gpu(P, dtype):
     Oc = torch.cat([ops.forward_causal_carry(q, k, v, *prm, *sharded.combine_exclusive(parts, r), case.eps)
                     for r, (q, k, v) in enumerate(blocks)], dim=2)
     args = (inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps)
-    assert _rel(Ob, oracle.forward_bidir(*args)) <= TOL
-    assert _rel(Oc, oracle.forward_causal(*args)) <= TOL
+    tol = TOL if dtype == "f32" else 1e-2  # bf16 d = K = 64 runs on the tensor cores
+    assert _rel(Ob, oracle.forward_bidir(*args)) <= tol
+    assert _rel(Oc, oracle.forward_causal(*args)) <= tol
 
 
 # ---------------------------------------------------------------- reparameterisation (Eqs. 14-15)
