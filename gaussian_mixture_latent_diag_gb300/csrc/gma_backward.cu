@@ -53,6 +53,11 @@ __device__ __forceinline__ bool failed(const unsigned *status) {
     return *reinterpret_cast<const volatile unsigned *>(status) != 0u;
 }
 
+// The thread-per-row kernels read Gamma / ds rows [K][N] with a stride of N, one
+// value per component: they load kLoadBatch components before using them, so
+// that many HBM round trips overlap (summation order unchanged).
+constexpr int kLoadBatch = 4;
+
 // upstream: one thread per query row.  mem [K][D_V + 1] = [Vt | Z] of the head.
 // dn[i] = [dnum_i (D_V) | dden_i].
 template <int D_V>
@@ -74,12 +79,18 @@ __global__ void __launch_bounds__(128) bwd_upstream_kernel(const float *__restri
     for (int c = 0; c < D_V; ++c) num[c] = 0.f;
     float den = 0.f;
     const float *g = gqt + (size_t)bh * K * N + i;
-    for (int k = 0; k < K; ++k) {
-        const float gk = g[(size_t)k * N];
-        const float *row = smem + k * W;
+    for (int k0 = 0; k0 < K; k0 += kLoadBatch) {
+        float gv[kLoadBatch];
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) num[c] = fmaf(gk, row[c], num[c]);
-        den = fmaf(gk, row[D_V], den);
+        for (int u = 0; u < kLoadBatch; ++u) gv[u] = k0 + u < K ? g[(size_t)(k0 + u) * N] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            if (k0 + u >= K) break;
+            const float *row = smem + (k0 + u) * W;
+#pragma unroll
+            for (int c = 0; c < D_V; ++c) num[c] = fmaf(gv[u], row[c], num[c]);
+            den = fmaf(gv[u], row[D_V], den);
+        }
     }
     den += eps;
     const float r = 1.0f / den;
@@ -120,15 +131,32 @@ __global__ void __launch_bounds__(128) bwd_score_grad_kernel(const float *__rest
     const float *g = gt + (size_t)bh * K * N + i;
     float *d = ds + (size_t)bh * K * N + i;
     float mean = 0.f;
-    for (int k = 0; k < K; ++k) {
-        const float *row = smem + k * W;
-        float u = beta * row[D_V];
+    for (int k0 = 0; k0 < K; k0 += kLoadBatch) {
+        float gv[kLoadBatch];
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) u = fmaf(a[c], row[c], u);
-        d[(size_t)k * N] = u;
-        mean = fmaf(g[(size_t)k * N], u, mean);
+        for (int u = 0; u < kLoadBatch; ++u) gv[u] = k0 + u < K ? g[(size_t)(k0 + u) * N] : 0.f;
+#pragma unroll
+        for (int v = 0; v < kLoadBatch; ++v) {
+            if (k0 + v >= K) break;
+            const float *row = smem + (k0 + v) * W;
+            float u = beta * row[D_V];
+#pragma unroll
+            for (int c = 0; c < D_V; ++c) u = fmaf(a[c], row[c], u);
+            d[(size_t)(k0 + v) * N] = u;
+            mean = fmaf(gv[v], u, mean);
+        }
     }
-    for (int k = 0; k < K; ++k) d[(size_t)k * N] = g[(size_t)k * N] * (d[(size_t)k * N] - mean);
+    for (int k0 = 0; k0 < K; k0 += kLoadBatch) {
+        float gv[kLoadBatch], uv[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            gv[u] = k0 + u < K ? g[(size_t)(k0 + u) * N] : 0.f;
+            uv[u] = k0 + u < K ? d[(size_t)(k0 + u) * N] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u)
+            if (k0 + u < K) d[(size_t)(k0 + u) * N] = gv[u] * (uv[u] - mean);
+    }
 }
 
 // Column sums over a range of rows: part[bh][split][k][c] = sum_{i in split} G[k][i] B[i][c]
@@ -225,11 +253,17 @@ __global__ void __launch_bounds__(128) bwd_dv_kernel(const float *__restrict__ g
 #pragma unroll
     for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
     const float *g = gkt + (size_t)bh * K * N + j;
-    for (int k = 0; k < K; ++k) {
-        const float gk = g[(size_t)k * N];
-        const float *row = smem + k * W;
+    for (int k0 = 0; k0 < K; k0 += kLoadBatch) {
+        float gv[kLoadBatch];
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(gk, row[c], acc[c]);
+        for (int u = 0; u < kLoadBatch; ++u) gv[u] = k0 + u < K ? g[(size_t)(k0 + u) * N] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            if (k0 + u >= K) break;
+            const float *row = smem + (k0 + u) * W;
+#pragma unroll
+            for (int c = 0; c < D_V; ++c) acc[c] = fmaf(gv[u], row[c], acc[c]);
+        }
     }
     float *o = dV + ((size_t)bh * N + j) * D_V;
 #pragma unroll
@@ -238,74 +272,96 @@ __global__ void __launch_bounds__(128) bwd_dv_kernel(const float *__restrict__ g
 
 // dx_im = sum_k ds_ik (mu_km - x_im) / sigma2_km for columns [32 z, 32 z + 32),
 // one thread per row; the block's (mu, 1/sigma2) columns are staged in shared
-// memory (K x 32 pairs).
+// memory as {mu_m, mu_m+1, 1/sigma2_m, 1/sigma2_m+1} per column pair (K x 16), and
+// the column pairs use packed f32x2 arithmetic: each element is rounded as
+// fmaf(ds * (1/sigma2), mu - x, acc) would round it, in component order.
 template <typename T>
 __global__ void __launch_bounds__(128) bwd_dx_kernel(const T *__restrict__ X, const float *__restrict__ ds,
                                                      const float *__restrict__ mu, const float *__restrict__ inv,
                                                      int H, int N, int K, int d_r, float *__restrict__ dX,
                                                      const unsigned *status) {
     if (failed(status)) return;
-    constexpr int JC = 32;
-    __shared__ float2 sp[128][JC];
+    constexpr int JC = 32, J2 = JC / 2;
+    __shared__ float4 sp[128][J2];
     const int bh = blockIdx.y, h = bh % H, j0 = JC * blockIdx.z;
     const int nj = min(JC, d_r - j0);
-    for (int e = threadIdx.x; e < K * JC; e += blockDim.x) {
-        const int k = e / JC, j = e % JC;
+    for (int e = threadIdx.x; e < K * J2; e += blockDim.x) {
+        const int k = e / J2, j = 2 * (e % J2);
         const size_t o = ((size_t)h * K + k) * d_r + j0 + j;
-        sp[k][j] = j < nj ? make_float2(mu[o], inv[o]) : make_float2(0.f, 0.f);
+        sp[k][e % J2] = j < nj ? make_float4(mu[o], mu[o + 1], inv[o], inv[o + 1]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= N) return;
-    float x[JC], acc[JC];
+    float2 nx[J2], acc[J2];
     const T *xr = X + ((size_t)bh * N + i) * d_r + j0;
 #pragma unroll
-    for (int j = 0; j < JC; ++j) {
-        x[j] = j < nj ? to_f32(xr[j]) : 0.f;
-        acc[j] = 0.f;
+    for (int j = 0; j < J2; ++j) {
+        nx[j] = 2 * j < nj ? make_float2(-to_f32(xr[2 * j]), -to_f32(xr[2 * j + 1])) : make_float2(0.f, 0.f);
+        acc[j] = make_float2(0.f, 0.f);
     }
     const float *d = ds + (size_t)bh * K * N + i;
-    for (int k = 0; k < K; ++k) {
-        const float dk = d[(size_t)k * N];
+    constexpr int KB = kLoadBatch;
+    for (int k0 = 0; k0 < K; k0 += KB) {
+        float dk[KB];
 #pragma unroll
-        for (int j = 0; j < JC; ++j) {
-            const float2 mv = sp[k][j];
-            acc[j] = fmaf(dk * mv.y, mv.x - x[j], acc[j]);
+        for (int u = 0; u < KB; ++u) dk[u] = k0 + u < K ? d[(size_t)(k0 + u) * N] : 0.f;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            if (k0 + u >= K) break;
+            const float2 dd = make_float2(dk[u], dk[u]);
+#pragma unroll
+            for (int j = 0; j < J2; ++j) {
+                const float4 pv = sp[k0 + u][j];
+                acc[j] = __ffma2_rn(__fmul2_rn(dd, make_float2(pv.z, pv.w)),
+                                    __fadd2_rn(make_float2(pv.x, pv.y), nx[j]), acc[j]);
+            }
         }
     }
     float *o = dX + ((size_t)bh * N + i) * d_r + j0;
 #pragma unroll
-    for (int j = 0; j < JC; ++j)
-        if (j < nj) o[j] = acc[j];
+    for (int j = 0; j < J2; ++j)
+        if (2 * j < nj) {
+            o[2 * j] = acc[j].x;
+            o[2 * j + 1] = acc[j].y;
+        }
 }
 
-// Parameter statistics of one side over a range of rows, columns [32 z, 32 z + 32):
+// Parameter statistics of one side over a range of rows, columns
+// [4 TM z, 4 TM (z + 1)):
 //   st[k][0] = sum ds_ik,  st[k][1 + m] = sum ds_ik (x_im - mu_km),
 //   st[k][1 + d_r + m] = sum ds_ik (x_im - mu_km)^2
 // (centred on mu_km, so no cancellation).  Block: 256 threads, each a 4 (k) x 4 (m)
-// tile; rows staged 32 at a time in shared memory.
-template <typename T>
+// tile, TM threads across the columns and 256 / TM down the components (TM = 16
+// for K <= 64, so no thread is idle at K = d_r = 64); rows staged kCT at a time in
+// shared memory.  The column pairs use packed f32x2 arithmetic, which rounds each
+// element as the scalar operations do, so every sum has the same bits as a
+// thread-per-element loop over the rows in order.
+template <typename T, int TM>
 __global__ void __launch_bounds__(256) bwd_param_stats_kernel(const T *__restrict__ X, const float *__restrict__ ds,
                                                               const float *__restrict__ mu, int H, int N, int K,
                                                               int d_r, int rows_per_split, int nsplit, int side,
                                                               float *__restrict__ st, const unsigned *status) {
     if (failed(status)) return;
-    __shared__ float sd[128][kCT + 1];
-    __shared__ float sx[kCT][32 + 1];
+    constexpr int TK = 256 / TM, MC = 4 * TM, KC = 4 * TK;
+    __shared__ float sd[KC][kCT + 1];
+    __shared__ __align__(16) float sx[kCT][MC + 4];
     const int split = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int m0 = 32 * blockIdx.z;
+    const int m0 = MC * blockIdx.z;
     const int r0 = split * rows_per_split, r1 = min(N, r0 + rows_per_split);
-    const int tk = threadIdx.x >> 3, tm = threadIdx.x & 7;
+    const int tk = threadIdx.x / TM, tm = threadIdx.x % TM;
     const bool active = 4 * tk < K;
-    float a1[4][4], a2[4][4], a0[4], mk[4][4];
+    float2 a1[4][2], a2[4][2], nm[4][2];
+    float a0[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
         a0[a] = 0.f;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            a1[a][b] = a2[a][b] = 0.f;
-            const int k = 4 * tk + a, m = m0 + 4 * tm + b;
-            mk[a][b] = (k < K && m < d_r) ? mu[((size_t)h * K + k) * d_r + m] : 0.f;
+        for (int b = 0; b < 2; ++b) {
+            a1[a][b] = a2[a][b] = make_float2(0.f, 0.f);
+            const int k = 4 * tk + a, m = m0 + 4 * tm + 2 * b;
+            const float *mk = mu + ((size_t)h * K + k) * d_r + m;
+            nm[a][b] = make_float2((k < K && m < d_r) ? -mk[0] : 0.f, (k < K && m + 1 < d_r) ? -mk[1] : 0.f);
         }
     }
     const float *dsb = ds + (size_t)bh * K * N;
@@ -317,23 +373,26 @@ __global__ void __launch_bounds__(256) bwd_param_stats_kernel(const T *__restric
             const int k = e / kCT, t = e % kCT;
             sd[k][t] = t < n ? dsb[(size_t)k * N + base + t] : 0.f;
         }
-        for (int e = threadIdx.x; e < kCT * 32; e += blockDim.x) {
-            const int t = e / 32, m = e % 32;
+        for (int e = threadIdx.x; e < kCT * MC; e += blockDim.x) {
+            const int t = e / MC, m = e % MC;
             sx[t][m] = (t < n && m0 + m < d_r) ? to_f32(xb[(size_t)(base + t) * d_r + m0 + m]) : 0.f;
         }
         __syncthreads();
         if (active) {
             for (int t = 0; t < n; ++t) {
+                const float4 xv = *reinterpret_cast<const float4 *>(&sx[t][4 * tm]);
+                const float2 x2[2] = {make_float2(xv.x, xv.y), make_float2(xv.z, xv.w)};
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
                     const float d = 4 * tk + a < K ? sd[4 * tk + a][t] : 0.f;
                     a0[a] += d;
+                    const float2 dd = make_float2(d, d);
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const float diff = sx[t][4 * tm + b] - mk[a][b];
-                        const float dd = d * diff;
-                        a1[a][b] += dd;
-                        a2[a][b] = fmaf(dd, diff, a2[a][b]);
+                    for (int b = 0; b < 2; ++b) {
+                        const float2 diff = __fadd2_rn(x2[b], nm[a][b]);
+                        const float2 p = __fmul2_rn(dd, diff);
+                        a1[a][b] = __fadd2_rn(a1[a][b], p);
+                        a2[a][b] = __ffma2_rn(p, diff, a2[a][b]);
                     }
                 }
             }
@@ -351,8 +410,8 @@ __global__ void __launch_bounds__(256) bwd_param_stats_kernel(const T *__restric
         for (int b = 0; b < 4; ++b) {
             const int m = m0 + 4 * tm + b;
             if (m < d_r) {
-                p[(size_t)k * E + 1 + m] = a1[a][b];
-                p[(size_t)k * E + 1 + d_r + m] = a2[a][b];
+                p[(size_t)k * E + 1 + m] = b & 1 ? a1[a][b >> 1].y : a1[a][b >> 1].x;
+                p[(size_t)k * E + 1 + d_r + m] = b & 1 ? a2[a][b >> 1].y : a2[a][b >> 1].x;
             }
         }
     }
@@ -385,94 +444,117 @@ __global__ void bwd_param_final_kernel(const float *__restrict__ st, const float
     if (m == 0) dlog_pi[(size_t)h * K + k] = s0;
 }
 
-// Causal query rows, one block per chunk of C tokens, one thread per query
-// row i: num_i, den_i from the chunk's exclusive prefix (S, Z) plus the
-// intra-chunk terms j <= i; dnum_i, dden_i (written to dn); then
+// The causal chunk kernels give each row kBwdParts threads (a quad of adjacent
+// lanes): a thread holds the value columns c = kBwdParts q + l (l its lane in
+// the quad), splits the sums over components and over the rows of the chunk
+// the same way, and the quad adds its partial sums with two xor shuffles.  The
+// shuffle pattern gives every lane of the quad the same bits (each step adds
+// the same two values), so the lanes agree on every shared result.
+constexpr int kBwdParts = 4;
+// Row strides (floats) of the staged Gamma rows and of the b rows: 8 and 4
+// banks apart per component / row, so the four lanes of a quad and the eight
+// quads of a warp hit 32 different banks.
+constexpr int kBwdGS = kSimtCausalChunk + 8;
+constexpr int kBwdBS = kSimtCausalChunk + 4;
+
+__device__ __forceinline__ float quad_sum(float v, unsigned mask) {
+    v += __shfl_xor_sync(mask, v, 1);
+    v += __shfl_xor_sync(mask, v, 2);
+    return v;
+}
+
+// Causal query rows, one block per chunk of C tokens, one quad per query row i:
+// num_i, den_i from the chunk's exclusive prefix (S, Z) plus the intra-chunk
+// terms j <= i; dnum_i, dden_i (written to dn); then
 //   u_ik = dnum_i . S_k + dden_i Z_k + sum_{t0<=j<=i} gK_jk (dnum_i . V_j + dden_i)
 // and ds^Q_ik = gQ_ik (u_ik - sum_l gQ_il u_il) ([GMA, Eq. (18)]).
 template <int D_V, typename T>
-__global__ void __launch_bounds__(kSimtCausalChunk) bwd_causal_query_kernel(
+__global__ void __launch_bounds__(kSimtCausalChunk * kBwdParts, 2) bwd_causal_query_kernel(
     const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
     const float *__restrict__ prefix, const float *__restrict__ dO, int N, int K, int nchunk, float eps,
     float *__restrict__ dn, float *__restrict__ dsq, const unsigned *status) {
     if (failed(status)) return;
-    constexpr int C = kSimtCausalChunk;
+    constexpr int C = kSimtCausalChunk, P = kBwdParts, CQ = D_V / P, GS = kBwdGS, BS = kBwdBS;
     constexpr int W = D_V + 1;
     extern __shared__ float smem[];
-    float *sgq = smem;              // [K][C]
-    float *sgk = sgq + K * C;       // [K][C]
-    float *sv = sgk + K * C;        // [C][D_V]
+    float *sgq = smem;              // [K][GS]
+    float *sgk = sgq + K * GS;      // [K][GS]
+    float *sv = sgk + K * GS;       // [C][D_V]
     float *ss = sv + C * D_V;       // [K][W]
-    float *sb = ss + K * W;         // [C][C + 1]: b_ij of query row i
+    float *sb = ss + K * W;         // [C][BS]: b_ij of query row i
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int t0 = chunk * C;
     const int n = min(C, N - t0);
     const float *gq = gqt + (size_t)bh * K * N, *gk = gkt + (size_t)bh * K * N;
     for (int e = threadIdx.x; e < K * C; e += blockDim.x) {
         const int k = e / C, t = e % C;
-        sgq[e] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
-        sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
+        sgq[k * GS + t] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
+        sgk[k * GS + t] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
     }
     const T *v = V + ((size_t)bh * N + t0) * D_V;
     for (int e = threadIdx.x; e < C * D_V; e += blockDim.x) sv[e] = e < n * D_V ? to_f32(v[e]) : 0.f;
     const float *pre = prefix + ((size_t)bh * nchunk + chunk) * K * W;
     for (int e = threadIdx.x; e < K * W; e += blockDim.x) ss[e] = pre[e];
     __syncthreads();
-    const int i = threadIdx.x;
-    if (i >= n) return;
-    float acc[D_V];
+    const int i = threadIdx.x / P, l = threadIdx.x % P;
+    if (i >= n) return;  // whole quads leave together
+    const unsigned qm = 0xfu << (threadIdx.x & 28);
+    float acc[CQ];
 #pragma unroll
-    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
-    float den = 0.f;
+    for (int q = 0; q < CQ; ++q) acc[q] = 0.f;
+    float den = 0.f;  // the same in every lane of the quad
     for (int k = 0; k < K; ++k) {
-        const float g = sgq[k * C + i];
-        const float *row = ss + k * W;
+        const float g = sgq[k * GS + i];
+        const float *row = ss + k * W + l;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(g, row[c], acc[c]);
-        den = fmaf(g, row[D_V], den);
+        for (int q = 0; q < CQ; ++q) acc[q] = fmaf(g, row[P * q], acc[q]);
+        den = fmaf(g, ss[k * W + D_V], den);
     }
     for (int j = 0; j <= i; ++j) {
         float a = 0.f;
-        for (int k = 0; k < K; ++k) a = fmaf(sgq[k * C + i], sgk[k * C + j], a);
+        for (int k = l; k < K; k += P) a = fmaf(sgq[k * GS + i], sgk[k * GS + j], a);
+        a = quad_sum(a, qm);
         den += a;
-        const float *vr = sv + j * D_V;
+        const float *vr = sv + j * D_V + l;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(a, vr[c], acc[c]);
+        for (int q = 0; q < CQ; ++q) acc[q] = fmaf(a, vr[P * q], acc[q]);
     }
     den += eps;
     const float r = 1.0f / den;
-    const float *go = dO + ((size_t)bh * N + t0 + i) * D_V;
+    const float *go = dO + ((size_t)bh * N + t0 + i) * D_V + l;
     float *out = dn + ((size_t)bh * N + t0 + i) * W;
     float dot = 0.f;
 #pragma unroll
-    for (int c = 0; c < D_V; ++c) {
-        const float d = go[c];
-        dot = fmaf(d, acc[c] * r, dot);
-        acc[c] = d * r;  // dnum
-        out[c] = acc[c];
+    for (int q = 0; q < CQ; ++q) {
+        const float d = go[P * q];
+        dot = fmaf(d, acc[q] * r, dot);
+        acc[q] = d * r;  // dnum
+        out[P * q + l] = acc[q];
     }
-    const float dden = -dot * r;
-    out[D_V] = dden;
-    float *bi = sb + i * (C + 1);
+    const float dden = -quad_sum(dot, qm) * r;
+    if (l == 0) out[D_V] = dden;
+    float *bi = sb + i * BS;
     for (int j = 0; j <= i; ++j) {
-        const float *vr = sv + j * D_V;
-        float b = dden;
+        const float *vr = sv + j * D_V + l;
+        float b = 0.f;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) b = fmaf(acc[c], vr[c], b);
-        bi[j] = b;
+        for (int q = 0; q < CQ; ++q) b = fmaf(acc[q], vr[P * q], b);
+        b = quad_sum(b, qm) + dden;
+        if ((j & (P - 1)) == l) bi[j] = b;  // read back by this lane only
     }
     float *d = dsq + (size_t)bh * K * N + t0 + i;
     float mean = 0.f;
     for (int k = 0; k < K; ++k) {
-        const float *row = ss + k * W;
-        float u = dden * row[D_V];
+        const float *row = ss + k * W + l;
+        float u = 0.f;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) u = fmaf(acc[c], row[c], u);
-        for (int j = 0; j <= i; ++j) u = fmaf(sgk[k * C + j], bi[j], u);
-        d[(size_t)k * N] = u;
-        mean = fmaf(sgq[k * C + i], u, mean);
+        for (int q = 0; q < CQ; ++q) u = fmaf(acc[q], row[P * q], u);
+        for (int j = l; j <= i; j += P) u = fmaf(sgk[k * GS + j], bi[j], u);
+        u = quad_sum(u, qm) + dden * ss[k * W + D_V];
+        if ((k & (P - 1)) == l) d[(size_t)k * N] = u;
+        mean = fmaf(sgq[k * GS + i], u, mean);
     }
-    for (int k = 0; k < K; ++k) d[(size_t)k * N] = sgq[k * C + i] * (d[(size_t)k * N] - mean);
+    for (int k = l; k < K; k += P) d[(size_t)k * N] = sgq[k * GS + i] * (d[(size_t)k * N] - mean);
 }
 
 // In-place exclusive suffix over the chunk aggregates of each head, in reverse
@@ -504,85 +586,93 @@ __global__ void bwd_suffix_scan_kernel(float *__restrict__ part, int nchunk, int
     }
 }
 
-// Causal key rows, one block per chunk, one thread per key row j: with (D, E)
+// Causal key rows, one block per chunk, one quad per key row j: with (D, E)
 // the suffix over the later chunks (suf) plus the intra-chunk queries i >= j,
 //   u_jk = V_j . D_k + E_k,   ds^K_jk = gK_jk (u_jk - sum_l gK_jl u_jl),
 //   dV_j = sum_k gK_jk D_k = gK_j . suf + sum_{i>=j} <gK_j, gQ_i> dnum_i.
+// The loops over the chunk's queries run from the last row down, so the quads
+// of a warp (consecutive j) visit the same row i at the same time.
 template <int D_V, typename T>
-__global__ void __launch_bounds__(kSimtCausalChunk) bwd_causal_key_kernel(
+__global__ void __launch_bounds__(kSimtCausalChunk * kBwdParts, 2) bwd_causal_key_kernel(
     const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
     const float *__restrict__ dn, const float *__restrict__ suf, int N, int K, int nchunk,
     float *__restrict__ dsk, float *__restrict__ dV, const unsigned *status) {
     if (failed(status)) return;
-    constexpr int C = kSimtCausalChunk;
+    constexpr int C = kSimtCausalChunk, P = kBwdParts, CQ = D_V / P, GS = kBwdGS, BS = kBwdBS;
     constexpr int W = D_V + 1;
     extern __shared__ float smem[];
-    float *sgq = smem;              // [K][C]
-    float *sgk = sgq + K * C;       // [K][C]
-    float *sdn = sgk + K * C;       // [C][W]: dnum | dden of the chunk's queries
+    float *sgq = smem;              // [K][GS]
+    float *sgk = sgq + K * GS;      // [K][GS]
+    float *sdn = sgk + K * GS;      // [C][W]: dnum | dden of the chunk's queries
     float *ss = sdn + C * W;        // [K][W]: suffix over the later chunks
-    float *sb = ss + K * W;         // [C][C + 1]: b_ji of key row j
+    float *sb = ss + K * W;         // [C][BS]: b_ji of key row j
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int t0 = chunk * C;
     const int n = min(C, N - t0);
     const float *gq = gqt + (size_t)bh * K * N, *gk = gkt + (size_t)bh * K * N;
     for (int e = threadIdx.x; e < K * C; e += blockDim.x) {
         const int k = e / C, t = e % C;
-        sgq[e] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
-        sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
+        sgq[k * GS + t] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
+        sgk[k * GS + t] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
     }
     const float *dnc = dn + ((size_t)bh * N + t0) * W;
     for (int e = threadIdx.x; e < C * W; e += blockDim.x) sdn[e] = e < n * W ? dnc[e] : 0.f;
     const float *sp = suf + ((size_t)bh * nchunk + chunk) * K * W;
     for (int e = threadIdx.x; e < K * W; e += blockDim.x) ss[e] = sp[e];
     __syncthreads();
-    const int j = threadIdx.x;
-    if (j >= n) return;
-    float *bj = sb + j * (C + 1);
+    const int j = threadIdx.x / P, l = threadIdx.x % P;
+    if (j >= n) return;  // whole quads leave together
+    const unsigned qm = 0xfu << (threadIdx.x & 28);
+    float *bj = sb + j * BS;
     float *d = dsk + (size_t)bh * K * N + t0 + j;
     {
-        float v[D_V];
-        const T *vr = V + ((size_t)bh * N + t0 + j) * D_V;
+        float v[CQ];
+        const T *vr = V + ((size_t)bh * N + t0 + j) * D_V + l;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) v[c] = to_f32(vr[c]);
-        for (int i = j; i < n; ++i) {
-            const float *dr = sdn + i * W;
-            float b = dr[D_V];
+        for (int q = 0; q < CQ; ++q) v[q] = to_f32(vr[P * q]);
+        for (int i = n - 1; i >= j; --i) {
+            const float *dr = sdn + i * W + l;
+            float b = 0.f;
 #pragma unroll
-            for (int c = 0; c < D_V; ++c) b = fmaf(v[c], dr[c], b);
-            bj[i] = b;
+            for (int q = 0; q < CQ; ++q) b = fmaf(v[q], dr[P * q], b);
+            b = quad_sum(b, qm) + sdn[i * W + D_V];
+            if ((i & (P - 1)) == l) bj[i] = b;  // read back by this lane only
         }
+        const int i0 = (j & ~(P - 1)) + l;  // first row of this lane's share (rows below j skipped)
         float mean = 0.f;
         for (int k = 0; k < K; ++k) {
-            const float *row = ss + k * W;
-            float u = row[D_V];
+            const float *row = ss + k * W + l;
+            float u = 0.f;
 #pragma unroll
-            for (int c = 0; c < D_V; ++c) u = fmaf(v[c], row[c], u);
-            for (int i = j; i < n; ++i) u = fmaf(sgq[k * C + i], bj[i], u);
-            d[(size_t)k * N] = u;
-            mean = fmaf(sgk[k * C + j], u, mean);
+            for (int q = 0; q < CQ; ++q) u = fmaf(v[q], row[P * q], u);
+            for (int i = i0; i < n; i += P)
+                if (i >= j) u = fmaf(sgq[k * GS + i], bj[i], u);
+            u = quad_sum(u, qm) + ss[k * W + D_V];
+            if ((k & (P - 1)) == l) d[(size_t)k * N] = u;
+            mean = fmaf(sgk[k * GS + j], u, mean);
         }
-        for (int k = 0; k < K; ++k) d[(size_t)k * N] = sgk[k * C + j] * (d[(size_t)k * N] - mean);
+        for (int k = l; k < K; k += P) d[(size_t)k * N] = sgk[k * GS + j] * (d[(size_t)k * N] - mean);
     }
-    float acc[D_V];
+    float acc[CQ];
 #pragma unroll
-    for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
+    for (int q = 0; q < CQ; ++q) acc[q] = 0.f;
     for (int k = 0; k < K; ++k) {
-        const float g = sgk[k * C + j];
-        const float *row = ss + k * W;
+        const float g = sgk[k * GS + j];
+        const float *row = ss + k * W + l;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(g, row[c], acc[c]);
+        for (int q = 0; q < CQ; ++q) acc[q] = fmaf(g, row[P * q], acc[q]);
     }
-    for (int i = j; i < n; ++i) {
+    for (int i = n - 1; i >= j; --i) {
         float w = 0.f;
-        for (int k = 0; k < K; ++k) w = fmaf(sgk[k * C + j], sgq[k * C + i], w);
-        const float *dr = sdn + i * W;
+        for (int k = l; k < K; k += P) w = fmaf(sgk[k * GS + j], sgq[k * GS + i], w);
+        w = quad_sum(w, qm);
+        const float *dr = sdn + i * W + l;
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(w, dr[c], acc[c]);
+        for (int q = 0; q < CQ; ++q) acc[q] = fmaf(w, dr[P * q], acc[q]);
     }
-    float *o = dV + ((size_t)bh * N + t0 + j) * D_V;
+    float *o = dV + ((size_t)bh * N + t0 + j) * D_V + l;
 #pragma unroll
-    for (int c = 0; c < D_V; ++c) o[c] = acc[c];
+    for (int q = 0; q < CQ; ++q) o[P * q] = acc[q];
 }
 
 struct BwdLayout {
@@ -685,13 +775,20 @@ cudaError_t launch_inputs(const Problem &p, const BwdLayout &L, const BackwardAr
     bwd_dx_kernel<T><<<gx, 128, 0, s>>>(Kx, dsk, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dK, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    const dim3 gs(L.sn, p.BH(), (p.d_r + 31) / 32);  // z: 32-column block of d_r
-    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Q, dsq, p.mu, p.H, p.N, p.K, p.d_r, L.srows, L.sn, 0, st,
-                                                status);
-    GMA_TRY(cudaGetLastError());
-    bwd_param_stats_kernel<T><<<gs, 256, 0, s>>>(Kx, dsk, p.mu, p.H, p.N, p.K, p.d_r, L.srows, L.sn, 1, st,
-                                                status);
-    GMA_TRY(cudaGetLastError());
+    // 64 columns x 64 components per block when K <= 64 and d_r >= 64, else 32 x 128
+    const bool wide = p.K <= 64 && p.d_r >= 64;
+    const dim3 gs(L.sn, p.BH(), (p.d_r + (wide ? 63 : 31)) / (wide ? 64 : 32));  // z: column block of d_r
+    for (int side = 0; side < 2; ++side) {
+        const T *X = side ? Kx : Q;
+        const float *dss = side ? dsk : dsq;
+        if (wide)
+            bwd_param_stats_kernel<T, 16><<<gs, 256, 0, s>>>(X, dss, p.mu, p.H, p.N, p.K, p.d_r, L.srows, L.sn,
+                                                            side, st, status);
+        else
+            bwd_param_stats_kernel<T, 8><<<gs, 256, 0, s>>>(X, dss, p.mu, p.H, p.N, p.K, p.d_r, L.srows, L.sn,
+                                                           side, st, status);
+        GMA_TRY(cudaGetLastError());
+    }
     bwd_param_final_kernel<<<dim3((p.K * p.d_r + 127) / 128, p.H), 128, 0, s>>>(
         st, inv, p.B, p.H, p.K, p.d_r, L.sn, g.dmu, g.dsigma2, g.dlog_pi, status);
     GMA_TRY(cudaGetLastError());
@@ -711,11 +808,12 @@ cudaError_t launch_causal_rows(const Problem &p, const BwdLayout &L, const Backw
     const T *V = static_cast<const T *>(p.V);
     const int nchunk = L.F.nsplit;
     const dim3 grid(nchunk, p.BH());
-    const size_t smq = sizeof(float) * ((size_t)2 * p.K * C + (size_t)C * D_V + (size_t)p.K * W + (size_t)C * (C + 1));
-    const size_t smk = sizeof(float) * ((size_t)2 * p.K * C + (size_t)C * W + (size_t)p.K * W + (size_t)C * (C + 1));
+    constexpr int GS = kBwdGS, BS = kBwdBS, NT = C * kBwdParts;
+    const size_t smq = sizeof(float) * ((size_t)2 * p.K * GS + (size_t)C * D_V + (size_t)p.K * W + (size_t)C * BS);
+    const size_t smk = sizeof(float) * ((size_t)2 * p.K * GS + (size_t)C * W + (size_t)p.K * W + (size_t)C * BS);
     GMA_TRY(cudaFuncSetAttribute(bwd_causal_query_kernel<D_V, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smq));
-    bwd_causal_query_kernel<D_V, T><<<grid, C, smq, s>>>(gq, gk, V, prefix, g.dO, p.N, p.K, nchunk, p.eps, dn, dsq,
+    bwd_causal_query_kernel<D_V, T><<<grid, NT, smq, s>>>(gq, gk, V, prefix, g.dO, p.N, p.K, nchunk, p.eps, dn, dsq,
                                                          status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
@@ -727,7 +825,7 @@ cudaError_t launch_causal_rows(const Problem &p, const BwdLayout &L, const Backw
     clk.mark();
     GMA_TRY(cudaFuncSetAttribute(bwd_causal_key_kernel<D_V, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smk));
-    bwd_causal_key_kernel<D_V, T><<<grid, C, smk, s>>>(gq, gk, V, dn, dpart, p.N, p.K, nchunk, dsk, g.dV, status);
+    bwd_causal_key_kernel<D_V, T><<<grid, NT, smk, s>>>(gq, gk, V, dn, dpart, p.N, p.K, nchunk, dsk, g.dV, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     return cudaSuccess;
