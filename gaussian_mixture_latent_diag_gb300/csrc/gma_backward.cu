@@ -160,10 +160,13 @@ __global__ void __launch_bounds__(128) bwd_score_grad_kernel(const float *__rest
 }
 
 // Column sums over a range of rows: part[bh][split][k][c] = sum_{i in split} G[k][i] B[i][c]
-// for c in [64 z, 64 z + 64) and c < ncol.  G [K][N] (component-major), B rows of
-// ldb floats.  Block: 256 threads, each 4 components (k) x 8 columns (c, taken
-// interleaved, c = tc + 8 b, so a warp reads consecutive columns); rows staged
-// 32 at a time in shared memory; fixed summation order.
+// for c in [64 z, 64 z + 64) and c < ncol; the last block also takes column
+// 64 (z + 1) when that is the last column (ncol = 64 m + 1: the [dnum | dden]
+// rows), so the lone column needs no block of its own.  G [K][N]
+// (component-major), B rows of ldb floats.  Block: 256 threads, each 4
+// components (k) x 8 columns (c, taken interleaved, c = tc + 8 b, so a warp
+// reads consecutive columns; the extra column by the tc = 0 threads); rows
+// staged 32 at a time in shared memory; fixed summation order.
 constexpr int kCT = 32;
 __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict__ Gt,
                                                          const float *__restrict__ B, int ldb, int ncol,
@@ -176,11 +179,15 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict
     const int r0 = split * rows_per_split, r1 = min(N, r0 + rows_per_split);
     const int tk = threadIdx.x >> 3, tc = threadIdx.x & 7;  // k tile (4 rows), c tile (8 columns)
     const bool active = 4 * tk < K;
-    float acc[4][8];
+    const bool extra = c0 + 64 == ncol - 1;  // the lone last column rides with this block
+    const int sc = extra ? 65 : 64;          // staged columns
+    float acc[4][8], ex[4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 4; ++a) {
+        ex[a] = 0.f;
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+    }
     const float *g = Gt + (size_t)bh * K * N;
     const float *bb = B + (size_t)bh * N * ldb;
     for (int base = r0; base < r1; base += kCT) {
@@ -190,8 +197,8 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict
             const int k = e / kCT, t = e % kCT;
             sg[k][t] = t < n ? g[(size_t)k * N + base + t] : 0.f;
         }
-        for (int e = threadIdx.x; e < kCT * 64; e += blockDim.x) {
-            const int t = e / 64, c = e % 64;
+        for (int e = threadIdx.x; e < kCT * sc; e += blockDim.x) {
+            const int t = e / sc, c = e % sc;
             sb[t][c] = (t < n && c0 + c < ncol) ? bb[(size_t)(base + t) * ldb + c0 + c] : 0.f;
         }
         __syncthreads();
@@ -206,6 +213,11 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
                     for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(ga[a], vb[b], acc[a][b]);
+                if (extra && tc == 0) {
+                    const float ve = sb[t][64];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) ex[a] = fmaf(ga[a], ve, ex[a]);
+                }
             }
         }
     }
@@ -220,8 +232,13 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float *__restrict
             const int c = c0 + tc + 8 * b;
             if (c < ncol) p[(size_t)k * ncol + c] = acc[a][b];
         }
+        if (extra && tc == 0) p[(size_t)k * ncol + c0 + 64] = ex[a];
     }
 }
+
+// Column blocks of bwd_colsum_kernel for ncol columns: 64 each, a lone last column
+// taken by the block before it.
+inline int colsum_blocks(int ncol) { return ncol > 64 && ncol % 64 == 1 ? ncol / 64 : (ncol + 63) / 64; }
 
 // Fixed-order sum of split partials: out[bh][e] = sum_s part[bh][s][e].
 __global__ void bwd_reduce_kernel(const float *__restrict__ part, int nsplit, int E, float *__restrict__ out,
@@ -689,8 +706,10 @@ struct BwdLayout {
 BwdLayout bwd_layout(const Problem &p, int causal, int splits) {
     BwdLayout L;
     L.F = simt_layout(p, causal, causal ? 0 : splits);
-    if (causal) {
-        L.srows = 1024;
+    if (causal || splits <= 0) {
+        // 512 rows per block of the parameter statistics: twice the blocks of the
+        // write's 1024-row splits, so the last wave of the grid is not mostly empty
+        L.srows = 512;
         L.sn = (p.N + L.srows - 1) / L.srows;
     } else {
         L.srows = L.F.tokens_per_split;
@@ -737,7 +756,7 @@ cudaError_t launch_rows(const Problem &p, const BwdLayout &L, const BackwardArgs
     GMA_TRY(cudaGetLastError());
     clk.mark();
     const int W = D_V + 1;
-    bwd_colsum_kernel<<<dim3(L.F.nsplit, p.BH(), (W + 63) / 64), 256, 0, s>>>(gq, dn, W, W, p.N, p.K,
+    bwd_colsum_kernel<<<dim3(L.F.nsplit, p.BH(), colsum_blocks(W)), 256, 0, s>>>(gq, dn, W, W, p.N, p.K,
                                                                              L.F.tokens_per_split, L.F.nsplit,
                                                                              dpart, status);
     GMA_TRY(cudaGetLastError());
@@ -817,7 +836,7 @@ cudaError_t launch_causal_rows(const Problem &p, const BwdLayout &L, const Backw
                                                          status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
-    bwd_colsum_kernel<<<dim3(nchunk, p.BH(), (W + 63) / 64), 256, 0, s>>>(gq, dn, W, W, p.N, p.K, C, nchunk, dpart,
+    bwd_colsum_kernel<<<dim3(nchunk, p.BH(), colsum_blocks(W)), 256, 0, s>>>(gq, dn, W, W, p.N, p.K, C, nchunk, dpart,
                                                                          status);
     GMA_TRY(cudaGetLastError());
     bwd_suffix_scan_kernel<<<dim3((p.K * W + 255) / 256, p.BH()), 256, 0, s>>>(dpart, nchunk, p.K * W, status);

@@ -146,14 +146,35 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
         }
     }
     if (!valid) return;
+    // The row goes through global memory twice more (exponentials, then the
+    // scale).  Eight components are loaded before any of them is stored back, so
+    // eight round trips overlap (the stores would otherwise order every load
+    // behind the previous store); the sum runs in component order as before.
+    constexpr int KB = 8;
     float z = 0.f;
-    for (int k = 0; k < K; ++k) {
-        float e = expf(o[(size_t)k * out_stride_k] - m);
-        o[(size_t)k * out_stride_k] = e;
-        z += e;
+    for (int k0 = 0; k0 < K; k0 += KB) {
+        float e[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) e[u] = k0 + u < K ? o[(size_t)(k0 + u) * out_stride_k] : 0.f;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            if (k0 + u >= K) break;
+            e[u] = expf(e[u] - m);
+            z += e[u];
+        }
+#pragma unroll
+        for (int u = 0; u < KB; ++u)
+            if (k0 + u < K) o[(size_t)(k0 + u) * out_stride_k] = e[u];
     }
     const float rz = 1.0f / z;
-    for (int k = 0; k < K; ++k) o[(size_t)k * out_stride_k] *= rz;
+    for (int k0 = 0; k0 < K; k0 += KB) {
+        float e[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) e[u] = k0 + u < K ? o[(size_t)(k0 + u) * out_stride_k] : 0.f;
+#pragma unroll
+        for (int u = 0; u < KB; ++u)
+            if (k0 + u < K) o[(size_t)(k0 + u) * out_stride_k] = e[u] * rz;
+    }
 }
 
 // Latent aggregation over one range of keys ([GMA, Eqs. (5)-(6)]):
@@ -356,12 +377,21 @@ __global__ void __launch_bounds__(128) read_simt_kernel(
     for (int c = 0; c < D_V; ++c) acc[c] = 0.f;
     float den = 0.f;
     const float *g = gqt + (size_t)bh * K * N + i;
-    for (int k = 0; k < K; ++k) {
-        float gk = g[(size_t)k * N];
-        const float *row = smem + k * W;
+    // Gamma^Q is read with a stride of N: four components are loaded before
+    // their use, so four round trips overlap (component order unchanged)
+    constexpr int KB = 4;
+    for (int k0 = 0; k0 < K; k0 += KB) {
+        float gv[KB];
 #pragma unroll
-        for (int c = 0; c < D_V; ++c) acc[c] = fmaf(gk, row[c], acc[c]);
-        den = fmaf(gk, row[D_V], den);
+        for (int u = 0; u < KB; ++u) gv[u] = k0 + u < K ? g[(size_t)(k0 + u) * N] : 0.f;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            if (k0 + u >= K) break;
+            const float *row = smem + (k0 + u) * W;
+#pragma unroll
+            for (int c = 0; c < D_V; ++c) acc[c] = fmaf(gv[u], row[c], acc[c]);
+            den = fmaf(gv[u], row[D_V], den);
+        }
     }
     const float r = 1.0f / (den + eps);
     TO *o = O + ((size_t)bh * N + i) * D_V;
