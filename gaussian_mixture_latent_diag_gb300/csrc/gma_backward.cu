@@ -527,7 +527,25 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kBwdParts, 2) bwd_causal_qu
         for (int q = 0; q < CQ; ++q) acc[q] = fmaf(g, row[P * q], acc[q]);
         den = fmaf(g, ss[k * W + D_V], den);
     }
-    for (int j = 0; j <= i; ++j) {
+    // Rows j in pairs: two independent dot / shuffle chains per iteration; the
+    // accumulations still run in j order.
+    int j = 0;
+    for (; j + 1 <= i; j += 2) {
+        float a0 = 0.f, a1 = 0.f;
+        for (int k = l; k < K; k += P) {
+            const float gqk = sgq[k * GS + i];
+            a0 = fmaf(gqk, sgk[k * GS + j], a0);
+            a1 = fmaf(gqk, sgk[k * GS + j + 1], a1);
+        }
+        a0 = quad_sum(a0, qm);
+        a1 = quad_sum(a1, qm);
+        den += a0;
+        den += a1;
+        const float *v0 = sv + j * D_V + l, *v1 = v0 + D_V;
+#pragma unroll
+        for (int q = 0; q < CQ; ++q) acc[q] = fmaf(a1, v1[P * q], fmaf(a0, v0[P * q], acc[q]));
+    }
+    if (j == i) {
         float a = 0.f;
         for (int k = l; k < K; k += P) a = fmaf(sgq[k * GS + i], sgk[k * GS + j], a);
         a = quad_sum(a, qm);
@@ -551,22 +569,56 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kBwdParts, 2) bwd_causal_qu
     const float dden = -quad_sum(dot, qm) * r;
     if (l == 0) out[D_V] = dden;
     float *bi = sb + i * BS;
-    for (int j = 0; j <= i; ++j) {
+    for (j = 0; j + 1 <= i; j += 2) {
+        const float *v0 = sv + j * D_V + l, *v1 = v0 + D_V;
+        float b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < CQ; ++q) {
+            b0 = fmaf(acc[q], v0[P * q], b0);
+            b1 = fmaf(acc[q], v1[P * q], b1);
+        }
+        b0 = quad_sum(b0, qm) + dden;
+        b1 = quad_sum(b1, qm) + dden;
+        if ((j & (P - 1)) == l) bi[j] = b0;  // read back by this lane only
+        if (((j + 1) & (P - 1)) == l) bi[j + 1] = b1;
+    }
+    if (j == i) {
         const float *vr = sv + j * D_V + l;
         float b = 0.f;
 #pragma unroll
         for (int q = 0; q < CQ; ++q) b = fmaf(acc[q], vr[P * q], b);
         b = quad_sum(b, qm) + dden;
-        if ((j & (P - 1)) == l) bi[j] = b;  // read back by this lane only
+        if ((j & (P - 1)) == l) bi[j] = b;
     }
     float *d = dsq + (size_t)bh * K * N + t0 + i;
     float mean = 0.f;
-    for (int k = 0; k < K; ++k) {
+    int k = 0;
+    for (; k + 1 < K; k += 2) {  // components in pairs, accumulated in k order
+        const float *r0 = ss + k * W + l, *r1 = r0 + W;
+        float u0 = 0.f, u1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < CQ; ++q) {
+            u0 = fmaf(acc[q], r0[P * q], u0);
+            u1 = fmaf(acc[q], r1[P * q], u1);
+        }
+        for (int jj = l; jj <= i; jj += P) {
+            const float bj = bi[jj];
+            u0 = fmaf(sgk[k * GS + jj], bj, u0);
+            u1 = fmaf(sgk[(k + 1) * GS + jj], bj, u1);
+        }
+        u0 = quad_sum(u0, qm) + dden * ss[k * W + D_V];
+        u1 = quad_sum(u1, qm) + dden * ss[(k + 1) * W + D_V];
+        if ((k & (P - 1)) == l) d[(size_t)k * N] = u0;
+        if (((k + 1) & (P - 1)) == l) d[(size_t)(k + 1) * N] = u1;
+        mean = fmaf(sgq[k * GS + i], u0, mean);
+        mean = fmaf(sgq[(k + 1) * GS + i], u1, mean);
+    }
+    if (k < K) {
         const float *row = ss + k * W + l;
         float u = 0.f;
 #pragma unroll
         for (int q = 0; q < CQ; ++q) u = fmaf(acc[q], row[P * q], u);
-        for (int j = l; j <= i; j += P) u = fmaf(sgk[k * GS + j], bi[j], u);
+        for (int jj = l; jj <= i; jj += P) u = fmaf(sgk[k * GS + jj], bi[jj], u);
         u = quad_sum(u, qm) + dden * ss[k * W + D_V];
         if ((k & (P - 1)) == l) d[(size_t)k * N] = u;
         mean = fmaf(sgq[k * GS + i], u, mean);
@@ -647,23 +699,59 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kBwdParts, 2) bwd_causal_ke
         const T *vr = V + ((size_t)bh * N + t0 + j) * D_V + l;
 #pragma unroll
         for (int q = 0; q < CQ; ++q) v[q] = to_f32(vr[P * q]);
-        for (int i = n - 1; i >= j; --i) {
+        int i = n - 1;
+        for (; i - 1 >= j; i -= 2) {  // rows in pairs: two independent shuffle chains
+            const float *d0 = sdn + i * W + l, *d1 = d0 - W;
+            float b0 = 0.f, b1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < CQ; ++q) {
+                b0 = fmaf(v[q], d0[P * q], b0);
+                b1 = fmaf(v[q], d1[P * q], b1);
+            }
+            b0 = quad_sum(b0, qm) + sdn[i * W + D_V];
+            b1 = quad_sum(b1, qm) + sdn[(i - 1) * W + D_V];
+            if ((i & (P - 1)) == l) bj[i] = b0;  // read back by this lane only
+            if (((i - 1) & (P - 1)) == l) bj[i - 1] = b1;
+        }
+        if (i == j) {
             const float *dr = sdn + i * W + l;
             float b = 0.f;
 #pragma unroll
             for (int q = 0; q < CQ; ++q) b = fmaf(v[q], dr[P * q], b);
             b = quad_sum(b, qm) + sdn[i * W + D_V];
-            if ((i & (P - 1)) == l) bj[i] = b;  // read back by this lane only
+            if ((i & (P - 1)) == l) bj[i] = b;
         }
         const int i0 = (j & ~(P - 1)) + l;  // first row of this lane's share (rows below j skipped)
         float mean = 0.f;
-        for (int k = 0; k < K; ++k) {
+        int k = 0;
+        for (; k + 1 < K; k += 2) {  // components in pairs, accumulated in k order
+            const float *r0 = ss + k * W + l, *r1 = r0 + W;
+            float u0 = 0.f, u1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < CQ; ++q) {
+                u0 = fmaf(v[q], r0[P * q], u0);
+                u1 = fmaf(v[q], r1[P * q], u1);
+            }
+            for (int ii = i0; ii < n; ii += P)
+                if (ii >= j) {
+                    const float b = bj[ii];
+                    u0 = fmaf(sgq[k * GS + ii], b, u0);
+                    u1 = fmaf(sgq[(k + 1) * GS + ii], b, u1);
+                }
+            u0 = quad_sum(u0, qm) + ss[k * W + D_V];
+            u1 = quad_sum(u1, qm) + ss[(k + 1) * W + D_V];
+            if ((k & (P - 1)) == l) d[(size_t)k * N] = u0;
+            if (((k + 1) & (P - 1)) == l) d[(size_t)(k + 1) * N] = u1;
+            mean = fmaf(sgk[k * GS + j], u0, mean);
+            mean = fmaf(sgk[(k + 1) * GS + j], u1, mean);
+        }
+        if (k < K) {
             const float *row = ss + k * W + l;
             float u = 0.f;
 #pragma unroll
             for (int q = 0; q < CQ; ++q) u = fmaf(v[q], row[P * q], u);
-            for (int i = i0; i < n; i += P)
-                if (i >= j) u = fmaf(sgq[k * GS + i], bj[i], u);
+            for (int ii = i0; ii < n; ii += P)
+                if (ii >= j) u = fmaf(sgq[k * GS + ii], bj[ii], u);
             u = quad_sum(u, qm) + ss[k * W + D_V];
             if ((k & (P - 1)) == l) d[(size_t)k * N] = u;
             mean = fmaf(sgk[k * GS + j], u, mean);
@@ -679,7 +767,21 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kBwdParts, 2) bwd_causal_ke
 #pragma unroll
         for (int q = 0; q < CQ; ++q) acc[q] = fmaf(g, row[P * q], acc[q]);
     }
-    for (int i = n - 1; i >= j; --i) {
+    int i = n - 1;
+    for (; i - 1 >= j; i -= 2) {  // rows in pairs, accumulated in the same (descending) order
+        float w0 = 0.f, w1 = 0.f;
+        for (int k = l; k < K; k += P) {
+            const float gkj = sgk[k * GS + j];
+            w0 = fmaf(gkj, sgq[k * GS + i], w0);
+            w1 = fmaf(gkj, sgq[k * GS + i - 1], w1);
+        }
+        w0 = quad_sum(w0, qm);
+        w1 = quad_sum(w1, qm);
+        const float *d0 = sdn + i * W + l, *d1 = d0 - W;
+#pragma unroll
+        for (int q = 0; q < CQ; ++q) acc[q] = fmaf(w1, d1[P * q], fmaf(w0, d0[P * q], acc[q]));
+    }
+    if (i == j) {
         float w = 0.f;
         for (int k = l; k < K; k += P) w = fmaf(sgk[k * GS + j], sgq[k * GS + i], w);
         w = quad_sum(w, qm);
