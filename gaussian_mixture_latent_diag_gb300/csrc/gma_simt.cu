@@ -406,18 +406,22 @@ __global__ void __launch_bounds__(128) read_simt_kernel(
 // Four threads per query row (kCausalParts), each owning a quarter of the
 // output columns.  The intra-chunk dots <gQ_i, gK_j> are split over j: part q
 // computes them for j = 4m + q and the four parts exchange them by shuffles,
-// so the shared-memory reads are broadcasts without padding.  The prefix rows
-// are staged kCausalKT at a time, each row as four column quarters padded to a
-// multiple of 4 floats, then Z, and V likewise, so the four parts read
-// distinct banks with 16-byte loads.
-// Summation orders are those of the definition: k for the prefix, then j.
+// so the Gamma reads are broadcasts: the chunk's Gamma^Q and Gamma^K are staged
+// token-major ([C][KS], components zero-padded to a multiple of 4, rows 16 bytes
+// apart modulo 128) and the dots read four components per 16-byte load.  The
+// prefix rows are staged kCausalKT at a time, each row as four column quarters
+// padded to a multiple of 4 floats, then Z, and V likewise, so the four parts
+// read distinct banks with 16-byte loads.
+// Summation orders are those of the definition: k for the prefix, then j (the
+// zero padding adds exact zeros).
 constexpr int kCausalParts = 4;
 constexpr int kCausalKT = 16;
 template <int D_V>
 struct CausalSmem {
     static constexpr int P = kCausalParts, CW = D_V / P, SQ = CW + 4, SR = P * SQ + 4;
+    __host__ __device__ static int ks(int K) { return ((K + 3) & ~3) + 4; }  // floats per staged Gamma row
     static size_t floats(int K) {
-        return (size_t)2 * K * kSimtCausalChunk + (size_t)kSimtCausalChunk * P * SQ + (size_t)kCausalKT * SR;
+        return (size_t)2 * ks(K) * kSimtCausalChunk + (size_t)kSimtCausalChunk * P * SQ + (size_t)kCausalKT * SR;
     }
 };
 template <int D_V, typename T, typename TO>
@@ -431,18 +435,20 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
     using L = CausalSmem<D_V>;
     constexpr int P = L::P, CW = L::CW, SQ = L::SQ, SR = L::SR;
     extern __shared__ __align__(16) float smem[];
-    float *sgq = smem;              // [K][C]
-    float *sgk = sgq + K * C;       // [K][C]
-    float *sv = sgk + K * C;        // [C][P * SQ]: V rows in padded quarters
+    const int KS = L::ks(K), K4 = (K + 3) / 4;
+    float *sgq = smem;              // [C][KS]: token-major Gamma^Q of the chunk
+    float *sgk = sgq + C * KS;      // [C][KS]
+    float *sv = sgk + C * KS;       // [C][P * SQ]: V rows in padded quarters
     float *ss = sv + C * P * SQ;    // [kCausalKT][SR]: prefix rows in padded quarters, then Z
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int t0 = chunk * C;
     const int n = min(C, N - t0);
     const float *gq = gqt + (size_t)bh * K * N, *gk = gkt + (size_t)bh * K * N;
-    for (int e = threadIdx.x; e < K * C; e += blockDim.x) {
-        int k = e / C, t = e % C;
-        sgq[e] = t < n ? gq[(size_t)k * N + t0 + t] : 0.f;
-        sgk[e] = t < n ? gk[(size_t)k * N + t0 + t] : 0.f;
+    for (int e = threadIdx.x; e < 4 * K4 * C; e += blockDim.x) {
+        const int k = e / C, t = e % C;
+        const bool in = t < n && k < K;
+        sgq[t * KS + k] = in ? gq[(size_t)k * N + t0 + t] : 0.f;
+        sgk[t * KS + k] = in ? gk[(size_t)k * N + t0 + t] : 0.f;
     }
     const T *v = V + ((size_t)bh * N + t0) * D_V;
     for (int e = threadIdx.x; e < C * D_V; e += blockDim.x) {
@@ -464,7 +470,7 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
         }
         __syncthreads();
         for (int kk = 0; kk < nk; ++kk) {
-            const float g = sgq[(k0 + kk) * C + i];
+            const float g = sgq[i * KS + k0 + kk];
             const float4 *row = reinterpret_cast<const float4 *>(ss + kk * SR + q * SQ);
 #pragma unroll
             for (int c4 = 0; c4 < CW / 4; ++c4) {
@@ -479,26 +485,46 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
     }
     // intra-chunk terms j <= i; the loop runs to the warp's last row, so every
     // lane of the warp takes part in every shuffle
+    // Two groups of P rows per iteration: each lane runs two independent dot
+    // chains (rows j0 + q and j0 + P + q, each in component order), and the
+    // groups are accumulated in row order.
     const int wlast = min(n - 1, (threadIdx.x / 32) * (32 / P) + (32 / P) - 1);
-    for (int j0 = 0; j0 <= wlast; j0 += P) {
-        const int j = j0 + q;
-        float a = 0.f;
-        if (j <= wlast)
-            for (int k = 0; k < K; ++k) a = fmaf(sgq[k * C + i], sgk[k * C + j], a);
+    for (int j0 = 0; j0 <= wlast; j0 += 2 * P) {
+        const int ja = j0 + q, jb = j0 + P + q;
+        float ab[2] = {0.f, 0.f};
+        const float4 *gi = reinterpret_cast<const float4 *>(sgq + i * KS);
+        const float4 *ga = reinterpret_cast<const float4 *>(sgk + min(ja, C - 1) * KS);
+        const float4 *gb = reinterpret_cast<const float4 *>(sgk + min(jb, C - 1) * KS);
+        if (jb <= wlast) {
+            for (int k4 = 0; k4 < K4; ++k4) {
+                const float4 g = gi[k4], x = ga[k4], y = gb[k4];
+                ab[0] = fmaf(g.w, x.w, fmaf(g.z, x.z, fmaf(g.y, x.y, fmaf(g.x, x.x, ab[0]))));
+                ab[1] = fmaf(g.w, y.w, fmaf(g.z, y.z, fmaf(g.y, y.y, fmaf(g.x, y.x, ab[1]))));
+            }
+        } else if (ja <= wlast) {
+            for (int k4 = 0; k4 < K4; ++k4) {
+                const float4 g = gi[k4], x = ga[k4];
+                ab[0] = fmaf(g.w, x.w, fmaf(g.z, x.z, fmaf(g.y, x.y, fmaf(g.x, x.x, ab[0]))));
+            }
+        }
 #pragma unroll
-        for (int p2 = 0; p2 < P; ++p2) {
-            const float ap = __shfl_sync(0xffffffffu, a, (lane & ~(P - 1)) | p2);
-            const int jj = j0 + p2;
-            if (jj <= i) {
-                den += ap;
-                const float4 *vr = reinterpret_cast<const float4 *>(sv + jj * P * SQ + q * SQ);
+        for (int gsel = 0; gsel < 2; ++gsel) {
+            if (j0 + gsel * P > wlast) break;  // the same for the whole warp
 #pragma unroll
-                for (int c4 = 0; c4 < CW / 4; ++c4) {
-                    const float4 r = vr[c4];
-                    acc[4 * c4 + 0] = fmaf(ap, r.x, acc[4 * c4 + 0]);
-                    acc[4 * c4 + 1] = fmaf(ap, r.y, acc[4 * c4 + 1]);
-                    acc[4 * c4 + 2] = fmaf(ap, r.z, acc[4 * c4 + 2]);
-                    acc[4 * c4 + 3] = fmaf(ap, r.w, acc[4 * c4 + 3]);
+            for (int p2 = 0; p2 < P; ++p2) {
+                const float ap = __shfl_sync(0xffffffffu, ab[gsel], (lane & ~(P - 1)) | p2);
+                const int jj = j0 + gsel * P + p2;
+                if (jj <= i) {
+                    den += ap;
+                    const float4 *vr = reinterpret_cast<const float4 *>(sv + jj * P * SQ + q * SQ);
+#pragma unroll
+                    for (int c4 = 0; c4 < CW / 4; ++c4) {
+                        const float4 r = vr[c4];
+                        acc[4 * c4 + 0] = fmaf(ap, r.x, acc[4 * c4 + 0]);
+                        acc[4 * c4 + 1] = fmaf(ap, r.y, acc[4 * c4 + 1]);
+                        acc[4 * c4 + 2] = fmaf(ap, r.z, acc[4 * c4 + 2]);
+                        acc[4 * c4 + 3] = fmaf(ap, r.w, acc[4 * c4 + 3]);
+                    }
                 }
             }
         }
