@@ -1921,10 +1921,19 @@ TcLayout2 tc_layout2(const Problem &p, int splits, int causal) {
 // Read operand image of a caller's memory [Vt | Z] (fp32) for each head, the
 // same bf16 hi | lo layout the combine builds: row n < 64 holds Vt[:, n], row 64
 // Z, rows 65 .. 79 zero; column k of every row is component k (zero past K).
+// It is the first kernel of its call after the coefficient prep, so its first
+// warp also turns the prep's parameter checks into the call's status (the read
+// kernel then returns at once).
 __global__ void __launch_bounds__(256) pack_memory_tc_kernel(const float *__restrict__ Vt, const float *__restrict__ Z,
-                                                             int K, uint8_t *__restrict__ mem, size_t stride) {
+                                                             int K, uint8_t *__restrict__ mem, size_t stride,
+                                                             const unsigned *__restrict__ head_err, int H,
+                                                             unsigned *status) {
     constexpr int NBR = 64 + 16;
     const int bh = blockIdx.x;
+    if (bh == 0 && threadIdx.x < 32) {
+        const unsigned herr = head_error_warp(head_err, H, threadIdx.x);
+        if (herr && threadIdx.x == 0) set_status(status, herr);
+    }
     __nv_bfloat16 *bhi = reinterpret_cast<__nv_bfloat16 *>(mem + (size_t)bh * stride);
     __nv_bfloat16 *blo = reinterpret_cast<__nv_bfloat16 *>(mem + (size_t)bh * stride + NBR * 128);
     for (int e = threadIdx.x; e < NBR * kKP; e += blockDim.x) {
@@ -1964,7 +1973,8 @@ cudaError_t run_bidir2(const Problem &p, const TcLayout2 &L, uint8_t *ws, cudaSt
     if (pack_from) {
         // after the prep (a plain launch: the read's dependent-launch wait then
         // covers both), so the read sees the coefficients and the operand images
-        pack_memory_tc_kernel<<<p.BH(), 256, 0, s>>>(io.carry_vt, io.carry_z, p.K, mem, L.mem_stride);
+        pack_memory_tc_kernel<<<p.BH(), 256, 0, s>>>(io.carry_vt, io.carry_z, p.K, mem, L.mem_stride, head_err, p.H,
+                                                     status);
         GMA_TRY(cudaGetLastError());
     } else {
         GMA_TRY(set_smem(tc_write2_kernel, Write2Smem::kAlloc));

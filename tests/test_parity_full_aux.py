@@ -7,7 +7,9 @@ fp64 oracle on sampled outputs that it computes one by one:
 * diagnostics: the peaked-routing workload (B=16, H=4, N=16384, d_r = K = 32),
   usage, counts and hard assignments of 3 whole heads;
 * projections: X [4, 16384, 1024] to three [4, 8, 16384, 64] bf16 tensors,
-  64 sampled tokens, every output feature."""
+  64 sampled tokens, every output feature;
+* the tensor-core latent memory, read from a memory and carried causal
+  forward at B=4, H=8, N=16384, d = K = 64: 3 whole heads."""
 import numpy as np
 import pytest
 import torch
@@ -83,3 +85,39 @@ def test_projection_full_size():
         mag = np.einsum("bni,oi->bno", absx, np.abs(W.double().numpy())).reshape(1, -1, H, dh).transpose(0, 2, 1, 3)
         bound = D * 2.0 ** -23 * mag[0] + bf16_ulp(R[0])
         assert np.all(np.abs(got - R[0]) <= bound)
+
+
+def test_tc_memory_calls_full_size():
+    """The three per-shard calls on the tensor cores at the size the shard
+    benchmark times (B=4, H=8, N=16384, d_r = d_v = K = 64, bf16), against the
+    fp64 oracle on 3 whole heads: the latent memory, the read of that memory
+    (= the bidirectional forward), and the causal forward in two 8192-token
+    pieces, the second carried from the first's returned state."""
+    import oracle
+    case = Case("tc_mem_full", True, 4, 8, 16384, 64, 64, 64, "bf16")
+    inp = make_inputs(case, seed=5)
+    d = to_dev(inp)
+    prm = (d["mu"], d["sigma2"], d["log_pi"])
+    TC = gma.PATH_TC
+    Vt, Z = gma.latent_memory(d["K"], d["V"], *prm, path=TC, sync_status=True)
+    Ob = gma.read_memory(d["Q"], *prm, Vt, Z, eps=case.eps, path=TC, sync_status=True)
+    half = case.N // 2
+    blk = lambda a, b: [d[n][:, :, a:b].contiguous() for n in ("Q", "K", "V")]  # noqa: E731
+    O1, vt1, z1 = gma.forward_causal_carry(*blk(0, half), *prm, eps=case.eps, path=TC, sync_status=True)
+    O2, vt2, z2 = gma.forward_causal_carry(*blk(half, case.N), *prm, Vt_in=vt1, Z_in=z1, eps=case.eps, path=TC,
+                                           sync_status=True)
+    Oc = torch.cat([O1, O2], dim=2)
+    for bh in (0, 13, case.B * case.H - 1):
+        b, h = divmod(bh, case.H)
+        one = lambda n: inp[n][b:b + 1, h:h + 1]  # noqa: E731
+        p1 = (inp["mu"][h:h + 1], inp["sigma2"][h:h + 1], inp["log_pi"][h:h + 1])
+        vt_ref, z_ref = oracle.latent_memory(one("K"), one("V"), *p1)
+        rel = lambda g, r: float(np.max(np.abs(g - r)) / np.sqrt(np.mean(r ** 2)))  # noqa: E731
+        assert rel(Vt[b, h].double().cpu().numpy(), vt_ref[0, 0]) <= 1e-2
+        assert rel(Z[b, h].double().cpu().numpy(), z_ref[0, 0]) <= 1e-2
+        assert rel(vt2[b, h].double().cpu().numpy(), vt_ref[0, 0]) <= 1e-2
+        assert rel(z2[b, h].double().cpu().numpy(), z_ref[0, 0]) <= 1e-2
+        ob_ref = oracle.forward_bidir(one("Q"), one("K"), one("V"), *p1, case.eps)[0, 0]
+        assert rel(Ob[b, h].double().cpu().numpy(), ob_ref) <= 1e-2
+        oc_ref = oracle.forward_causal(one("Q"), one("K"), one("V"), *p1, case.eps)[0, 0]
+        assert rel(Oc[b, h].double().cpu().numpy(), oc_ref) <= 1e-2

@@ -160,3 +160,37 @@ def test_tc_memory_paths_reject_unsupported_sizes():
     f = {k: (v.float() if k in ("Q", "K", "V") else v) for k, v in d.items()}
     with pytest.raises(gma.GmaError):
         gma.forward_causal_carry(f["Q"], f["K"], f["V"], f["mu"], f["sigma2"], f["log_pi"], path=TC)
+
+
+def test_tc_memory_paths_report_invalid_parameters():
+    """A non-positive sigma2 in one head: each of the three tensor-core calls
+    reports GMA_ERR_NONFINITE_PARAM (the read from a memory, whose first kernel
+    after the coefficient prep is the pack of the caller's memory, included),
+    and a valid call on the same workspace afterwards matches a fresh one."""
+    case = Case("tcmem_bad", True, 1, 2, 300, 64, 64, 64, "bf16")
+    d = to_dev(make_inputs(case, seed=3))
+    good = d["sigma2"].clone()
+    bad = good.clone()
+    bad[1, 5, 7] = -1.0
+    prm_bad = (d["mu"], bad, d["log_pi"])
+    prm = (d["mu"], good, d["log_pi"])
+    Vt, Z = gma.latent_memory(d["K"], d["V"], *prm, path=TC, sync_status=True)
+    import ctypes
+    lib, shape = gma.load(), (1, 2, 300, 64, 64, 64, gma.GMA_BF16)
+    nb = max(int(lib.gma_latent_memory_workspace_size(*shape, ctypes.byref(gma.options(path=TC)))),
+             int(lib.gma_read_memory_workspace_size(*shape)), int(lib.gma_causal_carry_workspace_size(*shape)))
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    calls = [
+        lambda p: gma.latent_memory(d["K"], d["V"], *p, path=TC, workspace=ws, sync_status=True),
+        lambda p: gma.read_memory(d["Q"], *p, Vt, Z, eps=case.eps, path=TC, workspace=ws, sync_status=True),
+        lambda p: gma.forward_causal_carry(d["Q"], d["K"], d["V"], *p, Vt, Z, eps=case.eps, path=TC, workspace=ws,
+                                           sync_status=True),
+    ]
+    for call in calls:
+        with pytest.raises(gma.GmaError) as e:
+            call(prm_bad)
+        assert e.value.status == 6
+        first = call(prm)
+        again = call(prm)
+        for a, b in zip(first if isinstance(first, tuple) else (first,), again if isinstance(again, tuple) else (again,)):
+            assert torch.equal(a, b)
