@@ -179,12 +179,14 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
 
 // Latent aggregation over one range of keys ([GMA, Eqs. (5)-(6)]):
 //   part[k][c] = sum_{j in range} gK_jk V_jc (c < d_v),  part[k][d_v] = sum gK_jk.
-// Block: 256 threads, each owns 8 components k = 8 tk + a and 8 value columns
+// Block: 256 threads, each owns TA components k = TA tk + a and TB value columns
 // c = tc + b * tiles_c (interleaved, so the threads of a warp read consecutive
 // columns of a staged key row: no bank conflicts); keys staged 32 at a time in
-// shared memory.  Fixed summation order.
+// shared memory.  4 x 4 tiles when 256 of them cover K x d_v, else 8 x 8 (at
+// K = d_v = 64 an 8 x 8 tiling leaves three quarters of the threads idle).
+// Every element sums its keys in order, whatever the tile: fixed summation order.
 constexpr int kWT = 32;  // keys per shared-memory stage
-template <typename T>
+template <typename T, int TA, int TB>
 __global__ void __launch_bounds__(256) write_simt_kernel(
     const float *__restrict__ gkt, const T *__restrict__ V, int N, int K, int d_v,
     int tokens_per_split, int nsplit, float *__restrict__ part, const unsigned *status) {
@@ -194,16 +196,16 @@ __global__ void __launch_bounds__(256) write_simt_kernel(
     const int split = blockIdx.x, bh = blockIdx.y;
     const int t0 = split * tokens_per_split;
     const int t1 = min(N, t0 + tokens_per_split);
-    const int tiles_c = (d_v + 7) / 8, tiles_k = (K + 7) / 8;
+    const int tiles_c = (d_v + TB - 1) / TB, tiles_k = (K + TA - 1) / TA;
     const int tk = threadIdx.x / tiles_c, tc = threadIdx.x % tiles_c;
     const bool active = tk < tiles_k;
-    float acc[8][8];
-    float zacc[8];
+    float acc[TA][TB];
+    float zacc[TA];
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
+    for (int a = 0; a < TA; ++a) {
         zacc[a] = 0.f;
 #pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        for (int b = 0; b < TB; ++b) acc[a][b] = 0.f;
     }
     const float *g = gkt + (size_t)bh * K * N;
     const T *v = V + (size_t)bh * N * d_v;
@@ -221,22 +223,22 @@ __global__ void __launch_bounds__(256) write_simt_kernel(
         __syncthreads();
         if (active) {
             for (int t = 0; t < n; ++t) {
-                float ga[8], vb[8];
+                float ga[TA], vb[TB];
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    int k = tk * 8 + a;
+                for (int a = 0; a < TA; ++a) {
+                    int k = tk * TA + a;
                     ga[a] = k < K ? sg[k][t] : 0.f;
                 }
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
+                for (int b = 0; b < TB; ++b) {
                     int c = tc + b * tiles_c;
                     vb[b] = c < d_v ? sv[t][c] : 0.f;
                 }
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
+                for (int a = 0; a < TA; ++a) {
                     zacc[a] += ga[a];
 #pragma unroll
-                    for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(ga[a], vb[b], acc[a][b]);
+                    for (int b = 0; b < TB; ++b) acc[a][b] = fmaf(ga[a], vb[b], acc[a][b]);
                 }
             }
         }
@@ -245,11 +247,11 @@ __global__ void __launch_bounds__(256) write_simt_kernel(
     const int W = d_v + 1;
     float *p = part + ((size_t)bh * nsplit + split) * K * W;
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        int k = tk * 8 + a;
+    for (int a = 0; a < TA; ++a) {
+        int k = tk * TA + a;
         if (k >= K) continue;
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
+        for (int b = 0; b < TB; ++b) {
             int c = tc + b * tiles_c;
             if (c < d_v) p[(size_t)k * W + c] = acc[a][b];
         }
@@ -653,12 +655,28 @@ cudaError_t resp_both(const Problem &p, const Ptrs &P, cudaStream_t s, StageCloc
 
 cudaError_t write_parts(const Problem &p, const SimtLayout &L, const Ptrs &P, cudaStream_t s) {
     dim3 grid(L.nsplit, p.BH());
-    if (p.dtype == GMA_F32)
-        write_simt_kernel<float><<<grid, 256, 0, s>>>(P.gk, static_cast<const float *>(p.V), p.N, p.K, p.d_v,
-                                                      L.tokens_per_split, L.nsplit, P.part, P.status);
-    else
-        write_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(P.gk, static_cast<const __nv_bfloat16 *>(p.V), p.N,
-                                                              p.K, p.d_v, L.tokens_per_split, L.nsplit, P.part, P.status);
+    // 4 x 4 tiles when they cover K x d_v with the block's 256 threads, else 8 x 8
+    // (which always do: K, d_v <= 128)
+    const bool big = ((p.K + 3) / 4) * ((p.d_v + 3) / 4) > 256;
+    if (p.dtype == GMA_F32) {
+        const float *V = static_cast<const float *>(p.V);
+        if (big)
+            write_simt_kernel<float, 8, 8><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v, L.tokens_per_split,
+                                                                L.nsplit, P.part, P.status);
+        else
+            write_simt_kernel<float, 4, 4><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v, L.tokens_per_split,
+                                                                L.nsplit, P.part, P.status);
+    } else {
+        const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V);
+        if (big)
+            write_simt_kernel<__nv_bfloat16, 8, 8><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v,
+                                                                        L.tokens_per_split, L.nsplit, P.part,
+                                                                        P.status);
+        else
+            write_simt_kernel<__nv_bfloat16, 4, 4><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v,
+                                                                        L.tokens_per_split, L.nsplit, P.part,
+                                                                        P.status);
+    }
     return cudaGetLastError();
 }
 
