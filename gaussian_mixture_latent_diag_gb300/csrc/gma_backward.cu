@@ -383,18 +383,39 @@ __global__ void __launch_bounds__(256) bwd_param_stats_kernel(const T *__restric
     }
     const float *dsb = ds + (size_t)bh * K * N;
     const T *xb = X + (size_t)bh * N * d_r;
+    // The next stage's rows are loaded into registers while this stage computes
+    // (the loads of a stage are in flight under the previous stage's arithmetic).
+    constexpr int ND = KC * kCT / 256, NX = kCT * MC / 256;
+    float rd[ND], rx[NX];
+    auto load_stage = [&](int base) {
+        const int n = min(kCT, r1 - base);
+#pragma unroll
+        for (int u = 0; u < ND; ++u) {
+            const int e = threadIdx.x + 256 * u, k = e / kCT, t = e % kCT;
+            rd[u] = (k < K && t < n) ? dsb[(size_t)k * N + base + t] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < NX; ++u) {
+            const int e = threadIdx.x + 256 * u, t = e / MC, m = e % MC;
+            rx[u] = (t < n && m0 + m < d_r) ? to_f32(xb[(size_t)(base + t) * d_r + m0 + m]) : 0.f;
+        }
+    };
+    if (r0 < r1) load_stage(r0);
     for (int base = r0; base < r1; base += kCT) {
         const int n = min(kCT, r1 - base);
         __syncthreads();
-        for (int e = threadIdx.x; e < K * kCT; e += blockDim.x) {
-            const int k = e / kCT, t = e % kCT;
-            sd[k][t] = t < n ? dsb[(size_t)k * N + base + t] : 0.f;
+#pragma unroll
+        for (int u = 0; u < ND; ++u) {
+            const int e = threadIdx.x + 256 * u;
+            sd[e / kCT][e % kCT] = rd[u];
         }
-        for (int e = threadIdx.x; e < kCT * MC; e += blockDim.x) {
-            const int t = e / MC, m = e % MC;
-            sx[t][m] = (t < n && m0 + m < d_r) ? to_f32(xb[(size_t)(base + t) * d_r + m0 + m]) : 0.f;
+#pragma unroll
+        for (int u = 0; u < NX; ++u) {
+            const int e = threadIdx.x + 256 * u;
+            sx[e / MC][e % MC] = rx[u];
         }
         __syncthreads();
+        if (base + kCT < r1) load_stage(base + kCT);
         if (active) {
             for (int t = 0; t < n; ++t) {
                 const float4 xv = *reinterpret_cast<const float4 *>(&sx[t][4 * tm]);
