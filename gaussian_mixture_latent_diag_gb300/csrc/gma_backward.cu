@@ -287,61 +287,76 @@ __global__ void __launch_bounds__(128) bwd_dv_kernel(const float *__restrict__ g
     for (int c = 0; c < D_V; ++c) o[c] = acc[c];
 }
 
-// dx_im = sum_k ds_ik (mu_km - x_im) / sigma2_km for columns [32 z, 32 z + 32),
-// one thread per row; the block's (mu, 1/sigma2) columns are staged in shared
-// memory as {mu_m, mu_m+1, 1/sigma2_m, 1/sigma2_m+1} per column pair (K x 16), and
-// the column pairs use packed f32x2 arithmetic: each element is rounded as
-// fmaf(ds * (1/sigma2), mu - x, acc) would round it, in component order.
+// dx_im = sum_k ds_ik (mu_km - x_im) / sigma2_km, computed as dx_im = SB_im - x_im SA_im with
+// SA_im = sum_k ds_ik / sigma2_km and SB_im = sum_k ds_ik mu_km / sigma2_km, two
+// [N x K] x [K x d_r] products.  Block: 64 rows x 64 columns of one head, 256
+// threads each 4 rows x 4 columns (every staged value feeds 4 or 8 products);
+// components staged kDxKC at a time: ds [kDxKC][64 rows], 1/sigma2 and mu/sigma2
+// [kDxKC][64 columns].  Components are summed in order.  The two sums share no
+// large cancelling terms beyond those of the centred form (sum_k ds_ik = 0 per
+// row keeps SA and SB of the size of dx), and the fp32 result is checked
+// against the fp64 oracle like every gradient.
+constexpr int kDxKC = 32;
 template <typename T>
-__global__ void __launch_bounds__(128) bwd_dx_kernel(const T *__restrict__ X, const float *__restrict__ ds,
-                                                     const float *__restrict__ mu, const float *__restrict__ inv,
-                                                     int H, int N, int K, int d_r, float *__restrict__ dX,
-                                                     const unsigned *status) {
+__global__ void __launch_bounds__(256) bwd_dx_tiled_kernel(const T *__restrict__ X, const float *__restrict__ ds,
+                                                           const float *__restrict__ mu,
+                                                           const float *__restrict__ inv, int H, int N, int K,
+                                                           int d_r, float *__restrict__ dX,
+                                                           const unsigned *status) {
     if (failed(status)) return;
-    constexpr int JC = 32, J2 = JC / 2;
-    __shared__ float4 sp[128][J2];
-    const int bh = blockIdx.y, h = bh % H, j0 = JC * blockIdx.z;
-    const int nj = min(JC, d_r - j0);
-    for (int e = threadIdx.x; e < K * J2; e += blockDim.x) {
-        const int k = e / J2, j = 2 * (e % J2);
-        const size_t o = ((size_t)h * K + k) * d_r + j0 + j;
-        sp[k][e % J2] = j < nj ? make_float4(mu[o], mu[o + 1], inv[o], inv[o + 1]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= N) return;
-    float2 nx[J2], acc[J2];
-    const T *xr = X + ((size_t)bh * N + i) * d_r + j0;
+    __shared__ __align__(16) float sd[kDxKC][64 + 4];
+    __shared__ __align__(16) float sa[kDxKC][64 + 4];
+    __shared__ __align__(16) float sb[kDxKC][64 + 4];
+    const int bh = blockIdx.y, h = bh % H;
+    const int r0 = 64 * blockIdx.x, c0 = 64 * blockIdx.z;
+    const int tr = threadIdx.x / 16, tc = threadIdx.x % 16;
+    float acc_a[4][4], acc_b[4][4];
 #pragma unroll
-    for (int j = 0; j < J2; ++j) {
-        nx[j] = 2 * j < nj ? make_float2(-to_f32(xr[2 * j]), -to_f32(xr[2 * j + 1])) : make_float2(0.f, 0.f);
-        acc[j] = make_float2(0.f, 0.f);
-    }
-    const float *d = ds + (size_t)bh * K * N + i;
-    constexpr int KB = kLoadBatch;
-    for (int k0 = 0; k0 < K; k0 += KB) {
-        float dk[KB];
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int u = 0; u < KB; ++u) dk[u] = k0 + u < K ? d[(size_t)(k0 + u) * N] : 0.f;
+        for (int j = 0; j < 4; ++j) acc_a[i][j] = acc_b[i][j] = 0.f;
+    const float *dsb = ds + (size_t)bh * K * N;
+    for (int k0 = 0; k0 < K; k0 += kDxKC) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kDxKC * 64; e += 256) {
+            const int k = e / 64, c = e % 64, kk = k0 + k;
+            const int row = r0 + c, col = c0 + c;
+            sd[k][c] = (kk < K && row < N) ? dsb[(size_t)kk * N + row] : 0.f;
+            const size_t o = ((size_t)h * K + kk) * d_r + col;
+            const float iv = (kk < K && col < d_r) ? inv[o] : 0.f;
+            sa[k][c] = iv;
+            sb[k][c] = (kk < K && col < d_r) ? mu[o] * iv : 0.f;
+        }
+        __syncthreads();
+        const int nk = min(kDxKC, K - k0);
+        for (int k = 0; k < nk; ++k) {
+            const float4 d = *reinterpret_cast<const float4 *>(&sd[k][4 * tr]);
+            const float4 a = *reinterpret_cast<const float4 *>(&sa[k][4 * tc]);
+            const float4 b = *reinterpret_cast<const float4 *>(&sb[k][4 * tc]);
+            const float dv[4] = {d.x, d.y, d.z, d.w}, av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int u = 0; u < KB; ++u) {
-            if (k0 + u >= K) break;
-            const float2 dd = make_float2(dk[u], dk[u]);
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < J2; ++j) {
-                const float4 pv = sp[k0 + u][j];
-                acc[j] = __ffma2_rn(__fmul2_rn(dd, make_float2(pv.z, pv.w)),
-                                    __fadd2_rn(make_float2(pv.x, pv.y), nx[j]), acc[j]);
-            }
+                for (int j = 0; j < 4; ++j) {
+                    acc_a[i][j] = fmaf(dv[i], av[j], acc_a[i][j]);
+                    acc_b[i][j] = fmaf(dv[i], bv[j], acc_b[i][j]);
+                }
         }
     }
-    float *o = dX + ((size_t)bh * N + i) * d_r + j0;
+    const int col = c0 + 4 * tc;
+    if (col >= d_r) return;  // d_r is a multiple of 16, so a thread's 4 columns are all in or all out
 #pragma unroll
-    for (int j = 0; j < J2; ++j)
-        if (2 * j < nj) {
-            o[2 * j] = acc[j].x;
-            o[2 * j + 1] = acc[j].y;
-        }
+    for (int i = 0; i < 4; ++i) {
+        const int row = r0 + 4 * tr + i;
+        if (row >= N) break;
+        const T *xr = X + ((size_t)bh * N + row) * d_r + col;
+        float4 o;
+        o.x = fmaf(-to_f32(xr[0]), acc_a[i][0], acc_b[i][0]);
+        o.y = fmaf(-to_f32(xr[1]), acc_a[i][1], acc_b[i][1]);
+        o.z = fmaf(-to_f32(xr[2]), acc_a[i][2], acc_b[i][2]);
+        o.w = fmaf(-to_f32(xr[3]), acc_a[i][3], acc_b[i][3]);
+        *reinterpret_cast<float4 *>(dX + ((size_t)bh * N + row) * d_r + col) = o;
+    }
 }
 
 // Parameter statistics of one side over a range of rows, columns
@@ -911,10 +926,10 @@ cudaError_t launch_inputs(const Problem &p, const BwdLayout &L, const BackwardAr
     const float *dsq = reinterpret_cast<const float *>(b + L.dsq), *dsk = reinterpret_cast<const float *>(b + L.dsk);
     float *st = reinterpret_cast<float *>(b + L.st);
     const T *Q = static_cast<const T *>(p.Q), *Kx = static_cast<const T *>(p.Kx);
-    const dim3 gx((p.N + 127) / 128, p.BH(), (p.d_r + 31) / 32);
-    bwd_dx_kernel<T><<<gx, 128, 0, s>>>(Q, dsq, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dQ, status);
+    const dim3 gx((p.N + 63) / 64, p.BH(), (p.d_r + 63) / 64);
+    bwd_dx_tiled_kernel<T><<<gx, 256, 0, s>>>(Q, dsq, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dQ, status);
     GMA_TRY(cudaGetLastError());
-    bwd_dx_kernel<T><<<gx, 128, 0, s>>>(Kx, dsk, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dK, status);
+    bwd_dx_tiled_kernel<T><<<gx, 256, 0, s>>>(Kx, dsk, p.mu, inv, p.H, p.N, p.K, p.d_r, g.dK, status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     // 64 columns x 64 components per block when K <= 64 and d_r >= 64, else 32 x 128
