@@ -97,3 +97,32 @@ def test_rank_order_combination():
     assert torch.equal(Vt, torch.full((2, 3), 6.0)) and torch.equal(Z, torch.full((2,), 60.0))
     # the inputs are not modified
     assert torch.equal(parts[0][0], torch.full((2, 3), 1.0))
+
+
+def test_cuda_ops_pick_the_unsharded_kernel_family():
+    """sharded.CudaOps runs a shard on the tensor cores exactly where the
+    unsharded forward would (bf16, d_r in {32, 64}, d_v = 64, K <= 64), so a
+    sharded call has the unsharded call's accuracy.  Host logic only: the choice
+    comes from gma_selected_path, which needs no GPU."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300.sharded import CudaOps
+
+    def pick(dtype, d_r, d_v, K, causal=0, n=300):
+        X = torch.empty(1, 2, n, d_r, dtype=dtype)
+        V = torch.empty(1, 2, n, d_v, dtype=dtype)
+        mu = torch.empty(2, K, d_r)
+        return CudaOps._path(X, V, mu, causal)
+
+    bf, f32 = torch.bfloat16, torch.float32
+    assert pick(bf, 64, 64, 64) == gma.PATH_TC
+    assert pick(bf, 32, 64, 17, causal=1) == gma.PATH_TC
+    assert pick(bf, 64, 64, 64, n=1) == gma.PATH_TC
+    assert pick(f32, 64, 64, 64) == gma.PATH_SIMT
+    assert pick(bf, 64, 32, 64) == gma.PATH_SIMT
+    assert pick(bf, 128, 64, 64, causal=1) == gma.PATH_SIMT
+    assert pick(bf, 64, 64, 128) == gma.PATH_SIMT
+    for dtype, d_r, d_v, K in [(bf, 64, 64, 64), (f32, 16, 32, 8), (bf, 128, 128, 128)]:
+        for causal in (0, 1):
+            want = gma.selected_path(300, d_r, d_v, K, "bf16" if dtype == bf else "f32", causal)
+            assert pick(dtype, d_r, d_v, K, causal) == want
