@@ -39,6 +39,19 @@ def test_workspace_queries(lib):
     assert lib.gma_latent_memory_workspace_size(1, 1, 64, 64, 64, 64, 0, ctypes.byref(tc)) == 0
     assert lib.gma_latent_memory_workspace_size(1, 1, 64, 64, 64, 128, 1, ctypes.byref(tc)) == 0
     assert lib.gma_decode_workspace_size(8, 64, 64) > 0
+    # the read and carried-prefix queries take no options, so their size covers either
+    # kernel family: the tensor-core read and carried forward use the forward's
+    # tensor-core workspace (0 where that path does not take the sizes), and the
+    # CUDA-core carried forward the CUDA-core causal forward's
+    for B, H, N, d_r, d_v, K, dt in [(4, 8, 16384, 64, 64, 64, 1), (2, 3, 1000, 32, 64, 17, 1),
+                                      (1, 2, 517, 64, 32, 8, 0)]:
+        cases = ((0, lib.gma_read_memory_workspace_size, (2,)), (1, lib.gma_causal_carry_workspace_size, (1, 2)))
+        for causal, fn, paths in cases:
+            got = fn(B, H, N, d_r, d_v, K, dt)
+            assert got > 0
+            for path in paths:
+                opt = _native.Options(path, 0, 0, 0)
+                assert got >= lib.gma_workspace_size(B, H, N, d_r, d_v, K, dt, causal, ctypes.byref(opt))
 
 
 def test_stage_names(lib):
