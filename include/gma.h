@@ -18,7 +18,8 @@
  * - Every pointer argument except the host-side `options` is a DEVICE pointer
  *   on the current CUDA device.  The caller owns all buffers, including the
  *   workspace; the library never allocates or frees device memory and keeps
- *   no state between calls.
+ *   no state between calls.  One exception: gma_forward_bidir_noalloc keeps
+ *   its scratch in a fixed device array of the library (see there).
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Calls are asynchronous on that stream.
  * - Host-detectable errors (null pointers, bad sizes, aliasing, short
@@ -72,7 +73,10 @@ enum {
 /* Optional knobs; pass NULL for all defaults.  Zero in a field = default. */
 typedef struct gma_options {
     int path;         /* GMA_PATH_* */
-    int chunk;        /* causal chunk length in tokens (0 = the kernel family's only supported value) */
+    int chunk;        /* causal chunk length in tokens: 0 or the kernel family's length (tensor cores 128,
+                       * CUDA cores 64); any other value makes a causal call (forward, carried-prefix
+                       * forward, backward) return GMA_ERR_UNSUPPORTED_SHAPE (negative:
+                       * GMA_ERR_INVALID_ARG); ignored by the other calls */
     int splits;       /* number of N-splits of the key pass per head (0 = chosen from the grid) */
     int sync_status;  /* nonzero: synchronise `stream` before returning and return the device status */
     int o_bf16;       /* nonzero: O is bfloat16, rounded to nearest even from fp32 (default fp32) */
@@ -170,13 +174,19 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
  * library holds until the process exits.  It calls no cudaMalloc, cudaFree
  * or allocating library routine.  The caller still passes the inputs and O.
  *
- * - Arguments and results are those of gma_forward_bidir.
- * - Sizes whose workspace (gma_workspace_size(..., causal = 0, options))
- *   exceeds GMA_NOALLOC_SCRATCH_BYTES return GMA_ERR_WORKSPACE_TOO_SMALL
- *   without touching the device.
- * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture on the device.
+ * - Arguments and results are those of gma_forward_bidir.  Argument errors
+ *   (null pointers, a bad dtype, negative options->chunk or splits) are
+ *   checked first (GMA_ERR_INVALID_ARG), then the sizes: unsupported sizes
+ *   return GMA_ERR_UNSUPPORTED_SHAPE, and sizes whose workspace
+ *   (gma_workspace_size(..., causal = 0, options)) exceeds
+ *   GMA_NOALLOC_SCRATCH_BYTES return GMA_ERR_WORKSPACE_TOO_SMALL, in both
+ *   cases without touching the device.
+ * - Every call looks up the array's device address in the CUDA context
+ *   current on the calling thread (cudaGetSymbolAddress, which allocates
+ *   nothing), so a call made after cudaDeviceReset, or with another context
+ *   current, uses that context's copy of the array.  The first call in a
+ *   context may load the library's device code, array included, into it:
+ *   make that first call before any stream capture in that context.
  * - Every call on a device shares the one array, which keeps the last call's
  *   contents.  Calls whose work overlaps on the GPU (different streams, or
  *   different host threads without ordering) race on it: order them, e.g. on
@@ -370,6 +380,23 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
                                     void *O, int B, int H, int N, int d_r, int d_v, int K,
                                     const gma_options *options, void *workspace, size_t workspace_bytes,
                                     void *stream);
+
+/*
+ * Rank-order sum of latent memories ([GMA, Eqs. (5)-(6)]: the memory is a sum
+ * over positions, so the memories of consecutive blocks of a sequence add up;
+ * [GMA, causal variant, Eq. (8b)]: the prefix memory at a block boundary is
+ * the sum of every earlier block's memory).  parts is a [P, n] fp32 device
+ * array, one row per block in sequence order (e.g. each rank's packed
+ * [Vt | Z] after an all-gather); out[e] = sum_{r < count} parts[r * n + e],
+ * summed in fp32 one row after another from row 0, so every holder of the same
+ * rows gets bitwise the same result.  count = P gives the whole sequence's
+ * memory (the bidirectional read of every block), count = r the exclusive
+ * prefix of block r (its causal carry-in).  1 <= count <= P, n >= 1
+ * (GMA_ERR_UNSUPPORTED_SHAPE otherwise); both pointers 4-byte aligned and out
+ * not overlapping parts (GMA_ERR_INVALID_ARG).  One kernel launch on `stream`;
+ * no workspace.
+ */
+gma_status gma_combine_memories(const float *parts, int P, long long n, int count, float *out, void *stream);
 
 /*
  * Reparameterised mixture parameters ([GMA, Eqs. (14)-(15)]), per head h:

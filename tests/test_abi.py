@@ -120,3 +120,41 @@ def test_path_selection(lib):
     assert lib.gma_selected_path(256, 16, 32, 8, 0, 0, ctypes.byref(simt)) == 1
     assert lib.gma_selected_path(256, 16, 32, 8, 0, 0, None) == 1   # fp32 runs on SIMT
     assert lib.gma_selected_path(256, 15, 32, 8, 0, 0, None) == -1
+
+
+def test_noalloc_argument_errors_come_first(lib):
+    """gma_forward_bidir_noalloc reports argument errors before the size
+    check, as gma_forward_bidir does, and never touches the device for them."""
+    vp = ctypes.c_void_p
+    big = dict(B=64, H=64, N=65536)  # far beyond the fixed scratch array
+
+    def call(Q=FAKE, O=FAKE + (6 << 32), dtype=1, opt=None, B=1, H=1, N=64, d_r=64):
+        o = ctypes.byref(opt) if opt is not None else None
+        return lib.gma_forward_bidir_noalloc(vp(Q), vp(FAKE + (1 << 32)), vp(FAKE + (2 << 32)), dtype,
+                                             vp(FAKE + (3 << 32)), vp(FAKE + (4 << 32)),
+                                             vp(FAKE + (5 << 32)), 1e-6, vp(O), B, H, N, d_r, 64, 64, o,
+                                             None)
+    assert call(Q=0, **big) == 1                               # null pointer, whatever the size
+    assert call(O=0, **big) == 1
+    assert call(dtype=7, **big) == 1                           # bad dtype
+    assert call(opt=_native.Options(0, 0, -1, 0), **big) == 1  # negative splits
+    assert call(opt=_native.Options(0, -2, 0, 0), **big) == 1  # negative chunk
+    assert call(d_r=48) == 2                                   # unsupported sizes
+    assert call(**big) == 3                                    # too large for the array
+
+
+def test_chunk_option(lib):
+    """Causal calls run only the kernel family's chunk length (tensor cores 128,
+    CUDA cores 64); any other positive value is rejected, negative values are
+    invalid, and the bidirectional call ignores the field."""
+    def ws(causal, path, chunk):
+        o = _native.Options(path, chunk, 0, 0)
+        return lib.gma_workspace_size(1, 1, 512, 64, 64, 64, 1, causal, ctypes.byref(o))
+    assert ws(1, 2, 0) > 0 and ws(1, 2, 128) > 0
+    assert ws(1, 2, 64) == 0 and ws(1, 2, 256) == 0
+    assert ws(1, 1, 64) > 0 and ws(1, 1, 128) == 0
+    assert ws(0, 2, 256) > 0                                   # bidirectional: no chunks
+    assert lib.gma_selected_path(512, 64, 64, 64, 1, 1, ctypes.byref(_native.Options(0, 256, 0, 0))) == -1
+    need = ws(1, 2, 0)
+    for chunk, code in ((256, 2), (64, 2), (-1, 1)):
+        assert _fwd(lib, "gma_forward_causal", opt=_native.Options(2, chunk, 0, 0), wsb=need) == code
