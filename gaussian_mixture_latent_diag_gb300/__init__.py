@@ -151,10 +151,11 @@ def forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=Non
 
 
 def forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None,
-                   path=PATH_AUTO, splits=0, sync_status=False, o_bf16=False):
-    """Causal GMA: prefix memories over keys j <= i; O fp32 (or bf16)."""
+                   path=PATH_AUTO, splits=0, sync_status=False, o_bf16=False, chunk=0):
+    """Causal GMA: prefix memories over keys j <= i; O fp32 (or bf16).  ``chunk``:
+    0 or the kernel family's chunk length (see gma_options.chunk)."""
     return _forward("gma_forward_causal", Q, K, V, mu, sigma2, log_pi, eps, out, workspace,
-                    stream, path, splits, sync_status, o_bf16)
+                    stream, path, splits, sync_status, o_bf16, chunk)
 
 
 def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, stream=None,
@@ -389,6 +390,24 @@ def forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in=None, Z_in=None, eps
     if st != 0:
         raise GmaError(st, "gma_forward_causal_carry")
     return out, Vt_out, Z_out
+
+
+def combine_memories(parts, count=None, out=None, stream=None):
+    """Rank-order sum of latent memories (gma_combine_memories): ``parts`` is a
+    [P, n] fp32 CUDA tensor, one row per sequence block in order; returns the
+    [n] sum of rows 0..count-1 (count = P by default), summed in row order."""
+    import torch
+    _check_dev(parts)
+    if parts.dim() != 2 or parts.dtype != torch.float32 or not parts.is_contiguous():
+        raise ValueError("parts must be a contiguous fp32 [P, n] tensor")
+    P, n = parts.shape
+    count = P if count is None else int(count)
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=parts.device)
+    st = load().gma_combine_memories(_ptr(parts), P, n, count, _ptr(out), _stream(stream))
+    if st != 0:
+        raise GmaError(st, "gma_combine_memories")
+    return out
 
 
 def reparameterize(omega, alpha, eps_sigma=1e-3, stream=None):

@@ -40,6 +40,16 @@ int choose_path(const Problem &p, int causal, const gma_options *opt) {
     return tc ? GMA_PATH_TC : GMA_PATH_SIMT;
 }
 
+// The causal chunk length of a kernel family: the tensor-core scan runs in
+// chunks of 128 tokens (its tile), the CUDA-core scan in chunks of
+// kSimtCausalChunk.  options->chunk must be 0 (the family's value) or exactly
+// that value; other lengths are not built.
+int family_chunk(int path) { return path == GMA_PATH_TC ? 128 : gma::kSimtCausalChunk; }
+bool chunk_ok(int path, int causal, const gma_options *opt) {
+    if (!opt || opt->chunk == 0 || causal != 1) return true;
+    return opt->chunk == family_chunk(path);
+}
+
 size_t workspace_for(const Problem &p, int causal, const gma_options *opt, int path) {
     int splits = opt ? opt->splits : 0;
     if (path == GMA_PATH_TC) return gma::tc_workspace(p, causal, splits);
@@ -109,7 +119,7 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     const size_t nr = es * (size_t)B * H * N * d_r, nv = es * (size_t)B * H * N * d_v;
     const size_t no = (p.o_bf16 ? 2 : 4) * (size_t)B * H * N * d_v;
     const int path = choose_path(p, causal, options);
-    if (path < 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (path < 0 || !chunk_ok(path, causal, options)) return GMA_ERR_UNSUPPORTED_SHAPE;
     const size_t need = workspace_for(p, causal, options, path);
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     if (overlaps(O, no, Q_X, nr) || overlaps(O, no, K_X, nr) || overlaps(O, no, V_X, nv) ||
@@ -147,6 +157,8 @@ gma_status backward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype
     if (options && options->splits < 0) return GMA_ERR_INVALID_ARG;
     if (options && (options->o_bf16 || (options->path != GMA_PATH_AUTO && options->path != GMA_PATH_SIMT)))
         return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (options && options->chunk < 0) return GMA_ERR_INVALID_ARG;
+    if (!chunk_ok(GMA_PATH_SIMT, causal, options)) return GMA_ERR_UNSUPPORTED_SHAPE;
 
     Problem p;
     p.Q = Q_X; p.Kx = K_X; p.V = V_X; p.mu = mu; p.sigma2 = sigma2; p.log_pi = log_pi;
@@ -195,7 +207,7 @@ size_t gma_workspace_size(int B, int H, int N, int d_r, int d_v, int K, gma_dtyp
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = causal >= 0 ? d_v : 16; p.K = K;
     int path = choose_path(p, causal, options);
-    if (path < 0) return 0;
+    if (path < 0 || !chunk_ok(path, causal, options)) return 0;
     return workspace_for(p, causal, options, path);
 }
 
@@ -249,9 +261,10 @@ size_t gma_backward_workspace_size(int B, int H, int N, int d_r, int d_v, int K,
                                    int causal, const gma_options *options) {
     if ((causal != 0 && causal != 1) || (dtype != GMA_F32 && dtype != GMA_BF16)) return 0;
     if (!shape_ok(B, H, N, d_r, d_v, K, true)) return 0;
-    if (options && (options->splits < 0 || options->o_bf16 ||
+    if (options && (options->splits < 0 || options->chunk < 0 || options->o_bf16 ||
                     (options->path != GMA_PATH_AUTO && options->path != GMA_PATH_SIMT)))
         return 0;
+    if (!chunk_ok(GMA_PATH_SIMT, causal, options)) return 0;
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     return gma::backward_workspace(p, causal, options ? options->splits : 0);
@@ -497,8 +510,9 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
     p.dtype = dtype; p.eps = eps;
     p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     p.o_bf16 = options && options->o_bf16;
+    if (options && options->chunk < 0) return GMA_ERR_INVALID_ARG;
     const int path = memory_path(p, 1, options);
-    if (path < 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (path < 0 || !chunk_ok(path, 1, options)) return GMA_ERR_UNSUPPORTED_SHAPE;
     const size_t need = path == GMA_PATH_TC ? gma::tc_workspace(p, 1, 0) : gma::simt_layout(p, 1, 0).total;
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
@@ -633,7 +647,8 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
     if (!shape_ok(1, 1, N, d_r, d_v, K, true)) return -1;
     Problem p;
     p.dtype = dtype; p.B = 1; p.H = 1; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
-    return choose_path(p, causal, options);
+    const int path = choose_path(p, causal, options);
+    return path >= 0 && chunk_ok(path, causal, options) ? path : -1;
 }
 
 int gma_stage_count(int path, int variant) {

@@ -118,3 +118,22 @@ def test_invalid_parameters_reported(bad):
     # a clean call on the same workspace afterwards succeeds
     d2 = to_dev(make_inputs(case, seed=9))
     run_gpu(case, d2)
+
+
+@pytest.mark.parametrize("path,chunk", [(gma.PATH_SIMT, 64), (gma.PATH_TC, 128)], ids=["simt64", "tc128"])
+def test_causal_each_supported_chunk(path, chunk):
+    """options.chunk set to the kernel family's chunk length (the only one
+    each family runs; other lengths are rejected on the host): the same
+    result as the oracle, with ragged last chunks."""
+    case = _case(True, 3 * chunk + 37, 64, 64, 64, "bf16")
+    inp = make_inputs(case, seed=10)
+    O = gma.forward_causal(*(to_dev(inp)[k] for k in ("Q", "K", "V", "mu", "sigma2", "log_pi")),
+                           eps=case.eps, path=path, chunk=chunk, sync_status=True)
+    torch.cuda.synchronize()
+    err = normalised_error(O, oracle_full(case, inp))
+    assert err <= TOL["bf16"], err
+    other = 256 if chunk == 128 else 128
+    with pytest.raises(gma.GmaError) as e:
+        gma.forward_causal(*(to_dev(inp)[k] for k in ("Q", "K", "V", "mu", "sigma2", "log_pi")),
+                           eps=case.eps, path=path, chunk=other)
+    assert e.value.status == 2
