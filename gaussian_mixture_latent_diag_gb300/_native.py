@@ -29,7 +29,8 @@ EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_decode_workspace_size", "gma_decode_step", "gma_routing_stats_workspace_size",
             "gma_routing_stats", "gma_read_memory_workspace_size", "gma_read_memory",
             "gma_causal_carry_workspace_size", "gma_forward_causal_carry", "gma_reparameterize",
-            "gma_reparameterize_backward", "gma_project_workspace_size", "gma_project_qkv")
+            "gma_reparameterize_backward", "gma_project_workspace_size", "gma_project_qkv",
+            "gma_combine_memories")
 
 
 class Options(ctypes.Structure):
@@ -104,6 +105,8 @@ def load(path: str | None = None):
         lib.gma_reparameterize.restype = i
         lib.gma_reparameterize_backward.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp]
         lib.gma_reparameterize_backward.restype = i
+        lib.gma_combine_memories.argtypes = [vp, i, ctypes.c_longlong, i, vp, vp]
+        lib.gma_combine_memories.restype = i
         lib.gma_project_workspace_size.argtypes = []
         lib.gma_project_workspace_size.restype = sz
         lib.gma_project_qkv.argtypes = [vp] * 7 + [i] * 7 + [opt, vp, sz, vp]

@@ -15,9 +15,10 @@ Sequence Mixing via Probabilistic Latent Routing", arXiv 2606.18283):
 The exchange is one all_gather of each rank's [B, H, K, d_v + 1] memory
 (16.6 KB per head at K = d_v = 64) followed by a sum in rank order, so every
 rank computes bitwise the same total whatever the collective's internal
-reduction order.  All per-shard arithmetic runs in libgma.so's kernels
-(``CudaOps``); the orchestration takes any object with the same three methods,
-which is how its host logic is tested on CPU ranks.
+reduction order.  All arithmetic -- the per-shard steps and the rank-order sum
+-- runs in libgma.so's kernels (``CudaOps``); this module only moves tensors.
+The orchestration takes any object with the same four methods, which is how
+its host logic is tested on CPU ranks.
 """
 from __future__ import annotations
 
@@ -52,22 +53,32 @@ class CudaOps:
         return forward_causal_carry(Q, K, V, mu, sigma2, log_pi, Vt_in, Z_in, eps=eps, want_state=False,
                                     path=self._path(Q, V, mu, causal=1))[0]
 
-
-def combine_total(parts):
-    """Sum of the (Vt, Z) memories of every shard, in shard order."""
-    Vt, Z = parts[0][0].clone(), parts[0][1].clone()
-    for vt, z in parts[1:]:
-        Vt += vt
-        Z += z
-    return Vt, Z
+    def combine(self, packed, count):
+        """Rows 0..count-1 of a [P, n] packed array summed in row order (gma_combine_memories)."""
+        from . import combine_memories
+        return combine_memories(packed, count)
 
 
-def combine_exclusive(parts, rank: int):
+def pack_memories(parts):
+    """[P, n] array of the shards' memories, row r = [Vt_r | Z_r] flattened (a copy)."""
+    return torch.stack([torch.cat([vt.reshape(-1), z.reshape(-1)]) for vt, z in parts])
+
+
+def combine_total(parts, ops=None):
+    """Sum of the (Vt, Z) memories of every shard, in shard order (ops.combine)."""
+    ops = ops or CudaOps()
+    Vt0, Z0 = parts[0]
+    flat = ops.combine(pack_memories(parts), len(parts))
+    n = Vt0.numel()
+    return flat[:n].view_as(Vt0), flat[n:].view_as(Z0)
+
+
+def combine_exclusive(parts, rank: int, ops=None):
     """Sum of the memories of shards 0..rank-1 in shard order; (None, None) for
     rank 0 (an empty prefix)."""
     if rank == 0:
         return None, None
-    return combine_total(parts[:rank])
+    return combine_total(parts[:rank], ops)
 
 
 def gather_memories(Vt, Z, group=None):
@@ -85,7 +96,7 @@ def forward_bidir_sharded(Q, K, V, mu, sigma2, log_pi, eps=1e-6, group=None, ops
     [B, H, n_r, d] are its block of positions; returns its block of O."""
     ops = ops or CudaOps()
     Vt, Z = ops.latent_memory(K, V, mu, sigma2, log_pi)
-    Vt, Z = combine_total(gather_memories(Vt, Z, group))
+    Vt, Z = combine_total(gather_memories(Vt, Z, group), ops)
     return ops.read_memory(Q, mu, sigma2, log_pi, Vt, Z, eps)
 
 
@@ -94,5 +105,5 @@ def forward_causal_sharded(Q, K, V, mu, sigma2, log_pi, eps=1e-6, group=None, op
     positions): continues from the memories of all earlier ranks' blocks."""
     ops = ops or CudaOps()
     Vt, Z = ops.latent_memory(K, V, mu, sigma2, log_pi)
-    carry_v, carry_z = combine_exclusive(gather_memories(Vt, Z, group), dist.get_rank(group))
+    carry_v, carry_z = combine_exclusive(gather_memories(Vt, Z, group), dist.get_rank(group), ops)
     return ops.forward_causal_carry(Q, K, V, mu, sigma2, log_pi, carry_v, carry_z, eps)

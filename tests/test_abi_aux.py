@@ -151,3 +151,17 @@ def test_reparameterize_and_projection_validation(lib):
     assert proj(D=100) == 2             # D must be a multiple of 8
     assert proj(d_r=48) == 2
     assert proj(wsb=need - 1) == 3
+
+
+def test_combine_memories_validation(lib):
+    vp = ctypes.c_void_p
+    F = 1 << 40
+    n = 1000
+    assert lib.gma_combine_memories(vp(0), 3, n, 3, vp(F), None) == 1          # null parts
+    assert lib.gma_combine_memories(vp(F), 3, n, 3, vp(0), None) == 1          # null out
+    assert lib.gma_combine_memories(vp(F + 2), 3, n, 3, vp(F << 1), None) == 1  # misaligned
+    assert lib.gma_combine_memories(vp(F), 3, n, 4, vp(F << 1), None) == 2     # count > P
+    assert lib.gma_combine_memories(vp(F), 3, n, 0, vp(F << 1), None) == 2     # count < 1
+    assert lib.gma_combine_memories(vp(F), 0, n, 0, vp(F << 1), None) == 2     # no rows
+    assert lib.gma_combine_memories(vp(F), 3, 0, 1, vp(F << 1), None) == 2     # empty rows
+    assert lib.gma_combine_memories(vp(F), 3, n, 3, vp(F + 4 * n), None) == 1  # out inside parts

@@ -97,9 +97,9 @@ def test_sharded_over_n_emulated_on_one_gpu(P, dtype):
     ops = sharded.CudaOps()
     blocks = [[d[n][:, :, a:b].contiguous() for n in ("Q", "K", "V")] for a, b in zip(cuts[:-1], cuts[1:])]
     parts = [ops.latent_memory(k, v, *prm) for _, k, v in blocks]
-    Vt, Z = sharded.combine_total(parts)
+    Vt, Z = sharded.combine_total(parts, ops)
     Ob = torch.cat([ops.read_memory(q, *prm, Vt, Z, case.eps) for q, _, _ in blocks], dim=2)
-    Oc = torch.cat([ops.forward_causal_carry(q, k, v, *prm, *sharded.combine_exclusive(parts, r), case.eps)
+    Oc = torch.cat([ops.forward_causal_carry(q, k, v, *prm, *sharded.combine_exclusive(parts, r, ops), case.eps)
                     for r, (q, k, v) in enumerate(blocks)], dim=2)
     args = (inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps)
     tol = TOL if dtype == "f32" else 1e-2  # bf16 d = K = 64 runs on the tensor cores
@@ -149,3 +149,19 @@ def test_reparameterized_parameters_drive_the_forward():
     O = gma.forward_bidir(d["Q"], d["K"], d["V"], d["mu"], s2, lp, eps=case.eps, sync_status=True)
     ref = oracle.forward_bidir(inp["Q"], inp["K"], inp["V"], inp["mu"], s2_ref, lp_ref, case.eps)
     assert _rel(O, ref) <= TOL
+
+
+def test_combine_memories_rank_order():
+    """gma_combine_memories sums rows 0..count-1 one after another in fp32,
+    row 0 first: bitwise the same as that sequential sum on the host."""
+    import gaussian_mixture_latent_diag_gb300 as gma
+    g = torch.Generator().manual_seed(3)
+    parts = torch.randn(5, 10001, generator=g) * torch.logspace(-3, 3, 10001)
+    dparts = parts.cuda()
+    for count in (1, 2, 5):
+        want = parts[0].clone()
+        for r in range(1, count):
+            want += parts[r]
+        got = gma.combine_memories(dparts, count)
+        torch.cuda.synchronize()
+        assert torch.equal(got.cpu(), want), count

@@ -31,6 +31,13 @@ class OracleOps:
         O, _, _ = oracle.decode(Q, K, V, mu, sigma2, log_pi, eps, Vt_in, Z_in)
         return torch.from_numpy(O)
 
+    def combine(self, packed, count):
+        """Rows 0..count-1 summed one after another in row order (the library's order)."""
+        acc = packed[0].clone()
+        for r in range(1, count):
+            acc += packed[r]
+        return acc
+
 
 CUTS = {2: [0, 37, 90], 3: [0, 20, 21, 90]}
 
@@ -89,11 +96,14 @@ def test_sharded_forward_matches_unsharded(world):
 
 def test_rank_order_combination():
     from gaussian_mixture_latent_diag_gb300 import sharded
+    ops = OracleOps()
     parts = [(torch.full((2, 3), float(r + 1)), torch.full((2,), 10.0 * (r + 1))) for r in range(4)]
-    Vt, Z = sharded.combine_total(parts)
+    packed = sharded.pack_memories(parts)
+    assert packed.shape == (4, 8) and torch.equal(packed[2], torch.tensor([3.0] * 6 + [30.0] * 2))
+    Vt, Z = sharded.combine_total(parts, ops)
     assert torch.equal(Vt, torch.full((2, 3), 10.0)) and torch.equal(Z, torch.full((2,), 100.0))
-    assert sharded.combine_exclusive(parts, 0) == (None, None)
-    Vt, Z = sharded.combine_exclusive(parts, 3)
+    assert sharded.combine_exclusive(parts, 0, ops) == (None, None)
+    Vt, Z = sharded.combine_exclusive(parts, 3, ops)
     assert torch.equal(Vt, torch.full((2, 3), 6.0)) and torch.equal(Z, torch.full((2,), 60.0))
     # the inputs are not modified
     assert torch.equal(parts[0][0], torch.full((2, 3), 1.0))

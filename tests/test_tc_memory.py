@@ -140,9 +140,9 @@ def test_tc_sharded_over_n_emulated_on_one_gpu(P):
     cuts[1] += 129  # uneven shards with ragged tails
     blocks = [[d[n][:, :, a:b].contiguous() for n in ("Q", "K", "V")] for a, b in zip(cuts[:-1], cuts[1:])]
     parts = [ops.latent_memory(k, v, *prm) for _, k, v in blocks]
-    Vt, Z = sharded.combine_total(parts)
+    Vt, Z = sharded.combine_total(parts, ops)
     Ob = torch.cat([ops.read_memory(q, *prm, Vt, Z, case.eps) for q, _, _ in blocks], dim=2)
-    Oc = torch.cat([ops.forward_causal_carry(q, k, v, *prm, *sharded.combine_exclusive(parts, r), case.eps)
+    Oc = torch.cat([ops.forward_causal_carry(q, k, v, *prm, *sharded.combine_exclusive(parts, r, ops), case.eps)
                     for r, (q, k, v) in enumerate(blocks)], dim=2)
     args = (inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], case.eps)
     eb, ec = _rel(Ob, oracle.forward_bidir(*args)), _rel(Oc, oracle.forward_causal(*args))
