@@ -47,10 +47,11 @@ STAGE_TENSORS = {
 }
 
 
-def tensor_bytes(t: str, w=WORKLOAD) -> int:
-    """Bytes of the named path tensors; O is written in fp32."""
+def tensor_bytes(t: str, w=WORKLOAD, o_bytes: int = 4) -> int:
+    """Bytes of the named path tensors; O is written in fp32 (o_bytes = 2: the
+    byte count O would have in bf16, the metric's basis)."""
     es = 2 if w["dtype"] == "bf16" else 4
-    per = {"Q": es * w["d_r"], "K": es * w["d_r"], "V": es * w["d_v"], "O": 4 * w["d_v"]}
+    per = {"Q": es * w["d_r"], "K": es * w["d_r"], "V": es * w["d_v"], "O": o_bytes * w["d_v"]}
     return sum(per[c] for c in t) * w["B"] * w["H"] * w["N"]
 
 
@@ -151,14 +152,48 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle (CPU)
 
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def host_cpu_model() -> str:
+    """CPU model of the host (lscpu's model name, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        return f"implementer {fields.get('cpu implementer', '?')} part {fields.get('cpu part', '?')}"
+    except Exception:
+        import platform
+        return platform.processor() or platform.machine()
+
+
 def _oracle_head(args):
-    """One head of one variant through the fp64 oracle (runs in a worker)."""
-    causal, seed, head = args
+    """One head of one variant through the fp64 oracle (runs in a worker); an
+    optional fourth item sets the head's length (default: the workload's N)."""
+    causal, seed, head = args[:3]
+    n = args[3] if len(args) > 3 else WORKLOAD["N"]
     sys.path.insert(0, ROOT)
     import oracle
     from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
     w = WORKLOAD
-    case = Case("sample", bool(causal), 1, 1, w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"])
+    case = Case("sample", bool(causal), 1, 1, n, w["d_r"], w["d_v"], w["K"], w["dtype"])
     inp = make_inputs(case, seed=seed * 1000 + head)
     fn = oracle.forward_causal if causal else oracle.forward_bidir
     t = time.perf_counter()
@@ -189,12 +224,13 @@ class OraclePool:
         self.pool = mp.get_context("spawn").Pool(procs)
         self.pool.map(_oracle_head, [(0, 0, 0)] * procs)  # workers up, oracle loaded
 
-    def sample(self, pairs: int):
-        """Wall time and token*heads for `pairs` (bidir head, causal head) pairs."""
-        jobs = [(c, 7, i) for i in range(pairs) for c in (0, 1)]
+    def sample(self, pairs: int, n: int = WORKLOAD["N"]):
+        """Wall time and token*heads for `pairs` (bidir head, causal head) pairs of
+        n tokens each."""
+        jobs = [(c, 7, i, n) for i in range(pairs) for c in (0, 1)]
         t = time.perf_counter()
         self.pool.map(_oracle_head, jobs)
-        return time.perf_counter() - t, len(jobs) * WORKLOAD["N"]
+        return time.perf_counter() - t, len(jobs) * n
 
     def close(self):
         self.pool.close()
@@ -202,28 +238,42 @@ class OraclePool:
 
 
 def run_reference(args, rank: int):
+    """The fp64 oracle on the host cores: one spawned process per core, each
+    step one bidirectional and one causal head per process.  The heads are
+    whole (N = 16384) unless that would make the run longer than about two and
+    a half minutes; then every head of the run is the same shorter prefix of
+    the workload's sequence length (the oracle's cost per token does not
+    depend on N)."""
     if rank != 0:
         return
     import oracle
     oracle.build()
-    procs = 2
+    steps = args.steps if args.steps is not None else 3
+    procs = host_cores()
     pool = OraclePool(procs)
+    # calibration (untimed): one pair of 2048-token heads per process
+    wall, th = pool.sample(procs, 2048)
+    per_token = wall / (th / procs)              # seconds per token*head on one process
+    budget = 150.0 / (steps + args.warmup)       # seconds per step
+    n = int(min(WORKLOAD["N"], max(256, budget / (2 * per_token))))
+    n = 1 << (n.bit_length() - 1) if n < WORKLOAD["N"] else n
     times = []
-    for s in range(args.warmup + args.steps):
-        wall, th = pool.sample(1)
+    for s in range(args.warmup + steps):
+        wall, th = pool.sample(procs, n)
         if s >= args.warmup:
             times.append(wall)
     pool.close()
     ms = 1e3 * statistics.mean(times)
-    value = 2 * WORKLOAD["N"] / (ms / 1e3)
-    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+    value = th / (ms / 1e3)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps,
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-           "config": {"workload": "GMA forward, one bidirectional + one causal head per step "
-                                  "(sample of B=4,H=8,N=16384,d_r=d_v=K=64)", **WORKLOAD},
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
-                            "sample": "1 bidirectional + 1 causal head of N=16384 per step, "
-                                      "fp64 C oracle, one process per variant"},
+           "config": {"workload": f"GMA forward, {procs} bidirectional + {procs} causal heads of N={n} per "
+                                  "step (sample of B=4,H=8,N=16384,d_r=d_v=K=64)", **WORKLOAD},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "cpu_model": host_cpu_model(),
+                            "kind": "oracle",
+                            "sample": f"per step, one bidirectional + one causal head of N={n} tokens on "
+                                      f"each of {procs} processes (one per host core), fp64 C oracle"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -527,66 +577,84 @@ def run_aux(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+
+
+def time_configs(args, rank: int, dev) -> dict:
+    """One forward of each configured workload (the small fp32 bidirectional,
+    bidirectional N=4096, causal N=16384, peaked bidirectional N=16384, causal
+    large-head N=32768 K=d=128), each on the kernel family the library selects
+    for it, timed with CUDA events on the launching stream after 3 untimed
+    calls: as many calls as fill about 0.3 s (at least 5).  Per workload:
+    token*heads/s and the whole call's algorithmic bytes (Q, K, V read, O
+    written; O credited at 4 B, the fp32 it is written in, and at 2 B, the
+    metric's basis) against the measured HBM peak."""
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300 import _native
+    from gaussian_mixture_latent_diag_gb300.synthetic import WORKLOADS, make_inputs
+
+    stream = torch.cuda.current_stream()
+    peak, _ = measured_peaks()
+    per = {}
+    for name, case in WORKLOADS.items():
+        inp = make_inputs(case, seed=rank_seed(rank, 8))
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        fn = gma.forward_causal if case.causal else gma.forward_bidir
+        out = torch.empty(case.B, case.H, case.N, case.d_v, device=dev)
+        code = "f32" if case.dtype == "f32" else "bf16"
+        ws = torch.empty(gma.workspace_size(case.B, case.H, case.N, case.d_r, case.d_v, case.K, code,
+                                            int(case.causal)), dtype=torch.uint8, device=dev)
+
+        def call():
+            fn(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], eps=case.eps, out=out, workspace=ws)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        steps = max(5, min(2000, int(300.0 / max(t0.elapsed_time(t1), 1e-3))))
+        t0.record(stream)
+        for _ in range(steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        es = 4 if case.dtype == "f32" else 2
+        alg = case.token_heads * (es * (2 * case.d_r + case.d_v) + 4 * case.d_v)
+        alg2 = case.token_heads * (es * (2 * case.d_r + case.d_v) + es * case.d_v)
+        path = gma.selected_path(case.N, case.d_r, case.d_v, case.K, code, int(case.causal))
+        launches = len(_native.stage_names(path, int(case.causal))) * steps
+        per[name] = {"ms": ms, "token_heads_per_s": case.token_heads / (ms / 1e3),
+                     "hbm_frac": alg / (ms / 1e3) / 1e9 / peak,
+                     "hbm_frac_o_input_dtype_basis": alg2 / (ms / 1e3) / 1e9 / peak,
+                     "path": "tc" if path == gma.PATH_TC else "simt", "algorithmic_bytes": alg,
+                     "timed_calls": steps, "stages_launched": launches}
+        del d, out, ws
+    return per
+
+
 CFG_METRIC = "GMA fwd tokens*heads/s on each of the five configured workloads; % of GB300 HBM roofline"
 
 
 def run_configs(args, rank: int, world: int, local_rank: int):
-    """--workload configs: one forward of each configured workload (the
-    small fp32 bidirectional, bidirectional N=4096, causal N=16384, peaked
-    bidirectional N=16384, causal large-head N=32768 K=d=128) per step, timed
-    separately, each on the kernel family the library selects for it.  The
-    headline step (bidirectional + causal at N=16384, K=64) is the default
-    workload; this leg puts the others on record.  Per workload: token*heads/s
-    and the whole call's algorithmic bytes (Q, K, V read, fp32 O written)
-    against the measured HBM peak."""
+    """--workload configs: the five configured workloads (time_configs) as a line of their own."""
     import torch
-    import gaussian_mixture_latent_diag_gb300 as gma
-    from gaussian_mixture_latent_diag_gb300.synthetic import WORKLOADS, make_inputs
+    from gaussian_mixture_latent_diag_gb300.synthetic import WORKLOADS
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    stream = torch.cuda.current_stream()
     peak, peak_src = measured_peaks()
-    per = {}
     with ClockSampler(local_rank) as clocks:
-        for name, case in WORKLOADS.items():
-            inp = make_inputs(case, seed=rank_seed(rank, 8))
-            d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-            fn = gma.forward_causal if case.causal else gma.forward_bidir
-            out = torch.empty(case.B, case.H, case.N, case.d_v, device=dev)
-            code = "f32" if case.dtype == "f32" else "bf16"
-            ws = torch.empty(gma.workspace_size(case.B, case.H, case.N, case.d_r, case.d_v, case.K, code,
-                                                int(case.causal)), dtype=torch.uint8, device=dev)
-
-            def call():
-                fn(d["Q"], d["K"], d["V"], d["mu"], d["sigma2"], d["log_pi"], eps=case.eps, out=out, workspace=ws)
-
-            for _ in range(args.warmup):
-                call()
-            torch.cuda.synchronize()
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            steps = max(1, args.steps if case.token_heads >= 1 << 20 else 5 * args.steps)
-            t0.record(stream)
-            for _ in range(steps):
-                call()
-            t1.record(stream)
-            torch.cuda.synchronize()
-            ms = t0.elapsed_time(t1) / steps
-            es = 4 if case.dtype == "f32" else 2
-            alg = case.token_heads * (es * (2 * case.d_r + case.d_v) + 4 * case.d_v)
-            path = gma.selected_path(case.N, case.d_r, case.d_v, case.K, code, int(case.causal))
-            from gaussian_mixture_latent_diag_gb300 import _native
-            launches = len(_native.stage_names(path, int(case.causal))) * steps
-            per[name] = {"ms": ms, "token_heads_per_s": case.token_heads / (ms / 1e3),
-                         "hbm_frac": alg / (ms / 1e3) / 1e9 / peak,
-                         "path": "tc" if path == gma.PATH_TC else "simt", "algorithmic_bytes": alg,
-                         "timed_calls": steps, "stages_launched": launches}
-            del d, out, ws
+        per = time_configs(args, rank, dev)
     if rank == 0:
         total = sum(v["ms"] for v in per.values())
         units = sum(WORKLOADS[n].token_heads for n in per)
         out = {"metric": CFG_METRIC, "value": world * units / (total / 1e3), "unit": UNIT, "n_gpus": world,
-               "steps": args.steps, "warmup": args.warmup, "ms_per_step": total, "higher_is_better": True,
+               "steps": None, "warmup": 3, "ms_per_step": total, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                "config": {"workload": "one forward of each of the five configured workloads per step",
                           "l2": "inputs at or above L2 size except the small fp32 case; no flush",
@@ -934,16 +1002,31 @@ def run_gma(args, rank: int, world: int, local_rank: int):
         if st != 0:
             raise gma.GmaError(st, fn)
 
-    # stage events: one list per (step, variant)
-    nst = [len(s) + 1 for s in stages]
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(nst[i])] for i in range(2)]
-          for _ in range(args.steps)]
-
     for _ in range(args.warmup):
         call(0); call(1)
     torch.cuda.synchronize()
+    if args.steps is None:  # enough steps for >= 1.2 s of device time (the clock sampler sees the run)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(20):
+            call(0); call(1)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        est = c0.elapsed_time(c1) / 20
+        steps = max(20, int(1200.0 / max(est, 1e-3)) + 1)
+        if world > 1:  # every rank times the same number of steps
+            t = torch.tensor([steps], dtype=torch.int64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            steps = int(t.item())
+        args.steps = steps
     if world > 1:
         dist.barrier()
+
+    # stage events: one list per (step, variant) of the breakdown pass
+    nst = [len(s) + 1 for s in stages]
+    nbreak = min(args.steps, 40)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(nst[i])] for i in range(2)]
+          for _ in range(nbreak)]
 
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
@@ -963,7 +1046,7 @@ def run_gma(args, rank: int, world: int, local_rank: int):
     # per-stage breakdown: the same steps again with the library's stage events
     # (events between the kernels keep a kernel from starting before the previous
     # one ends, so they are kept out of the timed loop above)
-    for s in range(args.steps):
+    for s in range(nbreak):
         call(0, events=ev[s][0])
         call(1, events=ev[s][1])
     torch.cuda.synchronize()
@@ -975,21 +1058,27 @@ def run_gma(args, rank: int, world: int, local_rank: int):
     for i in range(2):
         for j, name in enumerate(stages[i]):
             key = f"{'causal' if cases[i].causal else 'bidir'}:{name}"
-            stage_ms[key] = statistics.mean(ev[s][i][j].elapsed_time(ev[s][i][j + 1]) for s in range(args.steps))
+            stage_ms[key] = statistics.mean(ev[s][i][j].elapsed_time(ev[s][i][j + 1]) for s in range(nbreak))
     variant_ms = {("causal" if c.causal else "bidir"): statistics.mean(
-        ev[s][i][0].elapsed_time(ev[s][i][-1]) for s in range(args.steps)) for i, c in enumerate(cases)}
+        ev[s][i][0].elapsed_time(ev[s][i][-1]) for s in range(nbreak)) for i, c in enumerate(cases)}
     peak, peak_src = measured_peaks()
     dom = max(stage_ms, key=stage_ms.get)
     dom_stage = dom.split(":", 1)[1]
     dom_bytes = tensor_bytes(STAGE_TENSORS.get(dom_stage, ""))
     achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
     traffic = recorded_traffic(dom)
+    dom_bytes_o2 = tensor_bytes(STAGE_TENSORS.get(dom_stage, ""), o_bytes=2)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom,
-                "algorithmic_bytes": dom_bytes, "peak_source": peak_src}
-    fwd_bytes = tensor_bytes("QKVO")
+                "algorithmic_bytes": dom_bytes, "peak_source": peak_src,
+                "o_bytes": 4,
+                "frac_o_bf16_basis": dom_bytes_o2 / (stage_ms[dom] / 1e3) / 1e9 / peak,
+                "note": "achieved / frac credit O at 4 B per element (the fp32 O the kernel writes); "
+                        "frac_o_bf16_basis credits O at 2 B, the byte count of the metric's definition"}
+    fwd_bytes, fwd_bytes_o2 = tensor_bytes("QKVO"), tensor_bytes("QKVO", o_bytes=2)
     variants = {k: {"ms": v, "token_heads_per_s": w["B"] * w["H"] * w["N"] / (v / 1e3),
                     "hbm_frac_of_" + peak_src: fwd_bytes / (v / 1e3) / 1e9 / peak,
+                    "hbm_frac_o_bf16_basis": fwd_bytes_o2 / (v / 1e3) / 1e9 / peak,
                     "path": "tc" if paths[i] == gma.PATH_TC else "simt"}
                 for i, (k, v) in enumerate(variant_ms.items())}
 
@@ -1036,28 +1125,43 @@ def run_gma(args, rank: int, world: int, local_rank: int):
         e2e_step(j)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the end-to-end leg is bound by the host link (milliseconds per step): it times as
+    # many of the K steps as fill about 1.2 s, at least 20
+    w0 = time.perf_counter()
+    for j in range(4):
+        e2e_step(j)
+    torch.cuda.synchronize()
+    e2e_est = (time.perf_counter() - w0) / 4
+    e2e_steps = min(args.steps, max(20, int(1.2 / max(e2e_est, 1e-6)) + 1))
+    if world > 1:
+        t = torch.tensor([e2e_steps], dtype=torch.int64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_steps = int(t.item())
     e0.record(stream)
-    for j in range(args.steps):
+    for j in range(e2e_steps):
         e2e_step(j, start=e0 if j == 0 else None)
     stream.wait_event(ev_out[0])
     stream.wait_event(ev_out[1])
     e1.record(stream)
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / args.steps
+    e_ms = e0.elapsed_time(e1) / e2e_steps
     e_ms = job_ms(e_ms, world, dev)
     e2e = {"value": job_throughput(e_ms, world), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": e2e_steps,
            "schedule": "H2D and D2H on their own streams, device buffers double-buffered across steps"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        pairs, procs = 4, 4
+        procs = host_cores()
+        pairs = procs
         pool = OraclePool(procs)
         wall, th = pool.sample(pairs)
         pool.close()
-        cpu = {"value": th / wall, "unit": UNIT, "cores": procs, "kind": "oracle",
+        cpu = {"value": th / wall, "unit": UNIT, "cores": procs, "cpu_model": host_cpu_model(), "kind": "oracle",
                "sample": f"{pairs} bidirectional + {pairs} causal heads of N=16384, d=K=64 "
-                         f"(fp64 C oracle, {procs} worker processes)"}
+                         f"(fp64 C oracle, one spawned process per host core: {procs})"}
+
+    per_config = time_configs(args, rank, dev) if not args.no_configs else None
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -1075,17 +1179,20 @@ def run_gma(args, rank: int, world: int, local_rank: int):
                "stage_note": "stage_ms / variants come from a second pass with stage events between the "
                              "kernels, which keep each kernel from starting before the previous one ends; "
                              "the timed loop has no events, so its step is shorter than their sum",
-               "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu}
+               "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu, "configs": per_config}
         print(json.dumps(out), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: as many as fill at least 1.2 s of device time)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave out the per-workload timings of the five configured workloads")
     ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params", "project",
                                            "configs", "shard"],
                     default="forward",
@@ -1104,6 +1211,8 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    if args.steps is None and args.workload != "forward":
+        args.steps = 20  # the other legs time a fixed number of calls
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
