@@ -37,13 +37,12 @@ UNIT = "token*heads/s"
 
 # Algorithmic HBM bytes each stage accounts for, as the tensors of the path it
 # reads or writes (Q_X, K_X, V_X read once, O written once per forward);
-# intermediate scratch traffic is not algorithmic.  The tensor-core causal scan
-# reads Q and V and the key responsibilities its aggregation launch stored (K is
-# read, and credited, there).
+# intermediate scratch traffic is not algorithmic.  The single-pass tensor-core
+# causal scan reads Q, K and V and writes O.
 STAGE_TENSORS = {
     "prep": "", "reset": "", "reduce": "", "scan": "",
     "resp_q": "Q", "resp_k": "K", "write": "V", "read": "O", "causal": "VO",
-    "tc_write": "KV", "tc_read": "QO", "tc_causal": "QVO", "tc_aggregate": "KV",
+    "tc_write": "KV", "tc_read": "QO", "tc_causal": "QVO", "tc_aggregate": "KV", "tc_scan": "QKVO",
 }
 
 
@@ -986,11 +985,15 @@ def run_gma(args, rank: int, world: int, local_rank: int):
     stream = torch.cuda.current_stream()
     lib = gma.load()
 
-    def call(i, O=None, events=None, d=None):
+    ws1 = torch.empty(max(256, gma.workspace_size(w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"], 1,
+                                                  path=gma.PATH_TC_SINGLE_PASS)), dtype=torch.uint8, device=dev)
+
+    def call(i, O=None, events=None, d=None, path=gma.PATH_AUTO):
         c = cases[i]
         d = dinp[i] if d is None else d
         fn = "gma_forward_causal" if c.causal else "gma_forward_bidir"
-        opt = _native.options(stage_events=events)
+        opt = _native.options(stage_events=events, path=path)
+        ws = ws1 if path == gma.PATH_TC_SINGLE_PASS else wss[i]
         import ctypes
         vp = ctypes.c_void_p
         st = getattr(lib, fn)(vp(d["Q"].data_ptr()), vp(d["K"].data_ptr()), vp(d["V"].data_ptr()),
@@ -998,7 +1001,7 @@ def run_gma(args, rank: int, world: int, local_rank: int):
                               vp(d["log_pi"].data_ptr()), float(w["eps"]),
                               vp((O if O is not None else outs[i]).data_ptr()),
                               w["B"], w["H"], w["N"], w["d_r"], w["d_v"], w["K"], ctypes.byref(opt),
-                              vp(wss[i].data_ptr()), wss[i].numel(), vp(stream.cuda_stream))
+                              vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream))
         if st != 0:
             raise gma.GmaError(st, fn)
 
@@ -1081,6 +1084,25 @@ def run_gma(args, rank: int, world: int, local_rank: int):
                     "hbm_frac_o_bf16_basis": fwd_bytes_o2 / (v / 1e3) / 1e9 / peak,
                     "path": "tc" if paths[i] == gma.PATH_TC else "simt"}
                 for i, (k, v) in enumerate(variant_ms.items())}
+    # the single-pass causal kernel (GMA_PATH_TC_SINGLE_PASS), timed on its own; not part of the step
+    if gma.selected_path(w["N"], w["d_r"], w["d_v"], w["K"], w["dtype"], 1, path=gma.PATH_TC_SINGLE_PASS) == \
+            gma.PATH_TC_SINGLE_PASS:
+        for _ in range(3):
+            call(1, path=gma.PATH_TC_SINGLE_PASS)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 40
+        s0.record(stream)
+        for _ in range(reps):
+            call(1, path=gma.PATH_TC_SINGLE_PASS)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        v = s0.elapsed_time(s1) / reps
+        variants["causal_single_pass"] = {
+            "ms": v, "token_heads_per_s": w["B"] * w["H"] * w["N"] / (v / 1e3),
+            "hbm_frac_of_" + peak_src: fwd_bytes / (v / 1e3) / 1e9 / peak,
+            "hbm_frac_o_bf16_basis": fwd_bytes_o2 / (v / 1e3) / 1e9 / peak, "path": "tc_single_pass",
+            "note": "GMA_PATH_TC_SINGLE_PASS (Gamma^K kept on chip, one kernel after the prep); timed alone, "
+                    "not part of the step"}
 
     # end to end through the public API: pinned host inputs; every step copies its inputs up and
     # its outputs down inside the timed region.  Host-to-device and device-to-host copies run on

@@ -20,15 +20,15 @@ from __future__ import annotations
 
 import ctypes
 
-from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, GmaError, load,
-                      options, status_string)
+from ._native import (GMA_BF16, GMA_F32, PATH_AUTO, PATH_SIMT, PATH_TC, PATH_TC_SINGLE_PASS, GmaError,
+                      load, options, status_string)
 
 __all__ = ["forward_bidir", "forward_causal", "backward_bidir", "backward_causal", "responsibilities",
            "latent_memory", "read_memory", "forward_causal_carry", "decode_step", "routing_stats",
            "reparameterize", "reparameterize_backward", "project_qkv",
            "workspace_size",
            "selected_path", "last_device_status", "GmaError", "PATH_AUTO", "PATH_SIMT",
-           "PATH_TC", "load"]
+           "PATH_TC", "PATH_TC_SINGLE_PASS", "load"]
 
 
 def _dtype_code(t) -> int:

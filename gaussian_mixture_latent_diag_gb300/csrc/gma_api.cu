@@ -36,6 +36,9 @@ int choose_path(const Problem &p, int causal, const gma_options *opt) {
     if (path == GMA_PATH_SIMT) return GMA_PATH_SIMT;
     bool tc = causal >= 0 && gma::tc_supported(p, causal);
     if (path == GMA_PATH_TC) return tc ? GMA_PATH_TC : -1;
+    // the single-pass kernel is a causal kernel; the bidirectional tensor-core call
+    // already keeps Gamma on chip
+    if (path == GMA_PATH_TC_SINGLE_PASS) return !tc ? -1 : causal == 1 ? GMA_PATH_TC_SINGLE_PASS : GMA_PATH_TC;
     if (path != GMA_PATH_AUTO) return -1;
     return tc ? GMA_PATH_TC : GMA_PATH_SIMT;
 }
@@ -44,7 +47,7 @@ int choose_path(const Problem &p, int causal, const gma_options *opt) {
 // chunks of 128 tokens (its tile), the CUDA-core scan in chunks of
 // kSimtCausalChunk.  options->chunk must be 0 (the family's value) or exactly
 // that value; other lengths are not built.
-int family_chunk(int path) { return path == GMA_PATH_TC ? 128 : gma::kSimtCausalChunk; }
+int family_chunk(int path) { return path == GMA_PATH_SIMT ? gma::kSimtCausalChunk : 128; }
 bool chunk_ok(int path, int causal, const gma_options *opt) {
     if (!opt || opt->chunk == 0 || causal != 1) return true;
     return opt->chunk == family_chunk(path);
@@ -52,6 +55,7 @@ bool chunk_ok(int path, int causal, const gma_options *opt) {
 
 size_t workspace_for(const Problem &p, int causal, const gma_options *opt, int path) {
     int splits = opt ? opt->splits : 0;
+    if (path == GMA_PATH_TC_SINGLE_PASS) return gma::tc_scan_workspace(p, splits);
     if (path == GMA_PATH_TC) return gma::tc_workspace(p, causal, splits);
     return gma::simt_layout(p, causal, splits).total;
 }
@@ -70,6 +74,8 @@ int memory_path(const Problem &p, int causal, const gma_options *opt) {
     const int path = opt ? opt->path : GMA_PATH_AUTO;
     if (path == GMA_PATH_AUTO || path == GMA_PATH_SIMT) return GMA_PATH_SIMT;
     if (path == GMA_PATH_TC) return gma::tc_supported(p, causal) ? GMA_PATH_TC : -1;
+    if (path == GMA_PATH_TC_SINGLE_PASS)
+        return !gma::tc_supported(p, causal) ? -1 : causal == 1 ? GMA_PATH_TC_SINGLE_PASS : GMA_PATH_TC;
     return -1;
 }
 
@@ -131,7 +137,9 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     const int splits = options ? options->splits : 0;
     gma::StageClock clk = clock_for(options, s);
     cudaError_t err;
-    if (path == GMA_PATH_TC)
+    if (path == GMA_PATH_TC_SINGLE_PASS)
+        err = gma::tc_causal_1pass(p, splits, workspace, s, clk);
+    else if (path == GMA_PATH_TC)
         err = causal ? gma::tc_causal(p, splits, workspace, s, clk) : gma::tc_bidir(p, splits, workspace, s, clk);
     else
         err = causal ? gma::simt_causal(p, workspace, s, clk) : gma::simt_bidir(p, splits, workspace, s, clk);
@@ -486,8 +494,10 @@ size_t gma_causal_carry_workspace_size(int B, int H, int N, int d_r, int d_v, in
     Problem p;
     p.dtype = dtype; p.B = B; p.H = H; p.N = N; p.d_r = d_r; p.d_v = d_v; p.K = K;
     const size_t simt = gma::simt_layout(p, 1, 0).total;
-    const size_t tc = gma::tc_supported(p, 1) ? gma::tc_workspace(p, 1, 0) : 0;
-    return simt > tc ? simt : tc;  // enough for either kernel family
+    size_t tc = gma::tc_supported(p, 1) ? gma::tc_carry_workspace(p) : 0;
+    const size_t tc1 = gma::tc_supported(p, 1) ? gma::tc_scan_workspace(p, 0) : 0;
+    tc = tc > tc1 ? tc : tc1;
+    return simt > tc ? simt : tc;  // enough for any kernel family
 }
 
 gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void *V_X, gma_dtype dtype,
@@ -513,7 +523,9 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
     if (options && options->chunk < 0) return GMA_ERR_INVALID_ARG;
     const int path = memory_path(p, 1, options);
     if (path < 0 || !chunk_ok(path, 1, options)) return GMA_ERR_UNSUPPORTED_SHAPE;
-    const size_t need = path == GMA_PATH_TC ? gma::tc_workspace(p, 1, 0) : gma::simt_layout(p, 1, 0).total;
+    const size_t need = path == GMA_PATH_TC_SINGLE_PASS ? gma::tc_scan_workspace(p, 0)
+                        : path == GMA_PATH_TC            ? gma::tc_carry_workspace(p)
+                                                         : gma::simt_layout(p, 1, 0).total;
     if (workspace_bytes < need) return GMA_ERR_WORKSPACE_TOO_SMALL;
     const size_t es = dtype == GMA_F32 ? 4 : 2, rows = (size_t)B * H * N;
     const size_t nvt = 4 * (size_t)B * H * K * d_v, nz = 4 * (size_t)B * H * K;
@@ -534,7 +546,9 @@ gma_status gma_forward_causal_carry(const void *Q_X, const void *K_X, const void
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gma::StageClock clk = clock_for(options, s);
     const cudaError_t err =
-        path == GMA_PATH_TC ? gma::tc_causal_carry(p, 0, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk)
+        path == GMA_PATH_TC_SINGLE_PASS
+            ? gma::tc_causal_carry_1pass(p, 0, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk)
+        : path == GMA_PATH_TC ? gma::tc_causal_carry(p, 0, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk)
                             : gma::simt_causal_carry(p, Vt_in, Z_in, Vt_out, Z_out, workspace, s, clk);
     return finish(err, options, workspace, s);
 }
@@ -652,6 +666,11 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
 }
 
 int gma_stage_count(int path, int variant) {
+    if (path == GMA_PATH_TC_SINGLE_PASS) {
+        if (variant == 1 || variant == 8) return 2;
+        if (variant == 0 || variant == 4 || variant == 7) path = GMA_PATH_TC;  // as GMA_PATH_TC
+        else return 0;
+    }
     const bool tc_aux = path == GMA_PATH_TC && (variant == 4 || variant == 7 || variant == 8);
     if (variant < -1 || variant > 8 || (variant >= 2 && path != GMA_PATH_SIMT && !tc_aux)) return 0;
     const char *const *names;
@@ -669,6 +688,10 @@ int gma_stage_count(int path, int variant) {
 const char *gma_stage_name(int path, int variant, int j) {
     int n = gma_stage_count(path, variant);
     if (j < 0 || j >= n) return nullptr;
+    if (path == GMA_PATH_TC_SINGLE_PASS) {
+        if (variant == 1 || variant == 8) return gma::kTcScanStages[j];
+        path = GMA_PATH_TC;
+    }
     if (variant >= 4) return path == GMA_PATH_TC ? gma::kAuxTcStages[variant - 4][j] : gma::kAuxStages[variant - 4][j];
     if (variant >= 2) return gma::kBackwardStages[variant - 2][j];
     return path == GMA_PATH_SIMT ? gma::kSimtStages[variant + 1][j] : gma::kTcStages[variant + 1][j];

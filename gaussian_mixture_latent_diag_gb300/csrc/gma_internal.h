@@ -145,6 +145,15 @@ cudaError_t tc_project_qkv(const void *X, const void *Wq, const void *Wk, const 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);
 size_t tc_workspace(const Problem &p, int causal, int splits);
+size_t tc_carry_workspace(const Problem &p);  // the carried-prefix causal forward (tc_causal_carry)
+// The single-pass causal forward (GMA_PATH_TC_SINGLE_PASS): one kernel after the
+// coefficient prep, key responsibilities kept on chip, prefix memories chained
+// between chunks through global memory (tc_supported(p, 1) sizes).
+size_t tc_scan_workspace(const Problem &p, int splits);
+cudaError_t tc_causal_1pass(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
+cudaError_t tc_causal_carry_1pass(const Problem &p, int splits, const float *Vt_in, const float *Z_in,
+                                  float *Vt_out, float *Z_out, void *ws, cudaStream_t s, StageClock &clk);
+extern const char *const kTcScanStages[8];  // stage names of both, NULL-terminated
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 extern const char *const kTcStages[3][8];    // [variant + 1][j], NULL-terminated

@@ -1775,6 +1775,691 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ causal, single pass
+//
+// Causal GMA ([GMA, Eq. (8b)]) in one pass over Q_X, K_X and V_X: each CTA
+// takes 128-token chunks and computes, for each, the key side (Gamma^K, kept
+// in shared memory, and the chunk's memory increment U = Gamma^K^T [V | 1])
+// and the query side (Gamma^Q, the masked intra-chunk P = Gamma^Q Gamma^K^T,
+// P [V | 1] and the read of the prefix memory S before the chunk):
+//   O_i = (sum_{j <= i in chunk} P_ij [V_j | 1] + gQ_i [S | Z]) split as [num | den],
+//   O_i = num / (den + eps r_i),  r_i the un-normalised query row sum.
+//
+// The prefix memory before chunk t of a head is the sum of the increments of
+// chunks 0 .. t-1 ("cumulative sums along the sequence dimension").  Chunks
+// are handed out in (chunk index, head) order, CTA c taking every G-th one, so
+// the CTAs working at one time hold consecutive chunks of each head.  Every
+// chunk publishes its increment in global memory as soon as its key side is
+// done; chunk t then sums, in a fixed order, the inclusive prefix published
+// by the last chunk of the previous block of kBlock chunks and the increments
+// of the chunks of its own block before it.  The last chunk of each block
+// publishes its inclusive prefix.  The summation order depends only on t, so
+// results are bitwise reproducible; the waits are bounded.  The published
+// memories have one slot per chunk, written once per call; the flags carry the
+// chunk index, and a reader checks them again after reading.
+//
+// Warps: 0 lane 0 TMA loads, 1 lane 0 MMA issue (a fixed order per chunk),
+// 2..5 key group (key softmax -> Gamma^K, half of the P split, increment),
+// 6..9 query group (query softmax -> Gamma^Q, half of the P split, x^2 of the
+// next key and query tiles, outputs), 10..13 scan group (look-back, prefix
+// operand).
+//
+// TMEM (512 columns):
+//   [0, 64)    x^2 of K (hi | lo);  [64, 128) x^2 of Q;  both free once the
+//              chunk's score MMAs are done: then [0, 80) holds U (M = 128:
+//              hi-part rows 0..63, lo-part rows 64..127; N = 80 = [V | 1])
+//   [128, 256) key scores (N = 64, first half), then P, then P hi | lo in place
+//              per 32-key block
+//   [256, 320) / [320, 384)  query scores (N = 64), then Gamma^Q hi | lo over
+//              them; chunks alternate between the two, so a chunk's Gamma^Q
+//              stays for its state read while the next chunk's is formed
+//   [384, 464) [num | den] (N = 80)
+// MMA issue order, chunk i:  U(i), P(i), state read(i - 1), P [V | 1](i),
+// key scores(i + 1), query scores(i + 1).  The state read of a chunk comes one
+// stage late, after the next chunk's P, so the look-back has about a chunk's
+// time to finish before anything waits for it.
+// MMAs per chunk: key scores 20, query scores 20 (five N = 64 products per
+// K step, one accumulator), U 8, P 12 (N = 128), P [V | 1] 16, state read 12.
+// Every MMA batch is unrolled with its operands a base plus constants.
+namespace scan {
+constexpr int kBlock = 4;              // chunks per look-back block
+constexpr int kState4 = kKP * kW / 4;  // float4 of one [64][68] memory (1088)
+constexpr int kQ4 = (kState4 + 127) / 128;  // float4 per key-group thread (9)
+constexpr uint32_t kAggBit = 1u, kInclBit = 2u;
+}  // namespace scan
+
+struct ScanSmem {
+    static constexpr int kQ = 0;                               // Q tile
+    static constexpr int kK = kQ + kTileBytes;                 // K tile
+    static constexpr int kV = kK + kTileBytes;                 // V tiles, 2 stages
+    static constexpr int kOnes = kV + 2 * kTileBytes;          // ones columns of [V | 1] (2 KB)
+    static constexpr int kGB = kOnes + 2048;                   // [Gamma^K ; S^T], 26 groups of 2 KB
+    static constexpr int kGroups = (kTile + 80) / 8;
+    static constexpr int kCoef = kGB + kGroups * 2048;
+    static constexpr int kAgg = (kCoef + kCoefBytes + 1023) & ~1023;  // this chunk's increment [64][68] fp32
+    static constexpr int kS = kAgg + kKP * kW * 4;             // exchange / prefix memory [64][68] fp32
+    static constexpr int kStage = (kS + kKP * kW * 4 + 1023) & ~1023;  // output staging 4 x 8 KB
+    static constexpr int kBars = kStage + 4 * 8192;
+    static constexpr int kBytes = kBars + 256;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kOnes % 1024 == 0 && kGB % 1024 == 0 && kCoef % 1024 == 0 && kStage % 1024 == 0, "SW128");
+    static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+// Softmax of one N = 64 score row (s_k + c_k, max-subtracted exponentials) and
+// the bf16 hi / lo split: key side (to_smem != 0): normalised (scale 0 for rows
+// past N), written as row `row` of the [Gamma^K ; S^T] buffer; query side:
+// un-normalised, hi words to t_out + 0..31 and lo words to t_out + 32..63.
+// Returns the row sum of the exponentials.
+__device__ __noinline__ float scan_softmax_row(uint32_t s_taddr, const float *cvec, int to_smem, uint32_t t_out,
+                                               uint8_t *gb, int row, int valid) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(s_taddr, r0);
+    tmem_ld32(s_taddr + 32, r1);
+    tmem_wait_ld();
+    tc_fence_before();
+    float e[kKP];
+    const float4 *c4 = reinterpret_cast<const float4 *>(cvec);
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 ca = c4[q], cb = c4[q + 8];
+        const float2 a0 = f2_add(make_float2(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1])),
+                                 make_float2(ca.x, ca.y));
+        const float2 a1 = f2_add(make_float2(__uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3])),
+                                 make_float2(ca.z, ca.w));
+        const float2 b0 = f2_add(make_float2(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1])),
+                                 make_float2(cb.x, cb.y));
+        const float2 b1 = f2_add(make_float2(__uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3])),
+                                 make_float2(cb.z, cb.w));
+        e[4 * q] = a0.x; e[4 * q + 1] = a0.y; e[4 * q + 2] = a1.x; e[4 * q + 3] = a1.y;
+        e[32 + 4 * q] = b0.x; e[32 + 4 * q + 1] = b0.y; e[32 + 4 * q + 2] = b1.x; e[32 + 4 * q + 3] = b1.y;
+        m0 = fmaxf(m0, fmaxf(fmaxf(a0.x, a0.y), fmaxf(a1.x, a1.y)));
+        m1 = fmaxf(m1, fmaxf(fmaxf(b0.x, b0.y), fmaxf(b1.x, b1.y)));
+    }
+    const float m = fmaxf(m0, m1);
+    const float2 mm = make_float2(m, m);
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kKP; k += 4) {
+        const float2 d0 = f2_sub(make_float2(e[k], e[k + 1]), mm), d1 = f2_sub(make_float2(e[k + 2], e[k + 3]), mm);
+        e[k] = ex2(d0.x); e[k + 1] = ex2(d0.y); e[k + 2] = ex2(d1.x); e[k + 3] = ex2(d1.y);
+        s0 = f2_add(s0, make_float2(e[k], e[k + 1]));
+        s1 = f2_add(s1, make_float2(e[k + 2], e[k + 3]));
+    }
+    const float rs = (s0.x + s0.y) + (s1.x + s1.y);
+    uint32_t wh[32], wl[32];
+    split_row(e, to_smem ? (valid ? 1.0f / rs : 0.0f) : 1.0f, wh, wl);
+    if (to_smem) {
+        store_gamma_words(gb, row, wh, wl);
+    } else {
+        tmem_st32(t_out, wh);
+        tmem_st32(t_out + 32, wl);
+        tmem_wait_st();
+    }
+    return rs;
+}
+
+// The chunk's memory increment out of the U accumulator: row `row` < 64 holds
+// the hi-part sums of component row, row 64 + k the lo-part sums of component
+// k (80 columns: 64 values, Z, zero padding).  Thread k keeps columns 0..31 of
+// component k, thread 64 + k columns 32..64; the other half goes to the
+// partner through Agg itself (each thread then reads back and overwrites only
+// the half it owns).  After the key group's barrier each thread writes its
+// columns of agg = hi + lo to Agg ([64][kW], shared) and to `gagg` (the
+// chunk's published slot, same layout); the padding columns 65..67 are written
+// as zeros.  `uread` is arrived on (lane 0) once U is in registers.
+__device__ __noinline__ void scan_take_increment(uint32_t u_taddr, float *Agg, float *gagg, int row,
+                                                 uint64_t *uread, int lane) {
+    float *X = Agg;
+    const int kc = row & (kKP - 1), half = row >> 6;
+    uint32_t a0[32], a1[32], z[16];
+    tmem_ld32(u_taddr, a0);
+    tmem_ld32(u_taddr + 32, a1);
+    tmem_ld16(u_taddr + 64, z);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(uread);
+    float *xr = X + kc * kW;
+    if (half == 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(xr + 32 + 4 * q) =
+                make_float4(__uint_as_float(a1[4 * q]), __uint_as_float(a1[4 * q + 1]),
+                            __uint_as_float(a1[4 * q + 2]), __uint_as_float(a1[4 * q + 3]));
+        xr[64] = __uint_as_float(z[0]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(xr + 4 * q) =
+                make_float4(__uint_as_float(a0[4 * q]), __uint_as_float(a0[4 * q + 1]),
+                            __uint_as_float(a0[4 * q + 2]), __uint_as_float(a0[4 * q + 3]));
+    }
+    named_sync(1, 128);
+    const uint32_t *own = half == 0 ? a0 : a1;
+    float *ar = Agg + kc * kW + 32 * half;
+    float *gr = gagg + kc * kW + 32 * half;
+    const float *pr = xr + 32 * half;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 p = *reinterpret_cast<const float4 *>(pr + 4 * q);
+        const float4 v = make_float4(__uint_as_float(own[4 * q]) + p.x, __uint_as_float(own[4 * q + 1]) + p.y,
+                                     __uint_as_float(own[4 * q + 2]) + p.z, __uint_as_float(own[4 * q + 3]) + p.w);
+        *reinterpret_cast<float4 *>(ar + 4 * q) = v;
+        __stcg(reinterpret_cast<float4 *>(gr + 4 * q), v);
+    }
+    if (half) {
+        const float4 v = make_float4(__uint_as_float(z[0]) + xr[64], 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(Agg + kc * kW + 64) = v;
+        __stcg(reinterpret_cast<float4 *>(gagg + kc * kW + 64), v);
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until the flag of chunk `t` carries `bit` (flag = (t + 1) << 2 |
+// published bits).  Returns 0, or GMA_ERR_TIMEOUT when the wait runs out or
+// the slot has been taken by a later chunk.
+__device__ __noinline__ unsigned scan_wait_flag(const unsigned *flag, int t, uint32_t bit, const int *abort_flag) {
+    const uint32_t want = (uint32_t)(t + 1);
+    uint64_t t0 = 0;
+    for (int spin = 0;; ++spin) {
+        const uint32_t f = ld_acquire_u32(flag);
+        if ((f >> 2) == want && (f & bit)) return 0u;
+        if ((f >> 2) > want) return (unsigned)GMA_ERR_TIMEOUT;
+        if ((spin & 255) == 255) {
+            if (*reinterpret_cast<const volatile int *>(abort_flag)) return (unsigned)GMA_ERR_TIMEOUT;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kWaitLimitNs) return (unsigned)GMA_ERR_TIMEOUT;
+        }
+    }
+}
+
+// Global state of the scan: flags [BH][R] and the published memories
+// [BH][R][2][64][kW] fp32 (0: increment, 1: inclusive prefix), R = chunks per head.
+struct ScanGlobal {
+    unsigned *flags;
+    float *ring;
+    int R;
+    __device__ __forceinline__ unsigned *flag(int bh, int t) const { return flags + (size_t)bh * R + (t % R); }
+    __device__ __forceinline__ float *slot(int bh, int t, int kind) const {
+        return ring + (((size_t)bh * R + (t % R)) * 2 + kind) * (size_t)(kKP * kW);
+    }
+};
+
+// Prefix memory before chunk t of head bh, by the key group (128 threads):
+// S = incl(base) + agg(base + 1) + ... + agg(t - 1), base the last chunk of the
+// previous block (an empty prefix before the first block), in that order.
+// The last chunk of a block then publishes incl(t) = S + agg(t).  S goes to
+// the shared [64][kW] buffer.  Returns 0 or an error code (the same in every
+// thread).
+__device__ __noinline__ unsigned scan_lookback(const ScanGlobal &G, int bh, int t, int ntiles, const float *Agg,
+                                               float *S, int tid, const int *abort_flag, unsigned *err_word,
+                                               const CombineIO &io, int bar_id) {
+    using namespace scan;
+    const int base = (t / kBlock) * kBlock - 1;
+    // thread j waits for one published memory: j = 0 the block base's prefix, j >= 1 increment base + j
+    if (tid == 0) *err_word = 0u;
+    named_sync(bar_id, 128);
+    if (tid < t - base) {
+        const int j = base + tid;
+        unsigned e = 0u;
+        if (tid == 0) {
+            if (base >= 0) e = scan_wait_flag(G.flag(bh, base), base, kInclBit, abort_flag);
+        } else {
+            e = scan_wait_flag(G.flag(bh, j), j, kAggBit, abort_flag);
+        }
+        if (e) atomicOr(err_word, e);
+    }
+    named_sync(bar_id, 128);
+    unsigned err = *reinterpret_cast<volatile unsigned *>(err_word);
+    float4 acc[kQ4];
+    if (!err) {
+        const float4 *src0 = base >= 0 ? reinterpret_cast<const float4 *>(G.slot(bh, base, 1)) : nullptr;
+#pragma unroll
+        for (int q = 0; q < kQ4; ++q) {
+            const int e4 = tid + 128 * q;
+            // the first block starts from the caller's carried-in memory, if any
+            acc[q] = e4 >= kState4 ? make_float4(0.f, 0.f, 0.f, 0.f)
+                     : src0        ? __ldcg(src0 + e4)
+                     : io.carry_vt ? io_load(io, bh, e4 / (kW / 4), 4 * (e4 % (kW / 4)))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // increments base + 1 .. t - 1, two at a time (loads in flight together, sums in order)
+        for (int j = base + 1; j < t; j += 2) {
+            const bool two = j + 1 < t;
+            const float4 *src0 = reinterpret_cast<const float4 *>(G.slot(bh, j, 0));
+            const float4 *src1 = reinterpret_cast<const float4 *>(G.slot(bh, two ? j + 1 : j, 0));
+            float4 v0[kQ4], v1[kQ4];
+#pragma unroll
+            for (int q = 0; q < kQ4; ++q) {
+                const int e4 = tid + 128 * q;
+                const bool in = e4 < kState4;
+                v0[q] = in ? __ldcg(src0 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v1[q] = (in && two) ? __ldcg(src1 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < kQ4; ++q) {
+                acc[q].x += v0[q].x; acc[q].y += v0[q].y; acc[q].z += v0[q].z; acc[q].w += v0[q].w;
+                if (two) {
+                    acc[q].x += v1[q].x; acc[q].y += v1[q].y; acc[q].z += v1[q].z; acc[q].w += v1[q].w;
+                }
+            }
+        }
+        // the slots read must still belong to the chunks they were read for
+        if (tid < t - base && !(tid == 0 && base < 0)) {
+            const int j = base + tid;
+            const uint32_t f = ld_acquire_u32(G.flag(bh, j));
+            if ((f >> 2) != (uint32_t)(j + 1)) atomicOr(err_word, (unsigned)GMA_ERR_TIMEOUT);
+        }
+    }
+    const bool publish = (t % kBlock == kBlock - 1) && t + 1 < ntiles;
+    const bool last_out = t + 1 == ntiles && io.out_vt;  // the memory after the last position, to the caller
+    if (!err) {
+        float4 *dst = publish ? reinterpret_cast<float4 *>(G.slot(bh, t, 1)) : nullptr;
+#pragma unroll
+        for (int q = 0; q < kQ4; ++q) {
+            const int e4 = tid + 128 * q;
+            if (e4 >= kState4) continue;
+            reinterpret_cast<float4 *>(S)[e4] = acc[q];
+            if (dst || last_out) {
+                const float4 a = reinterpret_cast<const float4 *>(Agg)[e4];
+                const float4 v = make_float4(acc[q].x + a.x, acc[q].y + a.y, acc[q].z + a.z, acc[q].w + a.w);
+                if (dst) __stcg(dst + e4, v);
+                if (last_out) io_store(io, bh, e4 / (kW / 4), 4 * (e4 % (kW / 4)), v);
+            }
+        }
+    }
+    // every thread's stores precede the barrier; thread 0's fence after it makes
+    // them visible device-wide (cumulatively) before the flag
+    named_sync(bar_id, 128);
+    err = *reinterpret_cast<volatile unsigned *>(err_word);
+    if (!err && publish && tid == 0) {
+        __threadfence();
+        st_release_u32(G.flag(bh, t), ((uint32_t)(t + 1) << 2) | kAggBit | kInclBit);
+    }
+    return err;
+}
+
+constexpr int kThreadsScan = 64 + 384;
+
+__global__ void __launch_bounds__(kThreadsScan, 1) tc_scan_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+    const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, ScanGlobal G, int H, int BH,
+    int N, float eps, int o_bf16, int stall, CombineIO io, unsigned *status) {
+    using L = ScanSmem;
+    using namespace scan;
+    constexpr int kTmemCols = 512;
+    constexpr uint32_t kX = 0, kU = 0, kP = 128, kSK = kP, kSQ = 256, kO = 384;
+    // query scores / Gamma^Q of chunk i: columns kSQ + 64 (i & 1)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qst = smem + L::kQ, *kst = smem + L::kK, *vst = smem + L::kV, *gb = smem + L::kGB, *coef = smem + L::kCoef;
+    float *Agg = reinterpret_cast<float *>(smem + L::kAgg), *S = reinterpret_cast<float *>(smem + L::kS);
+    uint8_t *stg = smem + L::kStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *qfull = bars, *qempty = bars + 1, *kfull = bars + 2, *kempty = bars + 3, *vfull = bars + 4,
+             *vempty = bars + 6, *cfull = bars + 8, *cfree = bars + 9, *xk = bars + 10, *xq = bars + 11,
+             *sk = bars + 12, *sq = bars + 13, *gk = bars + 14, *gq = bars + 15, *uf = bars + 16, *uread = bars + 17,
+             *pf = bars + 18, *psplit = bars + 19, *of = bars + 20, *oread = bars + 21, *sready = bars + 22;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 23);
+    int *abort_flag = reinterpret_cast<int *>(bars + 24);
+    unsigned *err_word = reinterpret_cast<unsigned *>(bars + 25);
+    uint64_t *fin = bars + 26, *aggready = bars + 27, *aggfree = bars + 28;
+    static_assert(29 * 8 <= 256, "barrier area");
+    const float *cvec = reinterpret_cast<const float *>(coef + 4 * kCoefMatBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, Gn = gridDim.x;
+    const int ntiles = (N + kTile - 1) / kTile;
+    const int total = BH * ntiles;
+    const int n = c < total ? (total - c + Gn - 1) / Gn : 0;  // chunks of this CTA
+    if (n == 0) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(qfull, 1); mbar_init(qempty, 1); mbar_init(kfull, 1); mbar_init(kempty, 1);
+        mbar_init(&vfull[0], 1); mbar_init(&vfull[1], 1); mbar_init(&vempty[0], 1); mbar_init(&vempty[1], 1);
+        mbar_init(cfull, 1); mbar_init(cfree, 8);
+        mbar_init(xk, 4); mbar_init(xq, 4); mbar_init(sk, 1); mbar_init(sq, 1); mbar_init(gk, 4); mbar_init(gq, 4);
+        mbar_init(uf, 1); mbar_init(uread, 4); mbar_init(pf, 1); mbar_init(psplit, 8); mbar_init(of, 1);
+        mbar_init(oread, 4); mbar_init(sready, 4); mbar_init(fin, 1); mbar_init(aggready, 4); mbar_init(aggfree, 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
+    }
+    {   // ones columns of [V | 1]; zero [Gamma^K ; S^T] (the S^T padding rows must be 0)
+        const uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        for (int i = tid; i < 2048 / 16; i += kThreadsScan) reinterpret_cast<uint4 *>(smem + L::kOnes)[i] = one4;
+        for (int i = tid; i < L::kGroups * 2048 / 16; i += kThreadsScan)
+            reinterpret_cast<uint4 *>(gb)[i] = make_uint4(0, 0, 0, 0);
+    }
+    // Everything below reads the coefficient prep's output (images, error words,
+    // cleared status and flags): wait for it, then let the next kernel launch.
+    pdl_wait();
+    pdl_trigger();
+    {
+        const unsigned herr = warp == 1 ? head_error_warp(head_err, H, lane) : 0u;
+        if (tid == 32 && (herr || failed(status))) {
+            if (herr) set_status(status, herr);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    cta_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (!aborted(abort_flag)) {
+        if (warp == 0) {
+            if (lane == 0) {
+                // ---------------- TMA: per chunk K, Q, V (2 stages), then the head's coefficients
+                int karm = -1, qarm = -1, varm[2] = {-1, -1}, carm = -1;
+                for (int i = 0; i < n; ++i) {
+                    const int g = c + i * Gn, t = g / BH, bh = g % BH, h = bh % H;
+                    if (!wait_or_abort(kempty, (i & 1) ^ 1, status, abort_flag)) break;
+                    if (!(stall && i == 0)) {  // test hook: the first key tile is never loaded
+                        mbar_arrive_expect_tx(kfull, kTileBytes);
+                        tma_load_3d(kst, &tmK, 0, t * kTile, bh, kfull);
+                        karm = i;
+                    }
+                    if (!wait_or_abort(qempty, (i & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(qfull, kTileBytes);
+                    tma_load_3d(qst, &tmQ, 0, t * kTile, bh, qfull);
+                    qarm = i;
+                    const int vs = i & 1;
+                    if (!wait_or_abort(&vempty[vs], ((i >> 1) & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(&vfull[vs], kTileBytes);
+                    tma_load_3d(vst + vs * kTileBytes, &tmV, 0, t * kTile, bh, &vfull[vs]);
+                    varm[vs] = i;
+                    if (i > 0 && !wait_or_abort(cfree, (i - 1) & 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(cfull, kCoefBytes);
+                    bulk_load(coef, coef_img + (size_t)h * kCoefStride, kCoefBytes, cfull);
+                    carm = i;
+                }
+                // every load armed here has landed before the CTA leaves
+                if (karm >= 0) mbar_wait(kfull, karm & 1);
+                if (qarm >= 0) mbar_wait(qfull, qarm & 1);
+                for (int s = 0; s < 2; ++s)
+                    if (varm[s] >= 0) mbar_wait(&vfull[s], (varm[s] >> 1) & 1);
+                if (carm >= 0) mbar_wait(cfull, carm & 1);
+            }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                // ---------------- MMA issue, a fixed order per chunk i:
+                //   U(i), P(i), P [V|1](i), key scores(i+1), state read(i), query scores(i+1)
+                // (chunk 0's scores first).  Each batch waits for its inputs.
+                const uint64_t dq = sdesc_sw128(smem_u32(qst), 16, 1024), dk = sdesc_sw128(smem_u32(kst), 16, 1024);
+                const uint64_t dc = sdesc_sw128(smem_u32(coef), 16, 1024);
+                const uint64_t dbh = sdesc_sw128(smem_u32(gb), 16, 2048), dbl = dadd(dbh, 1024);
+                const uint64_t dsh = dadd(dbh, (kTile / 8) * 2048), dsl = dadd(dsh, 1024);
+                const uint64_t dgt = sdesc_sw128(smem_u32(gb), 1024, 2048);
+                // MN-major [V | 1] of V stage s: step kk is step 0 plus a constant (start + 2048 kk
+                // bytes, LBO - 2048 kk bytes; the stages lie below the ones block)
+                auto dv0 = [&](int s) {
+                    const uint32_t a = smem_u32(vst + s * kTileBytes);
+                    return sdesc_sw128(a, smem_u32(smem + L::kOnes) - a, 1024);
+                };
+                constexpr uint64_t kDvStep = 128ull - (128ull << 16);
+                constexpr uint32_t i64 = idesc_bf16(kTile, 64, false, false), i128 = idesc_bf16(kTile, 128, false, false);
+                constexpr uint32_t i80 = idesc_bf16(kTile, 80, false, false), i80s = idesc_bf16(kTile, 80, false, true),
+                                   i80u = idesc_bf16(kTile, 80, true, true);
+                // five N = 64 products per K step: x2hi a_hi, x2hi a_lo, x2lo a_hi, x b_hi, x b_lo
+                auto scores = [&](uint32_t d, uint32_t x2, uint64_t dx) {
+#pragma unroll
+                    for (int kk = 0; kk < kDR / 16; ++kk) {
+                        const uint32_t o = kk * 32;
+                        umma_bf16_tA(d, x2 + kk * 8, dadd(dc, o), i64, kk > 0 ? 1u : 0u);
+                        umma_bf16_tA(d, x2 + kk * 8, dadd(dc, kCoefMatBytes + o), i64, 1u);
+                        umma_bf16_tA(d, x2 + 32 + kk * 8, dadd(dc, o), i64, 1u);
+                        umma_bf16(d, dadd(dx, o), dadd(dc, 2 * kCoefMatBytes + o), i64, 1u);
+                        umma_bf16(d, dadd(dx, o), dadd(dc, 3 * kCoefMatBytes + o), i64, 1u);
+                    }
+                };
+                auto key_scores = [&](int i) {
+                    if (!wait_or_abort(cfull, i & 1, status, abort_flag)) return false;
+                    if (!wait_or_abort(xk, i & 1, status, abort_flag)) return false;
+                    tc_fence_after();
+                    scores(tmem + kSK, tmem + kX, dk);
+                    umma_commit(sk);
+                    umma_commit(kempty);
+                    return true;
+                };
+                auto query_scores = [&](int i) {
+                    if (!wait_or_abort(xq, i & 1, status, abort_flag)) return false;
+                    tc_fence_after();
+                    scores(tmem + kSQ + 64 * (i & 1), tmem + kX + 64, dq);
+                    umma_commit(sq);
+                    umma_commit(qempty);
+                    return true;
+                };
+                // [num | den] += gQhi S^T_hi + gQhi S^T_lo + gQlo S^T_hi (the prefix memory of chunk j)
+                auto state_read = [&](int j) {
+                    if (!wait_or_abort(sready, j & 1, status, abort_flag)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kKP / 16; ++kk) {
+                        const uint32_t aq = tmem + kSQ + 64 * (j & 1) + kk * 8;
+                        umma_bf16_tA(tmem + kO, aq, dadd(dsh, kk * 32), i80, 1u);
+                        umma_bf16_tA(tmem + kO, aq, dadd(dsl, kk * 32), i80, 1u);
+                        umma_bf16_tA(tmem + kO, aq + 32, dadd(dsh, kk * 32), i80, 1u);
+                    }
+                    umma_commit(of);
+                    return true;
+                };
+                bool ok = key_scores(0) && query_scores(0);
+                for (int i = 0; ok && i < n; ++i) {
+                    const int vs = i & 1;
+                    // U = [gK_hi ; gK_lo]^T [V | 1] into the x^2 columns (the scores have read them)
+                    if (!(ok = wait_or_abort(gk, i & 1, status, abort_flag))) break;
+                    if (!(ok = wait_or_abort(&vfull[vs], (i >> 1) & 1, status, abort_flag))) break;
+                    tc_fence_after();
+                    {
+                        const uint64_t b0 = dv0(vs);
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            umma_bf16(tmem + kU, dadd(dgt, kk * 4096), b0 + kk * kDvStep, i80u, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(uf);
+                    // P = gQhi gKhi^T + gQhi gKlo^T + gQlo gKhi^T
+                    if (!(ok = wait_or_abort(gq, i & 1, status, abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kKP / 16; ++kk) {
+                        const uint32_t aq = tmem + kSQ + 64 * (i & 1) + kk * 8;
+                        umma_bf16_tA(tmem + kP, aq, dadd(dbh, kk * 32), i128, kk > 0 ? 1u : 0u);
+                        umma_bf16_tA(tmem + kP, aq, dadd(dbl, kk * 32), i128, 1u);
+                        umma_bf16_tA(tmem + kP, aq + 32, dadd(dbh, kk * 32), i128, 1u);
+                    }
+                    umma_commit(pf);
+                    // the previous chunk's prefix read (its look-back has had this chunk's key and
+                    // query sides to finish)
+                    if (i > 0 && !(ok = state_read(i - 1))) break;
+                    // [num | den] = P [V | 1] (P hi / lo in place: key block cb = kk / 2 holds hi
+                    // words at 32 cb, lo words at 32 cb + 16); the previous outputs are read
+                    if (!(ok = wait_or_abort(psplit, i & 1, status, abort_flag))) break;
+                    if (i > 0 && !(ok = wait_or_abort(oread, (i - 1) & 1, status, abort_flag))) break;
+                    tc_fence_after();
+                    {
+                        const uint64_t b0 = dv0(vs);
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk) {
+                            const uint32_t ap = tmem + kP + 32 * (kk >> 1) + 8 * (kk & 1);
+                            umma_bf16_tA(tmem + kO, ap, b0 + kk * kDvStep, i80s, kk > 0 ? 1u : 0u);
+                            umma_bf16_tA(tmem + kO, ap + 16, b0 + kk * kDvStep, i80s, 1u);
+                        }
+                    }
+                    umma_commit(&vempty[vs]);
+                    if (i + 1 < n && !(ok = key_scores(i + 1))) break;
+                    if (i + 1 < n && !(ok = query_scores(i + 1))) break;
+                }
+                if (ok) ok = state_read(n - 1);
+                // every MMA issued has completed before the CTA frees its tensor memory
+                umma_commit(fin);
+                mbar_wait(fin, 0);
+            }
+        } else if (warp < 6) {
+            // ---------------- key group
+            const int row = epi_row(warp, lane), kt = tid - 64;
+            const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            if (wait_or_abort(kfull, 0, status, abort_flag)) {
+                x2_row(kst, row, tmem + lb + kX);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xk);
+            }
+            for (int i = 0; i < n && !aborted(abort_flag); ++i) {
+                const int g = c + i * Gn, t = g / BH, bh = g % BH;
+                // key softmax -> Gamma^K (normalised, zero past N) into the [Gamma^K ; S^T] buffer
+                if (!wait_or_abort(sk, i & 1, status, abort_flag)) break;
+                if (!wait_or_abort(cfull, i & 1, status, abort_flag)) break;
+                tc_fence_after();
+                scan_softmax_row(tmem + lb + kSK, cvec, 1, 0u, gb, row, t * kTile + row < N);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(gk);
+                    mbar_arrive(cfree);
+                }
+                // masked intra-chunk affinity, key blocks 2 and 3 -> P hi | lo (in place); U was
+                // issued before P, so its result is ready by now too
+                if (!wait_or_abort(pf, i & 1, status, abort_flag)) break;
+                tc_fence_after();
+                split_p_blocks(tmem + lb + kP, 2, row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(psplit);
+                // the increment U: into Agg (once the scan group has read the previous one) and the
+                // chunk's published slot
+                if (!wait_or_abort(uf, i & 1, status, abort_flag)) break;
+                if (i > 0 && !wait_or_abort(aggfree, (i - 1) & 1, status, abort_flag)) break;
+                tc_fence_after();
+                scan_take_increment(tmem + lb + kU, Agg, G.slot(bh, t, 0), row, uread, lane);
+                // every thread's stores precede the barrier; thread 0's fence after it makes them
+                // visible device-wide (cumulatively) before the flag
+                named_sync(1, 128);
+                if (kt == 0) {
+                    __threadfence();
+                    st_release_u32(G.flag(bh, t), ((uint32_t)(t + 1) << 2) | kAggBit);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aggready);
+            }
+        } else if (warp >= 10) {
+            // ---------------- scan group: prefix memory before each chunk -> S, then its
+            // bf16 hi / lo operand (S^T rows)
+            const int st = tid - 320;
+            for (int i = 0; i < n && !aborted(abort_flag); ++i) {
+                const int g = c + i * Gn, t = g / BH, bh = g % BH;
+                if (!wait_or_abort(aggready, i & 1, status, abort_flag)) break;
+                const unsigned e = scan_lookback(G, bh, t, ntiles, Agg, S, st, abort_flag, err_word, io, 3);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aggfree);  // Agg has been read
+                if (e) {
+                    note_timeout(status, abort_flag);
+                    break;
+                }
+                // the previous chunk's state read has read its operand rows
+                if (i > 0 && !wait_or_abort(of, (i - 1) & 1, status, abort_flag)) break;
+                named_sync(3, 128);
+                state_operand(gb, S, st);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready);
+            }
+        } else {
+            // ---------------- query group
+            const int row = epi_row(warp, lane);
+            const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            uint8_t *stage = stg + (warp & 3) * 8192;
+            float rq_prev = 0.f;
+            int t_prev = 0, bh_prev = 0, n_out = 0;
+            // outputs of chunk j: O = num / (den + eps r), staged and stored by TMA
+            auto scan_output = [&](uint32_t o_taddr, float r, int tj, int bhj) {
+                if (!wait_or_abort(of, n_out & 1, status, abort_flag)) return false;
+                ++n_out;
+                tc_fence_after();
+                stage_output_row(o_taddr, r, eps, stage, lane, o_bf16, oread);
+                __syncwarp();
+                if (lane == 0) {
+                    const int row0 = tj * kTile + 32 * (warp & 3);
+                    tma_store_3d(&tmO, stage, 0, row0, bhj);
+                    if (!o_bf16) tma_store_3d(&tmO, stage + 4096, 32, row0, bhj);
+                    bulk_commit();
+                }
+                return true;
+            };
+            if (wait_or_abort(qfull, 0, status, abort_flag)) {
+                x2_row(qst, row, tmem + lb + kX + 64);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xq);
+            }
+            for (int i = 0; i < n && !aborted(abort_flag); ++i) {
+                const int g = c + i * Gn, t = g / BH, bh = g % BH;
+                // query softmax -> Gamma^Q hi | lo (un-normalised) over the score columns
+                if (!wait_or_abort(sq, i & 1, status, abort_flag)) break;
+                if (!wait_or_abort(cfull, i & 1, status, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t sqc = tmem + lb + kSQ + 64 * (i & 1);
+                const float rq = scan_softmax_row(sqc, cvec, 0, sqc, nullptr, row, 1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(gq);
+                    mbar_arrive(cfree);
+                }
+                // masked intra-chunk affinity, key blocks 0 and 1 -> P hi | lo (in place)
+                if (!wait_or_abort(pf, i & 1, status, abort_flag)) break;
+                tc_fence_after();
+                split_p_blocks(tmem + lb + kP, 0, row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(psplit);
+                // x^2 of the next key and query tiles (their columns are free once the increment
+                // is read out)
+                if (i + 1 < n) {
+                    if (!wait_or_abort(uread, i & 1, status, abort_flag)) break;
+                    if (!wait_or_abort(kfull, (i + 1) & 1, status, abort_flag)) break;
+                    tc_fence_after();
+                    x2_row(kst, row, tmem + lb + kX);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xk);
+                    if (!wait_or_abort(qfull, (i + 1) & 1, status, abort_flag)) break;
+                    x2_row(qst, row, tmem + lb + kX + 64);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xq);
+                }
+                // outputs of the previous chunk (its state read follows this chunk's P)
+                if (i > 0 && !scan_output(tmem + lb + kO, rq_prev, t_prev, bh_prev)) break;
+                rq_prev = rq;
+                t_prev = t;
+                bh_prev = bh;
+            }
+            if (!aborted(abort_flag)) scan_output(tmem + lb + kO, rq_prev, t_prev, bh_prev);
+            if (lane == 0) bulk_wait_read0();  // staging reusable; kernel completion publishes the stores
+        }
+    }
+    tc_fence_before();
+    cta_sync();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1918,6 +2603,65 @@ TcLayout2 tc_layout2(const Problem &p, int splits, int causal) {
     return L;
 }
 
+// Workspace of the single-pass causal scan: status | per-block parameter-error
+// words | per-head coefficient images | look-back flags [BH][R] | published
+// memories [BH][R][2][64][kW] fp32 (R = chunks per head).  coef_prep_tc_kernel clears the
+// status word and the flags; every other region is written before it is read.
+struct ScanLayout {
+    int R = 0, grid = 0;
+    size_t head_err = 0, coef = 0, flags = 0, ring = 0, total = 0;
+};
+
+ScanLayout scan_layout(const Problem &p, int splits) {
+    ScanLayout L;
+    const int ntiles = (p.N + kTile - 1) / kTile;
+    // one slot per chunk: a slot is written once per call, so no reader can see
+    // it change under it (a ring of fewer slots is only safe while no chunk lags
+    // the chunks that reuse its slot, which nothing guarantees)
+    L.R = ntiles;
+    const long long total = (long long)p.BH() * ntiles;
+    long long g = splits > 0 ? splits : num_sms();
+    L.grid = (int)(g < total ? g : total);
+    size_t off = kStatusBytes;
+    L.head_err = off;
+    off = align256(off + sizeof(unsigned) * (size_t)p.H * kPrepBlocks);
+    L.coef = off;
+    off = align256(off + kCoefStride * p.H);
+    L.flags = off;
+    off = align256(off + sizeof(unsigned) * (size_t)p.BH() * L.R);
+    L.ring = off;
+    off = align256(off + sizeof(float) * (size_t)p.BH() * L.R * 2 * kKP * kW);
+    L.total = off;
+    return L;
+}
+
+// The causal call on the single-pass kernel: coefficient prep (which also
+// clears the look-back flags), then the scan.
+// io.carry_vt: the prefix starts from the caller's memory; io.out_vt: the
+// prefix after the last position is written there.
+cudaError_t run_scan(const Problem &p, const ScanLayout &L, uint8_t *ws, cudaStream_t s, StageClock &clk,
+                     CombineIO io = CombineIO{nullptr, nullptr, nullptr, nullptr, 0}) {
+    unsigned *status = reinterpret_cast<unsigned *>(ws);
+    unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
+    unsigned *flags = reinterpret_cast<unsigned *>(ws + L.flags);
+    uint8_t *coef = ws + L.coef;
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map(&tq, p.Q, p.BH(), p.N, p.d_r) || !make_map(&tk, p.Kx, p.BH(), p.N, p.d_r) ||
+        !make_map(&tv, p.V, p.BH(), p.N, 64) || !make_out_map(&to, p.O, p.BH(), p.N, p.o_bf16))
+        return cudaErrorInvalidValue;
+    clk.mark();
+    GMA_TRY(launch_pdl(coef_prep_tc_kernel, dim3(kPrepBlocks, p.H), dim3(128), 0, s, p.mu, p.sigma2, p.log_pi, p.K,
+                       p.d_r, coef, status, head_err, flags, p.BH() * L.R));
+    clk.mark();
+    GMA_TRY(set_smem(tc_scan_kernel, ScanSmem::kAlloc));
+    const ScanGlobal G{flags, reinterpret_cast<float *>(ws + L.ring), L.R};
+    GMA_TRY(launch_pdl(tc_scan_kernel, dim3(L.grid), dim3(kThreadsScan), ScanSmem::kAlloc, s, tq, tk, tv, to,
+                       static_cast<const uint8_t *>(coef), static_cast<const unsigned *>(head_err), G, p.H, p.BH(),
+                       p.N, p.eps, p.o_bf16 ? 1 : 0, p.test_stall ? 1 : 0, io, status));
+    clk.mark();
+    return cudaSuccess;
+}
+
 // Read operand image of a caller's memory [Vt | Z] (fp32) for each head, the
 // same bf16 hi | lo layout the combine builds: row n < 64 holds Vt[:, n], row 64
 // Z, rows 65 .. 79 zero; column k of every row is component k (zero past K).
@@ -2029,6 +2773,8 @@ const char *const kTcStages[3][8] = {
     {"prep", "tc_aggregate", "tc_causal", nullptr},
 };
 
+const char *const kTcScanStages[8] = {"prep", "tc_scan", nullptr};
+
 const char *const kAuxTcStages[5][8] = {
     {"prep", "tc_write", nullptr},
     {nullptr},
@@ -2045,6 +2791,10 @@ bool tc_supported(const Problem &p, int causal) {
 
 size_t tc_workspace(const Problem &p, int causal, int splits) { return tc_layout2(p, splits, causal).total; }
 
+size_t tc_carry_workspace(const Problem &p) { return tc_layout2(p, 0, 1).total; }
+
+size_t tc_scan_workspace(const Problem &p, int splits) { return scan_layout(p, splits).total; }
+
 cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
     TcLayout2 L = tc_layout2(p, splits, 0);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -2054,6 +2804,10 @@ cudaError_t tc_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, Sta
 cudaError_t tc_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
     TcLayout2 L = tc_layout2(p, splits, 1);
     return run_causal2(p, L, static_cast<uint8_t *>(ws), s, clk);
+}
+
+cudaError_t tc_causal_1pass(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk) {
+    return run_scan(p, scan_layout(p, splits), static_cast<uint8_t *>(ws), s, clk);
 }
 
 cudaError_t tc_latent_memory(const Problem &p, int splits, float *Vt, float *Z, void *ws, cudaStream_t s,
@@ -2073,6 +2827,12 @@ cudaError_t tc_causal_carry(const Problem &p, int splits, const float *Vt_in, co
                             float *Z_out, void *ws, cudaStream_t s, StageClock &clk) {
     TcLayout2 L = tc_layout2(p, splits, 1);
     return run_causal2(p, L, static_cast<uint8_t *>(ws), s, clk, CombineIO{Vt_in, Z_in, Vt_out, Z_out, p.K});
+}
+
+cudaError_t tc_causal_carry_1pass(const Problem &p, int splits, const float *Vt_in, const float *Z_in,
+                                  float *Vt_out, float *Z_out, void *ws, cudaStream_t s, StageClock &clk) {
+    return run_scan(p, scan_layout(p, splits), static_cast<uint8_t *>(ws), s, clk,
+                    CombineIO{Vt_in, Z_in, Vt_out, Z_out, p.K});
 }
 
 }  // namespace gma

@@ -67,7 +67,17 @@ typedef enum gma_status {
 enum {
     GMA_PATH_AUTO = 0,   /* tensor-core path when the dtype/sizes allow it, else SIMT */
     GMA_PATH_SIMT = 1,   /* fp32 CUDA-core kernels (every supported size, fp32 or bf16 input) */
-    GMA_PATH_TC = 2      /* tcgen05 tensor-core kernels; GMA_ERR_UNSUPPORTED_SHAPE if not eligible */
+    GMA_PATH_TC = 2,     /* tcgen05 tensor-core kernels; GMA_ERR_UNSUPPORTED_SHAPE if not eligible */
+    /* Causal calls (gma_forward_causal, gma_forward_causal_carry): the single-pass
+     * tensor-core kernel, same sizes as GMA_PATH_TC.  Each 128-token chunk computes
+     * its key responsibilities in shared memory next to its query side, so
+     * Gamma^K never goes to device memory and Q_X, K_X, V_X are read once; the
+     * prefix memory before a chunk is the fixed-order sum of the published
+     * memories of earlier chunks (bitwise reproducible).  GMA_PATH_TC's two
+     * kernels instead store Gamma^K between an aggregation pass and the chunk
+     * scan; they are the faster of the two on GB300 (measured) and the
+     * default.  Other calls: as GMA_PATH_TC. */
+    GMA_PATH_TC_SINGLE_PASS = 3
 };
 
 /* Optional knobs; pass NULL for all defaults.  Zero in a field = default. */

@@ -158,3 +158,18 @@ def test_chunk_option(lib):
     need = ws(1, 2, 0)
     for chunk, code in ((256, 2), (64, 2), (-1, 1)):
         assert _fwd(lib, "gma_forward_causal", opt=_native.Options(2, chunk, 0, 0), wsb=need) == code
+
+
+def test_single_pass_path_selection(lib):
+    """GMA_PATH_TC_SINGLE_PASS: the single-pass kernel for causal calls on the
+    tensor-core sizes, the tensor-core path for bidirectional calls, rejected
+    elsewhere; two stages (prep, scan)."""
+    o = ctypes.byref(_native.Options(3, 0, 0, 0))
+    assert lib.gma_selected_path(16384, 64, 64, 64, 1, 1, o) == 3
+    assert lib.gma_selected_path(16384, 64, 64, 64, 1, 0, o) == 2
+    assert lib.gma_selected_path(16384, 128, 128, 128, 1, 1, o) == -1
+    assert lib.gma_selected_path(16384, 64, 64, 64, 0, 1, o) == -1    # fp32 inputs
+    assert _native.stage_names(3, 1) == ["prep", "tc_scan"]
+    assert _native.stage_names(3, 8) == ["prep", "tc_scan"]
+    assert _native.stage_names(2, 1) == ["prep", "tc_aggregate", "tc_causal"]
+    assert lib.gma_workspace_size(4, 8, 16384, 64, 64, 64, 1, 1, o) > 0

@@ -91,13 +91,29 @@ def test_responsibilities(dtype):
     assert np.max(np.abs(G - ref)) <= 1e-4
 
 
-@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
-def test_deterministic(causal):
+@pytest.mark.parametrize("causal,path", [(False, gma.PATH_AUTO), (True, gma.PATH_AUTO),
+                                         (True, gma.PATH_TC_SINGLE_PASS)], ids=["bidir", "causal", "causal1pass"])
+def test_deterministic(causal, path):
     case = _case(causal, 700, 64, 64, 64, "bf16")
     d = to_dev(make_inputs(case, seed=8))
-    a = run_gpu(case, d)
-    b = run_gpu(case, d)
+    a = run_gpu(case, d, path=path)
+    b = run_gpu(case, d, path=path)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("shape", [(300, 64, 64, 64), (417, 32, 64, 32), (1, 64, 64, 64), (129, 64, 64, 17)],
+                         ids=lambda s: "N%d_r%d_v%d_K%d" % s)
+@pytest.mark.parametrize("o_bf16", [False, True], ids=["o32", "o16"])
+def test_causal_single_pass_matches_oracle(shape, o_bf16):
+    """The single-pass causal kernel (key responsibilities kept on chip, block
+    look-back between chunks) against the oracle, ragged tails and padded
+    components, fp32 and bf16 O."""
+    case = _case(True, *shape, "bf16")
+    inp = make_inputs(case, seed=zlib.crc32(case.name.encode()) % 1000 + 7)
+    O = run_gpu(case, to_dev(inp), path=gma.PATH_TC_SINGLE_PASS, o_bf16=o_bf16)
+    ref = oracle_full(case, inp)
+    err = normalised_error_bf16_out(O, ref) if o_bf16 else normalised_error(O, ref)
+    assert err <= TOL["bf16"], f"{case.name}: normalised max error {err:.3e}"
 
 
 @pytest.mark.parametrize("bad", ["zero_var", "neg_var", "nan_mu", "inf_logpi"])
@@ -120,7 +136,8 @@ def test_invalid_parameters_reported(bad):
     run_gpu(case, d2)
 
 
-@pytest.mark.parametrize("path,chunk", [(gma.PATH_SIMT, 64), (gma.PATH_TC, 128)], ids=["simt64", "tc128"])
+@pytest.mark.parametrize("path,chunk", [(gma.PATH_SIMT, 64), (gma.PATH_TC, 128), (gma.PATH_TC_SINGLE_PASS, 128)],
+                         ids=["simt64", "tc128", "tc1pass128"])
 def test_causal_each_supported_chunk(path, chunk):
     """options.chunk set to the kernel family's chunk length (the only one
     each family runs; other lengths are rejected on the host): the same

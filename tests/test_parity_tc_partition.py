@@ -15,14 +15,37 @@ from gpu_helpers import TOL, normalised_error, oracle_full, run_gpu, to_dev
 pytestmark = pytest.mark.gpu
 
 
+PATHS = [pytest.param((False, gma.PATH_TC), id="bidir"), pytest.param((True, gma.PATH_TC), id="causal"),
+         pytest.param((True, gma.PATH_TC_SINGLE_PASS), id="causal1pass")]
+
+
 @pytest.mark.parametrize("splits", [1, 5, 7, 48])
 @pytest.mark.parametrize("d_r,K", [(64, 64), (64, 40), (32, 32)], ids=["r64K64", "r64K40", "r32K32"])
-@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
-def test_tc_partitions(causal, d_r, K, splits):
+@pytest.mark.parametrize("variant", PATHS)
+def test_tc_partitions(variant, d_r, K, splits):
+    """The CTA count forced: job ranges that cross head boundaries (two-kernel
+    paths), or chunks dealt round-robin to few CTAs (single-pass causal)."""
+    causal, path = variant
     # 6 heads x 8 tiles of 128 tokens (the last one ragged: 1000 = 7 x 128 + 104)
-    case = Case(f"tcpart_{int(causal)}_{d_r}_{K}_{splits}", causal, 2, 3, 1000, d_r, 64, K, "bf16")
-    assert gma.selected_path(case.N, d_r, 64, K, "bf16", int(causal)) == gma.PATH_TC
+    case = Case(f"tcpart_{int(causal)}_{path}_{d_r}_{K}_{splits}", causal, 2, 3, 1000, d_r, 64, K, "bf16")
+    assert gma.selected_path(case.N, d_r, 64, K, "bf16", int(causal), path=path) == path
     inp = make_inputs(case, seed=zlib.crc32(case.name.encode()) % 1000)
-    O = run_gpu(case, to_dev(inp), splits=splits)
+    O = run_gpu(case, to_dev(inp), splits=splits, path=path)
     err = normalised_error(O, oracle_full(case, inp))
     assert err <= TOL["bf16"], f"{case.name}: normalised max error {err:.3e}"
+
+
+@pytest.mark.parametrize("splits", [2, 3, 13, 0])
+def test_tc_single_pass_long_heads(splits):
+    """Single-pass causal kernel on heads of 40 chunks (the last one ragged):
+    the block look-back chains many blocks, with 2 to 120 CTAs taking the
+    chunks in turn (120: every chunk of every head in flight at once); bitwise
+    reproducible from call to call."""
+    case = Case(f"tclong_{splits}", True, 1, 3, 39 * 128 + 77, 64, 64, 64, "bf16")
+    inp = make_inputs(case, seed=31 + splits)
+    d = to_dev(inp)
+    O = run_gpu(case, d, splits=splits, path=gma.PATH_TC_SINGLE_PASS)
+    err = normalised_error(O, oracle_full(case, inp))
+    assert err <= TOL["bf16"], f"{case.name}: normalised max error {err:.3e}"
+    O2 = run_gpu(case, d, splits=splits, path=gma.PATH_TC_SINGLE_PASS)
+    assert (O == O2).all()

@@ -93,14 +93,15 @@ def test_tc_read_memory_matches_oracle(shape):
     assert normalised_error_bf16_out(Ob, ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("TC", [gma.PATH_TC, gma.PATH_TC_SINGLE_PASS], ids=["tc", "tc1pass"])
 @pytest.mark.parametrize("shape", SHAPES, ids=IDS)
-def test_tc_causal_carry_continues_a_prefix(shape):
+def test_tc_causal_carry_continues_a_prefix(shape, TC):
     """The first N0 positions from an empty prefix, the rest from the returned
-    state, both on the tensor cores: the two blocks equal the oracle's causal
-    rows, the final state the oracle's latent memory."""
+    state, both on the tensor cores (either causal kernel): the two blocks equal
+    the oracle's causal rows, the final state the oracle's latent memory."""
     import oracle
     case = _case(shape, True)
-    assert gma.selected_path(case.N, case.d_r, case.d_v, case.K, "bf16", 1) == TC
+    assert gma.selected_path(case.N, case.d_r, case.d_v, case.K, "bf16", 1, path=TC) == TC
     inp = make_inputs(case, seed=zlib.crc32(case.name.encode()) % 1000 + 1)
     d = to_dev(inp)
     N = shape[2]

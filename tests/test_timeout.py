@@ -20,15 +20,16 @@ GMA_ERR_TIMEOUT = 5
 vp = ctypes.c_void_p
 
 
-@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
-def test_forced_timeout_reports_status_and_recovers(causal):
+@pytest.mark.parametrize("causal,path", [(False, gma.PATH_TC), (True, gma.PATH_TC), (True, gma.PATH_TC_SINGLE_PASS)],
+                         ids=["bidir", "causal", "causal1pass"])
+def test_forced_timeout_reports_status_and_recovers(causal, path):
     lib = _native.load()
     case = Case("stall", causal, 1, 2, 512, 64, 64, 64, "bf16")
     inp = make_inputs(case, seed=21)
     d = to_dev(inp)
-    assert gma.selected_path(case.N, 64, 64, 64, "bf16", int(causal)) == gma.PATH_TC
-    opt = _native.options(sync_status=True, test_stall=True)
-    ws_bytes = gma.workspace_size(case.B, case.H, case.N, 64, 64, 64, "bf16", int(causal))
+    assert gma.selected_path(case.N, 64, 64, 64, "bf16", int(causal), path=path) == path
+    opt = _native.options(path=path, sync_status=True, test_stall=True)
+    ws_bytes = gma.workspace_size(case.B, case.H, case.N, 64, 64, 64, "bf16", int(causal), path=path)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     O = torch.empty(case.B, case.H, case.N, 64, dtype=torch.float32, device="cuda")
     fn = lib.gma_forward_causal if causal else lib.gma_forward_bidir
@@ -39,7 +40,7 @@ def test_forced_timeout_reports_status_and_recovers(causal):
     assert st == GMA_ERR_TIMEOUT, _native.status_string(st)
     torch.cuda.synchronize()  # no sticky CUDA error
     # the stream still works: a normal call right after matches the oracle
-    O2 = run_gpu(case, d)
+    O2 = run_gpu(case, d, path=path)
     assert normalised_error(O2, oracle_full(case, inp)) <= TOL["bf16"]
 
 
