@@ -34,11 +34,12 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 int choose_path(const Problem &p, int causal, const gma_options *opt) {
     int path = opt ? opt->path : GMA_PATH_AUTO;
     if (path == GMA_PATH_SIMT) return GMA_PATH_SIMT;
-    bool tc = causal >= 0 && gma::tc_supported(p, causal);
+    const bool tc64 = causal >= 0 && gma::tc_supported(p, causal);
+    const bool tc = tc64 || (causal >= 0 && gma::tc128_supported(p, causal));
     if (path == GMA_PATH_TC) return tc ? GMA_PATH_TC : -1;
-    // the single-pass kernel is a causal kernel; the bidirectional tensor-core call
-    // already keeps Gamma on chip
-    if (path == GMA_PATH_TC_SINGLE_PASS) return !tc ? -1 : causal == 1 ? GMA_PATH_TC_SINGLE_PASS : GMA_PATH_TC;
+    // the single-pass kernel is a causal kernel of the 64-wide family; the
+    // bidirectional tensor-core call already keeps Gamma on chip
+    if (path == GMA_PATH_TC_SINGLE_PASS) return !tc64 ? -1 : causal == 1 ? GMA_PATH_TC_SINGLE_PASS : GMA_PATH_TC;
     if (path != GMA_PATH_AUTO) return -1;
     return tc ? GMA_PATH_TC : GMA_PATH_SIMT;
 }
@@ -56,7 +57,8 @@ bool chunk_ok(int path, int causal, const gma_options *opt) {
 size_t workspace_for(const Problem &p, int causal, const gma_options *opt, int path) {
     int splits = opt ? opt->splits : 0;
     if (path == GMA_PATH_TC_SINGLE_PASS) return gma::tc_scan_workspace(p, splits);
-    if (path == GMA_PATH_TC) return gma::tc_workspace(p, causal, splits);
+    if (path == GMA_PATH_TC)
+        return gma::tc128_supported(p, causal) ? gma::tc128_workspace(p, splits) : gma::tc_workspace(p, causal, splits);
     return gma::simt_layout(p, causal, splits).total;
 }
 
@@ -139,6 +141,8 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     cudaError_t err;
     if (path == GMA_PATH_TC_SINGLE_PASS)
         err = gma::tc_causal_1pass(p, splits, workspace, s, clk);
+    else if (path == GMA_PATH_TC && gma::tc128_supported(p, causal))
+        err = gma::tc128_causal(p, splits, workspace, s, clk);
     else if (path == GMA_PATH_TC)
         err = causal ? gma::tc_causal(p, splits, workspace, s, clk) : gma::tc_bidir(p, splits, workspace, s, clk);
     else

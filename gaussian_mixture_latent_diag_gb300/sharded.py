@@ -27,17 +27,22 @@ import torch.distributed as dist
 
 
 class CudaOps:
-    """The per-shard steps in libgma.so's kernels: on the tensor cores whenever
-    the unsharded forward would run there (bf16, d_r in {32, 64}, d_v = 64,
-    K <= 64), so a sharded call has the unsharded call's accuracy, else on the
-    CUDA cores."""
+    """The per-shard steps in libgma.so's kernels: on the tensor cores wherever
+    the memory calls have tensor-core kernels (bf16, d_r in {32, 64}, d_v = 64,
+    K <= 64: the sizes of the 64-wide family, where the unsharded forward runs
+    on the tensor cores too, so a sharded call has the unsharded call's
+    accuracy), else on the CUDA cores.  The 128-wide tensor-core kernels serve
+    only the whole-sequence causal forward, so their sizes shard on the CUDA
+    cores."""
 
     @staticmethod
     def _path(X, V, mu, causal=0):
         from . import PATH_SIMT, PATH_TC, selected_path
         dtype = "bf16" if X.dtype == torch.bfloat16 else "f32"
         N, d_r = X.shape[-2:]
-        tc = selected_path(max(N, 1), d_r, V.shape[-1], mu.shape[1], dtype, causal) == PATH_TC
+        # the memory kernels exist wherever the bidirectional forward runs on the
+        # tensor cores (both directions of the 64-wide family have the same sizes)
+        tc = selected_path(max(N, 1), d_r, V.shape[-1], mu.shape[1], dtype, 0) == PATH_TC
         return PATH_TC if tc else PATH_SIMT
 
     def latent_memory(self, K, V, mu, sigma2, log_pi):

@@ -111,9 +111,12 @@ def test_rank_order_combination():
 
 def test_cuda_ops_pick_the_unsharded_kernel_family():
     """sharded.CudaOps runs a shard on the tensor cores exactly where the
-    unsharded forward would (bf16, d_r in {32, 64}, d_v = 64, K <= 64), so a
-    sharded call has the unsharded call's accuracy.  Host logic only: the choice
-    comes from gma_selected_path, which needs no GPU."""
+    memory calls have tensor-core kernels -- the sizes where the unsharded
+    bidirectional forward runs there (bf16, d_r in {32, 64}, d_v = 64, K <= 64),
+    so a sharded call has the unsharded call's accuracy; the 128-wide causal
+    tensor-core kernels have no memory calls, so those sizes shard on the CUDA
+    cores.  Host logic only: the choice comes from gma_selected_path, which
+    needs no GPU."""
     import torch
     import gaussian_mixture_latent_diag_gb300 as gma
     from gaussian_mixture_latent_diag_gb300.sharded import CudaOps
@@ -132,7 +135,9 @@ def test_cuda_ops_pick_the_unsharded_kernel_family():
     assert pick(bf, 64, 32, 64) == gma.PATH_SIMT
     assert pick(bf, 128, 64, 64, causal=1) == gma.PATH_SIMT
     assert pick(bf, 64, 64, 128) == gma.PATH_SIMT
+    assert pick(bf, 128, 128, 128, causal=1) == gma.PATH_SIMT
+    assert gma.selected_path(300, 128, 128, 128, "bf16", 1) == gma.PATH_TC  # the unsharded causal forward
     for dtype, d_r, d_v, K in [(bf, 64, 64, 64), (f32, 16, 32, 8), (bf, 128, 128, 128)]:
         for causal in (0, 1):
-            want = gma.selected_path(300, d_r, d_v, K, "bf16" if dtype == bf else "f32", causal)
+            want = gma.selected_path(300, d_r, d_v, K, "bf16" if dtype == bf else "f32", 0)
             assert pick(dtype, d_r, d_v, K, causal) == want
