@@ -180,41 +180,93 @@ __device__ __noinline__ void x2_row128(const uint8_t *x, int row, uint32_t taddr
 // slab by slab through the coefficient ring: for column half hf and K step kk
 // of it (routing columns 64 hf + 16 kk ..):
 //   a_hi: x2hi a_hi + x2lo a_hi;  a_lo: x2hi a_lo;  b_hi: x b_hi;  b_lo: x b_lo.
-// d: accumulator; ax: x^2 operand in tensor memory (x2hi +0, x2lo +64);
-// xs: shared address of the x tile; ring: slab ring (nslots x 16 KB) whose
-// slab `sc` lands on full[sc % nslots] and is released on empty[sc % nslots].
+// d: accumulator; ax: x^2 operand in tensor memory (x2hi +0, x2lo +64); dx0:
+// descriptor of the x tile's first column half; dring0: descriptor of ring slot
+// 0 (NS slots of 16 KB), slab `sc + s` landing on full[(sc + s) % NS] and
+// released on empty[...].  Unrolled, every operand a base plus a constant: a
+// rolled loop that builds descriptors costs several times the MMA itself.
 // Returns the slab count after the side, or -1 (after recording the timeout)
 // if a slab never arrived.
-__device__ __noinline__ int issue_scores128(uint32_t d, uint32_t ax, uint32_t xs, uint32_t ring, int nslots,
-                                            int sc, uint64_t *full, uint64_t *empty, unsigned *status,
-                                            int *abort_flag) {
+template <int NS>
+__device__ __noinline__ int issue_scores128(uint32_t d, uint32_t ax, uint64_t dx0, uint64_t dring0, int sc,
+                                            uint64_t *full, uint64_t *empty, unsigned *status, int *abort_flag) {
     constexpr uint32_t i128 = idesc_bf16(kT, 128, false, false);
-#pragma unroll 1
-    for (int s = 0; s < kSlabs; ++s, ++sc) {
-        const int slot = sc % nslots, hf = s >> 2, m = s & 3;
-        if (!mbar_wait(&full[slot], (sc / nslots) & 1)) {
+#pragma unroll
+    for (int s = 0; s < kSlabs; ++s) {
+        const int u = sc + s, slot = u % NS;
+        if (!mbar_wait(&full[slot], (u / NS) & 1)) {
             note_timeout(status, abort_flag);
             return -1;
         }
         tc_fence_after();
-        const uint64_t db = sdesc_sw128(ring + slot * kSlab, 16, 1024);
-        const uint64_t dx = sdesc_sw128(xs + hf * kHalf, 16, 1024);
+        const uint64_t db = dadd(dring0, slot * kSlab);
+        const int hf = s >> 2, m = s & 3;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = 4 * hf + k4;
-            const uint64_t b = dadd(db, k4 * 32);
+            const uint64_t bb = dadd(db, k4 * 32);
             if (m == 0) {
-                umma_bf16_tA(d, ax + kk * 8, b, i128, (s > 0 || k4 > 0) ? 1u : 0u);
-                umma_bf16_tA(d, ax + 64 + kk * 8, b, i128, 1u);
+                umma_bf16_tA(d, ax + kk * 8, bb, i128, (s > 0 || k4 > 0) ? 1u : 0u);
+                umma_bf16_tA(d, ax + 64 + kk * 8, bb, i128, 1u);
             } else if (m == 1) {
-                umma_bf16_tA(d, ax + kk * 8, b, i128, 1u);
+                umma_bf16_tA(d, ax + kk * 8, bb, i128, 1u);
             } else {
-                umma_bf16(d, dadd(dx, k4 * 32), b, i128, 1u);
+                umma_bf16(d, dadd(dx0, hf * kHalf + k4 * 32), bb, i128, 1u);
             }
         }
         umma_commit(&empty[slot]);
     }
-    return sc;
+    return sc + kSlabs;
+}
+
+// The other MMA batches of a chunk, out of line so that the compiler keeps
+// their 16-24 descriptors as a base plus constants instead of hoisting them all
+// out of the chunk loop (and spilling them).  All have M = N = 128.
+// num = Gamma^Q S: A = Gamma^Q hi | lo in tensor memory (aq0: hi, +64: lo), B =
+// the state operand (dS: hi, MN-major; lo 32 KB further); hi.hi, hi.lo, lo.hi.
+__device__ __noinline__ void issue_num128(uint32_t d, uint32_t aq0, uint64_t dS) {
+    constexpr uint32_t ikm = idesc_bf16(kT, 128, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kKC / 16; ++kk) {
+        const uint64_t bs = dadd(dS, kk * 2048);
+        umma_bf16_tA(d, aq0 + kk * 8, bs, ikm, kk > 0 ? 1u : 0u);
+        umma_bf16_tA(d, aq0 + kk * 8, dadd(bs, 2 * kHalf), ikm, 1u);
+        umma_bf16_tA(d, aq0 + 64 + kk * 8, bs, ikm, 1u);
+    }
+}
+// U = Gamma^Q Gamma^K^T: B = Gamma^K (dG: hi, K-major rows = keys; lo 1 KB further).
+__device__ __noinline__ void issue_u128(uint32_t d, uint32_t aq0, uint64_t dG) {
+    constexpr uint32_t ikk = idesc_bf16(kT, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kKC / 16; ++kk) {
+        const uint64_t bg = dadd(dG, (kk >> 2) * 2048 + (kk & 3) * 32);
+        umma_bf16_tA(d, aq0 + kk * 8, bg, ikk, kk > 0 ? 1u : 0u);
+        umma_bf16_tA(d, aq0 + kk * 8, dadd(bg, 1024), ikk, 1u);
+        umma_bf16_tA(d, aq0 + 64 + kk * 8, bg, ikk, 1u);
+    }
+}
+// S (+)= Gamma^K^T V: A = Gamma^K^T (dGT: hi, MN-major; lo 1 KB further), B = V
+// (dV, MN-major); `acc` = 0 starts the sum.
+__device__ __noinline__ void issue_supd128(uint32_t d, uint64_t dGT, uint64_t dV, uint32_t acc) {
+    constexpr uint32_t imm = idesc_bf16(kT, 128, true, true);
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk) {
+        const uint64_t b = dadd(dV, kk * 2048), a = dadd(dGT, kk * 2 * kGroupB);
+        umma_bf16(d, a, b, imm, (acc || kk > 0) ? 1u : 0u);
+        umma_bf16(d, dadd(a, 1024), b, imm, 1u);
+    }
+}
+// num += P V: A = P hi / lo in place in the U columns (key block cb = kk / 2: hi
+// words at 32 cb, lo words at 32 cb + 16), B = V (dV, MN-major).
+__device__ __noinline__ void issue_pv128(uint32_t d, uint32_t ap0, uint64_t dV) {
+    constexpr uint32_t ikm = idesc_bf16(kT, 128, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk) {
+        const uint64_t b = dadd(dV, kk * 2048);
+        const uint32_t ap = ap0 + 32 * (kk >> 1) + 8 * (kk & 1);
+        umma_bf16_tA(d, ap, b, ikm, 1u);
+        umma_bf16_tA(d, ap + 16, b, ikm, 1u);
+    }
 }
 
 // Score row -> e_k = 2^(s_k + c_k - max) in registers; returns the row sum.
@@ -403,7 +455,6 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
     cta_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t iupd = idesc_bf16(kT, 128, true, true);
 
     int rbase = 0, njob = 0, scount = 0;
     int carm = -1;  // last job whose c vector copy was armed (thread 0)
@@ -475,6 +526,9 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
             if (lane == 0) {
                 int sc = scount;
                 bool ok = true;
+                const uint64_t dk0 = sdesc_sw128(smem_u32(kst), 16, 1024), dring0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+                const uint64_t dgt = sdesc_sw128(smem_u32(gbuf), 2048, kGroupB);  // Gamma^K^T hi, MN-major A
+                const uint64_t dv = sdesc_sw128(smem_u32(vst), kHalf, 1024);       // V, MN-major B
                 // scores(i + 1) go before the state MMAs of tile i: the epilogue frees the
                 // score accumulator before it runs tile i's softmax
                 auto scores = [&](int i) {
@@ -483,8 +537,8 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                     if (!wait_or_abort(&kfull[r % KS], (r / KS) & 1, status, abort_flag)) return false;
                     if (r > 0 && !wait_or_abort(sfree, (r - 1) & 1, status, abort_flag)) return false;
                     tc_fence_after();
-                    sc = issue_scores128(tmem + kSC, tmem + kX0 + 128 * (r & 1), smem_u32(kst + (r % KS) * kTileB),
-                                         smem_u32(ring), CS, sc, cffull, cfempty, status, abort_flag);
+                    sc = issue_scores128<CS>(tmem + kSC, tmem + kX0 + 128 * (r & 1), dadd(dk0, (r % KS) * kTileB),
+                                             dring0, sc, cffull, cfempty, status, abort_flag);
                     if (sc < 0) return false;
                     umma_commit(sfull);
                     umma_commit(&kempty[r % KS]);
@@ -497,14 +551,7 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                     if (!(ok = wait_or_abort(gready, r & 1, status, abort_flag))) break;
                     if (!(ok = wait_or_abort(vfull, r & 1, status, abort_flag))) break;
                     tc_fence_after();
-                    const uint32_t gs = smem_u32(gbuf), vs = smem_u32(vst);
-#pragma unroll 1
-                    for (int kk = 0; kk < kT / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(vs + kk * 2048, kHalf, 1024);
-                        const uint64_t a = sdesc_sw128(gs + kk * 2 * kGroupB, 2048, kGroupB);
-                        umma_bf16(tmem + kSA, a, b, iupd, (i > 0 || kk > 0) ? 1u : 0u);
-                        umma_bf16(tmem + kSA, dadd(a, 1024), b, iupd, 1u);
-                    }
+                    issue_supd128(tmem + kSA, dgt, dv, i > 0 ? 1u : 0u);
                     umma_commit(wdone);
                     umma_commit(vempty);
                 }
@@ -626,6 +673,10 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
 // the job's prefix; 2..5 query group (x^2 of Q, query softmax -> Gamma^Q, P
 // split of key blocks 0 and 1, outputs); 6..9 key group (x^2 of K, key softmax
 // -> Gamma^K, P split of key blocks 2 and 3, state operand).
+//
+// The K tile buffer doubles as the output staging: the query warps stage and
+// store a chunk's O there once its MMAs are done, and the next key tile loads
+// after that.
 //
 // TMEM (512 columns):
 //   [0, 128)    X: x^2 of Q (hi | lo), then x^2 of K, then [num] (N = 128)
@@ -801,43 +852,73 @@ __device__ __noinline__ bool init_state128(uint8_t *R, int k, uint32_t s_taddr, 
     return true;
 }
 
-// Output row i: O = num / den from the accumulator, straight to global memory
-// (rows past N: loaded, not stored -- every lane of the warp takes part in the
-// tensor-memory loads, which are warp-collective).
-__device__ __noinline__ void output_row128(uint32_t o_taddr, float den, void *O, size_t row_off, int o_bf16,
-                                           int valid) {
-    const float inv = 1.0f / den;
+// Outputs of one chunk's query rows, O = num / den, by each query warp for its
+// 32 rows: staged in the warp's 8 KB slice of `stage` and written by TMA stores
+// (which clip rows past N): fp32 O in two rounds of 64 columns (two boxes of 32
+// rows x 32 columns each, 128-byte swizzle), bf16 O in one round (two boxes of
+// 32 rows x 64 columns).  Lane 0 issues the stores and waits until they have
+// read the staging slice.
+__device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t *stage, int lane, int o_bf16,
+                                            const CUtensorMap *tmO, int row0, int bh) {
+    const int sw = lane & 7;
+    if (o_bf16) {
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        uint32_t v[32];
-        tmem_ld32(o_taddr + 32 * q, v);
-        tmem_wait_ld();
-        if (!valid) continue;
-        if (o_bf16) {
-            uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(O) + row_off + 32 * q);
+        for (int q = 0; q < 4; ++q) {
+            uint32_t v[32];
+            tmem_ld32(o_taddr + 32 * q, v);
+            tmem_wait_ld();
+            uint8_t *rp = stage + (q >> 1) * 4096 + lane * 128;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 uint32_t w[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z)
                     w[z] = pack_bf2(__uint_as_float(v[8 * u + 2 * z]) * inv, __uint_as_float(v[8 * u + 2 * z + 1]) * inv);
-                o4[u] = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(rp + (((4 * (q & 1) + u) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-        } else {
-            float4 *o4 = reinterpret_cast<float4 *>(static_cast<float *>(O) + row_off + 32 * q);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                o4[u] = make_float4(__uint_as_float(v[4 * u]) * inv, __uint_as_float(v[4 * u + 1]) * inv,
-                                    __uint_as_float(v[4 * u + 2]) * inv, __uint_as_float(v[4 * u + 3]) * inv);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(tmO, stage, 0, row0, bh);
+            tma_store_3d(tmO, stage + 4096, 64, row0, bh);
+            bulk_commit();
+            bulk_wait_read0();
+        }
+        __syncwarp();
+        return;
+    }
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+        for (int b = 0; b < 2; ++b) {
+            uint32_t v[32];
+            tmem_ld32(o_taddr + 64 * h + 32 * b, v);
+            tmem_wait_ld();
+            uint8_t *rp = stage + b * 4096 + lane * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4 *>(rp + ((c ^ sw) << 4)) =
+                    make_float4(__uint_as_float(v[4 * c]) * inv, __uint_as_float(v[4 * c + 1]) * inv,
+                                __uint_as_float(v[4 * c + 2]) * inv, __uint_as_float(v[4 * c + 3]) * inv);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(tmO, stage, 64 * h, row0, bh);
+            tma_store_3d(tmO, stage + 4096, 64 * h + 32, row0, bh);
+            bulk_commit();
+            bulk_wait_read0();  // the slice is read before the next round overwrites it
+        }
+        __syncwarp();
     }
 }
 
 __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-    const __grid_constant__ CUtensorMap tmV, const uint8_t *__restrict__ coef_img, const float *__restrict__ part,
-    const float *__restrict__ ztile, void *__restrict__ O, int H, int N, Part128 P, float eps, int o_bf16,
-    unsigned *status) {
+    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+    const uint8_t *__restrict__ coef_img, const float *__restrict__ part, const float *__restrict__ ztile, int H,
+    int N, Part128 P, float eps, int o_bf16, unsigned *status) {
     using L = Causal128Smem;
     constexpr int CS = L::kCS;
     constexpr int kX = 0, kGQ = 128, kKU = 256, kSA = 384, kTmemCols = 512;
@@ -867,6 +948,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     }
     if (tid == 32) {
         for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+        mbar_init(kempty, 4);  // the K buffer is freed by the query warps once their outputs are out
         for (int i = 0; i < CS; ++i) {
             mbar_init(&cffull[i], 1);
             mbar_init(&cfempty[i], 1);
@@ -877,7 +959,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
         mbar_init(cfull, 1); mbar_init(xfull, 1); mbar_init(pread, 4);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     cta_sync();
@@ -952,72 +1034,49 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
         } else if (warp == 1) {
             if (lane == 0) {
                 int sc = scount;
-                const uint32_t qs = smem_u32(qst), ks = smem_u32(kst), vs = smem_u32(vst), rs = smem_u32(R);
-                const uint32_t rg = smem_u32(ring);
-                constexpr uint32_t ikk = idesc_bf16(kT, 128, false, false);   // A tmem, B K-major
-                constexpr uint32_t ikm = idesc_bf16(kT, 128, false, true);    // A tmem, B MN-major
-                constexpr uint32_t imm = idesc_bf16(kT, 128, true, true);     // A, B MN-major (smem)
+                // base descriptors; every MMA below adds a constant to one of them
+                const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024), dk0 = sdesc_sw128(smem_u32(kst), 16, 1024);
+                const uint64_t dring0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+                const uint64_t dS = sdesc_sw128(smem_u32(R), kHalf, 1024);     // state operand hi, MN-major B
+                const uint64_t dG = sdesc_sw128(smem_u32(R), 16, kGroupB);      // Gamma^K hi, K-major B
+                const uint64_t dGT = sdesc_sw128(smem_u32(R), 2048, kGroupB);   // Gamma^K^T hi, MN-major A
+                const uint64_t dV = sdesc_sw128(smem_u32(vst), kHalf, 1024);    // V, MN-major B
                 for (int i = 0; i < n; ++i) {
                     const int r = rbase + i, ph = r & 1;
                     // query scores
                     if (!wait_or_abort(xq, ph, status, abort_flag) || !wait_or_abort(qfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    if ((sc = issue_scores128(tmem + kGQ, tmem + kX, qs, rg, CS, sc, cffull, cfempty, status, abort_flag)) < 0)
+                    if ((sc = issue_scores128<CS>(tmem + kGQ, tmem + kX, dq0, dring0, sc, cffull, cfempty, status,
+                                                  abort_flag)) < 0)
                         break;
                     umma_commit(sq);
                     umma_commit(qempty);
                     // key scores
                     if (!wait_or_abort(xk, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    if ((sc = issue_scores128(tmem + kKU, tmem + kX, ks, rg, CS, sc, cffull, cfempty, status, abort_flag)) < 0)
+                    if ((sc = issue_scores128<CS>(tmem + kKU, tmem + kX, dk0, dring0, sc, cffull, cfempty, status,
+                                                  abort_flag)) < 0)
                         break;
                     umma_commit(sk);
-                    umma_commit(kempty);
                     // num = Gamma^Q S (hi.hi, hi.lo, lo.hi)
                     if (!wait_or_abort(gq, ph, status, abort_flag) || !wait_or_abort(sready, ph, status, abort_flag)) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < kKC / 16; ++kk) {
-                        const uint64_t bh_ = sdesc_sw128(rs + kk * 2048, kHalf, 1024);
-                        const uint32_t aq = tmem + kGQ + kk * 8;
-                        umma_bf16_tA(tmem + kX, aq, bh_, ikm, kk > 0 ? 1u : 0u);
-                        umma_bf16_tA(tmem + kX, aq, dadd(bh_, 2 * kHalf), ikm, 1u);
-                        umma_bf16_tA(tmem + kX, aq + 64, bh_, ikm, 1u);
-                    }
+                    issue_num128(tmem + kX, tmem + kGQ, dS);
                     umma_commit(ndone);
                     // U = Gamma^Q Gamma^K^T
                     if (!wait_or_abort(gk, ph, status, abort_flag)) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < kKC / 16; ++kk) {
-                        const uint64_t bg = sdesc_sw128(rs + (kk >> 2) * 2048 + (kk & 3) * 32, 16, kGroupB);
-                        const uint32_t aq = tmem + kGQ + kk * 8;
-                        umma_bf16_tA(tmem + kKU, aq, bg, ikk, kk > 0 ? 1u : 0u);
-                        umma_bf16_tA(tmem + kKU, aq, dadd(bg, 1024), ikk, 1u);
-                        umma_bf16_tA(tmem + kKU, aq + 64, bg, ikk, 1u);
-                    }
+                    issue_u128(tmem + kKU, tmem + kGQ, dG);
                     umma_commit(ufull);
                     // S += Gamma^K^T V (hi, lo)
                     if (!wait_or_abort(vfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < kT / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(vs + kk * 2048, kHalf, 1024);
-                        const uint64_t a = sdesc_sw128(rs + kk * 2 * kGroupB, 2048, kGroupB);
-                        umma_bf16(tmem + kSA, a, b, imm, 1u);
-                        umma_bf16(tmem + kSA, dadd(a, 1024), b, imm, 1u);
-                    }
+                    issue_supd128(tmem + kSA, dGT, dV, 1u);
                     umma_commit(wdone);
                     // num += P V (P hi / lo in place in the U columns)
                     if (!wait_or_abort(pready, ph, status, abort_flag)) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < kT / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(vs + kk * 2048, kHalf, 1024);
-                        const uint32_t ap = tmem + kKU + 32 * (kk >> 1) + 8 * (kk & 1);
-                        umma_bf16_tA(tmem + kX, ap, b, ikm, 1u);
-                        umma_bf16_tA(tmem + kX, ap + 16, b, ikm, 1u);
-                    }
+                    issue_pv128(tmem + kX, tmem + kKU, dV);
                     umma_commit(ofull);
                     umma_commit(vempty);
                 }
@@ -1051,10 +1110,12 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 if (!wait_or_abort(ofull, ph, status, abort_flag)) break;
                 if (!wait_or_abort(pready, ph, status, abort_flag)) break;  // the key group's row sums
                 tc_fence_after();
-                const int tok = (t0 + i) * kT + row;
-                output_row128(tmem + lb + kX, den0 + (rs0 + rsk[row]) + eps * rq, O, ((size_t)bh * N + tok) * kD,
-                              o_bf16, tok < N);
+                // outputs staged in the K tile buffer (the key score MMAs, its last readers,
+                // are complete: ofull), which the next key tile may then reuse
+                output_rows128(tmem + lb + kX, 1.0f / (den0 + (rs0 + rsk[row]) + eps * rq), kst + (warp & 3) * 8192,
+                               lane, o_bf16, &tmO, (t0 + i) * kT + 32 * (warp & 3), bh);
                 tc_fence_before();
+                if (lane == 0) mbar_arrive(kempty);
             }
         } else {
             // ---------------- key group
@@ -1136,6 +1197,22 @@ bool make_map128(CUtensorMap *map, const void *base, int BH, int N) {
     return r == CUDA_SUCCESS;
 }
 
+// O [BH][N][128] (fp32 or bf16) for TMA stores of [32 rows x 128 bytes] boxes,
+// 128-byte swizzle.
+bool make_out_map128(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * es, (cuuint64_t)N * kD * es};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Workspace: status | per-head job counters | prep error words | per-head
 // coefficient images | job memories [ctas][slots][kPartFloats] | key mass of
 // every tile [BH][ntiles][128].  The prep clears the status and the counters;
@@ -1187,9 +1264,9 @@ cudaError_t tc128_causal(const Problem &p, int splits, void *workspace, cudaStre
     uint8_t *coef = ws + L.coef;
     float *part = reinterpret_cast<float *>(ws + L.part);
     float *ztile = reinterpret_cast<float *>(ws + L.ztile);
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map128(&tq, p.Q, p.BH(), p.N) || !make_map128(&tk, p.Kx, p.BH(), p.N) ||
-        !make_map128(&tv, p.V, p.BH(), p.N))
+        !make_map128(&tv, p.V, p.BH(), p.N) || !make_out_map128(&to, p.O, p.BH(), p.N, p.o_bf16))
         return cudaErrorInvalidValue;
     clk.mark();
     GMA_TRY(launch_pdl(tc128_prep_kernel, dim3(kPrepBlocks128, p.H), dim3(128), 0, s, p.mu, p.sigma2, p.log_pi, p.K,
@@ -1202,8 +1279,8 @@ cudaError_t tc128_causal(const Problem &p, int splits, void *workspace, cudaStre
     clk.mark();
     GMA_TRY(set_smem(tc128_causal_kernel, Causal128Smem::kAlloc));
     GMA_TRY(launch_pdl(tc128_causal_kernel, dim3(L.nctas), dim3(kThreadsC128), Causal128Smem::kAlloc, s, tq, tk, tv,
-                       static_cast<const uint8_t *>(coef), static_cast<const float *>(part),
-                       static_cast<const float *>(ztile), p.O, p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status));
+                       to, static_cast<const uint8_t *>(coef), static_cast<const float *>(part),
+                       static_cast<const float *>(ztile), p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status));
     clk.mark();
     return cudaSuccess;
 }
