@@ -182,41 +182,89 @@ __device__ __noinline__ void x2_row128(const uint8_t *x, int row, uint32_t taddr
 //   a_hi: x2hi a_hi + x2lo a_hi;  a_lo: x2hi a_lo;  b_hi: x b_hi;  b_lo: x b_lo.
 // d: accumulator; ax: x^2 operand in tensor memory (x2hi +0, x2lo +64); dx0:
 // descriptor of the x tile's first column half; dring0: descriptor of ring slot
-// 0 (NS slots of 16 KB), slab `sc + s` landing on full[(sc + s) % NS] and
-// released on empty[...].  Unrolled, every operand a base plus a constant: a
-// rolled loop that builds descriptors costs several times the MMA itself.
-// Returns the slab count after the side, or -1 (after recording the timeout)
-// if a slab never arrived.
-template <int NS>
-__device__ __noinline__ int issue_scores128(uint32_t d, uint32_t ax, uint64_t dx0, uint64_t dring0, int sc,
-                                            uint64_t *full, uint64_t *empty, unsigned *status, int *abort_flag) {
+// 0 (NS slots of 16 KB, slab s always in slot s % NS).  Unrolled, every operand
+// a base plus a constant: a rolled loop that builds descriptors costs several
+// times the MMA itself.
+//
+// Slab schedule (SlabOrder): the sides of a job take the eight slabs in
+// alternating order, forward then backward, so a side begins with the NS slabs
+// the previous side ended with, still in the ring, and loads only the other
+// 8 - NS (the first side of a job loads all 8).  full[slot] completes once per
+// load (bit `slot` of *fpar is the parity of the next one), empty[slot] is
+// committed after a load's last use: at once for slabs that the next side does
+// not reuse, after the next side for the last NS slabs of a side.  Returns
+// false (after recording the timeout) if a slab never arrived.
+struct SlabOrder {
+    int first, last;  // the side is the first / last of its job
+};
+template <int NS, bool FWD>
+__device__ __noinline__ bool issue_scores128(uint32_t d, uint32_t ax, uint64_t dx0, uint64_t dring0, uint32_t *fpar,
+                                             SlabOrder so, uint64_t *full, uint64_t *empty, unsigned *status,
+                                             int *abort_flag) {
     constexpr uint32_t i128 = idesc_bf16(kT, 128, false, false);
+    static_assert(NS <= 4, "the first and last NS positions of a side must not overlap");
+    uint32_t fp = *fpar;
 #pragma unroll
-    for (int s = 0; s < kSlabs; ++s) {
-        const int u = sc + s, slot = u % NS;
-        if (!mbar_wait(&full[slot], (u / NS) & 1)) {
-            note_timeout(status, abort_flag);
-            return -1;
+    for (int k = 0; k < kSlabs; ++k) {
+        const int sl = FWD ? k : kSlabs - 1 - k, slot = sl % NS, hf = sl >> 2, m = sl & 3;
+        if (so.first || k >= NS) {  // a fresh load
+            if (!mbar_wait(&full[slot], (fp >> slot) & 1u)) {
+                note_timeout(status, abort_flag);
+                return false;
+            }
+            fp ^= 1u << slot;
         }
         tc_fence_after();
         const uint64_t db = dadd(dring0, slot * kSlab);
-        const int hf = s >> 2, m = s & 3;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = 4 * hf + k4;
             const uint64_t bb = dadd(db, k4 * 32);
+            const uint32_t acc = (k > 0 || k4 > 0) ? 1u : 0u;
             if (m == 0) {
-                umma_bf16_tA(d, ax + kk * 8, bb, i128, (s > 0 || k4 > 0) ? 1u : 0u);
+                umma_bf16_tA(d, ax + kk * 8, bb, i128, acc);
                 umma_bf16_tA(d, ax + 64 + kk * 8, bb, i128, 1u);
             } else if (m == 1) {
-                umma_bf16_tA(d, ax + kk * 8, bb, i128, 1u);
+                umma_bf16_tA(d, ax + kk * 8, bb, i128, acc);
             } else {
-                umma_bf16(d, dadd(dx0, hf * kHalf + k4 * 32), bb, i128, 1u);
+                umma_bf16(d, dadd(dx0, hf * kHalf + k4 * 32), bb, i128, acc);
             }
         }
-        umma_commit(&empty[slot]);
+        if (k < kSlabs - NS || so.last) umma_commit(&empty[slot]);  // this load's last use
     }
-    return sc + kSlabs;
+    *fpar = fp;
+    return true;
+}
+
+// Producer side of the slab schedule: the loads of one side (all 8 for the first
+// side of a job, else the 8 - NS the previous side did not leave in the ring), each
+// once the slot's previous load has had its last use.  Bit `slot` of *lpar is the
+// parity of the slot's load count; bit `slot` of *lmask is set once the slot has
+// been loaded.  Returns false on a timeout.
+template <int NS>
+__device__ __forceinline__ bool load_slabs128(uint8_t *ring, const uint8_t *himg, int fwd, int first, uint32_t *lpar,
+                                              uint32_t *lmask, uint64_t *full, uint64_t *empty, unsigned *status,
+                                              int *abort_flag) {
+    uint32_t lp = *lpar;
+    for (int k = first ? 0 : NS; k < kSlabs; ++k) {
+        const int sl = fwd ? k : kSlabs - 1 - k, slot = sl % NS;
+        if (!wait_or_abort(&empty[slot], ((lp >> slot) & 1u) ^ 1u, status, abort_flag)) return false;
+        lp ^= 1u << slot;
+        *lmask |= 1u << slot;
+        mbar_arrive_expect_tx(&full[slot], kSlab);
+        bulk_load(ring + slot * kSlab, himg + sl * kSlab, kSlab, &full[slot]);
+        *lpar = lp;
+    }
+    return true;
+}
+
+// Waits (bounded) until the last load into every slot that has been loaded has
+// landed, so that no slab copy is in flight when the CTA moves on or leaves.
+template <int NS>
+__device__ __forceinline__ void drain_slabs128(uint32_t lpar, uint32_t lmask, uint64_t *full) {
+#pragma unroll
+    for (int q = 0; q < NS; ++q)
+        if ((lmask >> q) & 1u) mbar_wait(&full[q], ((lpar >> q) & 1u) ^ 1u);
 }
 
 // The other MMA batches of a chunk, out of line so that the compiler keeps
@@ -456,8 +504,11 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    int rbase = 0, njob = 0, scount = 0;
+    int rbase = 0, njob = 0;
     int carm = -1;  // last job whose c vector copy was armed (thread 0)
+    // slab ring state of the producer (load parities) and of the MMA thread (full
+    // parities), per slot; slab_lmask: the slots loaded at least once
+    uint32_t slab_lpar = 0u, slab_fpar = 0u, slab_lmask = 0u;
     for (int g = aborted(abort_flag) ? gend : g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
@@ -508,23 +559,16 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                     if (karm[q] >= 0) mbar_wait(&kfull[q], (karm[q] / KS) & 1);
                 if (varm >= 0) mbar_wait(vfull, varm & 1);
             } else if (lane == 1) {
-                int sc = scount, sarm[CS];
-#pragma unroll
-                for (int q = 0; q < CS; ++q) sarm[q] = -1;
-                for (int i = 0; i < n * kSlabs; ++i, ++sc) {
-                    const int slot = sc % CS;
-                    if (!wait_or_abort(&cfempty[slot], ((sc / CS) & 1) ^ 1, status, abort_flag)) break;
-                    mbar_arrive_expect_tx(&cffull[slot], kSlab);
-                    bulk_load(ring + slot * kSlab, himg + (i % kSlabs) * kSlab, kSlab, &cffull[slot]);
-                    sarm[slot] = sc;
-                }
-#pragma unroll
-                for (int q = 0; q < CS; ++q)
-                    if (sarm[q] >= 0) mbar_wait(&cffull[q], (sarm[q] / CS) & 1);
+                // slabs: one side per key tile, alternating direction
+                for (int i = 0; i < n; ++i)
+                    if (!load_slabs128<CS>(ring, himg, (i & 1) == 0, i == 0, &slab_lpar, &slab_lmask, cffull, cfempty,
+                                           status, abort_flag))
+                        break;
+                // every slab load armed here has landed before the CTA moves on or leaves
+                drain_slabs128<CS>(slab_lpar, slab_lmask, cffull);
             }
         } else if (warp == 1) {
             if (lane == 0) {
-                int sc = scount;
                 bool ok = true;
                 const uint64_t dk0 = sdesc_sw128(smem_u32(kst), 16, 1024), dring0 = sdesc_sw128(smem_u32(ring), 16, 1024);
                 const uint64_t dgt = sdesc_sw128(smem_u32(gbuf), 2048, kGroupB);  // Gamma^K^T hi, MN-major A
@@ -537,9 +581,15 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                     if (!wait_or_abort(&kfull[r % KS], (r / KS) & 1, status, abort_flag)) return false;
                     if (r > 0 && !wait_or_abort(sfree, (r - 1) & 1, status, abort_flag)) return false;
                     tc_fence_after();
-                    sc = issue_scores128<CS>(tmem + kSC, tmem + kX0 + 128 * (r & 1), dadd(dk0, (r % KS) * kTileB),
-                                             dring0, sc, cffull, cfempty, status, abort_flag);
-                    if (sc < 0) return false;
+                    const SlabOrder so{i == 0, i == n - 1};
+                    const uint32_t ax = tmem + kX0 + 128 * (r & 1);
+                    const uint64_t dx = dadd(dk0, (r % KS) * kTileB);
+                    if (!((i & 1) == 0
+                              ? issue_scores128<CS, true>(tmem + kSC, ax, dx, dring0, &slab_fpar, so, cffull, cfempty,
+                                                          status, abort_flag)
+                              : issue_scores128<CS, false>(tmem + kSC, ax, dx, dring0, &slab_fpar, so, cffull, cfempty,
+                                                           status, abort_flag)))
+                        return false;
                     umma_commit(sfull);
                     umma_commit(&kempty[r % KS]);
                     return true;
@@ -655,7 +705,6 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
             }
         }
         rbase += n;
-        scount += n * kSlabs;
         g += n;
         if (aborted(abort_flag)) break;
     }
@@ -670,9 +719,10 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
 // One 128-token chunk at a time per CTA (its tile range, as in the
 // aggregation; the job's carried-in prefix comes from there).  Warps: 0 lane 0
 // Q / K / V tile loads, lane 1 coefficient slabs; 1 lane 0 MMA issue, lane 1
-// the job's prefix; 2..5 query group (x^2 of Q, query softmax -> Gamma^Q, P
-// split of key blocks 0 and 1, outputs); 6..9 key group (x^2 of K, key softmax
-// -> Gamma^K, P split of key blocks 2 and 3, state operand).
+// the job's prefix; 2..5 query group (query softmax -> Gamma^Q, components
+// 64-127 of the key softmax, P split of key blocks 0 and 1, outputs); 6..9 key
+// group (x^2 of Q and K, components 0-63 of the key softmax, P split of key
+// blocks 2 and 3, state operand).
 //
 // The K tile buffer doubles as the output staging: the query warps stage and
 // store a chunk's O there once its MMAs are done, and the next key tile loads
@@ -700,7 +750,7 @@ struct Causal128Smem {
     static constexpr int kZp = kC + 512;                // key mass before the chunk [128] fp32
     static constexpr int kRs = kZp + 512;               // key group's P row sums [128] fp32
     static constexpr int kBars = kRs + 512;
-    static constexpr int kBytes = kBars + 256;
+    static constexpr int kBytes = kBars + 512;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kR % 1024 == 0 && kCf % 1024 == 0, "SW128 alignment");
     static_assert(kAlloc <= 232448, "shared memory budget");
@@ -774,15 +824,79 @@ __device__ __noinline__ float query_row128(uint32_t s_taddr, const float *cvec, 
     return r;
 }
 
-// Key softmax of one row and the normalised Gamma^K row into R, once `freed`
-// (phase `ph`) says the state MMAs have read R.  Returns false on a timeout.
-__device__ __noinline__ bool key_row128(uint32_t s_taddr, const float *cvec, int valid, uint8_t *R, int row,
-                                        uint64_t *freed, uint32_t ph, unsigned *status, int *abort_flag) {
-    float e[kKC];
-    const float r = score_exp128(s_taddr, cvec, e);
+// Key softmax of half `hf` of one row (components 64 hf .. 64 hf + 63), run by
+// the threads of both warp groups that own the row: the halves' maxima and sums
+// meet in xb ([max | sum][half][128] fp32) through the mbarriers mx and ms (8
+// warps each, phase ph); the row sum is the half-0 sum plus the half-1 sum.
+// The half's normalised Gamma^K goes into R (its 64-component atom of the 4 KB
+// groups) once `freed` says num has read S from there.  Returns false on a
+// timeout.
+__device__ __noinline__ bool key_half128(uint32_t s_taddr, const float *cvec, int hf, int valid, uint8_t *R,
+                                         int row, float *xb, uint64_t *mx, uint64_t *ms, uint64_t *freed,
+                                         uint32_t ph, unsigned *status, int *abort_flag) {
+    float e[64];
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint32_t v[32];
+        tmem_ld32(s_taddr + 64 * hf + 32 * q, v);
+        tmem_wait_ld();
+        const float4 *c4 = reinterpret_cast<const float4 *>(cvec + 64 * hf + 32 * q);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 c = c4[i];
+            const float2 a = f2_add(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                                    make_float2(c.x, c.y));
+            const float2 b = f2_add(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                                    make_float2(c.z, c.w));
+            e[32 * q + 4 * i] = a.x;
+            e[32 * q + 4 * i + 1] = a.y;
+            e[32 * q + 4 * i + 2] = b.x;
+            e[32 * q + 4 * i + 3] = b.y;
+            m = fmaxf(m, fmaxf(fmaxf(a.x, a.y), fmaxf(b.x, b.y)));
+        }
+    }
     tc_fence_before();
+    const int lane = threadIdx.x & 31;
+    xb[hf * kT + row] = m;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(mx);
+    if (!wait_or_abort(mx, ph, status, abort_flag)) return false;
+    const float M = fmaxf(xb[row], xb[kT + row]);
+    const float2 mm = make_float2(M, M);
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 64; k += 4) {
+        const float2 d0 = f2_sub(make_float2(e[k], e[k + 1]), mm), d1 = f2_sub(make_float2(e[k + 2], e[k + 3]), mm);
+        e[k] = ex2(d0.x);
+        e[k + 1] = ex2(d0.y);
+        e[k + 2] = ex2(d1.x);
+        e[k + 3] = ex2(d1.y);
+        s0 = f2_add(s0, make_float2(e[k], e[k + 1]));
+        s1 = f2_add(s1, make_float2(e[k + 2], e[k + 3]));
+    }
+    xb[2 * kT + hf * kT + row] = (s0.x + s0.y) + (s1.x + s1.y);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ms);
+    if (!wait_or_abort(ms, ph, status, abort_flag)) return false;
+    const float sc = valid ? 1.0f / (xb[2 * kT + row] + xb[3 * kT + row]) : 0.0f;
     if (!wait_or_abort(freed, ph, status, abort_flag)) return false;
-    store_gamma128(R, row, e, valid ? 1.0f / r : 0.0f);
+    const float2 s2 = make_float2(sc, sc);
+    uint8_t *rb = R + (row >> 3) * kGroupB + (row & 7) * 128 + hf * 2048;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {  // 8 components per 16-byte chunk
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 g = f2_mul(make_float2(e[8 * w + 2 * q], e[8 * w + 2 * q + 1]), s2);
+            h[q] = pack_bf2(g.x, g.y);
+            const float2 r = f2_sub(g, make_float2(bf_lo(h[q]), bf_hi(h[q])));
+            l[q] = pack_bf2(r.x, r.y);
+        }
+        uint8_t *p = rb + ((w ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(p) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(p + 1024) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
     return true;
 }
 
@@ -856,10 +970,12 @@ __device__ __noinline__ bool init_state128(uint8_t *R, int k, uint32_t s_taddr, 
 // 32 rows: staged in the warp's 8 KB slice of `stage` and written by TMA stores
 // (which clip rows past N): fp32 O in two rounds of 64 columns (two boxes of 32
 // rows x 32 columns each, 128-byte swizzle), bf16 O in one round (two boxes of
-// 32 rows x 64 columns).  Lane 0 issues the stores and waits until they have
-// read the staging slice.
+// 32 rows x 64 columns).  The whole accumulator row is read first (the second
+// fp32 half into registers), and lane 0 arrives on `xfree`, so the columns can
+// take the next chunk's x^2 while the stores go out; lane 0 issues the stores
+// and waits until they have read the staging slice.
 __device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t *stage, int lane, int o_bf16,
-                                            const CUtensorMap *tmO, int row0, int bh) {
+                                            const CUtensorMap *tmO, int row0, int bh, uint64_t *xfree) {
     const int sw = lane & 7;
     if (o_bf16) {
 #pragma unroll 1
@@ -877,9 +993,11 @@ __device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t
                 *reinterpret_cast<uint4 *>(rp + (((4 * (q & 1) + u) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
+        tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+            mbar_arrive(xfree);
             tma_store_3d(tmO, stage, 0, row0, bh);
             tma_store_3d(tmO, stage + 4096, 64, row0, bh);
             bulk_commit();
@@ -888,30 +1006,53 @@ __device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t
         __syncwarp();
         return;
     }
+    // columns 0 .. 63 staged, 64 .. 127 held in registers
 #pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll 1
-        for (int b = 0; b < 2; ++b) {
-            uint32_t v[32];
-            tmem_ld32(o_taddr + 64 * h + 32 * b, v);
-            tmem_wait_ld();
-            uint8_t *rp = stage + b * 4096 + lane * 128;
+    for (int b = 0; b < 2; ++b) {
+        uint32_t v[32];
+        tmem_ld32(o_taddr + 32 * b, v);
+        tmem_wait_ld();
+        uint8_t *rp = stage + b * 4096 + lane * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<float4 *>(rp + ((c ^ sw) << 4)) =
-                    make_float4(__uint_as_float(v[4 * c]) * inv, __uint_as_float(v[4 * c + 1]) * inv,
-                                __uint_as_float(v[4 * c + 2]) * inv, __uint_as_float(v[4 * c + 3]) * inv);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_3d(tmO, stage, 64 * h, row0, bh);
-            tma_store_3d(tmO, stage + 4096, 64 * h + 32, row0, bh);
-            bulk_commit();
-            bulk_wait_read0();  // the slice is read before the next round overwrites it
-        }
-        __syncwarp();
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4 *>(rp + ((c ^ sw) << 4)) =
+                make_float4(__uint_as_float(v[4 * c]) * inv, __uint_as_float(v[4 * c + 1]) * inv,
+                            __uint_as_float(v[4 * c + 2]) * inv, __uint_as_float(v[4 * c + 3]) * inv);
     }
+    uint32_t h0[32], h1[32];
+    tmem_ld32(o_taddr + 64, h0);
+    tmem_ld32(o_taddr + 96, h1);
+    tmem_wait_ld();
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        mbar_arrive(xfree);
+        tma_store_3d(tmO, stage, 0, row0, bh);
+        tma_store_3d(tmO, stage + 4096, 32, row0, bh);
+        bulk_commit();
+        bulk_wait_read0();  // the slice is read before the second round overwrites it
+    }
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const uint32_t *v = b ? h1 : h0;
+        uint8_t *rp = stage + b * 4096 + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4 *>(rp + ((c ^ sw) << 4)) =
+                make_float4(__uint_as_float(v[4 * c]) * inv, __uint_as_float(v[4 * c + 1]) * inv,
+                            __uint_as_float(v[4 * c + 2]) * inv, __uint_as_float(v[4 * c + 3]) * inv);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmO, stage, 64, row0, bh);
+        tma_store_3d(tmO, stage + 4096, 96, row0, bh);
+        bulk_commit();
+        bulk_wait_read0();
+    }
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
@@ -932,10 +1073,10 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
              *vempty = bars + 5, *cffull = bars + 6, *cfempty = cffull + CS, *xq = cfempty + CS, *xk = xq + 1,
              *sq = xq + 2, *sk = xq + 3, *gq = xq + 4, *gk = xq + 5, *sready = xq + 6, *ndone = xq + 7,
              *ufull = xq + 8, *wdone = xq + 9, *pready = xq + 10, *ofull = xq + 11, *cfull = xq + 12,
-             *xfull = xq + 13, *pread = xq + 14;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pread + 1);
-    int *abort_flag = reinterpret_cast<int *>(pread + 2);
-    static_assert((6 + 2 * CS + 15) * 8 + 16 <= 256, "barrier area");
+             *xfull = xq + 13, *pread = xq + 14, *kmx = xq + 15, *ksm = xq + 16, *xfree = xq + 17;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfree + 1);
+    int *abort_flag = reinterpret_cast<int *>(xfree + 2);
+    static_assert((6 + 2 * CS + 18) * 8 + 16 <= 512, "barrier area");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -954,9 +1095,10 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             mbar_init(&cfempty[i], 1);
         }
         mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
-        mbar_init(gq, 4); mbar_init(gk, 4); mbar_init(sready, 4); mbar_init(ndone, 1);
+        mbar_init(gq, 4); mbar_init(gk, 8); mbar_init(sready, 4); mbar_init(ndone, 1);
         mbar_init(ufull, 1); mbar_init(wdone, 1); mbar_init(pready, 8); mbar_init(ofull, 1);
         mbar_init(cfull, 1); mbar_init(xfull, 1); mbar_init(pread, 4);
+        mbar_init(kmx, 8); mbar_init(ksm, 8); mbar_init(xfree, 4);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
@@ -969,8 +1111,9 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     if (warp >= 6) pdl_wait();
     const uint32_t tmem = *tmem_slot;
 
-    int rbase = 0, njob = 0, scount = 0;
+    int rbase = 0, njob = 0;
     int barm = -1;  // last job whose c vector and prefix copies were armed
+    uint32_t slab_lpar = 0u, slab_fpar = 0u, slab_lmask = 0u;  // slab ring state (see issue_scores128)
     for (int g = g0; g < gend; ++njob) {
         const int bh = g / P.ntiles, t0 = g % P.ntiles;
         const int n = min(P.ntiles - t0, gend - g);
@@ -1017,23 +1160,15 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 if (ka >= 0) mbar_wait(kfull, ka & 1);
                 if (va >= 0) mbar_wait(vfull, va & 1);
             } else if (lane == 1) {
-                int sc = scount, sarm[CS];
-#pragma unroll
-                for (int q = 0; q < CS; ++q) sarm[q] = -1;
-                for (int i = 0; i < n * 2 * kSlabs; ++i, ++sc) {  // Q side, then K side, per chunk
-                    const int slot = sc % CS;
-                    if (!wait_or_abort(&cfempty[slot], ((sc / CS) & 1) ^ 1, status, abort_flag)) break;
-                    mbar_arrive_expect_tx(&cffull[slot], kSlab);
-                    bulk_load(ring + slot * kSlab, himg + (i % kSlabs) * kSlab, kSlab, &cffull[slot]);
-                    sarm[slot] = sc;
-                }
-#pragma unroll
-                for (int q = 0; q < CS; ++q)
-                    if (sarm[q] >= 0) mbar_wait(&cffull[q], (sarm[q] / CS) & 1);
+                // slabs: two sides per chunk (query forward, key backward)
+                for (int i = 0; i < 2 * n; ++i)
+                    if (!load_slabs128<CS>(ring, himg, (i & 1) == 0, i == 0, &slab_lpar, &slab_lmask, cffull, cfempty,
+                                           status, abort_flag))
+                        break;
+                drain_slabs128<CS>(slab_lpar, slab_lmask, cffull);
             }
         } else if (warp == 1) {
             if (lane == 0) {
-                int sc = scount;
                 // base descriptors; every MMA below adds a constant to one of them
                 const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024), dk0 = sdesc_sw128(smem_u32(kst), 16, 1024);
                 const uint64_t dring0 = sdesc_sw128(smem_u32(ring), 16, 1024);
@@ -1046,16 +1181,16 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                     // query scores
                     if (!wait_or_abort(xq, ph, status, abort_flag) || !wait_or_abort(qfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    if ((sc = issue_scores128<CS>(tmem + kGQ, tmem + kX, dq0, dring0, sc, cffull, cfempty, status,
-                                                  abort_flag)) < 0)
+                    if (!issue_scores128<CS, true>(tmem + kGQ, tmem + kX, dq0, dring0, &slab_fpar, SlabOrder{i == 0, 0},
+                                                   cffull, cfempty, status, abort_flag))
                         break;
                     umma_commit(sq);
                     umma_commit(qempty);
                     // key scores
                     if (!wait_or_abort(xk, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    if ((sc = issue_scores128<CS>(tmem + kKU, tmem + kX, dk0, dring0, sc, cffull, cfempty, status,
-                                                  abort_flag)) < 0)
+                    if (!issue_scores128<CS, false>(tmem + kKU, tmem + kX, dk0, dring0, &slab_fpar,
+                                                    SlabOrder{0, i == n - 1}, cffull, cfempty, status, abort_flag))
                         break;
                     umma_commit(sk);
                     // num = Gamma^Q S (hi.hi, hi.lo, lo.hi)
@@ -1085,13 +1220,9 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             // ---------------- query group
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            float *xb = reinterpret_cast<float *>(kst);  // key softmax exchange (the K tile is consumed)
             for (int i = 0; i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                if (!wait_or_abort(qfull, ph, status, abort_flag)) break;
-                x2_row128(qst, row, tmem + lb + kX);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xq);
                 if (!wait_or_abort(sq, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
                 if (!wait_or_abort(sready, ph, status, abort_flag)) break;                 // key mass Zp visible
@@ -1101,6 +1232,15 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gq);
+                // components 64 .. 127 of the key softmax
+                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
+                tc_fence_after();
+                if (!key_half128(tmem + lb + kKU, cvec, 1, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone, ph,
+                                 status, abort_flag))
+                    break;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gk);
                 if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
                 tc_fence_after();
                 const float rs0 = split_p_blocks128(tmem + lb + kKU, 0, row);
@@ -1113,14 +1253,24 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 // outputs staged in the K tile buffer (the key score MMAs, its last readers,
                 // are complete: ofull), which the next key tile may then reuse
                 output_rows128(tmem + lb + kX, 1.0f / (den0 + (rs0 + rsk[row]) + eps * rq), kst + (warp & 3) * 8192,
-                               lane, o_bf16, &tmO, (t0 + i) * kT + 32 * (warp & 3), bh);
+                               lane, o_bf16, &tmO, (t0 + i) * kT + 32 * (warp & 3), bh, xfree);
                 tc_fence_before();
                 if (lane == 0) mbar_arrive(kempty);
             }
         } else {
-            // ---------------- key group
+            // ---------------- key group: x^2 of both sides, half of the key softmax, half of
+            // the P split, the state operand
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            float *xb = reinterpret_cast<float *>(kst);
+            auto x2q = [&](int r) {  // x^2 of the query tile of chunk r
+                if (!wait_or_abort(qfull, r & 1, status, abort_flag)) return false;
+                x2_row128(qst, row, tmem + lb + kX);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xq);
+                return true;
+            };
             // job start: the carried-in state (fp32 rows in R) -> tensor memory and the
             // state operand
             if (wait_or_abort(xfull, njob & 1, status, abort_flag))
@@ -1129,7 +1279,8 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sready);
-            for (int i = 0; i < n; ++i) {
+            bool ok = x2q(rbase);
+            for (int i = 0; ok && i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
                 const float zt = __ldcg(ztile + ((size_t)bh * P.ntiles + t0 + i) * kKC + row);
                 if (!wait_or_abort(sq, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
@@ -1140,8 +1291,9 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 if (!wait_or_abort(sk, ph, status, abort_flag)) break;
                 if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;
                 tc_fence_after();
-                // Gamma^K into R once num has read S from there
-                if (!key_row128(tmem + lb + kKU, cvec, (t0 + i) * kT + row < N, R, row, ndone, ph, status, abort_flag))
+                // components 0 .. 63 of the key softmax; Gamma^K into R once num has read S
+                if (!key_half128(tmem + lb + kKU, cvec, 0, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone, ph,
+                                 status, abort_flag))
                     break;
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -1153,7 +1305,8 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
                 // the next chunk's state operand and key mass, once U and the state
-                // update have read Gamma^K
+                // update have read Gamma^K; then its query x^2, once this chunk's
+                // outputs are out of the X columns
                 if (!wait_or_abort(wdone, ph, status, abort_flag)) break;
                 tc_fence_after();
                 if (i + 1 < n) {
@@ -1163,11 +1316,13 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sready);
+                    if (!wait_or_abort(xfree, ph, status, abort_flag)) break;
+                    tc_fence_after();
+                    if (!(ok = x2q(r + 1))) break;
                 }
             }
         }
         rbase += n;
-        scount += n * 2 * kSlabs;
         g += n;
         cta_sync();
         if (aborted(abort_flag)) break;
