@@ -38,8 +38,11 @@ int choose_path(const Problem &p, int causal, const gma_options *opt) {
     const bool tc = tc64 || (causal >= 0 && gma::tc128_supported(p, causal));
     if (path == GMA_PATH_TC) return tc ? GMA_PATH_TC : -1;
     // the single-pass kernel is a causal kernel of the 64-wide family; the
-    // bidirectional tensor-core call already keeps Gamma on chip
-    if (path == GMA_PATH_TC_SINGLE_PASS) return !tc64 ? -1 : causal == 1 ? GMA_PATH_TC_SINGLE_PASS : GMA_PATH_TC;
+    // bidirectional tensor-core calls already keep Gamma on chip
+    if (path == GMA_PATH_TC_SINGLE_PASS) {
+        if (causal == 1) return tc64 ? GMA_PATH_TC_SINGLE_PASS : -1;
+        return tc ? GMA_PATH_TC : -1;
+    }
     if (path != GMA_PATH_AUTO) return -1;
     return tc ? GMA_PATH_TC : GMA_PATH_SIMT;
 }
@@ -142,7 +145,7 @@ gma_status forward(const void *Q_X, const void *K_X, const void *V_X, gma_dtype 
     if (path == GMA_PATH_TC_SINGLE_PASS)
         err = gma::tc_causal_1pass(p, splits, workspace, s, clk);
     else if (path == GMA_PATH_TC && gma::tc128_supported(p, causal))
-        err = gma::tc128_causal(p, splits, workspace, s, clk);
+        err = causal ? gma::tc128_causal(p, splits, workspace, s, clk) : gma::tc128_bidir(p, splits, workspace, s, clk);
     else if (path == GMA_PATH_TC)
         err = causal ? gma::tc_causal(p, splits, workspace, s, clk) : gma::tc_bidir(p, splits, workspace, s, clk);
     else

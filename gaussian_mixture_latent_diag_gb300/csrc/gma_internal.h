@@ -169,10 +169,12 @@ cudaError_t tc_causal_carry(const Problem &p, int splits, const float *Vt_in, co
 extern const char *const kAuxTcStages[5][8];  // as kAuxStages, tensor-core path (entries 0, 3, 4)
 
 // ---------------------------------------------------------------- tensor-core path, d_r = d_v = 128 (gma_tc128.cu)
-// The causal forward at d_r = d_v = 128, K <= 128, bf16 (stages as kTcStages[2]:
-// prep, aggregation, chunk scan); workspace tc128_workspace(p, splits).
+// The forward at d_r = d_v = 128, K <= 128, bf16: causal (stages as kTcStages[2]:
+// prep, aggregation, chunk scan) and bidirectional (kTcStages[1]: prep, key side,
+// query side); workspace tc128_workspace(p, splits) for both.
 bool tc128_supported(const Problem &p, int causal);
 size_t tc128_workspace(const Problem &p, int splits);
 cudaError_t tc128_causal(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
+cudaError_t tc128_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, StageClock &clk);
 
 }  // namespace gma

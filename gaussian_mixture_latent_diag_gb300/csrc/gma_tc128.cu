@@ -434,8 +434,8 @@ __device__ __forceinline__ int column_sums_warp(float (&v)[kKC], int lane) {
 __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part128 P,
-    float *__restrict__ part, float *__restrict__ ztile, unsigned *__restrict__ counters, int stall,
-    unsigned *status) {
+    float *__restrict__ part, float *__restrict__ ztile, float *__restrict__ mem, unsigned *__restrict__ counters,
+    int mode, int stall, unsigned *status) {
     using L = Agg128Smem;
     constexpr int KS = L::kKS, CS = L::kCS;
     constexpr int kX0 = 0, kSC = 256, kSA = 384, kTmemCols = 512;
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                 if (!(ok = wait_or_abort(&zfull[r & 1], (r >> 1) & 1, status, abort_flag))) break;
                 const float *zr = zw + (r & 1) * 4 * kKC;
                 const float zt = ((zr[row] + zr[kKC + row]) + zr[2 * kKC + row]) + zr[3 * kKC + row];
-                __stcg(ztile + ((size_t)bh * P.ntiles + t0 + i) * kKC + row, zt);
+                if (mode == 1) __stcg(ztile + ((size_t)bh * P.ntiles + t0 + i) * kKC + row, zt);
                 zjob += zt;
             }
             // job end: the memory increment and key mass -> this job's memory slot
@@ -675,7 +675,9 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                 tc_fence_before();
             }
         }
-        // ---- the head's last job to finish turns the job memories into exclusive prefixes
+        // ---- the head's last job to finish combines the job memories in job order:
+        // mode 1, each replaced by the exclusive prefix before it; mode 0, the sum of all
+        // of them into the head's memory
         __threadfence();
         cta_sync();
         if (!aborted(abort_flag)) {
@@ -694,12 +696,13 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                         float4 *p4 = reinterpret_cast<float4 *>(part + ((size_t)cc * P.slots + slot128(P, cc, bh)) *
                                                                            kPartFloats) + e4;
                         const float4 v = __ldcg(p4);
-                        __stcg(p4, acc);
+                        if (mode == 1) __stcg(p4, acc);
                         acc.x += v.x;
                         acc.y += v.y;
                         acc.z += v.z;
                         acc.w += v.w;
                     }
+                    if (mode == 0) __stcg(reinterpret_cast<float4 *>(mem + (size_t)bh * kPartFloats) + e4, acc);
                 }
                 if (tid == 0) counters[bh] = 0u;  // ready for the next call
             }
@@ -1335,6 +1338,216 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ bidirectional read
+//
+// Eq. (7) at d_r = d_v = 128: O = Gamma^Q [Vt | Z] / (. + eps) from the head's
+// memory (the aggregation's mode-0 total).  Per query tile: x^2, 40 score MMAs
+// (slabs in the snake order, one side per tile), the query softmax (Gamma^Q =
+// e un-normalised, in place; e . Z and the row sum r in fp32), num = Gamma^Q Vt
+// (24 MMAs against the memory's bf16 hi | lo operand, built in shared memory at
+// each job start), O = num / (e . Z + eps r) staged and stored by TMA.
+// Warps: 0 lane 0 Q loads (two stages), lane 1 slabs; 1 lane 0 MMA issue; 2..5
+// epilogue.  TMEM: x^2 of tile t at [128 (t % 2), +128); scores -> Gamma^Q
+// [256, 384); num [384, 512).  The next tile's score MMAs run beside this
+// tile's outputs.
+struct Read128Smem {
+    static constexpr int kQS = 2, kCS = 4;
+    static constexpr int kQ = 0;                        // Q stages
+    static constexpr int kR = kQ + kQS * kTileB;        // memory operand (hi 32 KB | lo 32 KB)
+    static constexpr int kCf = kR + 65536;              // coefficient slab ring
+    static constexpr int kStage = kCf + kCS * kSlab;    // output staging, 4 warps x 8 KB
+    static constexpr int kC = kStage + 4 * 8192;        // c [128] fp32
+    static constexpr int kZ = kC + 512;                 // Z [128] fp32
+    static constexpr int kBars = kZ + 512;
+    static constexpr int kBytes = kBars + 256;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kR % 1024 == 0 && kCf % 1024 == 0 && kStage % 1024 == 0, "SW128 alignment");
+    static_assert(kAlloc <= 232448, "shared memory budget");
+};
+constexpr int kThreadsRead128 = 64 + 128;
+
+__global__ void __launch_bounds__(kThreadsRead128, 1) tc128_read_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+    const uint8_t *__restrict__ coef_img, const float *__restrict__ mem, int H, Part128 P, float eps, int o_bf16,
+    unsigned *status) {
+    using L = Read128Smem;
+    constexpr int QS = L::kQS, CS = L::kCS;
+    constexpr int kX0 = 0, kGQ = 256, kO = 384, kTmemCols = 512;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qst = smem + L::kQ, *R = smem + L::kR, *ring = smem + L::kCf, *stg = smem + L::kStage;
+    float *cvec = reinterpret_cast<float *>(smem + L::kC), *zs = reinterpret_cast<float *>(smem + L::kZ);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *qfull = bars, *qempty = qfull + QS, *cffull = qempty + QS, *cfempty = cffull + CS,
+             *xq = cfempty + CS, *sq = xq + 2, *gq = sq + 1, *nfull = gq + 1, *ofree = nfull + 1, *sready = ofree + 1,
+             *cfull = sready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cfull + 1);
+    int *abort_flag = reinterpret_cast<int *>(cfull + 2);
+    static_assert((2 * QS + 2 * CS + 9) * 8 + 16 <= 256, "barrier area");
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    if (failed(status) || g0 >= gend) return;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int i = 0; i < QS; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+        }
+        for (int i = 0; i < CS; ++i) {
+            mbar_init(&cffull[i], 1);
+            mbar_init(&cfempty[i], 1);
+        }
+        mbar_init(&xq[0], 4); mbar_init(&xq[1], 4); mbar_init(sq, 1); mbar_init(gq, 4); mbar_init(nfull, 1);
+        mbar_init(ofree, 4); mbar_init(sready, 4); mbar_init(cfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmO);
+    }
+    tc_fence_before();
+    cta_sync();
+    tc_fence_after();
+    pdl_trigger();  // the next call's coefficient prep waits for this kernel's completion
+    // the epilogue reads the aggregation's memories directly
+    if (warp >= 2) pdl_wait();
+    const uint32_t tmem = *tmem_slot;
+
+    int rbase = 0, njob = 0;
+    uint32_t slab_lpar = 0u, slab_fpar = 0u, slab_lmask = 0u;  // slab ring state (see issue_scores128)
+    for (int g = g0; g < gend; ++njob) {
+        const int bh = g / P.ntiles, t0 = g % P.ntiles;
+        const int n = min(P.ntiles - t0, gend - g);
+        const int h = bh % H;
+        const uint8_t *himg = coef_img + (size_t)h * kImgStride;
+        fence_proxy_async_smem();
+        cta_sync();  // the previous job is done with c, the memory operand and Z
+        if (tid == 0) {
+            mbar_arrive_expect_tx(cfull, 512);
+            bulk_load(cvec, himg + kCoefC, 512, cfull);
+        }
+        if (warp == 0) {
+            if (lane == 0) {
+                int qarm[QS];
+#pragma unroll
+                for (int q = 0; q < QS; ++q) qarm[q] = -1;
+                for (int i = 0; i < n; ++i) {
+                    const int r = rbase + i, s = r % QS;
+                    if (!wait_or_abort(&qempty[s], ((r / QS) & 1) ^ 1, status, abort_flag)) break;
+                    mbar_arrive_expect_tx(&qfull[s], kTileB);
+                    tma_load_3d(qst + s * kTileB, &tmQ, 0, (t0 + i) * kT, bh, &qfull[s]);
+                    tma_load_3d(qst + s * kTileB + kHalf, &tmQ, 64, (t0 + i) * kT, bh, &qfull[s]);
+                    qarm[s] = r;
+                }
+#pragma unroll
+                for (int q = 0; q < QS; ++q)
+                    if (qarm[q] >= 0) mbar_wait(&qfull[q], (qarm[q] / QS) & 1);
+            } else if (lane == 1) {
+                for (int i = 0; i < n; ++i)
+                    if (!load_slabs128<CS>(ring, himg, (i & 1) == 0, i == 0, &slab_lpar, &slab_lmask, cffull, cfempty,
+                                           status, abort_flag))
+                        break;
+                drain_slabs128<CS>(slab_lpar, slab_lmask, cffull);
+            }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                const uint64_t dq0 = sdesc_sw128(smem_u32(qst), 16, 1024), dring0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+                const uint64_t dS = sdesc_sw128(smem_u32(R), kHalf, 1024);
+                for (int i = 0; i < n; ++i) {
+                    const int r = rbase + i, ph = r & 1;
+                    if (!wait_or_abort(&xq[r & 1], (r >> 1) & 1, status, abort_flag) ||
+                        !wait_or_abort(&qfull[r % QS], (r / QS) & 1, status, abort_flag))
+                        break;
+                    tc_fence_after();
+                    const SlabOrder so{i == 0, i == n - 1};
+                    const uint32_t ax = tmem + kX0 + 128 * (r & 1);
+                    const uint64_t dx = dadd(dq0, (r % QS) * kTileB);
+                    if (!((i & 1) == 0 ? issue_scores128<CS, true>(tmem + kGQ, ax, dx, dring0, &slab_fpar, so, cffull,
+                                                                   cfempty, status, abort_flag)
+                                       : issue_scores128<CS, false>(tmem + kGQ, ax, dx, dring0, &slab_fpar, so, cffull,
+                                                                    cfempty, status, abort_flag)))
+                        break;
+                    umma_commit(sq);
+                    umma_commit(&qempty[r % QS]);
+                    // num = Gamma^Q [Vt], once the previous tile's outputs are out of its columns
+                    if (!wait_or_abort(gq, ph, status, abort_flag)) break;
+                    if (i == 0 && !wait_or_abort(sready, njob & 1, status, abort_flag)) break;
+                    if (r > 0 && !wait_or_abort(ofree, (r - 1) & 1, status, abort_flag)) break;
+                    tc_fence_after();
+                    issue_num128(tmem + kO, tmem + kGQ, dS);
+                    umma_commit(nfull);
+                }
+            }
+        } else {
+            // ---------------- epilogue: one thread per tile row (and per memory row)
+            const int row = epi_row(warp, lane);
+            const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            uint8_t *stage = stg + (warp & 3) * 8192;
+            // job start: the head's memory (fp32 [Vt | Z] rows) -> the bf16 hi | lo operand and Z
+            {
+                const float *mr = mem + (size_t)bh * kPartFloats + (size_t)row * kD;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 a = __ldcg(reinterpret_cast<const float4 *>(mr + 32 * q) + u);
+                        v[4 * u] = __float_as_uint(a.x);
+                        v[4 * u + 1] = __float_as_uint(a.y);
+                        v[4 * u + 2] = __float_as_uint(a.z);
+                        v[4 * u + 3] = __float_as_uint(a.w);
+                    }
+                    state_row128(R, row, v, q);
+                }
+                zs[row] = __ldcg(mem + (size_t)bh * kPartFloats + kKC * kD + row);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready);
+            }
+            auto x2 = [&](int r) {
+                if (!wait_or_abort(&qfull[r % QS], (r / QS) & 1, status, abort_flag)) return false;
+                x2_row128(qst + (r % QS) * kTileB, row, tmem + lb + kX0 + 128 * (r & 1));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xq[r & 1]);
+                return true;
+            };
+            bool ok = x2(rbase) && wait_or_abort(cfull, njob & 1, status, abort_flag) &&
+                      wait_or_abort(sready, njob & 1, status, abort_flag);  // c and every Z row visible
+            for (int i = 0; ok && i < n; ++i) {
+                const int r = rbase + i, ph = r & 1;
+                if (!(ok = wait_or_abort(sq, ph, status, abort_flag))) break;
+                tc_fence_after();
+                float den0;
+                const float rq = query_row128(tmem + lb + kGQ, cvec, zs, &den0);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gq);
+                // the next tile's x^2 (its buffer was read by tile i - 1's score MMAs)
+                if (i + 1 < n && !(ok = x2(r + 1))) break;
+                if (!(ok = wait_or_abort(nfull, ph, status, abort_flag))) break;
+                tc_fence_after();
+                output_rows128(tmem + lb + kO, 1.0f / (den0 + eps * rq), stage, lane, o_bf16, &tmO,
+                               (t0 + i) * kT + 32 * (warp & 3), bh, ofree);
+                tc_fence_before();
+            }
+        }
+        rbase += n;
+        g += n;
+        cta_sync();
+        if (aborted(abort_flag)) break;
+    }
+    if (tid == 0 && njob > 0) mbar_wait(cfull, (njob - 1) & 1);
+    tc_fence_before();
+    cta_sync();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host side
 
 // [BH][N][128] bf16 tensor, boxes of 64 columns x 128 rows x 1 head, 128-byte
@@ -1375,7 +1588,7 @@ bool make_out_map128(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
 struct Tc128Layout {
     Part128 P;
     int nctas = 0;
-    size_t counters = 0, head_err = 0, coef = 0, part = 0, ztile = 0, total = 0;
+    size_t counters = 0, head_err = 0, coef = 0, part = 0, ztile = 0, mem = 0, total = 0;
 };
 
 Tc128Layout tc128_layout(const Problem &p, int splits) {
@@ -1398,6 +1611,8 @@ Tc128Layout tc128_layout(const Problem &p, int splits) {
     off = align256(off + sizeof(float) * (size_t)L.nctas * L.P.slots * kPartFloats);
     L.ztile = off;
     off = align256(off + sizeof(float) * (size_t)p.BH() * ntiles * kKC);
+    L.mem = off;  // the bidirectional call's per-head memories
+    off = align256(off + sizeof(float) * (size_t)p.BH() * kPartFloats);
     L.total = off;
     return L;
 }
@@ -1405,7 +1620,7 @@ Tc128Layout tc128_layout(const Problem &p, int splits) {
 }  // namespace
 
 bool tc128_supported(const Problem &p, int causal) {
-    return causal == 1 && p.dtype == GMA_BF16 && p.d_r == kD && p.d_v == kD && p.K <= kKC;
+    return (causal == 0 || causal == 1) && p.dtype == GMA_BF16 && p.d_r == kD && p.d_v == kD && p.K <= kKC;
 }
 
 size_t tc128_workspace(const Problem &p, int splits) { return tc128_layout(p, splits).total; }
@@ -1430,12 +1645,42 @@ cudaError_t tc128_causal(const Problem &p, int splits, void *workspace, cudaStre
     GMA_TRY(set_smem(tc128_aggregate_kernel, Agg128Smem::kAlloc));
     GMA_TRY(launch_pdl(tc128_aggregate_kernel, dim3(L.nctas), dim3(kThreadsAgg), Agg128Smem::kAlloc, s, tk, tv,
                        static_cast<const uint8_t *>(coef), static_cast<const unsigned *>(head_err), p.H, p.N, L.P,
-                       part, ztile, counters, p.test_stall ? 1 : 0, status));
+                       part, ztile, static_cast<float *>(nullptr), counters, 1, p.test_stall ? 1 : 0, status));
     clk.mark();
     GMA_TRY(set_smem(tc128_causal_kernel, Causal128Smem::kAlloc));
     GMA_TRY(launch_pdl(tc128_causal_kernel, dim3(L.nctas), dim3(kThreadsC128), Causal128Smem::kAlloc, s, tq, tk, tv,
                        to, static_cast<const uint8_t *>(coef), static_cast<const float *>(part),
                        static_cast<const float *>(ztile), p.H, p.N, L.P, p.eps, p.o_bf16 ? 1 : 0, status));
+    clk.mark();
+    return cudaSuccess;
+}
+
+cudaError_t tc128_bidir(const Problem &p, int splits, void *workspace, cudaStream_t s, StageClock &clk) {
+    const Tc128Layout L = tc128_layout(p, splits);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    unsigned *status = reinterpret_cast<unsigned *>(ws);
+    unsigned *counters = reinterpret_cast<unsigned *>(ws + L.counters);
+    unsigned *head_err = reinterpret_cast<unsigned *>(ws + L.head_err);
+    uint8_t *coef = ws + L.coef;
+    float *part = reinterpret_cast<float *>(ws + L.part);
+    float *mem = reinterpret_cast<float *>(ws + L.mem);
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map128(&tq, p.Q, p.BH(), p.N) || !make_map128(&tk, p.Kx, p.BH(), p.N) ||
+        !make_map128(&tv, p.V, p.BH(), p.N) || !make_out_map128(&to, p.O, p.BH(), p.N, p.o_bf16))
+        return cudaErrorInvalidValue;
+    clk.mark();
+    GMA_TRY(launch_pdl(tc128_prep_kernel, dim3(kPrepBlocks128, p.H), dim3(128), 0, s, p.mu, p.sigma2, p.log_pi, p.K,
+                       coef, status, head_err, counters, p.BH()));
+    clk.mark();
+    GMA_TRY(set_smem(tc128_aggregate_kernel, Agg128Smem::kAlloc));
+    GMA_TRY(launch_pdl(tc128_aggregate_kernel, dim3(L.nctas), dim3(kThreadsAgg), Agg128Smem::kAlloc, s, tk, tv,
+                       static_cast<const uint8_t *>(coef), static_cast<const unsigned *>(head_err), p.H, p.N, L.P,
+                       part, static_cast<float *>(nullptr), mem, counters, 0, p.test_stall ? 1 : 0, status));
+    clk.mark();
+    GMA_TRY(set_smem(tc128_read_kernel, Read128Smem::kAlloc));
+    GMA_TRY(launch_pdl(tc128_read_kernel, dim3(L.nctas), dim3(kThreadsRead128), Read128Smem::kAlloc, s, tq, to,
+                       static_cast<const uint8_t *>(coef), static_cast<const float *>(mem), p.H, L.P, p.eps,
+                       p.o_bf16 ? 1 : 0, status));
     clk.mark();
     return cudaSuccess;
 }

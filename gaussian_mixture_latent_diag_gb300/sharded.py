@@ -32,18 +32,20 @@ class CudaOps:
     K <= 64: the sizes of the 64-wide family, where the unsharded forward runs
     on the tensor cores too, so a sharded call has the unsharded call's
     accuracy), else on the CUDA cores.  The 128-wide tensor-core kernels serve
-    only the whole-sequence causal forward, so their sizes shard on the CUDA
-    cores."""
+    only the whole-sequence forwards, so their sizes shard on the CUDA cores."""
 
     @staticmethod
     def _path(X, V, mu, causal=0):
-        from . import PATH_SIMT, PATH_TC, selected_path
-        dtype = "bf16" if X.dtype == torch.bfloat16 else "f32"
+        import ctypes
+        from . import PATH_SIMT, PATH_TC, _native
+        code = _native.GMA_BF16 if X.dtype == torch.bfloat16 else _native.GMA_F32
         N, d_r = X.shape[-2:]
-        # the memory kernels exist wherever the bidirectional forward runs on the
-        # tensor cores (both directions of the 64-wide family have the same sizes)
-        tc = selected_path(max(N, 1), d_r, V.shape[-1], mu.shape[1], dtype, 0) == PATH_TC
-        return PATH_TC if tc else PATH_SIMT
+        # the library's own answer: the memory calls' workspace query with
+        # GMA_PATH_TC is 0 where they have no tensor-core kernels
+        opt = _native.options(path=PATH_TC)
+        nb = _native.load().gma_latent_memory_workspace_size(1, 1, max(N, 1), d_r, V.shape[-1], mu.shape[1], code,
+                                                             ctypes.byref(opt))
+        return PATH_TC if nb > 0 else PATH_SIMT
 
     def latent_memory(self, K, V, mu, sigma2, log_pi):
         from . import latent_memory

@@ -67,9 +67,13 @@ typedef enum gma_status {
 enum {
     GMA_PATH_AUTO = 0,   /* tensor-core path when the dtype/sizes allow it, else SIMT */
     GMA_PATH_SIMT = 1,   /* fp32 CUDA-core kernels (every supported size, fp32 or bf16 input) */
-    GMA_PATH_TC = 2,     /* tcgen05 tensor-core kernels; GMA_ERR_UNSUPPORTED_SHAPE if not eligible */
+    /* tcgen05 tensor-core kernels, bf16 inputs: the forward calls at d_r in {32, 64},
+     * d_v = 64, K <= 64 or at d_r = d_v = 128, K <= 128; the latent-memory calls
+     * at the first of those sizes.  GMA_ERR_UNSUPPORTED_SHAPE if not eligible. */
+    GMA_PATH_TC = 2,
     /* Causal calls (gma_forward_causal, gma_forward_causal_carry): the single-pass
-     * tensor-core kernel, same sizes as GMA_PATH_TC.  Each 128-token chunk computes
+     * tensor-core kernel, at d_r in {32, 64}, d_v = 64, K <= 64 (other sizes:
+     * GMA_ERR_UNSUPPORTED_SHAPE).  Each 128-token chunk computes
      * its key responsibilities in shared memory next to its query side, so
      * Gamma^K never goes to device memory and Q_X, K_X, V_X are read once; the
      * prefix memory before a chunk is the fixed-order sum of the published

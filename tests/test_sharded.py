@@ -135,9 +135,10 @@ def test_cuda_ops_pick_the_unsharded_kernel_family():
     assert pick(bf, 64, 32, 64) == gma.PATH_SIMT
     assert pick(bf, 128, 64, 64, causal=1) == gma.PATH_SIMT
     assert pick(bf, 64, 64, 128) == gma.PATH_SIMT
-    assert pick(bf, 128, 128, 128, causal=1) == gma.PATH_SIMT
-    assert gma.selected_path(300, 128, 128, 128, "bf16", 1) == gma.PATH_TC  # the unsharded causal forward
-    for dtype, d_r, d_v, K in [(bf, 64, 64, 64), (f32, 16, 32, 8), (bf, 128, 128, 128)]:
+    for causal in (0, 1):  # the unsharded forward is on the tensor cores, the memory calls are not
+        assert pick(bf, 128, 128, 128, causal=causal) == gma.PATH_SIMT
+        assert gma.selected_path(300, 128, 128, 128, "bf16", causal) == gma.PATH_TC
+    for dtype, d_r, d_v, K in [(bf, 64, 64, 64), (f32, 16, 32, 8)]:
         for causal in (0, 1):
-            want = gma.selected_path(300, d_r, d_v, K, "bf16" if dtype == bf else "f32", 0)
+            want = gma.selected_path(300, d_r, d_v, K, "bf16" if dtype == bf else "f32", causal)
             assert pick(dtype, d_r, d_v, K, causal) == want

@@ -1,9 +1,10 @@
-"""The causal forward on the 128-wide tensor-core kernels (d_r = d_v = 128,
-K <= 128, bf16): element by element against the fp64 oracle on sizes the
-oracle finishes in seconds -- several 128-token chunks and a ragged tail,
-padded components, one token, one component -- under every partition of the
-chunks over CTAs (jobs that cross a head boundary, CTAs with several jobs), fp32
-and bf16 O, bitwise reproducibility, parameter errors and a forced timeout."""
+"""The causal and bidirectional forwards on the 128-wide tensor-core kernels
+(d_r = d_v = 128, K <= 128, bf16): element by element against the fp64 oracle
+on sizes the oracle finishes in seconds -- several 128-token chunks and a
+ragged tail, padded components, one token, one component -- under every
+partition of the chunks over CTAs (jobs that cross a head boundary, CTAs with
+several jobs), fp32 and bf16 O, bitwise reproducibility, parameter errors and a
+forced timeout."""
 import zlib
 
 import numpy as np
@@ -17,8 +18,8 @@ from gpu_helpers import TOL, normalised_error, normalised_error_bf16_out, oracle
 pytestmark = pytest.mark.gpu
 
 
-def _case(B, H, N, K, **kw):
-    return Case(f"tc128_B{B}_H{H}_N{N}_K{K}", True, B, H, N, 128, 128, K, "bf16", **kw)
+def _case(B, H, N, K, causal=True, **kw):
+    return Case(f"tc128_{'c' if causal else 'b'}_B{B}_H{H}_N{N}_K{K}", causal, B, H, N, 128, 128, K, "bf16", **kw)
 
 
 def _inputs(case, salt=0):
@@ -28,7 +29,7 @@ def _inputs(case, salt=0):
 def test_selected_path_is_tensor_core():
     assert gma.selected_path(32768, 128, 128, 128, "bf16", 1) == gma.PATH_TC
     assert gma.selected_path(32768, 128, 128, 100, "bf16", 1) == gma.PATH_TC
-    assert gma.selected_path(32768, 128, 128, 128, "bf16", 0) == gma.PATH_SIMT   # no 128-wide bidirectional kernels
+    assert gma.selected_path(32768, 128, 128, 128, "bf16", 0) == gma.PATH_TC
     assert gma.selected_path(32768, 128, 128, 128, "f32", 1) == gma.PATH_SIMT
     assert gma.selected_path(32768, 128, 128, 129, "bf16", 1) == -1              # K > 128: no kernel
     assert gma.selected_path(32768, 128, 128, 128, "bf16", 1, path=gma.PATH_TC_SINGLE_PASS) == -1
@@ -37,8 +38,9 @@ def test_selected_path_is_tensor_core():
 @pytest.mark.parametrize("B,H,N,K", [(2, 3, 260, 128), (1, 2, 700, 100), (1, 1, 1, 128), (2, 1, 129, 1),
                                      (1, 2, 513, 64)], ids=lambda v: str(v))
 @pytest.mark.parametrize("o_bf16", [False, True], ids=["o32", "o16"])
-def test_matches_oracle(B, H, N, K, o_bf16):
-    case = _case(B, H, N, K)
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "bidir"])
+def test_matches_oracle(B, H, N, K, o_bf16, causal):
+    case = _case(B, H, N, K, causal)
     inp = _inputs(case)
     O = run_gpu(case, to_dev(inp), path=gma.PATH_TC, o_bf16=o_bf16)
     ref = oracle_full(case, inp)
@@ -46,13 +48,14 @@ def test_matches_oracle(B, H, N, K, o_bf16):
     assert err <= TOL["bf16"], f"{case.name}: normalised max error {err:.3e}"
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "bidir"])
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 11, 0])
-def test_every_partition_matches_oracle(splits):
+def test_every_partition_matches_oracle(splits, causal):
     """Six heads of eight chunks (the last ragged) cut into `splits` contiguous
     ranges: jobs start and end inside heads, a CTA may hold parts of several
     heads, and each job's carried-in prefix comes from the aggregation's
-    combine."""
-    case = _case(2, 3, 1000, 128)
+    combine (causal) or the head's whole memory (bidirectional)."""
+    case = _case(2, 3, 1000, 128, causal)
     inp = _inputs(case, 3)
     O = run_gpu(case, to_dev(inp), path=gma.PATH_TC, splits=splits)
     err = normalised_error(O, oracle_full(case, inp))
@@ -74,17 +77,19 @@ def test_long_head_matches_oracle_rows():
     assert err <= TOL["bf16"], err
 
 
-def test_deterministic():
-    case = _case(2, 2, 900, 128)
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "bidir"])
+def test_deterministic(causal):
+    case = _case(2, 2, 900, 128, causal)
     d = to_dev(_inputs(case, 8))
     a = run_gpu(case, d, path=gma.PATH_TC, splits=5)
     b = run_gpu(case, d, path=gma.PATH_TC, splits=5)
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "bidir"])
 @pytest.mark.parametrize("bad", ["zero_var", "nan_mu", "inf_logpi"])
-def test_invalid_parameters_reported(bad):
-    case = _case(1, 2, 300, 128)
+def test_invalid_parameters_reported(bad, causal):
+    case = _case(1, 2, 300, 128, causal)
     d = to_dev(_inputs(case, 9))
     if bad == "zero_var":
         d["sigma2"][1, 100, 127] = 0.0
