@@ -236,26 +236,34 @@ __device__ __noinline__ bool issue_scores128(uint32_t d, uint32_t ax, uint64_t d
     return true;
 }
 
-// Producer side of the slab schedule: the loads of one side (all 8 for the first
-// side of a job, else the 8 - NS the previous side did not leave in the ring), each
-// once the slot's previous load has had its last use.  Bit `slot` of *lpar is the
-// parity of the slot's load count; bit `slot` of *lmask is set once the slot has
-// been loaded.  Returns false on a timeout.
+// Producer side of the slab schedule: the loads of one side (all NU units for
+// the first side of a job, else the NU - NS the previous side did not leave in
+// the ring), each once the slot's previous load has had its last use.  A unit
+// is UB bytes of the coefficient image (a slab, or a pair of adjacent slabs);
+// unit u always goes to slot u % NS.  Bit `slot` of *lpar is the parity of the
+// slot's load count; bit `slot` of *lmask is set once the slot has been loaded.
+// Returns false on a timeout.
+template <int NS, int NU, int UB>
+__device__ __forceinline__ bool load_units128(uint8_t *ring, const uint8_t *himg, int fwd, int first, uint32_t *lpar,
+                                              uint32_t *lmask, uint64_t *full, uint64_t *empty, unsigned *status,
+                                              int *abort_flag) {
+    uint32_t lp = *lpar;
+    for (int k = first ? 0 : NS; k < NU; ++k) {
+        const int u = fwd ? k : NU - 1 - k, slot = u % NS;
+        if (!wait_or_abort(&empty[slot], ((lp >> slot) & 1u) ^ 1u, status, abort_flag)) return false;
+        lp ^= 1u << slot;
+        *lmask |= 1u << slot;
+        mbar_arrive_expect_tx(&full[slot], UB);
+        bulk_load(ring + slot * UB, himg + u * UB, UB, &full[slot]);
+        *lpar = lp;
+    }
+    return true;
+}
 template <int NS>
 __device__ __forceinline__ bool load_slabs128(uint8_t *ring, const uint8_t *himg, int fwd, int first, uint32_t *lpar,
                                               uint32_t *lmask, uint64_t *full, uint64_t *empty, unsigned *status,
                                               int *abort_flag) {
-    uint32_t lp = *lpar;
-    for (int k = first ? 0 : NS; k < kSlabs; ++k) {
-        const int sl = fwd ? k : kSlabs - 1 - k, slot = sl % NS;
-        if (!wait_or_abort(&empty[slot], ((lp >> slot) & 1u) ^ 1u, status, abort_flag)) return false;
-        lp ^= 1u << slot;
-        *lmask |= 1u << slot;
-        mbar_arrive_expect_tx(&full[slot], kSlab);
-        bulk_load(ring + slot * kSlab, himg + sl * kSlab, kSlab, &full[slot]);
-        *lpar = lp;
-    }
-    return true;
+    return load_units128<NS, kSlabs, kSlab>(ring, himg, fwd, first, lpar, lmask, full, empty, status, abort_flag);
 }
 
 // Waits (bounded) until the last load into every slot that has been loaded has
@@ -265,6 +273,99 @@ __device__ __forceinline__ void drain_slabs128(uint32_t lpar, uint32_t lmask, ui
 #pragma unroll
     for (int q = 0; q < NS; ++q)
         if ((lmask >> q) & 1u) mbar_wait(&full[q], ((lpar >> q) & 1u) ^ 1u);
+}
+
+// Score MMAs of one key tile of the aggregation, 24 instructions: the slabs
+// stream as four 32 KB pairs -- [a_hi ; a_lo] and [b_hi ; b_lo] of each column
+// half, adjacent in the image, so each pair is one N = 256 B operand (rows: the
+// 128 components' hi parts, then their lo parts) -- and per K step
+//   D[:, 0:256] += x2hi [a_hi | a_lo],  D[:, 0:128] += x2lo a_hi,  D[:, 0:256] += x [b_hi | b_lo];
+// the score of component k is D[:, k] + D[:, 128 + k] (+ c_k).  Pairs in the
+// snake order of issue_scores128 (unit u in slot u % NS).
+template <int NS, bool FWD>
+__device__ __noinline__ bool issue_score_pairs128(uint32_t d, uint32_t ax, uint64_t dx0, uint64_t dring0,
+                                                  uint32_t *fpar, SlabOrder so, uint64_t *full, uint64_t *empty,
+                                                  unsigned *status, int *abort_flag) {
+    constexpr uint32_t i256 = idesc_bf16(kT, 256, false, false), i128 = idesc_bf16(kT, 128, false, false);
+    constexpr int NU = kSlabs / 2;
+    static_assert(2 * NS <= NU, "the first and last NS positions of a side must not overlap");
+    uint32_t fp = *fpar;
+#pragma unroll
+    for (int k = 0; k < NU; ++k) {
+        const int u = FWD ? k : NU - 1 - k, slot = u % NS, hf = u >> 1;
+        const bool a_pair = (u & 1) == 0;
+        if (so.first || k >= NS) {  // a fresh load
+            if (!mbar_wait(&full[slot], (fp >> slot) & 1u)) {
+                note_timeout(status, abort_flag);
+                return false;
+            }
+            fp ^= 1u << slot;
+        }
+        tc_fence_after();
+        const uint64_t db = dadd(dring0, slot * 2 * kSlab);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * hf + k4;
+            const uint64_t bb = dadd(db, k4 * 32);
+            const uint32_t acc = (k > 0 || k4 > 0) ? 1u : 0u;
+            if (a_pair) {
+                umma_bf16_tA(d, ax + kk * 8, bb, i256, acc);
+                umma_bf16_tA(d, ax + 64 + kk * 8, bb, i128, 1u);
+            } else {
+                umma_bf16(d, dadd(dx0, hf * kHalf + k4 * 32), bb, i256, acc);
+            }
+        }
+        if (k < NU - NS || so.last) umma_commit(&empty[slot]);  // this load's last use
+    }
+    *fpar = fp;
+    return true;
+}
+
+// Score row of the N = 256 accumulator: e_k = s_k + c_k into registers (s_k the
+// sum of columns k and 128 + k, c from the head's image in global memory);
+// returns the row maximum.  exp_row128 then turns e into 2^(e - max) and
+// returns the row sum: the accumulator is free between the two.
+__device__ __forceinline__ float score_sum256(uint32_t taddr, const float *cg, float (&e)[kKC]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t a[32], b[32];
+        tmem_ld32(taddr + 32 * q, a);
+        tmem_ld32(taddr + 128 + 32 * q, b);
+        tmem_wait_ld();
+        const float4 *c4 = reinterpret_cast<const float4 *>(cg + 32 * q);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 c = __ldg(c4 + i);
+            const float2 x0 = f2_add(f2_add(make_float2(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1])),
+                                            make_float2(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]))),
+                                     make_float2(c.x, c.y));
+            const float2 x1 = f2_add(f2_add(make_float2(__uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3])),
+                                            make_float2(__uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]))),
+                                     make_float2(c.z, c.w));
+            e[32 * q + 4 * i] = x0.x;
+            e[32 * q + 4 * i + 1] = x0.y;
+            e[32 * q + 4 * i + 2] = x1.x;
+            e[32 * q + 4 * i + 3] = x1.y;
+            m = fmaxf(m, fmaxf(fmaxf(x0.x, x0.y), fmaxf(x1.x, x1.y)));
+        }
+    }
+    return m;
+}
+__device__ __forceinline__ float exp_row128(float (&e)[kKC], float m) {
+    const float2 mm = make_float2(m, m);
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kKC; k += 4) {
+        const float2 d0 = f2_sub(make_float2(e[k], e[k + 1]), mm), d1 = f2_sub(make_float2(e[k + 2], e[k + 3]), mm);
+        e[k] = ex2(d0.x);
+        e[k + 1] = ex2(d0.y);
+        e[k + 2] = ex2(d1.x);
+        e[k + 3] = ex2(d1.y);
+        s0 = f2_add(s0, make_float2(e[k], e[k + 1]));
+        s1 = f2_add(s1, make_float2(e[k + 2], e[k + 3]));
+    }
+    return (s0.x + s0.y) + (s1.x + s1.y);
 }
 
 // The other MMA batches of a chunk, out of line so that the compiler keeps
@@ -387,24 +488,25 @@ __device__ __forceinline__ void store_gamma128(uint8_t *gbuf, int row, const flo
 
 // ------------------------------------------------------------------ aggregation
 //
-// Warps: 0 lane 0 K / V tile loads, lane 1 coefficient slabs; 1 lane 0 MMA
+// Warps: 0 lane 0 K / V tile loads, lane 1 coefficient slab pairs; 1 lane 0 MMA
 // issue; 2..5 epilogue (one thread per tile row / component).
-// TMEM: x^2 of tile t at [128 (t % 2), +128); scores [256, 384); the job's
-// memory increment S (M = 128 components, N = 128 value columns) [384, 512).
-// Per tile: 40 score MMAs, then 16 state MMAs (Gamma^K_hi, Gamma^K_lo times V,
-// both operands MN-major).  The epilogue loads a tile's scores into registers,
-// frees the accumulator for the next tile's score MMAs, prepares the next
+// TMEM: x^2 [0, 128); scores [128, 384) (N = 256: hi-part and lo-part
+// products); the job's memory increment S (M = 128 components, N = 128 value
+// columns) [384, 512).  Per tile: 24 score MMAs, then 16 state MMAs
+// (Gamma^K_hi, Gamma^K_lo times V, both operands MN-major).  The epilogue loads
+// a tile's scores into registers, frees the accumulator, prepares the next
 // tile's x^2, and only then runs the softmax and stores Gamma^K, so the next
-// score MMAs overlap it.
+// score MMAs overlap it.  The key mass of a tile (column sums of Gamma^K) is
+// left as four per-warp partial rows (a fixed-order butterfly over each warp's
+// 32 rows): the scan adds them in warp order, and the job's total is summed in
+// registers and combined across the warps once, at the job's end.
 struct Agg128Smem {
-    static constexpr int kKS = 2, kCS = 3;
+    static constexpr int kKS = 2, kCS = 2;              // K stages; slab-pair slots
     static constexpr int kK = 0;                        // K stages
     static constexpr int kV = kK + kKS * kTileB;        // V stage
     static constexpr int kG = kV + kTileB;              // Gamma^K buffer (16 groups x 4 KB)
-    static constexpr int kCf = kG + 16 * kGroupB;       // coefficient slab ring
-    static constexpr int kC = kCf + kCS * kSlab;        // c [128] fp32
-    static constexpr int kZw = kC + 512;                // column-sum partials [2][4 warps][128] fp32
-    static constexpr int kBars = kZw + 2 * 4 * kKC * 4;
+    static constexpr int kCf = kG + 16 * kGroupB;       // slab-pair ring (32 KB slots)
+    static constexpr int kBars = kCf + kCS * 2 * kSlab;
     static constexpr int kBytes = kBars + 256;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kV % 1024 == 0 && kG % 1024 == 0 && kCf % 1024 == 0, "SW128 alignment");
@@ -431,6 +533,60 @@ __device__ __forceinline__ int column_sums_warp(float (&v)[kKC], int lane) {
     return base;
 }
 
+// The combine of head bh's job memories (fp32, kPartFloats each), in job order,
+// by the whole CTA: mode 1 replaces each by the exclusive prefix before it,
+// mode 0 writes their sum to the head's memory.  Each thread takes NQ float4
+// slots per round and keeps the loads of NB jobs for all of them in flight at
+// once (the sums stay in job order).
+__device__ __noinline__ void combine_jobs128(float *__restrict__ part, float *__restrict__ mem, const Part128 &P,
+                                             int bh, int mode, int tid) {
+    constexpr int kP4 = kPartFloats / 4, NQ = 4, NB = 4;
+    const int cf = first_cta128(P, bh), cl = last_cta128(P, bh);
+    for (int e0 = tid; e0 < kP4; e0 += NQ * kThreadsAgg) {
+        float4 acc[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cb = cf; cb <= cl; cb += NB) {
+            float4 v[NB][NQ];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int cc = cb + u;
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    part + ((size_t)cc * P.slots + (cc <= cl ? slot128(P, cc, bh) : 0)) * kPartFloats);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const int e4 = e0 + q * kThreadsAgg;
+                    v[u][q] = (cc <= cl && e4 < kP4) ? __ldcg(src + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int cc = cb + u;
+                if (cc > cl) break;
+                float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)cc * P.slots + slot128(P, cc, bh)) *
+                                                                     kPartFloats);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const int e4 = e0 + q * kThreadsAgg;
+                    if (e4 >= kP4) continue;
+                    if (mode == 1) __stcg(dst + e4, acc[q]);
+                    acc[q].x += v[u][q].x;
+                    acc[q].y += v[u][q].y;
+                    acc[q].z += v[u][q].z;
+                    acc[q].w += v[u][q].w;
+                }
+            }
+        }
+        if (mode == 0) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int e4 = e0 + q * kThreadsAgg;
+                if (e4 < kP4) __stcg(reinterpret_cast<float4 *>(mem + (size_t)bh * kPartFloats) + e4, acc[q]);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part128 P,
@@ -438,20 +594,18 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
     int mode, int stall, unsigned *status) {
     using L = Agg128Smem;
     constexpr int KS = L::kKS, CS = L::kCS;
-    constexpr int kX0 = 0, kSC = 256, kSA = 384, kTmemCols = 512;
+    constexpr int kX = 0, kSC = 128, kSA = 384, kTmemCols = 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *kst = smem + L::kK, *vst = smem + L::kV, *gbuf = smem + L::kG, *ring = smem + L::kCf;
-    float *cvec = reinterpret_cast<float *>(smem + L::kC), *zw = reinterpret_cast<float *>(smem + L::kZw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *kfull = bars, *kempty = kfull + KS, *vfull = kempty + KS, *vempty = vfull + 1, *cffull = vempty + 1,
-             *cfempty = cffull + CS, *xready = cfempty + CS, *sfull = xready + 2, *sfree = sfull + 1,
-             *gready = sfree + 1, *wdone = gready + 1, *accfull = wdone + 1, *cfull = accfull + 1,
-             *zfull = cfull + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(zfull + 2);
-    int *abort_flag = reinterpret_cast<int *>(zfull + 3);
+             *cfempty = cffull + CS, *xready = cfempty + CS, *sfull = xready + 1, *sfree = sfull + 1,
+             *gready = sfree + 1, *wdone = gready + 1, *accfull = wdone + 1, *zjob = accfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(zjob + 1);
+    int *abort_flag = reinterpret_cast<int *>(zjob + 2);
     int *last_flag = abort_flag + 1;
-    static_assert((2 * KS + 2 + 2 * CS + 10) * 8 + 16 <= 256, "barrier area");
+    static_assert((2 * KS + 2 + 2 * CS + 7) * 8 + 16 <= 256, "barrier area");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -473,16 +627,13 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
             mbar_init(&cffull[i], 1);
             mbar_init(&cfempty[i], 1);
         }
-        mbar_init(&xready[0], 4);
-        mbar_init(&xready[1], 4);
+        mbar_init(xready, 4);
         mbar_init(sfull, 1);
         mbar_init(sfree, 4);
         mbar_init(gready, 4);
         mbar_init(wdone, 1);
         mbar_init(accfull, 1);
-        mbar_init(cfull, 1);
-        mbar_init(&zfull[0], 4);
-        mbar_init(&zfull[1], 4);
+        mbar_init(zjob, 4);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmK);
@@ -505,7 +656,6 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
     const uint32_t tmem = *tmem_slot;
 
     int rbase = 0, njob = 0;
-    int carm = -1;  // last job whose c vector copy was armed (thread 0)
     // slab ring state of the producer (load parities) and of the MMA thread (full
     // parities), per slot; slab_lmask: the slots loaded at least once
     uint32_t slab_lpar = 0u, slab_fpar = 0u, slab_lmask = 0u;
@@ -514,12 +664,7 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
         const int n = min(P.ntiles - t0, gend - g);
         const int h = bh % H;
         const uint8_t *himg = coef_img + (size_t)h * kImgStride;
-        cta_sync();  // the previous job is done with c and the job memory
-        if (tid == 0) {
-            mbar_arrive_expect_tx(cfull, 512);
-            bulk_load(cvec, himg + kCoefC, 512, cfull);
-            carm = njob;
-        }
+        cta_sync();  // the previous job is done with the Gamma buffer and the job memory
         if (warp == 0) {
             if (lane == 0) {
                 // K two stages ahead, V one stage
@@ -559,10 +704,10 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                     if (karm[q] >= 0) mbar_wait(&kfull[q], (karm[q] / KS) & 1);
                 if (varm >= 0) mbar_wait(vfull, varm & 1);
             } else if (lane == 1) {
-                // slabs: one side per key tile, alternating direction
+                // slab pairs: one side per key tile, alternating direction
                 for (int i = 0; i < n; ++i)
-                    if (!load_slabs128<CS>(ring, himg, (i & 1) == 0, i == 0, &slab_lpar, &slab_lmask, cffull, cfempty,
-                                           status, abort_flag))
+                    if (!load_units128<CS, kSlabs / 2, 2 * kSlab>(ring, himg, (i & 1) == 0, i == 0, &slab_lpar,
+                                                                  &slab_lmask, cffull, cfempty, status, abort_flag))
                         break;
                 // every slab load armed here has landed before the CTA moves on or leaves
                 drain_slabs128<CS>(slab_lpar, slab_lmask, cffull);
@@ -574,21 +719,19 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                 const uint64_t dgt = sdesc_sw128(smem_u32(gbuf), 2048, kGroupB);  // Gamma^K^T hi, MN-major A
                 const uint64_t dv = sdesc_sw128(smem_u32(vst), kHalf, 1024);       // V, MN-major B
                 // scores(i + 1) go before the state MMAs of tile i: the epilogue frees the
-                // score accumulator before it runs tile i's softmax
+                // score accumulator and prepares the next x^2 before tile i's softmax
                 auto scores = [&](int i) {
                     const int r = rbase + i;
-                    if (!wait_or_abort(&xready[r & 1], (r >> 1) & 1, status, abort_flag)) return false;
+                    if (!wait_or_abort(xready, r & 1, status, abort_flag)) return false;
                     if (!wait_or_abort(&kfull[r % KS], (r / KS) & 1, status, abort_flag)) return false;
                     if (r > 0 && !wait_or_abort(sfree, (r - 1) & 1, status, abort_flag)) return false;
                     tc_fence_after();
                     const SlabOrder so{i == 0, i == n - 1};
-                    const uint32_t ax = tmem + kX0 + 128 * (r & 1);
                     const uint64_t dx = dadd(dk0, (r % KS) * kTileB);
-                    if (!((i & 1) == 0
-                              ? issue_scores128<CS, true>(tmem + kSC, ax, dx, dring0, &slab_fpar, so, cffull, cfempty,
-                                                          status, abort_flag)
-                              : issue_scores128<CS, false>(tmem + kSC, ax, dx, dring0, &slab_fpar, so, cffull, cfempty,
-                                                           status, abort_flag)))
+                    if (!((i & 1) == 0 ? issue_score_pairs128<CS, true>(tmem + kSC, tmem + kX, dx, dring0, &slab_fpar,
+                                                                        so, cffull, cfempty, status, abort_flag)
+                                       : issue_score_pairs128<CS, false>(tmem + kSC, tmem + kX, dx, dring0, &slab_fpar,
+                                                                         so, cffull, cfempty, status, abort_flag)))
                         return false;
                     umma_commit(sfull);
                     umma_commit(&kempty[r % KS]);
@@ -611,28 +754,30 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
             // ---------------- epilogue: one thread per tile row (and per component)
             const int row = epi_row(warp, lane), ew = warp - 2;
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-            float zjob = 0.f;
-            auto x2 = [&](int i) {
+            const float *cg = reinterpret_cast<const float *>(himg + kCoefC);
+            float zacc[4] = {0.f, 0.f, 0.f, 0.f};
+            int zbase = 0;
+            auto x2 = [&](int i) {  // x^2 of tile i, once the previous score MMAs are done (sfull)
                 const int r = rbase + i;
                 if (!wait_or_abort(&kfull[r % KS], (r / KS) & 1, status, abort_flag)) return false;
-                x2_row128(kst + (r % KS) * kTileB, row, tmem + lb + kX0 + 128 * (r & 1));
+                x2_row128(kst + (r % KS) * kTileB, row, tmem + lb + kX);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&xready[r & 1]);
+                if (lane == 0) mbar_arrive(xready);
                 return true;
             };
-            bool ok = x2(0) && wait_or_abort(cfull, njob & 1, status, abort_flag);
+            bool ok = x2(0);
             for (int i = 0; ok && i < n; ++i) {
                 const int r = rbase + i;
-                // x^2 of the next tile (its buffer was read by the score MMAs of tile i - 1)
-                if (i + 1 < n && !(ok = x2(i + 1))) break;
                 if (!(ok = wait_or_abort(sfull, r & 1, status, abort_flag))) break;
                 tc_fence_after();
                 float e[kKC];
-                const float rs = score_exp128(tmem + lb + kSC, cvec, e);
+                const float mx = score_sum256(tmem + lb + kSC, cg, e);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sfree);
+                if (i + 1 < n && !(ok = x2(i + 1))) break;
+                const float rs = exp_row128(e, mx);
                 const int tok = (t0 + i) * kT + row;
                 const float sc = tok < N ? 1.0f / rs : 0.0f;
                 if (r > 0 && !(ok = wait_or_abort(wdone, (r - 1) & 1, status, abort_flag))) break;
@@ -640,23 +785,18 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gready);
-                // key mass of the tile: column sums of the normalised Gamma^K
+                // key mass of the tile: this warp's column sums of the normalised Gamma^K
 #pragma unroll
                 for (int k = 0; k < kKC; ++k) e[k] *= sc;
-                const int base = column_sums_warp(e, lane);
-                // through partial buffer r % 2: it is written again two tiles later, after
-                // every warp has arrived for the tile between, i.e. finished reading it
-                float *zb = zw + (r & 1) * 4 * kKC + ew * kKC;
-                *reinterpret_cast<float4 *>(zb + base) = make_float4(e[0], e[1], e[2], e[3]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&zfull[r & 1]);
-                if (!(ok = wait_or_abort(&zfull[r & 1], (r >> 1) & 1, status, abort_flag))) break;
-                const float *zr = zw + (r & 1) * 4 * kKC;
-                const float zt = ((zr[row] + zr[kKC + row]) + zr[2 * kKC + row]) + zr[3 * kKC + row];
-                if (mode == 1) __stcg(ztile + ((size_t)bh * P.ntiles + t0 + i) * kKC + row, zt);
-                zjob += zt;
+                zbase = column_sums_warp(e, lane);
+                if (mode == 1)
+                    __stcg(reinterpret_cast<float4 *>(ztile + (((size_t)bh * P.ntiles + t0 + i) * 4 + ew) * kKC + zbase),
+                           make_float4(e[0], e[1], e[2], e[3]));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) zacc[q] += e[q];
             }
-            // job end: the memory increment and key mass -> this job's memory slot
+            // job end: the memory increment and key mass -> this job's memory slot; the
+            // warps' key-mass partials meet in the (now idle) Gamma buffer
             if (ok && wait_or_abort(accfull, njob & 1, status, abort_flag)) {
                 tc_fence_after();
                 float *out = part + ((size_t)c * P.slots + slot128(P, c, bh)) * kPartFloats;
@@ -671,8 +811,13 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
                         __stcg(o4 + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
                                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
                 }
-                __stcg(out + kKC * kD + row, zjob);
                 tc_fence_before();
+                float *zw = reinterpret_cast<float *>(gbuf);  // [4 warps][128]
+                *reinterpret_cast<float4 *>(zw + ew * kKC + zbase) = make_float4(zacc[0], zacc[1], zacc[2], zacc[3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(zjob);
+                if (wait_or_abort(zjob, njob & 1, status, abort_flag))
+                    __stcg(out + kKC * kD + row, ((zw[row] + zw[kKC + row]) + zw[2 * kKC + row]) + zw[3 * kKC + row]);
             }
         }
         // ---- the head's last job to finish combines the job memories in job order:
@@ -689,21 +834,7 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
             cta_sync();
             if (*last_flag) {
                 __threadfence();
-                const int cf = first_cta128(P, bh), cl = last_cta128(P, bh);
-                for (int e4 = tid; e4 < kPartFloats / 4; e4 += kThreadsAgg) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int cc = cf; cc <= cl; ++cc) {
-                        float4 *p4 = reinterpret_cast<float4 *>(part + ((size_t)cc * P.slots + slot128(P, cc, bh)) *
-                                                                           kPartFloats) + e4;
-                        const float4 v = __ldcg(p4);
-                        if (mode == 1) __stcg(p4, acc);
-                        acc.x += v.x;
-                        acc.y += v.y;
-                        acc.z += v.z;
-                        acc.w += v.w;
-                    }
-                    if (mode == 0) __stcg(reinterpret_cast<float4 *>(mem + (size_t)bh * kPartFloats) + e4, acc);
-                }
+                combine_jobs128(part, mem, P, bh, mode, tid);
                 if (tid == 0) counters[bh] = 0u;  // ready for the next call
             }
         }
@@ -711,7 +842,6 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
         g += n;
         if (aborted(abort_flag)) break;
     }
-    if (tid == 0 && carm >= 0) mbar_wait(cfull, carm & 1);  // the last c copy has landed
     tc_fence_before();
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -1285,7 +1415,8 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             bool ok = x2q(rbase);
             for (int i = 0; ok && i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                const float zt = __ldcg(ztile + ((size_t)bh * P.ntiles + t0 + i) * kKC + row);
+                const float *zr = ztile + ((size_t)bh * P.ntiles + t0 + i) * 4 * kKC + row;
+                const float zt = ((__ldcg(zr) + __ldcg(zr + kKC)) + __ldcg(zr + 2 * kKC)) + __ldcg(zr + 3 * kKC);
                 if (!wait_or_abort(sq, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
                 x2_row128(kst, row, tmem + lb + kX);
                 tc_fence_before();
@@ -1583,7 +1714,8 @@ bool make_out_map128(CUtensorMap *map, void *base, int BH, int N, bool bf16) {
 
 // Workspace: status | per-head job counters | prep error words | per-head
 // coefficient images | job memories [ctas][slots][kPartFloats] | key mass of
-// every tile [BH][ntiles][128].  The prep clears the status and the counters;
+// every tile [BH][ntiles][4][128] (per-warp partials) | per-head memories
+// [BH][kPartFloats] (bidirectional).  The prep clears the status and the counters;
 // everything else is written before it is read.
 struct Tc128Layout {
     Part128 P;
@@ -1609,8 +1741,8 @@ Tc128Layout tc128_layout(const Problem &p, int splits) {
     off = align256(off + kImgStride * p.H);
     L.part = off;
     off = align256(off + sizeof(float) * (size_t)L.nctas * L.P.slots * kPartFloats);
-    L.ztile = off;
-    off = align256(off + sizeof(float) * (size_t)p.BH() * ntiles * kKC);
+    L.ztile = off;  // key mass of every tile as four per-warp partial rows
+    off = align256(off + sizeof(float) * (size_t)p.BH() * ntiles * 4 * kKC);
     L.mem = off;  // the bidirectional call's per-head memories
     off = align256(off + sizeof(float) * (size_t)p.BH() * kPartFloats);
     L.total = off;
