@@ -54,12 +54,14 @@ def tensor_bytes(t: str, w=WORKLOAD, o_bytes: int = 4) -> int:
     return sum(per[c] for c in t) * w["B"] * w["H"] * w["N"]
 
 
+TC_SOURCES = ("gma_tc.cu", "gma_tc128.cu", "tc_common.cuh", "tc_ptx.cuh")
+
+
 def source_digest() -> str:
     """Digest of the sources of the profiled tensor-core kernels."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", "gma_tc.cu")) +
-                    glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", "tc_ptx.cuh"))):
-        with open(f, "rb") as fh:
+    for name in TC_SOURCES:
+        with open(os.path.join(ROOT, "gaussian_mixture_latent_diag_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -665,6 +667,84 @@ def run_configs(args, rank: int, world: int, local_rank: int):
         print(json.dumps(out), flush=True)
 
 
+SHAPE_METRIC = "GMA fwd tokens*heads/s on a given shape; % of GB300 HBM roofline"
+
+
+def run_shape(args, rank: int, world: int, local_rank: int):
+    """--workload shape: one forward call (--causal 0/1) of the shape given by
+    --shape B,H,N,d_r,d_v,K (bf16 inputs drawn as the configured workloads,
+    fp32 O) on the kernel family the library selects, timed over --steps calls
+    after the warm-up, with the per-stage times of a second pass (stage events
+    between the kernels).  For sizes the five configured workloads do not
+    cover, and for profiling one kernel on a smaller case."""
+    import ctypes
+    import torch
+    import gaussian_mixture_latent_diag_gb300 as gma
+    from gaussian_mixture_latent_diag_gb300 import _native
+    from gaussian_mixture_latent_diag_gb300.synthetic import Case, make_inputs
+
+    B, H, N, d_r, d_v, K = (int(x) for x in args.shape.split(","))
+    causal = int(args.causal)
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    case = Case("shape", bool(causal), B, H, N, d_r, d_v, K, "bf16")
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in make_inputs(case, seed=rank_seed(rank, 9)).items()}
+    path = gma.selected_path(N, d_r, d_v, K, "bf16", causal)
+    ws = torch.empty(max(256, gma.workspace_size(B, H, N, d_r, d_v, K, "bf16", causal)), dtype=torch.uint8, device=dev)
+    O = torch.empty(B, H, N, d_v, device=dev)
+    names = _native.stage_names(path, causal)
+    stream = torch.cuda.current_stream()
+    lib = gma.load()
+    vp = ctypes.c_void_p
+    fn = lib.gma_forward_causal if causal else lib.gma_forward_bidir
+
+    def call(events=None):
+        opt = _native.options(stage_events=events)
+        st = fn(vp(d["Q"].data_ptr()), vp(d["K"].data_ptr()), vp(d["V"].data_ptr()), _native.GMA_BF16,
+                vp(d["mu"].data_ptr()), vp(d["sigma2"].data_ptr()), vp(d["log_pi"].data_ptr()), float(case.eps),
+                vp(O.data_ptr()), B, H, N, d_r, d_v, K, ctypes.byref(opt), vp(ws.data_ptr()), ws.numel(),
+                vp(stream.cuda_stream))
+        if st != 0:
+            raise gma.GmaError(st, "forward")
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    peak, peak_src = measured_peaks()
+    with ClockSampler(local_rank) as clocks:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = job_ms(t0.elapsed_time(t1) / args.steps, world, dev)
+    stage = [0.0] * len(names)
+    reps = min(args.steps, 10)
+    for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        call(ev)
+        torch.cuda.synchronize()
+        for j in range(len(names)):
+            stage[j] += ev[j].elapsed_time(ev[j + 1]) / reps
+    th = B * H * N
+    alg = th * (2 * (2 * d_r + d_v) + 4 * d_v)
+    if rank == 0:
+        out = {"metric": SHAPE_METRIC, "value": world * th / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": f"GMA {'causal' if causal else 'bidirectional'} forward, B={B} H={H} N={N} "
+                                      f"d_r={d_r} d_v={d_v} K={K} bf16, fp32 O (per GPU)",
+                          "parallelism": f"replicas x{world}"},
+               "gpu_launches": len(names) * args.steps, "path": {1: "simt", 2: "tc"}.get(path, str(path)),
+               "stage_ms": dict(zip(names, stage)),
+               "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                            "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "kernel": "whole call",
+                            "algorithmic_bytes": alg, "peak_source": peak_src},
+               "clocks": clocks.summary()}
+        print(json.dumps(out), flush=True)
+
+
 SHARD_METRIC = "GMA per-shard steps of sequence sharding token*heads/s (N=16K, K=64); % of GB300 HBM roofline"
 
 
@@ -1216,14 +1296,16 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="leave out the per-workload timings of the five configured workloads")
     ap.add_argument("--workload", choices=["forward", "backward", "decode", "stats", "params", "project",
-                                           "configs", "shard"],
+                                           "configs", "shard", "shape"],
                     default="forward",
                     help="forward: the bidirectional + causal forward step (default); "
                          "backward: the bidirectional + causal backward; decode: one causal decode "
                          "step over B=2048 x H=8 carried states; stats: the component-usage diagnostics; "
                          "params: the reparameterisation and its gradient; project: the Q/K/V projections; "
                          "configs: each of the five configured workloads; shard: the per-shard steps of "
-                         "sequence sharding")
+                         "sequence sharding; shape: one forward of --shape (B,H,N,d_r,d_v,K) --causal 0/1")
+    ap.add_argument("--shape", default="1,8,32768,128,128,128", help="B,H,N,d_r,d_v,K of --workload shape")
+    ap.add_argument("--causal", type=int, default=1, choices=[0, 1], help="direction of --workload shape")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1251,6 +1333,8 @@ def main():
             run_configs(args, rank, world, local_rank)
         elif args.workload == "shard":
             run_shard(args, rank, world, local_rank)
+        elif args.workload == "shape":
+            run_shape(args, rank, world, local_rank)
         else:
             run_gma(args, rank, world, local_rank)
     finally:
