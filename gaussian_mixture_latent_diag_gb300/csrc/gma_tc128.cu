@@ -853,19 +853,25 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
 // aggregation; the job's carried-in prefix comes from there).  Warps: 0 lane 0
 // Q / K / V tile loads, lane 1 coefficient slabs; 1 lane 0 MMA issue, lane 1
 // the job's prefix; 2..5 query group (query softmax -> Gamma^Q, components
-// 64-127 of the key softmax, P split of key blocks 0 and 1, outputs); 6..9 key
-// group (x^2 of Q and K, components 0-63 of the key softmax, P split of key
-// blocks 2 and 3, state operand).
+// 64-127 of the key softmax, P split of key blocks 0 and 1, outputs, then the
+// next chunk's x^2 of K); 6..9 key group (components 0-63 of the key softmax,
+// P split of key blocks 2 and 3, state operand, then the next chunk's x^2 of Q).
 //
-// The K tile buffer doubles as the output staging: the query warps stage and
-// store a chunk's O there once its MMAs are done, and the next key tile loads
-// after that.
+// The K tile buffer also holds the key softmax's exchange once the key score
+// MMAs are done (the next key tile loads after that), and the V tile buffer the
+// output staging once the state update and P V are done (the next value tile
+// loads once the stores have read it).
 //
 // TMEM (512 columns):
-//   [0, 128)    X: x^2 of Q (hi | lo), then x^2 of K, then [num] (N = 128)
+//   [0, 128)    A: x^2 of Q (hi | lo), then the key scores, then U, then P hi /
+//               lo in place per 32-key block
 //   [128, 256)  query scores, then Gamma^Q hi [128, 192) | lo [192, 256) in place
-//   [256, 384)  key scores, then U, then P hi / lo in place per 32-key block
+//   [256, 384)  B: x^2 of K, then num (N = 128)
 //   [384, 512)  S, the fp32 state (M = 128 components, N = 128 value columns)
+// The x^2 of both sides of the next chunk are prepared while this chunk ends,
+// so the key score MMAs follow the query ones at once (each MMA's accumulator
+// may be a column range an earlier MMA reads as its A operand: a single thread
+// issues them, and issue order is execution order).
 // MMA issue order per chunk: Q scores (40), K scores (40), num = Gamma^Q S (24:
 // hi.hi, hi.lo, lo.hi), U (24), S += Gamma^K^T V (16), num += P V (16).
 //
@@ -1104,9 +1110,9 @@ __device__ __noinline__ bool init_state128(uint8_t *R, int k, uint32_t s_taddr, 
 // (which clip rows past N): fp32 O in two rounds of 64 columns (two boxes of 32
 // rows x 32 columns each, 128-byte swizzle), bf16 O in one round (two boxes of
 // 32 rows x 64 columns).  The whole accumulator row is read first (the second
-// fp32 half into registers), and lane 0 arrives on `xfree`, so the columns can
-// take the next chunk's x^2 while the stores go out; lane 0 issues the stores
-// and waits until they have read the staging slice.
+// fp32 half into registers), and lane 0 arrives on `xfree` (if given), so the
+// columns can take the next tile's operands while the stores go out; lane 0
+// issues the stores and waits until they have read the staging slice.
 __device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t *stage, int lane, int o_bf16,
                                             const CUtensorMap *tmO, int row0, int bh, uint64_t *xfree) {
     const int sw = lane & 7;
@@ -1130,7 +1136,7 @@ __device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(xfree);
+            if (xfree) mbar_arrive(xfree);
             tma_store_3d(tmO, stage, 0, row0, bh);
             tma_store_3d(tmO, stage + 4096, 64, row0, bh);
             bulk_commit();
@@ -1160,7 +1166,7 @@ __device__ __noinline__ void output_rows128(uint32_t o_taddr, float inv, uint8_t
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        mbar_arrive(xfree);
+        if (xfree) mbar_arrive(xfree);
         tma_store_3d(tmO, stage, 0, row0, bh);
         tma_store_3d(tmO, stage + 4096, 32, row0, bh);
         bulk_commit();
@@ -1195,7 +1201,8 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     int N, Part128 P, float eps, int o_bf16, unsigned *status) {
     using L = Causal128Smem;
     constexpr int CS = L::kCS;
-    constexpr int kX = 0, kGQ = 128, kKU = 256, kSA = 384, kTmemCols = 512;
+    // kA: x^2 of Q, then the key scores, U and P; kB: x^2 of K, then num and O
+    constexpr int kA = 0, kGQ = 128, kB = 256, kSA = 384, kTmemCols = 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qst = smem + L::kQ, *kst = smem + L::kK, *vst = smem + L::kV, *R = smem + L::kR, *ring = smem + L::kCf;
@@ -1206,10 +1213,10 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
              *vempty = bars + 5, *cffull = bars + 6, *cfempty = cffull + CS, *xq = cfempty + CS, *xk = xq + 1,
              *sq = xq + 2, *sk = xq + 3, *gq = xq + 4, *gk = xq + 5, *sready = xq + 6, *ndone = xq + 7,
              *ufull = xq + 8, *wdone = xq + 9, *pready = xq + 10, *ofull = xq + 11, *cfull = xq + 12,
-             *xfull = xq + 13, *pread = xq + 14, *kmx = xq + 15, *ksm = xq + 16, *xfree = xq + 17;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfree + 1);
-    int *abort_flag = reinterpret_cast<int *>(xfree + 2);
-    static_assert((6 + 2 * CS + 18) * 8 + 16 <= 512, "barrier area");
+             *xfull = xq + 13, *pread = xq + 14, *kmx = xq + 15, *ksm = xq + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ksm + 1);
+    int *abort_flag = reinterpret_cast<int *>(ksm + 2);
+    static_assert((6 + 2 * CS + 17) * 8 + 16 <= 512, "barrier area");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -1222,7 +1229,8 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     }
     if (tid == 32) {
         for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
-        mbar_init(kempty, 4);  // the K buffer is freed by the query warps once their outputs are out
+        mbar_init(kempty, 8);  // both groups, once the key softmax exchange in the K buffer is done
+        mbar_init(vempty, 4);  // the query warps, once their outputs staged in the V buffer are out
         for (int i = 0; i < CS; ++i) {
             mbar_init(&cffull[i], 1);
             mbar_init(&cfempty[i], 1);
@@ -1231,7 +1239,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
         mbar_init(gq, 4); mbar_init(gk, 8); mbar_init(sready, 4); mbar_init(ndone, 1);
         mbar_init(ufull, 1); mbar_init(wdone, 1); mbar_init(pready, 8); mbar_init(ofull, 1);
         mbar_init(cfull, 1); mbar_init(xfull, 1); mbar_init(pread, 4);
-        mbar_init(kmx, 8); mbar_init(ksm, 8); mbar_init(xfree, 4);
+        mbar_init(kmx, 8); mbar_init(ksm, 8);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
@@ -1314,27 +1322,28 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                     // query scores
                     if (!wait_or_abort(xq, ph, status, abort_flag) || !wait_or_abort(qfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    if (!issue_scores128<CS, true>(tmem + kGQ, tmem + kX, dq0, dring0, &slab_fpar, SlabOrder{i == 0, 0},
+                    if (!issue_scores128<CS, true>(tmem + kGQ, tmem + kA, dq0, dring0, &slab_fpar, SlabOrder{i == 0, 0},
                                                    cffull, cfempty, status, abort_flag))
                         break;
                     umma_commit(sq);
                     umma_commit(qempty);
-                    // key scores
+                    // key scores, into the x^2 columns of Q that the query scores read (issue order
+                    // is execution order), from the x^2 of K prepared during the previous chunk
                     if (!wait_or_abort(xk, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    if (!issue_scores128<CS, false>(tmem + kKU, tmem + kX, dk0, dring0, &slab_fpar,
+                    if (!issue_scores128<CS, false>(tmem + kA, tmem + kB, dk0, dring0, &slab_fpar,
                                                     SlabOrder{0, i == n - 1}, cffull, cfempty, status, abort_flag))
                         break;
                     umma_commit(sk);
                     // num = Gamma^Q S (hi.hi, hi.lo, lo.hi)
                     if (!wait_or_abort(gq, ph, status, abort_flag) || !wait_or_abort(sready, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    issue_num128(tmem + kX, tmem + kGQ, dS);
+                    issue_num128(tmem + kB, tmem + kGQ, dS);
                     umma_commit(ndone);
                     // U = Gamma^Q Gamma^K^T
                     if (!wait_or_abort(gk, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    issue_u128(tmem + kKU, tmem + kGQ, dG);
+                    issue_u128(tmem + kA, tmem + kGQ, dG);
                     umma_commit(ufull);
                     // S += Gamma^K^T V (hi, lo)
                     if (!wait_or_abort(vfull, ph, status, abort_flag)) break;
@@ -1344,21 +1353,30 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                     // num += P V (P hi / lo in place in the U columns)
                     if (!wait_or_abort(pready, ph, status, abort_flag)) break;
                     tc_fence_after();
-                    issue_pv128(tmem + kX, tmem + kKU, dV);
+                    issue_pv128(tmem + kB, tmem + kA, dV);
                     umma_commit(ofull);
-                    umma_commit(vempty);
                 }
             }
         } else if (warp < 6) {
-            // ---------------- query group
+            // ---------------- query group: query softmax, half of the key softmax, half of
+            // the P split, the outputs, and the next chunk's x^2 of K
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             float *xb = reinterpret_cast<float *>(kst);  // key softmax exchange (the K tile is consumed)
-            for (int i = 0; i < n; ++i) {
+            auto x2k = [&](int r) {  // x^2 of the key tile of chunk r, into the kB columns
+                if (!wait_or_abort(kfull, r & 1, status, abort_flag)) return false;
+                x2_row128(kst, row, tmem + lb + kB);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xk);
+                return true;
+            };
+            bool ok = x2k(rbase);
+            for (int i = 0; ok && i < n; ++i) {
                 const int r = rbase + i, ph = r & 1;
-                if (!wait_or_abort(sq, ph, status, abort_flag)) break;
-                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;  // c_k visible
-                if (!wait_or_abort(sready, ph, status, abort_flag)) break;                 // key mass Zp visible
+                if (!(ok = wait_or_abort(sq, ph, status, abort_flag))) break;
+                if (i == 0 && !(ok = wait_or_abort(cfull, njob & 1, status, abort_flag))) break;  // c_k visible
+                if (!(ok = wait_or_abort(sready, ph, status, abort_flag))) break;                 // key mass Zp visible
                 tc_fence_after();
                 float den0;
                 const float rq = query_row128(tmem + lb + kGQ, cvec, zp, &den0);
@@ -1366,39 +1384,44 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gq);
                 // components 64 .. 127 of the key softmax
-                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
+                if (!(ok = wait_or_abort(sk, ph, status, abort_flag))) break;
                 tc_fence_after();
-                if (!key_half128(tmem + lb + kKU, cvec, 1, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone, ph,
-                                 status, abort_flag))
+                if (!(ok = key_half128(tmem + lb + kA, cvec, 1, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone,
+                                       ph, status, abort_flag)))
                     break;
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(gk);
-                if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
+                if (lane == 0) {
+                    mbar_arrive(gk);
+                    mbar_arrive(kempty);  // this warp is done with the exchange in the K buffer
+                }
+                if (!(ok = wait_or_abort(ufull, ph, status, abort_flag))) break;
                 tc_fence_after();
-                const float rs0 = split_p_blocks128(tmem + lb + kKU, 0, row);
+                const float rs0 = split_p_blocks128(tmem + lb + kA, 0, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
-                if (!wait_or_abort(ofull, ph, status, abort_flag)) break;
-                if (!wait_or_abort(pready, ph, status, abort_flag)) break;  // the key group's row sums
+                if (!(ok = wait_or_abort(ofull, ph, status, abort_flag))) break;
+                if (!(ok = wait_or_abort(pready, ph, status, abort_flag))) break;  // the key group's row sums
                 tc_fence_after();
-                // outputs staged in the K tile buffer (the key score MMAs, its last readers,
-                // are complete: ofull), which the next key tile may then reuse
-                output_rows128(tmem + lb + kX, 1.0f / (den0 + (rs0 + rsk[row]) + eps * rq), kst + (warp & 3) * 8192,
-                               lane, o_bf16, &tmO, (t0 + i) * kT + 32 * (warp & 3), bh, xfree);
+                // outputs staged in the V tile buffer (the state update and P V, its last
+                // readers, are complete: ofull), which the next value tile may then reuse
+                output_rows128(tmem + lb + kB, 1.0f / (den0 + (rs0 + rsk[row]) + eps * rq), vst + (warp & 3) * 8192,
+                               lane, o_bf16, &tmO, (t0 + i) * kT + 32 * (warp & 3), bh, nullptr);
                 tc_fence_before();
-                if (lane == 0) mbar_arrive(kempty);
+                if (lane == 0) mbar_arrive(vempty);
+                // the next chunk's x^2 of K, now that this chunk's outputs are out of kB
+                if (i + 1 < n && !(ok = x2k(r + 1))) break;
             }
         } else {
-            // ---------------- key group: x^2 of both sides, half of the key softmax, half of
-            // the P split, the state operand
+            // ---------------- key group: the next chunk's x^2 of Q, half of the key softmax,
+            // half of the P split, the state operand
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             float *xb = reinterpret_cast<float *>(kst);
-            auto x2q = [&](int r) {  // x^2 of the query tile of chunk r
+            auto x2q = [&](int r) {  // x^2 of the query tile of chunk r, into the kA columns
                 if (!wait_or_abort(qfull, r & 1, status, abort_flag)) return false;
-                x2_row128(qst, row, tmem + lb + kX);
+                x2_row128(qst, row, tmem + lb + kA);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xq);
@@ -1417,31 +1440,28 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 const int r = rbase + i, ph = r & 1;
                 const float *zr = ztile + ((size_t)bh * P.ntiles + t0 + i) * 4 * kKC + row;
                 const float zt = ((__ldcg(zr) + __ldcg(zr + kKC)) + __ldcg(zr + 2 * kKC)) + __ldcg(zr + 3 * kKC);
-                if (!wait_or_abort(sq, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
-                x2_row128(kst, row, tmem + lb + kX);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xk);
-                if (!wait_or_abort(sk, ph, status, abort_flag)) break;
-                if (i == 0 && !wait_or_abort(cfull, njob & 1, status, abort_flag)) break;
+                if (!(ok = wait_or_abort(sk, ph, status, abort_flag))) break;
+                if (i == 0 && !(ok = wait_or_abort(cfull, njob & 1, status, abort_flag))) break;
                 tc_fence_after();
                 // components 0 .. 63 of the key softmax; Gamma^K into R once num has read S
-                if (!key_half128(tmem + lb + kKU, cvec, 0, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone, ph,
-                                 status, abort_flag))
+                if (!(ok = key_half128(tmem + lb + kA, cvec, 0, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone,
+                                       ph, status, abort_flag)))
                     break;
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(gk);
-                if (!wait_or_abort(ufull, ph, status, abort_flag)) break;
+                if (lane == 0) {
+                    mbar_arrive(gk);
+                    mbar_arrive(kempty);
+                }
+                if (!(ok = wait_or_abort(ufull, ph, status, abort_flag))) break;
                 tc_fence_after();
-                rsk[row] = split_p_blocks128(tmem + lb + kKU, 2, row);
+                rsk[row] = split_p_blocks128(tmem + lb + kA, 2, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pready);
                 // the next chunk's state operand and key mass, once U and the state
-                // update have read Gamma^K; then its query x^2, once this chunk's
-                // outputs are out of the X columns
-                if (!wait_or_abort(wdone, ph, status, abort_flag)) break;
+                // update have read Gamma^K; then its x^2 of Q, once P V has read P (kA)
+                if (!(ok = wait_or_abort(wdone, ph, status, abort_flag))) break;
                 tc_fence_after();
                 if (i + 1 < n) {
                     state_operand128(tmem + lb + kSA, R, row);
@@ -1450,7 +1470,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sready);
-                    if (!wait_or_abort(xfree, ph, status, abort_flag)) break;
+                    if (!(ok = wait_or_abort(ofull, ph, status, abort_flag))) break;
                     tc_fence_after();
                     if (!(ok = x2q(r + 1))) break;
                 }
