@@ -852,13 +852,13 @@ __global__ void __launch_bounds__(kThreadsAgg, 1) tc128_aggregate_kernel(
 // One 128-token chunk at a time per CTA (its tile range, as in the
 // aggregation; the job's carried-in prefix comes from there).  Warps: 0 lane 0
 // Q / K / V tile loads, lane 1 coefficient slabs; 1 lane 0 MMA issue, lane 1
-// the job's prefix; 2..5 query group (query softmax -> Gamma^Q, components
-// 64-127 of the key softmax, P split of key blocks 0 and 1, outputs, then the
-// next chunk's x^2 of K); 6..9 key group (components 0-63 of the key softmax,
-// P split of key blocks 2 and 3, state operand, then the next chunk's x^2 of Q).
+// the job's prefix; 2..5 query group (components 64-127 of the query and of
+// the key softmax, P split of key blocks 0 and 1, outputs, then the next
+// chunk's x^2 of K); 6..9 key group (components 0-63 of both softmaxes, P split
+// of key blocks 2 and 3, state operand, then the next chunk's x^2 of Q).
 //
-// The K tile buffer also holds the key softmax's exchange once the key score
-// MMAs are done (the next key tile loads after that), and the V tile buffer the
+// The Q and K tile buffers also hold the query and key softmaxes' exchanges once
+// their score MMAs are done (the next tiles load after that), and the V tile buffer the
 // output staging once the state update and P V are done (the next value tile
 // loads once the stores have read it).
 //
@@ -961,6 +961,96 @@ __device__ __noinline__ float query_row128(uint32_t s_taddr, const float *cvec, 
     }
     tmem_wait_st();
     return r;
+}
+
+// Query softmax of half `hf` of one row (components 64 hf .. 64 hf + 63), run by
+// the threads of both warp groups that own the row: Gamma^Q = e (un-normalised)
+// as bf16 hi | lo in place of the scores -- hi words of the half's components at
+// s_taddr + 32 hf, lo words at s_taddr + 64 + 32 hf, written only once both
+// halves have read their scores.  The halves' maxima, then their row sums and
+// e . Zp sums, meet in xb ([max | sum | e.Zp][half][128] fp32) through the
+// mbarriers mx and ms (8 warps each, phase ph).  Returns false on a timeout;
+// *r and *den0 get the whole row's sums (half 0 + half 1).
+__device__ __noinline__ bool query_half128(uint32_t s_taddr, const float *cvec, const float *zp, int hf, int row,
+                                           float *xb, uint64_t *mx, uint64_t *ms, uint32_t ph, float *r,
+                                           float *den0, unsigned *status, int *abort_flag) {
+    float e[64];
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint32_t v[32];
+        tmem_ld32(s_taddr + 64 * hf + 32 * q, v);
+        tmem_wait_ld();
+        const float4 *c4 = reinterpret_cast<const float4 *>(cvec + 64 * hf + 32 * q);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 c = c4[i];
+            const float2 a = f2_add(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                                    make_float2(c.x, c.y));
+            const float2 b = f2_add(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                                    make_float2(c.z, c.w));
+            e[32 * q + 4 * i] = a.x;
+            e[32 * q + 4 * i + 1] = a.y;
+            e[32 * q + 4 * i + 2] = b.x;
+            e[32 * q + 4 * i + 3] = b.y;
+            m = fmaxf(m, fmaxf(fmaxf(a.x, a.y), fmaxf(b.x, b.y)));
+        }
+    }
+    tc_fence_before();
+    const int lane = threadIdx.x & 31;
+    xb[hf * kT + row] = m;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(mx);
+    if (!wait_or_abort(mx, ph, status, abort_flag)) return false;  // both halves' scores are read
+    tc_fence_after();
+    const float2 mm = make_float2(fmaxf(xb[row], xb[kT + row]), fmaxf(xb[row], xb[kT + row]));
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+    float d0 = 0.f, d1 = 0.f;
+    const float *zh = zp + 64 * hf;
+#pragma unroll
+    for (int k = 0; k < 64; k += 4) {
+        const float2 x0 = f2_sub(make_float2(e[k], e[k + 1]), mm), x1 = f2_sub(make_float2(e[k + 2], e[k + 3]), mm);
+        e[k] = ex2(x0.x);
+        e[k + 1] = ex2(x0.y);
+        e[k + 2] = ex2(x1.x);
+        e[k + 3] = ex2(x1.y);
+        s0 = f2_add(s0, make_float2(e[k], e[k + 1]));
+        s1 = f2_add(s1, make_float2(e[k + 2], e[k + 3]));
+        d0 = fmaf(e[k], zh[k], d0);
+        d1 = fmaf(e[k + 1], zh[k + 1], d1);
+        d0 = fmaf(e[k + 2], zh[k + 2], d0);
+        d1 = fmaf(e[k + 3], zh[k + 3], d1);
+    }
+#pragma unroll
+    for (int w4 = 0; w4 < 2; ++w4) {  // components 64 hf + 32 w4 .. + 31
+        uint32_t h[16], l[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint32_t hh[4], ll[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = e[32 * w4 + 8 * u + 2 * q], b = e[32 * w4 + 8 * u + 2 * q + 1];
+                hh[q] = pack_bf2(a, b);
+                ll[q] = pack_bf2(a - bf_lo(hh[q]), b - bf_hi(hh[q]));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                h[4 * u + q] = hh[q];
+                l[4 * u + q] = ll[q];
+            }
+        }
+        tmem_st16(s_taddr + 32 * hf + 16 * w4, h);
+        tmem_st16(s_taddr + 64 + 32 * hf + 16 * w4, l);
+    }
+    tmem_wait_st();
+    xb[2 * kT + hf * kT + row] = (s0.x + s0.y) + (s1.x + s1.y);
+    xb[4 * kT + hf * kT + row] = d0 + d1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ms);
+    if (!wait_or_abort(ms, ph, status, abort_flag)) return false;
+    *r = xb[2 * kT + row] + xb[3 * kT + row];
+    *den0 = xb[4 * kT + row] + xb[5 * kT + row];
+    return true;
 }
 
 // Key softmax of half `hf` of one row (components 64 hf .. 64 hf + 63), run by
@@ -1213,10 +1303,11 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
              *vempty = bars + 5, *cffull = bars + 6, *cfempty = cffull + CS, *xq = cfempty + CS, *xk = xq + 1,
              *sq = xq + 2, *sk = xq + 3, *gq = xq + 4, *gk = xq + 5, *sready = xq + 6, *ndone = xq + 7,
              *ufull = xq + 8, *wdone = xq + 9, *pready = xq + 10, *ofull = xq + 11, *cfull = xq + 12,
-             *xfull = xq + 13, *pread = xq + 14, *kmx = xq + 15, *ksm = xq + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ksm + 1);
-    int *abort_flag = reinterpret_cast<int *>(ksm + 2);
-    static_assert((6 + 2 * CS + 17) * 8 + 16 <= 512, "barrier area");
+             *xfull = xq + 13, *pread = xq + 14, *kmx = xq + 15, *ksm = xq + 16, *qmx = xq + 17,
+             *qsm = xq + 18;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qsm + 1);
+    int *abort_flag = reinterpret_cast<int *>(qsm + 2);
+    static_assert((6 + 2 * CS + 19) * 8 + 16 <= 512, "barrier area");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -1229,6 +1320,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
     }
     if (tid == 32) {
         for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+        mbar_init(qempty, 8);  // both groups, once the query softmax exchange in the Q buffer is done
         mbar_init(kempty, 8);  // both groups, once the key softmax exchange in the K buffer is done
         mbar_init(vempty, 4);  // the query warps, once their outputs staged in the V buffer are out
         for (int i = 0; i < CS; ++i) {
@@ -1236,10 +1328,10 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             mbar_init(&cfempty[i], 1);
         }
         mbar_init(xq, 4); mbar_init(xk, 4); mbar_init(sq, 1); mbar_init(sk, 1);
-        mbar_init(gq, 4); mbar_init(gk, 8); mbar_init(sready, 4); mbar_init(ndone, 1);
+        mbar_init(gq, 8); mbar_init(gk, 8); mbar_init(sready, 4); mbar_init(ndone, 1);
         mbar_init(ufull, 1); mbar_init(wdone, 1); mbar_init(pready, 8); mbar_init(ofull, 1);
         mbar_init(cfull, 1); mbar_init(xfull, 1); mbar_init(pread, 4);
-        mbar_init(kmx, 8); mbar_init(ksm, 8);
+        mbar_init(kmx, 8); mbar_init(ksm, 8); mbar_init(qmx, 8); mbar_init(qsm, 8);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmO);
@@ -1326,7 +1418,6 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                                                    cffull, cfempty, status, abort_flag))
                         break;
                     umma_commit(sq);
-                    umma_commit(qempty);
                     // key scores, into the x^2 columns of Q that the query scores read (issue order
                     // is execution order), from the x^2 of K prepared during the previous chunk
                     if (!wait_or_abort(xk, ph, status, abort_flag) || !wait_or_abort(kfull, ph, status, abort_flag)) break;
@@ -1363,6 +1454,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             float *xb = reinterpret_cast<float *>(kst);  // key softmax exchange (the K tile is consumed)
+            float *xq_b = reinterpret_cast<float *>(qst);  // query softmax exchange (the Q tile is consumed)
             auto x2k = [&](int r) {  // x^2 of the key tile of chunk r, into the kB columns
                 if (!wait_or_abort(kfull, r & 1, status, abort_flag)) return false;
                 x2_row128(kst, row, tmem + lb + kB);
@@ -1378,11 +1470,18 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 if (i == 0 && !(ok = wait_or_abort(cfull, njob & 1, status, abort_flag))) break;  // c_k visible
                 if (!(ok = wait_or_abort(sready, ph, status, abort_flag))) break;                 // key mass Zp visible
                 tc_fence_after();
-                float den0;
-                const float rq = query_row128(tmem + lb + kGQ, cvec, zp, &den0);
+                // components 64 .. 127 of the query softmax (exchange in the consumed Q tile)
+                float rq, den0;
+                if (!(ok = query_half128(tmem + lb + kGQ, cvec, zp, 1, row, xq_b, qmx, qsm, ph, &rq, &den0, status,
+                                         abort_flag)))
+                    break;
+                fence_proxy_async_smem();  // the exchange's writes, before the next Q tile lands there
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(gq);
+                if (lane == 0) {
+                    mbar_arrive(gq);
+                    mbar_arrive(qempty);
+                }
                 // components 64 .. 127 of the key softmax
                 if (!(ok = wait_or_abort(sk, ph, status, abort_flag))) break;
                 tc_fence_after();
@@ -1419,6 +1518,7 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
             const int row = epi_row(warp, lane);
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             float *xb = reinterpret_cast<float *>(kst);
+            float *xq_b = reinterpret_cast<float *>(qst);
             auto x2q = [&](int r) {  // x^2 of the query tile of chunk r, into the kA columns
                 if (!wait_or_abort(qfull, r & 1, status, abort_flag)) return false;
                 x2_row128(qst, row, tmem + lb + kA);
@@ -1440,8 +1540,25 @@ __global__ void __launch_bounds__(kThreadsC128, 1) tc128_causal_kernel(
                 const int r = rbase + i, ph = r & 1;
                 const float *zr = ztile + ((size_t)bh * P.ntiles + t0 + i) * 4 * kKC + row;
                 const float zt = ((__ldcg(zr) + __ldcg(zr + kKC)) + __ldcg(zr + 2 * kKC)) + __ldcg(zr + 3 * kKC);
+                // components 0 .. 63 of the query softmax
+                if (!(ok = wait_or_abort(sq, ph, status, abort_flag))) break;
+                if (i == 0 && !(ok = wait_or_abort(cfull, njob & 1, status, abort_flag))) break;  // c_k visible
+                if (!(ok = wait_or_abort(sready, ph, status, abort_flag))) break;                 // every Zp row
+                tc_fence_after();
+                {
+                    float rq_, den0_;
+                    if (!(ok = query_half128(tmem + lb + kGQ, cvec, zp, 0, row, xq_b, qmx, qsm, ph, &rq_, &den0_,
+                                             status, abort_flag)))
+                        break;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(gq);
+                    mbar_arrive(qempty);
+                }
                 if (!(ok = wait_or_abort(sk, ph, status, abort_flag))) break;
-                if (i == 0 && !(ok = wait_or_abort(cfull, njob & 1, status, abort_flag))) break;
                 tc_fence_after();
                 // components 0 .. 63 of the key softmax; Gamma^K into R once num has read S
                 if (!(ok = key_half128(tmem + lb + kA, cvec, 0, (t0 + i) * kT + row < N, R, row, xb, kmx, ksm, ndone,
