@@ -236,20 +236,28 @@ __device__ __noinline__ bool issue_scores128(uint32_t d, uint32_t ax, uint64_t d
     return true;
 }
 
+// Position p of a forward side takes unit unit_at<PAIRS>(p) of the image.  Slabs
+// go in image order.  The four 32 KB pairs go as [b ; a] of column half 0, then
+// [a ; b] of half 1 ([b_hi ; b_lo] = 4 MMAs, [a_hi ; a_lo] = 8): with two slots,
+// each fresh load of a side then follows an 8-MMA pair (in image order one of
+// them would follow a 4-MMA pair, half the time to hide its load).
+template <bool PAIRS>
+__device__ __forceinline__ int unit_at(int p) { return PAIRS ? (p < 2 ? 1 - p : p) : p; }
+
 // Producer side of the slab schedule: the loads of one side (all NU units for
 // the first side of a job, else the NU - NS the previous side did not leave in
 // the ring), each once the slot's previous load has had its last use.  A unit
 // is UB bytes of the coefficient image (a slab, or a pair of adjacent slabs);
-// unit u always goes to slot u % NS.  Bit `slot` of *lpar is the parity of the
-// slot's load count; bit `slot` of *lmask is set once the slot has been loaded.
-// Returns false on a timeout.
+// the unit at position p (unit_at) always goes to slot p % NS.  Bit `slot` of
+// *lpar is the parity of the slot's load count; bit `slot` of *lmask is set once
+// the slot has been loaded.  Returns false on a timeout.
 template <int NS, int NU, int UB>
 __device__ __forceinline__ bool load_units128(uint8_t *ring, const uint8_t *himg, int fwd, int first, uint32_t *lpar,
                                               uint32_t *lmask, uint64_t *full, uint64_t *empty, unsigned *status,
                                               int *abort_flag) {
     uint32_t lp = *lpar;
     for (int k = first ? 0 : NS; k < NU; ++k) {
-        const int u = fwd ? k : NU - 1 - k, slot = u % NS;
+        const int pos = fwd ? k : NU - 1 - k, u = unit_at<(UB > kSlab)>(pos), slot = pos % NS;
         if (!wait_or_abort(&empty[slot], ((lp >> slot) & 1u) ^ 1u, status, abort_flag)) return false;
         lp ^= 1u << slot;
         *lmask |= 1u << slot;
@@ -281,7 +289,8 @@ __device__ __forceinline__ void drain_slabs128(uint32_t lpar, uint32_t lmask, ui
 // 128 components' hi parts, then their lo parts) -- and per K step
 //   D[:, 0:256] += x2hi [a_hi | a_lo],  D[:, 0:128] += x2lo a_hi,  D[:, 0:256] += x [b_hi | b_lo];
 // the score of component k is D[:, k] + D[:, 128 + k] (+ c_k).  Pairs in the
-// snake order of issue_scores128 (unit u in slot u % NS).
+// snake order of issue_scores128, in the order of unit_at<true> (the pair at
+// position p in slot p % NS).
 template <int NS, bool FWD>
 __device__ __noinline__ bool issue_score_pairs128(uint32_t d, uint32_t ax, uint64_t dx0, uint64_t dring0,
                                                   uint32_t *fpar, SlabOrder so, uint64_t *full, uint64_t *empty,
@@ -292,7 +301,7 @@ __device__ __noinline__ bool issue_score_pairs128(uint32_t d, uint32_t ax, uint6
     uint32_t fp = *fpar;
 #pragma unroll
     for (int k = 0; k < NU; ++k) {
-        const int u = FWD ? k : NU - 1 - k, slot = u % NS, hf = u >> 1;
+        const int pos = FWD ? k : NU - 1 - k, u = unit_at<true>(pos), slot = pos % NS, hf = u >> 1;
         const bool a_pair = (u & 1) == 0;
         if (so.first || k >= NS) {  // a fresh load
             if (!mbar_wait(&full[slot], (fp >> slot) & 1u)) {
