@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -143,19 +144,37 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
 constexpr int kNG = 2;                       // epilogue groups (tiles in flight)
 constexpr int kThreadsG = 64 + 128 * kNG;    // TMA warp, MMA warp, NG x 4 epilogue warps
 
+// The tiles in (head, tile) order cut into one contiguous range per CTA: CTA c
+// takes [start[c], start[c + 1]).  The cuts balance the CTAs' time, not their
+// tile counts: a range that crosses a head boundary pays a job end and a job
+// start (the accumulator drained, the next head's coefficients and first tiles
+// loaded behind a CTA-wide barrier), about kSwitchTiles tiles of work, so such
+// a range gets that many fewer tiles (part_cuts).
+constexpr int kMaxPartCtas = 320;
+constexpr int kSwitchTiles = 4;
 struct Part {
     int ntiles;  // tiles per head
     int total;   // B*H*ntiles
-    int tpc;     // tiles per CTA
+    int nctas;   // ranges (CTAs)
     int slots;   // partial slots per CTA (jobs per CTA, upper bound)
+    int start[kMaxPartCtas + 1];
 };
 
-__host__ __device__ inline int first_cta_of_head(const Part &P, int bh) { return (bh * P.ntiles) / P.tpc; }
-__host__ __device__ inline int last_cta_of_head(const Part &P, int bh) {
-    return ((bh + 1) * P.ntiles - 1) / P.tpc;
+// CTA whose range holds tile x (ranges are non-empty and in order).
+__host__ __device__ inline int cta_of_tile(const Part &P, int x) {
+    int lo = 0, hi = P.nctas - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.start[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
-// Slot of head bh's job inside CTA c (CTA c's range starts in head (c*tpc)/ntiles).
-__host__ __device__ inline int slot_of(const Part &P, int c, int bh) { return bh - (c * P.tpc) / P.ntiles; }
+__host__ __device__ inline int first_cta_of_head(const Part &P, int bh) { return cta_of_tile(P, bh * P.ntiles); }
+__host__ __device__ inline int last_cta_of_head(const Part &P, int bh) {
+    return cta_of_tile(P, (bh + 1) * P.ntiles - 1);
+}
+// Slot of head bh's job inside CTA c (CTA c's range starts in head start[c] / ntiles).
+__host__ __device__ inline int slot_of(const Part &P, int c, int bh) { return bh - P.start[c] / P.ntiles; }
 
 
 // Parameter-error check of the first persistent kernel of a call, by one
@@ -430,7 +449,7 @@ struct Write2Smem {
 // [128 NG + 64 g, +64); accumulator [Vt | Z] (N = 80) at 192 NG.
 __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-    const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, Part P,
+    const uint8_t *__restrict__ coef_img, const unsigned *__restrict__ head_err, int H, int N, const __grid_constant__ Part P,
     float *__restrict__ part, unsigned *__restrict__ counters, uint8_t *__restrict__ mem_img, size_t mem_img_stride,
     uint8_t *__restrict__ gk_out, int mode, int stall, CombineIO io, unsigned *status) {
     using L = Write2Smem;
@@ -454,7 +473,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_write2_kernel(
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
-    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    const int g0 = P.start[c], gend = P.start[c + 1];
     if (g0 >= gend) return;
 
     if (warp == 0) {
@@ -856,7 +875,7 @@ __device__ __forceinline__ void stage_and_store_half(uint8_t *stage, const float
 
 __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
-    const uint8_t *__restrict__ coef_img, int H, int N, Part P,
+    const uint8_t *__restrict__ coef_img, int H, int N, const __grid_constant__ Part P,
     const uint8_t *__restrict__ mem_img, size_t mem_img_stride, float eps, int o_bf16, unsigned *status) {
     using L = Read3Smem;
     constexpr int NB = L::NB, QS = L::kQS;
@@ -877,7 +896,7 @@ __global__ void __launch_bounds__(kThreadsR, 1) tc_read3_kernel(
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
-    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    const int g0 = P.start[c], gend = P.start[c + 1];
     if (failed(status) || g0 >= gend) return;
 
     if (warp == 0) {
@@ -1356,7 +1375,7 @@ __device__ __noinline__ void state_operand(uint8_t *gb, const float *S, int t) {
 __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
     const __grid_constant__ CUtensorMap tmO, const uint8_t *__restrict__ coef_img, const uint8_t *__restrict__ gk_in,
-    const float *__restrict__ prefix, int H, int N, Part P, float eps, int o_bf16, unsigned *status) {
+    const float *__restrict__ prefix, int H, int N, const __grid_constant__ Part P, float eps, int o_bf16, unsigned *status) {
     using L = Causal2Smem;
     constexpr int W = L::W, QS = L::kQS, VS = L::kVS;
     constexpr int kTmemCols = 512;
@@ -1379,7 +1398,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) tc_causal2_kernel(
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
-    const int g0 = c * P.tpc, gend = min(P.total, g0 + P.tpc);
+    const int g0 = P.start[c], gend = P.start[c + 1];
     if (failed(status) || g0 >= gend) return;
 
     if (warp == 0) {
@@ -2461,15 +2480,63 @@ struct TcLayout2 {
     size_t counters = 0, head_err = 0, coef = 0, part = 0, mem = 0, mem_stride = 0, gk = 0, total = 0;
 };
 
+// End of the range that starts at tile a when a range may cost m (tiles, plus
+// kSwitchTiles per head boundary crossed); at least one tile.
+int range_end(int a, int ntiles, int total, long long m) {
+    int b = a;
+    long long left = m;
+    while (b < total) {
+        const int head_end = (b / ntiles + 1) * ntiles;
+        if (b > a && b % ntiles == 0) {  // entering a new head
+            if (left <= kSwitchTiles) break;
+            left -= kSwitchTiles;
+        }
+        const long long take = std::min<long long>(left, head_end - b);
+        b += (int)take;
+        left -= take;
+        if (left <= 0) break;
+    }
+    return b > a ? b : a + 1;
+}
+
+// Cuts with the smallest largest range cost that needs at most nct ranges
+// (binary search on the cost, greedy ranges); the slot count is the largest
+// number of heads a range touches.
+void part_cuts(Part *P, int ntiles, int total, int nct) {
+    P->ntiles = ntiles;
+    P->total = total;
+    const long long heads = (total + ntiles - 1) / ntiles;
+    long long lo = (total + nct - 1) / nct, hi = total + kSwitchTiles * heads;
+    auto count = [&](long long m) {
+        int n = 0;
+        for (int a = 0; a < total; a = range_end(a, ntiles, total, m)) ++n;
+        return n;
+    };
+    while (lo < hi) {
+        const long long mid = (lo + hi) / 2;
+        if (count(mid) <= nct) hi = mid; else lo = mid + 1;
+    }
+    int n = 0, slots = 1;
+    for (int a = 0; a < total;) {
+        const int b = range_end(a, ntiles, total, lo);
+        P->start[n++] = a;
+        slots = std::max(slots, (b - 1) / ntiles - a / ntiles + 1);
+        a = b;
+    }
+    P->start[n] = total;
+    P->nctas = n;
+    P->slots = slots;
+}
+
 TcLayout2 tc_layout2(const Problem &p, int splits, int causal) {
     TcLayout2 L;
     const int ntiles = (p.N + kTile - 1) / kTile;
     const int total = p.BH() * ntiles;
     int nct = splits > 0 ? splits : num_sms();
     nct = nct < 1 ? 1 : (nct > total ? total : nct);
-    const int tpc = (total + nct - 1) / nct;
-    L.nctas = (total + tpc - 1) / tpc;
-    L.P = Part{ntiles, total, tpc, tpc / ntiles + 2};
+    nct = nct > kMaxPartCtas ? kMaxPartCtas : nct;
+    part_cuts(&L.P, ntiles, total, nct);
+    L.nctas = L.P.nctas;
     size_t off = kStatusBytes;
     L.counters = off;
     off = align256(off + sizeof(unsigned) * (size_t)p.BH());
