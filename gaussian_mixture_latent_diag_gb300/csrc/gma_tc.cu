@@ -72,11 +72,6 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
                                                            unsigned *head_err, unsigned *counters, int BH) {
     const int tid = threadIdx.x, h = blockIdx.y;
     const int gt = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + tid;
-    // The previous call's kernels may still read the status, counters and images.
-    pdl_wait();
-    pdl_trigger();
-    if (gt == 0) *status = 0u;
-    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     uint8_t *coef = img + (size_t)h * kCoefStride;
     const int k = blockIdx.x * 8 + (tid >> 4), j = (tid & 15) * 4;
     const bool realk = k < K;
@@ -111,16 +106,23 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
     }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) det += __shfl_xor_sync(0xffffffffu, det, o);
+    if (j == 0 && realk && !isfinite(lp)) bad = true;
+    const int any = __syncthreads_or(bad ? 1 : 0);
+    // Everything above only reads the parameters; the previous call's kernels may
+    // still read the status, counters and images written below.  The next kernel
+    // launches after the wait (launching it earlier, while the previous kernel's
+    // CTAs drain, placed its CTAs on SMs in the order they freed and measured
+    // slower).
+    pdl_wait();
+    pdl_trigger();
+    if (gt == 0) *status = 0u;
+    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     const uint32_t off = sw128_offset(k, j, 1024);  // 8-byte aligned (j % 4 == 0)
     *reinterpret_cast<uint2 *>(coef + off) = make_uint2(ah[0], ah[1]);
     *reinterpret_cast<uint2 *>(coef + kCoefMatBytes + off) = make_uint2(al[0], al[1]);
     *reinterpret_cast<uint2 *>(coef + 2 * kCoefMatBytes + off) = make_uint2(bh[0], bh[1]);
     *reinterpret_cast<uint2 *>(coef + 3 * kCoefMatBytes + off) = make_uint2(bl[0], bl[1]);
-    if (j == 0) {
-        if (realk && !isfinite(lp)) bad = true;
-        reinterpret_cast<float *>(coef + 4 * kCoefMatBytes)[k] = realk ? kLog2e * (lp - 0.5f * det) : -INFINITY;
-    }
-    const int any = __syncthreads_or(bad ? 1 : 0);
+    if (j == 0) reinterpret_cast<float *>(coef + 4 * kCoefMatBytes)[k] = realk ? kLog2e * (lp - 0.5f * det) : -INFINITY;
     if (tid == 0) head_err[h * kPrepBlocks + blockIdx.x] = any ? (unsigned)GMA_ERR_NONFINITE_PARAM : 0u;
 }
 

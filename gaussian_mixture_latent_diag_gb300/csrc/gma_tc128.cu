@@ -78,10 +78,6 @@ __global__ void __launch_bounds__(128) tc128_prep_kernel(const float *__restrict
                                                          unsigned *head_err, unsigned *counters, int BH) {
     const int tid = threadIdx.x, h = blockIdx.y;
     const int gt = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + tid;
-    pdl_wait();  // the previous call's kernels may still read the status, counters and images
-    pdl_trigger();
-    if (gt == 0) *status = 0u;
-    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     uint8_t *coef = img + (size_t)h * kImgStride;
     const int k = blockIdx.x * 8 + (tid >> 4), j0 = (tid & 15) * 8;
     const bool realk = k < K;
@@ -118,18 +114,25 @@ __global__ void __launch_bounds__(128) tc128_prep_kernel(const float *__restrict
     }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) det += __shfl_xor_sync(0xffffffffu, det, o);
+    const float lp = realk ? log_pi[(size_t)h * K + k] : 0.f;
+    if ((tid & 15) == 0 && realk && !isfinite(lp)) bad = true;
+    const int any = __syncthreads_or(bad ? 1 : 0);
+    // Everything above only reads the parameters; the previous call's kernels may
+    // still read the status, counters and images written below.  The next kernel
+    // launches after the wait (launching it earlier, while the previous kernel's
+    // CTAs drain, placed its CTAs on SMs in the order they freed and measured
+    // slower).
+    pdl_wait();
+    pdl_trigger();
+    if (gt == 0) *status = 0u;
+    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     uint8_t *slabs = coef + (j0 >> 6) * 4 * kSlab;
     const uint32_t off = sw128_offset(k, j0 & 63, 1024);  // 16-byte aligned (j0 % 8 == 0)
     *reinterpret_cast<uint4 *>(slabs + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
     *reinterpret_cast<uint4 *>(slabs + kSlab + off) = make_uint4(al[0], al[1], al[2], al[3]);
     *reinterpret_cast<uint4 *>(slabs + 2 * kSlab + off) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
     *reinterpret_cast<uint4 *>(slabs + 3 * kSlab + off) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-    if ((tid & 15) == 0) {
-        const float lp = realk ? log_pi[(size_t)h * K + k] : 0.f;
-        if (realk && !isfinite(lp)) bad = true;
-        reinterpret_cast<float *>(coef + kCoefC)[k] = realk ? kLog2e128 * (lp - 0.5f * det) : -INFINITY;
-    }
-    const int any = __syncthreads_or(bad ? 1 : 0);
+    if ((tid & 15) == 0) reinterpret_cast<float *>(coef + kCoefC)[k] = realk ? kLog2e128 * (lp - 0.5f * det) : -INFINITY;
     if (tid == 0) head_err[h * kPrepBlocks128 + blockIdx.x] = any ? (unsigned)GMA_ERR_NONFINITE_PARAM : 0u;
 }
 
