@@ -49,3 +49,18 @@ def test_tc_single_pass_long_heads(splits):
     assert err <= TOL["bf16"], f"{case.name}: normalised max error {err:.3e}"
     O2 = run_gpu(case, d, splits=splits, path=gma.PATH_TC_SINGLE_PASS)
     assert (O == O2).all()
+
+
+@pytest.mark.parametrize("splits", [2, 9, 0])
+@pytest.mark.parametrize("variant", PATHS[:2])
+def test_tc_many_one_tile_heads(variant, splits):
+    """Forty heads of one ragged tile each: a CTA's range crosses a head boundary
+    at every tile, so the time-balanced cuts (each boundary costs a job end and
+    a job start) give CTAs many one-tile jobs and the job slots run deep; with
+    the default CTA count every CTA holds at most one head."""
+    causal, path = variant
+    case = Case(f"tcsmall_{int(causal)}_{splits}", causal, 4, 10, 100, 64, 64, 64, "bf16")
+    inp = make_inputs(case, seed=zlib.crc32(case.name.encode()) % 1000)
+    O = run_gpu(case, to_dev(inp), splits=splits, path=path)
+    err = normalised_error(O, oracle_full(case, inp))
+    assert err <= TOL["bf16"], f"{case.name}: normalised max error {err:.3e}"
