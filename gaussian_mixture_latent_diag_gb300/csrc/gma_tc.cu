@@ -76,6 +76,19 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
     const int k = blockIdx.x * 8 + (tid >> 4), j = (tid & 15) * 4;
     const bool realk = k < K;
     const bool real = realk && j < DR;  // d_r < 64: columns DR .. 63 are zero padding
+    // The previous call's kernels may still read the status, counters and images,
+    // and the kernel before this one may have written the parameters: they are read
+    // only after the dependency wait.  Their lines are brought into L2 meanwhile (a
+    // prefetch returns nothing, and L2 is where that kernel's writes land).
+    if (real) {
+        prefetch_l2(sigma2 + ((size_t)h * K + k) * DR + j);
+        prefetch_l2(mu + ((size_t)h * K + k) * DR + j);
+    }
+    if (realk && j == 0) prefetch_l2(log_pi + (size_t)h * K + k);
+    pdl_wait();
+    pdl_trigger();
+    if (gt == 0) *status = 0u;
+    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float lp = 0.f;
     if (real) {
@@ -108,15 +121,6 @@ __global__ void __launch_bounds__(128) coef_prep_tc_kernel(const float *__restri
     for (int o = 8; o > 0; o >>= 1) det += __shfl_xor_sync(0xffffffffu, det, o);
     if (j == 0 && realk && !isfinite(lp)) bad = true;
     const int any = __syncthreads_or(bad ? 1 : 0);
-    // Everything above only reads the parameters; the previous call's kernels may
-    // still read the status, counters and images written below.  The next kernel
-    // launches after the wait (launching it earlier, while the previous kernel's
-    // CTAs drain, placed its CTAs on SMs in the order they freed and measured
-    // slower).
-    pdl_wait();
-    pdl_trigger();
-    if (gt == 0) *status = 0u;
-    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     const uint32_t off = sw128_offset(k, j, 1024);  // 8-byte aligned (j % 4 == 0)
     *reinterpret_cast<uint2 *>(coef + off) = make_uint2(ah[0], ah[1]);
     *reinterpret_cast<uint2 *>(coef + kCoefMatBytes + off) = make_uint2(al[0], al[1]);

@@ -81,6 +81,18 @@ __global__ void __launch_bounds__(128) tc128_prep_kernel(const float *__restrict
     uint8_t *coef = img + (size_t)h * kImgStride;
     const int k = blockIdx.x * 8 + (tid >> 4), j0 = (tid & 15) * 8;
     const bool realk = k < K;
+    // The previous call's kernels may still read the status, counters and images,
+    // and the kernel before this one may have written the parameters: they are read
+    // only after the dependency wait, their lines brought into L2 meanwhile.
+    if (realk) {
+        prefetch_l2(sigma2 + ((size_t)h * K + k) * kD + j0);
+        prefetch_l2(mu + ((size_t)h * K + k) * kD + j0);
+        if ((tid & 15) == 0) prefetch_l2(log_pi + (size_t)h * K + k);
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (gt == 0) *status = 0u;
+    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     float sv[8], mv[8];
     if (realk) {
         const float4 *s4 = reinterpret_cast<const float4 *>(sigma2 + ((size_t)h * K + k) * kD + j0);
@@ -117,15 +129,6 @@ __global__ void __launch_bounds__(128) tc128_prep_kernel(const float *__restrict
     const float lp = realk ? log_pi[(size_t)h * K + k] : 0.f;
     if ((tid & 15) == 0 && realk && !isfinite(lp)) bad = true;
     const int any = __syncthreads_or(bad ? 1 : 0);
-    // Everything above only reads the parameters; the previous call's kernels may
-    // still read the status, counters and images written below.  The next kernel
-    // launches after the wait (launching it earlier, while the previous kernel's
-    // CTAs drain, placed its CTAs on SMs in the order they freed and measured
-    // slower).
-    pdl_wait();
-    pdl_trigger();
-    if (gt == 0) *status = 0u;
-    for (int i = gt; i < BH; i += gridDim.x * gridDim.y * blockDim.x) counters[i] = 0u;
     uint8_t *slabs = coef + (j0 >> 6) * 4 * kSlab;
     const uint32_t off = sw128_offset(k, j0 & 63, 1024);  // 16-byte aligned (j0 % 8 == 0)
     *reinterpret_cast<uint4 *>(slabs + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
