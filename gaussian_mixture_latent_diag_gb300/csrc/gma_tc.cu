@@ -154,10 +154,12 @@ constexpr int kThreadsG = 64 + 128 * kNG;    // TMA warp, MMA warp, NG x 4 epilo
 // takes [start[c], start[c + 1]).  The cuts balance the CTAs' time, not their
 // tile counts: a range that crosses a head boundary pays a job end and a job
 // start (the accumulator drained, the next head's coefficients and first tiles
-// loaded behind a CTA-wide barrier), about kSwitchTiles tiles of work, so such
-// a range gets that many fewer tiles (part_cuts).
+// loaded behind a CTA-wide barrier), so such a range gets kSwitchTiles fewer
+// tiles (part_cuts).  Traces put a job switch near four tiles of work; six
+// measured fastest (3, 4 and 6 compared), as those ranges also tend to hold the
+// CTA that combines a head.
 constexpr int kMaxPartCtas = 320;
-constexpr int kSwitchTiles = 4;
+constexpr int kSwitchTiles = 6;
 struct Part {
     int ntiles;  // tiles per head
     int total;   // B*H*ntiles
