@@ -30,7 +30,7 @@ EXPORTED = ("gma_workspace_size", "gma_responsibilities", "gma_forward_bidir",
             "gma_routing_stats", "gma_read_memory_workspace_size", "gma_read_memory",
             "gma_causal_carry_workspace_size", "gma_forward_causal_carry", "gma_reparameterize",
             "gma_reparameterize_backward", "gma_project_workspace_size", "gma_project_qkv",
-            "gma_combine_memories")
+            "gma_combine_memories", "gma_tc_partition")
 
 
 class Options(ctypes.Structure):
@@ -117,6 +117,9 @@ def load(path: str | None = None):
         lib.gma_status_string.restype = ctypes.c_char_p
         lib.gma_selected_path.argtypes = [i, i, i, i, i, i, opt]
         lib.gma_selected_path.restype = i
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.gma_tc_partition.argtypes = [i, i, i, ip, i, ip]
+        lib.gma_tc_partition.restype = i
         lib.gma_stage_count.argtypes = [i, i]
         lib.gma_stage_count.restype = i
         lib.gma_stage_name.argtypes = [i, i, i]

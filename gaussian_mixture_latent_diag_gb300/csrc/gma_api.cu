@@ -672,6 +672,11 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
     return path >= 0 && chunk_ok(path, causal, options) ? path : -1;
 }
 
+int gma_tc_partition(int tiles_per_head, int total_tiles, int max_ctas, int *starts, int starts_len,
+                     int *switch_tiles) {
+    return gma::tc_partition(tiles_per_head, total_tiles, max_ctas, starts, starts_len, switch_tiles);
+}
+
 int gma_stage_count(int path, int variant) {
     if (path == GMA_PATH_TC_SINGLE_PASS) {
         if (variant == 1 || variant == 8) return 2;

@@ -145,6 +145,8 @@ cudaError_t tc_project_qkv(const void *X, const void *Wq, const void *Wk, const 
 // ---------------------------------------------------------------- tensor-core path
 bool tc_supported(const Problem &p, int causal);
 size_t tc_workspace(const Problem &p, int causal, int splits);
+// The per-CTA tile ranges of the 64-wide kernels (gma_tc_partition).
+int tc_partition(int ntiles, int total, int max_ctas, int *starts, int starts_len, int *switch_tiles);
 size_t tc_carry_workspace(const Problem &p);  // the carried-prefix causal forward (tc_causal_carry)
 // The single-pass causal forward (GMA_PATH_TC_SINGLE_PASS): one kernel after the
 // coefficient prep, key responsibilities kept on chip, prefix memories chained

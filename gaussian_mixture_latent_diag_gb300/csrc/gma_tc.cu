@@ -2751,6 +2751,18 @@ bool tc_supported(const Problem &p, int causal) {
     return causal == 1 && p.d_v == 64;
 }
 
+int tc_partition(int ntiles, int total, int max_ctas, int *starts, int starts_len, int *switch_tiles) {
+    if (ntiles < 1 || total < 1 || total % ntiles != 0 || max_ctas < 1 || !starts) return -1;
+    if (switch_tiles) *switch_tiles = kSwitchTiles;
+    int nct = max_ctas > total ? total : max_ctas;
+    nct = nct > kMaxPartCtas ? kMaxPartCtas : nct;
+    Part P;
+    part_cuts(&P, ntiles, total, nct);
+    if (starts_len < P.nctas + 1) return -1;
+    for (int i = 0; i <= P.nctas; ++i) starts[i] = P.start[i];
+    return P.nctas;
+}
+
 size_t tc_workspace(const Problem &p, int causal, int splits) { return tc_layout2(p, splits, causal).total; }
 
 size_t tc_carry_workspace(const Problem &p) { return tc_layout2(p, 0, 1).total; }

@@ -175,6 +175,23 @@ int gma_selected_path(int N, int d_r, int d_v, int K, gma_dtype dtype, int causa
                       const gma_options *options);
 
 /*
+ * Diagnostic, host only (no device work, no CUDA call): how the 64-wide
+ * tensor-core kernels (GMA_PATH_TC at d_r, d_v <= 64) cut a call's tiles into
+ * one contiguous range per CTA.  The call's B*H*ceil(N/128) tiles of 128 tokens
+ * are taken in (head, tile) order: total_tiles of them, tiles_per_head per head
+ * (total_tiles a multiple of tiles_per_head).  At most max_ctas ranges (the
+ * kernels pass the SM count, or options->splits when set); the library caps
+ * this at its own limit.  A range costs its tiles plus *switch_tiles for every
+ * head boundary inside it (the job end and job start it pays), and the cuts
+ * minimise the largest range cost.  Writes the first tile of every range, then
+ * total_tiles, into starts[0 .. n] and returns n, the number of ranges; writes
+ * the per-boundary cost to *switch_tiles when that pointer is not NULL.
+ * Returns -1 for an argument out of range or starts_len < n + 1.
+ */
+int gma_tc_partition(int tiles_per_head, int total_tiles, int max_ctas, int *starts, int starts_len,
+                     int *switch_tiles);
+
+/*
  * Allocation-free variant of gma_forward_bidir.  The paper has no
  * counterpart: this is a deployment convenience.
  *
