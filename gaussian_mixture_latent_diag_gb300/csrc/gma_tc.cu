@@ -2489,22 +2489,22 @@ struct TcLayout2 {
 };
 
 // End of the range that starts at tile a when a range may cost m (tiles, plus
-// kSwitchTiles per head boundary crossed); at least one tile.
+// kSwitchTiles per head boundary crossed); at least one tile.  The rest of a's
+// head first, then as many whole heads as the budget pays for (each its tiles
+// plus the switch), then part of one more head if the budget left exceeds the
+// switch: constant time, so the cuts of a call cost O(CTAs) per search step
+// whatever the number of heads.
 int range_end(int a, int ntiles, int total, long long m) {
-    int b = a;
-    long long left = m;
-    while (b < total) {
-        const int head_end = (b / ntiles + 1) * ntiles;
-        if (b > a && b % ntiles == 0) {  // entering a new head
-            if (left <= kSwitchTiles) break;
-            left -= kSwitchTiles;
-        }
-        const long long take = std::min<long long>(left, head_end - b);
-        b += (int)take;
-        left -= take;
-        if (left <= 0) break;
-    }
-    return b > a ? b : a + 1;
+    const int head_end = (a / ntiles + 1) * ntiles;
+    const long long first = std::min<long long>(m, head_end - a);
+    long long b = a + first, left = m - first;
+    if (left <= 0 || b >= total) return b > a ? (int)b : a + 1;
+    const long long whole = left / (kSwitchTiles + ntiles), heads_left = (total - b) / ntiles;
+    if (whole >= heads_left) return total;
+    b += whole * ntiles;
+    left -= whole * (kSwitchTiles + ntiles);
+    if (left > kSwitchTiles) b += left - kSwitchTiles;  // < ntiles: part of the next head
+    return (int)b;
 }
 
 // Cuts with the smallest largest range cost that needs at most nct ranges
