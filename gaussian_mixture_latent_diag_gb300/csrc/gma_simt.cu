@@ -21,6 +21,33 @@
 namespace gma {
 namespace {
 
+// Every kernel of this family starts with dep_wait, so it may be launched with
+// programmatic stream serialisation (launch_dep): it begins launching while
+// the previous kernel of the stream is still running, and waits, before any
+// memory access, until that kernel has completed and its writes are visible.
+// The launch latency of the next kernel then overlaps this one, which is most
+// of the time of a small call.  dep_trigger lets the next kernel launch as
+// soon as every CTA of this one has started (it waits the same way).
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialisation; a launch error is left for
+// the caller's cudaGetLastError, as with <<< >>>.
+template <typename... KArgs, typename... Args>
+void launch_dep(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_f32(float x);
@@ -53,6 +80,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_simt_kernel(const float *__
                                  const float *__restrict__ log_pi, int K, int d_r,
                                  float *__restrict__ inv, float *__restrict__ cprime,
                                  unsigned *status) {
+    dep_wait();
+    dep_trigger();
     extern __shared__ float slog[];  // [K][d_r + 1]
     const int h = blockIdx.x;
     const size_t base = (size_t)h * K * d_r;
@@ -92,6 +121,8 @@ __global__ void __launch_bounds__(128) resp_simt_kernel(
     const float *__restrict__ inv, const float *__restrict__ cprime, float *out,
     long long out_bh_stride, long long out_stride_n, long long out_stride_k,
     const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     constexpr int D2 = D_R / 2;
     __shared__ float4 sp[kRespKC][D2];
@@ -190,6 +221,8 @@ template <typename T, int TA, int TB>
 __global__ void __launch_bounds__(256) write_simt_kernel(
     const float *__restrict__ gkt, const T *__restrict__ V, int N, int K, int d_v,
     int tokens_per_split, int nsplit, float *__restrict__ part, const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     __shared__ float sg[128][kWT + 1];
     __shared__ float sv[kWT][128 + 4];
@@ -262,6 +295,8 @@ __global__ void __launch_bounds__(256) write_simt_kernel(
 // Fixed-order sum of the split partials: mem[bh] = sum_s part[bh][s].
 __global__ void reduce_splits_kernel(const float *__restrict__ part, int nsplit, int E,
                                      float *__restrict__ mem, const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     const int bh = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -277,6 +312,8 @@ __global__ void reduce_splits_kernel(const float *__restrict__ part, int nsplit,
 __global__ void reduce_to_memory_kernel(const float *__restrict__ part, int nsplit, int K, int d_v,
                                         float *__restrict__ Vt, float *__restrict__ Z,
                                         const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     const int bh = blockIdx.y, W = d_v + 1, E = K * W;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -315,6 +352,8 @@ __device__ __forceinline__ void exclusive_prefix_strided(float *p, int n, int E,
 // mem[bh][k] = [Vt[bh][k][0..d_v) | Z[bh][k]].
 __global__ void pack_memory_kernel(const float *__restrict__ Vt, const float *__restrict__ Z, int K, int d_v,
                                    float *__restrict__ mem, const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     const int bh = blockIdx.y, W = d_v + 1, E = K * W;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -331,6 +370,8 @@ __global__ void scan_chunks_carry_kernel(float *__restrict__ part, int nchunk, i
                                          const float *__restrict__ Vt_in, const float *__restrict__ Z_in,
                                          float *__restrict__ Vt_out, float *__restrict__ Z_out,
                                          const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     const int bh = blockIdx.y, W = d_v + 1, E = K * W;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -351,6 +392,8 @@ __global__ void scan_chunks_carry_kernel(float *__restrict__ part, int nchunk, i
 // start of chunk c, [GMA, causal variant, cumulative sums]).
 __global__ void scan_chunks_kernel(float *__restrict__ part, int nchunk, int E,
                                    const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     const int bh = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -366,6 +409,8 @@ template <int D_V, typename TO>
 __global__ void __launch_bounds__(128) read_simt_kernel(
     const float *__restrict__ gqt, const float *__restrict__ mem, int N, int K, float eps,
     TO *__restrict__ O, const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     extern __shared__ float smem[];
     const int W = D_V + 1;
@@ -431,6 +476,8 @@ __global__ void __launch_bounds__(kSimtCausalChunk * kCausalParts) causal_simt_k
     const float *__restrict__ gqt, const float *__restrict__ gkt, const T *__restrict__ V,
     const float *__restrict__ prefix, int N, int K, int nchunk, float eps, TO *__restrict__ O,
     const unsigned *status) {
+    dep_wait();
+    dep_trigger();
     if (failed(status)) return;
     constexpr int C = kSimtCausalChunk;
     constexpr int W = D_V + 1;
@@ -547,10 +594,10 @@ cudaError_t launch_resp(const Problem &p, const void *X, const float *inv, const
     dim3 grid((p.N + 127) / 128, p.BH());
     const T *x = static_cast<const T *>(X);
     switch (p.d_r) {
-        case 16: resp_simt_kernel<16, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
-        case 32: resp_simt_kernel<32, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
-        case 64: resp_simt_kernel<64, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
-        case 128: resp_simt_kernel<128, T><<<grid, 128, 0, s>>>(x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 16: launch_dep(resp_simt_kernel<16, T>, grid, 128, 0, s, x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 32: launch_dep(resp_simt_kernel<32, T>, grid, 128, 0, s, x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 64: launch_dep(resp_simt_kernel<64, T>, grid, 128, 0, s, x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
+        case 128: launch_dep(resp_simt_kernel<128, T>, grid, 128, 0, s, x, p.H, p.N, p.K, p.mu, inv, cprime, out, bh_stride, sn, sk, status); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -564,7 +611,7 @@ cudaError_t launch_read_dv(const Problem &p, const float *gq, const float *mem,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.N + 127) / 128, p.BH());
-    kern<<<grid, 128, smem, s>>>(gq, mem, p.N, p.K, p.eps, static_cast<TO *>(p.O), status);
+    launch_dep(kern, grid, 128, smem, s, gq, mem, p.N, p.K, p.eps, static_cast<TO *>(p.O), status);
     return cudaGetLastError();
 }
 
@@ -592,7 +639,7 @@ cudaError_t launch_causal_dv(const Problem &p, const float *gq, const float *gk,
         if (e != cudaSuccess) return e;
     }
     dim3 grid(nchunk, p.BH());
-    kern<<<grid, C * kCausalParts, smem, s>>>(gq, gk, static_cast<const T *>(p.V), prefix, p.N, p.K, nchunk,
+    launch_dep(kern, grid, C * kCausalParts, smem, s, gq, gk, static_cast<const T *>(p.V), prefix, p.N, p.K, nchunk,
                                               p.eps, static_cast<TO *>(p.O), status);
     return cudaGetLastError();
 }
@@ -634,7 +681,7 @@ cudaError_t prep(const Problem &p, const Ptrs &P, cudaStream_t s) {
     const size_t smem = sizeof(float) * (size_t)p.K * (p.d_r + 1);
     if (smem > 48 * 1024)  // above the default limit only: the call costs host time
         GMA_TRY(cudaFuncSetAttribute(prep_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    prep_simt_kernel<<<p.H, kPrepThreads, smem, s>>>(p.mu, p.sigma2, p.log_pi, p.K, p.d_r, P.inv, P.cprime, P.status);
+    launch_dep(prep_simt_kernel, p.H, kPrepThreads, smem, s, p.mu, p.sigma2, p.log_pi, p.K, p.d_r, P.inv, P.cprime, P.status);
     return cudaGetLastError();
 }
 
@@ -661,19 +708,19 @@ cudaError_t write_parts(const Problem &p, const SimtLayout &L, const Ptrs &P, cu
     if (p.dtype == GMA_F32) {
         const float *V = static_cast<const float *>(p.V);
         if (big)
-            write_simt_kernel<float, 8, 8><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v, L.tokens_per_split,
+            launch_dep(write_simt_kernel<float, 8, 8>, grid, 256, 0, s, P.gk, V, p.N, p.K, p.d_v, L.tokens_per_split,
                                                                 L.nsplit, P.part, P.status);
         else
-            write_simt_kernel<float, 4, 4><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v, L.tokens_per_split,
+            launch_dep(write_simt_kernel<float, 4, 4>, grid, 256, 0, s, P.gk, V, p.N, p.K, p.d_v, L.tokens_per_split,
                                                                 L.nsplit, P.part, P.status);
     } else {
         const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V);
         if (big)
-            write_simt_kernel<__nv_bfloat16, 8, 8><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v,
+            launch_dep(write_simt_kernel<__nv_bfloat16, 8, 8>, grid, 256, 0, s, P.gk, V, p.N, p.K, p.d_v,
                                                                         L.tokens_per_split, L.nsplit, P.part,
                                                                         P.status);
         else
-            write_simt_kernel<__nv_bfloat16, 4, 4><<<grid, 256, 0, s>>>(P.gk, V, p.N, p.K, p.d_v,
+            launch_dep(write_simt_kernel<__nv_bfloat16, 4, 4>, grid, 256, 0, s, P.gk, V, p.N, p.K, p.d_v,
                                                                         L.tokens_per_split, L.nsplit, P.part,
                                                                         P.status);
     }
@@ -741,7 +788,7 @@ cudaError_t simt_bidir(const Problem &p, int splits, void *ws, cudaStream_t s, S
     GMA_TRY(write_parts(p, L, P, s));
     clk.mark();
     const int E = p.K * (p.d_v + 1);
-    reduce_splits_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.mem, P.status);
+    launch_dep(reduce_splits_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, P.part, L.nsplit, E, P.mem, P.status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     if (p.o_bf16) GMA_TRY(launch_read<__nv_bfloat16>(p, P.gq, P.mem, P.status, s));
@@ -759,7 +806,7 @@ cudaError_t simt_bidir_state(const Problem &p, int splits, void *ws, cudaStream_
     GMA_TRY(resp_both(p, P, s, none));
     GMA_TRY(write_parts(p, L, P, s));
     const int E = p.K * (p.d_v + 1);
-    reduce_splits_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.mem, P.status);
+    launch_dep(reduce_splits_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, P.part, L.nsplit, E, P.mem, P.status);
     return cudaGetLastError();
 }
 
@@ -772,7 +819,7 @@ cudaError_t simt_causal_state(const Problem &p, void *ws, cudaStream_t s) {
     GMA_TRY(resp_both(p, P, s, none));
     GMA_TRY(write_parts(p, L, P, s));
     const int E = p.K * (p.d_v + 1);
-    scan_chunks_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.status);
+    launch_dep(scan_chunks_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, P.part, L.nsplit, E, P.status);
     return cudaGetLastError();
 }
 
@@ -786,7 +833,7 @@ cudaError_t simt_causal(const Problem &p, void *ws, cudaStream_t s, StageClock &
     GMA_TRY(write_parts(p, L, P, s));
     clk.mark();
     const int E = p.K * (p.d_v + 1);
-    scan_chunks_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, E, P.status);
+    launch_dep(scan_chunks_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, P.part, L.nsplit, E, P.status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     if (p.dtype == GMA_F32 && !p.o_bf16)
@@ -813,7 +860,7 @@ cudaError_t simt_read_memory(const Problem &p, const float *Vt, const float *Z, 
     else GMA_TRY(launch_resp<__nv_bfloat16>(p, p.Q, P.inv, P.cprime, P.gq, bhs, 1, p.N, P.status, s));
     clk.mark();
     const int E = p.K * (p.d_v + 1);
-    pack_memory_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(Vt, Z, p.K, p.d_v, P.mem, P.status);
+    launch_dep(pack_memory_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, Vt, Z, p.K, p.d_v, P.mem, P.status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
     if (p.o_bf16) GMA_TRY(launch_read<__nv_bfloat16>(p, P.gq, P.mem, P.status, s));
@@ -833,7 +880,7 @@ cudaError_t simt_causal_carry(const Problem &p, const float *Vt_in, const float 
     GMA_TRY(write_parts(p, L, P, s));
     clk.mark();
     const int E = p.K * (p.d_v + 1);
-    scan_chunks_carry_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, p.K, p.d_v, Vt_in, Z_in,
+    launch_dep(scan_chunks_carry_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, P.part, L.nsplit, p.K, p.d_v, Vt_in, Z_in,
                                                                            Vt_out, Z_out, P.status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
@@ -867,7 +914,7 @@ cudaError_t simt_latent_memory(const Problem &p, int splits, float *Vt, float *Z
     GMA_TRY(write_parts(p, L, P, s));
     clk.mark();
     const int E = p.K * (p.d_v + 1);
-    reduce_to_memory_kernel<<<dim3((E + 255) / 256, p.BH()), 256, 0, s>>>(P.part, L.nsplit, p.K, p.d_v, Vt, Z,
+    launch_dep(reduce_to_memory_kernel, dim3((E + 255) / 256, p.BH()), 256, 0, s, P.part, L.nsplit, p.K, p.d_v, Vt, Z,
                                                                           P.status);
     GMA_TRY(cudaGetLastError());
     clk.mark();
